@@ -1,0 +1,249 @@
+"""Thin ctypes binding of libcpthd.so (declared in include/cpthd.h).
+
+Argument marshalling only: every function here validates Python-side types,
+turns torch tensors into raw pointers and the current CUDA stream into a
+cudaStream_t, calls the C entry point of the same name and raises CpError on
+a non-zero status.  All computation runs in the library's CUDA kernels; there
+is no fallback -- importing this module on a machine without the built
+library raises immediately when a function is first called.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+DUAL_CHUNK_SWAP = 0
+NO_LOAD_BALANCE = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcpthd.so")
+_lib = None
+
+_c_i32p = ctypes.POINTER(ctypes.c_int32)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "cp_status_string": ([_I], ctypes.c_char_p),
+    "cp_version": ([], _I),
+    "cp_detect_pad_between_seqs": ([_P, _P, _I, ctypes.POINTER(_I)], _I),
+    "cp_validate_seqlens": ([_P, _P, _I, _I64, _I, _I, _I], _I),
+    "cp_valid_end": ([_P, _P, _I, _I, _I, _I, _I, ctypes.POINTER(_I64)], _I),
+    "cp_meta_bytes": ([_I, _I64], _SZ),
+    "cp_partition_index": ([_P, _P, _I, _I64, _I, _I, _I, _I, _P, _P, _P, _SZ, _P], _I),
+    "cp_thd_gather": ([_P, _P, _I, _P, _I64, _I64, _I64, _P], _I),
+    "cp_thd_scatter": ([_P, _P, _I, _P, _I64, _I64, _I64, _P], _I),
+    "cp_reduce_scatter_emul": ([_P, _P, _I, _P, _I64, _I64, _I64, _I, _I, _P], _I),
+    "cp_zero_tail": ([_P, _I, _I64, _I64, _I64, _P, _P, ctypes.POINTER(_I)], _I),
+    "cp_attn_fwd": ([_P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I, ctypes.c_float, _P], _I),
+    "cp_attn_bwd_workspace_bytes": ([_I64, _I], _SZ),
+    "cp_attn_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
+                     ctypes.c_float, _P, _SZ, _P], _I),
+    "cp_device_status": ([ctypes.POINTER(_I), _I], _I),
+}
+
+EXPORTED = tuple(_SIGNATURES)
+
+
+class CpError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libcpthd.so is not built ({LIB_PATH}); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().cp_status_string(int(status)).decode()
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise CpError(fn, st)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return _ptr(t)
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _host_i32(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _ptr_array(ts: Sequence[torch.Tensor], name: str):
+    arr = (ctypes.c_void_p * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = _dev(t, name).value
+    return arr
+
+
+# ---------------------------------------------------------------------------
+# host metadata helpers
+# ---------------------------------------------------------------------------
+
+def cp_detect_pad_between_seqs(cu, cup) -> int:
+    a = _host_i32(cu)
+    b = None if cup is None else _host_i32(cup)
+    out = _I(0)
+    st = lib().cp_detect_pad_between_seqs(a.ctypes.data, None if b is None else b.ctypes.data,
+                                          len(a) - 1, ctypes.byref(out))
+    _check("cp_detect_pad_between_seqs", st)
+    return int(out.value)
+
+
+def cp_validate_seqlens(cu, cup, total_tokens: int, cp_size: int, strategy: int,
+                        pad_between_seqs: int) -> int:
+    """Returns the status code (0 = valid) without raising."""
+    a, b = _host_i32(cu), _host_i32(cup)
+    return int(lib().cp_validate_seqlens(a.ctypes.data, b.ctypes.data, len(b) - 1, total_tokens,
+                                         cp_size, strategy, pad_between_seqs))
+
+
+def cp_valid_end(cu, cup, cp_size: int, rank: int, strategy: int, pad_between_seqs: int) -> int:
+    a, b = _host_i32(cu), _host_i32(cup)
+    out = _I64(0)
+    st = lib().cp_valid_end(a.ctypes.data, b.ctypes.data, len(b) - 1, cp_size, rank, strategy,
+                            pad_between_seqs, ctypes.byref(out))
+    _check("cp_valid_end", st)
+    return int(out.value)
+
+
+def cp_meta_bytes(n_docs: int, s_local: int) -> int:
+    return int(lib().cp_meta_bytes(n_docs, s_local))
+
+
+def cp_attn_bwd_workspace_bytes(s_local: int, H: int) -> int:
+    return int(lib().cp_attn_bwd_workspace_bytes(s_local, H))
+
+
+# ---------------------------------------------------------------------------
+# device entry points
+# ---------------------------------------------------------------------------
+
+def cp_partition_index(d_cu: Optional[torch.Tensor], d_cup: torch.Tensor, total_tokens: int,
+                       cp_size: int, rank: int, strategy: int, pad_between_seqs: int,
+                       d_idx: torch.Tensor, d_restore: Optional[torch.Tensor],
+                       d_meta: torch.Tensor, stream=None) -> None:
+    n_docs = d_cup.numel() - 1
+    st = lib().cp_partition_index(None if d_cu is None else _dev(d_cu, "cu"), _dev(d_cup, "cup"),
+                                  n_docs, total_tokens, cp_size, rank, strategy,
+                                  pad_between_seqs, _dev(d_idx, "idx"),
+                                  None if d_restore is None else _dev(d_restore, "restore"),
+                                  _dev(d_meta, "meta"), d_meta.numel() * d_meta.element_size(),
+                                  _stream(stream))
+    _check("cp_partition_index", st)
+
+
+def _row_bytes(t: torch.Tensor) -> int:
+    return t[0].numel() * t.element_size() if t.shape[0] > 0 else t.numel() * t.element_size()
+
+
+def cp_thd_gather(srcs: Sequence[torch.Tensor], dsts: Sequence[torch.Tensor],
+                  d_idx: torch.Tensor, stream=None) -> None:
+    n_rows = d_idx.numel()
+    src_rows = srcs[0].shape[0]
+    st = lib().cp_thd_gather(_ptr_array(srcs, "src"), _ptr_array(dsts, "dst"), len(srcs),
+                             _dev(d_idx, "idx"), n_rows, src_rows, _row_bytes(srcs[0]),
+                             _stream(stream))
+    _check("cp_thd_gather", st)
+
+
+def cp_thd_scatter(srcs: Sequence[torch.Tensor], dsts: Sequence[torch.Tensor],
+                   d_idx: torch.Tensor, stream=None) -> None:
+    n_rows = d_idx.numel()
+    dst_rows = dsts[0].shape[0]
+    st = lib().cp_thd_scatter(_ptr_array(srcs, "src"), _ptr_array(dsts, "dst"), len(srcs),
+                              _dev(d_idx, "idx"), n_rows, dst_rows, _row_bytes(srcs[0]),
+                              _stream(stream))
+    _check("cp_thd_scatter", st)
+
+
+def cp_reduce_scatter_emul(accums: Sequence[torch.Tensor], dsts: Sequence[torch.Tensor],
+                           d_idx: Optional[torch.Tensor], row0: int, n_rows: int,
+                           stream=None) -> None:
+    T, H, D = accums[0].shape
+    st = lib().cp_reduce_scatter_emul(_ptr_array(accums, "accum"), _ptr_array(dsts, "dst"),
+                                      len(accums), None if d_idx is None else _dev(d_idx, "idx"),
+                                      row0, n_rows, T, H, D, _stream(stream))
+    _check("cp_reduce_scatter_emul", st)
+
+
+def cp_zero_tail(tensors: Sequence[torch.Tensor], valid_end: int,
+                 d_valid_end: Optional[torch.Tensor] = None, stream=None) -> bool:
+    """Returns True when a kernel was launched."""
+    rows = tensors[0].shape[0]
+    launched = _I(0)
+    st = lib().cp_zero_tail(_ptr_array(tensors, "rows"), len(tensors), rows,
+                            _row_bytes(tensors[0]), valid_end,
+                            None if d_valid_end is None else _dev(d_valid_end, "valid_end"),
+                            _stream(stream), ctypes.byref(launched))
+    _check("cp_zero_tail", st)
+    return bool(launched.value)
+
+
+def cp_attn_fwd(q_local, k_full, v_full, o_local, lse_local, d_meta, total_tokens: int,
+                cp_size: int, rank: int, strategy: int, softmax_scale: float,
+                stream=None) -> None:
+    _, H, D = k_full.shape
+    st = lib().cp_attn_fwd(_dev(q_local, "q"), _dev(k_full, "k"), _dev(v_full, "v"),
+                           _dev(o_local, "o"), _dev(lse_local, "lse"), _dev(d_meta, "meta"),
+                           d_meta.numel() * d_meta.element_size(), total_tokens, H, D, cp_size,
+                           rank, strategy, float(softmax_scale), _stream(stream))
+    _check("cp_attn_fwd", st)
+
+
+def cp_attn_bwd(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local, dk_accum,
+                dv_accum, d_meta, total_tokens: int, cp_size: int, rank: int, strategy: int,
+                softmax_scale: float, d_workspace, stream=None) -> None:
+    _, H, D = k_full.shape
+    st = lib().cp_attn_bwd(_dev(q_local, "q"), _dev(k_full, "k"), _dev(v_full, "v"),
+                           _dev(o_local, "o"), _dev(lse_local, "lse"), _dev(do_local, "do"),
+                           _dev(dq_local, "dq"), _dev(dk_accum, "dk"), _dev(dv_accum, "dv"),
+                           _dev(d_meta, "meta"), d_meta.numel() * d_meta.element_size(),
+                           total_tokens, H, D, cp_size, rank, strategy, float(softmax_scale),
+                           _dev(d_workspace, "workspace"),
+                           d_workspace.numel() * d_workspace.element_size(), _stream(stream))
+    _check("cp_attn_bwd", st)
+
+
+def cp_device_status(reset: bool = True) -> int:
+    out = _I(0)
+    _check("cp_device_status", lib().cp_device_status(ctypes.byref(out), int(reset)))
+    return int(out.value)

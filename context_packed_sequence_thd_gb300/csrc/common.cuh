@@ -1,0 +1,235 @@
+// common.cuh -- shared host/device definitions of libcpthd (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "cpthd.h"
+
+namespace cpthd {
+
+// ---------------------------------------------------------------------------
+// Rank metadata written by the partition kernel and read by the attention
+// kernels.  Layout in device memory:
+//   [0, 64)                   MetaHeader
+//   [64, 64 + 32*max_segs)    Segment[max_segs], sorted by local_start
+//   then int32 row_lo[s_local], int32 row_hi[s_local]
+// A segment is a maximal run of local rows that are consecutive global rows
+// of one document: one DUAL_CHUNK_SWAP chunk, or one document's piece of a
+// NO_LOAD_BALANCE range.  Row t of a segment (u = t - local_start) is global
+// row global_start + u; it is a real token when u < valid_len.
+// row_lo/row_hi: the keys local row t attends are [row_lo[t], row_hi[t]]
+// (row_hi = -1, row_lo = 0 for padding rows).
+// ---------------------------------------------------------------------------
+constexpr int32_t kMetaMagic = 0x43505448;  // "CPTH"
+
+struct MetaHeader {
+  int32_t magic;
+  int32_t status;
+  int32_t strategy;
+  int32_t cp_size;
+  int32_t rank;
+  int32_t n_docs;
+  int32_t s_local;
+  int32_t n_segs;
+  int32_t valid_end;  // one past the last real-token local row
+  int32_t pad_between_seqs;
+  int32_t total_tokens;
+  int32_t max_segs;
+  int32_t seg_offset;   // bytes
+  int32_t rows_offset;  // bytes; row_lo at rows_offset, row_hi 4*s_local later
+  int32_t reserved[2];
+};
+static_assert(sizeof(MetaHeader) == 64, "header is 64 bytes");
+
+struct Segment {
+  int32_t local_start;
+  int32_t global_start;
+  int32_t len;
+  int32_t doc_lo;     // first row of the document (cup[i])
+  int32_t valid_len;  // real-token rows at the start of this segment
+  int32_t doc;
+  int32_t reserved[2];
+};
+static_assert(sizeof(Segment) == 32, "segment is 32 bytes");
+
+inline __host__ __device__ int max_segs_for(int n_docs) { return 2 * n_docs + 2; }
+inline __host__ __device__ size_t seg_offset_bytes() { return 64; }
+inline __host__ __device__ size_t rows_offset_bytes(int n_docs) {
+  return 64 + 32 * (size_t)max_segs_for(n_docs);
+}
+inline __host__ __device__ size_t meta_bytes_for(int n_docs, int64_t s_local) {
+  return rows_offset_bytes(n_docs) + 8 * (size_t)s_local;
+}
+
+struct MetaView {
+  const MetaHeader* hdr;
+  const Segment* segs;
+  const int32_t* row_lo;
+  const int32_t* row_hi;
+};
+
+inline __device__ MetaView meta_view(const void* meta) {
+  MetaView v;
+  const char* base = reinterpret_cast<const char*>(meta);
+  v.hdr = reinterpret_cast<const MetaHeader*>(base);
+  v.segs = reinterpret_cast<const Segment*>(base + v.hdr->seg_offset);
+  v.row_lo = reinterpret_cast<const int32_t*>(base + v.hdr->rows_offset);
+  v.row_hi = v.row_lo + v.hdr->s_local;
+  return v;
+}
+
+// Index of the last segment whose local_start <= t (segments are sorted and
+// tile [0, s_local) without gaps).
+inline __device__ int find_segment_local(const Segment* segs, int n_segs, int t) {
+  int lo = 0, hi = n_segs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (segs[mid].local_start <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Index of the first segment whose global range ends after key j, i.e.
+// global_start + len > j (global ranges increase with the segment index).
+inline __device__ int find_segment_global_end(const Segment* segs, int n_segs, int j) {
+  int lo = 0, hi = n_segs;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (segs[mid].global_start + segs[mid].len > j) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+// Key-block intervals [first, last] (inclusive, block size BN) that the local
+// query rows [t0, t0+rows) attend, merged and in increasing order.  Written to
+// out[] (capacity cap); returns the number of intervals.  One thread.
+inline __device__ int build_kv_intervals(const MetaView& m, int t0, int rows, int BN, int2* out,
+                                         int cap) {
+  const int n_segs = m.hdr->n_segs;
+  if (n_segs <= 0) return 0;
+  int k = find_segment_local(m.segs, n_segs, t0);
+  int next = 0, count = 0;
+  const int t1 = t0 + rows;
+  for (; k < n_segs; ++k) {
+    const Segment s = m.segs[k];
+    if (s.local_start >= t1) break;
+    int u0 = max(0, t0 - s.local_start);
+    int u1 = min(s.valid_len, t1 - s.local_start);
+    if (u0 >= u1) continue;
+    int first = s.doc_lo / BN;
+    int last = (s.global_start + u1 - 1) / BN;
+    first = max(first, next);
+    if (first > last) continue;
+    if (count > 0 && out[count - 1].y + 1 == first) {
+      out[count - 1].y = last;
+    } else if (count < cap) {
+      out[count++] = make_int2(first, last);
+    } else {
+      out[count - 1].y = last;  // over capacity: widen the last interval (still correct)
+    }
+    next = last + 1;
+  }
+  return count;
+}
+
+// Query-tile intervals (tiles of BM local rows) whose queries attend at least
+// one key in [j0, j1], merged and increasing.  One thread.
+inline __device__ int build_q_intervals(const MetaView& m, int j0, int j1, int BM, int2* out,
+                                        int cap) {
+  const int n_segs = m.hdr->n_segs;
+  if (n_segs <= 0) return 0;
+  int k = find_segment_global_end(m.segs, n_segs, j0);
+  int next = 0, count = 0;
+  for (; k < n_segs; ++k) {
+    const Segment s = m.segs[k];
+    if (s.doc_lo > j1) break;
+    // queries of this segment attending some key in [j0, j1]: real tokens at
+    // global rows >= max(j0, doc_lo)
+    int g_first = max(j0, s.doc_lo);
+    int u0 = max(0, g_first - s.global_start);
+    int u1 = s.valid_len;
+    if (u0 >= u1) continue;
+    int first = (s.local_start + u0) / BM;
+    int last = (s.local_start + u1 - 1) / BM;
+    first = max(first, next);
+    if (first > last) continue;
+    if (count > 0 && out[count - 1].y + 1 == first) {
+      out[count - 1].y = last;
+    } else if (count < cap) {
+      out[count++] = make_int2(first, last);
+    } else {
+      out[count - 1].y = last;
+    }
+    next = last + 1;
+  }
+  return count;
+}
+
+// ---------------------------------------------------------------------------
+// small PTX helpers (sm_80+ forms that remain valid on sm_103a)
+// ---------------------------------------------------------------------------
+inline __device__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+inline __device__ void cp_async_16(uint32_t dst, const void* src, bool pred) {
+  const int n = pred ? 16 : 0;  // 0 source bytes = zero fill
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n)
+               : "memory");
+}
+inline __device__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+inline __device__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+inline __device__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                               uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+inline __device__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                 uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulators.
+inline __device__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+inline __device__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits)
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of 16-byte chunk `c` of row `r` in a [rows][row_chunks*16 B]
+// tile whose chunks are XOR-swizzled by (r & 7) (conflict-free ldmatrix).
+inline __device__ uint32_t swz(int r, int c, int row_chunks) {
+  return (uint32_t)((r * row_chunks + (c ^ (r & 7))) * 16);
+}
+
+}  // namespace cpthd
+
+// host-side helpers shared by the translation units
+namespace cpthd_host {
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline int launch_status() {
+  return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+}  // namespace cpthd_host
+
+// per-translation-unit device status word accessors (defined in each .cu)
+extern "C" int cpthd_status_partition(int reset);
+extern "C" int cpthd_status_rows(int reset);
+extern "C" int cpthd_status_attn(int reset);

@@ -1,0 +1,222 @@
+// partition.cu -- per-rank THD partition index (one launch).
+//
+// "[PyTorch] Add no-load-balance THD all-gather CP", §What changed / §Why:
+// DUAL_CHUNK_SWAP gives rank r chunks r and 2*cp-1-r of every document's
+// padded range (2*cp equal chunks); NO_LOAD_BALANCE gives rank r the
+// contiguous physical rows [r*s_local, (r+1)*s_local) while the THD metadata
+// keeps the logical document boundaries.  The per-rank valid-token counts
+// (the quantity the P2P issue's get_cu_seqlens_on_cp_rank helper recomputes
+// with many small launches) fall out of the same pass.
+//
+// One CTA of 1024 threads: documents are processed 1024 at a time; a
+// block-wide exclusive scan (warp __shfl_up_sync scans + one scan of the warp
+// totals) turns per-document segment counts and local row counts into
+// offsets.  A second pass writes the row tables, one warp per segment.
+#include "common.cuh"
+
+namespace cpthd {
+
+static __device__ int g_status_partition;
+
+namespace {
+
+constexpr int kThreads = 1024;
+
+// Block-wide exclusive scan of v; *total receives the block sum.  All threads
+// of the block must call it.
+__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < kThreads / 32) ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  int excl = x - v + (warp > 0 ? s_warp[warp - 1] : 0);
+  *total = s_warp[kThreads / 32 - 1];
+  __syncthreads();  // s_warp is reused by the next call
+  return excl;
+}
+
+__device__ __forceinline__ int clampi(int x, int lo, int hi) { return min(max(x, lo), hi); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+partition_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup, int n_docs,
+                 int T, int cp, int rank, int strategy, int pad, int32_t* __restrict__ idx,
+                 int32_t* __restrict__ restore, char* __restrict__ meta) {
+  __shared__ int s_warp[32];
+  __shared__ int s_err;
+  __shared__ int s_valid_end;
+  __shared__ int s_carry_segs, s_carry_rows;
+
+  MetaHeader* hdr = reinterpret_cast<MetaHeader*>(meta);
+  Segment* segs = reinterpret_cast<Segment*>(meta + seg_offset_bytes());
+  const int s_local = T / cp;
+  const int max_segs = max_segs_for(n_docs);
+  int32_t* row_lo = reinterpret_cast<int32_t*>(meta + rows_offset_bytes(n_docs));
+  int32_t* row_hi = row_lo + s_local;
+  const int R0 = rank * s_local, R1 = R0 + s_local;
+
+  if (threadIdx.x == 0) {
+    int e = 0;
+    if (cup[0] != 0 || cup[n_docs] != T) e = CP_ERR_METADATA;
+    if (pad && cu[0] != 0) e = CP_ERR_METADATA;
+    s_err = e;
+    s_valid_end = 0;
+    s_carry_segs = 0;
+    s_carry_rows = 0;
+  }
+  __syncthreads();
+
+  for (int base = 0; base < n_docs; base += kThreads) {
+    const int i = base + threadIdx.x;
+    int nseg = 0, nrows = 0, a = 0, P = 0, L = 0, c = 0, lo = 0, hi = 0;
+    if (i < n_docs) {
+      a = cup[i];
+      P = cup[i + 1] - a;
+      L = pad ? (cu[i + 1] - cu[i]) : P;
+      if (P < 0 || L < 0 || L > P) atomicCAS(&s_err, 0, CP_ERR_METADATA);
+      if (strategy == CP_DUAL_CHUNK_SWAP) {
+        if (P > 0 && (P % (2 * cp)) != 0) atomicCAS(&s_err, 0, CP_ERR_DIVISIBILITY);
+        c = P / (2 * cp);
+        nseg = (c > 0) ? 2 : 0;
+        nrows = 2 * c;
+      } else {
+        lo = max(a, R0);
+        hi = min(a + max(P, 0), R1);
+        nrows = max(0, hi - lo);
+        nseg = nrows > 0 ? 1 : 0;
+      }
+    }
+    int tot_segs, tot_rows;
+    const int seg_off = block_exclusive_scan(nseg, s_warp, &tot_segs) + s_carry_segs;
+    const int row_off = block_exclusive_scan(nrows, s_warp, &tot_rows) + s_carry_rows;
+    if (i < n_docs && nseg > 0 && seg_off + nseg <= max_segs) {
+      if (strategy == CP_DUAL_CHUNK_SWAP) {
+        const int chunks[2] = {rank, 2 * cp - 1 - rank};
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          Segment s;
+          s.local_start = row_off + q * c;
+          s.global_start = a + chunks[q] * c;
+          s.len = c;
+          s.doc_lo = a;
+          s.valid_len = clampi(L - chunks[q] * c, 0, c);
+          s.doc = i;
+          s.reserved[0] = s.reserved[1] = 0;
+          segs[seg_off + q] = s;
+          if (s.valid_len > 0) atomicMax(&s_valid_end, s.local_start + s.valid_len);
+        }
+      } else {
+        Segment s;
+        s.local_start = lo - R0;
+        s.global_start = lo;
+        s.len = nrows;
+        s.doc_lo = a;
+        s.valid_len = clampi(a + L - lo, 0, nrows);
+        s.doc = i;
+        s.reserved[0] = s.reserved[1] = 0;
+        segs[seg_off] = s;
+        if (s.valid_len > 0) atomicMax(&s_valid_end, s.local_start + s.valid_len);
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      s_carry_segs += tot_segs;
+      s_carry_rows += tot_rows;
+    }
+    __syncthreads();
+  }
+
+  if (threadIdx.x == 0) {
+    int e = s_err;
+    if (e == 0 && (s_carry_rows != s_local || s_carry_segs > max_segs)) e = CP_ERR_METADATA;
+    s_err = e;
+    hdr->magic = kMetaMagic;
+    hdr->status = e;
+    hdr->strategy = strategy;
+    hdr->cp_size = cp;
+    hdr->rank = rank;
+    hdr->n_docs = n_docs;
+    hdr->s_local = s_local;
+    hdr->n_segs = e ? 0 : s_carry_segs;
+    hdr->valid_end = s_valid_end;
+    hdr->pad_between_seqs = pad;
+    hdr->total_tokens = T;
+    hdr->max_segs = max_segs;
+    hdr->seg_offset = (int32_t)seg_offset_bytes();
+    hdr->rows_offset = (int32_t)rows_offset_bytes(n_docs);
+    hdr->reserved[0] = hdr->reserved[1] = 0;
+    if (e) atomicCAS(&g_status_partition, 0, e);
+  }
+  __syncthreads();
+  if (s_err) return;
+
+  // pass 2: per-row tables, one warp per segment
+  const int n_segs = s_carry_segs;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int k = warp; k < n_segs; k += kThreads / 32) {
+    const Segment s = segs[k];
+    for (int u = lane; u < s.len; u += 32) {
+      const int t = s.local_start + u;
+      const int g = s.global_start + u;
+      const bool valid = u < s.valid_len;
+      idx[t] = g;
+      if (restore) restore[g] = R0 + t;
+      row_lo[t] = valid ? s.doc_lo : 0;
+      row_hi[t] = valid ? g : -1;
+    }
+  }
+}
+
+}  // namespace
+}  // namespace cpthd
+
+using namespace cpthd;
+
+extern "C" size_t cp_meta_bytes(int n_docs, int64_t s_local) {
+  if (n_docs < 0 || s_local < 0) return 0;
+  return meta_bytes_for(n_docs, s_local);
+}
+
+extern "C" int cp_partition_index(const int32_t* d_cu, const int32_t* d_cup, int n_docs,
+                                  int64_t total_tokens, int cp_size, int rank,
+                                  cp_strategy_t strategy, int pad_between_seqs, int32_t* d_idx,
+                                  int32_t* d_restore, void* d_meta, size_t meta_bytes,
+                                  void* stream) {
+  if (!d_cup || !d_idx || !d_meta) return CP_ERR_INVALID_ARG;
+  if (pad_between_seqs && !d_cu) return CP_ERR_INVALID_ARG;
+  if (n_docs < 1 || cp_size < 1 || rank < 0 || rank >= cp_size) return CP_ERR_INVALID_ARG;
+  if (strategy != CP_DUAL_CHUNK_SWAP && strategy != CP_NO_LOAD_BALANCE) return CP_ERR_INVALID_ARG;
+  if (total_tokens < 0 || total_tokens > INT32_MAX) return CP_ERR_INVALID_ARG;
+  if (total_tokens % cp_size) return CP_ERR_DIVISIBILITY;
+  const int64_t s_local = total_tokens / cp_size;
+  if (meta_bytes < meta_bytes_for(n_docs, s_local)) return CP_ERR_WORKSPACE;
+  if (!cpthd_host::aligned16(d_meta)) return CP_ERR_ALIGNMENT;
+  partition_kernel<<<1, 1024, 0, cpthd_host::as_stream(stream)>>>(
+      d_cu, d_cup, n_docs, (int)total_tokens, cp_size, rank, (int)strategy,
+      pad_between_seqs ? 1 : 0, d_idx, d_restore, reinterpret_cast<char*>(d_meta));
+  return cpthd_host::launch_status();
+}
+
+extern "C" int cpthd_status_partition(int reset) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_partition, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
+  if (reset) {
+    int z = 0;
+    if (cudaMemcpyToSymbol(g_status_partition, &z, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
+  }
+  return v;
+}

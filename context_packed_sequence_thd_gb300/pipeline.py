@@ -1,0 +1,279 @@
+"""Host orchestration of the emulated context-parallel attention step.
+
+Every CP rank of one all-gather CP group runs on one GPU, one after another
+on one stream.  The data movement the pages describe maps onto the library
+as follows ("[PyTorch] Add no-load-balance THD all-gather CP", §Sequence
+Diagram; "[PyTorch] Extend no-load-balance CP to the a2a comm type"):
+
+  get_batch_on_this_cp_rank   cp_partition_index + cp_thd_gather (Q/K/V/dO
+                              in one launch per rank, DUAL_CHUNK_SWAP); with
+                              NO_LOAD_BALANCE a rank's shard is a contiguous
+                              slice, so no copy is made at all
+  all-gather K/V              the ranks' local shards live side by side in one
+                              [cp*s_local, H, D] buffer, which *is* the
+                              all-gathered, rank-concatenated tensor
+  restore K/V order           cp_thd_gather with the restore index
+                              (DUAL_CHUNK_SWAP); a no-op for NO_LOAD_BALANCE,
+                              whose rank-concatenated order is the original
+                              order (the reorder the a2a page removes)
+  attention fwd / bwd         cp_attn_fwd / cp_attn_bwd per rank
+  unrestore + reduce-scatter  per-rank partial dK/dV summed in fp32 in
+                              original order, then cp_reduce_scatter_emul
+                              (gather by the rank's index + bf16 cast)
+  dQ/dK/dV tail-zeroing       cp_zero_tail, gated by the host-known valid end
+
+Only argument marshalling and buffer management happen here; every step is
+a kernel of libcpthd.
+"""
+from __future__ import annotations
+
+import contextlib
+import math
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional
+
+import numpy as np
+import torch
+
+from . import api
+
+DCS = api.DUAL_CHUNK_SWAP
+NLB = api.NO_LOAD_BALANCE
+STRATEGY_NAMES = {DCS: "dual_chunk_swap", NLB: "no_load_balance"}
+
+
+def rank_pairs(cu, cup, cp: int, rank: int, strategy: int, pad: int) -> int:
+    """(query, key) pairs attended by rank `rank`'s real-token queries, summed
+    per segment in closed form: a run of v real queries at global rows
+    gs..gs+v-1 of a document starting at a attends
+    v*(gs-a+1) + v*(v-1)/2 keys."""
+    cu = np.asarray(cu, dtype=np.int64)
+    cup = np.asarray(cup, dtype=np.int64)
+    T = int(cup[-1])
+    total = 0
+
+    def run(gs, v, a):
+        return v * (gs - a + 1) + v * (v - 1) // 2 if v > 0 else 0
+
+    for i in range(len(cup) - 1):
+        a, P = int(cup[i]), int(cup[i + 1] - cup[i])
+        L = int(cu[i + 1] - cu[i]) if pad else P
+        if strategy == DCS:
+            c = P // (2 * cp)
+            for ch in (rank, 2 * cp - 1 - rank):
+                gs = a + ch * c
+                v = min(max(L - ch * c, 0), c)
+                total += run(gs, v, a)
+        else:
+            s_local = T // cp
+            lo, hi = max(a, rank * s_local), min(a + P, (rank + 1) * s_local)
+            if hi > lo:
+                v = min(max(a + L - lo, 0), hi - lo)
+                total += run(lo, v, a)
+    return total
+
+
+@dataclass
+class RankMeta:
+    idx: torch.Tensor          # int32 [s_local]
+    meta: torch.Tensor         # uint8 [meta_bytes]
+    valid_end: int             # host-known local valid end (gates the tail-zero)
+    pairs: int
+
+
+@dataclass
+class CPPlan:
+    """Partition metadata of all ranks for one (cu, cup, cp, strategy)."""
+    cu: np.ndarray
+    cup: np.ndarray
+    cp: int
+    strategy: int
+    pad: int
+    H: int
+    D: int
+    device: torch.device
+    d_cu: torch.Tensor = field(init=False)
+    d_cup: torch.Tensor = field(init=False)
+    restore: torch.Tensor = field(init=False)
+    ranks: List[RankMeta] = field(init=False)
+
+    def __post_init__(self):
+        self.cu = np.asarray(self.cu, dtype=np.int32)
+        self.cup = np.asarray(self.cup, dtype=np.int32)
+        st = api.cp_validate_seqlens(self.cu, self.cup, self.T, self.cp, self.strategy, self.pad)
+        if st != 0:
+            raise api.CpError("cp_validate_seqlens", st)
+        self.d_cu = torch.from_numpy(self.cu).to(self.device)
+        self.d_cup = torch.from_numpy(self.cup).to(self.device)
+        self.restore = torch.empty(self.T, dtype=torch.int32, device=self.device)
+        nbytes = api.cp_meta_bytes(self.n_docs, self.s_local)
+        self.ranks = []
+        for r in range(self.cp):
+            self.ranks.append(RankMeta(
+                idx=torch.empty(self.s_local, dtype=torch.int32, device=self.device),
+                meta=torch.empty(nbytes, dtype=torch.uint8, device=self.device),
+                valid_end=api.cp_valid_end(self.cu, self.cup, self.cp, r, self.strategy, self.pad),
+                pairs=rank_pairs(self.cu, self.cup, self.cp, r, self.strategy, self.pad)))
+        self.build_index()
+
+    @property
+    def T(self) -> int:
+        return int(self.cup[-1])
+
+    @property
+    def n_docs(self) -> int:
+        return len(self.cup) - 1
+
+    @property
+    def s_local(self) -> int:
+        return self.T // self.cp
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def build_index(self, stream=None) -> int:
+        """One partition launch per rank (fills idx, meta and the restore index)."""
+        for r, rm in enumerate(self.ranks):
+            api.cp_partition_index(self.d_cu if self.pad else None, self.d_cup, self.T, self.cp, r,
+                                   self.strategy, self.pad, rm.idx, self.restore, rm.meta, stream)
+        return self.cp
+
+    def local(self, buf: torch.Tensor, r: int) -> torch.Tensor:
+        return buf[r * self.s_local:(r + 1) * self.s_local]
+
+
+class CPAttention:
+    """Buffers and the full emulated CP forward/backward for one plan."""
+
+    def __init__(self, plan: CPPlan):
+        self.plan = plan
+        p = plan
+        dev, T, H, D = p.device, p.T, p.H, p.D
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        # rank-concatenated buffers: rank r's shard is rows [r*s_local, (r+1)*s_local);
+        # NO_LOAD_BALANCE shards are views of the inputs, so nothing is allocated
+        dcs = p.strategy == DCS
+        self.qc = torch.empty(T, H, D, **bf) if dcs else None
+        self.kc = torch.empty(T, H, D, **bf) if dcs else None
+        self.vc = torch.empty(T, H, D, **bf) if dcs else None
+        self.doc = torch.empty(T, H, D, **bf) if dcs else None
+        self.oc = torch.empty(T, H, D, **bf)
+        self.lse = torch.empty(p.cp, H, p.s_local, dtype=torch.float32, device=dev)
+        self.k_full = torch.empty(T, H, D, **bf) if p.strategy == DCS else None
+        self.v_full = torch.empty(T, H, D, **bf) if p.strategy == DCS else None
+        self.dqc = torch.empty(T, H, D, **bf)
+        self.dkc = torch.empty(T, H, D, **bf)
+        self.dvc = torch.empty(T, H, D, **bf)
+        self.dk_acc = torch.empty(T, H, D, dtype=torch.float32, device=dev)
+        self.dv_acc = torch.empty(T, H, D, dtype=torch.float32, device=dev)
+        ws = api.cp_attn_bwd_workspace_bytes(p.s_local, H)
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.launches = 0
+        # optional per-call CUDA-event timing: category -> [(start, end), ...]
+        self.events: Optional[Dict[str, list]] = None
+
+    @contextlib.contextmanager
+    def _timed(self, category: str, stream=None):
+        if self.events is None:
+            yield
+            return
+        s = torch.cuda.current_stream() if stream is None else stream
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        yield
+        e1.record(s)
+        self.events.setdefault(category, []).append((e0, e1))
+
+    def event_ms(self) -> Dict[str, List[float]]:
+        """Per-call durations (ms) recorded since events were enabled."""
+        return {k: [a.elapsed_time(b) for a, b in v] for k, v in (self.events or {}).items()}
+
+    # -- data movement ------------------------------------------------------
+    def shard_inputs(self, q, k, v, do=None, stream=None):
+        """get_batch_on_this_cp_rank for every rank (plus dO for the backward)."""
+        p = self.plan
+        if p.strategy == NLB:
+            # contiguous shards: the rank-concatenated buffer is the input itself
+            self.qc, self.kc, self.vc = q, k, v
+            if do is not None:
+                self.doc = do
+            return
+        srcs = [q, k, v] + ([do] if do is not None else [])
+        for r, rm in enumerate(p.ranks):
+            dsts = [p.local(self.qc, r), p.local(self.kc, r), p.local(self.vc, r)]
+            if do is not None:
+                dsts.append(p.local(self.doc, r))
+            with self._timed("partition_gather", stream):
+                api.cp_thd_gather(srcs, dsts, rm.idx, stream)
+            self.launches += 1
+
+    def restore_kv(self, stream=None):
+        """All-gather (free: shards are side by side) + restore to original order."""
+        p = self.plan
+        if p.strategy == NLB:
+            return self.kc, self.vc
+        with self._timed("restore_gather", stream):
+            api.cp_thd_gather([self.kc, self.vc], [self.k_full, self.v_full], p.restore, stream)
+        self.launches += 1
+        return self.k_full, self.v_full
+
+    # -- attention ------------------------------------------------------------
+    def forward(self, stream=None):
+        p = self.plan
+        k_full, v_full = self.restore_kv(stream)
+        for r in range(p.cp):
+            with self._timed("attn_fwd", stream):
+                api.cp_attn_fwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
+                                self.lse[r], p.ranks[r].meta, p.T, p.cp, r, p.strategy, p.scale,
+                                stream)
+            self.launches += 1
+        return k_full, v_full
+
+    def backward(self, k_full, v_full, stream=None):
+        p = self.plan
+        if api.cp_zero_tail([self.dk_acc, self.dv_acc], 0, stream=stream):
+            self.launches += 1
+        for r in range(p.cp):
+            with self._timed("attn_bwd", stream):
+                api.cp_attn_bwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
+                                self.lse[r], p.local(self.doc, r), p.local(self.dqc, r),
+                                self.dk_acc, self.dv_acc, p.ranks[r].meta, p.T, p.cp, r,
+                                p.strategy, p.scale, self.ws, stream)
+            self.launches += 3
+        for r, rm in enumerate(p.ranks):
+            with self._timed("reduce_scatter_emul", stream):
+                if p.strategy == DCS:
+                    api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc],
+                                               [p.local(self.dkc, r), p.local(self.dvc, r)],
+                                               rm.idx, 0, p.s_local, stream)
+                else:
+                    api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc],
+                                               [p.local(self.dkc, r), p.local(self.dvc, r)],
+                                               None, r * p.s_local, p.s_local, stream)
+            self.launches += 1
+            if api.cp_zero_tail([p.local(self.dqc, r), p.local(self.dkc, r), p.local(self.dvc, r)],
+                                rm.valid_end, stream=stream):
+                self.launches += 1
+
+    def step(self, q, k, v, do=None, stream=None, rebuild_index: bool = True):
+        """One pass of the whole hot path: partition, shard, restore, fwd (+bwd)."""
+        if rebuild_index:
+            self.launches += self.plan.build_index(stream)
+        self.shard_inputs(q, k, v, do, stream)
+        k_full, v_full = self.forward(stream)
+        if do is not None:
+            self.backward(k_full, v_full, stream)
+
+    # -- results in original order (for checks) ------------------------------
+    def rank_rows(self, r: int) -> torch.Tensor:
+        return self.plan.ranks[r].idx.long()
+
+    def flops(self, bwd: bool) -> Dict[str, float]:
+        p = self.plan
+        pairs = sum(rm.pairs for rm in p.ranks)
+        f = {"fwd": 4.0 * p.D * p.H * pairs}
+        if bwd:
+            f["bwd"] = 10.0 * p.D * p.H * pairs
+        return f

@@ -1,0 +1,223 @@
+/*
+ * cpthd.h -- C ABI of libcpthd.so: context-parallel causal self-attention over
+ * THD-packed documents, every context-parallel (CP) rank emulated on one GPU.
+ *
+ * Sources of the operations (TransformerEngine pages):
+ *   [AG]  "[PyTorch] Add no-load-balance THD all-gather CP"
+ *   [A2A] "[PyTorch] Extend no-load-balance CP to the a2a comm type"
+ *   [P2P] "THD P2P context-parallel regression when padded cu_seqlens are
+ *          value-equal but not object-identical"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout "THD": a packed tensor [rows, H, D] of bf16, row-major, one row per
+ *   token (row_bytes = 2*H*D).  Documents are delimited by
+ *   cu_seqlens_padded ("cup", int32 [n_docs+1], physical offsets, cup[0]=0,
+ *   cup[n_docs] = total_tokens = T).  cu_seqlens ("cu", int32 [n_docs+1])
+ *   gives the real token counts L_i = cu[i+1]-cu[i] <= P_i = cup[i+1]-cup[i];
+ *   document i's real tokens are rows [cup[i], cup[i]+L_i), the rest of its
+ *   padded range is padding.  When pad_between_seqs == 0, cu is not read and
+ *   L_i = P_i.
+ * Strategies ([AG] §What changed, §Why; [A2A] first paragraph):
+ *   DUAL_CHUNK_SWAP: each document's padded range is cut into 2*cp_size equal
+ *     chunks; rank r holds chunk r then chunk 2*cp_size-1-r of every document,
+ *     documents in order.  Needs P_i % (2*cp_size) == 0 for every document.
+ *   NO_LOAD_BALANCE: rank r holds the contiguous physical rows
+ *     [r*s_local, (r+1)*s_local), s_local = T/cp_size.  Needs T % cp_size == 0.
+ *   Both: causal self-attention without a sliding window, equal Q/K/V lengths
+ *   ([AG] §Scope and constraints).  Forward and backward must use the same
+ *   strategy and the same metadata ([AG] §What changed, 4th item).
+ * Memory: the caller owns every buffer (host and device) and the stream.  No
+ *   entry point allocates or frees memory or synchronises, except
+ *   cp_device_status (documented below).  Device pointers must be 16-byte
+ *   aligned.  All launches are asynchronous on `stream` (a cudaStream_t; NULL
+ *   is the legacy default stream).
+ * Errors: every entry point returns a cp_status_t.  Arguments are validated on
+ *   the host before anything is launched; a failed validation launches
+ *   nothing.  A failed launch returns CP_ERR_CUDA.  Errors that only the
+ *   device can see (bad cu_seqlens values, an out-of-range index) are written
+ *   to the metadata header (status field) and to a per-device status word that
+ *   cp_device_status reads; kernels given metadata with a non-zero status
+ *   write nothing.  Nothing traps the GPU.
+ */
+#ifndef CPTHD_H
+#define CPTHD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CP_DUAL_CHUNK_SWAP = 0, /* default of [AG] */
+  CP_NO_LOAD_BALANCE = 1  /* "flat" sharding of [AG] / [A2A] */
+} cp_strategy_t;
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = -1,  /* null pointer, negative size, rank out of range ... */
+  CP_ERR_DIVISIBILITY = -2, /* P_i % (2*cp) != 0 (DCS) or T % cp != 0 (NLB) */
+  CP_ERR_UNSUPPORTED = -3,  /* head dim other than 64/128, too many heads ... */
+  CP_ERR_ALIGNMENT = -4,    /* pointer or row size not 16-byte aligned */
+  CP_ERR_CUDA = -5,         /* a CUDA launch or runtime call failed */
+  CP_ERR_WORKSPACE = -6,    /* metadata or workspace buffer too small */
+  CP_ERR_METADATA = -7      /* cu_seqlens values inconsistent (device-detected) */
+} cp_status_t;
+
+/* Human-readable name of a status code (static storage). */
+const char* cp_status_string(int status);
+
+/* ABI version of this header (major*100 + minor). */
+int cp_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Host-side metadata helpers (host pointers, no GPU work).
+ * ------------------------------------------------------------------------- */
+
+/* pad_between_seqs decided from VALUES, never from object identity
+ * ([P2P] §Describe the bug, §Expected behavior): *out = 1 when any of the
+ * n_docs+1 entries of cu_host and cup_host differ, else 0.  cup_host == NULL
+ * means "no padded offsets given" and yields 0.  cu_host, out must be
+ * non-NULL; n_docs >= 0. */
+int cp_detect_pad_between_seqs(const int32_t* cu_host, const int32_t* cup_host, int n_docs,
+                               int* out);
+
+/* Checks host copies of the offsets against the strategy's constraints:
+ * cup[0]==0, cup[n]==total_tokens, cup non-decreasing; with pad_between_seqs,
+ * cu[0]==0 and 0 <= L_i <= P_i; DCS: P_i % (2*cp_size) == 0; NLB:
+ * total_tokens % cp_size == 0.  Returns CP_OK or the first violation. */
+int cp_validate_seqlens(const int32_t* cu_host, const int32_t* cup_host, int n_docs,
+                        int64_t total_tokens, int cp_size, cp_strategy_t strategy,
+                        int pad_between_seqs);
+
+/* Host-known valid end of a layout: one past the last real-token row.
+ * rank in [0, cp_size): rank-local layout under `strategy`;
+ * rank == -1: the full packed layout.  Used to gate cp_zero_tail. */
+int cp_valid_end(const int32_t* cu_host, const int32_t* cup_host, int n_docs, int cp_size,
+                 int rank, cp_strategy_t strategy, int pad_between_seqs, int64_t* out);
+
+/* ---------------------------------------------------------------------------
+ * Partition index ([AG] §What changed: native THD partition index for CUDA
+ * batch slicing; metadata keeps logical document boundaries).
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of device metadata cp_partition_index writes for one rank:
+ * a 64-byte header, a segment table (32 bytes x (2*n_docs+2)) and two int32
+ * tables of s_local entries (each local row's document start and last
+ * attended key, -1 for padding rows). */
+size_t cp_meta_bytes(int n_docs, int64_t s_local);
+
+/* One launch.  Reads d_cu / d_cup (device, int32 [n_docs+1]; d_cu is only
+ * read when pad_between_seqs != 0) and writes, for rank `rank`:
+ *   d_idx[s_local]     global row of each local row, in local order;
+ *   d_restore[...]     (nullable) d_restore[d_idx[t]] = rank*s_local + t, i.e.
+ *                      this rank's entries of the inverse of the
+ *                      rank-concatenated partition (the K/V restore index of
+ *                      [AG] §Sequence Diagram; call once per rank to fill all
+ *                      total_tokens entries);
+ *   d_meta[meta_bytes] the rank's segment table and per-row tables consumed
+ *                      by the attention kernels.
+ * s_local = total_tokens / cp_size.  Offsets that break the strategy's
+ * constraints set the header status (CP_ERR_DIVISIBILITY / CP_ERR_METADATA)
+ * and the device status word; idx/restore are then left unwritten. */
+int cp_partition_index(const int32_t* d_cu, const int32_t* d_cup, int n_docs,
+                       int64_t total_tokens, int cp_size, int rank, cp_strategy_t strategy,
+                       int pad_between_seqs, int32_t* d_idx, int32_t* d_restore, void* d_meta,
+                       size_t meta_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * THD row gather / scatter: the index_select restore/unrestore of [AG]
+ * §Sequence Diagram, bandwidth bound per [A2A] (paragraph on the 8xH200
+ * measurement).  Up to 4 tensors share one index and one launch.
+ * ------------------------------------------------------------------------- */
+
+/* d_dst[k] row i = d_src[k] row d_idx[i], i in [0, n_rows), for k < n_tensors.
+ * d_src / d_dst are HOST arrays of n_tensors DEVICE pointers; rows are
+ * row_bytes long (row_bytes % 16 == 0); d_idx is device int32 [n_rows] with
+ * values in [0, src_rows) (a value outside is skipped and sets the device
+ * status word).  Destinations must not overlap sources. */
+int cp_thd_gather(const void* const* d_src, void* const* d_dst, int n_tensors,
+                  const int32_t* d_idx, int64_t n_rows, int64_t src_rows, int64_t row_bytes,
+                  void* stream);
+
+/* d_dst[k] row d_idx[i] = d_src[k] row i, i in [0, n_rows).  d_idx values in
+ * [0, dst_rows) and pairwise distinct (an injective map; duplicates give an
+ * unspecified winner). */
+int cp_thd_scatter(const void* const* d_src, void* const* d_dst, int n_tensors,
+                   const int32_t* d_idx, int64_t n_rows, int64_t dst_rows, int64_t row_bytes,
+                   void* stream);
+
+/* Emulated reduce-scatter epilogue of the dK/dV path ([AG] §Sequence Diagram,
+ * "unrestore dK/dV for reduce-scatter"): the fp32 accumulators hold the sum
+ * over ranks of the per-rank partials in original order; rank r's local
+ * gradient is that sum gathered by its partition index and rounded to bf16:
+ *   d_dst[k] row t = bf16(d_accum[k] row (d_idx ? d_idx[t] : row0 + t)).
+ * Rows are H*D values: fp32 in, bf16 out.  d_accum / d_dst are host arrays of
+ * n_tensors (<= 4) device pointers. */
+int cp_reduce_scatter_emul(const float* const* d_accum, void* const* d_dst, int n_tensors,
+                           const int32_t* d_idx, int64_t row0, int64_t n_rows,
+                           int64_t accum_rows, int H, int D, void* stream);
+
+/* Gradient tail-zeroing ([P2P] §Describe the bug, last paragraph; §Expected
+ * behavior: gated when no tail exists, graph-safe).  Zeroes rows
+ * [valid_end, rows) of each of n_tensors (<= 4) tensors of row_bytes-long rows.
+ *   valid_end >= 0: host-known; valid_end == rows launches NOTHING.
+ *   valid_end <  0: read *d_valid_end on the device (graph-safe form; one
+ *                   launch that exits early when there is no tail).
+ * *launched (nullable host int) reports whether a kernel was launched.
+ * valid_end = 0 zeroes whole tensors (used to clear dK/dV accumulators). */
+int cp_zero_tail(void* const* d_rows, int n_tensors, int64_t rows, int64_t row_bytes,
+                 int64_t valid_end, const int32_t* d_valid_end, void* stream, int* launched);
+
+/* ---------------------------------------------------------------------------
+ * Causal varlen attention of one rank's local queries against the full K/V
+ * ([AG] §Why, §Scope and constraints: causal, window_size=(-1,0), document
+ * boundaries from THD metadata).  For local row t at global row g of document
+ * i: keys j in [cup[i], g] when g is a real token; padding rows get O = 0,
+ * LSE = -inf, dQ = 0.  Scores s = softmax_scale * q.k; LSE in natural log.
+ * DUAL_CHUNK_SWAP's two chunks per rank are handled in ONE launch.
+ * ------------------------------------------------------------------------- */
+
+/* q_local [s_local,H,D] bf16 (rank-local order); k_full, v_full [T,H,D] bf16
+ * in original order (the restored all-gather); o_local [s_local,H,D] bf16;
+ * lse_local [H, s_local] fp32.  d_meta is the rank's metadata from
+ * cp_partition_index (same cp_size, rank, strategy).  D in {64, 128};
+ * H*D*2 <= 65535*16.  Deterministic. */
+int cp_attn_fwd(const void* q_local, const void* k_full, const void* v_full, void* o_local,
+                float* lse_local, const void* d_meta, size_t meta_bytes, int64_t total_tokens,
+                int H, int D, int cp_size, int rank, cp_strategy_t strategy,
+                float softmax_scale, void* stream);
+
+/* Device scratch cp_attn_bwd needs: Delta = rowsum(dO * O), fp32 [H, s_local]. */
+size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H);
+
+/* Backward of cp_attn_fwd for one rank.  Inputs as for cp_attn_fwd plus
+ * o_local / lse_local from the forward and do_local [s_local,H,D] bf16.
+ * Writes dq_local [s_local,H,D] bf16 (overwritten) and ADDS this rank's
+ * partial dK/dV into dk_accum / dv_accum (fp32 [T,H,D], original order; zero
+ * them before rank 0 -- e.g. cp_zero_tail with valid_end = 0).  Calling the
+ * ranks in a fixed order on one stream gives a bitwise deterministic sum (no
+ * atomics).  d_workspace: cp_attn_bwd_workspace_bytes bytes of device scratch,
+ * contents need not be initialised. */
+int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full, const void* o_local,
+                const float* lse_local, const void* do_local, void* dq_local, float* dk_accum,
+                float* dv_accum, const void* d_meta, size_t meta_bytes, int64_t total_tokens,
+                int H, int D, int cp_size, int rank, cp_strategy_t strategy, float softmax_scale,
+                void* d_workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics
+ * ------------------------------------------------------------------------- */
+
+/* Reads (and when reset != 0 clears) the current device's status word:
+ * CP_OK or the first device-detected error since the last reset.  This is
+ * the one entry point that synchronises (it waits for all prior work). */
+int cp_device_status(int* status, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPTHD_H */

@@ -247,3 +247,13 @@ def attn_bwd(q, k, v, o, lse, dout, cu, cup, pad: int, scale: Optional[float] = 
                         None if qm is None else qm.ctypes.data, hs.ctypes.data, len(hs),
                         dq.ctypes.data, dk.ctypes.data, dv.ctypes.data)
     return dq, dk, dv
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 round-to-nearest-even, returned as the bf16 bit patterns
+    (uint16).  Plain integer arithmetic on the fp32 bit pattern: add 0x7FFF
+    plus the lowest kept bit, then drop the low 16 bits (NaN is not handled;
+    the inputs here are finite)."""
+    b = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).view(np.uint32).astype(np.uint64)
+    lsb = (b >> 16) & 1
+    return ((b + 0x7FFF + lsb) >> 16).astype(np.uint16)

@@ -151,3 +151,18 @@ def test_workload_recipes():
     assert oracle.pad_between_seqs(wl5.cu, wl5.cup) == 1
     eq = inputs.cfg5(value_equal=True)
     assert eq.cu is not eq.cup and oracle.pad_between_seqs(eq.cu, eq.cup) == 0
+
+
+def test_bf16_round_nearest_even():
+    """The oracle's fp32->bf16 rounding, pinned to torch's CPU conversion and
+    to hand-made ties (1 + 2^-8 is a tie that rounds to even = 1.0;
+    1 + 3*2^-8 rounds up to 1 + 2^-6)."""
+    import torch
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.standard_normal(10000).astype(np.float32) * 10,
+                        np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 0.0, -0.0],
+                                 dtype=np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(oracle.bf16_round(x), want)
+    assert oracle.bf16_round(np.float32(1 + 2 ** -8)) == 0x3F80
+    assert oracle.bf16_round(np.float32(1 + 3 * 2 ** -8)) == 0x3F82
