@@ -624,9 +624,9 @@ attn_dkdv_mma(const AttnArgs a) {
 
 template <typename K>
 int launch(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const AttnArgs& a) {
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess)
+  // dynamic + static shared memory above 48 KB needs the opt-in attribute
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
     return CP_ERR_CUDA;
   kernel<<<grid, block, smem, st>>>(a);
   return cpthd_host::launch_status();
