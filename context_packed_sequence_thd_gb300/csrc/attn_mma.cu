@@ -19,6 +19,8 @@
 // the tile, keys [doc start, last real query], merged in increasing order.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace cpthd {
@@ -737,4 +739,80 @@ extern "C" int cpthd_status_attn(int reset) {
     if (cudaMemcpyToSymbol(g_status_attn, &z, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
   }
   return v;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free backward: the Delta scratch lives in a fixed device array
+// of this translation unit instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) float g_noalloc_scratch[CP_NOALLOC_MAX_SCRATCH_FLOATS];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device, with that device current, and cached.
+int noalloc_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CP_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return CP_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return CP_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return CP_OK;
+}
+
+}  // namespace
+
+extern "C" int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, const void* v_full,
+                                   const void* o_local, const float* lse_local,
+                                   const void* do_local, void* dq_local, float* dk_accum,
+                                   float* dv_accum, const void* d_meta, size_t meta_bytes,
+                                   int64_t total_tokens, int H, int D, int cp_size, int rank,
+                                   cp_strategy_t strategy, float softmax_scale, void* stream) {
+  int64_t s_local = 0;
+  int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
+                         rank, strategy, &s_local);
+  if (st != CP_OK) return st;
+  if (!o_local || !lse_local || !do_local || !dq_local || !dk_accum || !dv_accum)
+    return CP_ERR_INVALID_ARG;
+  if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local) ||
+      !cpthd_host::aligned16(do_local) || !cpthd_host::aligned16(dq_local) ||
+      !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum))
+    return CP_ERR_ALIGNMENT;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
+  if (s_local * (int64_t)H > (int64_t)CP_NOALLOC_MAX_SCRATCH_FLOATS) return CP_ERR_WORKSPACE;
+  if (s_local == 0) return CP_OK;
+  float* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != CP_OK) return st;
+  AttnArgs a{};
+  a.q = (const bf16*)q_local; a.k = (const bf16*)k_full; a.v = (const bf16*)v_full;
+  a.out = (const bf16*)o_local; a.lse = const_cast<float*>(lse_local);
+  a.dout = (const bf16*)do_local; a.dq = (bf16*)dq_local; a.dk = dk_accum; a.dv = dv_accum;
+  a.delta = scratch; a.meta = d_meta; a.meta_bytes = meta_bytes;
+  a.T = (int)total_tokens; a.H = H; a.s_local = (int)s_local; a.cp = cp_size; a.rank = rank;
+  a.strategy = (int)strategy; a.scale = softmax_scale; a.scale_log2 = softmax_scale * kLog2e;
+  cudaStream_t s = cpthd_host::as_stream(stream);
+  const int64_t threads = s_local * H * (D / 8);
+  dim3 dgrid((unsigned)((threads + 255) / 256));
+  if (D == 64) attn_delta<64><<<dgrid, 256, 0, s>>>(a);
+  else attn_delta<128><<<dgrid, 256, 0, s>>>(a);
+  if ((st = cpthd_host::launch_status()) != CP_OK) return st;
+  dim3 qgrid((unsigned)((s_local + BM - 1) / BM), (unsigned)H);
+  const size_t qsmem = (size_t)6 * 64 * D * 2;
+  st = D == 64 ? launch(attn_dq_mma<64>, qgrid, kThreads, qsmem, s, a)
+               : launch(attn_dq_mma<128>, qgrid, kThreads, qsmem, s, a);
+  if (st != CP_OK) return st;
+  dim3 kgrid((unsigned)((total_tokens + BN - 1) / BN), (unsigned)H);
+  const size_t ksmem = (size_t)6 * 64 * D * 2;
+  return D == 64 ? launch(attn_dkdv_mma<64>, kgrid, kThreads, ksmem, s, a)
+                 : launch(attn_dkdv_mma<128>, kgrid, kThreads, ksmem, s, a);
 }

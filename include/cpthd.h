@@ -207,6 +207,34 @@ int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full, con
                 int H, int D, int cp_size, int rank, cp_strategy_t strategy, float softmax_scale,
                 void* d_workspace, size_t workspace_bytes, void* stream);
 
+/* Largest Delta scratch cp_attn_bwd_noalloc can use: s_local*H <= this many
+ * floats (4 MiB of device memory per GPU that loads the library). */
+#define CP_NOALLOC_MAX_SCRATCH_FLOATS 1048576
+
+/* cp_attn_bwd without a caller-provided workspace, for callers that cannot
+ * allocate device memory at this point of their program: runtimes that hand
+ * out device memory only from an arena planned ahead of time, plugins whose
+ * host framework owns the device allocator and forbids allocations behind its
+ * back, and host code that must not pay the implicit device synchronisation
+ * of cudaMalloc/cudaFree.  The pages have no counterpart to this entry point;
+ * it only changes where the backward's scratch lives.
+ * Same arguments, results and errors as cp_attn_bwd, minus the workspace.
+ * The Delta scratch (fp32 [H, s_local]) lives in a fixed device array compiled
+ * into the library (CP_NOALLOC_MAX_SCRATCH_FLOATS floats, held on every GPU
+ * that loads the library until the process exits); nothing is allocated or
+ * freed.  s_local*H above that maximum returns CP_ERR_WORKSPACE before any
+ * launch.  The first call on a device looks up that array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  Every call shares the one array and leaves its last
+ * contents there; each call rewrites all the scratch it reads before reading
+ * it, so nothing has to start at zero.  Calls whose work overlaps on the GPU
+ * (other streams, other host threads) race on the array: serialise them. */
+int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, const void* v_full,
+                        const void* o_local, const float* lse_local, const void* do_local,
+                        void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
+                        size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
+                        int rank, cp_strategy_t strategy, float softmax_scale, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Diagnostics
  * ------------------------------------------------------------------------- */
