@@ -17,6 +17,7 @@ extern "C" const char* cp_status_string(int status) {
     case CP_ERR_CUDA: return "CP_ERR_CUDA";
     case CP_ERR_WORKSPACE: return "CP_ERR_WORKSPACE";
     case CP_ERR_METADATA: return "CP_ERR_METADATA";
+    case CP_ERR_TIMEOUT: return "CP_ERR_TIMEOUT";
     default: return "CP_ERR_UNKNOWN";
   }
 }
@@ -96,8 +97,8 @@ extern "C" int cp_device_status(int* status, int reset) {
   if (!status) return CP_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return CP_ERR_CUDA;
   int first = CP_OK;
-  const int parts[3] = {cpthd_status_partition(reset), cpthd_status_rows(reset),
-                        cpthd_status_attn(reset)};
+  const int parts[4] = {cpthd_status_partition(reset), cpthd_status_rows(reset),
+                        cpthd_status_attn(reset), cpthd_status_fwd_tc(reset)};
   for (int v : parts) {
     if (v == CP_ERR_CUDA) return CP_ERR_CUDA;
     if (first == CP_OK && v != CP_OK) first = v;

@@ -1,0 +1,476 @@
+// attn_fwd_tc.cu -- causal varlen attention forward of one CP rank on the
+// Blackwell tensor cores (tcgen05 + TMEM + TMA), built for sm_103a.
+//
+// What it computes ("[PyTorch] Add no-load-balance THD all-gather CP", §Why
+// and §Scope and constraints): for every local query row t of the rank (global
+// row g of document i), O_t = softmax_j(scale * q_t . k_j) v_j over the keys
+// j in [cup[i], g], and LSE_t in natural log; padding rows get O = 0,
+// LSE = -inf.  Both DUAL_CHUNK_SWAP chunks of a rank go through one launch:
+// the key range of every row comes from the rank's row tables.
+//
+// One CTA = one 128-row query tile of one head; 6 warps:
+//   warps 0-3  softmax: thread r owns query row r (TMEM lane r).  Loads S
+//              from TMEM, masks by the row's key range, online softmax in the
+//              log2 domain, rescales O in TMEM when the row max grows, writes
+//              P (bf16) into a 128B-swizzled K-major shared tile, and finally
+//              normalises O and stores O / LSE.
+//   warp 4     TMA producer: Q once, then K and V 128-key tiles into a
+//              2-stage ring (separate K / V barriers).
+//   warp 5     TMEM allocator and single-thread MMA issuer:
+//              S[j%2] = Q K_j^T (M=128, N=128, K=D) and O += P_j V_j
+//              (M=128, N=D, K=128, V as an MN-major operand), fp32
+//              accumulators in TMEM: S0 cols [0,128), S1 [128,256), O [256,256+D).
+// The MMA of S_{j+1} overlaps the softmax of S_j; the softmax of block j
+// waits for P V_{j-1} before it touches O or overwrites P.
+// Key blocks: only those some row of the tile attends (document and causal
+// skipping from the segment table), in increasing order.
+// Every wait is bounded (mbar_wait): a wait that runs out sets the device
+// status word to CP_ERR_TIMEOUT, the CTA drains its own copies / MMAs and
+// frees its TMEM before it returns.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace cpthd {
+
+static __device__ int g_status_fwd_tc;
+
+namespace {
+
+using namespace sm100;
+using bf16 = __nv_bfloat16;
+
+constexpr int TBM = 128;           // query rows per tile
+constexpr int TBN = 128;           // keys per block
+constexpr int kThreadsTc = 192;    // 6 warps
+constexpr int kStages = 2;         // K/V ring depth
+constexpr int kBoxBytes = 128 * 128;  // one 128-row x 128-byte TMA box
+constexpr int kMaxIvTc = TBM + 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr float kLn2f = 0.6931471805599453f;
+
+template <int D>
+struct Layout {
+  static constexpr int BOXES = D / 64;         // 64-element boxes along D
+  static constexpr int TILE = BOXES * kBoxBytes;  // one Q / K / V tile
+  static constexpr int Q = 0;
+  static constexpr int K = Q + TILE;
+  static constexpr int V = K + kStages * TILE;
+  static constexpr int P = V + kStages * TILE;  // 2 boxes: keys 0-63, 64-127
+  static constexpr int BYTES = P + 2 * kBoxBytes;
+};
+
+struct TcArgs {
+  bf16* o;
+  float* lse;
+  const void* meta;
+  size_t meta_bytes;
+  int T, H, s_local, cp, rank, strategy;
+  float scale_log2;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[kStages];
+  uint64_t v_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full;
+  uint64_t o_ready;
+  uint64_t mma_done;
+};
+
+__device__ __forceinline__ bool meta_ok_tc(const TcArgs& a, const MetaHeader* h) {
+  const bool fits = h->n_segs >= 0 && h->n_segs <= h->max_segs && h->seg_offset == 64 &&
+                    (int64_t)h->rows_offset >= 64 + 32 * (int64_t)h->max_segs &&
+                    (int64_t)h->rows_offset + 8 * (int64_t)a.s_local <= (int64_t)a.meta_bytes;
+  const bool ok = fits && h->magic == kMetaMagic && h->status == 0 && h->s_local == a.s_local &&
+                  h->rank == a.rank && h->cp_size == a.cp && h->strategy == a.strategy &&
+                  h->total_tokens == a.T;
+  if (!ok && threadIdx.x == 0)
+    atomicCAS(&g_status_fwd_tc, 0, h->status != 0 ? h->status : (int)CP_ERR_METADATA);
+  return ok;
+}
+
+__device__ __forceinline__ void fail(volatile int* abort) {
+  *abort = 1;
+  atomicCAS(&g_status_fwd_tc, 0, (int)CP_ERR_TIMEOUT);
+}
+
+struct Iter {  // flattened walk over the key-block intervals
+  const int2* iv;
+  int n, i, b;
+  __device__ void init(const int2* p, int cnt) { iv = p; n = cnt; i = 0; b = cnt > 0 ? p[0].x : 0; }
+  __device__ void next() {
+    if (b < iv[i].y) { ++b; } else { ++i; if (i < n) b = iv[i].x; }
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v, const TcArgs a) {
+  using L = Layout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ Bars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  __shared__ int2 s_iv[kMaxIvTc];
+  __shared__ int s_niv;
+
+  const MetaView m = meta_view(a.meta);
+  if (!meta_ok_tc(a, m.hdr)) return;
+  const int tile = gridDim.x - 1 - blockIdx.x;  // heavier (later) tiles first
+  const int h = blockIdx.y;
+  const int t0 = tile * TBM;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;  // 1024-aligned (128B swizzle)
+
+  auto bar = [](uint64_t& b) { return smem_u32(&b); };
+  if (threadIdx.x == 0) {
+    s_niv = build_kv_intervals(m, t0, min(TBM, a.s_local - t0), TBN, s_iv, kMaxIvTc);
+    s_abort = 0;
+    mbar_init(bar(bars.q_full), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(bars.k_full[s]), 1);
+      mbar_init(bar(bars.v_full[s]), 1);
+      mbar_init(bar(bars.kv_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(bars.s_full[s]), 1);
+      mbar_init(bar(bars.s_free[s]), 128);
+    }
+    mbar_init(bar(bars.p_full), 128);
+    mbar_init(bar(bars.o_ready), 1);
+    mbar_init(bar(bars.mma_done), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  int nb = 0;
+  for (int i = 0; i < s_niv; ++i) nb += s_iv[i].y - s_iv[i].x + 1;
+
+  if (nb == 0) {  // no real query row in this tile
+    if (threadIdx.x < TBM) {
+      const int t = t0 + threadIdx.x;
+      if (t < a.s_local) {
+        uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)t * a.H + h) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        a.lse[(int64_t)h * a.s_local + t] = -INFINITY;
+      }
+    }
+    return;
+  }
+
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(bars.q_full), L::TILE);
+#pragma unroll
+      for (int b = 0; b < L::BOXES; ++b)
+        tma_load_3d(sb + L::Q + b * kBoxBytes, &tm_q, bar(bars.q_full), b * 64, h, t0);
+      Iter it;
+      it.init(s_iv, s_niv);
+      int issued = 0;
+      for (int j = 0; j < nb; ++j, it.next()) {
+        const int st = j % kStages;
+        if (!mbar_wait(bar(bars.kv_empty[st]), ((j / kStages) & 1) ^ 1, &s_abort, kWaitLimitNs)) {
+          fail(&s_abort);
+          break;
+        }
+        const int key0 = it.b * TBN;
+        mbar_arrive_expect_tx(bar(bars.k_full[st]), L::TILE);
+#pragma unroll
+        for (int b = 0; b < L::BOXES; ++b)
+          tma_load_3d(sb + L::K + st * L::TILE + b * kBoxBytes, &tm_k, bar(bars.k_full[st]),
+                      b * 64, h, key0);
+        mbar_arrive_expect_tx(bar(bars.v_full[st]), L::TILE);
+#pragma unroll
+        for (int b = 0; b < L::BOXES; ++b)
+          tma_load_3d(sb + L::V + st * L::TILE + b * kBoxBytes, &tm_v, bar(bars.v_full[st]),
+                      b * 64, h, key0);
+        ++issued;
+      }
+      // drain: every copy this CTA issued must land before shared memory goes away
+      int never = 0;
+      mbar_wait(bar(bars.q_full), 0, &never, kWaitLimitNs);
+      for (int j = max(0, issued - kStages); j < issued; ++j) {
+        const int st = j % kStages;
+        mbar_wait(bar(bars.k_full[st]), (j / kStages) & 1, &never, kWaitLimitNs);
+        mbar_wait(bar(bars.v_full[st]), (j / kStages) & 1, &never, kWaitLimitNs);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, TBN, false, false);
+      constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+      bool ok = mbar_wait(bar(bars.q_full), 0, &s_abort, kWaitLimitNs);
+      if (!ok) fail(&s_abort);
+      tc_fence_after();
+      for (int j = 0; ok && j <= nb; ++j) {
+        if (j < nb) {
+          const int st = j % kStages, buf = j & 1;
+          if (!mbar_wait(bar(bars.k_full[st]), (j / kStages) & 1, &s_abort, kWaitLimitNs) ||
+              !mbar_wait(bar(bars.s_free[buf]), ((j >> 1) & 1) ^ 1, &s_abort, kWaitLimitNs)) {
+            fail(&s_abort);
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            const uint64_t da = sdesc_sw128(sb + L::Q + off, 16, 1024);
+            const uint64_t db = sdesc_sw128(sb + L::K + st * L::TILE + off, 16, 1024);
+            umma_bf16(tmem + buf * 128, da, db, idS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(bars.s_full[buf]));
+        }
+        if (j >= 1) {
+          const int i = j - 1, st = i % kStages;
+          if (!mbar_wait(bar(bars.p_full), i & 1, &s_abort, kWaitLimitNs) ||
+              !mbar_wait(bar(bars.v_full[st]), (i / kStages) & 1, &s_abort, kWaitLimitNs)) {
+            fail(&s_abort);
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < TBN / 16; ++kk) {
+            const uint64_t da =
+                sdesc_sw128(sb + L::P + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = sdesc_sw128(sb + L::V + st * L::TILE + kk * 2048, kBoxBytes, 1024);
+            umma_bf16(tmem + 256, da, db, idO, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(bar(bars.kv_empty[st]));
+          umma_commit(bar(bars.o_ready));
+        }
+      }
+      // drain: all MMAs issued by this thread must finish before TMEM is freed
+      umma_commit(bar(bars.mma_done));
+      int never = 0;
+      mbar_wait(bar(bars.mma_done), 0, &never, kWaitLimitNs);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax (warps 0-3)
+    const int row = threadIdx.x;  // = TMEM lane
+    const int t = t0 + row;
+    const int lo = t < a.s_local ? m.row_lo[t] : 0;
+    const int hi = t < a.s_local ? m.row_hi[t] : -1;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float sl2 = a.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    Iter it;
+    it.init(s_iv, s_niv);
+    bool ok = true;
+    uint8_t* p_row = smem_raw + (sb - smem_u32(smem_raw)) + L::P + row * 128;
+    // waits of the softmax warps are made warp-uniform (tcgen05.ld/st are
+    // .sync.aligned): the warp proceeds only when every lane saw the phase
+    auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool w = mbar_wait(b, parity, &s_abort, kWaitLimitNs);
+      return __all_sync(0xffffffffu, w);
+    };
+    for (int j = 0; j < nb; ++j, it.next()) {
+      const int buf = j & 1;
+      if (!wait_warp(bar(bars.s_full[buf]), (j >> 1) & 1)) {
+        fail(&s_abort);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[TBN];
+#pragma unroll
+      for (int c = 0; c < TBN / 32; ++c)
+        tmem_ld32(tmem + lane_base + buf * 128 + c * 32, reinterpret_cast<uint32_t*>(s + c * 32));
+      tc_fence_before();
+      mbar_arrive(bar(bars.s_free[buf]));
+
+      const int j0 = it.b * TBN;
+      if (!(lo <= j0 && hi >= j0 + TBN - 1)) {
+#pragma unroll
+        for (int c = 0; c < TBN; ++c) {
+          const int key = j0 + c;
+          if (key < lo || key > hi) s[c] = -INFINITY;
+        }
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < TBN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_new = fmaxf(m_run, mx);
+      const float mref = m_new == -INFINITY ? 0.f : m_new * sl2;
+      const float alpha = exp2f(m_run * sl2 - mref);
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < TBN; ++c) {
+        s[c] = exp2f(fmaf(s[c], sl2, -mref));
+        sum += s[c];
+      }
+      l_run = l_run * alpha + sum;
+      m_run = m_new;
+
+      if (j > 0) {
+        if (!wait_warp(bar(bars.o_ready), (j - 1) & 1)) {
+          fail(&s_abort);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tmem + lane_base + 256 + c * 32, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P row -> shared memory, bf16, K-major with the 128-byte swizzle
+#pragma unroll
+      for (int cc = 0; cc < TBN / 8; ++cc) {
+        uint4 v;
+        v.x = pack_bf16(s[cc * 8 + 0], s[cc * 8 + 1]);
+        v.y = pack_bf16(s[cc * 8 + 2], s[cc * 8 + 3]);
+        v.z = pack_bf16(s[cc * 8 + 4], s[cc * 8 + 5]);
+        v.w = pack_bf16(s[cc * 8 + 6], s[cc * 8 + 7]);
+        const int box = cc >> 3, chunk = (cc & 7) ^ (row & 7);
+        *reinterpret_cast<uint4*>(p_row + box * kBoxBytes + chunk * 16) = v;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(bars.p_full));
+    }
+    if (ok && !wait_warp(bar(bars.o_ready), (nb - 1) & 1)) {
+      fail(&s_abort);
+      ok = false;
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+        if (t < a.s_local) {
+          uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)t * a.H + h) * D + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(o[q * 8 + 0]) * inv, __uint_as_float(o[q * 8 + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(o[q * 8 + 2]) * inv, __uint_as_float(o[q * 8 + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(o[q * 8 + 4]) * inv, __uint_as_float(o[q * 8 + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(o[q * 8 + 6]) * inv, __uint_as_float(o[q * 8 + 7]) * inv);
+            dst[q] = v;
+          }
+        }
+      }
+      if (t < a.s_local)
+        a.lse[(int64_t)h * a.s_local + t] =
+            l_run > 0.f ? (m_run * sl2 + log2f(l_run)) * kLn2f : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [rows, H, D] bf16 viewed as a 3-D tensor (D, H, rows); 64 x 1 x 128 boxes,
+// 128-byte swizzle, zero fill outside.
+int make_map(CUtensorMap* map, const void* base, int64_t rows, int H, int D) {
+  auto enc = encode_fn();
+  if (!enc) return CP_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CP_OK : CP_ERR_CUDA;
+}
+
+template <int D>
+int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, cudaStream_t s) {
+  alignas(64) CUtensorMap mq, mk, mv;
+  int st;
+  if ((st = make_map(&mq, q, a.s_local, a.H, D)) != CP_OK) return st;
+  if ((st = make_map(&mk, k, a.T, a.H, D)) != CP_OK) return st;
+  if ((st = make_map(&mv, v, a.T, a.H, D)) != CP_OK) return st;
+  const int smem = Layout<D>::BYTES + 1024;
+  if (cudaFuncSetAttribute(attn_fwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return CP_ERR_CUDA;
+  dim3 grid((unsigned)((a.s_local + TBM - 1) / TBM), (unsigned)a.H);
+  attn_fwd_tc<D><<<grid, kThreadsTc, smem, s>>>(mq, mk, mv, a);
+  return cpthd_host::launch_status();
+}
+
+}  // namespace
+}  // namespace cpthd
+
+// Internal entry used by cp_attn_fwd (arguments already validated).
+int cpthd_attn_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse,
+                      const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
+                      int cp, int rank, int strategy, float scale_log2, cudaStream_t s) {
+  using namespace cpthd;
+  TcArgs a{};
+  a.o = (bf16*)o;
+  a.lse = lse;
+  a.meta = meta;
+  a.meta_bytes = meta_bytes;
+  a.T = T; a.H = H; a.s_local = s_local; a.cp = cp; a.rank = rank; a.strategy = strategy;
+  a.scale_log2 = scale_log2;
+  return D == 64 ? launch_fwd_tc<64>(q, k, v, a, s) : launch_fwd_tc<128>(q, k, v, a, s);
+}
+
+extern "C" int cpthd_status_fwd_tc(int reset) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, cpthd::g_status_fwd_tc, sizeof(int)) != cudaSuccess)
+    return CP_ERR_CUDA;
+  if (reset) {
+    int z = 0;
+    if (cudaMemcpyToSymbol(cpthd::g_status_fwd_tc, &z, sizeof(int)) != cudaSuccess)
+      return CP_ERR_CUDA;
+  }
+  return v;
+}

@@ -7,9 +7,9 @@
 // launch here because every local row carries its own global position and
 // document start (row tables built by the partition kernel).
 //
-// Kernels (bf16 in, fp32 accumulate, warp-level mma.sync m16n8k16):
-//   attn_fwd_mma   flash-style forward, 64-query tiles x 64-key blocks,
-//                  online softmax in registers, document/causal block skipping
+// The forward runs on the tcgen05 tensor cores (attn_fwd_tc.cu); this file
+// holds the entry points and the backward kernels (bf16 in, fp32 accumulate,
+// warp-level mma.sync m16n8k16):
 //   attn_delta     Delta = rowsum(dO * O) (fp32, [H, s_local])
 //   attn_dq_mma    dQ per 64-query tile, iterating its key blocks
 //   attn_dkdv_mma  dK/dV per 64-key block, iterating the query tiles that
@@ -31,7 +31,6 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kThreads = 128;  // 4 warps
 constexpr int BM = 64;         // query rows per tile (16 per warp)
 constexpr int BN = 64;         // keys per block
@@ -92,7 +91,6 @@ struct BlockIter {
   __device__ void init(const int2* p, int n) {
     iv = p; n_iv = n; i = 0; b = n > 0 ? p[0].x : 0;
   }
-  __device__ bool valid() const { return i < n_iv; }
   __device__ void next() {
     if (b < iv[i].y) { ++b; } else { ++i; if (i < n_iv) b = iv[i].x; }
   }
@@ -102,184 +100,6 @@ __device__ __forceinline__ int total_blocks(const int2* iv, int n) {
   int t = 0;
   for (int i = 0; i < n; ++i) t += iv[i].y - iv[i].x + 1;
   return t;
-}
-
-// ---------------------------------------------------------------------------
-// forward
-// ---------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(kThreads)
-attn_fwd_mma(const AttnArgs a) {
-  constexpr int RC = D / 8;
-  constexpr int TILE = 64 * D * 2;
-  extern __shared__ __align__(128) char smem[];
-  __shared__ int2 s_iv[kMaxIv];
-  __shared__ int s_niv;
-
-  const MetaView m = meta_view(a.meta);
-  if (!meta_ok(a, m)) return;
-  const int tile = gridDim.x - 1 - blockIdx.x;  // later tiles carry more causal work
-  const int h = blockIdx.y;
-  const int t0 = tile * BM;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK0 = sQ + TILE, sV0 = sQ + 3 * TILE;  // stages at +0 / +TILE
-
-  if (tid == 0) s_niv = build_kv_intervals(m, t0, min(BM, a.s_local - t0), BN, s_iv, kMaxIv);
-  load_tile<D>(sQ, a.q, t0, a.s_local, a.H, h);
-  cp_async_commit();
-  __syncthreads();
-
-  const int ra = warp * 16 + (lane >> 2), rb = ra + 8;
-  const int ta = t0 + ra, tb = t0 + rb;
-  const int lo_a = ta < a.s_local ? m.row_lo[ta] : 0, hi_a = ta < a.s_local ? m.row_hi[ta] : -1;
-  const int lo_b = tb < a.s_local ? m.row_lo[tb] : 0, hi_b = tb < a.s_local ? m.row_hi[tb] : -1;
-
-  BlockIter it;
-  it.init(s_iv, s_niv);
-  const int nb = total_blocks(s_iv, s_niv);
-
-  float o[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-  uint32_t qf[D / 16][4];
-
-  int cur_blk = 0;
-  if (nb > 0) {
-    cur_blk = it.b;
-    load_tile<D>(sK0, a.k, cur_blk * BN, a.T, a.H, h);
-    load_tile<D>(sV0, a.v, cur_blk * BN, a.T, a.H, h);
-    cp_async_commit();
-    it.next();
-  }
-  const int mi = lane >> 3, l8 = lane & 7;
-  for (int n = 0; n < nb; ++n) {
-    const int stage = n & 1;
-    if (n + 1 < nb) {
-      const uint32_t off = (stage ^ 1) * TILE;
-      load_tile<D>(sK0 + off, a.k, it.b * BN, a.T, a.H, h);
-      load_tile<D>(sV0 + off, a.v, it.b * BN, a.T, a.H, h);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    if (n == 0) {
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        ldsm_x4(sQ + swz(warp * 16 + (mi & 1) * 8 + l8, kk * 2 + (mi >> 1), RC), qf[kk][0],
-                qf[kk][1], qf[kk][2], qf[kk][3]);
-    }
-    const uint32_t sK = sK0 + stage * TILE, sV = sV0 + stage * TILE;
-    const int j0 = cur_blk * BN;
-
-    float s[BN / 8][4];
-#pragma unroll
-    for (int i = 0; i < BN / 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-      for (int np = 0; np < BN / 16; ++np) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sK + swz(np * 16 + (mi >> 1) * 8 + l8, kk * 2 + (mi & 1), RC), b0, b1, b2, b3);
-        mma_16816(s[2 * np], qf[kk], b0, b1);
-        mma_16816(s[2 * np + 1], qf[kk], b2, b3);
-      }
-    }
-    // mask + online softmax (log2 domain)
-    const bool full_a = lo_a <= j0 && hi_a >= j0 + BN - 1;
-    const bool full_b = lo_b <= j0 && hi_b >= j0 + BN - 1;
-    float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < BN / 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = j0 + nt * 8 + (lane & 3) * 2 + (e & 1);
-        float x = s[nt][e] * a.scale_log2;
-        if (e < 2) {
-          if (!full_a && !(key >= lo_a && key <= hi_a)) x = -INFINITY;
-          mx_a = fmaxf(mx_a, x);
-        } else {
-          if (!full_b && !(key >= lo_b && key <= hi_b)) x = -INFINITY;
-          mx_b = fmaxf(mx_b, x);
-        }
-        s[nt][e] = x;
-      }
-    }
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-    const float use_a = mn_a == -INFINITY ? 0.f : mn_a;
-    const float use_b = mn_b == -INFINITY ? 0.f : mn_b;
-    const float al_a = exp2f(m_a - use_a), al_b = exp2f(m_b - use_b);
-    m_a = mn_a;
-    m_b = mn_b;
-    float ps_a = 0.f, ps_b = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < BN / 8; ++nt) {
-      s[nt][0] = exp2f(s[nt][0] - use_a);
-      s[nt][1] = exp2f(s[nt][1] - use_a);
-      s[nt][2] = exp2f(s[nt][2] - use_b);
-      s[nt][3] = exp2f(s[nt][3] - use_b);
-      ps_a += s[nt][0] + s[nt][1];
-      ps_b += s[nt][2] + s[nt][3];
-    }
-    l_a = l_a * al_a + ps_a;
-    l_b = l_b * al_b + ps_b;
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      o[i][0] *= al_a; o[i][1] *= al_a;
-      o[i][2] *= al_b; o[i][3] *= al_b;
-    }
-    // O += P V
-#pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk) {
-      uint32_t pa[4];
-      pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-      pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-      pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sV + swz(kk * 16 + (mi & 1) * 8 + l8, dp * 2 + (mi >> 1), RC), b0, b1, b2, b3);
-        mma_16816(o[2 * dp], pa, b0, b1);
-        mma_16816(o[2 * dp + 1], pa, b2, b3);
-      }
-    }
-    __syncthreads();  // stage is refilled two iterations later
-    cur_blk = it.b;
-    it.next();
-  }
-
-  // epilogue
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-  const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f, inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
-  const int col = (lane & 3) * 2;
-  if (ta < a.s_local) {
-    bf16* dst = a.o + ((int64_t)ta * a.H + h) * D;
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt)
-      *reinterpret_cast<uint32_t*>(dst + nt * 8 + col) = pack_bf16(o[nt][0] * inv_a, o[nt][1] * inv_a);
-    if ((lane & 3) == 0)
-      a.lse[(int64_t)h * a.s_local + ta] = l_a > 0.f ? (m_a + log2f(l_a)) * kLn2 : -INFINITY;
-  }
-  if (tb < a.s_local) {
-    bf16* dst = a.o + ((int64_t)tb * a.H + h) * D;
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt)
-      *reinterpret_cast<uint32_t*>(dst + nt * 8 + col) = pack_bf16(o[nt][2] * inv_b, o[nt][3] * inv_b);
-    if ((lane & 3) == 0)
-      a.lse[(int64_t)h * a.s_local + tb] = l_b > 0.f ? (m_b + log2f(l_b)) * kLn2 : -INFINITY;
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -669,16 +489,9 @@ extern "C" int cp_attn_fwd(const void* q_local, const void* k_full, const void* 
   if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local)) return CP_ERR_ALIGNMENT;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
   if (s_local == 0) return CP_OK;
-  AttnArgs a{};
-  a.q = (const bf16*)q_local; a.k = (const bf16*)k_full; a.v = (const bf16*)v_full;
-  a.o = (bf16*)o_local; a.lse = lse_local; a.meta = d_meta; a.meta_bytes = meta_bytes;
-  a.T = (int)total_tokens; a.H = H; a.s_local = (int)s_local; a.cp = cp_size; a.rank = rank;
-  a.strategy = (int)strategy; a.scale = softmax_scale; a.scale_log2 = softmax_scale * kLog2e;
-  dim3 grid((unsigned)((s_local + BM - 1) / BM), (unsigned)H);
-  cudaStream_t s = cpthd_host::as_stream(stream);
-  const size_t smem = (size_t)5 * 64 * D * 2;
-  return D == 64 ? launch(attn_fwd_mma<64>, grid, kThreads, smem, s, a)
-                 : launch(attn_fwd_mma<128>, grid, kThreads, smem, s, a);
+  return cpthd_attn_fwd_tc(q_local, k_full, v_full, o_local, lse_local, d_meta, meta_bytes,
+                           (int)total_tokens, H, D, (int)s_local, cp_size, rank, (int)strategy,
+                           softmax_scale * kLog2e, cpthd_host::as_stream(stream));
 }
 
 extern "C" size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H) {

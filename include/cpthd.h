@@ -63,7 +63,8 @@ typedef enum {
   CP_ERR_ALIGNMENT = -4,    /* pointer or row size not 16-byte aligned */
   CP_ERR_CUDA = -5,         /* a CUDA launch or runtime call failed */
   CP_ERR_WORKSPACE = -6,    /* metadata or workspace buffer too small */
-  CP_ERR_METADATA = -7      /* cu_seqlens values inconsistent (device-detected) */
+  CP_ERR_METADATA = -7,     /* cu_seqlens values inconsistent (device-detected) */
+  CP_ERR_TIMEOUT = -8       /* a bounded device-side wait ran out; results are invalid */
 } cp_status_t;
 
 /* Human-readable name of a status code (static storage). */
