@@ -97,8 +97,9 @@ extern "C" int cp_device_status(int* status, int reset) {
   if (!status) return CP_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return CP_ERR_CUDA;
   int first = CP_OK;
-  const int parts[4] = {cpthd_status_partition(reset), cpthd_status_rows(reset),
-                        cpthd_status_attn(reset), cpthd_status_fwd_tc(reset)};
+  const int parts[5] = {cpthd_status_partition(reset), cpthd_status_rows(reset),
+                        cpthd_status_attn(reset), cpthd_status_fwd_tc(reset),
+                        cpthd_status_bwd_tc(reset)};
   for (int v : parts) {
     if (v == CP_ERR_CUDA) return CP_ERR_CUDA;
     if (first == CP_OK && v != CP_OK) first = v;

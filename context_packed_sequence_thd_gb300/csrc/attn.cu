@@ -1,0 +1,244 @@
+// attn.cu -- entry points of the causal varlen attention of one CP rank
+// (cp_attn_fwd, cp_attn_bwd, cp_attn_bwd_noalloc) and the Delta kernel of the
+// backward.
+//
+// "[PyTorch] Add no-load-balance THD all-gather CP", §Why / §Scope and
+// constraints: causal, no sliding window, document boundaries from the THD
+// metadata; DUAL_CHUNK_SWAP's two attention steps per rank are fused into one
+// launch here because every local row carries its own global position and
+// document start (row tables built by the partition kernel).
+//
+// The forward and the dQ / dK-dV backward kernels run on the tcgen05 tensor
+// cores (attn_fwd_tc.cu, attn_bwd_tc.cu).  This file holds argument
+// validation and
+//   attn_delta  Delta = rowsum(dO * O) (fp32, [H, s_local]), the backward's
+//               only scratch.
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace cpthd {
+
+static __device__ int g_status_attn;
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct AttnArgs {
+  const bf16* q;     // [s_local, H, D]
+  const bf16* k;     // [T, H, D]
+  const bf16* v;     // [T, H, D]
+  bf16* o;           // [s_local, H, D]
+  float* lse;        // [H, s_local]
+  const bf16* dout;  // [s_local, H, D]
+  const bf16* out;   // [s_local, H, D]  (forward output, for Delta)
+  float* delta;      // [H, s_local]
+  bf16* dq;          // [s_local, H, D]
+  float* dk;         // [T, H, D] fp32 accumulators
+  float* dv;
+  const void* meta;
+  size_t meta_bytes;
+  int T, H, s_local, cp, rank, strategy;
+  float scale, scale_log2;
+};
+
+// ---------------------------------------------------------------------------
+// backward: Delta = rowsum(dO * O)
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) attn_delta(const AttnArgs a) {
+  constexpr int G = D / 8;  // threads per (row, head)
+  const int64_t gid = int64_t(blockIdx.x) * 256 + threadIdx.x;
+  const int64_t pair = gid / G;  // row * H + head
+  const int part = (int)(gid % G);
+  const int64_t n_pairs = (int64_t)a.s_local * a.H;
+  float acc = 0.f;
+  if (pair < n_pairs) {
+    const uint4 x = *reinterpret_cast<const uint4*>(a.dout + pair * D + part * 8);
+    const uint4 y = *reinterpret_cast<const uint4*>(a.out + pair * D + part * 8);
+    const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&x);
+    const __nv_bfloat162* yp = reinterpret_cast<const __nv_bfloat162*>(&y);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 fx = __bfloat1622float2(xp[i]), fy = __bfloat1622float2(yp[i]);
+      acc += fx.x * fy.x + fx.y * fy.y;
+    }
+  }
+#pragma unroll
+  for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (pair < n_pairs && part == 0) {
+    const int64_t row = pair / a.H;
+    const int h = (int)(pair % a.H);
+    a.delta[(int64_t)h * a.s_local + row] = acc;
+  }
+}
+
+int common_checks(const void* q, const void* k, const void* v, const void* meta, size_t meta_bytes,
+                  int64_t T, int H, int D, int cp, int rank, cp_strategy_t strategy,
+                  int64_t* s_local) {
+  if (!q || !k || !v || !meta) return CP_ERR_INVALID_ARG;
+  if (H < 1 || T < 0 || T > INT32_MAX || cp < 1 || rank < 0 || rank >= cp) return CP_ERR_INVALID_ARG;
+  if (strategy != CP_DUAL_CHUNK_SWAP && strategy != CP_NO_LOAD_BALANCE) return CP_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return CP_ERR_UNSUPPORTED;
+  if (H > 65535) return CP_ERR_UNSUPPORTED;
+  if (T % cp) return CP_ERR_DIVISIBILITY;
+  *s_local = T / cp;
+  if ((int64_t)T * H * D > ((int64_t)1 << 40)) return CP_ERR_UNSUPPORTED;
+  if (meta_bytes < 64) return CP_ERR_WORKSPACE;
+  if (!cpthd_host::aligned16(q) || !cpthd_host::aligned16(k) || !cpthd_host::aligned16(v) ||
+      !cpthd_host::aligned16(meta))
+    return CP_ERR_ALIGNMENT;
+  return CP_OK;
+}
+
+}  // namespace
+}  // namespace cpthd
+
+using namespace cpthd;
+
+extern "C" int cp_attn_fwd(const void* q_local, const void* k_full, const void* v_full,
+                           void* o_local, float* lse_local, const void* d_meta, size_t meta_bytes,
+                           int64_t total_tokens, int H, int D, int cp_size, int rank,
+                           cp_strategy_t strategy, float softmax_scale, void* stream) {
+  int64_t s_local = 0;
+  int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
+                         rank, strategy, &s_local);
+  if (st != CP_OK) return st;
+  if (!o_local || !lse_local) return CP_ERR_INVALID_ARG;
+  if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local)) return CP_ERR_ALIGNMENT;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
+  if (s_local == 0) return CP_OK;
+  return cpthd_attn_fwd_tc(q_local, k_full, v_full, o_local, lse_local, d_meta, meta_bytes,
+                           (int)total_tokens, H, D, (int)s_local, cp_size, rank, (int)strategy,
+                           softmax_scale * kLog2e, cpthd_host::as_stream(stream));
+}
+
+extern "C" size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H) {
+  if (s_local < 0 || H < 1) return 0;
+  return (size_t)s_local * H * sizeof(float);
+}
+
+extern "C" int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full,
+                           const void* o_local, const float* lse_local, const void* do_local,
+                           void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
+                           size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
+                           int rank, cp_strategy_t strategy, float softmax_scale,
+                           void* d_workspace, size_t workspace_bytes, void* stream) {
+  int64_t s_local = 0;
+  int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
+                         rank, strategy, &s_local);
+  if (st != CP_OK) return st;
+  if (!o_local || !lse_local || !do_local || !dq_local || !dk_accum || !dv_accum)
+    return CP_ERR_INVALID_ARG;
+  if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local) ||
+      !cpthd_host::aligned16(do_local) || !cpthd_host::aligned16(dq_local) ||
+      !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum))
+    return CP_ERR_ALIGNMENT;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
+  if (s_local == 0) return CP_OK;
+  if (!d_workspace || workspace_bytes < cp_attn_bwd_workspace_bytes(s_local, H))
+    return CP_ERR_WORKSPACE;
+  if (!cpthd_host::aligned16(d_workspace)) return CP_ERR_ALIGNMENT;
+  AttnArgs a{};
+  a.q = (const bf16*)q_local; a.k = (const bf16*)k_full; a.v = (const bf16*)v_full;
+  a.out = (const bf16*)o_local; a.lse = const_cast<float*>(lse_local);
+  a.dout = (const bf16*)do_local; a.dq = (bf16*)dq_local; a.dk = dk_accum; a.dv = dv_accum;
+  a.delta = (float*)d_workspace; a.meta = d_meta; a.meta_bytes = meta_bytes;
+  a.T = (int)total_tokens; a.H = H; a.s_local = (int)s_local; a.cp = cp_size; a.rank = rank;
+  a.strategy = (int)strategy; a.scale = softmax_scale; a.scale_log2 = softmax_scale * kLog2e;
+  cudaStream_t s = cpthd_host::as_stream(stream);
+  const int64_t threads = s_local * H * (D / 8);
+  dim3 dgrid((unsigned)((threads + 255) / 256));
+  if (D == 64) attn_delta<64><<<dgrid, 256, 0, s>>>(a);
+  else attn_delta<128><<<dgrid, 256, 0, s>>>(a);
+  if ((st = cpthd_host::launch_status()) != CP_OK) return st;
+  return cpthd_attn_bwd_tc(q_local, k_full, v_full, do_local, lse_local, a.delta, dq_local,
+                           dk_accum, dv_accum, d_meta, meta_bytes, (int)total_tokens, H, D,
+                           (int)s_local, cp_size, rank, (int)strategy, softmax_scale,
+                           softmax_scale * kLog2e, s);
+}
+
+extern "C" int cpthd_status_attn(int reset) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_attn, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
+  if (reset) {
+    int z = 0;
+    if (cudaMemcpyToSymbol(g_status_attn, &z, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
+  }
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free backward: the Delta scratch lives in a fixed device array
+// of this translation unit instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) float g_noalloc_scratch[CP_NOALLOC_MAX_SCRATCH_FLOATS];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device, with that device current, and cached.
+int noalloc_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CP_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return CP_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return CP_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return CP_OK;
+}
+
+}  // namespace
+
+extern "C" int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, const void* v_full,
+                                   const void* o_local, const float* lse_local,
+                                   const void* do_local, void* dq_local, float* dk_accum,
+                                   float* dv_accum, const void* d_meta, size_t meta_bytes,
+                                   int64_t total_tokens, int H, int D, int cp_size, int rank,
+                                   cp_strategy_t strategy, float softmax_scale, void* stream) {
+  int64_t s_local = 0;
+  int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
+                         rank, strategy, &s_local);
+  if (st != CP_OK) return st;
+  if (!o_local || !lse_local || !do_local || !dq_local || !dk_accum || !dv_accum)
+    return CP_ERR_INVALID_ARG;
+  if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local) ||
+      !cpthd_host::aligned16(do_local) || !cpthd_host::aligned16(dq_local) ||
+      !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum))
+    return CP_ERR_ALIGNMENT;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
+  if (s_local * (int64_t)H > (int64_t)CP_NOALLOC_MAX_SCRATCH_FLOATS) return CP_ERR_WORKSPACE;
+  if (s_local == 0) return CP_OK;
+  float* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != CP_OK) return st;
+  AttnArgs a{};
+  a.q = (const bf16*)q_local; a.k = (const bf16*)k_full; a.v = (const bf16*)v_full;
+  a.out = (const bf16*)o_local; a.lse = const_cast<float*>(lse_local);
+  a.dout = (const bf16*)do_local; a.dq = (bf16*)dq_local; a.dk = dk_accum; a.dv = dv_accum;
+  a.delta = scratch; a.meta = d_meta; a.meta_bytes = meta_bytes;
+  a.T = (int)total_tokens; a.H = H; a.s_local = (int)s_local; a.cp = cp_size; a.rank = rank;
+  a.strategy = (int)strategy; a.scale = softmax_scale; a.scale_log2 = softmax_scale * kLog2e;
+  cudaStream_t s = cpthd_host::as_stream(stream);
+  const int64_t threads = s_local * H * (D / 8);
+  dim3 dgrid((unsigned)((threads + 255) / 256));
+  if (D == 64) attn_delta<64><<<dgrid, 256, 0, s>>>(a);
+  else attn_delta<128><<<dgrid, 256, 0, s>>>(a);
+  if ((st = cpthd_host::launch_status()) != CP_OK) return st;
+  return cpthd_attn_bwd_tc(q_local, k_full, v_full, do_local, lse_local, a.delta, dq_local,
+                           dk_accum, dv_accum, d_meta, meta_bytes, (int)total_tokens, H, D,
+                           (int)s_local, cp_size, rank, (int)strategy, softmax_scale,
+                           softmax_scale * kLog2e, s);
+}

@@ -1,0 +1,688 @@
+// attn_bwd_tc.cu -- causal varlen attention backward of one CP rank on the
+// Blackwell tensor cores (tcgen05 + TMEM + TMA), built for sm_103a.
+//
+// The backward of the forward in attn_fwd_tc.cu ("[PyTorch] Add
+// no-load-balance THD all-gather CP", §What changed: backward uses the
+// forward's token layout): with Delta_t = dO_t . O_t (attn_delta),
+//   P = exp(scale q.k - LSE), dS = P (dO.v - Delta),
+//   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+// Two kernels, no atomics (bitwise deterministic):
+//
+// attn_dq_tc   one CTA per (128-query tile, head), iterating the key blocks
+//              the tile attends.  S = Q K^T and dP = dO V^T into TMEM
+//              (M=128 queries, N=128 keys); 4 compute warps (thread = query
+//              row) form dS and write it back into TMEM as bf16 over S;
+//              dQ += dS K with A = dS from TMEM, B = K as an MN-major operand.
+// attn_dkdv_tc one CTA per (128-key block, head), iterating the rank's query
+//              tiles that attend the block (segment table).  S^T = K Q^T and
+//              dP^T = V dO^T into TMEM (M=128 keys, N=128 queries); compute
+//              warps (thread = key row) form P^T and dS^T in TMEM over S^T and
+//              dP^T; dV += P^T dO and dK += dS^T Q (A from TMEM, B = dO / Q as
+//              MN-major operands).  The block's partial dK/dV are added into
+//              the caller's fp32 accumulators by the block's only owner.
+// Warp roles as in the forward: warps 0-3 compute, warp 4 TMA producer,
+// warp 5 TMEM allocator + single-thread MMA issuer.  Every wait is bounded.
+#include <math.h>
+
+#include "common.cuh"
+#include "sm100.cuh"
+#include "tma_host.cuh"
+
+namespace cpthd {
+
+static __device__ int g_status_bwd_tc;
+
+namespace {
+
+using namespace sm100;
+using bf16 = __nv_bfloat16;
+
+constexpr int kThr = 192;
+constexpr int kStg = 2;
+constexpr int kBox = 128 * 128;  // one 128-row x 128-byte TMA box
+constexpr int kMaxIv = 64;
+constexpr uint32_t kCols = 512;
+constexpr uint64_t kLimitNs = 4000000000ull;
+constexpr float kLog2ef = 1.4426950408889634f;
+
+struct BwdArgs {
+  const float* lse;    // [H, s_local]
+  const float* delta;  // [H, s_local]
+  bf16* dq;            // [s_local, H, D]
+  float* dk;           // [T, H, D]
+  float* dv;
+  const void* meta;
+  size_t meta_bytes;
+  int T, H, s_local, cp, rank, strategy;
+  float scale, scale_log2;
+};
+
+__device__ __forceinline__ bool meta_ok_bwd(const BwdArgs& a, const MetaHeader* h) {
+  const bool fits = h->n_segs >= 0 && h->n_segs <= h->max_segs && h->seg_offset == 64 &&
+                    (int64_t)h->rows_offset >= 64 + 32 * (int64_t)h->max_segs &&
+                    (int64_t)h->rows_offset + 8 * (int64_t)a.s_local <= (int64_t)a.meta_bytes;
+  const bool ok = fits && h->magic == kMetaMagic && h->status == 0 && h->s_local == a.s_local &&
+                  h->rank == a.rank && h->cp_size == a.cp && h->strategy == a.strategy &&
+                  h->total_tokens == a.T;
+  if (!ok && threadIdx.x == 0)
+    atomicCAS(&g_status_bwd_tc, 0, h->status != 0 ? h->status : (int)CP_ERR_METADATA);
+  return ok;
+}
+
+__device__ __forceinline__ void fail(volatile int* abort) {
+  *abort = 1;
+  atomicCAS(&g_status_bwd_tc, 0, (int)CP_ERR_TIMEOUT);
+}
+
+struct Iter {
+  const int2* iv;
+  int n, i, b;
+  __device__ void init(const int2* p, int cnt) { iv = p; n = cnt; i = 0; b = cnt > 0 ? p[0].x : 0; }
+  __device__ void next() {
+    if (b < iv[i].y) { ++b; } else { ++i; if (i < n) b = iv[i].x; }
+  }
+};
+
+__device__ __forceinline__ uint32_t bar_addr(uint64_t& b) { return smem_u32(&b); }
+
+// K-major operand offset of k-step kk (16 elements) inside a tile of
+// 64-element (128-byte) boxes of 128 rows.
+__device__ __forceinline__ uint32_t kmajor_off(int kk) { return (kk >> 2) * kBox + (kk & 3) * 32; }
+
+// ===========================================================================
+// dQ
+// ===========================================================================
+template <int D>
+struct DqLayout {
+  static constexpr int TILE = (D / 64) * kBox;
+  static constexpr int Q = 0;
+  static constexpr int DO = TILE;
+  static constexpr int K = 2 * TILE;
+  static constexpr int V = K + kStg * TILE;
+  static constexpr int BYTES = V + kStg * TILE;
+};
+
+struct DqBars {
+  uint64_t qd_full;
+  uint64_t k_full[kStg], v_full[kStg], kv_empty[kStg];
+  uint64_t st_full, ds_full, done, mma_done;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThr, 1)
+attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+           const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+           const BwdArgs a) {
+  using L = DqLayout<D>;
+  constexpr int BOXES = D / 64;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ DqBars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  __shared__ int2 s_iv[kMaxIv];
+  __shared__ int s_niv;
+
+  const MetaView m = meta_view(a.meta);
+  if (!meta_ok_bwd(a, m.hdr)) return;
+  const int tile = gridDim.x - 1 - blockIdx.x;
+  const int h = blockIdx.y;
+  const int t0 = tile * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
+
+  if (threadIdx.x == 0) {
+    s_niv = build_kv_intervals(m, t0, min(128, a.s_local - t0), 128, s_iv, kMaxIv);
+    s_abort = 0;
+    mbar_init(bar_addr(bars.qd_full), 1);
+    for (int s = 0; s < kStg; ++s) {
+      mbar_init(bar_addr(bars.k_full[s]), 1);
+      mbar_init(bar_addr(bars.v_full[s]), 1);
+      mbar_init(bar_addr(bars.kv_empty[s]), 1);
+    }
+    mbar_init(bar_addr(bars.st_full), 1);
+    mbar_init(bar_addr(bars.ds_full), 128);
+    mbar_init(bar_addr(bars.done), 1);
+    mbar_init(bar_addr(bars.mma_done), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  int nb = 0;
+  for (int i = 0; i < s_niv; ++i) nb += s_iv[i].y - s_iv[i].x + 1;
+  if (nb == 0) {  // no real query row: dQ = 0
+    if (threadIdx.x < 128 && t0 + (int)threadIdx.x < a.s_local) {
+      uint4* dst = reinterpret_cast<uint4*>(a.dq + ((int64_t)(t0 + threadIdx.x) * a.H + h) * D);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&s_tmem), kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;  // S [0,128)  dP [128,256)  dQ [256,256+D)
+
+  if (warp == 4) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_addr(bars.qd_full), 2 * L::TILE);
+#pragma unroll
+      for (int b = 0; b < BOXES; ++b) {
+        tma_load_3d(sb + L::Q + b * kBox, &tm_q, bar_addr(bars.qd_full), b * 64, h, t0);
+        tma_load_3d(sb + L::DO + b * kBox, &tm_do, bar_addr(bars.qd_full), b * 64, h, t0);
+      }
+      Iter it;
+      it.init(s_iv, s_niv);
+      int issued = 0;
+      for (int j = 0; j < nb; ++j, it.next()) {
+        const int st = j % kStg;
+        if (!mbar_wait(bar_addr(bars.kv_empty[st]), ((j / kStg) & 1) ^ 1, &s_abort, kLimitNs)) {
+          fail(&s_abort);
+          break;
+        }
+        const int key0 = it.b * 128;
+        mbar_arrive_expect_tx(bar_addr(bars.k_full[st]), L::TILE);
+#pragma unroll
+        for (int b = 0; b < BOXES; ++b)
+          tma_load_3d(sb + L::K + st * L::TILE + b * kBox, &tm_k, bar_addr(bars.k_full[st]),
+                      b * 64, h, key0);
+        mbar_arrive_expect_tx(bar_addr(bars.v_full[st]), L::TILE);
+#pragma unroll
+        for (int b = 0; b < BOXES; ++b)
+          tma_load_3d(sb + L::V + st * L::TILE + b * kBox, &tm_v, bar_addr(bars.v_full[st]),
+                      b * 64, h, key0);
+        ++issued;
+      }
+      int never = 0;
+      mbar_wait(bar_addr(bars.qd_full), 0, &never, kLimitNs);
+      for (int j = max(0, issued - kStg); j < issued; ++j) {
+        const int st = j % kStg;
+        mbar_wait(bar_addr(bars.k_full[st]), (j / kStg) & 1, &never, kLimitNs);
+        mbar_wait(bar_addr(bars.v_full[st]), (j / kStg) & 1, &never, kLimitNs);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
+      bool ok = mbar_wait(bar_addr(bars.qd_full), 0, &s_abort, kLimitNs);
+      if (!ok) fail(&s_abort);
+      for (int j = 0; ok && j < nb; ++j) {
+        const int st = j % kStg;
+        if (!mbar_wait(bar_addr(bars.k_full[st]), (j / kStg) & 1, &s_abort, kLimitNs) ||
+            !mbar_wait(bar_addr(bars.v_full[st]), (j / kStg) & 1, &s_abort, kLimitNs)) {
+          fail(&s_abort);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = kmajor_off(kk);
+          umma_bf16(tmem, sdesc_sw128(sb + L::Q + off, 16, 1024),
+                    sdesc_sw128(sb + L::K + st * L::TILE + off, 16, 1024), idS, kk > 0);
+          umma_bf16(tmem + 128, sdesc_sw128(sb + L::DO + off, 16, 1024),
+                    sdesc_sw128(sb + L::V + st * L::TILE + off, 16, 1024), idS, kk > 0);
+        }
+        umma_commit(bar_addr(bars.st_full));
+        if (!mbar_wait(bar_addr(bars.ds_full), j & 1, &s_abort, kLimitNs)) {
+          fail(&s_abort);
+          break;
+        }
+        tc_fence_after();
+        // dQ += dS K : A = dS (bf16 in TMEM over S), B = K tile as MN-major (N = d)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ts(tmem + 256, tmem + kk * 8,
+                       sdesc_sw128(sb + L::K + st * L::TILE + kk * 2048, kBox, 1024), idQ,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar_addr(bars.kv_empty[st]));
+      }
+      umma_commit(bar_addr(bars.done));
+      umma_commit(bar_addr(bars.mma_done));
+      int never = 0;
+      mbar_wait(bar_addr(bars.mma_done), 0, &never, kLimitNs);
+    }
+  } else {
+    const int row = threadIdx.x;
+    const int t = t0 + row;
+    const bool in = t < a.s_local;
+    const int lo = in ? m.row_lo[t] : 0;
+    const int hi = in ? m.row_hi[t] : -1;
+    const float lse2 = hi >= 0 ? a.lse[(int64_t)h * a.s_local + t] * kLog2ef : 0.f;
+    const float dl = hi >= 0 ? a.delta[(int64_t)h * a.s_local + t] : 0.f;
+    const uint32_t lb = (uint32_t)(warp * 32) << 16;
+    const float sl2 = a.scale_log2;
+    auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
+      return __all_sync(0xffffffffu, w);
+    };
+    Iter it;
+    it.init(s_iv, s_niv);
+    bool ok = true;
+    for (int j = 0; j < nb; ++j, it.next()) {
+      if (!wait_warp(bar_addr(bars.st_full), j & 1)) {
+        fail(&s_abort);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float p[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lb + c * 32, reinterpret_cast<uint32_t*>(p + c * 32));
+      const int j0 = it.b * 128;
+      const bool full = lo <= j0 && hi >= j0 + 127;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const bool keep = full || (j0 + c >= lo && j0 + c <= hi);
+        p[c] = keep ? exp2f(fmaf(p[c], sl2, -lse2)) : 0.f;
+      }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t dp[32], pk[16];
+        tmem_ld32(tmem + lb + 128 + cc * 32, dp);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16(p[cc * 32 + 2 * e] * (__uint_as_float(dp[2 * e]) - dl),
+                            p[cc * 32 + 2 * e + 1] * (__uint_as_float(dp[2 * e + 1]) - dl));
+        tmem_st16(tmem + lb + cc * 16, pk);  // over S columns already read
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_addr(bars.ds_full));
+    }
+    if (ok && !wait_warp(bar_addr(bars.done), 0)) {
+      fail(&s_abort);
+      ok = false;
+    }
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lb + 256 + c * 32, o);
+        if (in) {
+          uint4* dst = reinterpret_cast<uint4*>(a.dq + ((int64_t)t * a.H + h) * D + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(o[q * 8 + 0]) * a.scale, __uint_as_float(o[q * 8 + 1]) * a.scale);
+            v.y = pack_bf16(__uint_as_float(o[q * 8 + 2]) * a.scale, __uint_as_float(o[q * 8 + 3]) * a.scale);
+            v.z = pack_bf16(__uint_as_float(o[q * 8 + 4]) * a.scale, __uint_as_float(o[q * 8 + 5]) * a.scale);
+            v.w = pack_bf16(__uint_as_float(o[q * 8 + 6]) * a.scale, __uint_as_float(o[q * 8 + 7]) * a.scale);
+            dst[q] = v;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
+// ===========================================================================
+// dK / dV
+// ===========================================================================
+template <int D>
+struct KvLayout {
+  static constexpr int TILE = (D / 64) * kBox;
+  static constexpr int K = 0;
+  static constexpr int V = TILE;
+  static constexpr int Q = 2 * TILE;
+  static constexpr int DO = Q + kStg * TILE;
+  static constexpr int BYTES = DO + kStg * TILE;
+};
+
+struct QInfo {  // per-query data of one 128-query step
+  int lo[128];
+  int hi[128];
+  float lse2[128];
+  float dl[128];
+  int max_lo, min_hi;
+};
+
+struct KvBars {
+  uint64_t kv_full;
+  uint64_t q_full[kStg], qi_full[kStg], q_empty[kStg];
+  uint64_t st_full, p_full, ds_full, done, mma_done;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThr, 1)
+attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+             const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+             const BwdArgs a) {
+  using L = KvLayout<D>;
+  constexpr int BOXES = D / 64;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ KvBars bars;
+  __shared__ QInfo qinfo[kStg];
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  __shared__ int2 s_iv[kMaxIv];
+  __shared__ int s_niv;
+
+  const MetaView m = meta_view(a.meta);
+  if (!meta_ok_bwd(a, m.hdr)) return;
+  const int h = blockIdx.y;
+  const int j0 = blockIdx.x * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
+
+  if (threadIdx.x == 0) {
+    s_niv = build_q_intervals(m, j0, min(j0 + 128, a.T) - 1, 128, s_iv, kMaxIv);
+    s_abort = 0;
+    mbar_init(bar_addr(bars.kv_full), 1);
+    for (int s = 0; s < kStg; ++s) {
+      mbar_init(bar_addr(bars.q_full[s]), 1);
+      mbar_init(bar_addr(bars.qi_full[s]), 32);
+      mbar_init(bar_addr(bars.q_empty[s]), 1);
+    }
+    mbar_init(bar_addr(bars.st_full), 1);
+    mbar_init(bar_addr(bars.p_full), 128);
+    mbar_init(bar_addr(bars.ds_full), 128);
+    mbar_init(bar_addr(bars.done), 1);
+    mbar_init(bar_addr(bars.mma_done), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  int nq = 0;
+  for (int i = 0; i < s_niv; ++i) nq += s_iv[i].y - s_iv[i].x + 1;
+  if (nq == 0) return;  // no query of this rank attends these keys
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&s_tmem), kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;  // S^T [0,128) dP^T [128,256) dK [256,256+D) dV [256+D,256+2D)
+
+  if (warp == 4) {
+    // all 32 lanes: lane 0 issues TMA, every lane loads per-query data
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_addr(bars.kv_full), 2 * L::TILE);
+#pragma unroll
+      for (int b = 0; b < BOXES; ++b) {
+        tma_load_3d(sb + L::K + b * kBox, &tm_k, bar_addr(bars.kv_full), b * 64, h, j0);
+        tma_load_3d(sb + L::V + b * kBox, &tm_v, bar_addr(bars.kv_full), b * 64, h, j0);
+      }
+    }
+    Iter it;
+    it.init(s_iv, s_niv);
+    int issued = 0;
+    for (int i = 0; i < nq; ++i, it.next()) {
+      const int st = i % kStg;
+      const bool w = mbar_wait(bar_addr(bars.q_empty[st]), ((i / kStg) & 1) ^ 1, &s_abort, kLimitNs);
+      if (!__all_sync(0xffffffffu, w)) {
+        if (lane == 0) fail(&s_abort);
+        break;
+      }
+      const int q0 = it.b * 128;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_addr(bars.q_full[st]), 2 * L::TILE);
+#pragma unroll
+        for (int b = 0; b < BOXES; ++b) {
+          tma_load_3d(sb + L::Q + st * L::TILE + b * kBox, &tm_q, bar_addr(bars.q_full[st]),
+                      b * 64, h, q0);
+          tma_load_3d(sb + L::DO + st * L::TILE + b * kBox, &tm_do, bar_addr(bars.q_full[st]),
+                      b * 64, h, q0);
+        }
+      }
+      ++issued;
+      QInfo& qi = qinfo[st];
+      int mlo = INT_MIN, mhi = INT_MAX;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int c = lane + 32 * r;
+        const int t = q0 + c;
+        const bool in = t < a.s_local;
+        const int hi = in ? m.row_hi[t] : -1;
+        const int lo = in ? m.row_lo[t] : 0;
+        qi.lo[c] = lo;
+        qi.hi[c] = hi;
+        qi.lse2[c] = hi >= 0 ? a.lse[(int64_t)h * a.s_local + t] * kLog2ef : 0.f;
+        qi.dl[c] = hi >= 0 ? a.delta[(int64_t)h * a.s_local + t] : 0.f;
+        mlo = max(mlo, lo);
+        mhi = min(mhi, hi);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mlo = max(mlo, __shfl_xor_sync(0xffffffffu, mlo, o));
+        mhi = min(mhi, __shfl_xor_sync(0xffffffffu, mhi, o));
+      }
+      if (lane == 0) {
+        qi.max_lo = mlo;
+        qi.min_hi = mhi;
+      }
+      __syncwarp();
+      mbar_arrive(bar_addr(bars.qi_full[st]));
+    }
+    if (lane == 0) {
+      int never = 0;
+      mbar_wait(bar_addr(bars.kv_full), 0, &never, kLimitNs);
+      for (int i = max(0, issued - kStg); i < issued; ++i)
+        mbar_wait(bar_addr(bars.q_full[i % kStg]), (i / kStg) & 1, &never, kLimitNs);
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
+      bool ok = mbar_wait(bar_addr(bars.kv_full), 0, &s_abort, kLimitNs);
+      if (!ok) fail(&s_abort);
+      for (int i = 0; ok && i < nq; ++i) {
+        const int st = i % kStg;
+        if (!mbar_wait(bar_addr(bars.q_full[st]), (i / kStg) & 1, &s_abort, kLimitNs)) {
+          fail(&s_abort);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = kmajor_off(kk);
+          umma_bf16(tmem, sdesc_sw128(sb + L::K + off, 16, 1024),
+                    sdesc_sw128(sb + L::Q + st * L::TILE + off, 16, 1024), idS, kk > 0);
+          umma_bf16(tmem + 128, sdesc_sw128(sb + L::V + off, 16, 1024),
+                    sdesc_sw128(sb + L::DO + st * L::TILE + off, 16, 1024), idS, kk > 0);
+        }
+        umma_commit(bar_addr(bars.st_full));
+        if (!mbar_wait(bar_addr(bars.p_full), i & 1, &s_abort, kLimitNs)) {
+          fail(&s_abort);
+          break;
+        }
+        tc_fence_after();
+        // dV += P^T dO : A = P^T (TMEM over S^T), B = dO tile as MN-major (N = d)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ts(tmem + 256 + D, tmem + kk * 8,
+                       sdesc_sw128(sb + L::DO + st * L::TILE + kk * 2048, kBox, 1024), idG,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+        if (!mbar_wait(bar_addr(bars.ds_full), i & 1, &s_abort, kLimitNs)) {
+          fail(&s_abort);
+          break;
+        }
+        tc_fence_after();
+        // dK += dS^T Q : A = dS^T (TMEM over dP^T), B = Q tile as MN-major
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ts(tmem + 256, tmem + 128 + kk * 8,
+                       sdesc_sw128(sb + L::Q + st * L::TILE + kk * 2048, kBox, 1024), idG,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar_addr(bars.q_empty[st]));
+      }
+      umma_commit(bar_addr(bars.done));
+      umma_commit(bar_addr(bars.mma_done));
+      int never = 0;
+      mbar_wait(bar_addr(bars.mma_done), 0, &never, kLimitNs);
+    }
+  } else {
+    const int row = threadIdx.x;
+    const int key = j0 + row;
+    const uint32_t lb = (uint32_t)(warp * 32) << 16;
+    const float sl2 = a.scale_log2;
+    auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
+      return __all_sync(0xffffffffu, w);
+    };
+    bool ok = true;
+    for (int i = 0; i < nq; ++i) {
+      const int st = i % kStg;
+      if (!wait_warp(bar_addr(bars.st_full), i & 1) ||
+          !wait_warp(bar_addr(bars.qi_full[st]), (i / kStg) & 1)) {
+        fail(&s_abort);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const QInfo& qi = qinfo[st];
+      float p[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lb + c * 32, reinterpret_cast<uint32_t*>(p + c * 32));
+      const bool full = key >= qi.max_lo && key <= qi.min_hi;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const bool keep = full || (key >= qi.lo[c] && key <= qi.hi[c]);
+        p[c] = keep ? exp2f(fmaf(p[c], sl2, -qi.lse2[c])) : 0.f;
+      }
+      // P^T -> TMEM (bf16 pairs over S^T)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(p[c * 64 + 2 * e], p[c * 64 + 2 * e + 1]);
+        tmem_st32(tmem + lb + c * 32, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_addr(bars.p_full));
+      // dS^T = P^T (dP^T - Delta) -> TMEM over dP^T (columns already read)
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t dp[32], pk[16];
+        tmem_ld32(tmem + lb + 128 + cc * 32, dp);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = cc * 32 + 2 * e;
+          pk[e] = pack_bf16(p[c0] * (__uint_as_float(dp[2 * e]) - qi.dl[c0]),
+                            p[c0 + 1] * (__uint_as_float(dp[2 * e + 1]) - qi.dl[c0 + 1]));
+        }
+        tmem_st16(tmem + lb + 128 + cc * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_addr(bars.ds_full));
+    }
+    if (ok && !wait_warp(bar_addr(bars.done), 0)) {
+      fail(&s_abort);
+      ok = false;
+    }
+    if (ok) {
+      tc_fence_after();
+      const bool in = key < a.T;
+      float* pk_ = a.dk + ((int64_t)key * a.H + h) * D;
+      float* pv_ = a.dv + ((int64_t)key * a.H + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t g[32];
+        tmem_ld32(tmem + lb + 256 + c * 32, g);
+        if (in) {
+          float4* dst = reinterpret_cast<float4*>(pk_ + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 x = dst[q];
+            x.x += __uint_as_float(g[4 * q + 0]) * a.scale;
+            x.y += __uint_as_float(g[4 * q + 1]) * a.scale;
+            x.z += __uint_as_float(g[4 * q + 2]) * a.scale;
+            x.w += __uint_as_float(g[4 * q + 3]) * a.scale;
+            dst[q] = x;
+          }
+        }
+        tmem_ld32(tmem + lb + 256 + D + c * 32, g);
+        if (in) {
+          float4* dst = reinterpret_cast<float4*>(pv_ + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 x = dst[q];
+            x.x += __uint_as_float(g[4 * q + 0]);
+            x.y += __uint_as_float(g[4 * q + 1]);
+            x.z += __uint_as_float(g[4 * q + 2]);
+            x.w += __uint_as_float(g[4 * q + 3]);
+            dst[q] = x;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
+template <int D>
+int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
+                  const BwdArgs& a, cudaStream_t s) {
+  alignas(64) CUtensorMap mq, mdo, mk, mv;
+  int st;
+  if ((st = tma::make_thd_map(&mq, q, a.s_local, a.H, D, 128)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mdo, dout, a.s_local, a.H, D, 128)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128)) != CP_OK) return st;
+  const int dq_smem = DqLayout<D>::BYTES + 1024;
+  const int kv_smem = KvLayout<D>::BYTES + 1024;
+  if (cudaFuncSetAttribute(attn_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(attn_dkdv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kv_smem) != cudaSuccess)
+    return CP_ERR_CUDA;
+  dim3 qgrid((unsigned)((a.s_local + 127) / 128), (unsigned)a.H);
+  attn_dq_tc<D><<<qgrid, kThr, dq_smem, s>>>(mq, mdo, mk, mv, a);
+  if ((st = cpthd_host::launch_status()) != CP_OK) return st;
+  dim3 kgrid((unsigned)((a.T + 127) / 128), (unsigned)a.H);
+  attn_dkdv_tc<D><<<kgrid, kThr, kv_smem, s>>>(mq, mdo, mk, mv, a);
+  return cpthd_host::launch_status();
+}
+
+}  // namespace
+}  // namespace cpthd
+
+// Internal entry used by the backward entry points (arguments validated, Delta
+// already computed into `delta`).
+int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
+                      const float* lse, const float* delta, void* dq, float* dk, float* dv,
+                      const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
+                      int cp, int rank, int strategy, float scale, float scale_log2,
+                      cudaStream_t s) {
+  using namespace cpthd;
+  BwdArgs a{};
+  a.lse = lse;
+  a.delta = delta;
+  a.dq = (bf16*)dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.meta = meta;
+  a.meta_bytes = meta_bytes;
+  a.T = T; a.H = H; a.s_local = s_local; a.cp = cp; a.rank = rank; a.strategy = strategy;
+  a.scale = scale;
+  a.scale_log2 = scale_log2;
+  return D == 64 ? launch_bwd_tc<64>(q, k, v, dout, a, s) : launch_bwd_tc<128>(q, k, v, dout, a, s);
+}
+
+extern "C" int cpthd_status_bwd_tc(int reset) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, cpthd::g_status_bwd_tc, sizeof(int)) != cudaSuccess)
+    return CP_ERR_CUDA;
+  if (reset) {
+    int z = 0;
+    if (cudaMemcpyToSymbol(cpthd::g_status_bwd_tc, &z, sizeof(int)) != cudaSuccess)
+      return CP_ERR_CUDA;
+  }
+  return v;
+}

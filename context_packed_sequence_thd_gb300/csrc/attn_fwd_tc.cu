@@ -12,14 +12,15 @@
 //   warps 0-3  softmax: thread r owns query row r (TMEM lane r).  Loads S
 //              from TMEM, masks by the row's key range, online softmax in the
 //              log2 domain, rescales O in TMEM when the row max grows, writes
-//              P (bf16) into a 128B-swizzled K-major shared tile, and finally
-//              normalises O and stores O / LSE.
+//              P (bf16 pairs) back into TMEM over S, and finally normalises O
+//              and stores O / LSE.
 //   warp 4     TMA producer: Q once, then K and V 128-key tiles into a
-//              2-stage ring (separate K / V barriers).
+//              3-stage ring (separate K / V barriers).
 //   warp 5     TMEM allocator and single-thread MMA issuer:
 //              S[j%2] = Q K_j^T (M=128, N=128, K=D) and O += P_j V_j
-//              (M=128, N=D, K=128, V as an MN-major operand), fp32
-//              accumulators in TMEM: S0 cols [0,128), S1 [128,256), O [256,256+D).
+//              (M=128, N=D, K=128; A = P from TMEM, B = V as an MN-major
+//              shared operand), fp32 accumulators in TMEM: S0 cols [0,128),
+//              S1 [128,256), O [256,256+D); P_j aliases the first 64 columns of S_j.
 // The MMA of S_{j+1} overlaps the softmax of S_j; the softmax of block j
 // waits for P V_{j-1} before it touches O or overwrites P.
 // Key blocks: only those some row of the tile attends (document and causal
@@ -27,13 +28,11 @@
 // Every wait is bounded (mbar_wait): a wait that runs out sets the device
 // status word to CP_ERR_TIMEOUT, the CTA drains its own copies / MMAs and
 // frees its TMEM before it returns.
-#include <cudaTypedefs.h>
 #include <math.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "sm100.cuh"
+#include "tma_host.cuh"
 
 namespace cpthd {
 
@@ -47,9 +46,9 @@ using bf16 = __nv_bfloat16;
 constexpr int TBM = 128;           // query rows per tile
 constexpr int TBN = 128;           // keys per block
 constexpr int kThreadsTc = 192;    // 6 warps
-constexpr int kStages = 2;         // K/V ring depth
+constexpr int kStages = 3;         // K/V ring depth
 constexpr int kBoxBytes = 128 * 128;  // one 128-row x 128-byte TMA box
-constexpr int kMaxIvTc = TBM + 4;
+constexpr int kMaxIvTc = 64;  // over capacity the last interval widens (still correct)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr float kLn2f = 0.6931471805599453f;
@@ -61,8 +60,7 @@ struct Layout {
   static constexpr int Q = 0;
   static constexpr int K = Q + TILE;
   static constexpr int V = K + kStages * TILE;
-  static constexpr int P = V + kStages * TILE;  // 2 boxes: keys 0-63, 64-127
-  static constexpr int BYTES = P + 2 * kBoxBytes;
+  static constexpr int BYTES = V + kStages * TILE;
 };
 
 struct TcArgs {
@@ -80,7 +78,6 @@ struct Bars {
   uint64_t v_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
-  uint64_t s_free[2];
   uint64_t p_full;
   uint64_t o_ready;
   uint64_t mma_done;
@@ -142,10 +139,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       mbar_init(bar(bars.v_full[s]), 1);
       mbar_init(bar(bars.kv_empty[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(bars.s_full[s]), 1);
-      mbar_init(bar(bars.s_free[s]), 128);
-    }
+    for (int s = 0; s < 2; ++s) mbar_init(bar(bars.s_full[s]), 1);
     mbar_init(bar(bars.p_full), 128);
     mbar_init(bar(bars.o_ready), 1);
     mbar_init(bar(bars.mma_done), 1);
@@ -229,8 +223,9 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       for (int j = 0; ok && j <= nb; ++j) {
         if (j < nb) {
           const int st = j % kStages, buf = j & 1;
-          if (!mbar_wait(bar(bars.k_full[st]), (j / kStages) & 1, &s_abort, kWaitLimitNs) ||
-              !mbar_wait(bar(bars.s_free[buf]), ((j >> 1) & 1) ^ 1, &s_abort, kWaitLimitNs)) {
+          // S_j overwrites P_{j-2} (same TMEM columns); P V_{j-2} was issued
+          // earlier by this thread and MMAs of one thread run in order
+          if (!mbar_wait(bar(bars.k_full[st]), (j / kStages) & 1, &s_abort, kWaitLimitNs)) {
             fail(&s_abort);
             break;
           }
@@ -252,12 +247,12 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             break;
           }
           tc_fence_after();
+          // A = P_i from TMEM (bf16 pairs over the first 64 columns of S_i's buffer)
 #pragma unroll
           for (int kk = 0; kk < TBN / 16; ++kk) {
-            const uint64_t da =
-                sdesc_sw128(sb + L::P + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
             const uint64_t db = sdesc_sw128(sb + L::V + st * L::TILE + kk * 2048, kBoxBytes, 1024);
-            umma_bf16(tmem + 256, da, db, idO, (i > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + 256, tmem + (i & 1) * 128 + kk * 8, db, idO,
+                         (i > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(bar(bars.kv_empty[st]));
           umma_commit(bar(bars.o_ready));
@@ -280,7 +275,6 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     Iter it;
     it.init(s_iv, s_niv);
     bool ok = true;
-    uint8_t* p_row = smem_raw + (sb - smem_u32(smem_raw)) + L::P + row * 128;
     // waits of the softmax warps are made warp-uniform (tcgen05.ld/st are
     // .sync.aligned): the warp proceeds only when every lane saw the phase
     auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
@@ -299,8 +293,6 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
       for (int c = 0; c < TBN / 32; ++c)
         tmem_ld32(tmem + lane_base + buf * 128 + c * 32, reinterpret_cast<uint32_t*>(s + c * 32));
-      tc_fence_before();
-      mbar_arrive(bar(bars.s_free[buf]));
 
       const int j0 = it.b * TBN;
       if (!(lo <= j0 && hi >= j0 + TBN - 1)) {
@@ -344,18 +336,15 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           tmem_st_wait();
         }
       }
-      // P row -> shared memory, bf16, K-major with the 128-byte swizzle
+      // P row -> TMEM as bf16 pairs, over the first 64 columns of S_j's buffer
 #pragma unroll
-      for (int cc = 0; cc < TBN / 8; ++cc) {
-        uint4 v;
-        v.x = pack_bf16(s[cc * 8 + 0], s[cc * 8 + 1]);
-        v.y = pack_bf16(s[cc * 8 + 2], s[cc * 8 + 3]);
-        v.z = pack_bf16(s[cc * 8 + 4], s[cc * 8 + 5]);
-        v.w = pack_bf16(s[cc * 8 + 6], s[cc * 8 + 7]);
-        const int box = cc >> 3, chunk = (cc & 7) ^ (row & 7);
-        *reinterpret_cast<uint4*>(p_row + box * kBoxBytes + chunk * 16) = v;
+      for (int c = 0; c < TBN / 64; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]);
+        tmem_st32(tmem + lane_base + buf * 128 + c * 32, pk);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(bars.p_full));
     }
@@ -400,42 +389,13 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// [rows, H, D] bf16 viewed as a 3-D tensor (D, H, rows); 64 x 1 x 128 boxes,
-// 128-byte swizzle, zero fill outside.
-int make_map(CUtensorMap* map, const void* base, int64_t rows, int H, int D) {
-  auto enc = encode_fn();
-  if (!enc) return CP_ERR_CUDA;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-  cuuint32_t box[3] = {64, 1, 128};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? CP_OK : CP_ERR_CUDA;
-}
-
 template <int D>
 int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, cudaStream_t s) {
   alignas(64) CUtensorMap mq, mk, mv;
   int st;
-  if ((st = make_map(&mq, q, a.s_local, a.H, D)) != CP_OK) return st;
-  if ((st = make_map(&mk, k, a.T, a.H, D)) != CP_OK) return st;
-  if ((st = make_map(&mv, v, a.T, a.H, D)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mq, q, a.s_local, a.H, D, 128)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128)) != CP_OK) return st;
   const int smem = Layout<D>::BYTES + 1024;
   if (cudaFuncSetAttribute(attn_fwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)

@@ -234,8 +234,16 @@ extern "C" int cpthd_status_partition(int reset);
 extern "C" int cpthd_status_rows(int reset);
 extern "C" int cpthd_status_attn(int reset);
 extern "C" int cpthd_status_fwd_tc(int reset);
+extern "C" int cpthd_status_bwd_tc(int reset);
 
 // tcgen05 forward (attn_fwd_tc.cu); arguments validated by cp_attn_fwd
 int cpthd_attn_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale_log2, cudaStream_t s);
+
+// tcgen05 dQ and dK/dV kernels (attn_bwd_tc.cu); Delta already in `delta`
+int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
+                      const float* lse, const float* delta, void* dq, float* dk, float* dv,
+                      const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
+                      int cp, int rank, int strategy, float scale, float scale_log2,
+                      cudaStream_t s);

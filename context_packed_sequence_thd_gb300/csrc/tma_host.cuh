@@ -1,0 +1,45 @@
+// tma_host.cuh -- host-side TMA tensor maps for THD tensors (one per
+// translation unit that launches TMA kernels).
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace cpthd {
+namespace tma {
+
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [rows, H, D] bf16 viewed as a 3-D tensor (D, H, rows): boxes of
+// 64 (d) x 1 (head) x box_rows (rows), 128-byte swizzle, zero fill outside.
+inline int make_thd_map(CUtensorMap* map, const void* base, int64_t rows, int H, int D,
+                        int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return CP_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CP_OK : CP_ERR_CUDA;
+}
+
+}  // namespace tma
+}  // namespace cpthd
