@@ -10,8 +10,8 @@
 //
 // attn_dq_tc   one CTA per (128-query tile, head), iterating the key blocks
 //              the tile attends.  S = Q K^T and dP = dO V^T into TMEM
-//              (M=128 queries, N=128 keys); 4 compute warps (thread = query
-//              row) form dS and write it back into TMEM as bf16 over S;
+//              (M=128 queries, N=128 keys); the compute warps (a query row
+//              per TMEM lane) form dS and write it back into TMEM as bf16 over S;
 //              dQ += dS K with A = dS from TMEM, B = K as an MN-major operand.
 // attn_dkdv_tc one CTA per (128-key block, head), iterating the rank's query
 //              tiles that attend the block (segment table).  S^T = K Q^T and
@@ -20,8 +20,12 @@
 //              dP^T; dV += P^T dO and dK += dS^T Q (A from TMEM, B = dO / Q as
 //              MN-major operands).  The block's partial dK/dV are added into
 //              the caller's fp32 accumulators by the block's only owner.
-// Warp roles as in the forward: warps 0-3 compute, warp 4 TMA producer,
-// warp 5 TMEM allocator + single-thread MMA issuer.  Every wait is bounded.
+// Warp roles: warps 0-7 compute (warp w serves TMEM lanes 32*(w%4).. and the
+// column half w/4 of every row, so two warps share each row's elementwise
+// work), warp 8 TMA producer, warp 9 TMEM allocator + single-thread MMA
+// issuer.  A compute thread writes P / dS back only into TMEM columns it has
+// itself already read (the first half of its own column range), so the two
+// halves never race.  Every wait is bounded.
 #include <math.h>
 
 #include "common.cuh"
@@ -37,7 +41,9 @@ namespace {
 using namespace sm100;
 using bf16 = __nv_bfloat16;
 
-constexpr int kThr = 192;
+constexpr int kThr = 320;
+constexpr int kCompute = 256;  // threads of warps 0-7
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kStg = 2;
 constexpr int kBox = 128 * 128;  // one 128-row x 128-byte TMA box
 constexpr int kMaxIv = 64;
@@ -88,6 +94,10 @@ __device__ __forceinline__ uint32_t bar_addr(uint64_t& b) { return smem_u32(&b);
 // K-major operand offset of k-step kk (16 elements) inside a tile of
 // 64-element (128-byte) boxes of 128 rows.
 __device__ __forceinline__ uint32_t kmajor_off(int kk) { return (kk >> 2) * kBox + (kk & 3) * 32; }
+
+// TMEM column of k-step kk (16 elements) of an A operand written by the two
+// column halves: elements [0,64) at columns [0,32), [64,128) at [64,96).
+__device__ __forceinline__ uint32_t ts_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 // ===========================================================================
 // dQ
@@ -140,7 +150,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mbar_init(bar_addr(bars.kv_empty[s]), 1);
     }
     mbar_init(bar_addr(bars.st_full), 1);
-    mbar_init(bar_addr(bars.ds_full), 128);
+    mbar_init(bar_addr(bars.ds_full), kCompute);
     mbar_init(bar_addr(bars.done), 1);
     mbar_init(bar_addr(bars.mma_done), 1);
     fence_barrier_init();
@@ -156,7 +166,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
     return;
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&s_tmem), kCols);
     tmem_relinquish();
   }
@@ -165,7 +175,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   tc_fence_after();
   const uint32_t tmem = s_tmem;  // S [0,128)  dP [128,256)  dQ [256,256+D)
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     if (lane == 0) {
       mbar_arrive_expect_tx(bar_addr(bars.qd_full), 2 * L::TILE);
 #pragma unroll
@@ -203,7 +213,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mbar_wait(bar_addr(bars.v_full[st]), (j / kStg) & 1, &never, kLimitNs);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
@@ -234,7 +244,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         // dQ += dS K : A = dS (bf16 in TMEM over S), B = K tile as MN-major (N = d)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + 256, tmem + kk * 8,
+          umma_bf16_ts(tmem + 256, tmem + ts_col(kk),
                        sdesc_sw128(sb + L::K + st * L::TILE + kk * 2048, kBox, 1024), idQ,
                        (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar_addr(bars.kv_empty[st]));
@@ -245,14 +255,15 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mbar_wait(bar_addr(bars.mma_done), 0, &never, kLimitNs);
     }
   } else {
-    const int row = threadIdx.x;
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane = query row of the tile
+    const int hf = warp >> 2;                // column half: keys [64hf, 64hf+64)
     const int t = t0 + row;
     const bool in = t < a.s_local;
     const int lo = in ? m.row_lo[t] : 0;
     const int hi = in ? m.row_hi[t] : -1;
     const float lse2 = hi >= 0 ? a.lse[(int64_t)h * a.s_local + t] * kLog2ef : 0.f;
     const float dl = hi >= 0 ? a.delta[(int64_t)h * a.s_local + t] : 0.f;
-    const uint32_t lb = (uint32_t)(warp * 32) << 16;
+    const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale_log2;
     auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
       const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
@@ -268,25 +279,27 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         break;
       }
       tc_fence_after();
-      float p[128];
+      float p[64];
+      tmem_ld32(tmem + lb + 64 * hf, reinterpret_cast<uint32_t*>(p));
+      tmem_ld32(tmem + lb + 64 * hf + 32, reinterpret_cast<uint32_t*>(p + 32));
+      const int k0 = it.b * 128 + 64 * hf;  // key of this thread's first column
+      if (lo <= k0 && hi >= k0 + 63) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lb + c * 32, reinterpret_cast<uint32_t*>(p + c * 32));
-      const int j0 = it.b * 128;
-      const bool full = lo <= j0 && hi >= j0 + 127;
+        for (int c = 0; c < 64; ++c) p[c] = ex2_approx(fmaf(p[c], sl2, -lse2));
+      } else {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const bool keep = full || (j0 + c >= lo && j0 + c <= hi);
-        p[c] = keep ? exp2f(fmaf(p[c], sl2, -lse2)) : 0.f;
+        for (int c = 0; c < 64; ++c)
+          p[c] = (k0 + c >= lo && k0 + c <= hi) ? ex2_approx(fmaf(p[c], sl2, -lse2)) : 0.f;
       }
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dp[32], pk[16];
-        tmem_ld32(tmem + lb + 128 + cc * 32, dp);
+        tmem_ld32(tmem + lb + 128 + 64 * hf + 32 * cc, dp);
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           pk[e] = pack_bf16(p[cc * 32 + 2 * e] * (__uint_as_float(dp[2 * e]) - dl),
                             p[cc * 32 + 2 * e + 1] * (__uint_as_float(dp[2 * e + 1]) - dl));
-        tmem_st16(tmem + lb + cc * 16, pk);  // over S columns already read
+        tmem_st16(tmem + lb + 64 * hf + 16 * cc, pk);  // dS over this half's S columns
       }
       tmem_st_wait();
       tc_fence_before();
@@ -299,11 +312,12 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     if (ok) {
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = hf * (D / 2) + c * 32;  // dQ columns of this half
         uint32_t o[32];
-        tmem_ld32(tmem + lb + 256 + c * 32, o);
+        tmem_ld32(tmem + lb + 256 + col, o);
         if (in) {
-          uint4* dst = reinterpret_cast<uint4*>(a.dq + ((int64_t)t * a.H + h) * D + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(a.dq + ((int64_t)t * a.H + h) * D + col);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 v;
@@ -319,7 +333,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kCols);
   }
@@ -338,7 +352,7 @@ struct KvLayout {
   static constexpr int BYTES = DO + kStg * TILE;
 };
 
-struct QInfo {  // per-query data of one 128-query step
+struct __align__(16) QInfo {  // per-query data of one 128-query step
   int lo[128];
   int hi[128];
   float lse2[128];
@@ -384,8 +398,8 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       mbar_init(bar_addr(bars.q_empty[s]), 1);
     }
     mbar_init(bar_addr(bars.st_full), 1);
-    mbar_init(bar_addr(bars.p_full), 128);
-    mbar_init(bar_addr(bars.ds_full), 128);
+    mbar_init(bar_addr(bars.p_full), kCompute);
+    mbar_init(bar_addr(bars.ds_full), kCompute);
     mbar_init(bar_addr(bars.done), 1);
     mbar_init(bar_addr(bars.mma_done), 1);
     fence_barrier_init();
@@ -394,7 +408,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   int nq = 0;
   for (int i = 0; i < s_niv; ++i) nq += s_iv[i].y - s_iv[i].x + 1;
   if (nq == 0) return;  // no query of this rank attends these keys
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&s_tmem), kCols);
     tmem_relinquish();
   }
@@ -403,7 +417,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = s_tmem;  // S^T [0,128) dP^T [128,256) dK [256,256+D) dV [256+D,256+2D)
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // all 32 lanes: lane 0 issues TMA, every lane loads per-query data
     if (lane == 0) {
       mbar_arrive_expect_tx(bar_addr(bars.kv_full), 2 * L::TILE);
@@ -469,7 +483,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       for (int i = max(0, issued - kStg); i < issued; ++i)
         mbar_wait(bar_addr(bars.q_full[i % kStg]), (i / kStg) & 1, &never, kLimitNs);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
@@ -499,7 +513,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // dV += P^T dO : A = P^T (TMEM over S^T), B = dO tile as MN-major (N = d)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + 256 + D, tmem + kk * 8,
+          umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk),
                        sdesc_sw128(sb + L::DO + st * L::TILE + kk * 2048, kBox, 1024), idG,
                        (i > 0 || kk > 0) ? 1u : 0u);
         if (!mbar_wait(bar_addr(bars.ds_full), i & 1, &s_abort, kLimitNs)) {
@@ -510,7 +524,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // dK += dS^T Q : A = dS^T (TMEM over dP^T), B = Q tile as MN-major
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + 256, tmem + 128 + kk * 8,
+          umma_bf16_ts(tmem + 256, tmem + 128 + ts_col(kk),
                        sdesc_sw128(sb + L::Q + st * L::TILE + kk * 2048, kBox, 1024), idG,
                        (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar_addr(bars.q_empty[st]));
@@ -521,9 +535,10 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       mbar_wait(bar_addr(bars.mma_done), 0, &never, kLimitNs);
     }
   } else {
-    const int row = threadIdx.x;
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane = key row of the block
+    const int hf = warp >> 2;                // column half: queries [64hf, 64hf+64)
     const int key = j0 + row;
-    const uint32_t lb = (uint32_t)(warp * 32) << 16;
+    const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale_log2;
     auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
       const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
@@ -540,38 +555,57 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       }
       tc_fence_after();
       const QInfo& qi = qinfo[st];
-      float p[128];
+      const float4* l4 = reinterpret_cast<const float4*>(qi.lse2 + 64 * hf);
+      const float4* d4 = reinterpret_cast<const float4*>(qi.dl + 64 * hf);
+      float p[64];
+      tmem_ld32(tmem + lb + 64 * hf, reinterpret_cast<uint32_t*>(p));
+      tmem_ld32(tmem + lb + 64 * hf + 32, reinterpret_cast<uint32_t*>(p + 32));
+      if (key >= qi.max_lo && key <= qi.min_hi) {  // every query of the step sees this key
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lb + c * 32, reinterpret_cast<uint32_t*>(p + c * 32));
-      const bool full = key >= qi.max_lo && key <= qi.min_hi;
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l = l4[c4];
+          p[4 * c4 + 0] = ex2_approx(fmaf(p[4 * c4 + 0], sl2, -l.x));
+          p[4 * c4 + 1] = ex2_approx(fmaf(p[4 * c4 + 1], sl2, -l.y));
+          p[4 * c4 + 2] = ex2_approx(fmaf(p[4 * c4 + 2], sl2, -l.z));
+          p[4 * c4 + 3] = ex2_approx(fmaf(p[4 * c4 + 3], sl2, -l.w));
+        }
+      } else {
+        const int4* lo4 = reinterpret_cast<const int4*>(qi.lo + 64 * hf);
+        const int4* hi4 = reinterpret_cast<const int4*>(qi.hi + 64 * hf);
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const bool keep = full || (key >= qi.lo[c] && key <= qi.hi[c]);
-        p[c] = keep ? exp2f(fmaf(p[c], sl2, -qi.lse2[c])) : 0.f;
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l = l4[c4];
+          const int4 lo = lo4[c4], hi = hi4[c4];
+          p[4 * c4 + 0] = (key >= lo.x && key <= hi.x) ? ex2_approx(fmaf(p[4 * c4 + 0], sl2, -l.x)) : 0.f;
+          p[4 * c4 + 1] = (key >= lo.y && key <= hi.y) ? ex2_approx(fmaf(p[4 * c4 + 1], sl2, -l.y)) : 0.f;
+          p[4 * c4 + 2] = (key >= lo.z && key <= hi.z) ? ex2_approx(fmaf(p[4 * c4 + 2], sl2, -l.z)) : 0.f;
+          p[4 * c4 + 3] = (key >= lo.w && key <= hi.w) ? ex2_approx(fmaf(p[4 * c4 + 3], sl2, -l.w)) : 0.f;
+        }
       }
-      // P^T -> TMEM (bf16 pairs over S^T)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      {  // P^T -> TMEM (bf16 pairs over this half's S^T columns)
         uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(p[c * 64 + 2 * e], p[c * 64 + 2 * e + 1]);
-        tmem_st32(tmem + lb + c * 32, pk);
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
+        tmem_st32(tmem + lb + 64 * hf, pk);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_addr(bars.p_full));
-      // dS^T = P^T (dP^T - Delta) -> TMEM over dP^T (columns already read)
+      // dS^T = P^T (dP^T - Delta) -> TMEM over this half's dP^T columns (already read)
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dp[32], pk[16];
-        tmem_ld32(tmem + lb + 128 + cc * 32, dp);
+        tmem_ld32(tmem + lb + 128 + 64 * hf + 32 * cc, dp);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c0 = cc * 32 + 2 * e;
-          pk[e] = pack_bf16(p[c0] * (__uint_as_float(dp[2 * e]) - qi.dl[c0]),
-                            p[c0 + 1] * (__uint_as_float(dp[2 * e + 1]) - qi.dl[c0 + 1]));
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 d = d4[cc * 8 + e4];
+          const int c0 = cc * 32 + 4 * e4;
+          pk[2 * e4] = pack_bf16(p[c0] * (__uint_as_float(dp[4 * e4]) - d.x),
+                                 p[c0 + 1] * (__uint_as_float(dp[4 * e4 + 1]) - d.y));
+          pk[2 * e4 + 1] = pack_bf16(p[c0 + 2] * (__uint_as_float(dp[4 * e4 + 2]) - d.z),
+                                     p[c0 + 3] * (__uint_as_float(dp[4 * e4 + 3]) - d.w));
         }
-        tmem_st16(tmem + lb + 128 + cc * 16, pk);
+        tmem_st16(tmem + lb + 128 + 64 * hf + 16 * cc, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -587,32 +621,32 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       float* pk_ = a.dk + ((int64_t)key * a.H + h) * D;
       float* pv_ = a.dv + ((int64_t)key * a.H + h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t g[32];
-        tmem_ld32(tmem + lb + 256 + c * 32, g);
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = hf * (D / 2) + c * 32;  // this half's dK / dV columns
+        uint32_t g[32], u[32];
+        tmem_ld32(tmem + lb + 256 + col, g);
+        tmem_ld32(tmem + lb + 256 + D + col, u);
         if (in) {
-          float4* dst = reinterpret_cast<float4*>(pk_ + c * 32);
+          float4* dk4 = reinterpret_cast<float4*>(pk_ + col);
+          float4* dv4 = reinterpret_cast<float4*>(pv_ + col);
+          float4 xk[8], xv[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            float4 x = dst[q];
-            x.x += __uint_as_float(g[4 * q + 0]) * a.scale;
-            x.y += __uint_as_float(g[4 * q + 1]) * a.scale;
-            x.z += __uint_as_float(g[4 * q + 2]) * a.scale;
-            x.w += __uint_as_float(g[4 * q + 3]) * a.scale;
-            dst[q] = x;
+            xk[q] = dk4[q];
+            xv[q] = dv4[q];
           }
-        }
-        tmem_ld32(tmem + lb + 256 + D + c * 32, g);
-        if (in) {
-          float4* dst = reinterpret_cast<float4*>(pv_ + c * 32);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            float4 x = dst[q];
-            x.x += __uint_as_float(g[4 * q + 0]);
-            x.y += __uint_as_float(g[4 * q + 1]);
-            x.z += __uint_as_float(g[4 * q + 2]);
-            x.w += __uint_as_float(g[4 * q + 3]);
-            dst[q] = x;
+            xk[q].x += __uint_as_float(g[4 * q + 0]) * a.scale;
+            xk[q].y += __uint_as_float(g[4 * q + 1]) * a.scale;
+            xk[q].z += __uint_as_float(g[4 * q + 2]) * a.scale;
+            xk[q].w += __uint_as_float(g[4 * q + 3]) * a.scale;
+            xv[q].x += __uint_as_float(u[4 * q + 0]);
+            xv[q].y += __uint_as_float(u[4 * q + 1]);
+            xv[q].z += __uint_as_float(u[4 * q + 2]);
+            xv[q].w += __uint_as_float(u[4 * q + 3]);
+            dk4[q] = xk[q];
+            dv4[q] = xv[q];
           }
         }
       }
@@ -620,7 +654,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kCols);
   }

@@ -307,11 +307,11 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       for (int c = 1; c < TBN; ++c) mx = fmaxf(mx, s[c]);
       const float m_new = fmaxf(m_run, mx);
       const float mref = m_new == -INFINITY ? 0.f : m_new * sl2;
-      const float alpha = exp2f(m_run * sl2 - mref);
+      const float alpha = ex2_approx(m_run * sl2 - mref);
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < TBN; ++c) {
-        s[c] = exp2f(fmaf(s[c], sl2, -mref));
+        s[c] = ex2_approx(fmaf(s[c], sl2, -mref));
         sum += s[c];
       }
       l_run = l_run * alpha + sum;

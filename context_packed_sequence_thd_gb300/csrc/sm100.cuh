@@ -147,6 +147,14 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
+// 2^x with the SFU instruction (approximate, subnormal results flushed to 0;
+// the softmax only evaluates it at x <= 0 where that is harmless).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ----------------------------------------------------------------------------
 // UMMA (tcgen05.mma, one CTA)
 // ----------------------------------------------------------------------------
