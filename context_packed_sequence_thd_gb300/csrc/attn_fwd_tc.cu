@@ -8,15 +8,16 @@
 // LSE = -inf.  Both DUAL_CHUNK_SWAP chunks of a rank go through one launch:
 // the key range of every row comes from the rank's row tables.
 //
-// One CTA = one 128-row query tile of one head; 6 warps:
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r).  Loads S
+// One CTA = one 128-row query tile of one head; 10 warps:
+//   warps 0-7  softmax: TMEM lane r = query row r, shared by warps r/32 and
+//              r/32+4 which take one half of the key columns each.  Loads S
 //              from TMEM, masks by the row's key range, online softmax in the
 //              log2 domain, rescales O in TMEM when the row max grows, writes
 //              P (bf16 pairs) back into TMEM over S, and finally normalises O
 //              and stores O / LSE.
-//   warp 4     TMA producer: Q once, then K and V 128-key tiles into a
-//              3-stage ring (separate K / V barriers).
-//   warp 5     TMEM allocator and single-thread MMA issuer:
+//   warp 8     TMA producer: Q once, then K and V 128-key tiles into a
+//              2-stage ring (separate K / V barriers).
+//   warp 9     TMEM allocator and single-thread MMA issuer:
 //              S[j%2] = Q K_j^T (M=128, N=128, K=D) and O += P_j V_j
 //              (M=128, N=D, K=128; A = P from TMEM, B = V as an MN-major
 //              shared operand), fp32 accumulators in TMEM: S0 cols [0,128),
@@ -45,7 +46,9 @@ using bf16 = __nv_bfloat16;
 
 constexpr int TBM = 128;           // query rows per tile
 constexpr int TBN = 128;           // keys per block
-constexpr int kThreadsTc = 192;    // 6 warps
+constexpr int kThreadsTc = 320;    // 10 warps
+constexpr int kSoftmax = 256;      // threads of the softmax warps 0-7
+constexpr int kProdWarp = 8, kMmaWarp = 9;
 constexpr int kStages = 3;         // K/V ring depth
 constexpr int kBoxBytes = 128 * 128;  // one 128-row x 128-byte TMA box
 constexpr int kMaxIvTc = 64;  // over capacity the last interval widens (still correct)
@@ -83,6 +86,20 @@ struct Bars {
   uint64_t mma_done;
 };
 
+// Barriers and small per-CTA state, placed right after the tiles in the
+// dynamic shared memory (the kernel has no static shared memory, so the
+// dynamic window starts 1024-aligned and the tiles need no alignment slack).
+struct Ctl {
+  Bars bars;
+  uint64_t pair[4][2];  // row-max / row-sum exchange of softmax warps w, w+4
+  uint32_t tmem;
+  int abort;
+  int niv;
+  int pad;
+  int2 iv[kMaxIvTc];
+  float red[2][2][TBM];  // [exchange parity][column half][row]
+};
+
 __device__ __forceinline__ bool meta_ok_tc(const TcArgs& a, const MetaHeader* h) {
   const bool fits = h->n_segs >= 0 && h->n_segs <= h->max_segs && h->seg_offset == 64 &&
                     (int64_t)h->rows_offset >= 64 + 32 * (int64_t)h->max_segs &&
@@ -115,19 +132,24 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const __grid_constant__ CUtensorMap tm_v, const TcArgs a) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ Bars bars;
-  __shared__ uint32_t s_tmem;
-  __shared__ volatile int s_abort;
-  __shared__ int2 s_iv[kMaxIvTc];
-  __shared__ int s_niv;
-
   const MetaView m = meta_view(a.meta);
   if (!meta_ok_tc(a, m.hdr)) return;
   const int tile = gridDim.x - 1 - blockIdx.x;  // heavier (later) tiles first
   const int h = blockIdx.y;
   const int t0 = tile * TBM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;  // 1024-aligned (128B swizzle)
+  const uint32_t sb = smem_u32(smem_raw);  // tiles need 1024-byte alignment (128B swizzle)
+  if (sb & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(&g_status_fwd_tc, 0, (int)CP_ERR_UNSUPPORTED);
+    return;
+  }
+  Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw + L::BYTES);
+  Bars& bars = ctl.bars;
+  volatile int& s_abort = *reinterpret_cast<volatile int*>(&ctl.abort);
+  int2* s_iv = ctl.iv;
+  int& s_niv = ctl.niv;
+  float (*s_red)[2][TBM] = ctl.red;
+  uint64_t (*s_pair)[2] = ctl.pair;
 
   auto bar = [](uint64_t& b) { return smem_u32(&b); };
   if (threadIdx.x == 0) {
@@ -140,9 +162,13 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       mbar_init(bar(bars.kv_empty[s]), 1);
     }
     for (int s = 0; s < 2; ++s) mbar_init(bar(bars.s_full[s]), 1);
-    mbar_init(bar(bars.p_full), 128);
+    mbar_init(bar(bars.p_full), kSoftmax);
     mbar_init(bar(bars.o_ready), 1);
     mbar_init(bar(bars.mma_done), 1);
+    for (int w = 0; w < 4; ++w) {
+      mbar_init(bar(s_pair[w][0]), 64);
+      mbar_init(bar(s_pair[w][1]), 64);
+    }
     fence_barrier_init();
   }
   __syncthreads();
@@ -162,16 +188,16 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     return;
   }
 
-  if (warp == 5) {
-    tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&ctl.tmem), kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s_tmem;
+  const uint32_t tmem = ctl.tmem;
 
-  if (warp == 4) {
+  if (warp == kProdWarp) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -212,7 +238,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         mbar_wait(bar(bars.v_full[st]), (j / kStages) & 1, &never, kWaitLimitNs);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, TBN, false, false);
@@ -247,11 +273,12 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             break;
           }
           tc_fence_after();
-          // A = P_i from TMEM (bf16 pairs over the first 64 columns of S_i's buffer)
+          // A = P_i from TMEM: keys [0,64) over columns [0,32) and keys
+          // [64,128) over [64,96) of S_i's buffer (written by the two halves)
 #pragma unroll
           for (int kk = 0; kk < TBN / 16; ++kk) {
             const uint64_t db = sdesc_sw128(sb + L::V + st * L::TILE + kk * 2048, kBoxBytes, 1024);
-            umma_bf16_ts(tmem + 256, tmem + (i & 1) * 128 + kk * 8, db, idO,
+            umma_bf16_ts(tmem + 256, tmem + (i & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8, db, idO,
                          (i > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(bar(bars.kv_empty[st]));
@@ -264,12 +291,18 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       mbar_wait(bar(bars.mma_done), 0, &never, kWaitLimitNs);
     }
   } else {
-    // ---------------------------------------------------------------- softmax (warps 0-3)
-    const int row = threadIdx.x;  // = TMEM lane
+    // ---------------------------------------------------------------- softmax (warps 0-7)
+    // Warps w and w+4 share TMEM lanes 32*(w%4).. (one query row per lane):
+    // warp w takes key columns [0,64) of each block, warp w+4 columns
+    // [64,128).  The row max is combined through shared memory once per
+    // block (an mbarrier of the two warps, bounded wait); each half keeps its own
+    // partial row sum and rescales / normalises its half of O.
+    const int row = (warp & 3) * 32 + lane;  // = TMEM lane
+    const int hf = warp >> 2;
     const int t = t0 + row;
     const int lo = t < a.s_local ? m.row_lo[t] : 0;
     const int hi = t < a.s_local ? m.row_hi[t] : -1;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     Iter it;
@@ -281,6 +314,15 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       const bool w = mbar_wait(b, parity, &s_abort, kWaitLimitNs);
       return __all_sync(0xffffffffu, w);
     };
+    // exchange u of the two warps of a pair: publish a value, wait for the
+    // partner's (bounded, like every other wait), return the partner's value
+    auto exchange = [&](int u, float v, float* out) -> bool {
+      s_red[u & 1][hf][row] = v;
+      mbar_arrive(bar(s_pair[warp & 3][u & 1]));
+      if (!wait_warp(bar(s_pair[warp & 3][u & 1]), (u >> 1) & 1)) return false;
+      *out = s_red[u & 1][hf ^ 1][row];
+      return true;
+    };
     for (int j = 0; j < nb; ++j, it.next()) {
       const int buf = j & 1;
       if (!wait_warp(bar(bars.s_full[buf]), (j >> 1) & 1)) {
@@ -289,33 +331,52 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         break;
       }
       tc_fence_after();
-      float s[TBN];
-#pragma unroll
-      for (int c = 0; c < TBN / 32; ++c)
-        tmem_ld32(tmem + lane_base + buf * 128 + c * 32, reinterpret_cast<uint32_t*>(s + c * 32));
+      float s[64];
+      tmem_ld32(tmem + lane_base + buf * 128 + 64 * hf, reinterpret_cast<uint32_t*>(s));
+      tmem_ld32(tmem + lane_base + buf * 128 + 64 * hf + 32, reinterpret_cast<uint32_t*>(s + 32));
 
-      const int j0 = it.b * TBN;
-      if (!(lo <= j0 && hi >= j0 + TBN - 1)) {
+      const int k0 = it.b * TBN + 64 * hf;  // key of this thread's first column
+      if (!(lo <= k0 && hi >= k0 + 63)) {
 #pragma unroll
-        for (int c = 0; c < TBN; ++c) {
-          const int key = j0 + c;
+        for (int c = 0; c < 64; ++c) {
+          const int key = k0 + c;
           if (key < lo || key > hi) s[c] = -INFINITY;
         }
       }
-      float mx = s[0];
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < TBN; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m_run, mx);
-      const float mref = m_new == -INFINITY ? 0.f : m_new * sl2;
-      const float alpha = ex2_approx(m_run * sl2 - mref);
-      float sum = 0.f;
+      for (int q = 0; q < 8; ++q) mx8[q] = s[q];
 #pragma unroll
-      for (int c = 0; c < TBN; ++c) {
-        s[c] = ex2_approx(fmaf(s[c], sl2, -mref));
-        sum += s[c];
+      for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      float mx_other;
+      if (!exchange(j, mx, &mx_other)) {
+        fail(&s_abort);
+        ok = false;
+        break;
       }
+      mx = fmaxf(mx, mx_other);
+      // The running max m_run is only moved (and O, l rescaled) when the new
+      // block's max exceeds it by more than 8 in log2 units; otherwise the
+      // stale max stays in use for this block's P, which then stays below
+      // 2^8 -- P and l always use the same reference, so O/l is unchanged.
+      float alpha = 1.f;
+      if (m_run == -INFINITY || (mx - m_run) * sl2 > 8.f) {
+        const float m_new = fmaxf(m_run, mx);
+        alpha = m_run == -INFINITY ? 0.f : ex2_approx((m_run - m_new) * sl2);
+        m_run = m_new;
+      }
+      const float mref = m_run == -INFINITY ? 0.f : m_run * sl2;
+      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        s[c] = ex2_approx(fmaf(s[c], sl2, -mref));
+        sum8[c & 7] += s[c];
+      }
+      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                        ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l_run = l_run * alpha + sum;
-      m_run = m_new;
 
       if (j > 0) {
         if (!wait_warp(bar(bars.o_ready), (j - 1) & 1)) {
@@ -326,23 +387,22 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < D / 64; ++c) {
+            const uint32_t col = 256 + hf * (D / 2) + c * 32;
             uint32_t o[32];
-            tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+            tmem_ld32(tmem + lane_base + col, o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tmem + lane_base + 256 + c * 32, o);
+            tmem_st32(tmem + lane_base + col, o);
           }
           tmem_st_wait();
         }
       }
-      // P row -> TMEM as bf16 pairs, over the first 64 columns of S_j's buffer
-#pragma unroll
-      for (int c = 0; c < TBN / 64; ++c) {
+      {  // P (bf16 pairs) -> TMEM over the first 32 of this half's S columns
         uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]);
-        tmem_st32(tmem + lane_base + buf * 128 + c * 32, pk);
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
+        tmem_st32(tmem + lane_base + buf * 128 + 64 * hf, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -352,15 +412,23 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       fail(&s_abort);
       ok = false;
     }
+    // the row sum is the sum of the two halves' partial sums (same max)
+    float l_other = 0.f;
+    if (ok && !exchange(nb, l_run, &l_other)) {
+      fail(&s_abort);
+      ok = false;
+    }
+    const float l_tot = l_run + l_other;
     if (ok) {
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = hf * (D / 2) + c * 32;
         uint32_t o[32];
-        tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+        tmem_ld32(tmem + lane_base + 256 + col, o);
         if (t < a.s_local) {
-          uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)t * a.H + h) * D + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)t * a.H + h) * D + col);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 v;
@@ -372,15 +440,15 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           }
         }
       }
-      if (t < a.s_local)
+      if (t < a.s_local && hf == 0)
         a.lse[(int64_t)h * a.s_local + t] =
-            l_run > 0.f ? (m_run * sl2 + log2f(l_run)) * kLn2f : -INFINITY;
+            l_tot > 0.f ? (m_run * sl2 + log2f(l_tot)) * kLn2f : -INFINITY;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -396,7 +464,7 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, 
   if ((st = tma::make_thd_map(&mq, q, a.s_local, a.H, D, 128)) != CP_OK) return st;
   if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128)) != CP_OK) return st;
   if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128)) != CP_OK) return st;
-  const int smem = Layout<D>::BYTES + 1024;
+  const int smem = Layout<D>::BYTES + (int)sizeof(Ctl);
   if (cudaFuncSetAttribute(attn_fwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return CP_ERR_CUDA;
