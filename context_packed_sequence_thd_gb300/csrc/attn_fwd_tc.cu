@@ -22,8 +22,9 @@
 //              (M=128, N=D, K=128; A = P from TMEM, B = V as an MN-major
 //              shared operand), fp32 accumulators in TMEM: S0 cols [0,128),
 //              S1 [128,256), O [256,256+D); P_j aliases the first 64 columns of S_j.
-// The MMA of S_{j+1} overlaps the softmax of S_j; the softmax of block j
-// waits for P V_{j-1} before it touches O or overwrites P.
+// The MMA of S_{j+1} overlaps the softmax of S_j; P_j goes to the other
+// S buffer than P_{j-1}, and the softmax waits for P V_{j-1} only when it has
+// to rescale O, so consecutive P V products are issued back to back.
 // Key blocks: only those some row of the tile attends (document and causal
 // skipping from the segment table), in increasing order.
 // Every wait is bounded (mbar_wait): a wait that runs out sets the device
@@ -53,6 +54,7 @@ constexpr int kStages = 3;         // K/V ring depth
 constexpr int kBoxBytes = 128 * 128;  // one 128-row x 128-byte TMA box
 constexpr int kMaxIvTc = 64;  // over capacity the last interval widens (still correct)
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kQCol = 384;  // Q (bf16 pairs) in TMEM: columns [384, 384 + D/2)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr float kLn2f = 0.6931471805599453f;
 
@@ -77,12 +79,13 @@ struct TcArgs {
 
 struct Bars {
   uint64_t q_full;
+  uint64_t q_tmem;  // Q copied from shared memory into TMEM by the softmax warps
   uint64_t k_full[kStages];
   uint64_t v_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
   uint64_t p_full;
-  uint64_t o_ready;
+  uint64_t o_ready[kStages];  // P V_i commits to o_ready[i % kStages]
   uint64_t mma_done;
 };
 
@@ -156,6 +159,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     s_niv = build_kv_intervals(m, t0, min(TBM, a.s_local - t0), TBN, s_iv, kMaxIvTc);
     s_abort = 0;
     mbar_init(bar(bars.q_full), 1);
+    mbar_init(bar(bars.q_tmem), kSoftmax);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(bars.k_full[s]), 1);
       mbar_init(bar(bars.v_full[s]), 1);
@@ -163,7 +167,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     }
     for (int s = 0; s < 2; ++s) mbar_init(bar(bars.s_full[s]), 1);
     mbar_init(bar(bars.p_full), kSoftmax);
-    mbar_init(bar(bars.o_ready), 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(bar(bars.o_ready[s]), 1);
     mbar_init(bar(bars.mma_done), 1);
     for (int w = 0; w < 4; ++w) {
       mbar_init(bar(s_pair[w][0]), 64);
@@ -243,7 +247,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, TBN, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-      bool ok = mbar_wait(bar(bars.q_full), 0, &s_abort, kWaitLimitNs);
+      bool ok = mbar_wait(bar(bars.q_tmem), 0, &s_abort, kWaitLimitNs);
       if (!ok) fail(&s_abort);
       tc_fence_after();
       for (int j = 0; ok && j <= nb; ++j) {
@@ -256,12 +260,12 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             break;
           }
           tc_fence_after();
+          // A = Q from TMEM (columns kQCol.., bf16 pairs), B = K tile (K-major)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            const uint64_t da = sdesc_sw128(sb + L::Q + off, 16, 1024);
             const uint64_t db = sdesc_sw128(sb + L::K + st * L::TILE + off, 16, 1024);
-            umma_bf16(tmem + buf * 128, da, db, idS, kk > 0 ? 1u : 0u);
+            umma_bf16_ts(tmem + buf * 128, tmem + kQCol + kk * 8, db, idS, kk > 0 ? 1u : 0u);
           }
           umma_commit(bar(bars.s_full[buf]));
         }
@@ -282,7 +286,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                          (i > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(bar(bars.kv_empty[st]));
-          umma_commit(bar(bars.o_ready));
+          umma_commit(bar(bars.o_ready[i % kStages]));
         }
       }
       // drain: all MMAs issued by this thread must finish before TMEM is freed
@@ -323,7 +327,28 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       *out = s_red[u & 1][hf ^ 1][row];
       return true;
     };
-    for (int j = 0; j < nb; ++j, it.next()) {
+    // Q rows -> TMEM (bf16 pairs), each half of a row by one of the two warps
+    if (!wait_warp(bar(bars.q_full), 0)) {
+      fail(&s_abort);
+      ok = false;
+    } else {
+      constexpr int kChunks = D / 16;  // 16-byte chunks per half row
+      uint32_t qv[4 * kChunks];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int e0 = hf * (D / 2) + c * 8;  // first element of the chunk
+        const int box = e0 >> 6, chunk = (e0 & 63) >> 3;
+        const uint4 v = *reinterpret_cast<const uint4*>(
+            smem_raw + L::Q + box * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4));
+        qv[4 * c] = v.x; qv[4 * c + 1] = v.y; qv[4 * c + 2] = v.z; qv[4 * c + 3] = v.w;
+      }
+      if constexpr (D == 128) tmem_st32(tmem + lane_base + kQCol + hf * 32, qv);
+      else tmem_st16(tmem + lane_base + kQCol + hf * 16, qv);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(bars.q_tmem));
+    }
+    for (int j = 0; ok && j < nb; ++j, it.next()) {
       const int buf = j & 1;
       if (!wait_warp(bar(bars.s_full[buf]), (j >> 1) & 1)) {
         fail(&s_abort);
@@ -378,14 +403,22 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l_run = l_run * alpha + sum;
 
-      if (j > 0) {
-        if (!wait_warp(bar(bars.o_ready), (j - 1) & 1)) {
+      // O only has to be complete (P V_{j-1} done) when it is rescaled.  P_j
+      // goes to the other TMEM buffer than P_{j-1}, so without a rescale the
+      // softmax does not wait for the tensor core and P V_j can follow
+      // P V_{j-1} back to back.  P V_i commits to o_ready[i % kStages]; when
+      // the softmax holds S_j, K_j has been loaded into the stage that
+      // P V_{j-kStages} released, so at most kStages-1 products are still in
+      // flight and the parity wait on o_ready[(j-1) % kStages] is unambiguous.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const int i = j - 1;
+        if (!wait_warp(bar(bars.o_ready[i % kStages]), (i / kStages) & 1)) {
           fail(&s_abort);
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        {
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
             const uint32_t col = 256 + hf * (D / 2) + c * 32;
@@ -408,7 +441,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       tc_fence_before();
       mbar_arrive(bar(bars.p_full));
     }
-    if (ok && !wait_warp(bar(bars.o_ready), (nb - 1) & 1)) {
+    if (ok && !wait_warp(bar(bars.o_ready[(nb - 1) % kStages]), ((nb - 1) / kStages) & 1)) {
       fail(&s_abort);
       ok = false;
     }
