@@ -35,7 +35,7 @@ _SIGNATURES = {
     "cp_detect_pad_between_seqs": ([_P, _P, _I, ctypes.POINTER(_I)], _I),
     "cp_validate_seqlens": ([_P, _P, _I, _I64, _I, _I, _I], _I),
     "cp_valid_end": ([_P, _P, _I, _I, _I, _I, _I, ctypes.POINTER(_I64)], _I),
-    "cp_meta_bytes": ([_I, _I64], _SZ),
+    "cp_meta_bytes": ([_I, _I64, _I], _SZ),
     "cp_partition_index": ([_P, _P, _I, _I64, _I, _I, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "cp_thd_gather": ([_P, _P, _I, _P, _I64, _I64, _I64, _P], _I),
     "cp_thd_scatter": ([_P, _P, _I, _P, _I64, _I64, _I64, _P], _I),
@@ -147,8 +147,8 @@ def cp_valid_end(cu, cup, cp_size: int, rank: int, strategy: int, pad_between_se
     return int(out.value)
 
 
-def cp_meta_bytes(n_docs: int, s_local: int) -> int:
-    return int(lib().cp_meta_bytes(n_docs, s_local))
+def cp_meta_bytes(n_docs: int, total_tokens: int, cp_size: int) -> int:
+    return int(lib().cp_meta_bytes(n_docs, total_tokens, cp_size))
 
 
 def cp_attn_bwd_workspace_bytes(s_local: int, H: int) -> int:

@@ -64,12 +64,7 @@ struct BwdArgs {
 };
 
 __device__ __forceinline__ bool meta_ok_bwd(const BwdArgs& a, const MetaHeader* h) {
-  const bool fits = h->n_segs >= 0 && h->n_segs <= h->max_segs && h->seg_offset == 64 &&
-                    (int64_t)h->rows_offset >= 64 + 32 * (int64_t)h->max_segs &&
-                    (int64_t)h->rows_offset + 8 * (int64_t)a.s_local <= (int64_t)a.meta_bytes;
-  const bool ok = fits && h->magic == kMetaMagic && h->status == 0 && h->s_local == a.s_local &&
-                  h->rank == a.rank && h->cp_size == a.cp && h->strategy == a.strategy &&
-                  h->total_tokens == a.T;
+  const bool ok = meta_matches(h, a.meta_bytes, a.T, a.s_local, a.cp, a.rank, a.strategy);
   if (!ok && threadIdx.x == 0)
     atomicCAS(&g_status_bwd_tc, 0, h->status != 0 ? h->status : (int)CP_ERR_METADATA);
   return ok;
@@ -141,7 +136,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
 
   if (threadIdx.x == 0) {
-    s_niv = build_kv_intervals(m, t0, min(128, a.s_local - t0), 128, s_iv, kMaxIv);
+    s_niv = copy_list(m.qlists + (kListBytes / 8) * tile, s_iv);
     s_abort = 0;
     mbar_init(bar_addr(bars.qd_full), 1);
     for (int s = 0; s < kStg; ++s) {
@@ -389,7 +384,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
 
   if (threadIdx.x == 0) {
-    s_niv = build_q_intervals(m, j0, min(j0 + 128, a.T) - 1, 128, s_iv, kMaxIv);
+    s_niv = copy_list(m.klists + (kListBytes / 8) * blockIdx.x, s_iv);
     s_abort = 0;
     mbar_init(bar_addr(bars.kv_full), 1);
     for (int s = 0; s < kStg; ++s) {

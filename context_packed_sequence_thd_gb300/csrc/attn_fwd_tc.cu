@@ -104,12 +104,7 @@ struct Ctl {
 };
 
 __device__ __forceinline__ bool meta_ok_tc(const TcArgs& a, const MetaHeader* h) {
-  const bool fits = h->n_segs >= 0 && h->n_segs <= h->max_segs && h->seg_offset == 64 &&
-                    (int64_t)h->rows_offset >= 64 + 32 * (int64_t)h->max_segs &&
-                    (int64_t)h->rows_offset + 8 * (int64_t)a.s_local <= (int64_t)a.meta_bytes;
-  const bool ok = fits && h->magic == kMetaMagic && h->status == 0 && h->s_local == a.s_local &&
-                  h->rank == a.rank && h->cp_size == a.cp && h->strategy == a.strategy &&
-                  h->total_tokens == a.T;
+  const bool ok = meta_matches(h, a.meta_bytes, a.T, a.s_local, a.cp, a.rank, a.strategy);
   if (!ok && threadIdx.x == 0)
     atomicCAS(&g_status_fwd_tc, 0, h->status != 0 ? h->status : (int)CP_ERR_METADATA);
   return ok;
@@ -156,7 +151,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
   auto bar = [](uint64_t& b) { return smem_u32(&b); };
   if (threadIdx.x == 0) {
-    s_niv = build_kv_intervals(m, t0, min(TBM, a.s_local - t0), TBN, s_iv, kMaxIvTc);
+    s_niv = copy_list(m.qlists + (kListBytes / 8) * tile, s_iv);
     s_abort = 0;
     mbar_init(bar(bars.q_full), 1);
     mbar_init(bar(bars.q_tmem), kSoftmax);

@@ -14,15 +14,23 @@ namespace cpthd {
 // kernels.  Layout in device memory:
 //   [0, 64)                   MetaHeader
 //   [64, 64 + 32*max_segs)    Segment[max_segs], sorted by local_start
-//   then int32 row_lo[s_local], int32 row_hi[s_local]
+//   rows_offset:              int32 row_lo[s_local], int32 row_hi[s_local]
+//   lists_offset (16-aligned): one 64-byte block list per 128-row query tile
+//                             (the key blocks it attends), then one per
+//                             128-key block (the query tiles attending it)
 // A segment is a maximal run of local rows that are consecutive global rows
 // of one document: one DUAL_CHUNK_SWAP chunk, or one document's piece of a
 // NO_LOAD_BALANCE range.  Row t of a segment (u = t - local_start) is global
 // row global_start + u; it is a real token when u < valid_len.
 // row_lo/row_hi: the keys local row t attends are [row_lo[t], row_hi[t]]
 // (row_hi = -1, row_lo = 0 for padding rows).
+// A block list is int2[8]: {count, 0} then up to 7 merged, increasing
+// inclusive intervals [first, last] of 128-wide block indices.
 // ---------------------------------------------------------------------------
 constexpr int32_t kMetaMagic = 0x43505448;  // "CPTH"
+constexpr int kTile = 128;       // query-tile rows and key-block width of the lists
+constexpr int kListCap = 7;      // intervals per list (over capacity the last widens)
+constexpr int kListBytes = 64;
 
 struct MetaHeader {
   int32_t magic;
@@ -37,9 +45,10 @@ struct MetaHeader {
   int32_t pad_between_seqs;
   int32_t total_tokens;
   int32_t max_segs;
-  int32_t seg_offset;   // bytes
-  int32_t rows_offset;  // bytes; row_lo at rows_offset, row_hi 4*s_local later
-  int32_t reserved[2];
+  int32_t seg_offset;    // bytes
+  int32_t rows_offset;   // bytes; row_lo at rows_offset, row_hi 4*s_local later
+  int32_t lists_offset;  // bytes; query-tile lists, then key-block lists
+  int32_t n_kblocks;     // number of 128-key blocks (ceil(total_tokens / 128))
 };
 static_assert(sizeof(MetaHeader) == 64, "header is 64 bytes");
 
@@ -59,8 +68,13 @@ inline __host__ __device__ size_t seg_offset_bytes() { return 64; }
 inline __host__ __device__ size_t rows_offset_bytes(int n_docs) {
   return 64 + 32 * (size_t)max_segs_for(n_docs);
 }
-inline __host__ __device__ size_t meta_bytes_for(int n_docs, int64_t s_local) {
-  return rows_offset_bytes(n_docs) + 8 * (size_t)s_local;
+inline __host__ __device__ size_t lists_offset_bytes(int n_docs, int64_t s_local) {
+  return (rows_offset_bytes(n_docs) + 8 * (size_t)s_local + 15) & ~(size_t)15;
+}
+inline __host__ __device__ int64_t n_tiles_of(int64_t rows) { return (rows + kTile - 1) / kTile; }
+inline __host__ __device__ size_t meta_bytes_for(int n_docs, int64_t s_local, int cp) {
+  return lists_offset_bytes(n_docs, s_local) +
+         (size_t)kListBytes * (size_t)(n_tiles_of(s_local) + n_tiles_of(s_local * cp));
 }
 
 struct MetaView {
@@ -68,6 +82,8 @@ struct MetaView {
   const Segment* segs;
   const int32_t* row_lo;
   const int32_t* row_hi;
+  const int2* qlists;  // per 128-row query tile: key blocks attended
+  const int2* klists;  // per 128-key block: query tiles attending it
 };
 
 inline __device__ MetaView meta_view(const void* meta) {
@@ -77,7 +93,32 @@ inline __device__ MetaView meta_view(const void* meta) {
   v.segs = reinterpret_cast<const Segment*>(base + v.hdr->seg_offset);
   v.row_lo = reinterpret_cast<const int32_t*>(base + v.hdr->rows_offset);
   v.row_hi = v.row_lo + v.hdr->s_local;
+  v.qlists = reinterpret_cast<const int2*>(base + v.hdr->lists_offset);
+  v.klists = v.qlists + (kListBytes / 8) * n_tiles_of(v.hdr->s_local);
   return v;
+}
+
+// The metadata header belongs to this call and its tables lie inside the
+// caller's buffer of meta_bytes.
+inline __device__ bool meta_matches(const MetaHeader* h, size_t meta_bytes, int T, int s_local,
+                                    int cp, int rank, int strategy) {
+  const int64_t lists_end = (int64_t)h->lists_offset +
+                            (int64_t)kListBytes * (n_tiles_of(s_local) + (int64_t)h->n_kblocks);
+  const bool fits = h->n_segs >= 0 && h->n_segs <= h->max_segs && h->seg_offset == 64 &&
+                    (int64_t)h->rows_offset >= 64 + 32 * (int64_t)h->max_segs &&
+                    (int64_t)h->lists_offset >= (int64_t)h->rows_offset + 8 * (int64_t)s_local &&
+                    (h->lists_offset & 15) == 0 && h->n_kblocks == n_tiles_of(T) &&
+                    lists_end <= (int64_t)meta_bytes;
+  return fits && h->magic == kMetaMagic && h->status == 0 && h->s_local == s_local &&
+         h->rank == rank && h->cp_size == cp && h->strategy == strategy && h->total_tokens == T;
+}
+
+// Copies a precomputed block list (count, then intervals) to out[]; returns
+// the interval count.
+inline __device__ int copy_list(const int2* list, int2* out) {
+  const int n = min(list[0].x, kListCap);
+  for (int i = 0; i < n; ++i) out[i] = list[1 + i];
+  return n;
 }
 
 // Index of the last segment whose local_start <= t (segments are sorted and

@@ -6,7 +6,9 @@
 // contiguous physical rows [r*s_local, (r+1)*s_local) while the THD metadata
 // keeps the logical document boundaries.  The per-rank valid-token counts
 // (the quantity the P2P issue's get_cu_seqlens_on_cp_rank helper recomputes
-// with many small launches) fall out of the same pass.
+// with many small launches) fall out of the same pass, and so do the block
+// lists the attention kernels iterate: for every 128-row query tile the key
+// blocks it attends, for every 128-key block the query tiles attending it.
 //
 // One CTA of 1024 threads: documents are processed 1024 at a time; a
 // block-wide exclusive scan (warp __shfl_up_sync scans + one scan of the warp
@@ -158,7 +160,8 @@ partition_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup
     hdr->max_segs = max_segs;
     hdr->seg_offset = (int32_t)seg_offset_bytes();
     hdr->rows_offset = (int32_t)rows_offset_bytes(n_docs);
-    hdr->reserved[0] = hdr->reserved[1] = 0;
+    hdr->lists_offset = (int32_t)lists_offset_bytes(n_docs, s_local);
+    hdr->n_kblocks = (int32_t)n_tiles_of(T);
     if (e) atomicCAS(&g_status_partition, 0, e);
   }
   __syncthreads();
@@ -179,6 +182,25 @@ partition_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup
       row_hi[t] = valid ? g : -1;
     }
   }
+
+  // pass 3: block lists (from the segment table written above)
+  __syncthreads();
+  const MetaView mv = meta_view(meta);
+  const int n_qt = (int)n_tiles_of(s_local);
+  const int n_kb = (int)n_tiles_of(T);
+  int2* lists = reinterpret_cast<int2*>(meta + lists_offset_bytes(n_docs, s_local));
+  for (int q = threadIdx.x; q < n_qt + n_kb; q += kThreads) {
+    int2* out = lists + (kListBytes / 8) * q;
+    int cnt;
+    if (q < n_qt) {
+      const int t0 = q * kTile;
+      cnt = build_kv_intervals(mv, t0, min(kTile, s_local - t0), kTile, out + 1, kListCap);
+    } else {
+      const int j0 = (q - n_qt) * kTile;
+      cnt = build_q_intervals(mv, j0, min(j0 + kTile, T) - 1, kTile, out + 1, kListCap);
+    }
+    out[0] = make_int2(cnt, 0);
+  }
 }
 
 }  // namespace
@@ -186,9 +208,9 @@ partition_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup
 
 using namespace cpthd;
 
-extern "C" size_t cp_meta_bytes(int n_docs, int64_t s_local) {
-  if (n_docs < 0 || s_local < 0) return 0;
-  return meta_bytes_for(n_docs, s_local);
+extern "C" size_t cp_meta_bytes(int n_docs, int64_t total_tokens, int cp_size) {
+  if (n_docs < 0 || total_tokens < 0 || cp_size < 1 || total_tokens % cp_size) return 0;
+  return meta_bytes_for(n_docs, total_tokens / cp_size, cp_size);
 }
 
 extern "C" int cp_partition_index(const int32_t* d_cu, const int32_t* d_cup, int n_docs,
@@ -203,7 +225,7 @@ extern "C" int cp_partition_index(const int32_t* d_cu, const int32_t* d_cup, int
   if (total_tokens < 0 || total_tokens > INT32_MAX) return CP_ERR_INVALID_ARG;
   if (total_tokens % cp_size) return CP_ERR_DIVISIBILITY;
   const int64_t s_local = total_tokens / cp_size;
-  if (meta_bytes < meta_bytes_for(n_docs, s_local)) return CP_ERR_WORKSPACE;
+  if (meta_bytes < meta_bytes_for(n_docs, s_local, cp_size)) return CP_ERR_WORKSPACE;
   if (!cpthd_host::aligned16(d_meta)) return CP_ERR_ALIGNMENT;
   partition_kernel<<<1, 1024, 0, cpthd_host::as_stream(stream)>>>(
       d_cu, d_cup, n_docs, (int)total_tokens, cp_size, rank, (int)strategy,

@@ -106,7 +106,7 @@ class CPPlan:
         self.d_cu = torch.from_numpy(self.cu).to(self.device)
         self.d_cup = torch.from_numpy(self.cup).to(self.device)
         self.restore = torch.empty(self.T, dtype=torch.int32, device=self.device)
-        nbytes = api.cp_meta_bytes(self.n_docs, self.s_local)
+        nbytes = api.cp_meta_bytes(self.n_docs, self.T, self.cp)
         self.ranks = []
         for r in range(self.cp):
             self.ranks.append(RankMeta(

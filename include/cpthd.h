@@ -104,11 +104,13 @@ int cp_valid_end(const int32_t* cu_host, const int32_t* cup_host, int n_docs, in
  * batch slicing; metadata keeps logical document boundaries).
  * ------------------------------------------------------------------------- */
 
-/* Bytes of device metadata cp_partition_index writes for one rank:
- * a 64-byte header, a segment table (32 bytes x (2*n_docs+2)) and two int32
- * tables of s_local entries (each local row's document start and last
- * attended key, -1 for padding rows). */
-size_t cp_meta_bytes(int n_docs, int64_t s_local);
+/* Bytes of device metadata cp_partition_index writes for one rank
+ * (s_local = total_tokens / cp_size): a 64-byte header, a segment table
+ * (32 bytes x (2*n_docs+2)), two int32 tables of s_local entries (each local
+ * row's document start and last attended key, -1 for padding rows) and
+ * 64-byte block lists, one per 128-row query tile and one per 128-key block.
+ * Returns 0 for invalid sizes (total_tokens not divisible by cp_size). */
+size_t cp_meta_bytes(int n_docs, int64_t total_tokens, int cp_size);
 
 /* One launch.  Reads d_cu / d_cup (device, int32 [n_docs+1]; d_cu is only
  * read when pad_between_seqs != 0) and writes, for rank `rank`:

@@ -55,7 +55,7 @@ def test_partition_rejects_bad_metadata_on_device():
     d = dev()
     cup = torch.tensor([0, 10, 24], dtype=torch.int32, device=d)   # 10 % 4 != 0 for DCS, cp=2
     idx = torch.full((12,), -5, dtype=torch.int32, device=d)
-    meta = torch.zeros(api.cp_meta_bytes(2, 12), dtype=torch.uint8, device=d)
+    meta = torch.zeros(api.cp_meta_bytes(2, 24, 2), dtype=torch.uint8, device=d)
     api.cp_partition_index(None, cup, 24, 2, 0, pipeline.DCS, 0, idx, None, meta)
     torch.cuda.synchronize()
     assert _hdr(meta)[1] == -2
