@@ -8,25 +8,33 @@
 // LSE = -inf.  Both DUAL_CHUNK_SWAP chunks of a rank go through one launch:
 // the key range of every row comes from the rank's row tables.
 //
-// One CTA = one 128-row query tile of one head; 10 warps:
+// Persistent kernel: one CTA per SM walks a static list of work items
+// (128-row query tile, head), heaviest tiles first, item k going to CTA
+// k % gridDim.x.  Within a CTA the pipeline never drains between items: all
+// barrier phases follow global counters and Q is double buffered in TMEM
+// (the softmax warps copy the next item's Q there during the current item's
+// first block), so the next item's loads and S products overlap the current
+// item's last blocks and its epilogue.  10 warps:
 //   warps 0-7  softmax: TMEM lane r = query row r, shared by warps r/32 and
 //              r/32+4 which take one half of the key columns each.  Loads S
 //              from TMEM, masks by the row's key range, online softmax in the
-//              log2 domain, rescales O in TMEM when the row max grows, writes
-//              P (bf16 pairs) back into TMEM over S, and finally normalises O
-//              and stores O / LSE.
-//   warp 8     TMA producer: Q once, then K and V 128-key tiles into a
-//              2-stage ring (separate K / V barriers).
+//              log2 domain (the row max is exchanged between the two warps
+//              through shared memory), rescales O only when the max grows by
+//              more than 2^8, writes P (bf16 pairs) back into TMEM over S, and
+//              finally normalises O and stores O / LSE.
+//   warp 8     TMA producer: Q per item into a landing buffer, then K and V
+//              128-key tiles into a 3-stage ring.
 //   warp 9     TMEM allocator and single-thread MMA issuer:
-//              S[j%2] = Q K_j^T (M=128, N=128, K=D) and O += P_j V_j
-//              (M=128, N=D, K=128; A = P from TMEM, B = V as an MN-major
-//              shared operand), fp32 accumulators in TMEM: S0 cols [0,128),
-//              S1 [128,256), O [256,256+D); P_j aliases the first 64 columns of S_j.
-// The MMA of S_{j+1} overlaps the softmax of S_j; P_j goes to the other
-// S buffer than P_{j-1}, and the softmax waits for P V_{j-1} only when it has
-// to rescale O, so consecutive P V products are issued back to back.
-// Key blocks: only those some row of the tile attends (document and causal
-// skipping from the segment table), in increasing order.
+//              S[g%2] = Q K_g^T (M=128, N=128, K=D; A = Q from TMEM, B = K
+//              K-major in shared memory) and O += P_g V_g (M=128, N=D, K=128;
+//              A = P from TMEM, B = V as an MN-major shared operand).  TMEM:
+//              S0 cols [0,128), S1 [128,256), O [256,256+D), Q0 / Q1 (bf16
+//              pairs) at 256+D and 256+3D/2.
+// The MMA of S_{g+1} overlaps the softmax of S_g; P_g goes to the other S
+// buffer than P_{g-1}, and the softmax waits for P V_{g-1} only when it has to
+// rescale O, so consecutive P V products are issued back to back.
+// Key blocks per tile come from the precomputed block lists (document and
+// causal skipping), in increasing order.
 // Every wait is bounded (mbar_wait): a wait that runs out sets the device
 // status word to CP_ERR_TIMEOUT, the CTA drains its own copies / MMAs and
 // frees its TMEM before it returns.
@@ -52,17 +60,19 @@ constexpr int kSoftmax = 256;      // threads of the softmax warps 0-7
 constexpr int kProdWarp = 8, kMmaWarp = 9;
 constexpr int kStages = 3;         // K/V ring depth
 constexpr int kBoxBytes = 128 * 128;  // one 128-row x 128-byte TMA box
-constexpr int kMaxIvTc = 64;  // over capacity the last interval widens (still correct)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kQCol = 384;  // Q (bf16 pairs) in TMEM: columns [384, 384 + D/2)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr float kLn2f = 0.6931471805599453f;
+constexpr uint32_t kOCol = 256;  // O accumulator: columns [256, 256 + D)
+// Q of item ii as bf16 pairs: TMEM columns [q_col(ii % 2), + D/2)
+template <int D>
+__host__ __device__ constexpr uint32_t q_col(int b) { return 256 + D + b * (D / 2); }
 
 template <int D>
 struct Layout {
-  static constexpr int BOXES = D / 64;         // 64-element boxes along D
+  static constexpr int BOXES = D / 64;            // 64-element boxes along D
   static constexpr int TILE = BOXES * kBoxBytes;  // one Q / K / V tile
-  static constexpr int Q = 0;
+  static constexpr int Q = 0;                     // Q landing buffer
   static constexpr int K = Q + TILE;
   static constexpr int V = K + kStages * TILE;
   static constexpr int BYTES = V + kStages * TILE;
@@ -78,14 +88,16 @@ struct TcArgs {
 };
 
 struct Bars {
-  uint64_t q_full;
-  uint64_t q_tmem;  // Q copied from shared memory into TMEM by the softmax warps
+  uint64_t q_full;     // Q of the next item landed in shared memory
+  uint64_t q_sfree;    // ... and was copied out into TMEM (buffer reusable)
+  uint64_t q_tmem[2];  // Q of item ii is in TMEM buffer ii % 2
   uint64_t k_full[kStages];
   uint64_t v_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
-  uint64_t p_full;
-  uint64_t o_ready[kStages];  // P V_i commits to o_ready[i % kStages]
+  uint64_t p_full[2];  // P_g ready: p_full[g % 2] (two barriers so the softmax can
+                       // never complete a phase the MMA thread has not waited for)
+  uint64_t o_ready[kStages];  // P V_g commits to o_ready[g % kStages]
   uint64_t mma_done;
 };
 
@@ -97,9 +109,7 @@ struct Ctl {
   uint64_t pair[4][2];  // row-max / row-sum exchange of softmax warps w, w+4
   uint32_t tmem;
   int abort;
-  int niv;
-  int pad;
-  int2 iv[kMaxIvTc];
+  int pad[2];
   float red[2][2][TBM];  // [exchange parity][column half][row]
 };
 
@@ -115,7 +125,22 @@ __device__ __forceinline__ void fail(volatile int* abort) {
   atomicCAS(&g_status_fwd_tc, 0, (int)CP_ERR_TIMEOUT);
 }
 
-struct Iter {  // flattened walk over the key-block intervals
+// One work item: its tile, head and the key blocks of the tile's block list.
+struct Item {
+  const int2* list;  // precomputed list: list[0].x intervals in list[1..]
+  int t0, h, n_iv, nb;
+  __device__ void load(const MetaView& m, int k, int n_qt, int H) {
+    const int tile = n_qt - 1 - k / H;  // later tiles carry more causal work
+    h = k % H;
+    t0 = tile * TBM;
+    list = m.qlists + (kListBytes / 8) * tile;
+    n_iv = min(list[0].x, kListCap);
+    nb = 0;
+    for (int i = 0; i < n_iv; ++i) nb += list[1 + i].y - list[1 + i].x + 1;
+  }
+};
+
+struct Iter {  // flattened walk over an item's key-block intervals
   const int2* iv;
   int n, i, b;
   __device__ void init(const int2* p, int cnt) { iv = p; n = cnt; i = 0; b = cnt > 0 ? p[0].x : 0; }
@@ -132,9 +157,6 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const MetaView m = meta_view(a.meta);
   if (!meta_ok_tc(a, m.hdr)) return;
-  const int tile = gridDim.x - 1 - blockIdx.x;  // heavier (later) tiles first
-  const int h = blockIdx.y;
-  const int t0 = tile * TBM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sb = smem_u32(smem_raw);  // tiles need 1024-byte alignment (128B swizzle)
   if (sb & 1023u) {
@@ -144,49 +166,33 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw + L::BYTES);
   Bars& bars = ctl.bars;
   volatile int& s_abort = *reinterpret_cast<volatile int*>(&ctl.abort);
-  int2* s_iv = ctl.iv;
-  int& s_niv = ctl.niv;
-  float (*s_red)[2][TBM] = ctl.red;
-  uint64_t (*s_pair)[2] = ctl.pair;
+  const int n_qt = (int)n_tiles_of(a.s_local);
+  const int n_items = n_qt * a.H;
 
   auto bar = [](uint64_t& b) { return smem_u32(&b); };
   if (threadIdx.x == 0) {
-    s_niv = copy_list(m.qlists + (kListBytes / 8) * tile, s_iv);
-    s_abort = 0;
+    ctl.abort = 0;
     mbar_init(bar(bars.q_full), 1);
-    mbar_init(bar(bars.q_tmem), kSoftmax);
+    mbar_init(bar(bars.q_sfree), kSoftmax);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(bars.q_tmem[b]), kSoftmax);
+      mbar_init(bar(bars.s_full[b]), 1);
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(bars.k_full[s]), 1);
       mbar_init(bar(bars.v_full[s]), 1);
       mbar_init(bar(bars.kv_empty[s]), 1);
+      mbar_init(bar(bars.o_ready[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) mbar_init(bar(bars.s_full[s]), 1);
-    mbar_init(bar(bars.p_full), kSoftmax);
-    for (int s = 0; s < kStages; ++s) mbar_init(bar(bars.o_ready[s]), 1);
+    mbar_init(bar(bars.p_full[0]), kSoftmax);
+    mbar_init(bar(bars.p_full[1]), kSoftmax);
     mbar_init(bar(bars.mma_done), 1);
     for (int w = 0; w < 4; ++w) {
-      mbar_init(bar(s_pair[w][0]), 64);
-      mbar_init(bar(s_pair[w][1]), 64);
+      mbar_init(bar(ctl.pair[w][0]), 64);
+      mbar_init(bar(ctl.pair[w][1]), 64);
     }
     fence_barrier_init();
   }
-  __syncthreads();
-  int nb = 0;
-  for (int i = 0; i < s_niv; ++i) nb += s_iv[i].y - s_iv[i].x + 1;
-
-  if (nb == 0) {  // no real query row in this tile
-    if (threadIdx.x < TBM) {
-      const int t = t0 + threadIdx.x;
-      if (t < a.s_local) {
-        uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)t * a.H + h) * D);
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-        a.lse[(int64_t)h * a.s_local + t] = -INFINITY;
-      }
-    }
-    return;
-  }
-
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&ctl.tmem), kTmemCols);
     tmem_relinquish();
@@ -202,36 +208,78 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar(bars.q_full), L::TILE);
+      // Q of non-empty item qi into the landing buffer, once the softmax warps
+      // copied Q of item qi-1 out of it.  Q runs one item ahead of K/V: the
+      // softmax copies item qi+1's Q during item qi's first block.
+      auto load_q = [&](int qi, int k) -> bool {
+        if (!mbar_wait(bar(bars.q_sfree), (qi & 1) ^ 1, &s_abort, kWaitLimitNs)) return false;
+        Item it;
+        it.load(m, k, n_qt, a.H);
+        mbar_arrive_expect_tx(bar(bars.q_full), L::TILE);
 #pragma unroll
-      for (int b = 0; b < L::BOXES; ++b)
-        tma_load_3d(sb + L::Q + b * kBoxBytes, &tm_q, bar(bars.q_full), b * 64, h, t0);
-      Iter it;
-      it.init(s_iv, s_niv);
-      int issued = 0;
-      for (int j = 0; j < nb; ++j, it.next()) {
-        const int st = j % kStages;
-        if (!mbar_wait(bar(bars.kv_empty[st]), ((j / kStages) & 1) ^ 1, &s_abort, kWaitLimitNs)) {
-          fail(&s_abort);
-          break;
+        for (int b = 0; b < L::BOXES; ++b)
+          tma_load_3d(sb + L::Q + b * kBoxBytes, &tm_q, bar(bars.q_full), b * 64, it.h, it.t0);
+        return true;
+      };
+      auto next_item = [&](int k) -> int {
+        for (k += gridDim.x; k < n_items; k += gridDim.x) {
+          Item nx;
+          nx.load(m, k, n_qt, a.H);
+          if (nx.nb > 0) return k;
         }
-        const int key0 = it.b * TBN;
-        mbar_arrive_expect_tx(bar(bars.k_full[st]), L::TILE);
+        return n_items;
+      };
+      int ii = 0, ld = 0, nq = 0;
+      bool ok = true;
+      int kf = next_item((int)blockIdx.x - (int)gridDim.x);
+      if (kf < n_items) {
+        if (load_q(0, kf)) {
+          nq = 1;
+        } else {
+          fail(&s_abort);
+          ok = false;
+        }
+      }
+      for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+        Item it;
+        it.load(m, k, n_qt, a.H);
+        if (it.nb == 0) continue;
+        const int kn = next_item(k);
+        if (kn < n_items) {
+          if (!load_q(ii + 1, kn)) {
+            fail(&s_abort);
+            break;
+          }
+          nq = ii + 2;
+        }
+        ++ii;
+        Iter bi;
+        bi.init(it.list + 1, it.n_iv);
+        for (int j = 0; j < it.nb; ++j, bi.next(), ++ld) {
+          const int st = ld % kStages;
+          if (!mbar_wait(bar(bars.kv_empty[st]), ((ld / kStages) & 1) ^ 1, &s_abort,
+                         kWaitLimitNs)) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          const int key0 = bi.b * TBN;
+          mbar_arrive_expect_tx(bar(bars.k_full[st]), L::TILE);
 #pragma unroll
-        for (int b = 0; b < L::BOXES; ++b)
-          tma_load_3d(sb + L::K + st * L::TILE + b * kBoxBytes, &tm_k, bar(bars.k_full[st]),
-                      b * 64, h, key0);
-        mbar_arrive_expect_tx(bar(bars.v_full[st]), L::TILE);
+          for (int b = 0; b < L::BOXES; ++b)
+            tma_load_3d(sb + L::K + st * L::TILE + b * kBoxBytes, &tm_k, bar(bars.k_full[st]),
+                        b * 64, it.h, key0);
+          mbar_arrive_expect_tx(bar(bars.v_full[st]), L::TILE);
 #pragma unroll
-        for (int b = 0; b < L::BOXES; ++b)
-          tma_load_3d(sb + L::V + st * L::TILE + b * kBoxBytes, &tm_v, bar(bars.v_full[st]),
-                      b * 64, h, key0);
-        ++issued;
+          for (int b = 0; b < L::BOXES; ++b)
+            tma_load_3d(sb + L::V + st * L::TILE + b * kBoxBytes, &tm_v, bar(bars.v_full[st]),
+                        b * 64, it.h, key0);
+        }
       }
       // drain: every copy this CTA issued must land before shared memory goes away
       int never = 0;
-      mbar_wait(bar(bars.q_full), 0, &never, kWaitLimitNs);
-      for (int j = max(0, issued - kStages); j < issued; ++j) {
+      if (nq > 0) mbar_wait(bar(bars.q_full), (nq - 1) & 1, &never, kWaitLimitNs);
+      for (int j = max(0, ld - kStages); j < ld; ++j) {
         const int st = j % kStages;
         mbar_wait(bar(bars.k_full[st]), (j / kStages) & 1, &never, kWaitLimitNs);
         mbar_wait(bar(bars.v_full[st]), (j / kStages) & 1, &never, kWaitLimitNs);
@@ -242,48 +290,70 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, TBN, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-      bool ok = mbar_wait(bar(bars.q_tmem), 0, &s_abort, kWaitLimitNs);
-      if (!ok) fail(&s_abort);
-      tc_fence_after();
-      for (int j = 0; ok && j <= nb; ++j) {
-        if (j < nb) {
-          const int st = j % kStages, buf = j & 1;
-          // S_j overwrites P_{j-2} (same TMEM columns); P V_{j-2} was issued
+      // the previous block's P V is issued after the next block's S
+      int pv_g = -1, pv_st = 0;
+      bool pv_first = false;
+      auto issue_pv = [&]() -> bool {
+        if (!mbar_wait(bar(bars.p_full[pv_g & 1]), (pv_g >> 1) & 1, &s_abort, kWaitLimitNs) ||
+            !mbar_wait(bar(bars.v_full[pv_st]), (pv_g / kStages) & 1, &s_abort, kWaitLimitNs))
+          return false;
+        tc_fence_after();
+        // A = P from TMEM: keys [0,64) over columns [0,32) and keys [64,128)
+        // over [64,96) of S_g's buffer (written by the two column halves)
+#pragma unroll
+        for (int kk = 0; kk < TBN / 16; ++kk) {
+          const uint64_t db =
+              sdesc_sw128(sb + L::V + pv_st * L::TILE + kk * 2048, kBoxBytes, 1024);
+          umma_bf16_ts(tmem + kOCol,
+                       tmem + (pv_g & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8, db, idO,
+                       (!pv_first || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(bars.kv_empty[pv_st]));
+        umma_commit(bar(bars.o_ready[pv_g % kStages]));
+        return true;
+      };
+      int ii = 0, g = 0;
+      bool ok = true;
+      for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+        Item it;
+        it.load(m, k, n_qt, a.H);
+        if (it.nb == 0) continue;
+        const int qb = ii & 1;
+        if (!mbar_wait(bar(bars.q_tmem[qb]), (ii >> 1) & 1, &s_abort, kWaitLimitNs)) {
+          fail(&s_abort);
+          break;
+        }
+        ++ii;
+        for (int j = 0; j < it.nb; ++j, ++g) {
+          const int st = g % kStages, buf = g & 1;
+          // S_g overwrites P_{g-2} (same TMEM columns); P V_{g-2} was issued
           // earlier by this thread and MMAs of one thread run in order
-          if (!mbar_wait(bar(bars.k_full[st]), (j / kStages) & 1, &s_abort, kWaitLimitNs)) {
+          if (!mbar_wait(bar(bars.k_full[st]), (g / kStages) & 1, &s_abort, kWaitLimitNs)) {
             fail(&s_abort);
+            ok = false;
             break;
           }
           tc_fence_after();
-          // A = Q from TMEM (columns kQCol.., bf16 pairs), B = K tile (K-major)
+          // A = Q from TMEM buffer qb (bf16 pairs), B = K tile (K-major)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            const uint64_t db = sdesc_sw128(sb + L::K + st * L::TILE + off, 16, 1024);
-            umma_bf16_ts(tmem + buf * 128, tmem + kQCol + kk * 8, db, idS, kk > 0 ? 1u : 0u);
+            umma_bf16_ts(tmem + buf * 128, tmem + q_col<D>(qb) + kk * 8,
+                         sdesc_sw128(sb + L::K + st * L::TILE + off, 16, 1024), idS,
+                         kk > 0 ? 1u : 0u);
           }
           umma_commit(bar(bars.s_full[buf]));
-        }
-        if (j >= 1) {
-          const int i = j - 1, st = i % kStages;
-          if (!mbar_wait(bar(bars.p_full), i & 1, &s_abort, kWaitLimitNs) ||
-              !mbar_wait(bar(bars.v_full[st]), (i / kStages) & 1, &s_abort, kWaitLimitNs)) {
+          if (pv_g >= 0 && !issue_pv()) {
             fail(&s_abort);
+            ok = false;
             break;
           }
-          tc_fence_after();
-          // A = P_i from TMEM: keys [0,64) over columns [0,32) and keys
-          // [64,128) over [64,96) of S_i's buffer (written by the two halves)
-#pragma unroll
-          for (int kk = 0; kk < TBN / 16; ++kk) {
-            const uint64_t db = sdesc_sw128(sb + L::V + st * L::TILE + kk * 2048, kBoxBytes, 1024);
-            umma_bf16_ts(tmem + 256, tmem + (i & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8, db, idO,
-                         (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(bar(bars.kv_empty[st]));
-          umma_commit(bar(bars.o_ready[i % kStages]));
+          pv_g = g;
+          pv_st = st;
+          pv_first = (j == 0);
         }
       }
+      if (ok && pv_g >= 0 && !issue_pv()) fail(&s_abort);
       // drain: all MMAs issued by this thread must finish before TMEM is freed
       umma_commit(bar(bars.mma_done));
       int never = 0;
@@ -294,19 +364,12 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // Warps w and w+4 share TMEM lanes 32*(w%4).. (one query row per lane):
     // warp w takes key columns [0,64) of each block, warp w+4 columns
     // [64,128).  The row max is combined through shared memory once per
-    // block (an mbarrier of the two warps, bounded wait); each half keeps its own
-    // partial row sum and rescales / normalises its half of O.
+    // block (an mbarrier of the two warps, bounded wait); each half keeps its
+    // own partial row sum and rescales / normalises its half of O.
     const int row = (warp & 3) * 32 + lane;  // = TMEM lane
     const int hf = warp >> 2;
-    const int t = t0 + row;
-    const int lo = t < a.s_local ? m.row_lo[t] : 0;
-    const int hi = t < a.s_local ? m.row_hi[t] : -1;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
-    Iter it;
-    it.init(s_iv, s_niv);
-    bool ok = true;
     // waits of the softmax warps are made warp-uniform (tcgen05.ld/st are
     // .sync.aligned): the warp proceeds only when every lane saw the phase
     auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
@@ -316,17 +379,16 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // exchange u of the two warps of a pair: publish a value, wait for the
     // partner's (bounded, like every other wait), return the partner's value
     auto exchange = [&](int u, float v, float* out) -> bool {
-      s_red[u & 1][hf][row] = v;
-      mbar_arrive(bar(s_pair[warp & 3][u & 1]));
-      if (!wait_warp(bar(s_pair[warp & 3][u & 1]), (u >> 1) & 1)) return false;
-      *out = s_red[u & 1][hf ^ 1][row];
+      ctl.red[u & 1][hf][row] = v;
+      mbar_arrive(bar(ctl.pair[warp & 3][u & 1]));
+      if (!wait_warp(bar(ctl.pair[warp & 3][u & 1]), (u >> 1) & 1)) return false;
+      *out = ctl.red[u & 1][hf ^ 1][row];
       return true;
     };
-    // Q rows -> TMEM (bf16 pairs), each half of a row by one of the two warps
-    if (!wait_warp(bar(bars.q_full), 0)) {
-      fail(&s_abort);
-      ok = false;
-    } else {
+    // Q of non-empty item qi (landed in shared memory) -> TMEM buffer qi % 2,
+    // each half row by one of the two warps of the pair
+    auto copy_q = [&](int qi) -> bool {
+      if (!wait_warp(bar(bars.q_full), qi & 1)) return false;
       constexpr int kChunks = D / 16;  // 16-byte chunks per half row
       uint32_t qv[4 * kChunks];
 #pragma unroll
@@ -337,86 +399,131 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             smem_raw + L::Q + box * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4));
         qv[4 * c] = v.x; qv[4 * c + 1] = v.y; qv[4 * c + 2] = v.z; qv[4 * c + 3] = v.w;
       }
-      if constexpr (D == 128) tmem_st32(tmem + lane_base + kQCol + hf * 32, qv);
-      else tmem_st16(tmem + lane_base + kQCol + hf * 16, qv);
+      const uint32_t col = q_col<D>(qi & 1) + hf * (D / 4);
+      if constexpr (D == 128) tmem_st32(tmem + lane_base + col, qv);
+      else tmem_st16(tmem + lane_base + col, qv);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(bars.q_tmem));
+      mbar_arrive(bar(bars.q_tmem[qi & 1]));
+      mbar_arrive(bar(bars.q_sfree));
+      return true;
+    };
+    // next non-empty item after k (n_items if none)
+    auto next_item = [&](int k) -> int {
+      for (k += gridDim.x; k < n_items; k += gridDim.x) {
+        Item nx;
+        nx.load(m, k, n_qt, a.H);
+        if (nx.nb > 0) return k;
+      }
+      return n_items;
+    };
+    int ii = 0, g = 0, u = 0;
+    bool ok = true;
+    if (next_item((int)blockIdx.x - (int)gridDim.x) < n_items && !copy_q(0)) {
+      fail(&s_abort);
+      ok = false;
     }
-    for (int j = 0; ok && j < nb; ++j, it.next()) {
-      const int buf = j & 1;
-      if (!wait_warp(bar(bars.s_full[buf]), (j >> 1) & 1)) {
-        fail(&s_abort);
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[64];
-      tmem_ld32(tmem + lane_base + buf * 128 + 64 * hf, reinterpret_cast<uint32_t*>(s));
-      tmem_ld32(tmem + lane_base + buf * 128 + 64 * hf + 32, reinterpret_cast<uint32_t*>(s + 32));
-
-      const int k0 = it.b * TBN + 64 * hf;  // key of this thread's first column
-      if (!(lo <= k0 && hi >= k0 + 63)) {
+    for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+      Item itm;
+      itm.load(m, k, n_qt, a.H);
+      const int t = itm.t0 + row;
+      const bool in = t < a.s_local;
+      if (itm.nb == 0) {  // no real query row in this tile: O = 0, LSE = -inf
+        if (in) {
+          uint4* dst =
+              reinterpret_cast<uint4*>(a.o + ((int64_t)t * a.H + itm.h) * D + hf * (D / 2));
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int key = k0 + c;
-          if (key < lo || key > hi) s[c] = -INFINITY;
+          for (int c = 0; c < D / 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+          if (hf == 0) a.lse[(int64_t)itm.h * a.s_local + t] = -INFINITY;
         }
+        continue;
       }
-      float mx8[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mx8[q] = s[q];
-#pragma unroll
-      for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      float mx_other;
-      if (!exchange(j, mx, &mx_other)) {
-        fail(&s_abort);
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, mx_other);
-      // The running max m_run is only moved (and O, l rescaled) when the new
-      // block's max exceeds it by more than 8 in log2 units; otherwise the
-      // stale max stays in use for this block's P, which then stays below
-      // 2^8 -- P and l always use the same reference, so O/l is unchanged.
-      float alpha = 1.f;
-      if (m_run == -INFINITY || (mx - m_run) * sl2 > 8.f) {
-        const float m_new = fmaxf(m_run, mx);
-        alpha = m_run == -INFINITY ? 0.f : ex2_approx((m_run - m_new) * sl2);
-        m_run = m_new;
-      }
-      const float mref = m_run == -INFINITY ? 0.f : m_run * sl2;
-      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        s[c] = ex2_approx(fmaf(s[c], sl2, -mref));
-        sum8[c & 7] += s[c];
-      }
-      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                        ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      l_run = l_run * alpha + sum;
-
-      // O only has to be complete (P V_{j-1} done) when it is rescaled.  P_j
-      // goes to the other TMEM buffer than P_{j-1}, so without a rescale the
-      // softmax does not wait for the tensor core and P V_j can follow
-      // P V_{j-1} back to back.  P V_i commits to o_ready[i % kStages]; when
-      // the softmax holds S_j, K_j has been loaded into the stage that
-      // P V_{j-kStages} released, so at most kStages-1 products are still in
-      // flight and the parity wait on o_ready[(j-1) % kStages] is unambiguous.
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        const int i = j - 1;
-        if (!wait_warp(bar(bars.o_ready[i % kStages]), (i / kStages) & 1)) {
+      const int lo = in ? m.row_lo[t] : 0;
+      const int hi = in ? m.row_hi[t] : -1;
+      float m_run = -INFINITY, l_run = 0.f;
+      Iter bi;
+      bi.init(itm.list + 1, itm.n_iv);
+      for (int j = 0; j < itm.nb; ++j, bi.next(), ++g, ++u) {
+        const int buf = g & 1;
+        if (!wait_warp(bar(bars.s_full[buf]), (g >> 1) & 1)) {
           fail(&s_abort);
           ok = false;
           break;
         }
         tc_fence_after();
-        {
+        float s[64];
+        tmem_ld32(tmem + lane_base + buf * 128 + 64 * hf, reinterpret_cast<uint32_t*>(s));
+        tmem_ld32(tmem + lane_base + buf * 128 + 64 * hf + 32,
+                  reinterpret_cast<uint32_t*>(s + 32));
+        // the next item's Q goes into the TMEM buffer the previous item used;
+        // all of that item's S products are done (their s_full was waited for)
+        if (j == 0 && next_item(k) < n_items && !copy_q(ii + 1)) {
+          fail(&s_abort);
+          ok = false;
+          break;
+        }
+
+        const int k0 = bi.b * TBN + 64 * hf;  // key of this thread's first column
+        if (!(lo <= k0 && hi >= k0 + 63)) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int key = k0 + c;
+            if (key < lo || key > hi) s[c] = -INFINITY;
+          }
+        }
+        float mx8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx8[q] = s[q];
+#pragma unroll
+        for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        float mx_other;
+        if (!exchange(u, mx, &mx_other)) {
+          fail(&s_abort);
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, mx_other);
+        // The running max m_run is only moved (and O, l rescaled) when the new
+        // block's max exceeds it by more than 8 in log2 units; otherwise the
+        // stale max stays in use for this block's P, which then stays below
+        // 2^8 -- P and l always use the same reference, so O/l is unchanged.
+        float alpha = 1.f;
+        if (m_run == -INFINITY || (mx - m_run) * sl2 > 8.f) {
+          const float m_new = fmaxf(m_run, mx);
+          alpha = m_run == -INFINITY ? 0.f : ex2_approx((m_run - m_new) * sl2);
+          m_run = m_new;
+        }
+        const float mref = m_run == -INFINITY ? 0.f : m_run * sl2;
+        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          s[c] = ex2_approx(fmaf(s[c], sl2, -mref));
+          sum8[c & 7] += s[c];
+        }
+        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                          ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        l_run = l_run * alpha + sum;
+
+        // O only has to be complete (P V_{g-1} done) when it is rescaled.  P_g
+        // goes to the other TMEM buffer than P_{g-1}, so without a rescale
+        // the softmax does not wait for the tensor core.  P V_g commits to
+        // o_ready[g % kStages]; when the softmax holds S_g, K_g has been
+        // loaded into the stage that P V_{g-kStages} released, so at most
+        // kStages-1 products are in flight and the parity wait on
+        // o_ready[(g-1) % kStages] is unambiguous.
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          const int pv = g - 1;
+          if (!wait_warp(bar(bars.o_ready[pv % kStages]), (pv / kStages) & 1)) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
-            const uint32_t col = 256 + hf * (D / 2) + c * 32;
+            const uint32_t col = kOCol + hf * (D / 2) + c * 32;
             uint32_t o[32];
             tmem_ld32(tmem + lane_base + col, o);
 #pragma unroll
@@ -425,38 +532,41 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           }
           tmem_st_wait();
         }
-      }
-      {  // P (bf16 pairs) -> TMEM over the first 32 of this half's S columns
-        uint32_t pk[32];
+        {  // P (bf16 pairs) -> TMEM over the first 32 of this half's S columns
+          uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
-        tmem_st32(tmem + lane_base + buf * 128 + 64 * hf, pk);
+          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
+          tmem_st32(tmem + lane_base + buf * 128 + 64 * hf, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(bars.p_full[buf]));
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(bars.p_full));
-    }
-    if (ok && !wait_warp(bar(bars.o_ready[(nb - 1) % kStages]), ((nb - 1) / kStages) & 1)) {
-      fail(&s_abort);
-      ok = false;
-    }
-    // the row sum is the sum of the two halves' partial sums (same max)
-    float l_other = 0.f;
-    if (ok && !exchange(nb, l_run, &l_other)) {
-      fail(&s_abort);
-      ok = false;
-    }
-    const float l_tot = l_run + l_other;
-    if (ok) {
+      if (!ok) break;
+      // epilogue of the item: wait for its last P V, combine the halves' sums
+      const int last = g - 1;
+      if (!wait_warp(bar(bars.o_ready[last % kStages]), (last / kStages) & 1)) {
+        fail(&s_abort);
+        ok = false;
+        break;
+      }
+      float l_other = 0.f;
+      if (!exchange(u, l_run, &l_other)) {
+        fail(&s_abort);
+        ok = false;
+        break;
+      }
+      ++u;
+      const float l_tot = l_run + l_other;
       tc_fence_after();
       const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         const int col = hf * (D / 2) + c * 32;
         uint32_t o[32];
-        tmem_ld32(tmem + lane_base + 256 + col, o);
-        if (t < a.s_local) {
-          uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)t * a.H + h) * D + col);
+        tmem_ld32(tmem + lane_base + kOCol + col, o);
+        if (in) {
+          uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)t * a.H + itm.h) * D + col);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 v;
@@ -468,9 +578,10 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           }
         }
       }
-      if (t < a.s_local && hf == 0)
-        a.lse[(int64_t)h * a.s_local + t] =
+      if (in && hf == 0)
+        a.lse[(int64_t)itm.h * a.s_local + t] =
             l_tot > 0.f ? (m_run * sl2 + log2f(l_tot)) * kLn2f : -INFINITY;
+      ++ii;
     }
   }
 
@@ -485,6 +596,19 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      return 148;
+  }
+  return n;
+}
+
 template <int D>
 int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, cudaStream_t s) {
   alignas(64) CUtensorMap mq, mk, mv;
@@ -496,7 +620,8 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, 
   if (cudaFuncSetAttribute(attn_fwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return CP_ERR_CUDA;
-  dim3 grid((unsigned)((a.s_local + TBM - 1) / TBM), (unsigned)a.H);
+  const int64_t items = n_tiles_of(a.s_local) * (int64_t)a.H;
+  const int grid = (int)(items < sm_count() ? items : sm_count());
   attn_fwd_tc<D><<<grid, kThreadsTc, smem, s>>>(mq, mk, mv, a);
   return cpthd_host::launch_status();
 }
