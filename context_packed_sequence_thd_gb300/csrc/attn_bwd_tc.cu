@@ -6,26 +6,30 @@
 // forward's token layout): with Delta_t = dO_t . O_t (attn_delta),
 //   P = exp(scale q.k - LSE), dS = P (dO.v - Delta),
 //   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
-// Two kernels, no atomics (bitwise deterministic):
+// Two persistent kernels (one CTA per SM walking a static list of work
+// items, all barrier phases on global counters so the pipeline carries
+// across items), no atomics (bitwise deterministic):
 //
-// attn_dq_tc   one CTA per (128-query tile, head), iterating the key blocks
-//              the tile attends.  S = Q K^T and dP = dO V^T into TMEM
-//              (M=128 queries, N=128 keys); the compute warps (a query row
-//              per TMEM lane) form dS and write it back into TMEM as bf16 over S;
-//              dQ += dS K with A = dS from TMEM, B = K as an MN-major operand.
-// attn_dkdv_tc one CTA per (128-key block, head), iterating the rank's query
-//              tiles that attend the block (segment table).  S^T = K Q^T and
-//              dP^T = V dO^T into TMEM (M=128 keys, N=128 queries); compute
-//              warps (thread = key row) form P^T and dS^T in TMEM over S^T and
-//              dP^T; dV += P^T dO and dK += dS^T Q (A from TMEM, B = dO / Q as
-//              MN-major operands).  The block's partial dK/dV are added into
-//              the caller's fp32 accumulators by the block's only owner.
+// attn_dq_tc   items (128-query tile, head), iterating the key blocks the
+//              tile attends.  S = Q K^T and dP = dO V^T into TMEM (M=128
+//              queries, N=128 keys); the compute warps form dS and write it
+//              back into TMEM as bf16 over S; dQ += dS K with A = dS from TMEM,
+//              B = K as an MN-major operand.
+// attn_dkdv_tc items (128-key block, head), iterating the rank's query tiles
+//              that attend the block (precomputed block lists).  S^T = K Q^T
+//              and dP^T = V dO^T into TMEM (M=128 keys, N=128 queries); the
+//              compute warps form P^T and dS^T in TMEM over S^T and dP^T;
+//              dV += P^T dO and dK += dS^T Q (A from TMEM, B = dO / Q as
+//              MN-major operands).  Each item's partial dK/dV are added into
+//              the caller's fp32 accumulators by the item's only owner.
 // Warp roles: warps 0-7 compute (warp w serves TMEM lanes 32*(w%4).. and the
 // column half w/4 of every row, so two warps share each row's elementwise
 // work), warp 8 TMA producer, warp 9 TMEM allocator + single-thread MMA
 // issuer.  A compute thread writes P / dS back only into TMEM columns it has
 // itself already read (the first half of its own column range), so the two
-// halves never race.  Every wait is bounded.
+// halves never race.  The next item's Q/dO (K/V) tiles are loaded as soon as
+// the current item's last S products retire, and the epilogue of an item
+// overlaps the next item's first products.  Every wait is bounded.
 #include <math.h>
 
 #include "common.cuh"
@@ -46,7 +50,6 @@ constexpr int kCompute = 256;  // threads of warps 0-7
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kStg = 2;
 constexpr int kBox = 128 * 128;  // one 128-row x 128-byte TMA box
-constexpr int kMaxIv = 64;
 constexpr uint32_t kCols = 512;
 constexpr uint64_t kLimitNs = 4000000000ull;
 constexpr float kLog2ef = 1.4426950408889634f;
@@ -84,6 +87,21 @@ struct Iter {
   }
 };
 
+// One work item: a 128-row tile (dQ: query tile; dK/dV: key block), a head,
+// and the blocks of the tile's precomputed list.
+struct Item {
+  const int2* list;
+  int tile, h, n_iv, nb;
+  __device__ void load(const int2* lists, int k, int H, int n_tiles, bool heavy_last) {
+    tile = heavy_last ? n_tiles - 1 - k / H : k / H;
+    h = k % H;
+    list = lists + (kListBytes / 8) * tile;
+    n_iv = min(list[0].x, kListCap);
+    nb = 0;
+    for (int i = 0; i < n_iv; ++i) nb += list[1 + i].y - list[1 + i].x + 1;
+  }
+};
+
 __device__ __forceinline__ uint32_t bar_addr(uint64_t& b) { return smem_u32(&b); }
 
 // K-major operand offset of k-step kk (16 elements) inside a tile of
@@ -93,6 +111,19 @@ __device__ __forceinline__ uint32_t kmajor_off(int kk) { return (kk >> 2) * kBox
 // TMEM column of k-step kk (16 elements) of an A operand written by the two
 // column halves: elements [0,64) at columns [0,32), [64,128) at [64,96).
 __device__ __forceinline__ uint32_t ts_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      return 148;
+  }
+  return n;
+}
 
 // ===========================================================================
 // dQ
@@ -107,10 +138,12 @@ struct DqLayout {
   static constexpr int BYTES = V + kStg * TILE;
 };
 
-struct DqBars {
-  uint64_t qd_full;
+struct DqCtl {
+  uint64_t qd_full, qd_free;  // Q/dO of the item landed / all its S, dP products done
   uint64_t k_full[kStg], v_full[kStg], kv_empty[kStg];
   uint64_t st_full, ds_full, done, mma_done;
+  uint32_t tmem;
+  int abort;
 };
 
 template <int D>
@@ -121,198 +154,227 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   using L = DqLayout<D>;
   constexpr int BOXES = D / 64;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ DqBars bars;
-  __shared__ uint32_t s_tmem;
-  __shared__ volatile int s_abort;
-  __shared__ int2 s_iv[kMaxIv];
-  __shared__ int s_niv;
-
   const MetaView m = meta_view(a.meta);
   if (!meta_ok_bwd(a, m.hdr)) return;
-  const int tile = gridDim.x - 1 - blockIdx.x;
-  const int h = blockIdx.y;
-  const int t0 = tile * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
-
-  if (threadIdx.x == 0) {
-    s_niv = copy_list(m.qlists + (kListBytes / 8) * tile, s_iv);
-    s_abort = 0;
-    mbar_init(bar_addr(bars.qd_full), 1);
-    for (int s = 0; s < kStg; ++s) {
-      mbar_init(bar_addr(bars.k_full[s]), 1);
-      mbar_init(bar_addr(bars.v_full[s]), 1);
-      mbar_init(bar_addr(bars.kv_empty[s]), 1);
-    }
-    mbar_init(bar_addr(bars.st_full), 1);
-    mbar_init(bar_addr(bars.ds_full), kCompute);
-    mbar_init(bar_addr(bars.done), 1);
-    mbar_init(bar_addr(bars.mma_done), 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-  int nb = 0;
-  for (int i = 0; i < s_niv; ++i) nb += s_iv[i].y - s_iv[i].x + 1;
-  if (nb == 0) {  // no real query row: dQ = 0
-    if (threadIdx.x < 128 && t0 + (int)threadIdx.x < a.s_local) {
-      uint4* dst = reinterpret_cast<uint4*>(a.dq + ((int64_t)(t0 + threadIdx.x) * a.H + h) * D);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-    }
+  const uint32_t sb = smem_u32(smem_raw);  // tiles need 1024-byte alignment (128B swizzle)
+  if (sb & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(&g_status_bwd_tc, 0, (int)CP_ERR_UNSUPPORTED);
     return;
   }
+  DqCtl& c = *reinterpret_cast<DqCtl*>(smem_raw + L::BYTES);
+  volatile int& s_abort = *reinterpret_cast<volatile int*>(&c.abort);
+  const int n_qt = (int)n_tiles_of(a.s_local);
+  const int n_items = n_qt * a.H;
+
+  if (threadIdx.x == 0) {
+    c.abort = 0;
+    mbar_init(bar_addr(c.qd_full), 1);
+    mbar_init(bar_addr(c.qd_free), 1);
+    for (int s = 0; s < kStg; ++s) {
+      mbar_init(bar_addr(c.k_full[s]), 1);
+      mbar_init(bar_addr(c.v_full[s]), 1);
+      mbar_init(bar_addr(c.kv_empty[s]), 1);
+    }
+    mbar_init(bar_addr(c.st_full), 1);
+    mbar_init(bar_addr(c.ds_full), kCompute);
+    mbar_init(bar_addr(c.done), 1);
+    mbar_init(bar_addr(c.mma_done), 1);
+    fence_barrier_init();
+  }
   if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(&s_tmem), kCols);
+    tmem_alloc(smem_u32(&c.tmem), kCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s_tmem;  // S [0,128)  dP [128,256)  dQ [256,256+D)
+  const uint32_t tmem = c.tmem;  // S [0,128)  dP [128,256)  dQ [256,256+D)
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_addr(bars.qd_full), 2 * L::TILE);
-#pragma unroll
-      for (int b = 0; b < BOXES; ++b) {
-        tma_load_3d(sb + L::Q + b * kBox, &tm_q, bar_addr(bars.qd_full), b * 64, h, t0);
-        tma_load_3d(sb + L::DO + b * kBox, &tm_do, bar_addr(bars.qd_full), b * 64, h, t0);
-      }
-      Iter it;
-      it.init(s_iv, s_niv);
-      int issued = 0;
-      for (int j = 0; j < nb; ++j, it.next()) {
-        const int st = j % kStg;
-        if (!mbar_wait(bar_addr(bars.kv_empty[st]), ((j / kStg) & 1) ^ 1, &s_abort, kLimitNs)) {
+      int ii = 0, ld = 0;
+      bool ok = true;
+      for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+        Item it;
+        it.load(m.qlists, k, a.H, n_qt, true);
+        if (it.nb == 0) continue;
+        // single Q/dO buffer: free once the previous item's S, dP retired
+        if (!mbar_wait(bar_addr(c.qd_free), (ii & 1) ^ 1, &s_abort, kLimitNs)) {
           fail(&s_abort);
           break;
         }
-        const int key0 = it.b * 128;
-        mbar_arrive_expect_tx(bar_addr(bars.k_full[st]), L::TILE);
+        const int t0 = it.tile * 128;
+        mbar_arrive_expect_tx(bar_addr(c.qd_full), 2 * L::TILE);
 #pragma unroll
-        for (int b = 0; b < BOXES; ++b)
-          tma_load_3d(sb + L::K + st * L::TILE + b * kBox, &tm_k, bar_addr(bars.k_full[st]),
-                      b * 64, h, key0);
-        mbar_arrive_expect_tx(bar_addr(bars.v_full[st]), L::TILE);
+        for (int b = 0; b < BOXES; ++b) {
+          tma_load_3d(sb + L::Q + b * kBox, &tm_q, bar_addr(c.qd_full), b * 64, it.h, t0);
+          tma_load_3d(sb + L::DO + b * kBox, &tm_do, bar_addr(c.qd_full), b * 64, it.h, t0);
+        }
+        ++ii;
+        Iter bi;
+        bi.init(it.list + 1, it.n_iv);
+        for (int j = 0; j < it.nb; ++j, bi.next(), ++ld) {
+          const int st = ld % kStg;
+          if (!mbar_wait(bar_addr(c.kv_empty[st]), ((ld / kStg) & 1) ^ 1, &s_abort, kLimitNs)) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          const int key0 = bi.b * 128;
+          mbar_arrive_expect_tx(bar_addr(c.k_full[st]), L::TILE);
 #pragma unroll
-        for (int b = 0; b < BOXES; ++b)
-          tma_load_3d(sb + L::V + st * L::TILE + b * kBox, &tm_v, bar_addr(bars.v_full[st]),
-                      b * 64, h, key0);
-        ++issued;
+          for (int b = 0; b < BOXES; ++b)
+            tma_load_3d(sb + L::K + st * L::TILE + b * kBox, &tm_k, bar_addr(c.k_full[st]),
+                        b * 64, it.h, key0);
+          mbar_arrive_expect_tx(bar_addr(c.v_full[st]), L::TILE);
+#pragma unroll
+          for (int b = 0; b < BOXES; ++b)
+            tma_load_3d(sb + L::V + st * L::TILE + b * kBox, &tm_v, bar_addr(c.v_full[st]),
+                        b * 64, it.h, key0);
+        }
       }
       int never = 0;
-      mbar_wait(bar_addr(bars.qd_full), 0, &never, kLimitNs);
-      for (int j = max(0, issued - kStg); j < issued; ++j) {
+      if (ii > 0) mbar_wait(bar_addr(c.qd_full), (ii - 1) & 1, &never, kLimitNs);
+      for (int j = max(0, ld - kStg); j < ld; ++j) {
         const int st = j % kStg;
-        mbar_wait(bar_addr(bars.k_full[st]), (j / kStg) & 1, &never, kLimitNs);
-        mbar_wait(bar_addr(bars.v_full[st]), (j / kStg) & 1, &never, kLimitNs);
+        mbar_wait(bar_addr(c.k_full[st]), (j / kStg) & 1, &never, kLimitNs);
+        mbar_wait(bar_addr(c.v_full[st]), (j / kStg) & 1, &never, kLimitNs);
       }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
-      bool ok = mbar_wait(bar_addr(bars.qd_full), 0, &s_abort, kLimitNs);
-      if (!ok) fail(&s_abort);
-      for (int j = 0; ok && j < nb; ++j) {
-        const int st = j % kStg;
-        if (!mbar_wait(bar_addr(bars.k_full[st]), (j / kStg) & 1, &s_abort, kLimitNs) ||
-            !mbar_wait(bar_addr(bars.v_full[st]), (j / kStg) & 1, &s_abort, kLimitNs)) {
+      int ii = 0, g = 0;
+      bool ok = true;
+      for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+        Item it;
+        it.load(m.qlists, k, a.H, n_qt, true);
+        if (it.nb == 0) continue;
+        if (!mbar_wait(bar_addr(c.qd_full), ii & 1, &s_abort, kLimitNs)) {
           fail(&s_abort);
           break;
         }
-        tc_fence_after();
+        ++ii;
+        for (int j = 0; j < it.nb; ++j, ++g) {
+          const int st = g % kStg;
+          if (!mbar_wait(bar_addr(c.k_full[st]), (g / kStg) & 1, &s_abort, kLimitNs) ||
+              !mbar_wait(bar_addr(c.v_full[st]), (g / kStg) & 1, &s_abort, kLimitNs)) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = kmajor_off(kk);
-          umma_bf16(tmem, sdesc_sw128(sb + L::Q + off, 16, 1024),
-                    sdesc_sw128(sb + L::K + st * L::TILE + off, 16, 1024), idS, kk > 0);
-          umma_bf16(tmem + 128, sdesc_sw128(sb + L::DO + off, 16, 1024),
-                    sdesc_sw128(sb + L::V + st * L::TILE + off, 16, 1024), idS, kk > 0);
-        }
-        umma_commit(bar_addr(bars.st_full));
-        if (!mbar_wait(bar_addr(bars.ds_full), j & 1, &s_abort, kLimitNs)) {
-          fail(&s_abort);
-          break;
-        }
-        tc_fence_after();
-        // dQ += dS K : A = dS (bf16 in TMEM over S), B = K tile as MN-major (N = d)
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = kmajor_off(kk);
+            umma_bf16(tmem, sdesc_sw128(sb + L::Q + off, 16, 1024),
+                      sdesc_sw128(sb + L::K + st * L::TILE + off, 16, 1024), idS, kk > 0);
+            umma_bf16(tmem + 128, sdesc_sw128(sb + L::DO + off, 16, 1024),
+                      sdesc_sw128(sb + L::V + st * L::TILE + off, 16, 1024), idS, kk > 0);
+          }
+          umma_commit(bar_addr(c.st_full));
+          if (j == it.nb - 1) umma_commit(bar_addr(c.qd_free));
+          if (!mbar_wait(bar_addr(c.ds_full), g & 1, &s_abort, kLimitNs)) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // dQ += dS K : A = dS (bf16 in TMEM over S), B = K tile as MN-major (N = d)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + 256, tmem + ts_col(kk),
-                       sdesc_sw128(sb + L::K + st * L::TILE + kk * 2048, kBox, 1024), idQ,
-                       (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar_addr(bars.kv_empty[st]));
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16_ts(tmem + 256, tmem + ts_col(kk),
+                         sdesc_sw128(sb + L::K + st * L::TILE + kk * 2048, kBox, 1024), idQ,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar_addr(c.kv_empty[st]));
+        }
+        if (ok) umma_commit(bar_addr(c.done));
       }
-      umma_commit(bar_addr(bars.done));
-      umma_commit(bar_addr(bars.mma_done));
+      umma_commit(bar_addr(c.mma_done));
       int never = 0;
-      mbar_wait(bar_addr(bars.mma_done), 0, &never, kLimitNs);
+      mbar_wait(bar_addr(c.mma_done), 0, &never, kLimitNs);
     }
   } else {
     const int row = (warp & 3) * 32 + lane;  // TMEM lane = query row of the tile
     const int hf = warp >> 2;                // column half: keys [64hf, 64hf+64)
-    const int t = t0 + row;
-    const bool in = t < a.s_local;
-    const int lo = in ? m.row_lo[t] : 0;
-    const int hi = in ? m.row_hi[t] : -1;
-    const float lse2 = hi >= 0 ? a.lse[(int64_t)h * a.s_local + t] * kLog2ef : 0.f;
-    const float dl = hi >= 0 ? a.delta[(int64_t)h * a.s_local + t] : 0.f;
     const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale_log2;
     auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
       const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
       return __all_sync(0xffffffffu, w);
     };
-    Iter it;
-    it.init(s_iv, s_niv);
+    int ii = 0, g = 0;
     bool ok = true;
-    for (int j = 0; j < nb; ++j, it.next()) {
-      if (!wait_warp(bar_addr(bars.st_full), j & 1)) {
+    for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+      Item itm;
+      itm.load(m.qlists, k, a.H, n_qt, true);
+      const int t = itm.tile * 128 + row;
+      const bool in = t < a.s_local;
+      if (itm.nb == 0) {  // no real query row: dQ = 0
+        if (in) {
+          uint4* dst =
+              reinterpret_cast<uint4*>(a.dq + ((int64_t)t * a.H + itm.h) * D + hf * (D / 2));
+#pragma unroll
+          for (int q = 0; q < D / 16; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      const int lo = in ? m.row_lo[t] : 0;
+      const int hi = in ? m.row_hi[t] : -1;
+      const float lse2 = hi >= 0 ? a.lse[(int64_t)itm.h * a.s_local + t] * kLog2ef : 0.f;
+      const float dl = hi >= 0 ? a.delta[(int64_t)itm.h * a.s_local + t] : 0.f;
+      Iter bi;
+      bi.init(itm.list + 1, itm.n_iv);
+      for (int j = 0; j < itm.nb; ++j, bi.next(), ++g) {
+        if (!wait_warp(bar_addr(c.st_full), g & 1)) {
+          fail(&s_abort);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float p[64];
+        tmem_ld32(tmem + lb + 64 * hf, reinterpret_cast<uint32_t*>(p));
+        tmem_ld32(tmem + lb + 64 * hf + 32, reinterpret_cast<uint32_t*>(p + 32));
+        const int k0 = bi.b * 128 + 64 * hf;  // key of this thread's first column
+        if (lo <= k0 && hi >= k0 + 63) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) p[e] = ex2_approx(fmaf(p[e], sl2, -lse2));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            p[e] = (k0 + e >= lo && k0 + e <= hi) ? ex2_approx(fmaf(p[e], sl2, -lse2)) : 0.f;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t dp[32], pk[16];
+          tmem_ld32(tmem + lb + 128 + 64 * hf + 32 * cc, dp);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16(p[cc * 32 + 2 * e] * (__uint_as_float(dp[2 * e]) - dl),
+                              p[cc * 32 + 2 * e + 1] * (__uint_as_float(dp[2 * e + 1]) - dl));
+          tmem_st16(tmem + lb + 64 * hf + 16 * cc, pk);  // dS over this half's S columns
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_addr(c.ds_full));
+      }
+      if (!ok) break;
+      if (!wait_warp(bar_addr(c.done), ii & 1)) {
         fail(&s_abort);
         ok = false;
         break;
       }
-      tc_fence_after();
-      float p[64];
-      tmem_ld32(tmem + lb + 64 * hf, reinterpret_cast<uint32_t*>(p));
-      tmem_ld32(tmem + lb + 64 * hf + 32, reinterpret_cast<uint32_t*>(p + 32));
-      const int k0 = it.b * 128 + 64 * hf;  // key of this thread's first column
-      if (lo <= k0 && hi >= k0 + 63) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = ex2_approx(fmaf(p[c], sl2, -lse2));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          p[c] = (k0 + c >= lo && k0 + c <= hi) ? ex2_approx(fmaf(p[c], sl2, -lse2)) : 0.f;
-      }
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t dp[32], pk[16];
-        tmem_ld32(tmem + lb + 128 + 64 * hf + 32 * cc, dp);
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16(p[cc * 32 + 2 * e] * (__uint_as_float(dp[2 * e]) - dl),
-                            p[cc * 32 + 2 * e + 1] * (__uint_as_float(dp[2 * e + 1]) - dl));
-        tmem_st16(tmem + lb + 64 * hf + 16 * cc, pk);  // dS over this half's S columns
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar_addr(bars.ds_full));
-    }
-    if (ok && !wait_warp(bar_addr(bars.done), 0)) {
-      fail(&s_abort);
-      ok = false;
-    }
-    if (ok) {
+      ++ii;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = hf * (D / 2) + c * 32;  // dQ columns of this half
+      for (int cq = 0; cq < D / 64; ++cq) {
+        const int col = hf * (D / 2) + cq * 32;  // dQ columns of this half
         uint32_t o[32];
         tmem_ld32(tmem + lb + 256 + col, o);
         if (in) {
-          uint4* dst = reinterpret_cast<uint4*>(a.dq + ((int64_t)t * a.H + h) * D + col);
+          uint4* dst = reinterpret_cast<uint4*>(a.dq + ((int64_t)t * a.H + itm.h) * D + col);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 v;
@@ -324,6 +386,9 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           }
         }
       }
+      // dQ's TMEM columns are rewritten (accumulate = 0) only by the next
+      // item's first dQ product, which waits for this warp's next ds_full
+      tc_fence_before();
     }
   }
   tc_fence_before();
@@ -353,12 +418,16 @@ struct __align__(16) QInfo {  // per-query data of one 128-query step
   float lse2[128];
   float dl[128];
   int max_lo, min_hi;
+  int pad[2];
 };
 
-struct KvBars {
-  uint64_t kv_full;
+struct KvCtl {
+  QInfo qinfo[kStg];
+  uint64_t kv_full, kv_free;  // K/V of the item landed / all its S^T, dP^T products done
   uint64_t q_full[kStg], qi_full[kStg], q_empty[kStg];
   uint64_t st_full, p_full, ds_full, done, mma_done;
+  uint32_t tmem;
+  int abort;
 };
 
 template <int D>
@@ -369,258 +438,288 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   using L = KvLayout<D>;
   constexpr int BOXES = D / 64;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ KvBars bars;
-  __shared__ QInfo qinfo[kStg];
-  __shared__ uint32_t s_tmem;
-  __shared__ volatile int s_abort;
-  __shared__ int2 s_iv[kMaxIv];
-  __shared__ int s_niv;
-
   const MetaView m = meta_view(a.meta);
   if (!meta_ok_bwd(a, m.hdr)) return;
-  const int h = blockIdx.y;
-  const int j0 = blockIdx.x * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sb = smem_u32(smem_raw);
+  if (sb & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(&g_status_bwd_tc, 0, (int)CP_ERR_UNSUPPORTED);
+    return;
+  }
+  KvCtl& c = *reinterpret_cast<KvCtl*>(smem_raw + L::BYTES);
+  volatile int& s_abort = *reinterpret_cast<volatile int*>(&c.abort);
+  const int n_kb = (int)n_tiles_of(a.T);
+  const int n_items = n_kb * a.H;
 
   if (threadIdx.x == 0) {
-    s_niv = copy_list(m.klists + (kListBytes / 8) * blockIdx.x, s_iv);
-    s_abort = 0;
-    mbar_init(bar_addr(bars.kv_full), 1);
+    c.abort = 0;
+    mbar_init(bar_addr(c.kv_full), 1);
+    mbar_init(bar_addr(c.kv_free), 1);
     for (int s = 0; s < kStg; ++s) {
-      mbar_init(bar_addr(bars.q_full[s]), 1);
-      mbar_init(bar_addr(bars.qi_full[s]), 32);
-      mbar_init(bar_addr(bars.q_empty[s]), 1);
+      mbar_init(bar_addr(c.q_full[s]), 1);
+      mbar_init(bar_addr(c.qi_full[s]), 32);
+      mbar_init(bar_addr(c.q_empty[s]), 1);
     }
-    mbar_init(bar_addr(bars.st_full), 1);
-    mbar_init(bar_addr(bars.p_full), kCompute);
-    mbar_init(bar_addr(bars.ds_full), kCompute);
-    mbar_init(bar_addr(bars.done), 1);
-    mbar_init(bar_addr(bars.mma_done), 1);
+    mbar_init(bar_addr(c.st_full), 1);
+    mbar_init(bar_addr(c.p_full), kCompute);
+    mbar_init(bar_addr(c.ds_full), kCompute);
+    mbar_init(bar_addr(c.done), 1);
+    mbar_init(bar_addr(c.mma_done), 1);
     fence_barrier_init();
   }
-  __syncthreads();
-  int nq = 0;
-  for (int i = 0; i < s_niv; ++i) nq += s_iv[i].y - s_iv[i].x + 1;
-  if (nq == 0) return;  // no query of this rank attends these keys
   if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(&s_tmem), kCols);
+    tmem_alloc(smem_u32(&c.tmem), kCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s_tmem;  // S^T [0,128) dP^T [128,256) dK [256,256+D) dV [256+D,256+2D)
+  const uint32_t tmem = c.tmem;  // S^T [0,128) dP^T [128,256) dK [256,256+D) dV [256+D,256+2D)
 
   if (warp == kProducerWarp) {
     // all 32 lanes: lane 0 issues TMA, every lane loads per-query data
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_addr(bars.kv_full), 2 * L::TILE);
-#pragma unroll
-      for (int b = 0; b < BOXES; ++b) {
-        tma_load_3d(sb + L::K + b * kBox, &tm_k, bar_addr(bars.kv_full), b * 64, h, j0);
-        tma_load_3d(sb + L::V + b * kBox, &tm_v, bar_addr(bars.kv_full), b * 64, h, j0);
-      }
-    }
-    Iter it;
-    it.init(s_iv, s_niv);
-    int issued = 0;
-    for (int i = 0; i < nq; ++i, it.next()) {
-      const int st = i % kStg;
-      const bool w = mbar_wait(bar_addr(bars.q_empty[st]), ((i / kStg) & 1) ^ 1, &s_abort, kLimitNs);
-      if (!__all_sync(0xffffffffu, w)) {
+    int ii = 0, gs = 0;
+    bool ok = true;
+    for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+      Item it;
+      it.load(m.klists, k, a.H, n_kb, false);
+      if (it.nb == 0) continue;
+      // single K/V buffer: free once the previous item's S^T, dP^T retired
+      const bool wf = mbar_wait(bar_addr(c.kv_free), (ii & 1) ^ 1, &s_abort, kLimitNs);
+      if (!__all_sync(0xffffffffu, wf)) {
         if (lane == 0) fail(&s_abort);
         break;
       }
-      const int q0 = it.b * 128;
+      ++ii;
+      const int j0 = it.tile * 128;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar_addr(bars.q_full[st]), 2 * L::TILE);
+        mbar_arrive_expect_tx(bar_addr(c.kv_full), 2 * L::TILE);
 #pragma unroll
         for (int b = 0; b < BOXES; ++b) {
-          tma_load_3d(sb + L::Q + st * L::TILE + b * kBox, &tm_q, bar_addr(bars.q_full[st]),
-                      b * 64, h, q0);
-          tma_load_3d(sb + L::DO + st * L::TILE + b * kBox, &tm_do, bar_addr(bars.q_full[st]),
-                      b * 64, h, q0);
+          tma_load_3d(sb + L::K + b * kBox, &tm_k, bar_addr(c.kv_full), b * 64, it.h, j0);
+          tma_load_3d(sb + L::V + b * kBox, &tm_v, bar_addr(c.kv_full), b * 64, it.h, j0);
         }
       }
-      ++issued;
-      QInfo& qi = qinfo[st];
-      int mlo = INT_MIN, mhi = INT_MAX;
+      Iter bi;
+      bi.init(it.list + 1, it.n_iv);
+      for (int i = 0; i < it.nb; ++i, bi.next(), ++gs) {
+        const int st = gs % kStg;
+        const bool w = mbar_wait(bar_addr(c.q_empty[st]), ((gs / kStg) & 1) ^ 1, &s_abort, kLimitNs);
+        if (!__all_sync(0xffffffffu, w)) {
+          if (lane == 0) fail(&s_abort);
+          ok = false;
+          break;
+        }
+        const int q0 = bi.b * 128;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_addr(c.q_full[st]), 2 * L::TILE);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int c = lane + 32 * r;
-        const int t = q0 + c;
-        const bool in = t < a.s_local;
-        const int hi = in ? m.row_hi[t] : -1;
-        const int lo = in ? m.row_lo[t] : 0;
-        qi.lo[c] = lo;
-        qi.hi[c] = hi;
-        qi.lse2[c] = hi >= 0 ? a.lse[(int64_t)h * a.s_local + t] * kLog2ef : 0.f;
-        qi.dl[c] = hi >= 0 ? a.delta[(int64_t)h * a.s_local + t] : 0.f;
-        mlo = max(mlo, lo);
-        mhi = min(mhi, hi);
-      }
+          for (int b = 0; b < BOXES; ++b) {
+            tma_load_3d(sb + L::Q + st * L::TILE + b * kBox, &tm_q, bar_addr(c.q_full[st]),
+                        b * 64, it.h, q0);
+            tma_load_3d(sb + L::DO + st * L::TILE + b * kBox, &tm_do, bar_addr(c.q_full[st]),
+                        b * 64, it.h, q0);
+          }
+        }
+        QInfo& qi = c.qinfo[st];
+        int mlo = INT_MIN, mhi = INT_MAX;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        mlo = max(mlo, __shfl_xor_sync(0xffffffffu, mlo, o));
-        mhi = min(mhi, __shfl_xor_sync(0xffffffffu, mhi, o));
+        for (int r = 0; r < 4; ++r) {
+          const int cq = lane + 32 * r;
+          const int t = q0 + cq;
+          const bool in = t < a.s_local;
+          const int hi = in ? m.row_hi[t] : -1;
+          const int lo = in ? m.row_lo[t] : 0;
+          qi.lo[cq] = lo;
+          qi.hi[cq] = hi;
+          qi.lse2[cq] = hi >= 0 ? a.lse[(int64_t)it.h * a.s_local + t] * kLog2ef : 0.f;
+          qi.dl[cq] = hi >= 0 ? a.delta[(int64_t)it.h * a.s_local + t] : 0.f;
+          mlo = max(mlo, lo);
+          mhi = min(mhi, hi);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          mlo = max(mlo, __shfl_xor_sync(0xffffffffu, mlo, o));
+          mhi = min(mhi, __shfl_xor_sync(0xffffffffu, mhi, o));
+        }
+        if (lane == 0) {
+          qi.max_lo = mlo;
+          qi.min_hi = mhi;
+        }
+        __syncwarp();
+        mbar_arrive(bar_addr(c.qi_full[st]));
       }
-      if (lane == 0) {
-        qi.max_lo = mlo;
-        qi.min_hi = mhi;
-      }
-      __syncwarp();
-      mbar_arrive(bar_addr(bars.qi_full[st]));
     }
     if (lane == 0) {
       int never = 0;
-      mbar_wait(bar_addr(bars.kv_full), 0, &never, kLimitNs);
-      for (int i = max(0, issued - kStg); i < issued; ++i)
-        mbar_wait(bar_addr(bars.q_full[i % kStg]), (i / kStg) & 1, &never, kLimitNs);
+      if (ii > 0) mbar_wait(bar_addr(c.kv_full), (ii - 1) & 1, &never, kLimitNs);
+      for (int i = max(0, gs - kStg); i < gs; ++i)
+        mbar_wait(bar_addr(c.q_full[i % kStg]), (i / kStg) & 1, &never, kLimitNs);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
-      bool ok = mbar_wait(bar_addr(bars.kv_full), 0, &s_abort, kLimitNs);
-      if (!ok) fail(&s_abort);
-      for (int i = 0; ok && i < nq; ++i) {
-        const int st = i % kStg;
-        if (!mbar_wait(bar_addr(bars.q_full[st]), (i / kStg) & 1, &s_abort, kLimitNs)) {
+      int ii = 0, gs = 0;
+      bool ok = true;
+      for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+        Item it;
+        it.load(m.klists, k, a.H, n_kb, false);
+        if (it.nb == 0) continue;
+        if (!mbar_wait(bar_addr(c.kv_full), ii & 1, &s_abort, kLimitNs)) {
           fail(&s_abort);
           break;
         }
-        tc_fence_after();
+        ++ii;
+        for (int i = 0; i < it.nb; ++i, ++gs) {
+          const int st = gs % kStg;
+          if (!mbar_wait(bar_addr(c.q_full[st]), (gs / kStg) & 1, &s_abort, kLimitNs)) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = kmajor_off(kk);
-          umma_bf16(tmem, sdesc_sw128(sb + L::K + off, 16, 1024),
-                    sdesc_sw128(sb + L::Q + st * L::TILE + off, 16, 1024), idS, kk > 0);
-          umma_bf16(tmem + 128, sdesc_sw128(sb + L::V + off, 16, 1024),
-                    sdesc_sw128(sb + L::DO + st * L::TILE + off, 16, 1024), idS, kk > 0);
-        }
-        umma_commit(bar_addr(bars.st_full));
-        if (!mbar_wait(bar_addr(bars.p_full), i & 1, &s_abort, kLimitNs)) {
-          fail(&s_abort);
-          break;
-        }
-        tc_fence_after();
-        // dV += P^T dO : A = P^T (TMEM over S^T), B = dO tile as MN-major (N = d)
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = kmajor_off(kk);
+            umma_bf16(tmem, sdesc_sw128(sb + L::K + off, 16, 1024),
+                      sdesc_sw128(sb + L::Q + st * L::TILE + off, 16, 1024), idS, kk > 0);
+            umma_bf16(tmem + 128, sdesc_sw128(sb + L::V + off, 16, 1024),
+                      sdesc_sw128(sb + L::DO + st * L::TILE + off, 16, 1024), idS, kk > 0);
+          }
+          umma_commit(bar_addr(c.st_full));
+          if (i == it.nb - 1) umma_commit(bar_addr(c.kv_free));
+          if (!mbar_wait(bar_addr(c.p_full), gs & 1, &s_abort, kLimitNs)) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // dV += P^T dO : A = P^T (TMEM over S^T), B = dO tile as MN-major (N = d)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk),
-                       sdesc_sw128(sb + L::DO + st * L::TILE + kk * 2048, kBox, 1024), idG,
-                       (i > 0 || kk > 0) ? 1u : 0u);
-        if (!mbar_wait(bar_addr(bars.ds_full), i & 1, &s_abort, kLimitNs)) {
-          fail(&s_abort);
-          break;
-        }
-        tc_fence_after();
-        // dK += dS^T Q : A = dS^T (TMEM over dP^T), B = Q tile as MN-major
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk),
+                         sdesc_sw128(sb + L::DO + st * L::TILE + kk * 2048, kBox, 1024), idG,
+                         (i > 0 || kk > 0) ? 1u : 0u);
+          if (!mbar_wait(bar_addr(c.ds_full), gs & 1, &s_abort, kLimitNs)) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // dK += dS^T Q : A = dS^T (TMEM over dP^T), B = Q tile as MN-major
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + 256, tmem + 128 + ts_col(kk),
-                       sdesc_sw128(sb + L::Q + st * L::TILE + kk * 2048, kBox, 1024), idG,
-                       (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar_addr(bars.q_empty[st]));
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16_ts(tmem + 256, tmem + 128 + ts_col(kk),
+                         sdesc_sw128(sb + L::Q + st * L::TILE + kk * 2048, kBox, 1024), idG,
+                         (i > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar_addr(c.q_empty[st]));
+        }
+        if (ok) umma_commit(bar_addr(c.done));
       }
-      umma_commit(bar_addr(bars.done));
-      umma_commit(bar_addr(bars.mma_done));
+      umma_commit(bar_addr(c.mma_done));
       int never = 0;
-      mbar_wait(bar_addr(bars.mma_done), 0, &never, kLimitNs);
+      mbar_wait(bar_addr(c.mma_done), 0, &never, kLimitNs);
     }
   } else {
     const int row = (warp & 3) * 32 + lane;  // TMEM lane = key row of the block
     const int hf = warp >> 2;                // column half: queries [64hf, 64hf+64)
-    const int key = j0 + row;
     const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale_log2;
     auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
       const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
       return __all_sync(0xffffffffu, w);
     };
+    int ii = 0, gs = 0;
     bool ok = true;
-    for (int i = 0; i < nq; ++i) {
-      const int st = i % kStg;
-      if (!wait_warp(bar_addr(bars.st_full), i & 1) ||
-          !wait_warp(bar_addr(bars.qi_full[st]), (i / kStg) & 1)) {
+    for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+      Item itm;
+      itm.load(m.klists, k, a.H, n_kb, false);
+      if (itm.nb == 0) continue;  // no query of this rank attends these keys
+      const int key = itm.tile * 128 + row;
+      for (int i = 0; i < itm.nb; ++i, ++gs) {
+        const int st = gs % kStg;
+        if (!wait_warp(bar_addr(c.st_full), gs & 1) ||
+            !wait_warp(bar_addr(c.qi_full[st]), (gs / kStg) & 1)) {
+          fail(&s_abort);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const QInfo& qi = c.qinfo[st];
+        const float4* l4 = reinterpret_cast<const float4*>(qi.lse2 + 64 * hf);
+        const float4* d4 = reinterpret_cast<const float4*>(qi.dl + 64 * hf);
+        float p[64];
+        tmem_ld32(tmem + lb + 64 * hf, reinterpret_cast<uint32_t*>(p));
+        tmem_ld32(tmem + lb + 64 * hf + 32, reinterpret_cast<uint32_t*>(p + 32));
+        if (key >= qi.max_lo && key <= qi.min_hi) {  // every query of the step sees this key
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 l = l4[c4];
+            p[4 * c4 + 0] = ex2_approx(fmaf(p[4 * c4 + 0], sl2, -l.x));
+            p[4 * c4 + 1] = ex2_approx(fmaf(p[4 * c4 + 1], sl2, -l.y));
+            p[4 * c4 + 2] = ex2_approx(fmaf(p[4 * c4 + 2], sl2, -l.z));
+            p[4 * c4 + 3] = ex2_approx(fmaf(p[4 * c4 + 3], sl2, -l.w));
+          }
+        } else {
+          const int4* lo4 = reinterpret_cast<const int4*>(qi.lo + 64 * hf);
+          const int4* hi4 = reinterpret_cast<const int4*>(qi.hi + 64 * hf);
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 l = l4[c4];
+            const int4 lo = lo4[c4], hi = hi4[c4];
+            p[4 * c4 + 0] = (key >= lo.x && key <= hi.x) ? ex2_approx(fmaf(p[4 * c4 + 0], sl2, -l.x)) : 0.f;
+            p[4 * c4 + 1] = (key >= lo.y && key <= hi.y) ? ex2_approx(fmaf(p[4 * c4 + 1], sl2, -l.y)) : 0.f;
+            p[4 * c4 + 2] = (key >= lo.z && key <= hi.z) ? ex2_approx(fmaf(p[4 * c4 + 2], sl2, -l.z)) : 0.f;
+            p[4 * c4 + 3] = (key >= lo.w && key <= hi.w) ? ex2_approx(fmaf(p[4 * c4 + 3], sl2, -l.w)) : 0.f;
+          }
+        }
+        {  // P^T -> TMEM (bf16 pairs over this half's S^T columns)
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
+          tmem_st32(tmem + lb + 64 * hf, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_addr(c.p_full));
+        // dS^T = P^T (dP^T - Delta) -> TMEM over this half's dP^T columns (already read)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t dp[32], pk[16];
+          tmem_ld32(tmem + lb + 128 + 64 * hf + 32 * cc, dp);
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 d = d4[cc * 8 + e4];
+            const int c0 = cc * 32 + 4 * e4;
+            pk[2 * e4] = pack_bf16(p[c0] * (__uint_as_float(dp[4 * e4]) - d.x),
+                                   p[c0 + 1] * (__uint_as_float(dp[4 * e4 + 1]) - d.y));
+            pk[2 * e4 + 1] = pack_bf16(p[c0 + 2] * (__uint_as_float(dp[4 * e4 + 2]) - d.z),
+                                       p[c0 + 3] * (__uint_as_float(dp[4 * e4 + 3]) - d.w));
+          }
+          tmem_st16(tmem + lb + 128 + 64 * hf + 16 * cc, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_addr(c.ds_full));
+      }
+      if (!ok) break;
+      if (!wait_warp(bar_addr(c.done), ii & 1)) {
         fail(&s_abort);
         ok = false;
         break;
       }
-      tc_fence_after();
-      const QInfo& qi = qinfo[st];
-      const float4* l4 = reinterpret_cast<const float4*>(qi.lse2 + 64 * hf);
-      const float4* d4 = reinterpret_cast<const float4*>(qi.dl + 64 * hf);
-      float p[64];
-      tmem_ld32(tmem + lb + 64 * hf, reinterpret_cast<uint32_t*>(p));
-      tmem_ld32(tmem + lb + 64 * hf + 32, reinterpret_cast<uint32_t*>(p + 32));
-      if (key >= qi.max_lo && key <= qi.min_hi) {  // every query of the step sees this key
-#pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 l = l4[c4];
-          p[4 * c4 + 0] = ex2_approx(fmaf(p[4 * c4 + 0], sl2, -l.x));
-          p[4 * c4 + 1] = ex2_approx(fmaf(p[4 * c4 + 1], sl2, -l.y));
-          p[4 * c4 + 2] = ex2_approx(fmaf(p[4 * c4 + 2], sl2, -l.z));
-          p[4 * c4 + 3] = ex2_approx(fmaf(p[4 * c4 + 3], sl2, -l.w));
-        }
-      } else {
-        const int4* lo4 = reinterpret_cast<const int4*>(qi.lo + 64 * hf);
-        const int4* hi4 = reinterpret_cast<const int4*>(qi.hi + 64 * hf);
-#pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 l = l4[c4];
-          const int4 lo = lo4[c4], hi = hi4[c4];
-          p[4 * c4 + 0] = (key >= lo.x && key <= hi.x) ? ex2_approx(fmaf(p[4 * c4 + 0], sl2, -l.x)) : 0.f;
-          p[4 * c4 + 1] = (key >= lo.y && key <= hi.y) ? ex2_approx(fmaf(p[4 * c4 + 1], sl2, -l.y)) : 0.f;
-          p[4 * c4 + 2] = (key >= lo.z && key <= hi.z) ? ex2_approx(fmaf(p[4 * c4 + 2], sl2, -l.z)) : 0.f;
-          p[4 * c4 + 3] = (key >= lo.w && key <= hi.w) ? ex2_approx(fmaf(p[4 * c4 + 3], sl2, -l.w)) : 0.f;
-        }
-      }
-      {  // P^T -> TMEM (bf16 pairs over this half's S^T columns)
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
-        tmem_st32(tmem + lb + 64 * hf, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar_addr(bars.p_full));
-      // dS^T = P^T (dP^T - Delta) -> TMEM over this half's dP^T columns (already read)
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t dp[32], pk[16];
-        tmem_ld32(tmem + lb + 128 + 64 * hf + 32 * cc, dp);
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 d = d4[cc * 8 + e4];
-          const int c0 = cc * 32 + 4 * e4;
-          pk[2 * e4] = pack_bf16(p[c0] * (__uint_as_float(dp[4 * e4]) - d.x),
-                                 p[c0 + 1] * (__uint_as_float(dp[4 * e4 + 1]) - d.y));
-          pk[2 * e4 + 1] = pack_bf16(p[c0 + 2] * (__uint_as_float(dp[4 * e4 + 2]) - d.z),
-                                     p[c0 + 3] * (__uint_as_float(dp[4 * e4 + 3]) - d.w));
-        }
-        tmem_st16(tmem + lb + 128 + 64 * hf + 16 * cc, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar_addr(bars.ds_full));
-    }
-    if (ok && !wait_warp(bar_addr(bars.done), 0)) {
-      fail(&s_abort);
-      ok = false;
-    }
-    if (ok) {
+      ++ii;
       tc_fence_after();
       const bool in = key < a.T;
-      float* pk_ = a.dk + ((int64_t)key * a.H + h) * D;
-      float* pv_ = a.dv + ((int64_t)key * a.H + h) * D;
+      float* pk_ = a.dk + ((int64_t)key * a.H + itm.h) * D;
+      float* pv_ = a.dv + ((int64_t)key * a.H + itm.h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = hf * (D / 2) + c * 32;  // this half's dK / dV columns
-        uint32_t g[32], u[32];
-        tmem_ld32(tmem + lb + 256 + col, g);
-        tmem_ld32(tmem + lb + 256 + D + col, u);
+      for (int cq = 0; cq < D / 64; ++cq) {
+        const int col = hf * (D / 2) + cq * 32;  // this half's dK / dV columns
+        uint32_t gk[32], gv[32];
+        tmem_ld32(tmem + lb + 256 + col, gk);
+        tmem_ld32(tmem + lb + 256 + D + col, gv);
         if (in) {
           float4* dk4 = reinterpret_cast<float4*>(pk_ + col);
           float4* dv4 = reinterpret_cast<float4*>(pv_ + col);
@@ -632,19 +731,20 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           }
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            xk[q].x += __uint_as_float(g[4 * q + 0]) * a.scale;
-            xk[q].y += __uint_as_float(g[4 * q + 1]) * a.scale;
-            xk[q].z += __uint_as_float(g[4 * q + 2]) * a.scale;
-            xk[q].w += __uint_as_float(g[4 * q + 3]) * a.scale;
-            xv[q].x += __uint_as_float(u[4 * q + 0]);
-            xv[q].y += __uint_as_float(u[4 * q + 1]);
-            xv[q].z += __uint_as_float(u[4 * q + 2]);
-            xv[q].w += __uint_as_float(u[4 * q + 3]);
+            xk[q].x += __uint_as_float(gk[4 * q + 0]) * a.scale;
+            xk[q].y += __uint_as_float(gk[4 * q + 1]) * a.scale;
+            xk[q].z += __uint_as_float(gk[4 * q + 2]) * a.scale;
+            xk[q].w += __uint_as_float(gk[4 * q + 3]) * a.scale;
+            xv[q].x += __uint_as_float(gv[4 * q + 0]);
+            xv[q].y += __uint_as_float(gv[4 * q + 1]);
+            xv[q].z += __uint_as_float(gv[4 * q + 2]);
+            xv[q].w += __uint_as_float(gv[4 * q + 3]);
             dk4[q] = xk[q];
             dv4[q] = xv[q];
           }
         }
       }
+      tc_fence_before();
     }
   }
   tc_fence_before();
@@ -664,18 +764,19 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
   if ((st = tma::make_thd_map(&mdo, dout, a.s_local, a.H, D, 128)) != CP_OK) return st;
   if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128)) != CP_OK) return st;
   if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128)) != CP_OK) return st;
-  const int dq_smem = DqLayout<D>::BYTES + 1024;
-  const int kv_smem = KvLayout<D>::BYTES + 1024;
+  const int dq_smem = DqLayout<D>::BYTES + (int)sizeof(DqCtl);
+  const int kv_smem = KvLayout<D>::BYTES + (int)sizeof(KvCtl);
   if (cudaFuncSetAttribute(attn_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem) !=
           cudaSuccess ||
       cudaFuncSetAttribute(attn_dkdv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kv_smem) != cudaSuccess)
     return CP_ERR_CUDA;
-  dim3 qgrid((unsigned)((a.s_local + 127) / 128), (unsigned)a.H);
-  attn_dq_tc<D><<<qgrid, kThr, dq_smem, s>>>(mq, mdo, mk, mv, a);
+  const int sms = sm_count();
+  const int64_t q_items = n_tiles_of(a.s_local) * (int64_t)a.H;
+  attn_dq_tc<D><<<(int)(q_items < sms ? q_items : sms), kThr, dq_smem, s>>>(mq, mdo, mk, mv, a);
   if ((st = cpthd_host::launch_status()) != CP_OK) return st;
-  dim3 kgrid((unsigned)((a.T + 127) / 128), (unsigned)a.H);
-  attn_dkdv_tc<D><<<kgrid, kThr, kv_smem, s>>>(mq, mdo, mk, mv, a);
+  const int64_t k_items = n_tiles_of(a.T) * (int64_t)a.H;
+  attn_dkdv_tc<D><<<(int)(k_items < sms ? k_items : sms), kThr, kv_smem, s>>>(mq, mdo, mk, mv, a);
   return cpthd_host::launch_status();
 }
 
