@@ -10,26 +10,25 @@
 //
 // Persistent kernel: one CTA per SM walks a static list of work items
 // (128-row query tile, head), heaviest tiles first, item k going to CTA
-// k % gridDim.x.  Within a CTA the pipeline never drains between items: all
-// barrier phases follow global counters and Q is double buffered in TMEM
-// (the softmax warps copy the next item's Q there during the current item's
-// first block), so the next item's loads and S products overlap the current
-// item's last blocks and its epilogue.  10 warps:
+// k % gridDim.x.  The pipeline never drains between items: all barrier phases
+// follow global counters, Q and the O accumulator are double buffered, and an
+// item's epilogue is deferred until the next item's first block has been
+// handed to the tensor core, so it overlaps tensor-core work.  10 warps:
 //   warps 0-7  softmax: TMEM lane r = query row r, shared by warps r/32 and
 //              r/32+4 which take one half of the key columns each.  Loads S
 //              from TMEM, masks by the row's key range, online softmax in the
 //              log2 domain (the row max is exchanged between the two warps
 //              through shared memory), rescales O only when the max grows by
 //              more than 2^8, writes P (bf16 pairs) back into TMEM over S, and
-//              finally normalises O and stores O / LSE.
-//   warp 8     TMA producer: Q per item into a landing buffer, then K and V
-//              128-key tiles into a 3-stage ring.
+//              normalises O and stores O / LSE.
+//   warp 8     TMA producer: Q per item into one of two buffers, K tiles into
+//              a 3-stage ring released as soon as S is done, V tiles into a
+//              2-stage ring released after P V; K runs one block ahead of V.
 //   warp 9     TMEM allocator and single-thread MMA issuer:
-//              S[g%2] = Q K_g^T (M=128, N=128, K=D; A = Q from TMEM, B = K
-//              K-major in shared memory) and O += P_g V_g (M=128, N=D, K=128;
-//              A = P from TMEM, B = V as an MN-major shared operand).  TMEM:
-//              S0 cols [0,128), S1 [128,256), O [256,256+D), Q0 / Q1 (bf16
-//              pairs) at 256+D and 256+3D/2.
+//              S[g%2] = Q K_g^T (M=128, N=128, K=D, both operands K-major in
+//              shared memory) and O[item%2] += P_g V_g (M=128, N=D, K=128; A =
+//              P from TMEM, B = V as an MN-major shared operand).  TMEM: S0
+//              cols [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 // The MMA of S_{g+1} overlaps the softmax of S_g; P_g goes to the other S
 // buffer than P_{g-1}, and the softmax waits for P V_{g-1} only when it has to
 // rescale O, so consecutive P V products are issued back to back.
@@ -58,25 +57,25 @@ constexpr int TBN = 128;           // keys per block
 constexpr int kThreadsTc = 320;    // 10 warps
 constexpr int kSoftmax = 256;      // threads of the softmax warps 0-7
 constexpr int kProdWarp = 8, kMmaWarp = 9;
-constexpr int kStages = 3;         // K/V ring depth
+constexpr int kKStages = 3;        // K ring depth (released after S)
+constexpr int kVStages = 2;        // V ring depth (released after P V)
 constexpr int kBoxBytes = 128 * 128;  // one 128-row x 128-byte TMA box
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr float kLn2f = 0.6931471805599453f;
-constexpr uint32_t kOCol = 256;  // O accumulator: columns [256, 256 + D)
-// Q of item ii as bf16 pairs: TMEM columns [q_col(ii % 2), + D/2)
-template <int D>
-__host__ __device__ constexpr uint32_t q_col(int b) { return 256 + D + b * (D / 2); }
 
 template <int D>
 struct Layout {
   static constexpr int BOXES = D / 64;            // 64-element boxes along D
   static constexpr int TILE = BOXES * kBoxBytes;  // one Q / K / V tile
-  static constexpr int Q = 0;                     // Q landing buffer
-  static constexpr int K = Q + TILE;
-  static constexpr int V = K + kStages * TILE;
-  static constexpr int BYTES = V + kStages * TILE;
+  static constexpr int Q = 0;                     // two Q buffers
+  static constexpr int K = Q + 2 * TILE;
+  static constexpr int V = K + kKStages * TILE;
+  static constexpr int BYTES = V + kVStages * TILE;
 };
+
+template <int D>
+__host__ __device__ constexpr uint32_t o_col(int b) { return 256 + b * D; }
 
 struct TcArgs {
   bf16* o;
@@ -88,18 +87,23 @@ struct TcArgs {
 };
 
 struct Bars {
-  uint64_t q_full;     // Q of the next item landed in shared memory
-  uint64_t q_sfree;    // ... and was copied out into TMEM (buffer reusable)
-  uint64_t q_tmem[2];  // Q of item ii is in TMEM buffer ii % 2
-  uint64_t k_full[kStages];
-  uint64_t v_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t q_full[2];
+  uint64_t q_free[2];  // all S products of the item using Q buffer b are done
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
   uint64_t s_full[2];
-  uint64_t p_full[2];  // P_g ready: p_full[g % 2] (two barriers so the softmax can
-                       // never complete a phase the MMA thread has not waited for)
-  uint64_t o_ready[kStages];  // P V_g commits to o_ready[g % kStages]
+  uint64_t p_full[2];   // P_g ready: p_full[g % 2]
+  uint64_t o_ready[2];  // P V_g done: o_ready[g % 2]
   uint64_t mma_done;
 };
+// Why two alternating barriers suffice for s_full / p_full / o_ready: the MMA
+// thread issues S_g after P V_{g-2}, so when the softmax holds S_g every
+// P V up to g-2 is complete, and P V_{g+1} cannot be issued before the
+// softmax has produced P_{g+1}.  A parity wait on o_ready[(g-1) % 2] (or, for
+// a deferred epilogue at block L+1, on o_ready[L % 2]) therefore always sees
+// exactly the phase it is waiting for.
 
 // Barriers and small per-CTA state, placed right after the tiles in the
 // dynamic shared memory (the kernel has no static shared memory, so the
@@ -149,6 +153,9 @@ struct Iter {  // flattened walk over an item's key-block intervals
   }
 };
 
+// Register budget: the register file is split over the SM's four
+// sub-partitions (16K each) and 10 warps put 3 warps on two of them, so a
+// thread gets at most 168 registers.
 template <int D>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -172,20 +179,21 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   auto bar = [](uint64_t& b) { return smem_u32(&b); };
   if (threadIdx.x == 0) {
     ctl.abort = 0;
-    mbar_init(bar(bars.q_full), 1);
-    mbar_init(bar(bars.q_sfree), kSoftmax);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(bars.q_tmem[b]), kSoftmax);
+      mbar_init(bar(bars.q_full[b]), 1);
+      mbar_init(bar(bars.q_free[b]), 1);
       mbar_init(bar(bars.s_full[b]), 1);
+      mbar_init(bar(bars.p_full[b]), kSoftmax);
+      mbar_init(bar(bars.o_ready[b]), 1);
     }
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(bars.k_full[s]), 1);
-      mbar_init(bar(bars.v_full[s]), 1);
-      mbar_init(bar(bars.kv_empty[s]), 1);
-      mbar_init(bar(bars.o_ready[s]), 1);
+      mbar_init(bar(bars.k_empty[s]), 1);
     }
-    mbar_init(bar(bars.p_full[0]), kSoftmax);
-    mbar_init(bar(bars.p_full[1]), kSoftmax);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(bar(bars.v_full[s]), 1);
+      mbar_init(bar(bars.v_empty[s]), 1);
+    }
     mbar_init(bar(bars.mma_done), 1);
     for (int w = 0; w < 4; ++w) {
       mbar_init(bar(ctl.pair[w][0]), 64);
@@ -208,82 +216,72 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      // Q of non-empty item qi into the landing buffer, once the softmax warps
-      // copied Q of item qi-1 out of it.  Q runs one item ahead of K/V: the
-      // softmax copies item qi+1's Q during item qi's first block.
-      auto load_q = [&](int qi, int k) -> bool {
-        if (!mbar_wait(bar(bars.q_sfree), (qi & 1) ^ 1, &s_abort, kWaitLimitNs)) return false;
-        Item it;
-        it.load(m, k, n_qt, a.H);
-        mbar_arrive_expect_tx(bar(bars.q_full), L::TILE);
+      int ii = 0, g = 0, v_issued = 0;
+      int pv_h = 0, pv_key = 0;  // V of block v_issued still to load (when v_issued < g)
+      bool ok = true;
+      auto load_v = [&]() -> bool {
+        const int vs = v_issued % kVStages;
+        if (!mbar_wait(bar(bars.v_empty[vs]), ((v_issued / kVStages) & 1) ^ 1, &s_abort,
+                       kWaitLimitNs))
+          return false;
+        mbar_arrive_expect_tx(bar(bars.v_full[vs]), L::TILE);
 #pragma unroll
         for (int b = 0; b < L::BOXES; ++b)
-          tma_load_3d(sb + L::Q + b * kBoxBytes, &tm_q, bar(bars.q_full), b * 64, it.h, it.t0);
+          tma_load_3d(sb + L::V + vs * L::TILE + b * kBoxBytes, &tm_v, bar(bars.v_full[vs]),
+                      b * 64, pv_h, pv_key);
+        ++v_issued;
         return true;
       };
-      auto next_item = [&](int k) -> int {
-        for (k += gridDim.x; k < n_items; k += gridDim.x) {
-          Item nx;
-          nx.load(m, k, n_qt, a.H);
-          if (nx.nb > 0) return k;
-        }
-        return n_items;
-      };
-      int ii = 0, ld = 0, nq = 0;
-      bool ok = true;
-      int kf = next_item((int)blockIdx.x - (int)gridDim.x);
-      if (kf < n_items) {
-        if (load_q(0, kf)) {
-          nq = 1;
-        } else {
-          fail(&s_abort);
-          ok = false;
-        }
-      }
       for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
         Item it;
         it.load(m, k, n_qt, a.H);
         if (it.nb == 0) continue;
-        const int kn = next_item(k);
-        if (kn < n_items) {
-          if (!load_q(ii + 1, kn)) {
-            fail(&s_abort);
-            break;
-          }
-          nq = ii + 2;
+        const int qb = ii & 1;
+        if (!mbar_wait(bar(bars.q_free[qb]), ((ii >> 1) & 1) ^ 1, &s_abort, kWaitLimitNs)) {
+          fail(&s_abort);
+          break;
         }
+        mbar_arrive_expect_tx(bar(bars.q_full[qb]), L::TILE);
+#pragma unroll
+        for (int b = 0; b < L::BOXES; ++b)
+          tma_load_3d(sb + L::Q + qb * L::TILE + b * kBoxBytes, &tm_q, bar(bars.q_full[qb]),
+                      b * 64, it.h, it.t0);
         ++ii;
         Iter bi;
         bi.init(it.list + 1, it.n_iv);
-        for (int j = 0; j < it.nb; ++j, bi.next(), ++ld) {
-          const int st = ld % kStages;
-          if (!mbar_wait(bar(bars.kv_empty[st]), ((ld / kStages) & 1) ^ 1, &s_abort,
+        for (int j = 0; j < it.nb; ++j, bi.next()) {
+          const int ks = g % kKStages;
+          if (!mbar_wait(bar(bars.k_empty[ks]), ((g / kKStages) & 1) ^ 1, &s_abort,
                          kWaitLimitNs)) {
             fail(&s_abort);
             ok = false;
             break;
           }
           const int key0 = bi.b * TBN;
-          mbar_arrive_expect_tx(bar(bars.k_full[st]), L::TILE);
+          mbar_arrive_expect_tx(bar(bars.k_full[ks]), L::TILE);
 #pragma unroll
           for (int b = 0; b < L::BOXES; ++b)
-            tma_load_3d(sb + L::K + st * L::TILE + b * kBoxBytes, &tm_k, bar(bars.k_full[st]),
+            tma_load_3d(sb + L::K + ks * L::TILE + b * kBoxBytes, &tm_k, bar(bars.k_full[ks]),
                         b * 64, it.h, key0);
-          mbar_arrive_expect_tx(bar(bars.v_full[st]), L::TILE);
-#pragma unroll
-          for (int b = 0; b < L::BOXES; ++b)
-            tma_load_3d(sb + L::V + st * L::TILE + b * kBoxBytes, &tm_v, bar(bars.v_full[st]),
-                        b * 64, it.h, key0);
+          ++g;
+          if (v_issued < g - 1 && !load_v()) {  // V lags K by one block
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          pv_h = it.h;
+          pv_key = key0;
         }
       }
+      if (ok && v_issued < g && !load_v()) fail(&s_abort);
       // drain: every copy this CTA issued must land before shared memory goes away
       int never = 0;
-      if (nq > 0) mbar_wait(bar(bars.q_full), (nq - 1) & 1, &never, kWaitLimitNs);
-      for (int j = max(0, ld - kStages); j < ld; ++j) {
-        const int st = j % kStages;
-        mbar_wait(bar(bars.k_full[st]), (j / kStages) & 1, &never, kWaitLimitNs);
-        mbar_wait(bar(bars.v_full[st]), (j / kStages) & 1, &never, kWaitLimitNs);
-      }
+      for (int i = max(0, ii - 2); i < ii; ++i)
+        mbar_wait(bar(bars.q_full[i & 1]), (i >> 1) & 1, &never, kWaitLimitNs);
+      for (int j = max(0, g - kKStages); j < g; ++j)
+        mbar_wait(bar(bars.k_full[j % kKStages]), (j / kKStages) & 1, &never, kWaitLimitNs);
+      for (int j = max(0, v_issued - kVStages); j < v_issued; ++j)
+        mbar_wait(bar(bars.v_full[j % kVStages]), (j / kVStages) & 1, &never, kWaitLimitNs);
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
@@ -291,25 +289,25 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       constexpr uint32_t idS = idesc_bf16_f32(128, TBN, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
       // the previous block's P V is issued after the next block's S
-      int pv_g = -1, pv_st = 0;
+      int pv_g = -1, pv_ob = 0;
       bool pv_first = false;
       auto issue_pv = [&]() -> bool {
+        const int vs = pv_g % kVStages;
         if (!mbar_wait(bar(bars.p_full[pv_g & 1]), (pv_g >> 1) & 1, &s_abort, kWaitLimitNs) ||
-            !mbar_wait(bar(bars.v_full[pv_st]), (pv_g / kStages) & 1, &s_abort, kWaitLimitNs))
+            !mbar_wait(bar(bars.v_full[vs]), (pv_g / kVStages) & 1, &s_abort, kWaitLimitNs))
           return false;
         tc_fence_after();
         // A = P from TMEM: keys [0,64) over columns [0,32) and keys [64,128)
         // over [64,96) of S_g's buffer (written by the two column halves)
 #pragma unroll
         for (int kk = 0; kk < TBN / 16; ++kk) {
-          const uint64_t db =
-              sdesc_sw128(sb + L::V + pv_st * L::TILE + kk * 2048, kBoxBytes, 1024);
-          umma_bf16_ts(tmem + kOCol,
+          const uint64_t db = sdesc_sw128(sb + L::V + vs * L::TILE + kk * 2048, kBoxBytes, 1024);
+          umma_bf16_ts(tmem + o_col<D>(pv_ob),
                        tmem + (pv_g & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8, db, idO,
                        (!pv_first || kk > 0) ? 1u : 0u);
         }
-        umma_commit(bar(bars.kv_empty[pv_st]));
-        umma_commit(bar(bars.o_ready[pv_g % kStages]));
+        umma_commit(bar(bars.v_empty[vs]));
+        umma_commit(bar(bars.o_ready[pv_g & 1]));
         return true;
       };
       int ii = 0, g = 0;
@@ -319,37 +317,38 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         it.load(m, k, n_qt, a.H);
         if (it.nb == 0) continue;
         const int qb = ii & 1;
-        if (!mbar_wait(bar(bars.q_tmem[qb]), (ii >> 1) & 1, &s_abort, kWaitLimitNs)) {
+        if (!mbar_wait(bar(bars.q_full[qb]), (ii >> 1) & 1, &s_abort, kWaitLimitNs)) {
           fail(&s_abort);
           break;
         }
         ++ii;
         for (int j = 0; j < it.nb; ++j, ++g) {
-          const int st = g % kStages, buf = g & 1;
+          const int ks = g % kKStages, buf = g & 1;
           // S_g overwrites P_{g-2} (same TMEM columns); P V_{g-2} was issued
           // earlier by this thread and MMAs of one thread run in order
-          if (!mbar_wait(bar(bars.k_full[st]), (g / kStages) & 1, &s_abort, kWaitLimitNs)) {
+          if (!mbar_wait(bar(bars.k_full[ks]), (g / kKStages) & 1, &s_abort, kWaitLimitNs)) {
             fail(&s_abort);
             ok = false;
             break;
           }
           tc_fence_after();
-          // A = Q from TMEM buffer qb (bf16 pairs), B = K tile (K-major)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            umma_bf16_ts(tmem + buf * 128, tmem + q_col<D>(qb) + kk * 8,
-                         sdesc_sw128(sb + L::K + st * L::TILE + off, 16, 1024), idS,
-                         kk > 0 ? 1u : 0u);
+            umma_bf16(tmem + buf * 128, sdesc_sw128(sb + L::Q + qb * L::TILE + off, 16, 1024),
+                      sdesc_sw128(sb + L::K + ks * L::TILE + off, 16, 1024), idS,
+                      kk > 0 ? 1u : 0u);
           }
           umma_commit(bar(bars.s_full[buf]));
+          umma_commit(bar(bars.k_empty[ks]));
+          if (j == it.nb - 1) umma_commit(bar(bars.q_free[qb]));
           if (pv_g >= 0 && !issue_pv()) {
             fail(&s_abort);
             ok = false;
             break;
           }
           pv_g = g;
-          pv_st = st;
+          pv_ob = qb;
           pv_first = (j == 0);
         }
       }
@@ -378,37 +377,15 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     };
     // exchange u of the two warps of a pair: publish a value, wait for the
     // partner's (bounded, like every other wait), return the partner's value
-    auto exchange = [&](int u, float v, float* out) -> bool {
+    int u = 0;
+    auto exchange = [&](float v, float* out) -> bool {
       ctl.red[u & 1][hf][row] = v;
       mbar_arrive(bar(ctl.pair[warp & 3][u & 1]));
-      if (!wait_warp(bar(ctl.pair[warp & 3][u & 1]), (u >> 1) & 1)) return false;
-      *out = ctl.red[u & 1][hf ^ 1][row];
-      return true;
+      const bool w = wait_warp(bar(ctl.pair[warp & 3][u & 1]), (u >> 1) & 1);
+      if (w) *out = ctl.red[u & 1][hf ^ 1][row];
+      ++u;
+      return w;
     };
-    // Q of non-empty item qi (landed in shared memory) -> TMEM buffer qi % 2,
-    // each half row by one of the two warps of the pair
-    auto copy_q = [&](int qi) -> bool {
-      if (!wait_warp(bar(bars.q_full), qi & 1)) return false;
-      constexpr int kChunks = D / 16;  // 16-byte chunks per half row
-      uint32_t qv[4 * kChunks];
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const int e0 = hf * (D / 2) + c * 8;  // first element of the chunk
-        const int box = e0 >> 6, chunk = (e0 & 63) >> 3;
-        const uint4 v = *reinterpret_cast<const uint4*>(
-            smem_raw + L::Q + box * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4));
-        qv[4 * c] = v.x; qv[4 * c + 1] = v.y; qv[4 * c + 2] = v.z; qv[4 * c + 3] = v.w;
-      }
-      const uint32_t col = q_col<D>(qi & 1) + hf * (D / 4);
-      if constexpr (D == 128) tmem_st32(tmem + lane_base + col, qv);
-      else tmem_st16(tmem + lane_base + col, qv);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(bars.q_tmem[qi & 1]));
-      mbar_arrive(bar(bars.q_sfree));
-      return true;
-    };
-    // next non-empty item after k (n_items if none)
     auto next_item = [&](int k) -> int {
       for (k += gridDim.x; k < n_items; k += gridDim.x) {
         Item nx;
@@ -417,19 +394,62 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       }
       return n_items;
     };
-    int ii = 0, g = 0, u = 0;
+    // the finished item whose O still has to be normalised and stored
+    struct Pending {
+      int t, h, ob, last;
+      float m, l;
+    } pend{0, 0, 0, -1, 0.f, 0.f};
+    auto epilogue = [&]() -> bool {
+      if (!wait_warp(bar(bars.o_ready[pend.last & 1]), (pend.last >> 1) & 1)) return false;
+      float l_other = 0.f;
+      if (!exchange(pend.l, &l_other)) return false;
+      const float l_tot = pend.l + l_other;
+      const bool in = pend.t < a.s_local;
+      tc_fence_after();
+      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = hf * (D / 2) + c * 32;
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + o_col<D>(pend.ob) + col, o);
+        if (in) {
+          uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)pend.t * a.H + pend.h) * D + col);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(o[q * 8 + 0]) * inv, __uint_as_float(o[q * 8 + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(o[q * 8 + 2]) * inv, __uint_as_float(o[q * 8 + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(o[q * 8 + 4]) * inv, __uint_as_float(o[q * 8 + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(o[q * 8 + 6]) * inv, __uint_as_float(o[q * 8 + 7]) * inv);
+            dst[q] = v;
+          }
+        }
+      }
+      if (in && hf == 0)
+        a.lse[(int64_t)pend.h * a.s_local + pend.t] =
+            l_tot > 0.f ? (pend.m * sl2 + log2f(l_tot)) * kLn2f : -INFINITY;
+      pend.last = -1;
+      return true;
+    };
+
+    int ii = 0, g = 0;
     bool ok = true;
-    if (next_item((int)blockIdx.x - (int)gridDim.x) < n_items && !copy_q(0)) {
-      fail(&s_abort);
-      ok = false;
+    // row tables of the next non-empty item are fetched one item ahead
+    int k_pre = next_item((int)blockIdx.x - (int)gridDim.x);
+    int lo_pre = 0, hi_pre = -1;
+    if (k_pre < n_items) {
+      Item f;
+      f.load(m, k_pre, n_qt, a.H);
+      const int t = f.t0 + row;
+      lo_pre = t < a.s_local ? m.row_lo[t] : 0;
+      hi_pre = t < a.s_local ? m.row_hi[t] : -1;
     }
     for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
       Item itm;
       itm.load(m, k, n_qt, a.H);
       const int t = itm.t0 + row;
-      const bool in = t < a.s_local;
       if (itm.nb == 0) {  // no real query row in this tile: O = 0, LSE = -inf
-        if (in) {
+        if (t < a.s_local) {
           uint4* dst =
               reinterpret_cast<uint4*>(a.o + ((int64_t)t * a.H + itm.h) * D + hf * (D / 2));
 #pragma unroll
@@ -438,12 +458,21 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         continue;
       }
-      const int lo = in ? m.row_lo[t] : 0;
-      const int hi = in ? m.row_hi[t] : -1;
+      const int lo = lo_pre, hi = hi_pre;  // k == k_pre here
+      k_pre = next_item(k);
+      if (k_pre < n_items) {
+        Item f;
+        f.load(m, k_pre, n_qt, a.H);
+        const int tn = f.t0 + row;
+        lo_pre = tn < a.s_local ? m.row_lo[tn] : 0;
+        hi_pre = tn < a.s_local ? m.row_hi[tn] : -1;
+      }
+      const int ob = ii & 1;
+      ++ii;
       float m_run = -INFINITY, l_run = 0.f;
       Iter bi;
       bi.init(itm.list + 1, itm.n_iv);
-      for (int j = 0; j < itm.nb; ++j, bi.next(), ++g, ++u) {
+      for (int j = 0; j < itm.nb; ++j, bi.next(), ++g) {
         const int buf = g & 1;
         if (!wait_warp(bar(bars.s_full[buf]), (g >> 1) & 1)) {
           fail(&s_abort);
@@ -455,13 +484,6 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tmem_ld32(tmem + lane_base + buf * 128 + 64 * hf, reinterpret_cast<uint32_t*>(s));
         tmem_ld32(tmem + lane_base + buf * 128 + 64 * hf + 32,
                   reinterpret_cast<uint32_t*>(s + 32));
-        // the next item's Q goes into the TMEM buffer the previous item used;
-        // all of that item's S products are done (their s_full was waited for)
-        if (j == 0 && next_item(k) < n_items && !copy_q(ii + 1)) {
-          fail(&s_abort);
-          ok = false;
-          break;
-        }
 
         const int k0 = bi.b * TBN + 64 * hf;  // key of this thread's first column
         if (!(lo <= k0 && hi >= k0 + 63)) {
@@ -479,7 +501,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                          fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         float mx_other;
-        if (!exchange(u, mx, &mx_other)) {
+        if (!exchange(mx, &mx_other)) {
           fail(&s_abort);
           ok = false;
           break;
@@ -489,10 +511,12 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         // block's max exceeds it by more than 8 in log2 units; otherwise the
         // stale max stays in use for this block's P, which then stays below
         // 2^8 -- P and l always use the same reference, so O/l is unchanged.
+        // While m_run is still -inf every P so far was exactly 0, so O = 0 and
+        // l = 0 need no rescale.
         float alpha = 1.f;
         if (m_run == -INFINITY || (mx - m_run) * sl2 > 8.f) {
           const float m_new = fmaxf(m_run, mx);
-          alpha = m_run == -INFINITY ? 0.f : ex2_approx((m_run - m_new) * sl2);
+          if (m_run != -INFINITY) alpha = ex2_approx((m_run - m_new) * sl2);
           m_run = m_new;
         }
         const float mref = m_run == -INFINITY ? 0.f : m_run * sl2;
@@ -506,16 +530,11 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                           ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         l_run = l_run * alpha + sum;
 
-        // O only has to be complete (P V_{g-1} done) when it is rescaled.  P_g
-        // goes to the other TMEM buffer than P_{g-1}, so without a rescale
-        // the softmax does not wait for the tensor core.  P V_g commits to
-        // o_ready[g % kStages]; when the softmax holds S_g, K_g has been
-        // loaded into the stage that P V_{g-kStages} released, so at most
-        // kStages-1 products are in flight and the parity wait on
-        // o_ready[(g-1) % kStages] is unambiguous.
+        // O only has to be complete (P V_{g-1} done) when it is rescaled; the
+        // first block of an item starts a fresh accumulator.
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           const int pv = g - 1;
-          if (!wait_warp(bar(bars.o_ready[pv % kStages]), (pv / kStages) & 1)) {
+          if (!wait_warp(bar(bars.o_ready[pv & 1]), (pv >> 1) & 1)) {
             fail(&s_abort);
             ok = false;
             break;
@@ -523,7 +542,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
-            const uint32_t col = kOCol + hf * (D / 2) + c * 32;
+            const uint32_t col = o_col<D>(ob) + hf * (D / 2) + c * 32;
             uint32_t o[32];
             tmem_ld32(tmem + lane_base + col, o);
 #pragma unroll
@@ -541,48 +560,23 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(bars.p_full[buf]));
-      }
-      if (!ok) break;
-      // epilogue of the item: wait for its last P V, combine the halves' sums
-      const int last = g - 1;
-      if (!wait_warp(bar(bars.o_ready[last % kStages]), (last / kStages) & 1)) {
-        fail(&s_abort);
-        ok = false;
-        break;
-      }
-      float l_other = 0.f;
-      if (!exchange(u, l_run, &l_other)) {
-        fail(&s_abort);
-        ok = false;
-        break;
-      }
-      ++u;
-      const float l_tot = l_run + l_other;
-      tc_fence_after();
-      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = hf * (D / 2) + c * 32;
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_base + kOCol + col, o);
-        if (in) {
-          uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)t * a.H + itm.h) * D + col);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(o[q * 8 + 0]) * inv, __uint_as_float(o[q * 8 + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(o[q * 8 + 2]) * inv, __uint_as_float(o[q * 8 + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(o[q * 8 + 4]) * inv, __uint_as_float(o[q * 8 + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(o[q * 8 + 6]) * inv, __uint_as_float(o[q * 8 + 7]) * inv);
-            dst[q] = v;
-          }
+        // the previous item's epilogue runs once this item's first block is
+        // with the tensor core
+        if (j == 0 && pend.last >= 0 && !epilogue()) {
+          fail(&s_abort);
+          ok = false;
+          break;
         }
       }
-      if (in && hf == 0)
-        a.lse[(int64_t)itm.h * a.s_local + t] =
-            l_tot > 0.f ? (m_run * sl2 + log2f(l_tot)) * kLn2f : -INFINITY;
-      ++ii;
+      if (!ok) break;
+      pend.t = t;
+      pend.h = itm.h;
+      pend.ob = ob;
+      pend.last = g - 1;
+      pend.m = m_run;
+      pend.l = l_run;
     }
+    if (ok && pend.last >= 0 && !epilogue()) fail(&s_abort);
   }
 
   tc_fence_before();
