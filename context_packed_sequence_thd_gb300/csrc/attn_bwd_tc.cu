@@ -12,24 +12,28 @@
 //
 // attn_dq_tc   items (128-query tile, head), iterating the key blocks the
 //              tile attends.  S = Q K^T and dP = dO V^T into TMEM (M=128
-//              queries, N=128 keys); the compute warps form dS and write it
-//              back into TMEM as bf16 over S; dQ += dS K with A = dS from TMEM,
-//              B = K as an MN-major operand.
+//              queries, N=128 keys); the compute warps form dS into one of two
+//              separate TMEM buffers (bf16); dQ += dS K with A = dS from TMEM,
+//              B = K as an MN-major operand.  K tiles sit in a 3-stage ring
+//              (released after dQ), V tiles in a 2-stage ring (released after
+//              dP).
 // attn_dkdv_tc items (128-key block, head), iterating the rank's query tiles
 //              that attend the block (precomputed block lists).  S^T = K Q^T
 //              and dP^T = V dO^T into TMEM (M=128 keys, N=128 queries); the
 //              compute warps form P^T and dS^T in TMEM over S^T and dP^T;
 //              dV += P^T dO and dK += dS^T Q (A from TMEM, B = dO / Q as
 //              MN-major operands).  Each item's partial dK/dV are added into
-//              the caller's fp32 accumulators by the item's only owner.
+//              the caller's fp32 accumulators by the item's only owner, with
+//              fire-and-forget vector reductions (one add per element per
+//              launch, so the sums are still bitwise reproducible).
 // Warp roles: warps 0-7 compute (warp w serves TMEM lanes 32*(w%4).. and the
 // column half w/4 of every row, so two warps share each row's elementwise
 // work), warp 8 TMA producer, warp 9 TMEM allocator + single-thread MMA
-// issuer.  A compute thread writes P / dS back only into TMEM columns it has
-// itself already read (the first half of its own column range), so the two
-// halves never race.  The next item's Q/dO (K/V) tiles are loaded as soon as
-// the current item's last S products retire, and the epilogue of an item
-// overlaps the next item's first products.  Every wait is bounded.
+// issuer.  The MMA thread interleaves consecutive steps (the next S product
+// is issued before the previous step's gradient product) so the tensor core
+// keeps working while the compute warps run the elementwise part.  A compute
+// thread writes P / dS back only into TMEM columns it has itself already read,
+// so the two column halves never race.  Every wait is bounded.
 #include <math.h>
 
 #include "common.cuh"
@@ -48,7 +52,6 @@ using bf16 = __nv_bfloat16;
 constexpr int kThr = 320;
 constexpr int kCompute = 256;  // threads of warps 0-7
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr int kStg = 2;
 constexpr int kBox = 128 * 128;  // one 128-row x 128-byte TMA box
 constexpr uint32_t kCols = 512;
 constexpr uint64_t kLimitNs = 4000000000ull;
@@ -128,24 +131,42 @@ int sm_count() {
 // ===========================================================================
 // dQ
 // ===========================================================================
+constexpr int kDqKStages = 3;  // K ring (released after dQ)
+constexpr int kDqVStages = 2;  // V ring (released after dP)
+
 template <int D>
 struct DqLayout {
   static constexpr int TILE = (D / 64) * kBox;
   static constexpr int Q = 0;
   static constexpr int DO = TILE;
   static constexpr int K = 2 * TILE;
-  static constexpr int V = K + kStg * TILE;
-  static constexpr int BYTES = V + kStg * TILE;
+  static constexpr int V = K + kDqKStages * TILE;
+  static constexpr int BYTES = V + kDqVStages * TILE;
 };
+
+// TMEM of attn_dq_tc: S [0,128), dP [128,256), dQ [256,256+D), and two dS
+// buffers (bf16 pairs, 64 columns each) after dQ.
+template <int D>
+__host__ __device__ constexpr uint32_t dq_ds_col(int b) { return 256 + D + 64 * b; }
 
 struct DqCtl {
   uint64_t qd_full, qd_free;  // Q/dO of the item landed / all its S, dP products done
-  uint64_t k_full[kStg], v_full[kStg], kv_empty[kStg];
-  uint64_t st_full, ds_full, done, mma_done;
+  uint64_t k_full[kDqKStages], k_empty[kDqKStages];
+  uint64_t v_full[kDqVStages], v_empty[kDqVStages];
+  uint64_t s_full, s_free, dp_full, ds_full, done, mma_done;
   uint32_t tmem;
   int abort;
 };
 
+// Per key block g the MMA thread issues S_g, then the previous block's
+// dQ_{g-1} (once dS_{g-1} is in TMEM), then dP_g.  S has its own release
+// barrier (s_free: the compute warps have read S_g into registers), so S_{g+1}
+// is computed while the compute warps are still forming dS_g, and dS goes to
+// one of two separate TMEM buffers so that dQ_{g-1} and S_{g+1} do not
+// conflict.  Every per-block barrier completes once per block; the order
+// "wait ds_full(g-1) before committing dp_full(g)" (and "wait s_free(g-1)
+// before committing s_full(g)") keeps each of them at most one phase ahead of
+// its waiter, so the parity waits never alias.
 template <int D>
 __global__ void __launch_bounds__(kThr, 1)
 attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -171,12 +192,17 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     c.abort = 0;
     mbar_init(bar_addr(c.qd_full), 1);
     mbar_init(bar_addr(c.qd_free), 1);
-    for (int s = 0; s < kStg; ++s) {
+    for (int s = 0; s < kDqKStages; ++s) {
       mbar_init(bar_addr(c.k_full[s]), 1);
-      mbar_init(bar_addr(c.v_full[s]), 1);
-      mbar_init(bar_addr(c.kv_empty[s]), 1);
+      mbar_init(bar_addr(c.k_empty[s]), 1);
     }
-    mbar_init(bar_addr(c.st_full), 1);
+    for (int s = 0; s < kDqVStages; ++s) {
+      mbar_init(bar_addr(c.v_full[s]), 1);
+      mbar_init(bar_addr(c.v_empty[s]), 1);
+    }
+    mbar_init(bar_addr(c.s_full), 1);
+    mbar_init(bar_addr(c.s_free), kCompute);
+    mbar_init(bar_addr(c.dp_full), 1);
     mbar_init(bar_addr(c.ds_full), kCompute);
     mbar_init(bar_addr(c.done), 1);
     mbar_init(bar_addr(c.mma_done), 1);
@@ -189,11 +215,11 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = c.tmem;  // S [0,128)  dP [128,256)  dQ [256,256+D)
+  const uint32_t tmem = c.tmem;
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
-      int ii = 0, ld = 0;
+      int ii = 0, gk = 0, gv = 0;
       bool ok = true;
       for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
         Item it;
@@ -214,39 +240,64 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         ++ii;
         Iter bi;
         bi.init(it.list + 1, it.n_iv);
-        for (int j = 0; j < it.nb; ++j, bi.next(), ++ld) {
-          const int st = ld % kStg;
-          if (!mbar_wait(bar_addr(c.kv_empty[st]), ((ld / kStg) & 1) ^ 1, &s_abort, kLimitNs)) {
+        for (int j = 0; j < it.nb; ++j, bi.next()) {
+          const int key0 = bi.b * 128;
+          const int ks = gk % kDqKStages;
+          if (!mbar_wait(bar_addr(c.k_empty[ks]), ((gk / kDqKStages) & 1) ^ 1, &s_abort,
+                         kLimitNs)) {
             fail(&s_abort);
             ok = false;
             break;
           }
-          const int key0 = bi.b * 128;
-          mbar_arrive_expect_tx(bar_addr(c.k_full[st]), L::TILE);
+          mbar_arrive_expect_tx(bar_addr(c.k_full[ks]), L::TILE);
 #pragma unroll
           for (int b = 0; b < BOXES; ++b)
-            tma_load_3d(sb + L::K + st * L::TILE + b * kBox, &tm_k, bar_addr(c.k_full[st]),
+            tma_load_3d(sb + L::K + ks * L::TILE + b * kBox, &tm_k, bar_addr(c.k_full[ks]),
                         b * 64, it.h, key0);
-          mbar_arrive_expect_tx(bar_addr(c.v_full[st]), L::TILE);
+          ++gk;
+          const int vs = gv % kDqVStages;
+          if (!mbar_wait(bar_addr(c.v_empty[vs]), ((gv / kDqVStages) & 1) ^ 1, &s_abort,
+                         kLimitNs)) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_addr(c.v_full[vs]), L::TILE);
 #pragma unroll
           for (int b = 0; b < BOXES; ++b)
-            tma_load_3d(sb + L::V + st * L::TILE + b * kBox, &tm_v, bar_addr(c.v_full[st]),
+            tma_load_3d(sb + L::V + vs * L::TILE + b * kBox, &tm_v, bar_addr(c.v_full[vs]),
                         b * 64, it.h, key0);
+          ++gv;
         }
       }
+      // drain: every copy this CTA issued must land before shared memory goes away
       int never = 0;
       if (ii > 0) mbar_wait(bar_addr(c.qd_full), (ii - 1) & 1, &never, kLimitNs);
-      for (int j = max(0, ld - kStg); j < ld; ++j) {
-        const int st = j % kStg;
-        mbar_wait(bar_addr(c.k_full[st]), (j / kStg) & 1, &never, kLimitNs);
-        mbar_wait(bar_addr(c.v_full[st]), (j / kStg) & 1, &never, kLimitNs);
-      }
+      for (int j = max(0, gk - kDqKStages); j < gk; ++j)
+        mbar_wait(bar_addr(c.k_full[j % kDqKStages]), (j / kDqKStages) & 1, &never, kLimitNs);
+      for (int j = max(0, gv - kDqVStages); j < gv; ++j)
+        mbar_wait(bar_addr(c.v_full[j % kDqVStages]), (j / kDqVStages) & 1, &never, kLimitNs);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
       int ii = 0, g = 0;
+      int pend = -1;  // block whose dQ product is still to be issued
+      bool pend_first = false;
+      // dQ += dS K : A = dS (bf16 pairs in TMEM), B = K tile as MN-major (N = d)
+      auto issue_dq = [&]() -> bool {
+        if (!mbar_wait(bar_addr(c.ds_full), pend & 1, &s_abort, kLimitNs)) return false;
+        tc_fence_after();
+        const int ks = pend % kDqKStages;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ts(tmem + 256, tmem + dq_ds_col<D>(pend & 1) + (kk >> 2) * 32 + (kk & 3) * 8,
+                       sdesc_sw128(sb + L::K + ks * L::TILE + kk * 2048, kBox, 1024), idQ,
+                       (!pend_first || kk > 0) ? 1u : 0u);
+        umma_commit(bar_addr(c.k_empty[ks]));
+        return true;
+      };
       bool ok = true;
       for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
         Item it;
@@ -258,9 +309,10 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         ++ii;
         for (int j = 0; j < it.nb; ++j, ++g) {
-          const int st = g % kStg;
-          if (!mbar_wait(bar_addr(c.k_full[st]), (g / kStg) & 1, &s_abort, kLimitNs) ||
-              !mbar_wait(bar_addr(c.v_full[st]), (g / kStg) & 1, &s_abort, kLimitNs)) {
+          const int ks = g % kDqKStages, vs = g % kDqVStages;
+          // S_g overwrites S_{g-1}: the compute warps must have read it
+          if (!mbar_wait(bar_addr(c.k_full[ks]), (g / kDqKStages) & 1, &s_abort, kLimitNs) ||
+              (g > 0 && !mbar_wait(bar_addr(c.s_free), (g - 1) & 1, &s_abort, kLimitNs))) {
             fail(&s_abort);
             ok = false;
             break;
@@ -270,27 +322,42 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = kmajor_off(kk);
             umma_bf16(tmem, sdesc_sw128(sb + L::Q + off, 16, 1024),
-                      sdesc_sw128(sb + L::K + st * L::TILE + off, 16, 1024), idS, kk > 0);
-            umma_bf16(tmem + 128, sdesc_sw128(sb + L::DO + off, 16, 1024),
-                      sdesc_sw128(sb + L::V + st * L::TILE + off, 16, 1024), idS, kk > 0);
+                      sdesc_sw128(sb + L::K + ks * L::TILE + off, 16, 1024), idS, kk > 0);
           }
-          umma_commit(bar_addr(c.st_full));
-          if (j == it.nb - 1) umma_commit(bar_addr(c.qd_free));
-          if (!mbar_wait(bar_addr(c.ds_full), g & 1, &s_abort, kLimitNs)) {
+          umma_commit(bar_addr(c.s_full));
+          // dQ of the previous block (waits for its dS; that also means the
+          // compute warps have read dP_{g-1}, which dP_g overwrites)
+          if (pend >= 0 && !issue_dq()) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(bar_addr(c.v_full[vs]), (g / kDqVStages) & 1, &s_abort, kLimitNs)) {
             fail(&s_abort);
             ok = false;
             break;
           }
           tc_fence_after();
-          // dQ += dS K : A = dS (bf16 in TMEM over S), B = K tile as MN-major (N = d)
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + 256, tmem + ts_col(kk),
-                         sdesc_sw128(sb + L::K + st * L::TILE + kk * 2048, kBox, 1024), idQ,
-                         (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar_addr(c.kv_empty[st]));
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = kmajor_off(kk);
+            umma_bf16(tmem + 128, sdesc_sw128(sb + L::DO + off, 16, 1024),
+                      sdesc_sw128(sb + L::V + vs * L::TILE + off, 16, 1024), idS, kk > 0);
+          }
+          umma_commit(bar_addr(c.dp_full));
+          umma_commit(bar_addr(c.v_empty[vs]));
+          if (j == it.nb - 1) umma_commit(bar_addr(c.qd_free));
+          pend = g;
+          pend_first = (j == 0);
         }
-        if (ok) umma_commit(bar_addr(c.done));
+        if (!ok) break;
+        // the item's last dQ product, then its epilogue may read dQ
+        if (!issue_dq()) {
+          fail(&s_abort);
+          break;
+        }
+        pend = -1;
+        umma_commit(bar_addr(c.done));
       }
       umma_commit(bar_addr(c.mma_done));
       int never = 0;
@@ -328,7 +395,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       Iter bi;
       bi.init(itm.list + 1, itm.n_iv);
       for (int j = 0; j < itm.nb; ++j, bi.next(), ++g) {
-        if (!wait_warp(bar_addr(c.st_full), g & 1)) {
+        if (!wait_warp(bar_addr(c.s_full), g & 1)) {
           fail(&s_abort);
           ok = false;
           break;
@@ -337,6 +404,8 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         float p[64];
         tmem_ld32(tmem + lb + 64 * hf, reinterpret_cast<uint32_t*>(p));
         tmem_ld32(tmem + lb + 64 * hf + 32, reinterpret_cast<uint32_t*>(p + 32));
+        tc_fence_before();
+        mbar_arrive(bar_addr(c.s_free));  // S_{g+1} may now overwrite S
         const int k0 = bi.b * 128 + 64 * hf;  // key of this thread's first column
         if (lo <= k0 && hi >= k0 + 63) {
 #pragma unroll
@@ -346,6 +415,13 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           for (int e = 0; e < 64; ++e)
             p[e] = (k0 + e >= lo && k0 + e <= hi) ? ex2_approx(fmaf(p[e], sl2, -lse2)) : 0.f;
         }
+        if (!wait_warp(bar_addr(c.dp_full), g & 1)) {
+          fail(&s_abort);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dsc = dq_ds_col<D>(g & 1) + 32 * hf;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t dp[32], pk[16];
@@ -354,7 +430,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           for (int e = 0; e < 16; ++e)
             pk[e] = pack_bf16(p[cc * 32 + 2 * e] * (__uint_as_float(dp[2 * e]) - dl),
                               p[cc * 32 + 2 * e + 1] * (__uint_as_float(dp[2 * e + 1]) - dl));
-          tmem_st16(tmem + lb + 64 * hf + 16 * cc, pk);  // dS over this half's S columns
+          tmem_st16(tmem + lb + dsc + 16 * cc, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -402,6 +478,8 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 // ===========================================================================
 // dK / dV
 // ===========================================================================
+constexpr int kStg = 2;  // Q/dO stages of attn_dkdv_tc
+
 template <int D>
 struct KvLayout {
   static constexpr int TILE = (D / 64) * kBox;
@@ -423,13 +501,20 @@ struct __align__(16) QInfo {  // per-query data of one 128-query step
 
 struct KvCtl {
   QInfo qinfo[kStg];
-  uint64_t kv_full, kv_free;  // K/V of the item landed / all its S^T, dP^T products done
+  uint64_t k_full, k_free, v_full, v_free;  // single K and V tiles of the item
   uint64_t q_full[kStg], qi_full[kStg], q_empty[kStg];
-  uint64_t st_full, p_full, ds_full, done, mma_done;
+  uint64_t s_full, dp_full, p_full, ds_full, done, mma_done;
   uint32_t tmem;
   int abort;
 };
 
+// Per query step i the MMA thread issues S^T_i, then the previous step's
+// dK_{i-1} (once dS^T_{i-1} is in TMEM), then dP^T_i, then dV_i (once P^T_i
+// is in TMEM).  While the compute warps turn S^T_i into P^T_i the tensor core
+// runs dK_{i-1} and dP^T_i; while they form dS^T_i it runs dV_i and S^T_{i+1}.
+// dP^T_i is committed only after the MMA thread has consumed ds_full(i-1) and
+// S^T_{i+1} only after it has consumed p_full(i), so no per-step barrier gets
+// two phases ahead of its waiter.
 template <int D>
 __global__ void __launch_bounds__(kThr, 1)
 attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -453,14 +538,17 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 
   if (threadIdx.x == 0) {
     c.abort = 0;
-    mbar_init(bar_addr(c.kv_full), 1);
-    mbar_init(bar_addr(c.kv_free), 1);
+    mbar_init(bar_addr(c.k_full), 1);
+    mbar_init(bar_addr(c.k_free), 1);
+    mbar_init(bar_addr(c.v_full), 1);
+    mbar_init(bar_addr(c.v_free), 1);
     for (int s = 0; s < kStg; ++s) {
       mbar_init(bar_addr(c.q_full[s]), 1);
       mbar_init(bar_addr(c.qi_full[s]), 32);
       mbar_init(bar_addr(c.q_empty[s]), 1);
     }
-    mbar_init(bar_addr(c.st_full), 1);
+    mbar_init(bar_addr(c.s_full), 1);
+    mbar_init(bar_addr(c.dp_full), 1);
     mbar_init(bar_addr(c.p_full), kCompute);
     mbar_init(bar_addr(c.ds_full), kCompute);
     mbar_init(bar_addr(c.done), 1);
@@ -478,34 +566,47 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 
   if (warp == kProducerWarp) {
     // all 32 lanes: lane 0 issues TMA, every lane loads per-query data
-    int ii = 0, gs = 0;
+    int ii = 0, gs = 0, nk = 0, nv = 0;  // items, Q/dO steps, K and V tiles issued
     bool ok = true;
+    auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
+      return __all_sync(0xffffffffu, w);
+    };
     for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
       Item it;
       it.load(m.klists, k, a.H, n_kb, false);
       if (it.nb == 0) continue;
-      // single K/V buffer: free once the previous item's S^T, dP^T retired
-      const bool wf = mbar_wait(bar_addr(c.kv_free), (ii & 1) ^ 1, &s_abort, kLimitNs);
-      if (!__all_sync(0xffffffffu, wf)) {
+      const int j0 = it.tile * 128;
+      // single K (V) tile: free once the previous item's last S^T (dP^T) retired
+      if (!wait_all(bar_addr(c.k_free), (ii & 1) ^ 1)) {
         if (lane == 0) fail(&s_abort);
         break;
       }
-      ++ii;
-      const int j0 = it.tile * 128;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar_addr(c.kv_full), 2 * L::TILE);
+        mbar_arrive_expect_tx(bar_addr(c.k_full), L::TILE);
 #pragma unroll
-        for (int b = 0; b < BOXES; ++b) {
-          tma_load_3d(sb + L::K + b * kBox, &tm_k, bar_addr(c.kv_full), b * 64, it.h, j0);
-          tma_load_3d(sb + L::V + b * kBox, &tm_v, bar_addr(c.kv_full), b * 64, it.h, j0);
-        }
+        for (int b = 0; b < BOXES; ++b)
+          tma_load_3d(sb + L::K + b * kBox, &tm_k, bar_addr(c.k_full), b * 64, it.h, j0);
       }
+      ++nk;
+      if (!wait_all(bar_addr(c.v_free), (ii & 1) ^ 1)) {
+        if (lane == 0) fail(&s_abort);
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_addr(c.v_full), L::TILE);
+#pragma unroll
+        for (int b = 0; b < BOXES; ++b)
+          tma_load_3d(sb + L::V + b * kBox, &tm_v, bar_addr(c.v_full), b * 64, it.h, j0);
+      }
+      ++nv;
+      ++ii;
       Iter bi;
       bi.init(it.list + 1, it.n_iv);
       for (int i = 0; i < it.nb; ++i, bi.next(), ++gs) {
         const int st = gs % kStg;
-        const bool w = mbar_wait(bar_addr(c.q_empty[st]), ((gs / kStg) & 1) ^ 1, &s_abort, kLimitNs);
-        if (!__all_sync(0xffffffffu, w)) {
+        if (!wait_all(bar_addr(c.q_empty[st]), ((gs / kStg) & 1) ^ 1)) {
           if (lane == 0) fail(&s_abort);
           ok = false;
           break;
@@ -551,8 +652,10 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       }
     }
     if (lane == 0) {
+      // drain: every copy this CTA issued must land before shared memory goes away
       int never = 0;
-      if (ii > 0) mbar_wait(bar_addr(c.kv_full), (ii - 1) & 1, &never, kLimitNs);
+      if (nk > 0) mbar_wait(bar_addr(c.k_full), (nk - 1) & 1, &never, kLimitNs);
+      if (nv > 0) mbar_wait(bar_addr(c.v_full), (nv - 1) & 1, &never, kLimitNs);
       for (int i = max(0, gs - kStg); i < gs; ++i)
         mbar_wait(bar_addr(c.q_full[i % kStg]), (i / kStg) & 1, &never, kLimitNs);
     }
@@ -561,19 +664,57 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
       int ii = 0, gs = 0;
+      int pend = -1, pend_st = 0;  // step whose dK product is still to be issued
+      bool pend_first = false;
+      // dK += dS^T Q : A = dS^T (TMEM over dP^T), B = Q tile as MN-major
+      auto issue_dk = [&]() -> bool {
+        if (!mbar_wait(bar_addr(c.ds_full), pend & 1, &s_abort, kLimitNs)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ts(tmem + 256, tmem + 128 + ts_col(kk),
+                       sdesc_sw128(sb + L::Q + pend_st * L::TILE + kk * 2048, kBox, 1024), idG,
+                       (!pend_first || kk > 0) ? 1u : 0u);
+        umma_commit(bar_addr(c.q_empty[pend_st]));
+        return true;
+      };
       bool ok = true;
       for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
         Item it;
         it.load(m.klists, k, a.H, n_kb, false);
         if (it.nb == 0) continue;
-        if (!mbar_wait(bar_addr(c.kv_full), ii & 1, &s_abort, kLimitNs)) {
+        const int cur = ii++;
+        if (!mbar_wait(bar_addr(c.k_full), cur & 1, &s_abort, kLimitNs)) {
           fail(&s_abort);
           break;
         }
-        ++ii;
         for (int i = 0; i < it.nb; ++i, ++gs) {
           const int st = gs % kStg;
           if (!mbar_wait(bar_addr(c.q_full[st]), (gs / kStg) & 1, &s_abort, kLimitNs)) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          // S^T_gs overwrites P^T_{gs-1}: its reader dV_{gs-1} was issued
+          // earlier by this thread, and p_full(gs-1) (waited before it) means
+          // the compute warps are done with S^T_{gs-1}
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = kmajor_off(kk);
+            umma_bf16(tmem, sdesc_sw128(sb + L::K + off, 16, 1024),
+                      sdesc_sw128(sb + L::Q + st * L::TILE + off, 16, 1024), idS, kk > 0);
+          }
+          umma_commit(bar_addr(c.s_full));
+          if (i == it.nb - 1) umma_commit(bar_addr(c.k_free));
+          // dK of the previous step; its ds_full also means the compute warps
+          // have read dP^T_{gs-1}, which dP^T_gs overwrites
+          if (pend >= 0 && !issue_dk()) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          if (i == 0 && !mbar_wait(bar_addr(c.v_full), cur & 1, &s_abort, kLimitNs)) {
             fail(&s_abort);
             ok = false;
             break;
@@ -582,13 +723,11 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = kmajor_off(kk);
-            umma_bf16(tmem, sdesc_sw128(sb + L::K + off, 16, 1024),
-                      sdesc_sw128(sb + L::Q + st * L::TILE + off, 16, 1024), idS, kk > 0);
             umma_bf16(tmem + 128, sdesc_sw128(sb + L::V + off, 16, 1024),
                       sdesc_sw128(sb + L::DO + st * L::TILE + off, 16, 1024), idS, kk > 0);
           }
-          umma_commit(bar_addr(c.st_full));
-          if (i == it.nb - 1) umma_commit(bar_addr(c.kv_free));
+          umma_commit(bar_addr(c.dp_full));
+          if (i == it.nb - 1) umma_commit(bar_addr(c.v_free));
           if (!mbar_wait(bar_addr(c.p_full), gs & 1, &s_abort, kLimitNs)) {
             fail(&s_abort);
             ok = false;
@@ -601,21 +740,17 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk),
                          sdesc_sw128(sb + L::DO + st * L::TILE + kk * 2048, kBox, 1024), idG,
                          (i > 0 || kk > 0) ? 1u : 0u);
-          if (!mbar_wait(bar_addr(c.ds_full), gs & 1, &s_abort, kLimitNs)) {
-            fail(&s_abort);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // dK += dS^T Q : A = dS^T (TMEM over dP^T), B = Q tile as MN-major
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + 256, tmem + 128 + ts_col(kk),
-                         sdesc_sw128(sb + L::Q + st * L::TILE + kk * 2048, kBox, 1024), idG,
-                         (i > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar_addr(c.q_empty[st]));
+          pend = gs;
+          pend_st = st;
+          pend_first = (i == 0);
         }
-        if (ok) umma_commit(bar_addr(c.done));
+        if (!ok) break;
+        if (!issue_dk()) {
+          fail(&s_abort);
+          break;
+        }
+        pend = -1;
+        umma_commit(bar_addr(c.done));
       }
       umma_commit(bar_addr(c.mma_done));
       int never = 0;
@@ -639,7 +774,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const int key = itm.tile * 128 + row;
       for (int i = 0; i < itm.nb; ++i, ++gs) {
         const int st = gs % kStg;
-        if (!wait_warp(bar_addr(c.st_full), gs & 1) ||
+        if (!wait_warp(bar_addr(c.s_full), gs & 1) ||
             !wait_warp(bar_addr(c.qi_full[st]), (gs / kStg) & 1)) {
           fail(&s_abort);
           ok = false;
@@ -683,6 +818,12 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar_addr(c.p_full));
+        if (!wait_warp(bar_addr(c.dp_full), gs & 1)) {
+          fail(&s_abort);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         // dS^T = P^T (dP^T - Delta) -> TMEM over this half's dP^T columns (already read)
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -711,6 +852,8 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       }
       ++ii;
       tc_fence_after();
+      // This item is the only writer of these accumulator rows in this launch:
+      // one fp32 add per element, done in L2 without a round trip.
       const bool in = key < a.T;
       float* pk_ = a.dk + ((int64_t)key * a.H + itm.h) * D;
       float* pv_ = a.dv + ((int64_t)key * a.H + itm.h) * D;
@@ -721,26 +864,15 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         tmem_ld32(tmem + lb + 256 + col, gk);
         tmem_ld32(tmem + lb + 256 + D + col, gv);
         if (in) {
-          float4* dk4 = reinterpret_cast<float4*>(pk_ + col);
-          float4* dv4 = reinterpret_cast<float4*>(pv_ + col);
-          float4 xk[8], xv[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            xk[q] = dk4[q];
-            xv[q] = dv4[q];
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            xk[q].x += __uint_as_float(gk[4 * q + 0]) * a.scale;
-            xk[q].y += __uint_as_float(gk[4 * q + 1]) * a.scale;
-            xk[q].z += __uint_as_float(gk[4 * q + 2]) * a.scale;
-            xk[q].w += __uint_as_float(gk[4 * q + 3]) * a.scale;
-            xv[q].x += __uint_as_float(gv[4 * q + 0]);
-            xv[q].y += __uint_as_float(gv[4 * q + 1]);
-            xv[q].z += __uint_as_float(gv[4 * q + 2]);
-            xv[q].w += __uint_as_float(gv[4 * q + 3]);
-            dk4[q] = xk[q];
-            dv4[q] = xv[q];
+            red_add_v4(pk_ + col + 4 * q, __uint_as_float(gk[4 * q + 0]) * a.scale,
+                       __uint_as_float(gk[4 * q + 1]) * a.scale,
+                       __uint_as_float(gk[4 * q + 2]) * a.scale,
+                       __uint_as_float(gk[4 * q + 3]) * a.scale);
+            red_add_v4(pv_ + col + 4 * q, __uint_as_float(gv[4 * q + 0]),
+                       __uint_as_float(gv[4 * q + 1]), __uint_as_float(gv[4 * q + 2]),
+                       __uint_as_float(gv[4 * q + 3]));
           }
         }
       }
