@@ -95,8 +95,9 @@ struct Iter {
 struct Item {
   const int2* list;
   int tile, h, n_iv, nb;
-  __device__ void load(const int2* lists, int k, int H, int n_tiles, bool heavy_last) {
-    tile = heavy_last ? n_tiles - 1 - k / H : k / H;
+  __device__ void load(const int2* lists, int k, int H, int n_tiles) {
+    // the (k / H)-th heaviest tile of the precomputed order
+    tile = min(max(lists[(kListBytes / 8) * (k / H)].y, 0), n_tiles - 1);
     h = k % H;
     list = lists + (kListBytes / 8) * tile;
     n_iv = min(list[0].x, kListCap);
@@ -221,9 +222,11 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     if (lane == 0) {
       int ii = 0, gk = 0, gv = 0;
       bool ok = true;
-      for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+      for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
+        const int k = snake_item(j, blockIdx.x, gridDim.x);
+        if (k >= n_items) continue;
         Item it;
-        it.load(m.qlists, k, a.H, n_qt, true);
+        it.load(m.qlists, k, a.H, n_qt);
         if (it.nb == 0) continue;
         // single Q/dO buffer: free once the previous item's S, dP retired
         if (!mbar_wait(bar_addr(c.qd_free), (ii & 1) ^ 1, &s_abort, kLimitNs)) {
@@ -299,9 +302,11 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         return true;
       };
       bool ok = true;
-      for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+      for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
+        const int k = snake_item(j, blockIdx.x, gridDim.x);
+        if (k >= n_items) continue;
         Item it;
-        it.load(m.qlists, k, a.H, n_qt, true);
+        it.load(m.qlists, k, a.H, n_qt);
         if (it.nb == 0) continue;
         if (!mbar_wait(bar_addr(c.qd_full), ii & 1, &s_abort, kLimitNs)) {
           fail(&s_abort);
@@ -374,9 +379,11 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     };
     int ii = 0, g = 0;
     bool ok = true;
-    for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+    for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
+      const int k = snake_item(j, blockIdx.x, gridDim.x);
+      if (k >= n_items) continue;
       Item itm;
-      itm.load(m.qlists, k, a.H, n_qt, true);
+      itm.load(m.qlists, k, a.H, n_qt);
       const int t = itm.tile * 128 + row;
       const bool in = t < a.s_local;
       if (itm.nb == 0) {  // no real query row: dQ = 0
@@ -507,6 +514,10 @@ struct KvCtl {
   uint32_t tmem;
   int abort;
 };
+// per-warp staging of the dK / dV epilogue follows KvCtl (16-byte aligned)
+__host__ __device__ constexpr int kv_ctl_bytes() { return (int)((sizeof(KvCtl) + 15) & ~(size_t)15); }
+constexpr int kStageBytes = 8 * 32 * 16 * 4;  // 8 compute warps x 32 rows x 16 fp32
+
 
 // Per query step i the MMA thread issues S^T_i, then the previous step's
 // dK_{i-1} (once dS^T_{i-1} is in TMEM), then dP^T_i, then dV_i (once P^T_i
@@ -572,9 +583,11 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
       return __all_sync(0xffffffffu, w);
     };
-    for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+    for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
+      const int k = snake_item(j, blockIdx.x, gridDim.x);
+      if (k >= n_items) continue;
       Item it;
-      it.load(m.klists, k, a.H, n_kb, false);
+      it.load(m.klists, k, a.H, n_kb);
       if (it.nb == 0) continue;
       const int j0 = it.tile * 128;
       // single K (V) tile: free once the previous item's last S^T (dP^T) retired
@@ -679,9 +692,11 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         return true;
       };
       bool ok = true;
-      for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+      for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
+        const int k = snake_item(j, blockIdx.x, gridDim.x);
+        if (k >= n_items) continue;
         Item it;
-        it.load(m.klists, k, a.H, n_kb, false);
+        it.load(m.klists, k, a.H, n_kb);
         if (it.nb == 0) continue;
         const int cur = ii++;
         if (!mbar_wait(bar_addr(c.k_full), cur & 1, &s_abort, kLimitNs)) {
@@ -767,9 +782,11 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     };
     int ii = 0, gs = 0;
     bool ok = true;
-    for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+    for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
+      const int k = snake_item(j, blockIdx.x, gridDim.x);
+      if (k >= n_items) continue;
       Item itm;
-      itm.load(m.klists, k, a.H, n_kb, false);
+      itm.load(m.klists, k, a.H, n_kb);
       if (itm.nb == 0) continue;  // no query of this rank attends these keys
       const int key = itm.tile * 128 + row;
       for (int i = 0; i < itm.nb; ++i, ++gs) {
@@ -853,26 +870,42 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       ++ii;
       tc_fence_after();
       // This item is the only writer of these accumulator rows in this launch:
-      // one fp32 add per element, done in L2 without a round trip.
-      const bool in = key < a.T;
-      float* pk_ = a.dk + ((int64_t)key * a.H + itm.h) * D;
-      float* pv_ = a.dv + ((int64_t)key * a.H + itm.h) * D;
+      // one fp32 add per element, done in L2 without a round trip.  Each warp
+      // turns its 32 rows x 16 columns around in a private shared-memory
+      // buffer first, so that one vector reduction covers 64 contiguous bytes
+      // of 8 rows instead of 16 bytes of 32 rows.  The buffer's 16-byte units
+      // are rotated by (row >> 1) & 3, which keeps both the row-wise writes
+      // and the column-wise reads free of bank conflicts.
+      float* stg = reinterpret_cast<float*>(smem_raw + L::BYTES + kv_ctl_bytes()) + warp * 512;
+      const int rbase = itm.tile * 128 + (warp & 3) * 32;  // first key row of this warp
 #pragma unroll
       for (int cq = 0; cq < D / 64; ++cq) {
         const int col = hf * (D / 2) + cq * 32;  // this half's dK / dV columns
         uint32_t gk[32], gv[32];
         tmem_ld32(tmem + lb + 256 + col, gk);
         tmem_ld32(tmem + lb + 256 + D + col, gv);
-        if (in) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            red_add_v4(pk_ + col + 4 * q, __uint_as_float(gk[4 * q + 0]) * a.scale,
-                       __uint_as_float(gk[4 * q + 1]) * a.scale,
-                       __uint_as_float(gk[4 * q + 2]) * a.scale,
-                       __uint_as_float(gk[4 * q + 3]) * a.scale);
-            red_add_v4(pv_ + col + 4 * q, __uint_as_float(gv[4 * q + 0]),
-                       __uint_as_float(gv[4 * q + 1]), __uint_as_float(gv[4 * q + 2]),
-                       __uint_as_float(gv[4 * q + 3]));
+        for (int part = 0; part < 4; ++part) {  // dK, dK, dV, dV: 16 columns each
+          const uint32_t* src = (part < 2 ? gk : gv) + (part & 1) * 16;
+          const float sc = part < 2 ? a.scale : 1.f;
+          float* acc = part < 2 ? a.dk : a.dv;
+          const int c0 = col + (part & 1) * 16;
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<float4*>(stg + lane * 16 + ((u ^ ((lane >> 1) & 3)) * 4)) =
+                make_float4(__uint_as_float(src[4 * u]) * sc, __uint_as_float(src[4 * u + 1]) * sc,
+                            __uint_as_float(src[4 * u + 2]) * sc,
+                            __uint_as_float(src[4 * u + 3]) * sc);
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int rr = (lane >> 2) + 8 * it, uu = lane & 3;
+            const float4 v =
+                *reinterpret_cast<const float4*>(stg + rr * 16 + ((uu ^ ((rr >> 1) & 3)) * 4));
+            const int kr = rbase + rr;
+            if (kr < a.T)
+              red_add_v4(acc + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * uu, v.x, v.y, v.z, v.w);
           }
         }
       }
@@ -897,7 +930,7 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
   if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128)) != CP_OK) return st;
   if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128)) != CP_OK) return st;
   const int dq_smem = DqLayout<D>::BYTES + (int)sizeof(DqCtl);
-  const int kv_smem = KvLayout<D>::BYTES + (int)sizeof(KvCtl);
+  const int kv_smem = KvLayout<D>::BYTES + kv_ctl_bytes() + kStageBytes;
   if (cudaFuncSetAttribute(attn_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem) !=
           cudaSuccess ||
       cudaFuncSetAttribute(attn_dkdv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -9,8 +9,8 @@
 // the key range of every row comes from the rank's row tables.
 //
 // Persistent kernel: one CTA per SM walks a static list of work items
-// (128-row query tile, head), heaviest tiles first, item k going to CTA
-// k % gridDim.x.  The pipeline never drains between items: all barrier phases
+// (128-row query tile, head), heaviest tiles first, dealt to the CTAs in
+// rounds of alternating direction.  The pipeline never drains between items: all barrier phases
 // follow global counters, Q and the O accumulator are double buffered, and an
 // item's epilogue is deferred until the next item's first block has been
 // handed to the tensor core, so it overlaps tensor-core work.  10 warps:
@@ -134,7 +134,8 @@ struct Item {
   const int2* list;  // precomputed list: list[0].x intervals in list[1..]
   int t0, h, n_iv, nb;
   __device__ void load(const MetaView& m, int k, int n_qt, int H) {
-    const int tile = n_qt - 1 - k / H;  // later tiles carry more causal work
+    // the (k / H)-th heaviest tile of the precomputed order
+    const int tile = min(max(m.qlists[(kListBytes / 8) * (k / H)].y, 0), n_qt - 1);
     h = k % H;
     t0 = tile * TBM;
     list = m.qlists + (kListBytes / 8) * tile;
@@ -232,7 +233,9 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         ++v_issued;
         return true;
       };
-      for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+      for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
+        const int k = snake_item(j, blockIdx.x, gridDim.x);
+        if (k >= n_items) continue;
         Item it;
         it.load(m, k, n_qt, a.H);
         if (it.nb == 0) continue;
@@ -312,7 +315,9 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       };
       int ii = 0, g = 0;
       bool ok = true;
-      for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+      for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
+        const int k = snake_item(j, blockIdx.x, gridDim.x);
+        if (k >= n_items) continue;
         Item it;
         it.load(m, k, n_qt, a.H);
         if (it.nb == 0) continue;
@@ -386,8 +391,11 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       ++u;
       return w;
     };
-    auto next_item = [&](int k) -> int {
-      for (k += gridDim.x; k < n_items; k += gridDim.x) {
+    // the CTA's next non-empty work item after round j (n_items if none)
+    auto next_item = [&](int j) -> int {
+      for (++j; j * (int)gridDim.x < n_items; ++j) {
+        const int k = snake_item(j, blockIdx.x, gridDim.x);
+        if (k >= n_items) continue;
         Item nx;
         nx.load(m, k, n_qt, a.H);
         if (nx.nb > 0) return k;
@@ -435,7 +443,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     int ii = 0, g = 0;
     bool ok = true;
     // row tables of the next non-empty item are fetched one item ahead
-    int k_pre = next_item((int)blockIdx.x - (int)gridDim.x);
+    int k_pre = next_item(-1);
     int lo_pre = 0, hi_pre = -1;
     if (k_pre < n_items) {
       Item f;
@@ -444,7 +452,9 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       lo_pre = t < a.s_local ? m.row_lo[t] : 0;
       hi_pre = t < a.s_local ? m.row_hi[t] : -1;
     }
-    for (int k = blockIdx.x; ok && k < n_items; k += gridDim.x) {
+    for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
+      const int k = snake_item(j, blockIdx.x, gridDim.x);
+      if (k >= n_items) continue;
       Item itm;
       itm.load(m, k, n_qt, a.H);
       const int t = itm.t0 + row;
@@ -459,7 +469,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         continue;
       }
       const int lo = lo_pre, hi = hi_pre;  // k == k_pre here
-      k_pre = next_item(k);
+      k_pre = next_item(j);
       if (k_pre < n_items) {
         Item f;
         f.load(m, k_pre, n_qt, a.H);

@@ -24,8 +24,11 @@ namespace cpthd {
 // row global_start + u; it is a real token when u < valid_len.
 // row_lo/row_hi: the keys local row t attends are [row_lo[t], row_hi[t]]
 // (row_hi = -1, row_lo = 0 for padding rows).
-// A block list is int2[8]: {count, 0} then up to 7 merged, increasing
-// inclusive intervals [first, last] of 128-wide block indices.
+// A block list is int2[8]: {count, order} then up to 7 merged, increasing
+// inclusive intervals [first, last] of 128-wide block indices.  `order` of
+// the q-th list of a family (query tiles, or key blocks) is the index of the
+// tile with the q-th most blocks (ties by index): the attention kernels take
+// their work items heaviest first.
 // ---------------------------------------------------------------------------
 constexpr int32_t kMetaMagic = 0x43505448;  // "CPTH"
 constexpr int kTile = 128;       // query-tile rows and key-block width of the lists
@@ -75,6 +78,13 @@ inline __host__ __device__ int64_t n_tiles_of(int64_t rows) { return (rows + kTi
 inline __host__ __device__ size_t meta_bytes_for(int n_docs, int64_t s_local, int cp) {
   return lists_offset_bytes(n_docs, s_local) +
          (size_t)kListBytes * (size_t)(n_tiles_of(s_local) + n_tiles_of(s_local * cp));
+}
+
+// Work item of the j-th round of CTA c among G persistent CTAs: rounds of G
+// consecutive items (sorted heaviest first) alternate direction, so every
+// CTA's sum of item sizes stays close to the mean.
+__host__ __device__ __forceinline__ int snake_item(int j, int c, int G) {
+  return j * G + ((j & 1) ? G - 1 - c : c);
 }
 
 struct MetaView {

@@ -201,6 +201,40 @@ partition_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup
     }
     out[0] = make_int2(cnt, 0);
   }
+
+  // pass 4: heaviest-first work order of each list family (a rank by
+  // comparison against every other tile, block counts staged in shared
+  // memory; stable for equal counts)
+  __syncthreads();
+  __shared__ int s_nb[2048];
+  for (int fam = 0; fam < 2; ++fam) {
+    const int n = fam == 0 ? n_qt : n_kb;
+    int32_t* L = reinterpret_cast<int32_t*>(lists + (fam == 0 ? 0 : (kListBytes / 8) * n_qt));
+    auto blocks_of = [&](int q) {  // blocks in list q of this family
+      const int32_t* l = L + (kListBytes / 4) * q;
+      const int cnt = min(l[0], kListCap);
+      int nb = 0;
+      for (int i = 0; i < cnt; ++i) nb += l[3 + 2 * i] - l[2 + 2 * i] + 1;
+      return nb;
+    };
+    for (int q0 = 0; q0 < n; q0 += kThreads) {
+      const int q = q0 + threadIdx.x;
+      const int mine = q < n ? blocks_of(q) : 0;
+      int rank = 0;
+      for (int c0 = 0; c0 < n; c0 += 2048) {
+        const int cn = min(2048, n - c0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < cn; i += kThreads) s_nb[i] = blocks_of(c0 + i);
+        __syncthreads();
+        if (q < n)
+          for (int i = 0; i < cn; ++i) {
+            const int o = s_nb[i];
+            rank += (o > mine || (o == mine && c0 + i < q)) ? 1 : 0;
+          }
+      }
+      if (q < n) L[(kListBytes / 4) * rank + 1] = q;
+    }
+  }
 }
 
 }  // namespace
