@@ -285,6 +285,12 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
+      // operand descriptors at the tiles' first bytes (K-major, and K as MN-major)
+      const uint64_t dsc_q = sdesc_sw128(sb + L::Q, 16, 1024);
+      const uint64_t dsc_do = sdesc_sw128(sb + L::DO, 16, 1024);
+      const uint64_t dsc_k = sdesc_sw128(sb + L::K, 16, 1024);
+      const uint64_t dsc_v = sdesc_sw128(sb + L::V, 16, 1024);
+      const uint64_t dsc_kmn = sdesc_sw128(sb + L::K, kBox, 1024);
       int ii = 0, g = 0;
       int pend = -1;  // block whose dQ product is still to be issued
       bool pend_first = false;
@@ -293,10 +299,11 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (!mbar_wait(bar_addr(c.ds_full), pend & 1, &s_abort, kLimitNs)) return false;
         tc_fence_after();
         const int ks = pend % kDqKStages;
+        const uint64_t bk = sdesc_add(dsc_kmn, ks * L::TILE);
+        const uint32_t ads = tmem + dq_ds_col<D>(pend & 1);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + 256, tmem + dq_ds_col<D>(pend & 1) + (kk >> 2) * 32 + (kk & 3) * 8,
-                       sdesc_sw128(sb + L::K + ks * L::TILE + kk * 2048, kBox, 1024), idQ,
+          umma_bf16_ts(tmem + 256, ads + (kk >> 2) * 32 + (kk & 3) * 8, sdesc_add(bk, kk * 2048), idQ,
                        (!pend_first || kk > 0) ? 1u : 0u);
         umma_commit(bar_addr(c.k_empty[ks]));
         return true;
@@ -323,11 +330,11 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             break;
           }
           tc_fence_after();
+          const uint64_t bk = sdesc_add(dsc_k, ks * L::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = kmajor_off(kk);
-            umma_bf16(tmem, sdesc_sw128(sb + L::Q + off, 16, 1024),
-                      sdesc_sw128(sb + L::K + ks * L::TILE + off, 16, 1024), idS, kk > 0);
+            umma_bf16(tmem, sdesc_add(dsc_q, off), sdesc_add(bk, off), idS, kk > 0);
           }
           umma_commit(bar_addr(c.s_full));
           // dQ of the previous block (waits for its dS; that also means the
@@ -343,11 +350,11 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             break;
           }
           tc_fence_after();
+          const uint64_t bv = sdesc_add(dsc_v, vs * L::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = kmajor_off(kk);
-            umma_bf16(tmem + 128, sdesc_sw128(sb + L::DO + off, 16, 1024),
-                      sdesc_sw128(sb + L::V + vs * L::TILE + off, 16, 1024), idS, kk > 0);
+            umma_bf16(tmem + 128, sdesc_add(dsc_do, off), sdesc_add(bv, off), idS, kk > 0);
           }
           umma_commit(bar_addr(c.dp_full));
           umma_commit(bar_addr(c.v_empty[vs]));
@@ -676,6 +683,13 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
+      // operand descriptors at the tiles' first bytes (K-major, and Q / dO as MN-major)
+      const uint64_t dsc_k = sdesc_sw128(sb + L::K, 16, 1024);
+      const uint64_t dsc_v = sdesc_sw128(sb + L::V, 16, 1024);
+      const uint64_t dsc_q = sdesc_sw128(sb + L::Q, 16, 1024);
+      const uint64_t dsc_do = sdesc_sw128(sb + L::DO, 16, 1024);
+      const uint64_t dsc_qmn = sdesc_sw128(sb + L::Q, kBox, 1024);
+      const uint64_t dsc_domn = sdesc_sw128(sb + L::DO, kBox, 1024);
       int ii = 0, gs = 0;
       int pend = -1, pend_st = 0;  // step whose dK product is still to be issued
       bool pend_first = false;
@@ -683,10 +697,10 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       auto issue_dk = [&]() -> bool {
         if (!mbar_wait(bar_addr(c.ds_full), pend & 1, &s_abort, kLimitNs)) return false;
         tc_fence_after();
+        const uint64_t bq = sdesc_add(dsc_qmn, pend_st * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + 256, tmem + 128 + ts_col(kk),
-                       sdesc_sw128(sb + L::Q + pend_st * L::TILE + kk * 2048, kBox, 1024), idG,
+          umma_bf16_ts(tmem + 256, tmem + 128 + ts_col(kk), sdesc_add(bq, kk * 2048), idG,
                        (!pend_first || kk > 0) ? 1u : 0u);
         umma_commit(bar_addr(c.q_empty[pend_st]));
         return true;
@@ -714,11 +728,11 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           // earlier by this thread, and p_full(gs-1) (waited before it) means
           // the compute warps are done with S^T_{gs-1}
           tc_fence_after();
+          const uint64_t bq = sdesc_add(dsc_q, st * L::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = kmajor_off(kk);
-            umma_bf16(tmem, sdesc_sw128(sb + L::K + off, 16, 1024),
-                      sdesc_sw128(sb + L::Q + st * L::TILE + off, 16, 1024), idS, kk > 0);
+            umma_bf16(tmem, sdesc_add(dsc_k, off), sdesc_add(bq, off), idS, kk > 0);
           }
           umma_commit(bar_addr(c.s_full));
           if (i == it.nb - 1) umma_commit(bar_addr(c.k_free));
@@ -735,11 +749,11 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             break;
           }
           tc_fence_after();
+          const uint64_t bd = sdesc_add(dsc_do, st * L::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = kmajor_off(kk);
-            umma_bf16(tmem + 128, sdesc_sw128(sb + L::V + off, 16, 1024),
-                      sdesc_sw128(sb + L::DO + st * L::TILE + off, 16, 1024), idS, kk > 0);
+            umma_bf16(tmem + 128, sdesc_add(dsc_v, off), sdesc_add(bd, off), idS, kk > 0);
           }
           umma_commit(bar_addr(c.dp_full));
           if (i == it.nb - 1) umma_commit(bar_addr(c.v_free));
@@ -750,10 +764,10 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           }
           tc_fence_after();
           // dV += P^T dO : A = P^T (TMEM over S^T), B = dO tile as MN-major (N = d)
+          const uint64_t bdm = sdesc_add(dsc_domn, st * L::TILE);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk),
-                         sdesc_sw128(sb + L::DO + st * L::TILE + kk * 2048, kBox, 1024), idG,
+            umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk), sdesc_add(bdm, kk * 2048), idG,
                          (i > 0 || kk > 0) ? 1u : 0u);
           pend = gs;
           pend_st = st;

@@ -178,6 +178,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The same operand `bytes` further on in shared memory (a multiple of 16; the
+// start-address field is the shared-window address >> 4, which for the
+// window's < 256 KB never carries out of its 14 bits): one 64-bit add instead
+// of rebuilding the descriptor, so the single MMA-issuing thread spends few
+// instructions per MMA.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) {
+  return d + (uint64_t)(bytes >> 4);
+}
+
 // kind::f16 instruction descriptor: bf16 x bf16 -> f32, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
                                                       bool b_mn_major) {
