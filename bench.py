@@ -38,6 +38,15 @@ METRIC = "CP-rank causal THD attention TFLOP/s (% BF16 peak); THD gather GB/s (%
 WORKLOAD = "THD packed 32768 tokens: 16 docs, cp_size=4, H=16, D=128, bf16, causal fwd+bwd, both strategies"
 
 
+# DRAM bytes (read + write) of one attn_bwd call, from one ncu capture of the current kernels
+# (profiles/attn_bwd_tc_cfg2_dcs_rank0.md): attn_dq_tc 496.3 + 22.8 MB, attn_dkdv_tc 998.2 +
+# 481.9 MB; attn_delta (not captured) at its algorithmic 2 x 33.6 MB read + 0.5 MB written.
+BWD_TRAFFIC_BYTES = int((496.3 + 22.8 + 998.2 + 481.9 + 67.1 + 0.5) * 1e6)
+BWD_TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the DUAL_CHUNK_SWAP rank-0 call "
+                    "(dq + dkdv kernels measured, delta at its algorithmic bytes); 1.02 GB of it is the fp32 dK/dV "
+                    "accumulator update")
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -258,7 +267,9 @@ def run_own(args):
                        "l2": "inputs larger than L2 (4 x 134 MB bf16 inputs, ~2 GB touched per step)"},
             "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(ach, 2),
                          "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                         "peak_source": f"{peak_src} bf16 sustained", "traffic": None},
+                         "peak_source": f"{peak_src} bf16 sustained",
+                         "traffic": BWD_TRAFFIC_BYTES if dominant == "attn_bwd" else None,
+                         "traffic_note": BWD_TRAFFIC_NOTE if dominant == "attn_bwd" else None},
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "e2e": {"value": round(ws * flop_step / (e2e_ms * 1e-3) / 1e12, 3),
