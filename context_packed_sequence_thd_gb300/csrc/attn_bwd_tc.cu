@@ -81,29 +81,33 @@ __device__ __forceinline__ void fail(volatile int* abort) {
   atomicCAS(&g_status_bwd_tc, 0, (int)CP_ERR_TIMEOUT);
 }
 
-struct Iter {
+struct Iter {  // flattened walk over an item's block intervals
   const int2* iv;
   int n, i, b;
   __device__ void init(const int2* p, int cnt) { iv = p; n = cnt; i = 0; b = cnt > 0 ? p[0].x : 0; }
   __device__ void next() {
-    if (b < iv[i].y) { ++b; } else { ++i; if (i < n) b = iv[i].x; }
+    if (i < n && b < iv[i].y) {
+      ++b;
+    } else {
+      ++i;
+      if (i < n) b = iv[i].x;
+    }
   }
 };
 
 // One work item: a 128-row tile (dQ: query tile; dK/dV: key block), a head,
 // and the blocks of the tile's precomputed list.
 struct Item {
-  const int2* list;
-  int tile, h, n_iv, nb;
-  __device__ void load(const int2* lists, int k, int H, int n_tiles) {
-    // the (k / H)-th heaviest tile of the precomputed order
-    tile = min(max(lists[(kListBytes / 8) * (k / H)].y, 0), n_tiles - 1);
+  const int2* list;  // the tile's block list: count in list[0].x, intervals in list[1..]
+  int tile, h, nb;
+  __device__ void load(const int2* order, const int2* lists, int k, int H, int n_tiles) {
+    const int2 o = order[k / H];  // the (k / H)-th heaviest tile and its block count
+    tile = min(max(o.x, 0), n_tiles - 1);
     h = k % H;
     list = lists + (kListBytes / 8) * tile;
-    n_iv = min(list[0].x, kListCap);
-    nb = 0;
-    for (int i = 0; i < n_iv; ++i) nb += list[1 + i].y - list[1 + i].x + 1;
+    nb = o.y;
   }
+  __device__ int n_iv() const { return min(list[0].x, kListCap); }
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint64_t& b) { return smem_u32(&b); }
@@ -226,7 +230,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const int k = snake_item(j, blockIdx.x, gridDim.x);
         if (k >= n_items) continue;
         Item it;
-        it.load(m.qlists, k, a.H, n_qt);
+        it.load(m.qorder, m.qlists, k, a.H, n_qt);
         if (it.nb == 0) continue;
         // single Q/dO buffer: free once the previous item's S, dP retired
         if (!mbar_wait(bar_addr(c.qd_free), (ii & 1) ^ 1, &s_abort, kLimitNs)) {
@@ -242,7 +246,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         ++ii;
         Iter bi;
-        bi.init(it.list + 1, it.n_iv);
+        bi.init(it.list + 1, it.n_iv());
         for (int j = 0; j < it.nb; ++j, bi.next()) {
           const int key0 = bi.b * 128;
           const int ks = gk % kDqKStages;
@@ -313,7 +317,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const int k = snake_item(j, blockIdx.x, gridDim.x);
         if (k >= n_items) continue;
         Item it;
-        it.load(m.qlists, k, a.H, n_qt);
+        it.load(m.qorder, m.qlists, k, a.H, n_qt);
         if (it.nb == 0) continue;
         if (!mbar_wait(bar_addr(c.qd_full), ii & 1, &s_abort, kLimitNs)) {
           fail(&s_abort);
@@ -390,7 +394,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const int k = snake_item(j, blockIdx.x, gridDim.x);
       if (k >= n_items) continue;
       Item itm;
-      itm.load(m.qlists, k, a.H, n_qt);
+      itm.load(m.qorder, m.qlists, k, a.H, n_qt);
       const int t = itm.tile * 128 + row;
       const bool in = t < a.s_local;
       if (itm.nb == 0) {  // no real query row: dQ = 0
@@ -407,7 +411,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const float lse2 = hi >= 0 ? a.lse[(int64_t)itm.h * a.s_local + t] * kLog2ef : 0.f;
       const float dl = hi >= 0 ? a.delta[(int64_t)itm.h * a.s_local + t] : 0.f;
       Iter bi;
-      bi.init(itm.list + 1, itm.n_iv);
+      bi.init(itm.list + 1, itm.n_iv());
       for (int j = 0; j < itm.nb; ++j, bi.next(), ++g) {
         if (!wait_warp(bar_addr(c.s_full), g & 1)) {
           fail(&s_abort);
@@ -594,7 +598,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const int k = snake_item(j, blockIdx.x, gridDim.x);
       if (k >= n_items) continue;
       Item it;
-      it.load(m.klists, k, a.H, n_kb);
+      it.load(m.korder, m.klists, k, a.H, n_kb);
       if (it.nb == 0) continue;
       const int j0 = it.tile * 128;
       // single K (V) tile: free once the previous item's last S^T (dP^T) retired
@@ -623,7 +627,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       ++nv;
       ++ii;
       Iter bi;
-      bi.init(it.list + 1, it.n_iv);
+      bi.init(it.list + 1, it.n_iv());
       for (int i = 0; i < it.nb; ++i, bi.next(), ++gs) {
         const int st = gs % kStg;
         if (!wait_all(bar_addr(c.q_empty[st]), ((gs / kStg) & 1) ^ 1)) {
@@ -710,7 +714,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const int k = snake_item(j, blockIdx.x, gridDim.x);
         if (k >= n_items) continue;
         Item it;
-        it.load(m.klists, k, a.H, n_kb);
+        it.load(m.korder, m.klists, k, a.H, n_kb);
         if (it.nb == 0) continue;
         const int cur = ii++;
         if (!mbar_wait(bar_addr(c.k_full), cur & 1, &s_abort, kLimitNs)) {
@@ -800,7 +804,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const int k = snake_item(j, blockIdx.x, gridDim.x);
       if (k >= n_items) continue;
       Item itm;
-      itm.load(m.klists, k, a.H, n_kb);
+      itm.load(m.korder, m.klists, k, a.H, n_kb);
       if (itm.nb == 0) continue;  // no query of this rank attends these keys
       const int key = itm.tile * 128 + row;
       for (int i = 0; i < itm.nb; ++i, ++gs) {

@@ -131,18 +131,17 @@ __device__ __forceinline__ void fail(volatile int* abort) {
 
 // One work item: its tile, head and the key blocks of the tile's block list.
 struct Item {
-  const int2* list;  // precomputed list: list[0].x intervals in list[1..]
-  int t0, h, n_iv, nb;
+  const int2* list;  // the tile's block list: count in list[0].x, intervals in list[1..]
+  int t0, h, nb;
   __device__ void load(const MetaView& m, int k, int n_qt, int H) {
-    // the (k / H)-th heaviest tile of the precomputed order
-    const int tile = min(max(m.qlists[(kListBytes / 8) * (k / H)].y, 0), n_qt - 1);
+    const int2 o = m.qorder[k / H];  // the (k / H)-th heaviest tile and its block count
+    const int tile = min(max(o.x, 0), n_qt - 1);
     h = k % H;
     t0 = tile * TBM;
     list = m.qlists + (kListBytes / 8) * tile;
-    n_iv = min(list[0].x, kListCap);
-    nb = 0;
-    for (int i = 0; i < n_iv; ++i) nb += list[1 + i].y - list[1 + i].x + 1;
+    nb = o.y;
   }
+  __device__ int n_iv() const { return min(list[0].x, kListCap); }
 };
 
 struct Iter {  // flattened walk over an item's key-block intervals
@@ -150,13 +149,15 @@ struct Iter {  // flattened walk over an item's key-block intervals
   int n, i, b;
   __device__ void init(const int2* p, int cnt) { iv = p; n = cnt; i = 0; b = cnt > 0 ? p[0].x : 0; }
   __device__ void next() {
-    if (b < iv[i].y) { ++b; } else { ++i; if (i < n) b = iv[i].x; }
+    if (i < n && b < iv[i].y) {
+      ++b;
+    } else {
+      ++i;
+      if (i < n) b = iv[i].x;
+    }
   }
 };
 
-// Register budget: the register file is split over the SM's four
-// sub-partitions (16K each) and 10 warps put 3 warps on two of them, so a
-// thread gets at most 168 registers.
 template <int D>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -251,7 +252,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                       b * 64, it.h, it.t0);
         ++ii;
         Iter bi;
-        bi.init(it.list + 1, it.n_iv);
+        bi.init(it.list + 1, it.n_iv());
         for (int j = 0; j < it.nb; ++j, bi.next()) {
           const int ks = g % kKStages;
           if (!mbar_wait(bar(bars.k_empty[ks]), ((g / kKStages) & 1) ^ 1, &s_abort,
@@ -481,7 +482,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       ++ii;
       float m_run = -INFINITY, l_run = 0.f;
       Iter bi;
-      bi.init(itm.list + 1, itm.n_iv);
+      bi.init(itm.list + 1, itm.n_iv());
       for (int j = 0; j < itm.nb; ++j, bi.next(), ++g) {
         const int buf = g & 1;
         if (!wait_warp(bar(bars.s_full[buf]), (g >> 1) & 1)) {

@@ -18,17 +18,20 @@ namespace cpthd {
 //   lists_offset (16-aligned): one 64-byte block list per 128-row query tile
 //                             (the key blocks it attends), then one per
 //                             128-key block (the query tiles attending it)
+//   after the lists:          the work order, int2 {tile, blocks} per tile,
+//                             heaviest first: query tiles, then key blocks
 // A segment is a maximal run of local rows that are consecutive global rows
 // of one document: one DUAL_CHUNK_SWAP chunk, or one document's piece of a
 // NO_LOAD_BALANCE range.  Row t of a segment (u = t - local_start) is global
 // row global_start + u; it is a real token when u < valid_len.
 // row_lo/row_hi: the keys local row t attends are [row_lo[t], row_hi[t]]
 // (row_hi = -1, row_lo = 0 for padding rows).
-// A block list is int2[8]: {count, order} then up to 7 merged, increasing
-// inclusive intervals [first, last] of 128-wide block indices.  `order` of
-// the q-th list of a family (query tiles, or key blocks) is the index of the
-// tile with the q-th most blocks (ties by index): the attention kernels take
-// their work items heaviest first.
+// A block list is int2[8]: {count, blocks} then up to 7 merged, increasing
+// inclusive intervals [first, last] of 128-wide block indices; `blocks` is the
+// number of blocks the intervals cover.  Entry q of a family's work order is
+// {tile, blocks} of the tile with the q-th most blocks (ties by index): the
+// attention kernels take their work items heaviest first, and one 8-byte load
+// tells a warp which tile comes next and how many blocks it has.
 // ---------------------------------------------------------------------------
 constexpr int32_t kMetaMagic = 0x43505448;  // "CPTH"
 constexpr int kTile = 128;       // query-tile rows and key-block width of the lists
@@ -76,8 +79,8 @@ inline __host__ __device__ size_t lists_offset_bytes(int n_docs, int64_t s_local
 }
 inline __host__ __device__ int64_t n_tiles_of(int64_t rows) { return (rows + kTile - 1) / kTile; }
 inline __host__ __device__ size_t meta_bytes_for(int n_docs, int64_t s_local, int cp) {
-  return lists_offset_bytes(n_docs, s_local) +
-         (size_t)kListBytes * (size_t)(n_tiles_of(s_local) + n_tiles_of(s_local * cp));
+  const size_t n = (size_t)(n_tiles_of(s_local) + n_tiles_of(s_local * cp));
+  return lists_offset_bytes(n_docs, s_local) + (size_t)(kListBytes + 8) * n;
 }
 
 // Work item of the j-th round of CTA c among G persistent CTAs: rounds of G
@@ -94,6 +97,8 @@ struct MetaView {
   const int32_t* row_hi;
   const int2* qlists;  // per 128-row query tile: key blocks attended
   const int2* klists;  // per 128-key block: query tiles attending it
+  const int2* qorder;  // {tile, blocks} of the query tiles, heaviest first
+  const int2* korder;  // {block, tiles} of the key blocks, heaviest first
 };
 
 inline __device__ MetaView meta_view(const void* meta) {
@@ -105,6 +110,8 @@ inline __device__ MetaView meta_view(const void* meta) {
   v.row_hi = v.row_lo + v.hdr->s_local;
   v.qlists = reinterpret_cast<const int2*>(base + v.hdr->lists_offset);
   v.klists = v.qlists + (kListBytes / 8) * n_tiles_of(v.hdr->s_local);
+  v.qorder = v.klists + (kListBytes / 8) * v.hdr->n_kblocks;
+  v.korder = v.qorder + n_tiles_of(v.hdr->s_local);
   return v;
 }
 
@@ -112,8 +119,8 @@ inline __device__ MetaView meta_view(const void* meta) {
 // caller's buffer of meta_bytes.
 inline __device__ bool meta_matches(const MetaHeader* h, size_t meta_bytes, int T, int s_local,
                                     int cp, int rank, int strategy) {
-  const int64_t lists_end = (int64_t)h->lists_offset +
-                            (int64_t)kListBytes * (n_tiles_of(s_local) + (int64_t)h->n_kblocks);
+  const int64_t lists_end = (int64_t)h->lists_offset + (int64_t)(kListBytes + 8) *
+                                                         (n_tiles_of(s_local) + (int64_t)h->n_kblocks);
   const bool fits = h->n_segs >= 0 && h->n_segs <= h->max_segs && h->seg_offset == 64 &&
                     (int64_t)h->rows_offset >= 64 + 32 * (int64_t)h->max_segs &&
                     (int64_t)h->lists_offset >= (int64_t)h->rows_offset + 8 * (int64_t)s_local &&

@@ -199,32 +199,29 @@ partition_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup
       const int j0 = (q - n_qt) * kTile;
       cnt = build_q_intervals(mv, j0, min(j0 + kTile, T) - 1, kTile, out + 1, kListCap);
     }
-    out[0] = make_int2(cnt, 0);
+    int nb = 0;
+    for (int i = 0; i < min(cnt, kListCap); ++i) nb += out[1 + i].y - out[1 + i].x + 1;
+    out[0] = make_int2(cnt, nb);
   }
 
-  // pass 4: heaviest-first work order of each list family (a rank by
-  // comparison against every other tile, block counts staged in shared
-  // memory; stable for equal counts)
+  // pass 4: heaviest-first work order of each list family, {tile, blocks}
+  // (a rank by comparison against every other tile, block counts staged in
+  // shared memory; stable for equal counts)
   __syncthreads();
   __shared__ int s_nb[2048];
+  int2* order = lists + (kListBytes / 8) * (n_qt + n_kb);
   for (int fam = 0; fam < 2; ++fam) {
     const int n = fam == 0 ? n_qt : n_kb;
-    int32_t* L = reinterpret_cast<int32_t*>(lists + (fam == 0 ? 0 : (kListBytes / 8) * n_qt));
-    auto blocks_of = [&](int q) {  // blocks in list q of this family
-      const int32_t* l = L + (kListBytes / 4) * q;
-      const int cnt = min(l[0], kListCap);
-      int nb = 0;
-      for (int i = 0; i < cnt; ++i) nb += l[3 + 2 * i] - l[2 + 2 * i] + 1;
-      return nb;
-    };
+    const int2* L = lists + (fam == 0 ? 0 : (kListBytes / 8) * n_qt);
+    int2* ord = order + (fam == 0 ? 0 : n_qt);
     for (int q0 = 0; q0 < n; q0 += kThreads) {
       const int q = q0 + threadIdx.x;
-      const int mine = q < n ? blocks_of(q) : 0;
+      const int mine = q < n ? L[(kListBytes / 8) * q].y : 0;
       int rank = 0;
       for (int c0 = 0; c0 < n; c0 += 2048) {
         const int cn = min(2048, n - c0);
         __syncthreads();
-        for (int i = threadIdx.x; i < cn; i += kThreads) s_nb[i] = blocks_of(c0 + i);
+        for (int i = threadIdx.x; i < cn; i += kThreads) s_nb[i] = L[(kListBytes / 8) * (c0 + i)].y;
         __syncthreads();
         if (q < n)
           for (int i = 0; i < cn; ++i) {
@@ -232,7 +229,7 @@ partition_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup
             rank += (o > mine || (o == mine && c0 + i < q)) ? 1 : 0;
           }
       }
-      if (q < n) L[(kListBytes / 4) * rank + 1] = q;
+      if (q < n) ord[rank] = make_int2(q, mine);
     }
   }
 }

@@ -87,8 +87,9 @@ def test_valid_end_and_pairs_match_oracle(lib, wl):
 def test_meta_and_workspace_sizes(lib):
     # header + segments (2n+2) + row tables + one 64-byte list per 128-row
     # query tile and per 128-key block
-    assert api.cp_meta_bytes(3, 128, 2) == 64 + 32 * 8 + 8 * 64 + 64 * (1 + 1)
-    assert api.cp_meta_bytes(3, 1000, 4) == (64 + 32 * 8 + 8 * 250 + 15) // 16 * 16 + 64 * (2 + 8)
+    # header, segments, row tables, then per tile a 64-byte block list and an 8-byte order entry
+    assert api.cp_meta_bytes(3, 128, 2) == 64 + 32 * 8 + 8 * 64 + (64 + 8) * (1 + 1)
+    assert api.cp_meta_bytes(3, 1000, 4) == (64 + 32 * 8 + 8 * 250 + 15) // 16 * 16 + (64 + 8) * (2 + 8)
     assert api.cp_meta_bytes(-1, 64, 1) == 0
     assert api.cp_meta_bytes(3, 65, 2) == 0
     assert api.cp_attn_bwd_workspace_bytes(8192, 16) == 8192 * 16 * 4

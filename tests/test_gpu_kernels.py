@@ -31,6 +31,8 @@ def _check_block_lists(meta, h, lo, hi, T, cap=7):
     n_qt, n_kb = -(-s_local // 128), -(-T // 128)
     raw = meta[lists_off:lists_off + 64 * (n_qt + n_kb)].cpu().numpy().view(np.int32)
     raw = raw.reshape(n_qt + n_kb, 16)
+    ord_off = lists_off + 64 * (n_qt + n_kb)
+    orders = meta[ord_off:ord_off + 8 * (n_qt + n_kb)].cpu().numpy().view(np.int32).reshape(-1, 2)
     want_q = [set() for _ in range(n_qt)]
     want_k = [set() for _ in range(n_kb)]
     for t in range(s_local):
@@ -38,7 +40,7 @@ def _check_block_lists(meta, h, lo, hi, T, cap=7):
             for b in range(lo[t] // 128, hi[t] // 128 + 1):
                 want_q[t // 128].add(b)
                 want_k[b].add(t // 128)
-    for fam, want in ((raw[:n_qt], want_q), (raw[n_qt:], want_k)):
+    for fam, want, order in ((raw[:n_qt], want_q, orders[:n_qt]), (raw[n_qt:], want_k, orders[n_qt:])):
         counts = []
         for q, l in enumerate(fam):
             n = min(int(l[0]), cap)
@@ -51,9 +53,11 @@ def _check_block_lists(meta, h, lo, hi, T, cap=7):
             else:                      # over capacity the last interval widens
                 assert want[q] <= got
             counts.append(len(got))
-        order = fam[:, 1]
-        assert sorted(order.tolist()) == list(range(len(fam)))
-        keys = [(-counts[o], o) for o in order]
+            assert l[1] == len(got)        # header: {count, blocks covered}
+        tiles = order[:, 0]
+        assert sorted(tiles.tolist()) == list(range(len(fam)))
+        assert [counts[t] for t in tiles] == order[:, 1].tolist()
+        keys = [(-counts[t], t) for t in tiles]
         assert keys == sorted(keys)    # heaviest first, ties by index
 
 
