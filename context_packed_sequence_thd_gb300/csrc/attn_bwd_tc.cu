@@ -497,6 +497,17 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 // dK / dV
 // ===========================================================================
 constexpr int kStg = 2;  // Q/dO stages of attn_dkdv_tc
+// attn_dkdv_tc runs 16 warps: 0-7 compute, 8-11 epilogue, 12 TMA producer,
+// 13 TMEM allocator + MMA issuer, 14-15 idle.  Registers per thread after the
+// split: compute 168, epilogue 96, the rest 80 (block total 65,536, the
+// 512 x 128 it is launched with).
+constexpr int kKvThr = 512;
+constexpr int kKvEpi0 = 8, kKvProducer = 12, kKvMma = 13;
+constexpr int kKvLaunchRegs = 128;
+constexpr uint32_t kRegsCompute = 168, kRegsEpi = 96, kRegsRest = 80;
+static_assert(8 * 32 * kRegsCompute + 4 * 32 * kRegsEpi + 4 * 32 * kRegsRest <=
+                  kKvThr * kKvLaunchRegs, "register split exceeds the launch allocation");
+constexpr int kEpiThreads = 128;
 
 template <int D>
 struct KvLayout {
@@ -522,12 +533,13 @@ struct KvCtl {
   uint64_t k_full, k_free, v_full, v_free;  // single K and V tiles of the item
   uint64_t q_full[kStg], qi_full[kStg], q_empty[kStg];
   uint64_t s_full, dp_full, p_full, ds_full, done, mma_done;
+  uint64_t dv_free, dk_free;  // the epilogue warps have read the item's dV / dK out of TMEM
   uint32_t tmem;
   int abort;
 };
 // per-warp staging of the dK / dV epilogue follows KvCtl (16-byte aligned)
 __host__ __device__ constexpr int kv_ctl_bytes() { return (int)((sizeof(KvCtl) + 15) & ~(size_t)15); }
-constexpr int kStageBytes = 8 * 32 * 16 * 4;  // 8 compute warps x 32 rows x 16 fp32
+constexpr int kStageBytes = 4 * 32 * 32 * 4;  // 4 epilogue warps x 32 rows x 32 fp32
 
 
 // Per query step i the MMA thread issues S^T_i, then the previous step's
@@ -538,7 +550,7 @@ constexpr int kStageBytes = 8 * 32 * 16 * 4;  // 8 compute warps x 32 rows x 16 
 // S^T_{i+1} only after it has consumed p_full(i), so no per-step barrier gets
 // two phases ahead of its waiter.
 template <int D>
-__global__ void __launch_bounds__(kThr, 1)
+__global__ void __launch_bounds__(kKvThr, 1)
 attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
              const BwdArgs a) {
@@ -575,9 +587,11 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     mbar_init(bar_addr(c.ds_full), kCompute);
     mbar_init(bar_addr(c.done), 1);
     mbar_init(bar_addr(c.mma_done), 1);
+    mbar_init(bar_addr(c.dv_free), kEpiThreads);
+    mbar_init(bar_addr(c.dk_free), kEpiThreads);
     fence_barrier_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kKvMma) {
     tmem_alloc(smem_u32(&c.tmem), kCols);
     tmem_relinquish();
   }
@@ -585,8 +599,11 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c.tmem;  // S^T [0,128) dP^T [128,256) dK [256,256+D) dV [256+D,256+2D)
-
-  if (warp == kProducerWarp) {
+  // Each warpgroup changes its register budget first thing in its own branch
+  // (all four warps of a warpgroup execute the same setmaxnreg).
+  if (warp >= kKvProducer) {
+    reg_dealloc<kRegsRest>();
+    if (warp == kKvProducer) {
     // all 32 lanes: lane 0 issues TMA, every lane loads per-query data
     int ii = 0, gs = 0, nk = 0, nv = 0;  // items, Q/dO steps, K and V tiles issued
     bool ok = true;
@@ -683,7 +700,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       for (int i = max(0, gs - kStg); i < gs; ++i)
         mbar_wait(bar_addr(c.q_full[i % kStg]), (i / kStg) & 1, &never, kLimitNs);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kKvMma) {
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
@@ -695,11 +712,16 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const uint64_t dsc_qmn = sdesc_sw128(sb + L::Q, kBox, 1024);
       const uint64_t dsc_domn = sdesc_sw128(sb + L::DO, kBox, 1024);
       int ii = 0, gs = 0;
-      int pend = -1, pend_st = 0;  // step whose dK product is still to be issued
+      int pend = -1, pend_st = 0, pend_item = 0;  // step whose dK product is still to be issued
       bool pend_first = false;
-      // dK += dS^T Q : A = dS^T (TMEM over dP^T), B = Q tile as MN-major
+      // dK += dS^T Q : A = dS^T (TMEM over dP^T), B = Q tile as MN-major.  An
+      // item's first dK starts dK afresh: the epilogue warps must have read the
+      // previous item's dK out of TMEM first.
       auto issue_dk = [&]() -> bool {
         if (!mbar_wait(bar_addr(c.ds_full), pend & 1, &s_abort, kLimitNs)) return false;
+        if (pend_first && pend_item > 0 &&
+            !mbar_wait(bar_addr(c.dk_free), (pend_item - 1) & 1, &s_abort, kLimitNs))
+          return false;
         tc_fence_after();
         const uint64_t bq = sdesc_add(dsc_qmn, pend_st * L::TILE);
 #pragma unroll
@@ -761,13 +783,16 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           }
           umma_commit(bar_addr(c.dp_full));
           if (i == it.nb - 1) umma_commit(bar_addr(c.v_free));
-          if (!mbar_wait(bar_addr(c.p_full), gs & 1, &s_abort, kLimitNs)) {
+          if (!mbar_wait(bar_addr(c.p_full), gs & 1, &s_abort, kLimitNs) ||
+              (i == 0 && cur > 0 &&
+               !mbar_wait(bar_addr(c.dv_free), (cur - 1) & 1, &s_abort, kLimitNs))) {
             fail(&s_abort);
             ok = false;
             break;
           }
           tc_fence_after();
-          // dV += P^T dO : A = P^T (TMEM over S^T), B = dO tile as MN-major (N = d)
+          // dV += P^T dO : A = P^T (TMEM over S^T), B = dO tile as MN-major (N = d);
+          // an item's first dV starts afresh once the previous dV has been read out
           const uint64_t bdm = sdesc_add(dsc_domn, st * L::TILE);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -776,6 +801,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           pend = gs;
           pend_st = st;
           pend_first = (i == 0);
+          pend_item = cur;
         }
         if (!ok) break;
         if (!issue_dk()) {
@@ -789,7 +815,71 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       int never = 0;
       mbar_wait(bar_addr(c.mma_done), 0, &never, kLimitNs);
     }
+    }
+  } else if (warp >= kKvEpi0) {
+    // ------------------------------------------------------------ epilogue warps 8-11
+    reg_dealloc<kRegsEpi>();
+    // Warp w reads TMEM lanes 32*(w%4).. (one key row per lane) of the finished
+    // item's dV, then dK, 32 columns at a time, releases each accumulator as
+    // soon as its last columns are in registers, and adds them into the fp32
+    // accumulators.  This item is the only writer of these rows in this launch:
+    // one fp32 add per element, done in L2 without a round trip.  Each chunk
+    // is turned around in a private shared-memory buffer first (16-byte units
+    // of row r rotated by r & 7, conflict-free both ways), so one vector
+    // reduction covers 128 contiguous bytes of 4 rows.
+    const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
+    float* stg = reinterpret_cast<float*>(smem_raw + L::BYTES + kv_ctl_bytes()) +
+                 (warp - kKvEpi0) * 32 * 32;
+    auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
+      return __all_sync(0xffffffffu, w);
+    };
+    int ii = 0;
+    for (int j = 0; j * (int)gridDim.x < n_items; ++j) {
+      const int k = snake_item(j, blockIdx.x, gridDim.x);
+      if (k >= n_items) continue;
+      Item itm;
+      itm.load(m.korder, m.klists, k, a.H, n_kb);
+      if (itm.nb == 0) continue;
+      if (!wait_warp(bar_addr(c.done), ii & 1)) {
+        fail(&s_abort);
+        break;
+      }
+      ++ii;
+      tc_fence_after();
+      const int rbase = itm.tile * 128 + (warp & 3) * 32;  // first key row of this warp
+#pragma unroll 1
+      for (int ch = 0; ch < 2 * (D / 32); ++ch) {
+        const bool is_v = ch < D / 32;  // dV first, then dK
+        const int c0 = (is_v ? ch : ch - D / 32) * 32;
+        uint32_t v[32];
+        tmem_ld32(tmem + lb + 256 + (is_v ? D : 0) + c0, v);
+        if (ch == D / 32 - 1 || ch == 2 * (D / 32) - 1) {
+          tc_fence_before();
+          mbar_arrive(bar_addr(is_v ? c.dv_free : c.dk_free));
+        }
+        const float sc = is_v ? 1.f : a.scale;
+        float* acc = is_v ? a.dv : a.dk;
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<float4*>(stg + lane * 32 + ((u ^ (lane & 7)) * 4)) =
+              make_float4(__uint_as_float(v[4 * u]) * sc, __uint_as_float(v[4 * u + 1]) * sc,
+                          __uint_as_float(v[4 * u + 2]) * sc, __uint_as_float(v[4 * u + 3]) * sc);
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int rr = (lane >> 3) + 4 * it, uu = lane & 7;
+          const float4 x =
+              *reinterpret_cast<const float4*>(stg + rr * 32 + ((uu ^ (rr & 7)) * 4));
+          const int kr = rbase + rr;
+          if (kr < a.T)
+            red_add_v4(acc + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * uu, x.x, x.y, x.z, x.w);
+        }
+      }
+    }
   } else {
+    reg_alloc<kRegsCompute>();
     const int row = (warp & 3) * 32 + lane;  // TMEM lane = key row of the block
     const int hf = warp >> 2;                // column half: queries [64hf, 64hf+64)
     const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
@@ -798,7 +888,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
       return __all_sync(0xffffffffu, w);
     };
-    int ii = 0, gs = 0;
+    int gs = 0;
     bool ok = true;
     for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
       const int k = snake_item(j, blockIdx.x, gridDim.x);
@@ -880,59 +970,11 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         mbar_arrive(bar_addr(c.ds_full));
       }
       if (!ok) break;
-      if (!wait_warp(bar_addr(c.done), ii & 1)) {
-        fail(&s_abort);
-        ok = false;
-        break;
-      }
-      ++ii;
-      tc_fence_after();
-      // This item is the only writer of these accumulator rows in this launch:
-      // one fp32 add per element, done in L2 without a round trip.  Each warp
-      // turns its 32 rows x 16 columns around in a private shared-memory
-      // buffer first, so that one vector reduction covers 64 contiguous bytes
-      // of 8 rows instead of 16 bytes of 32 rows.  The buffer's 16-byte units
-      // are rotated by (row >> 1) & 3, which keeps both the row-wise writes
-      // and the column-wise reads free of bank conflicts.
-      float* stg = reinterpret_cast<float*>(smem_raw + L::BYTES + kv_ctl_bytes()) + warp * 512;
-      const int rbase = itm.tile * 128 + (warp & 3) * 32;  // first key row of this warp
-#pragma unroll
-      for (int cq = 0; cq < D / 64; ++cq) {
-        const int col = hf * (D / 2) + cq * 32;  // this half's dK / dV columns
-        uint32_t gk[32], gv[32];
-        tmem_ld32(tmem + lb + 256 + col, gk);
-        tmem_ld32(tmem + lb + 256 + D + col, gv);
-#pragma unroll
-        for (int part = 0; part < 4; ++part) {  // dK, dK, dV, dV: 16 columns each
-          const uint32_t* src = (part < 2 ? gk : gv) + (part & 1) * 16;
-          const float sc = part < 2 ? a.scale : 1.f;
-          float* acc = part < 2 ? a.dk : a.dv;
-          const int c0 = col + (part & 1) * 16;
-          __syncwarp();
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<float4*>(stg + lane * 16 + ((u ^ ((lane >> 1) & 3)) * 4)) =
-                make_float4(__uint_as_float(src[4 * u]) * sc, __uint_as_float(src[4 * u + 1]) * sc,
-                            __uint_as_float(src[4 * u + 2]) * sc,
-                            __uint_as_float(src[4 * u + 3]) * sc);
-          __syncwarp();
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            const int rr = (lane >> 2) + 8 * it, uu = lane & 3;
-            const float4 v =
-                *reinterpret_cast<const float4*>(stg + rr * 16 + ((uu ^ ((rr >> 1) & 3)) * 4));
-            const int kr = rbase + rr;
-            if (kr < a.T)
-              red_add_v4(acc + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * uu, v.x, v.y, v.z, v.w);
-          }
-        }
-      }
-      tc_fence_before();
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kKvMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kCols);
   }
@@ -959,7 +1001,15 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
   attn_dq_tc<D><<<(int)(q_items < sms ? q_items : sms), kThr, dq_smem, s>>>(mq, mdo, mk, mv, a);
   if ((st = cpthd_host::launch_status()) != CP_OK) return st;
   const int64_t k_items = n_tiles_of(a.T) * (int64_t)a.H;
-  attn_dkdv_tc<D><<<(int)(k_items < sms ? k_items : sms), kThr, kv_smem, s>>>(mq, mdo, mk, mv, a);
+  // the register split inside attn_dkdv_tc assumes exactly kKvLaunchRegs per thread at launch
+  static int kv_regs = -1;
+  if (kv_regs < 0) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, attn_dkdv_tc<D>) != cudaSuccess) return CP_ERR_CUDA;
+    kv_regs = fa.numRegs;
+  }
+  if (kv_regs != kKvLaunchRegs) return CP_ERR_UNSUPPORTED;
+  attn_dkdv_tc<D><<<(int)(k_items < sms ? k_items : sms), kKvThr, kv_smem, s>>>(mq, mdo, mk, mv, a);
   return cpthd_host::launch_status();
 }
 

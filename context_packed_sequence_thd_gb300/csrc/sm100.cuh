@@ -163,6 +163,18 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
+// Register reallocation between warpgroups (executed by all four warps of a
+// warpgroup).  The increases draw on what the decreases released; the block's
+// total stays the registers it was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
 // ----------------------------------------------------------------------------
 // UMMA (tcgen05.mma, one CTA)
 // ----------------------------------------------------------------------------
