@@ -45,6 +45,8 @@ _SIGNATURES = {
     "cp_attn_bwd_workspace_bytes": ([_I64, _I], _SZ),
     "cp_attn_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
                      ctypes.c_float, _P, _SZ, _P], _I),
+    "cp_attn_bwd_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
+                        ctypes.c_float, _I, _P, _SZ, _P], _I),
     "cp_attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I,
                              _I, ctypes.c_float, _P], _I),
     "cp_device_status": ([ctypes.POINTER(_I), _I], _I),
@@ -231,18 +233,25 @@ def cp_attn_fwd(q_local, k_full, v_full, o_local, lse_local, d_meta, total_token
     _check("cp_attn_fwd", st)
 
 
+BWD_ACCUMULATE, BWD_STORE = 0, 1
+
+
 def cp_attn_bwd(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local, dk_accum,
                 dv_accum, d_meta, total_tokens: int, cp_size: int, rank: int, strategy: int,
-                softmax_scale: float, d_workspace, stream=None) -> None:
+                softmax_scale: float, d_workspace, stream=None, mode: int = BWD_ACCUMULATE) -> None:
+    """cp_attn_bwd (mode BWD_ACCUMULATE) or cp_attn_bwd_ex with the given mode."""
     _, H, D = k_full.shape
-    st = lib().cp_attn_bwd(_dev(q_local, "q"), _dev(k_full, "k"), _dev(v_full, "v"),
-                           _dev(o_local, "o"), _dev(lse_local, "lse"), _dev(do_local, "do"),
-                           _dev(dq_local, "dq"), _dev(dk_accum, "dk"), _dev(dv_accum, "dv"),
-                           _dev(d_meta, "meta"), d_meta.numel() * d_meta.element_size(),
-                           total_tokens, H, D, cp_size, rank, strategy, float(softmax_scale),
-                           _dev(d_workspace, "workspace"),
-                           d_workspace.numel() * d_workspace.element_size(), _stream(stream))
-    _check("cp_attn_bwd", st)
+    args = (_dev(q_local, "q"), _dev(k_full, "k"), _dev(v_full, "v"),
+            _dev(o_local, "o"), _dev(lse_local, "lse"), _dev(do_local, "do"),
+            _dev(dq_local, "dq"), _dev(dk_accum, "dk"), _dev(dv_accum, "dv"),
+            _dev(d_meta, "meta"), d_meta.numel() * d_meta.element_size(),
+            total_tokens, H, D, cp_size, rank, strategy, float(softmax_scale))
+    tail = (_dev(d_workspace, "workspace"), d_workspace.numel() * d_workspace.element_size(),
+            _stream(stream))
+    if mode == BWD_ACCUMULATE:
+        _check("cp_attn_bwd", lib().cp_attn_bwd(*args, *tail))
+    else:
+        _check("cp_attn_bwd_ex", lib().cp_attn_bwd_ex(*args, int(mode), *tail))
 
 
 NOALLOC_MAX_SCRATCH_FLOATS = 1048576  # CP_NOALLOC_MAX_SCRATCH_FLOATS in cpthd.h

@@ -122,12 +122,14 @@ extern "C" size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H) {
   return (size_t)s_local * H * sizeof(float);
 }
 
-extern "C" int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full,
-                           const void* o_local, const float* lse_local, const void* do_local,
-                           void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
-                           size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
-                           int rank, cp_strategy_t strategy, float softmax_scale,
-                           void* d_workspace, size_t workspace_bytes, void* stream) {
+extern "C" int cp_attn_bwd_ex(const void* q_local, const void* k_full, const void* v_full,
+                              const void* o_local, const float* lse_local, const void* do_local,
+                              void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
+                              size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
+                              int rank, cp_strategy_t strategy, float softmax_scale,
+                              cp_bwd_mode_t mode, void* d_workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (mode != CP_BWD_ACCUMULATE && mode != CP_BWD_STORE) return CP_ERR_INVALID_ARG;
   int64_t s_local = 0;
   int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
                          rank, strategy, &s_local);
@@ -159,7 +161,18 @@ extern "C" int cp_attn_bwd(const void* q_local, const void* k_full, const void* 
   return cpthd_attn_bwd_tc(q_local, k_full, v_full, do_local, lse_local, a.delta, dq_local,
                            dk_accum, dv_accum, d_meta, meta_bytes, (int)total_tokens, H, D,
                            (int)s_local, cp_size, rank, (int)strategy, softmax_scale,
-                           softmax_scale * kLog2e, s);
+                           softmax_scale * kLog2e, mode == CP_BWD_STORE ? 1 : 0, s);
+}
+
+extern "C" int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full,
+                           const void* o_local, const float* lse_local, const void* do_local,
+                           void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
+                           size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
+                           int rank, cp_strategy_t strategy, float softmax_scale,
+                           void* d_workspace, size_t workspace_bytes, void* stream) {
+  return cp_attn_bwd_ex(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local, dk_accum,
+                        dv_accum, d_meta, meta_bytes, total_tokens, H, D, cp_size, rank, strategy,
+                        softmax_scale, CP_BWD_ACCUMULATE, d_workspace, workspace_bytes, stream);
 }
 
 extern "C" int cpthd_status_attn(int reset) {
@@ -240,5 +253,5 @@ extern "C" int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, cons
   return cpthd_attn_bwd_tc(q_local, k_full, v_full, do_local, lse_local, a.delta, dq_local,
                            dk_accum, dv_accum, d_meta, meta_bytes, (int)total_tokens, H, D,
                            (int)s_local, cp_size, rank, (int)strategy, softmax_scale,
-                           softmax_scale * kLog2e, s);
+                           softmax_scale * kLog2e, 0, s);
 }

@@ -67,6 +67,7 @@ struct BwdArgs {
   size_t meta_bytes;
   int T, H, s_local, cp, rank, strategy;
   float scale, scale_log2;
+  int store;  // dK/dV partials stored (every row written) instead of added
 };
 
 __device__ __forceinline__ bool meta_ok_bwd(const BwdArgs& a, const MetaHeader* h) {
@@ -840,7 +841,25 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       if (k >= n_items) continue;
       Item itm;
       itm.load(m.korder, m.klists, k, a.H, n_kb);
-      if (itm.nb == 0) continue;
+      if (itm.nb == 0) {
+        // no query of this rank attends these keys: a stored partial is zero
+        if (a.store) {
+          const int rb = itm.tile * 128 + (warp & 3) * 32;
+          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32)
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int kr = rb + (lane >> 3) + 4 * it;
+              if (kr < a.T) {
+                const int64_t o = ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * (lane & 7);
+                *reinterpret_cast<float4*>(a.dk + o) = z;
+                *reinterpret_cast<float4*>(a.dv + o) = z;
+              }
+            }
+        }
+        continue;
+      }
       if (!wait_warp(bar_addr(c.done), ii & 1)) {
         fail(&s_abort);
         break;
@@ -873,8 +892,15 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           const float4 x =
               *reinterpret_cast<const float4*>(stg + rr * 32 + ((uu ^ (rr & 7)) * 4));
           const int kr = rbase + rr;
-          if (kr < a.T)
-            red_add_v4(acc + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * uu, x.x, x.y, x.z, x.w);
+          if (kr < a.T) {
+            float* dst = acc + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * uu;
+            if (a.store)  // p + 0: the value the first addition into a cleared buffer gives
+              *reinterpret_cast<float4*>(dst) =
+                  make_float4(__fadd_rn(x.x, 0.f), __fadd_rn(x.y, 0.f), __fadd_rn(x.z, 0.f),
+                              __fadd_rn(x.w, 0.f));
+            else
+              red_add_v4(dst, x.x, x.y, x.z, x.w);
+          }
         }
       }
     }
@@ -1022,7 +1048,7 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
                       const float* lse, const float* delta, void* dq, float* dk, float* dv,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale, float scale_log2,
-                      cudaStream_t s) {
+                      int store, cudaStream_t s) {
   using namespace cpthd;
   BwdArgs a{};
   a.lse = lse;
@@ -1035,6 +1061,7 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
   a.T = T; a.H = H; a.s_local = s_local; a.cp = cp; a.rank = rank; a.strategy = strategy;
   a.scale = scale;
   a.scale_log2 = scale_log2;
+  a.store = store;
   return D == 64 ? launch_bwd_tc<64>(q, k, v, dout, a, s) : launch_bwd_tc<128>(q, k, v, dout, a, s);
 }
 

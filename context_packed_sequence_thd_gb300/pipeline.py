@@ -232,15 +232,17 @@ class CPAttention:
         return k_full, v_full
 
     def backward(self, k_full, v_full, stream=None):
+        """Every rank's backward; rank 0 stores its partial dK/dV into the fp32
+        accumulators (no clearing pass), the others add theirs in rank order:
+        the emulated reduce-scatter's sum."""
         p = self.plan
-        if api.cp_zero_tail([self.dk_acc, self.dv_acc], 0, stream=stream):
-            self.launches += 1
         for r in range(p.cp):
             with self._timed("attn_bwd", stream):
                 api.cp_attn_bwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
                                 self.lse[r], p.local(self.doc, r), p.local(self.dqc, r),
                                 self.dk_acc, self.dv_acc, p.ranks[r].meta, p.T, p.cp, r,
-                                p.strategy, p.scale, self.ws, stream)
+                                p.strategy, p.scale, self.ws, stream,
+                                mode=api.BWD_STORE if r == 0 else api.BWD_ACCUMULATE)
             self.launches += 3
         for r, rm in enumerate(p.ranks):
             with self._timed("reduce_scatter_emul", stream):

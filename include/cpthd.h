@@ -200,15 +200,38 @@ size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H);
  * o_local / lse_local from the forward and do_local [s_local,H,D] bf16.
  * Writes dq_local [s_local,H,D] bf16 (overwritten) and ADDS this rank's
  * partial dK/dV into dk_accum / dv_accum (fp32 [T,H,D], original order; zero
- * them before rank 0 -- e.g. cp_zero_tail with valid_end = 0).  Calling the
- * ranks in a fixed order on one stream gives a bitwise deterministic sum (no
- * atomics).  d_workspace: cp_attn_bwd_workspace_bytes bytes of device scratch,
- * contents need not be initialised. */
+ * them before rank 0 -- e.g. cp_zero_tail with valid_end = 0 -- or start the
+ * sum with cp_attn_bwd_ex in CP_BWD_STORE mode).  Each element receives
+ * exactly one fp32 addition per call, so calling the ranks in a fixed order
+ * on one stream gives a bitwise deterministic sum.  d_workspace:
+ * cp_attn_bwd_workspace_bytes bytes of device scratch, contents need not be
+ * initialised. */
 int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full, const void* o_local,
                 const float* lse_local, const void* do_local, void* dq_local, float* dk_accum,
                 float* dv_accum, const void* d_meta, size_t meta_bytes, int64_t total_tokens,
                 int H, int D, int cp_size, int rank, cp_strategy_t strategy, float softmax_scale,
                 void* d_workspace, size_t workspace_bytes, void* stream);
+
+/* How cp_attn_bwd_ex delivers this rank's partial dK/dV to dk_accum / dv_accum. */
+typedef enum {
+  CP_BWD_ACCUMULATE = 0, /* add into the buffers (cp_attn_bwd) */
+  CP_BWD_STORE = 1       /* store into the buffers, every row written */
+} cp_bwd_mode_t;
+
+/* cp_attn_bwd with a choice of mode.  CP_BWD_STORE writes every element of
+ * dk_accum / dv_accum (rows that no query of this rank attends get +0.0), so
+ * the first rank of the emulated reduce-scatter needs no cleared buffers: the
+ * sum started by CP_BWD_STORE on one rank and continued by CP_BWD_ACCUMULATE
+ * on the others, in a fixed order on one stream, is bitwise the sum over
+ * cleared buffers (a stored partial is p + 0.0, like the first addition).
+ * Same arguments, results and errors as cp_attn_bwd otherwise; an unknown
+ * mode returns CP_ERR_INVALID_ARG. */
+int cp_attn_bwd_ex(const void* q_local, const void* k_full, const void* v_full,
+                   const void* o_local, const float* lse_local, const void* do_local,
+                   void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
+                   size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size, int rank,
+                   cp_strategy_t strategy, float softmax_scale, cp_bwd_mode_t mode,
+                   void* d_workspace, size_t workspace_bytes, void* stream);
 
 /* Largest Delta scratch cp_attn_bwd_noalloc can use: s_local*H <= this many
  * floats (4 MiB of device memory per GPU that loads the library). */

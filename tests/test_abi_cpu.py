@@ -138,6 +138,10 @@ def test_argument_validation_before_launch(lib):
     assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 127, 2, 64, 2, 0, 0, f(0.1), None) == -2
     assert L.cp_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64,
                          2, 0, 0, f(0.1), FAKE, 8, None) == -6
+    assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
+                            64, 2, 0, 0, f(0.1), 7, FAKE, 1 << 20, None) == -1    # unknown mode
+    assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
+                            64, 2, 0, 0, f(0.1), 1, FAKE, 8, None) == -6           # store mode, small workspace
     assert L.cp_reduce_scatter_emul(_arr(FAKE), _arr(FAKE), 1, None, 0, 10, 5, 2, 64, None) == -1
 
 

@@ -108,6 +108,38 @@ def test_rank_partial_accumulators():
         assert_close(to_np(att.dv_acc), dv_p, f"dV partial through rank {r}")
 
 
+@pytest.mark.parametrize("strategy", [pipeline.DCS, pipeline.NLB], ids=["dcs", "nlb"])
+def test_store_mode_starts_the_sum_bitwise(strategy):
+    """Rank 0 in store mode over NaN-filled accumulators, then ranks 1.. adding,
+    gives bitwise the accumulators of clear-then-add-all: every element is
+    written, and the stored partial is what the first addition would give."""
+    d = dev()
+    wl = inputs.custom([200, 56, 128, 640], cp=4, H=2, D=64, seed=71)
+    plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, 0, wl.H, wl.D, d)
+    att = pipeline.CPAttention(plan)
+    g = {k: v.to(d) for k, v in wl.tensors().items()}
+    att.shard_inputs(g["q"], g["k"], g["v"], g["do"])
+    kf, vf = att.forward()
+
+    def run(first_mode):
+        for r in range(wl.cp):
+            api.cp_attn_bwd(plan.local(att.qc, r), kf, vf, plan.local(att.oc, r), att.lse[r],
+                            plan.local(att.doc, r), plan.local(att.dqc, r), att.dk_acc, att.dv_acc,
+                            plan.ranks[r].meta, plan.T, plan.cp, r, plan.strategy, plan.scale,
+                            att.ws, mode=first_mode if r == 0 else api.BWD_ACCUMULATE)
+        torch.cuda.synchronize()
+        return att.dk_acc.clone(), att.dv_acc.clone()
+
+    api.cp_zero_tail([att.dk_acc, att.dv_acc], 0)
+    want = run(api.BWD_ACCUMULATE)
+    att.dk_acc.fill_(float("nan"))
+    att.dv_acc.fill_(float("nan"))
+    got = run(api.BWD_STORE)
+    assert api.cp_device_status() == 0
+    for w, x in zip(want, got):
+        assert torch.equal(w.view(torch.int32), x.view(torch.int32))
+
+
 def test_document_isolation_bitwise():
     """Perturbing the other documents' K/V leaves a document's O, LSE and dQ
     bitwise unchanged on the GPU."""
