@@ -300,16 +300,23 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       int pend = -1;  // block whose dQ product is still to be issued
       bool pend_first = false;
       // dQ += dS K : A = dS (bf16 pairs in TMEM), B = K tile as MN-major (N = d)
-      auto issue_dq = [&]() -> bool {
-        if (!mbar_wait(bar_addr(c.ds_full), pend & 1, &s_abort, kLimitNs)) return false;
+      // Barrier phases of the next group, tested (without blocking) while the
+      // current group is still being issued; a phase seen complete needs no wait.
+      bool seen_k = false, seen_s = false, seen_ds = false, seen_v = false;
+      auto issue_dq = [&](int vs_next, int g_next) -> bool {
+        if (!seen_ds && !mbar_wait(bar_addr(c.ds_full), pend & 1, &s_abort, kLimitNs)) return false;
+        seen_ds = false;
         tc_fence_after();
         const int ks = pend % kDqKStages;
         const uint64_t bk = sdesc_add(dsc_kmn, ks * L::TILE);
         const uint32_t ads = tmem + dq_ds_col<D>(pend & 1);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        for (int kk = 0; kk < 8; ++kk) {
           umma_bf16_ts(tmem + 256, ads + (kk >> 2) * 32 + (kk & 3) * 8, sdesc_add(bk, kk * 2048), idQ,
                        (!pend_first || kk > 0) ? 1u : 0u);
+          if (kk == 4 && vs_next >= 0 && !seen_v)
+            seen_v = mbar_test_wait(bar_addr(c.v_full[vs_next]), (g_next / kDqVStages) & 1);
+        }
         umma_commit(bar_addr(c.k_empty[ks]));
         return true;
       };
@@ -328,38 +335,52 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         for (int j = 0; j < it.nb; ++j, ++g) {
           const int ks = g % kDqKStages, vs = g % kDqVStages;
           // S_g overwrites S_{g-1}: the compute warps must have read it
-          if (!mbar_wait(bar_addr(c.k_full[ks]), (g / kDqKStages) & 1, &s_abort, kLimitNs) ||
-              (g > 0 && !mbar_wait(bar_addr(c.s_free), (g - 1) & 1, &s_abort, kLimitNs))) {
+          if ((!seen_k &&
+               !mbar_wait(bar_addr(c.k_full[ks]), (g / kDqKStages) & 1, &s_abort, kLimitNs)) ||
+              (g > 0 && !seen_s &&
+               !mbar_wait(bar_addr(c.s_free), (g - 1) & 1, &s_abort, kLimitNs))) {
             fail(&s_abort);
             ok = false;
             break;
           }
+          seen_k = seen_s = false;
           tc_fence_after();
           const uint64_t bk = sdesc_add(dsc_k, ks * L::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = kmajor_off(kk);
             umma_bf16(tmem, sdesc_add(dsc_q, off), sdesc_add(bk, off), idS, kk > 0);
+            if (kk == D / 32) {
+              if (pend >= 0) seen_ds = mbar_test_wait(bar_addr(c.ds_full), pend & 1);
+              seen_v = mbar_test_wait(bar_addr(c.v_full[vs]), (g / kDqVStages) & 1);
+            }
           }
           umma_commit(bar_addr(c.s_full));
           // dQ of the previous block (waits for its dS; that also means the
           // compute warps have read dP_{g-1}, which dP_g overwrites)
-          if (pend >= 0 && !issue_dq()) {
+          if (pend >= 0 && !issue_dq(vs, g)) {
             fail(&s_abort);
             ok = false;
             break;
           }
-          if (!mbar_wait(bar_addr(c.v_full[vs]), (g / kDqVStages) & 1, &s_abort, kLimitNs)) {
+          if (!seen_v &&
+              !mbar_wait(bar_addr(c.v_full[vs]), (g / kDqVStages) & 1, &s_abort, kLimitNs)) {
             fail(&s_abort);
             ok = false;
             break;
           }
+          seen_v = false;
           tc_fence_after();
           const uint64_t bv = sdesc_add(dsc_v, vs * L::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = kmajor_off(kk);
             umma_bf16(tmem + 128, sdesc_add(dsc_do, off), sdesc_add(bv, off), idS, kk > 0);
+            if (kk == D / 32) {  // the next block's S: its K tile, and S_g read out
+              const int gn = g + 1;
+              seen_k = mbar_test_wait(bar_addr(c.k_full[gn % kDqKStages]), (gn / kDqKStages) & 1);
+              seen_s = mbar_test_wait(bar_addr(c.s_free), g & 1);
+            }
           }
           umma_commit(bar_addr(c.dp_full));
           umma_commit(bar_addr(c.v_empty[vs]));
@@ -369,7 +390,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         if (!ok) break;
         // the item's last dQ product, then its epilogue may read dQ
-        if (!issue_dq()) {
+        if (!issue_dq(-1, 0)) {
           fail(&s_abort);
           break;
         }
