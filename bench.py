@@ -207,10 +207,10 @@ def run_own(args):
         ach = bwd_flop_per_call / (bwd_ms * 1e-3) / 1e12
     else:
         ach = fwd_flop_per_call / (fwd_ms * 1e-3) / 1e12
-    # gather bandwidth: partition gather of Q/K/V/dO (DCS) + K/V restore
+    # gather bandwidth: partition gather of Q/K/V/dO for every rank (DCS) + K/V restore
     row_bytes = wl.H * wl.D * 2
     pg = per.get("partition_gather", [])
-    pg_bytes = 4 * 2 * wl.s_local * row_bytes + 4 * wl.s_local
+    pg_bytes = 4 * 2 * wl.total_tokens * row_bytes + 4 * wl.total_tokens  # all ranks, one launch
     rg = per.get("restore_gather", [])
     rg_bytes = 2 * 2 * wl.total_tokens * row_bytes + 4 * wl.total_tokens
     gather_gbs = pg_bytes / (statistics.mean(pg) * 1e-3) / 1e9 if pg else None

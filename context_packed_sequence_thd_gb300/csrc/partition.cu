@@ -23,6 +23,7 @@ static __device__ int g_status_partition;
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kNbCap = 4096;  // block counts kept in shared memory (16 KB)
 
 // Block-wide exclusive scan of v; *total receives the block sum.  All threads
 // of the block must call it.
@@ -62,6 +63,7 @@ partition_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup
   __shared__ int s_err;
   __shared__ int s_valid_end;
   __shared__ int s_carry_segs, s_carry_rows;
+  __shared__ int s_nb[kNbCap];
 
   MetaHeader* hdr = reinterpret_cast<MetaHeader*>(meta);
   Segment* segs = reinterpret_cast<Segment*>(meta + seg_offset_bytes());
@@ -183,11 +185,13 @@ partition_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup
     }
   }
 
-  // pass 3: block lists (from the segment table written above)
+  // pass 3: block lists (from the segment table written above); each list's
+  // block count is also kept in shared memory when both families fit
   __syncthreads();
   const MetaView mv = meta_view(meta);
   const int n_qt = (int)n_tiles_of(s_local);
   const int n_kb = (int)n_tiles_of(T);
+  const bool counts_in_smem = n_qt + n_kb <= kNbCap;
   int2* lists = reinterpret_cast<int2*>(meta + lists_offset_bytes(n_docs, s_local));
   for (int q = threadIdx.x; q < n_qt + n_kb; q += kThreads) {
     int2* out = lists + (kListBytes / 8) * q;
@@ -202,32 +206,42 @@ partition_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup
     int nb = 0;
     for (int i = 0; i < min(cnt, kListCap); ++i) nb += out[1 + i].y - out[1 + i].x + 1;
     out[0] = make_int2(cnt, nb);
+    if (counts_in_smem) s_nb[q] = nb;
   }
 
   // pass 4: heaviest-first work order of each list family, {tile, blocks}
-  // (a rank by comparison against every other tile, block counts staged in
-  // shared memory; stable for equal counts)
+  // (a rank by comparison against every other tile of the family; stable for
+  // equal counts).  Counts come from shared memory, or, for very long
+  // sequences, are staged there from the lists in chunks.
   __syncthreads();
-  __shared__ int s_nb[2048];
   int2* order = lists + (kListBytes / 8) * (n_qt + n_kb);
   for (int fam = 0; fam < 2; ++fam) {
     const int n = fam == 0 ? n_qt : n_kb;
-    const int2* L = lists + (fam == 0 ? 0 : (kListBytes / 8) * n_qt);
-    int2* ord = order + (fam == 0 ? 0 : n_qt);
+    const int base = fam == 0 ? 0 : n_qt;
+    int2* ord = order + base;
     for (int q0 = 0; q0 < n; q0 += kThreads) {
       const int q = q0 + threadIdx.x;
-      const int mine = q < n ? L[(kListBytes / 8) * q].y : 0;
+      const int mine = q < n ? lists[(kListBytes / 8) * (base + q)].y : 0;
       int rank = 0;
-      for (int c0 = 0; c0 < n; c0 += 2048) {
-        const int cn = min(2048, n - c0);
-        __syncthreads();
-        for (int i = threadIdx.x; i < cn; i += kThreads) s_nb[i] = L[(kListBytes / 8) * (c0 + i)].y;
-        __syncthreads();
+      if (counts_in_smem) {
         if (q < n)
-          for (int i = 0; i < cn; ++i) {
-            const int o = s_nb[i];
-            rank += (o > mine || (o == mine && c0 + i < q)) ? 1 : 0;
+          for (int i = 0; i < n; ++i) {
+            const int o = s_nb[base + i];
+            rank += (o > mine || (o == mine && i < q)) ? 1 : 0;
           }
+      } else {
+        for (int c0 = 0; c0 < n; c0 += kNbCap) {
+          const int cn = min(kNbCap, n - c0);
+          __syncthreads();
+          for (int i = threadIdx.x; i < cn; i += kThreads)
+            s_nb[i] = lists[(kListBytes / 8) * (base + c0 + i)].y;
+          __syncthreads();
+          if (q < n)
+            for (int i = 0; i < cn; ++i) {
+              const int o = s_nb[i];
+              rank += (o > mine || (o == mine && c0 + i < q)) ? 1 : 0;
+            }
+        }
       }
       if (q < n) ord[rank] = make_int2(q, mine);
     }

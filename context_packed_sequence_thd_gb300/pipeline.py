@@ -94,6 +94,7 @@ class CPPlan:
     device: torch.device
     d_cu: torch.Tensor = field(init=False)
     d_cup: torch.Tensor = field(init=False)
+    idx_all: torch.Tensor = field(init=False)
     restore: torch.Tensor = field(init=False)
     ranks: List[RankMeta] = field(init=False)
 
@@ -106,11 +107,14 @@ class CPPlan:
         self.d_cu = torch.from_numpy(self.cu).to(self.device)
         self.d_cup = torch.from_numpy(self.cup).to(self.device)
         self.restore = torch.empty(self.T, dtype=torch.int32, device=self.device)
+        # the ranks' partition indices side by side: rank r's is rows
+        # [r*s_local, (r+1)*s_local), so idx_all indexes the rank-concatenated buffers
+        self.idx_all = torch.empty(self.T, dtype=torch.int32, device=self.device)
         nbytes = api.cp_meta_bytes(self.n_docs, self.T, self.cp)
         self.ranks = []
         for r in range(self.cp):
             self.ranks.append(RankMeta(
-                idx=torch.empty(self.s_local, dtype=torch.int32, device=self.device),
+                idx=self.local(self.idx_all, r),
                 meta=torch.empty(nbytes, dtype=torch.uint8, device=self.device),
                 valid_end=api.cp_valid_end(self.cu, self.cup, self.cp, r, self.strategy, self.pad),
                 pairs=rank_pairs(self.cu, self.cup, self.cp, r, self.strategy, self.pad)))
@@ -200,14 +204,13 @@ class CPAttention:
             if do is not None:
                 self.doc = do
             return
+        # every rank's shard in one gather: the rank-concatenated buffer is the
+        # input gathered by the ranks' indices side by side
         srcs = [q, k, v] + ([do] if do is not None else [])
-        for r, rm in enumerate(p.ranks):
-            dsts = [p.local(self.qc, r), p.local(self.kc, r), p.local(self.vc, r)]
-            if do is not None:
-                dsts.append(p.local(self.doc, r))
-            with self._timed("partition_gather", stream):
-                api.cp_thd_gather(srcs, dsts, rm.idx, stream)
-            self.launches += 1
+        dsts = [self.qc, self.kc, self.vc] + ([self.doc] if do is not None else [])
+        with self._timed("partition_gather", stream):
+            api.cp_thd_gather(srcs, dsts, p.idx_all, stream)
+        self.launches += 1
 
     def restore_kv(self, stream=None):
         """All-gather (free: shards are side by side) + restore to original order."""
@@ -244,17 +247,14 @@ class CPAttention:
                                 p.strategy, p.scale, self.ws, stream,
                                 mode=api.BWD_STORE if r == 0 else api.BWD_ACCUMULATE)
             self.launches += 3
+        # the scatter half of the reduce-scatter for every rank in one launch:
+        # rank r's rows of the rank-concatenated dK/dV are the summed
+        # accumulators at its partition index (NO_LOAD_BALANCE: contiguous)
+        with self._timed("reduce_scatter_emul", stream):
+            api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc], [self.dkc, self.dvc],
+                                       p.idx_all if p.strategy == DCS else None, 0, p.T, stream)
+        self.launches += 1
         for r, rm in enumerate(p.ranks):
-            with self._timed("reduce_scatter_emul", stream):
-                if p.strategy == DCS:
-                    api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc],
-                                               [p.local(self.dkc, r), p.local(self.dvc, r)],
-                                               rm.idx, 0, p.s_local, stream)
-                else:
-                    api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc],
-                                               [p.local(self.dkc, r), p.local(self.dvc, r)],
-                                               None, r * p.s_local, p.s_local, stream)
-            self.launches += 1
             if api.cp_zero_tail([p.local(self.dqc, r), p.local(self.dkc, r), p.local(self.dvc, r)],
                                 rm.valid_end, stream=stream):
                 self.launches += 1
