@@ -320,6 +320,34 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         umma_commit(bar_addr(c.k_empty[ks]));
         return true;
       };
+      // S_g = Q K_g^T into TMEM columns [0,128).  S_g overwrites S_{g-1}: the
+      // compute warps must have read it (s_free), and K_g must have landed.
+      auto issue_s = [&](int gs_) -> bool {
+        const int ks = gs_ % kDqKStages, vs = gs_ % kDqVStages;
+        if ((!seen_k &&
+             !mbar_wait(bar_addr(c.k_full[ks]), (gs_ / kDqKStages) & 1, &s_abort, kLimitNs)) ||
+            (gs_ > 0 && !seen_s &&
+             !mbar_wait(bar_addr(c.s_free), (gs_ - 1) & 1, &s_abort, kLimitNs)))
+          return false;
+        seen_k = seen_s = false;
+        tc_fence_after();
+        const uint64_t bk = sdesc_add(dsc_k, ks * L::TILE);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = kmajor_off(kk);
+          umma_bf16(tmem, sdesc_add(dsc_q, off), sdesc_add(bk, off), idS, kk > 0);
+          if (kk == D / 32) {  // the next groups' barriers: dS of the pending block, V_g
+            if (pend >= 0) seen_ds = mbar_test_wait(bar_addr(c.ds_full), pend & 1);
+            seen_v = mbar_test_wait(bar_addr(c.v_full[vs]), (gs_ / kDqVStages) & 1);
+          }
+        }
+        umma_commit(bar_addr(c.s_full));
+        return true;
+      };
+      // Order per key block g: [S_g issued earlier], dQ_{g-1}, dP_g, S_{g+1}.  The
+      // next block's S goes in right after dP_g -- before the buffer-release
+      // commits and the loop bookkeeping -- so the tensor pipe has queued work
+      // while this thread competes for issue slots with the compute warps.
       bool ok = true;
       for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
         const int k = snake_item(j, blockIdx.x, gridDim.x);
@@ -332,30 +360,12 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           break;
         }
         ++ii;
+        if (!issue_s(g)) {  // the item's first S
+          fail(&s_abort);
+          break;
+        }
         for (int j = 0; j < it.nb; ++j, ++g) {
-          const int ks = g % kDqKStages, vs = g % kDqVStages;
-          // S_g overwrites S_{g-1}: the compute warps must have read it
-          if ((!seen_k &&
-               !mbar_wait(bar_addr(c.k_full[ks]), (g / kDqKStages) & 1, &s_abort, kLimitNs)) ||
-              (g > 0 && !seen_s &&
-               !mbar_wait(bar_addr(c.s_free), (g - 1) & 1, &s_abort, kLimitNs))) {
-            fail(&s_abort);
-            ok = false;
-            break;
-          }
-          seen_k = seen_s = false;
-          tc_fence_after();
-          const uint64_t bk = sdesc_add(dsc_k, ks * L::TILE);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = kmajor_off(kk);
-            umma_bf16(tmem, sdesc_add(dsc_q, off), sdesc_add(bk, off), idS, kk > 0);
-            if (kk == D / 32) {
-              if (pend >= 0) seen_ds = mbar_test_wait(bar_addr(c.ds_full), pend & 1);
-              seen_v = mbar_test_wait(bar_addr(c.v_full[vs]), (g / kDqVStages) & 1);
-            }
-          }
-          umma_commit(bar_addr(c.s_full));
+          const int vs = g % kDqVStages;
           // dQ of the previous block (waits for its dS; that also means the
           // compute warps have read dP_{g-1}, which dP_g overwrites)
           if (pend >= 0 && !issue_dq(vs, g)) {
@@ -383,10 +393,15 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             }
           }
           umma_commit(bar_addr(c.dp_full));
-          umma_commit(bar_addr(c.v_empty[vs]));
-          if (j == it.nb - 1) umma_commit(bar_addr(c.qd_free));
           pend = g;
           pend_first = (j == 0);
+          if (j + 1 < it.nb && !issue_s(g + 1)) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
+          umma_commit(bar_addr(c.v_empty[vs]));
+          if (j == it.nb - 1) umma_commit(bar_addr(c.qd_free));
         }
         if (!ok) break;
         // the item's last dQ product, then its epilogue may read dQ
