@@ -40,6 +40,7 @@ _SIGNATURES = {
     "cp_thd_gather": ([_P, _P, _I, _P, _I64, _I64, _I64, _P], _I),
     "cp_thd_scatter": ([_P, _P, _I, _P, _I64, _I64, _I64, _P], _I),
     "cp_reduce_scatter_emul": ([_P, _P, _I, _P, _I64, _I64, _I64, _I, _I, _P], _I),
+    "cp_a2a_exchange": ([_P, _P, _I, _P, _I64, _I, _I, _I, _I, _P], _I),
     "cp_zero_tail": ([_P, _I, _I64, _I64, _I64, _P, _P, ctypes.POINTER(_I)], _I),
     "cp_attn_fwd": ([_P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I, ctypes.c_float, _P], _I),
     "cp_attn_bwd_workspace_bytes": ([_I64, _I], _SZ),
@@ -197,6 +198,21 @@ def cp_thd_scatter(srcs: Sequence[torch.Tensor], dsts: Sequence[torch.Tensor],
                               _dev(d_idx, "idx"), n_rows, dst_rows, _row_bytes(srcs[0]),
                               _stream(stream))
     _check("cp_thd_scatter", st)
+
+
+A2A_SEQ_TO_HEAD, A2A_HEAD_TO_SEQ = 0, 1
+
+
+def cp_a2a_exchange(srcs: Sequence[torch.Tensor], dsts: Sequence[torch.Tensor],
+                    d_perm: Optional[torch.Tensor], cp_size: int, direction: int,
+                    stream=None) -> None:
+    """Sequence side [T, H, D] <-> head side [cp, T, H/cp, D] (see cp_a2a_exchange)."""
+    seq = srcs[0] if direction == A2A_SEQ_TO_HEAD else dsts[0]
+    T, H, D = seq.shape
+    st = lib().cp_a2a_exchange(_ptr_array(srcs, "src"), _ptr_array(dsts, "dst"), len(srcs),
+                               _dev(d_perm, "perm") if d_perm is not None else None, T, cp_size,
+                               H, D, int(direction), _stream(stream))
+    _check("cp_a2a_exchange", st)
 
 
 def cp_reduce_scatter_emul(accums: Sequence[torch.Tensor], dsts: Sequence[torch.Tensor],

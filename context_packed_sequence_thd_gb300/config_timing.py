@@ -1,4 +1,5 @@
-"""Per-workload attention throughput of the C-ABI entry points (GB300).
+"""Per-workload attention throughput of the C-ABI entry points (GB300), and
+the emulated a2a comm type (exchange GB/s, attention TFLOP/s).
 
     python -m context_packed_sequence_thd_gb300.config_timing
 
@@ -9,7 +10,7 @@ events over 10 repetitions after one warm-up pass, reported as algorithmic TFLOP
 """
 import torch
 
-from . import inputs, pipeline
+from . import api, inputs, pipeline
 
 
 def run(wl, strategies, label, bwd=True, reps=10, dev=None):
@@ -45,12 +46,75 @@ def run(wl, strategies, label, bwd=True, reps=10, dev=None):
     return rows
 
 
+def a2a_exchange(T, cp, H, D, strategy, reps=20, dev=None):
+    """GB/s of the seq->head exchange of Q, K and V (the a2a page's before_attn
+    exchange) for one document of T tokens; under DUAL_CHUNK_SWAP the restore
+    reorder is part of the same pass."""
+    dev = dev or torch.device("cuda", torch.cuda.current_device())
+    wl = inputs.custom([T], cp=cp, H=H, D=D, seed=7)
+    plan = pipeline.CPPlan(wl.cu, wl.cup, cp, strategy, 0, H, D, dev)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    seq = [torch.randn(T, H, D, generator=g).bfloat16().to(dev) for _ in range(3)]
+    head = [torch.empty(cp, T, H // cp, D, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    perm = plan.restore if strategy == pipeline.DCS else None
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # larger than L2
+    api.cp_a2a_exchange(seq, head, perm, cp, api.A2A_SEQ_TO_HEAD)
+    ms = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        api.cp_a2a_exchange(seq, head, perm, cp, api.A2A_SEQ_TO_HEAD)
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    ms.sort()
+    t = ms[len(ms) // 2]
+    nbytes = 3 * 2 * T * H * D * 2 + (4 * T if perm is not None else 0)
+    gbs = nbytes / (t * 1e-3) / 1e9
+    name = "dual_chunk_swap" if strategy == pipeline.DCS else "no_load_balance"
+    print(f"a2a q+k+v exchange, s={T:6d} cp={cp} H={H} D={D} {name:16s}: "
+          f"{t * 1e3:8.1f} us  {gbs:7.1f} GB/s", flush=True)
+    return t, gbs
+
+
+def run_a2a(wl, strategies, label, reps=10, dev=None):
+    """Forward / backward TFLOP/s of the emulated a2a comm type (exchanges included)."""
+    dev = dev or torch.device("cuda", torch.cuda.current_device())
+    t = {k: v.to(dev) for k, v in wl.tensors(with_grad=True).items()}
+    for s in strategies:
+        plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, s, wl.pad_between_seqs, wl.H, wl.D, dev)
+        att = pipeline.CPA2AAttention(plan)
+        att.shard_inputs(t["q"], t["k"], t["v"], t["do"])
+        att.forward()
+        att.backward()
+        torch.cuda.synchronize()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        for _ in range(reps):
+            att.forward()
+        e[1].record()
+        for _ in range(reps):
+            att.backward()
+        e[2].record()
+        torch.cuda.synchronize()
+        f = att.flops(True)
+        tf = f["fwd"] / (e[0].elapsed_time(e[1]) / reps) / 1e9
+        tb = f["bwd"] / (e[1].elapsed_time(e[2]) / reps) / 1e9
+        print(f"{label:32s} a2a strategy {s}: fwd {tf:7.1f} TFLOP/s   bwd {tb:7.1f} TFLOP/s",
+              flush=True)
+
+
 def main():
     run(inputs.cfg2(), (pipeline.DCS, pipeline.NLB), "cfg2 32k tokens, 16 docs, cp4 H16")
     run(inputs.custom([32768], cp=1, H=16, D=128, seed=5), (pipeline.NLB,), "one 32k doc, cp1 H16")
     run(inputs.custom([32768], cp=8, H=16, D=128, seed=5), (pipeline.DCS, pipeline.NLB),
         "one 32k doc, cp8 H16")
     run(inputs.cfg3(), (pipeline.DCS, pipeline.NLB), "cfg3 32k seq, cp8 H40", bwd=False)
+    run_a2a(inputs.cfg2(), (pipeline.DCS, pipeline.NLB), "cfg2 32k tokens, 16 docs, cp4 H16")
+    for T in (8192, 32768, 75600):
+        for s in (pipeline.DCS, pipeline.NLB):
+            a2a_exchange(T, 8, 40, 128, s)
 
 
 if __name__ == "__main__":

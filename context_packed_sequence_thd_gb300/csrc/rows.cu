@@ -5,6 +5,8 @@
 // context-parallel regression when padded cu_seqlens are value-equal but not
 // object-identical" (§Describe the bug, §Expected behavior).
 //
+// Also the all-to-all exchange of the a2a comm type (see a2a_kernel).
+//
 // Design: one warp moves one row at a time; lanes stride over the row's
 // 16-byte chunks with several independent loads in flight before the stores
 // (rows are 256 B .. 10 KB).  Up to four tensors share one index load and one
@@ -65,6 +67,46 @@ rows_kernel(Ptrs p, int n_tensors, const int32_t* __restrict__ idx, int64_t n_ro
     const int64_t di = MODE == 0 ? i : j;
     for (int k = 0; k < n_tensors; ++k)
       copy_row(p.src[k] + si * chunks, p.dst[k] + di * chunks, chunks, lane);
+  }
+}
+
+// All-to-all exchange of the a2a comm type ("[PyTorch] Extend no-load-balance
+// CP to the a2a comm type", ¶1-2 and §Diagram), every rank on one GPU.  The
+// sequence side is the rank-concatenated buffer [T, H, D] (rank r's token
+// shard is rows [r*s_local, (r+1)*s_local)); the head side is cp buffers
+// [T, H/cp, D] side by side (rank r: all tokens in original order, heads
+// [r*H/cp, (r+1)*H/cp)).  Token g of the head side lives at sequence-side row
+// perm[g] (the restore index under DUAL_CHUNK_SWAP, so the dual-chunk reorder
+// is part of the same pass), or row g when perm is null (flat sharding: the
+// rank-concatenated order already is the original order).
+// DIR 0 (seq -> head): head[r][g] = seq[perm(g)][slice r]
+// DIR 1 (head -> seq): seq[perm(g)][slice r] = head[r][g]
+// One warp per (token, rank) unit, units token-major so that consecutive
+// warps move consecutive slices of one sequence-side row.
+template <int DIR>
+__global__ void __launch_bounds__(kRowThreads)
+a2a_kernel(Ptrs p, int n_tensors, const int32_t* __restrict__ perm, int64_t T, int cp,
+           int slice_chunks, int row_chunks) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t(blockIdx.x) * kRowThreads + threadIdx.x) >> 5;
+  const int64_t n_warps = (int64_t(gridDim.x) * kRowThreads) >> 5;
+  const int64_t units = T * cp;
+  for (int64_t u = warp; u < units; u += n_warps) {
+    const int64_t g = u / cp;
+    const int r = (int)(u - g * cp);
+    const int64_t pos = perm ? (int64_t)perm[g] : g;
+    if (pos < 0 || pos >= T) {
+      if (lane == 0) atomicCAS(&g_status_rows, 0, CP_ERR_INVALID_ARG);
+      continue;
+    }
+    const int64_t seq_off = pos * row_chunks + (int64_t)r * slice_chunks;
+    const int64_t head_off = ((int64_t)r * T + g) * slice_chunks;
+    for (int k = 0; k < n_tensors; ++k) {
+      if (DIR == 0)
+        copy_row(p.src[k] + seq_off, p.dst[k] + head_off, slice_chunks, lane);
+      else
+        copy_row(p.src[k] + head_off, p.dst[k] + seq_off, slice_chunks, lane);
+    }
   }
 }
 
@@ -236,6 +278,35 @@ extern "C" int cp_zero_tail(void* const* d_rows, int n_tensors, int64_t rows, in
   zero_tail_kernel<<<(int)grid, kRowThreads, 0, cpthd_host::as_stream(stream)>>>(
       p, n_tensors, rows, valid_end, valid_end >= 0 ? nullptr : d_valid_end, chunks);
   if (launched) *launched = 1;
+  return cpthd_host::launch_status();
+}
+
+extern "C" int cp_a2a_exchange(const void* const* d_src, void* const* d_dst, int n_tensors,
+                               const int32_t* d_perm, int64_t total_tokens, int cp_size, int H,
+                               int D, cp_a2a_dir_t dir, void* stream) {
+  if (cp_size < 1 || H < 1 || D < 1 || H % cp_size) return CP_ERR_INVALID_ARG;
+  if (dir != CP_A2A_SEQ_TO_HEAD && dir != CP_A2A_HEAD_TO_SEQ) return CP_ERR_INVALID_ARG;
+  if (total_tokens < 0 || total_tokens > INT32_MAX) return CP_ERR_INVALID_ARG;
+  const int64_t slice_bytes = (int64_t)(H / cp_size) * D * 2;
+  int st = validate_rows(d_src, reinterpret_cast<const void* const*>(d_dst), n_tensors,
+                         total_tokens, slice_bytes);
+  if (st != CP_OK) return st;
+  if (total_tokens == 0) return CP_OK;
+  Ptrs p{};
+  for (int k = 0; k < n_tensors; ++k) {
+    p.src[k] = reinterpret_cast<const uint4*>(d_src[k]);
+    p.dst[k] = reinterpret_cast<uint4*>(d_dst[k]);
+  }
+  const int slice_chunks = (int)(slice_bytes / 16);
+  const int row_chunks = slice_chunks * cp_size;
+  const int grid = grid_for(total_tokens * cp_size, 1);
+  cudaStream_t s = cpthd_host::as_stream(stream);
+  if (dir == CP_A2A_SEQ_TO_HEAD)
+    a2a_kernel<0><<<grid, kRowThreads, 0, s>>>(p, n_tensors, d_perm, total_tokens, cp_size,
+                                                slice_chunks, row_chunks);
+  else
+    a2a_kernel<1><<<grid, kRowThreads, 0, s>>>(p, n_tensors, d_perm, total_tokens, cp_size,
+                                                slice_chunks, row_chunks);
   return cpthd_host::launch_status();
 }
 

@@ -279,3 +279,91 @@ class CPAttention:
         if bwd:
             f["bwd"] = 10.0 * p.D * p.H * pairs
         return f
+
+
+class CPA2AAttention(CPAttention):
+    """The a2a comm type with every rank on one GPU ("[PyTorch] Extend
+    no-load-balance CP to the a2a comm type", ¶1-2, §Diagram).
+
+    Token shards come from the plan's partition (gathered under
+    DUAL_CHUNK_SWAP, views under NO_LOAD_BALANCE).  The seq->head exchange gives
+    rank r the whole sequence with heads [r*H/cp, (r+1)*H/cp) -- under
+    DUAL_CHUNK_SWAP the restore reorder is folded into that pass, under flat
+    sharding there is none -- so every rank's attention uses cp_size = 1
+    metadata for the whole packed sequence, and owns the full dQ/dK/dV of its
+    heads (no reduction).  The head->seq exchange brings outputs and gradients
+    back to token shards.
+    """
+
+    def __init__(self, plan: CPPlan):
+        super().__init__(plan)
+        p = plan
+        if p.H % p.cp:
+            raise ValueError("the a2a comm type needs H divisible by cp_size")
+        dev, T, D = p.device, p.T, p.D
+        self.Hc = p.H // p.cp
+        # cp = 1 metadata of the whole packed sequence, for every rank's head slice
+        self.full = CPPlan(p.cu, p.cup, 1, NLB, p.pad, self.Hc, D, dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        shape = (p.cp, T, self.Hc, D)
+        self.qh, self.kh, self.vh, self.doh = (torch.empty(shape, **bf) for _ in range(4))
+        self.oh, self.dqh, self.dkh, self.dvh = (torch.empty(shape, **bf) for _ in range(4))
+        self.lse_h = torch.empty(p.cp, self.Hc, T, dtype=torch.float32, device=dev)
+        self.acc_k = torch.empty(T, self.Hc, D, dtype=torch.float32, device=dev)
+        self.acc_v = torch.empty(T, self.Hc, D, dtype=torch.float32, device=dev)
+        ws = api.cp_attn_bwd_workspace_bytes(T, self.Hc)
+        self.ws_h = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+
+    def _perm(self):
+        return self.plan.restore if self.plan.strategy == DCS else None
+
+    def forward(self, stream=None):
+        p = self.plan
+        with self._timed("a2a_exchange", stream):
+            api.cp_a2a_exchange([self.qc, self.kc, self.vc], [self.qh, self.kh, self.vh],
+                                self._perm(), p.cp, api.A2A_SEQ_TO_HEAD, stream)
+        self.launches += 1
+        for r in range(p.cp):
+            with self._timed("attn_fwd", stream):
+                api.cp_attn_fwd(self.qh[r], self.kh[r], self.vh[r], self.oh[r], self.lse_h[r],
+                                self.full.ranks[0].meta, p.T, 1, 0, NLB, p.scale, stream)
+            self.launches += 1
+        with self._timed("a2a_exchange", stream):
+            api.cp_a2a_exchange([self.oh], [self.oc], self._perm(), p.cp, api.A2A_HEAD_TO_SEQ,
+                                stream)
+        self.launches += 1
+        return None, None
+
+    def backward(self, k_full=None, v_full=None, stream=None):
+        p = self.plan
+        with self._timed("a2a_exchange", stream):
+            api.cp_a2a_exchange([self.doc], [self.doh], self._perm(), p.cp, api.A2A_SEQ_TO_HEAD,
+                                stream)
+        self.launches += 1
+        for r in range(p.cp):
+            with self._timed("attn_bwd", stream):
+                api.cp_attn_bwd(self.qh[r], self.kh[r], self.vh[r], self.oh[r], self.lse_h[r],
+                                self.doh[r], self.dqh[r], self.acc_k, self.acc_v,
+                                self.full.ranks[0].meta, p.T, 1, 0, NLB, p.scale, self.ws_h,
+                                stream, mode=api.BWD_STORE)
+            self.launches += 3
+            with self._timed("grad_cast", stream):
+                api.cp_reduce_scatter_emul([self.acc_k, self.acc_v], [self.dkh[r], self.dvh[r]],
+                                           None, 0, p.T, stream)
+            self.launches += 1
+        with self._timed("a2a_exchange", stream):
+            api.cp_a2a_exchange([self.dqh, self.dkh, self.dvh], [self.dqc, self.dkc, self.dvc],
+                                self._perm(), p.cp, api.A2A_HEAD_TO_SEQ, stream)
+        self.launches += 1
+        for r, rm in enumerate(p.ranks):
+            if api.cp_zero_tail([p.local(self.dqc, r), p.local(self.dkc, r), p.local(self.dvc, r)],
+                                rm.valid_end, stream=stream):
+                self.launches += 1
+
+    def step(self, q, k, v, do=None, stream=None, rebuild_index: bool = True):
+        if rebuild_index:
+            self.launches += self.plan.build_index(stream) + self.full.build_index(stream)
+        self.shard_inputs(q, k, v, do, stream)
+        self.forward(stream)
+        if do is not None:
+            self.backward(stream=stream)

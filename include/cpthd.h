@@ -163,6 +163,35 @@ int cp_reduce_scatter_emul(const float* const* d_accum, void* const* d_dst, int 
                            const int32_t* d_idx, int64_t row0, int64_t n_rows,
                            int64_t accum_rows, int H, int D, void* stream);
 
+/* Direction of cp_a2a_exchange. */
+typedef enum {
+  CP_A2A_SEQ_TO_HEAD = 0, /* before attention: token shards -> full sequence, head slice */
+  CP_A2A_HEAD_TO_SEQ = 1  /* after attention: full sequence, head slice -> token shards */
+} cp_a2a_dir_t;
+
+/* All-to-all exchange of the a2a comm type ("[PyTorch] Extend no-load-balance
+ * CP to the a2a comm type", ¶1-2, §Diagram), every rank on one GPU.  After the
+ * exchange each rank holds the whole sequence and only its own head slice, so
+ * its attention uses cp_size = 1 metadata.
+ *   sequence side: [T, H, D] rank-concatenated buffer (rank r's token shard
+ *     is rows [r*T/cp, (r+1)*T/cp)).
+ *   head side: cp buffers [T, H/cp, D] side by side ([cp, T, H/cp, D]); rank
+ *     r's holds every token in original order and heads [r*H/cp, (r+1)*H/cp).
+ *   d_perm (device int32 [T], nullable): sequence-side row of original token
+ *     g -- the restore index of DUAL_CHUNK_SWAP, which folds the dual-chunk
+ *     reorder into the same pass; NULL for flat (NO_LOAD_BALANCE) sharding,
+ *     whose rank-concatenated order already is the original order.  It must
+ *     be a permutation of [0, T); a value outside is skipped and sets the
+ *     device status word.
+ * SEQ_TO_HEAD reads d_src[k] (sequence side) and writes d_dst[k] (head side);
+ * HEAD_TO_SEQ the reverse.  d_src / d_dst: host arrays of n_tensors (<= 4)
+ * device pointers, 16-byte aligned; (H/cp)*D*2 must be a multiple of 16 and H
+ * a multiple of cp_size (else CP_ERR_ALIGNMENT / CP_ERR_INVALID_ARG before any
+ * launch).  Bit copy.  Destinations must not overlap sources. */
+int cp_a2a_exchange(const void* const* d_src, void* const* d_dst, int n_tensors,
+                    const int32_t* d_perm, int64_t total_tokens, int cp_size, int H, int D,
+                    cp_a2a_dir_t dir, void* stream);
+
 /* Gradient tail-zeroing ([P2P] §Describe the bug, last paragraph; §Expected
  * behavior: gated when no tail exists, graph-safe).  Zeroes rows
  * [valid_end, rows) of each of n_tensors (<= 4) tensors of row_bytes-long rows.

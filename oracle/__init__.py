@@ -141,6 +141,31 @@ def scatter_rows(dst: np.ndarray, idx: np.ndarray, src: np.ndarray) -> np.ndarra
     return out
 
 
+def a2a_seq_to_head(seq: np.ndarray, cp: int, perm=None) -> np.ndarray:
+    """All-to-all before attention ("[PyTorch] Extend no-load-balance CP to the
+    a2a comm type", ¶2 and §Diagram): from the rank-concatenated token shards
+    [T, H, D] to cp head slices [cp, T, H/cp, D], rank r holding every token in
+    original order with heads [r*H/cp, (r+1)*H/cp).  Original token g sits at
+    sequence-side row perm[g] (the restore index for DUAL_CHUNK_SWAP; identity
+    for flat sharding when perm is None)."""
+    T, H = seq.shape[0], seq.shape[1]
+    rows = np.arange(T) if perm is None else np.asarray(perm, dtype=np.int64)
+    ordered = seq[rows]                        # [T, H, ...] in original order
+    hc = H // cp
+    return np.stack([ordered[:, r * hc:(r + 1) * hc] for r in range(cp)])
+
+
+def a2a_head_to_seq(head: np.ndarray, perm=None) -> np.ndarray:
+    """The reverse exchange after attention: head slices [cp, T, H/cp, D] back
+    to the rank-concatenated token shards [T, H, D]."""
+    cp, T = head.shape[0], head.shape[1]
+    ordered = np.concatenate([head[r] for r in range(cp)], axis=1)   # [T, H, ...]
+    rows = np.arange(T) if perm is None else np.asarray(perm, dtype=np.int64)
+    out = np.empty_like(ordered)
+    out[rows] = ordered
+    return out
+
+
 def pad_between_seqs(cu: Sequence[int], cup: Optional[Sequence[int]]) -> int:
     """1 when any entry of the padded offsets differs from the actual offsets."""
     if cup is None:

@@ -166,3 +166,37 @@ def test_bf16_round_nearest_even():
     np.testing.assert_array_equal(oracle.bf16_round(x), want)
     assert oracle.bf16_round(np.float32(1 + 2 ** -8)) == 0x3F80
     assert oracle.bf16_round(np.float32(1 + 3 * 2 ** -8)) == 0x3F82
+
+
+# ---------------------------------------------------------------------------
+# a2a exchange ("[PyTorch] Extend no-load-balance CP to the a2a comm type")
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("strategy", [0, 1])
+def test_a2a_exchange_restores_sequence_and_splits_heads(strategy):
+    """After the seq->head exchange of the ranks' shards, rank r holds the
+    original sequence with heads [r*H/cp, (r+1)*H/cp); the reverse exchange
+    gives the shards back (round trip = identity)."""
+    rng = np.random.default_rng(5)
+    cup = [0, 16, 48, 64]
+    cp, H = 2, 6
+    x = rng.integers(0, 2 ** 16, size=(64, H, 4), dtype=np.uint16)   # original order
+    G = np.concatenate([oracle.partition_index(cup, cp, r, strategy) for r in range(cp)])
+    seq = x[G]                                                       # rank-concatenated shards
+    perm = oracle.restore_index(cup, cp, strategy) if strategy == 0 else None
+    head = oracle.a2a_seq_to_head(seq, cp, perm)
+    assert head.shape == (cp, 64, H // cp, 4)
+    for r in range(cp):
+        np.testing.assert_array_equal(head[r], x[:, r * 3:(r + 1) * 3])
+    np.testing.assert_array_equal(oracle.a2a_head_to_seq(head, perm), seq)
+
+
+def test_a2a_flat_needs_no_reorder():
+    """Flat sharding: the rank-concatenated order is the original order, so the
+    exchange with no permutation equals the one with the identity restore."""
+    rng = np.random.default_rng(6)
+    cup = [0, 10, 40, 64]
+    x = rng.integers(0, 2 ** 16, size=(64, 4, 2), dtype=np.uint16)
+    R = oracle.restore_index(cup, 4, 1)
+    np.testing.assert_array_equal(R, np.arange(64))
+    np.testing.assert_array_equal(oracle.a2a_seq_to_head(x, 4, None), oracle.a2a_seq_to_head(x, 4, R))
