@@ -58,23 +58,42 @@ def a2a_exchange(T, cp, H, D, strategy, reps=20, dev=None):
     head = [torch.empty(cp, T, H // cp, D, dtype=torch.bfloat16, device=dev) for _ in range(3)]
     perm = plan.restore if strategy == pipeline.DCS else None
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # larger than L2
-    api.cp_a2a_exchange(seq, head, perm, cp, api.A2A_SEQ_TO_HEAD)
-    ms = []
-    for _ in range(reps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        api.cp_a2a_exchange(seq, head, perm, cp, api.A2A_SEQ_TO_HEAD)
-        e1.record()
-        torch.cuda.synchronize()
-        ms.append(e0.elapsed_time(e1))
-    ms.sort()
-    t = ms[len(ms) // 2]
+
+    def timed(fn):
+        fn()
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        ms.sort()
+        return ms[len(ms) // 2]
+
+    t = timed(lambda: api.cp_a2a_exchange(seq, head, perm, cp, api.A2A_SEQ_TO_HEAD))
     nbytes = 3 * 2 * T * H * D * 2 + (4 * T if perm is not None else 0)
     gbs = nbytes / (t * 1e-3) / 1e9
     name = "dual_chunk_swap" if strategy == pipeline.DCS else "no_load_balance"
     print(f"a2a q+k+v exchange, s={T:6d} cp={cp} H={H} D={D} {name:16s}: "
           f"{t * 1e3:8.1f} us  {gbs:7.1f} GB/s", flush=True)
+    if perm is not None:
+        # the pages' dual-chunk path: the exchange in rank order, then a
+        # separate index_select to the original order (per head slice)
+        tmp = [torch.empty_like(h) for h in head]
+        rows = (torch.arange(cp, device=dev, dtype=torch.int64)[:, None] * T +
+                perm.to(torch.int64)[None, :]).reshape(-1).to(torch.int32)
+        flat_t = [x.view(cp * T, H // cp, D) for x in tmp]
+        flat_h = [x.view(cp * T, H // cp, D) for x in head]
+
+        def unfused():
+            api.cp_a2a_exchange(seq, tmp, None, cp, api.A2A_SEQ_TO_HEAD)
+            api.cp_thd_gather(flat_t, flat_h, rows)
+        t2 = timed(unfused)
+        print(f"a2a q+k+v exchange, s={T:6d} cp={cp} H={H} D={D} {'dual_chunk_swap, exchange + separate reorder':16s}: "
+              f"{t2 * 1e3:8.1f} us  ({t2 / t:.2f}x the fused pass)", flush=True)
     return t, gbs
 
 
