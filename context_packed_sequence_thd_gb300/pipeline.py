@@ -30,7 +30,7 @@ from __future__ import annotations
 import contextlib
 import math
 from dataclasses import dataclass, field
-from typing import Dict, List, Optional
+from typing import Dict, List, Optional, Sequence
 
 import numpy as np
 import torch
@@ -367,3 +367,44 @@ class CPA2AAttention(CPAttention):
         self.forward(stream)
         if do is not None:
             self.backward(stream=stream)
+
+
+# ---------------------------------------------------------------------------
+# bshd / sbhd batches ("[PyTorch] Extend no-load-balance CP to the a2a comm
+# type", §Tests: flat a2a over bshd, sbhd and THD)
+# ---------------------------------------------------------------------------
+
+def bshd_seqlens(B: int, S: int) -> np.ndarray:
+    """cu_seqlens of a bshd batch [B, S, H, D] seen as THD: B documents of S
+    tokens, token (b, s) at row b*S + s -- the same memory, no copy."""
+    return (np.arange(B + 1, dtype=np.int64) * S).astype(np.int32)
+
+
+def sbhd_rows(B: int, S: int, device) -> Dict[str, torch.Tensor]:
+    """Row maps between an sbhd batch [S, B, H, D] (token (s, b) at row s*B + b)
+    and its THD form (row b*S + s): ``to_thd`` gathers sbhd -> THD,
+    ``to_sbhd`` gathers THD -> sbhd."""
+    b = np.arange(B)[:, None]
+    s = np.arange(S)[None, :]
+    to_thd = (s * B + b).reshape(-1)                 # THD row b*S+s reads sbhd row s*B+b
+    to_sbhd = np.empty_like(to_thd)
+    to_sbhd[to_thd] = np.arange(B * S)
+    return {k: torch.from_numpy(v.astype(np.int32)).to(device)
+            for k, v in (("to_thd", to_thd), ("to_sbhd", to_sbhd))}
+
+
+def sbhd_to_thd(xs: Sequence[torch.Tensor], rows: Dict[str, torch.Tensor], stream=None):
+    """[S, B, H, D] tensors -> THD [B*S, H, D] copies (one gather launch)."""
+    S, B = xs[0].shape[:2]
+    flat = [x.view(S * B, *x.shape[2:]) for x in xs]
+    out = [torch.empty_like(f) for f in flat]
+    api.cp_thd_gather(flat, out, rows["to_thd"], stream)
+    return out
+
+
+def thd_to_sbhd(xs: Sequence[torch.Tensor], rows: Dict[str, torch.Tensor], S: int, B: int,
+                stream=None):
+    """THD [B*S, H, D] tensors -> sbhd [S, B, H, D] copies (one gather launch)."""
+    out = [torch.empty_like(x) for x in xs]
+    api.cp_thd_gather(list(xs), out, rows["to_sbhd"], stream)
+    return [o.view(S, B, *o.shape[1:]) for o in out]

@@ -106,3 +106,50 @@ def test_a2a_forward_bitwise_matches_all_gather_forward():
     a2a.step(t["q"], t["k"], t["v"])
     torch.cuda.synchronize()
     assert torch.equal(ag.oc.view(torch.int16), a2a.oc.view(torch.int16))
+
+
+@pytest.mark.parametrize("strategy", [pipeline.DCS, pipeline.NLB], ids=["dcs", "nlb"])
+def test_a2a_bshd_and_sbhd_batches(strategy):
+    """A bshd batch is THD with B equal documents (no copy); an sbhd batch is
+    the same tokens in [S, B] order, carried to THD and back by one gather each
+    way.  Both give the oracle's result, and bitwise the same as each other."""
+    d = dev()
+    B, S, H, D, cp = 3, 256, 8, 64, 4
+    g = torch.Generator().manual_seed(91)
+    bshd = {k: torch.randn(B, S, H, D, generator=g).bfloat16() for k in ("q", "k", "v", "do")}
+    cu = pipeline.bshd_seqlens(B, S)
+    t = {k: v.reshape(B * S, H, D) for k, v in bshd.items()}          # THD view of bshd
+    o, lse = oracle.attn_fwd(t["q"], t["k"], t["v"], cu, cu, 0)
+    dq, dk, dv = oracle.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], cu, cu, 0)
+
+    def run(thd):
+        plan = pipeline.CPPlan(cu, cu, cp, strategy, 0, H, D, d)
+        att = pipeline.CPA2AAttention(plan)
+        att.step(thd["q"], thd["k"], thd["v"], thd["do"])
+        torch.cuda.synchronize()
+        assert api.cp_device_status() == 0
+        # back to original token order: rank-concatenated rows -> global rows
+        G = torch.cat([plan.ranks[r].idx.long() for r in range(cp)])
+        out = {}
+        for name, buf in (("o", att.oc), ("dq", att.dqc), ("dk", att.dkc), ("dv", att.dvc)):
+            x = torch.empty_like(buf)
+            x[G] = buf
+            out[name] = x
+        return out
+
+    got_b = run({k: v.to(d) for k, v in t.items()})
+    for name, want in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert_close(to_np(got_b[name]), want, f"bshd {name}")
+    # sbhd: the same tokens stored [S, B, H, D]
+    rows = pipeline.sbhd_rows(B, S, d)
+    sbhd = [bshd[k].transpose(0, 1).contiguous().to(d) for k in ("q", "k", "v", "do")]
+    thd = dict(zip(("q", "k", "v", "do"), pipeline.sbhd_to_thd(sbhd, rows)))
+    for k in thd:
+        assert torch.equal(thd[k].cpu().view(torch.int16), t[k].view(torch.int16))
+    got_s = run(thd)
+    back = pipeline.thd_to_sbhd([got_s["o"], got_s["dq"]], rows, S, B)
+    for name, x in zip(("o", "dq"), back):
+        assert torch.equal(x.transpose(0, 1).contiguous().view(torch.int16),
+                           got_b[name].view(B, S, H, D).view(torch.int16))
+    for name in ("dk", "dv"):
+        assert torch.equal(got_s[name].view(torch.int16), got_b[name].view(torch.int16))
