@@ -50,6 +50,9 @@ _SIGNATURES = {
                         ctypes.c_float, _I, _P, _SZ, _P], _I),
     "cp_attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I,
                              _I, ctypes.c_float, _P], _I),
+    "cp_p2p_meta_bytes": ([_I, _I64, _I], _SZ),
+    "cp_p2p_index": ([_P, _P, _I, _I64, _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "cp_p2p_merge": ([_P, _P, _I, _I64, _I, _I, _P, _P, _P], _I),
     "cp_device_status": ([ctypes.POINTER(_I), _I], _I),
 }
 
@@ -249,7 +252,7 @@ def cp_attn_fwd(q_local, k_full, v_full, o_local, lse_local, d_meta, total_token
     _check("cp_attn_fwd", st)
 
 
-BWD_ACCUMULATE, BWD_STORE = 0, 1
+BWD_ACCUMULATE, BWD_STORE, BWD_DQ_F32_STORE, BWD_DQ_F32_ACCUMULATE = 0, 1, 2, 4
 
 
 def cp_attn_bwd(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local, dk_accum,
@@ -288,6 +291,30 @@ def cp_attn_bwd_noalloc(q_local, k_full, v_full, o_local, lse_local, do_local, d
                                    total_tokens, H, D, cp_size, rank, strategy,
                                    float(softmax_scale), _stream(stream))
     _check("cp_attn_bwd_noalloc", st)
+
+
+def cp_p2p_meta_bytes(n_docs: int, total_tokens: int, cp_size: int) -> int:
+    return int(lib().cp_p2p_meta_bytes(n_docs, total_tokens, cp_size))
+
+
+def cp_p2p_index(d_cu: Optional[torch.Tensor], d_cup: torch.Tensor, total_tokens: int,
+                 cp_size: int, rank: int, strategy: int, pad_between_seqs: int,
+                 d_meta: torch.Tensor, stream=None) -> None:
+    """Metadata of all cp_size ring steps of `rank` (step i at i * cp_p2p_meta_bytes)."""
+    st = lib().cp_p2p_index(None if d_cu is None else _dev(d_cu, "cu"), _dev(d_cup, "cup"),
+                            d_cup.numel() - 1, total_tokens, cp_size, rank, strategy,
+                            pad_between_seqs, _dev(d_meta, "meta"),
+                            d_meta.numel() * d_meta.element_size(), _stream(stream))
+    _check("cp_p2p_index", st)
+
+
+def cp_p2p_merge(o_steps: torch.Tensor, lse_steps: torch.Tensor, out: torch.Tensor,
+                 lse: torch.Tensor, stream=None) -> None:
+    """o_steps [n, s_local, H, D] bf16, lse_steps [n, H, s_local] -> out, lse."""
+    n, s_local, H, D = o_steps.shape
+    st = lib().cp_p2p_merge(_dev(o_steps, "o_steps"), _dev(lse_steps, "lse_steps"), n, s_local,
+                            H, D, _dev(out, "out"), _dev(lse, "lse"), _stream(stream))
+    _check("cp_p2p_merge", st)
 
 
 def cp_device_status(reset: bool = True) -> int:

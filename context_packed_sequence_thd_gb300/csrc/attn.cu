@@ -129,7 +129,8 @@ extern "C" int cp_attn_bwd_ex(const void* q_local, const void* k_full, const voi
                               int rank, cp_strategy_t strategy, float softmax_scale,
                               cp_bwd_mode_t mode, void* d_workspace, size_t workspace_bytes,
                               void* stream) {
-  if (mode != CP_BWD_ACCUMULATE && mode != CP_BWD_STORE) return CP_ERR_INVALID_ARG;
+  const int m = (int)mode;
+  if ((m & ~7) != 0 || (m & 6) == 6) return CP_ERR_INVALID_ARG;
   int64_t s_local = 0;
   int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
                          rank, strategy, &s_local);
@@ -161,7 +162,7 @@ extern "C" int cp_attn_bwd_ex(const void* q_local, const void* k_full, const voi
   return cpthd_attn_bwd_tc(q_local, k_full, v_full, do_local, lse_local, a.delta, dq_local,
                            dk_accum, dv_accum, d_meta, meta_bytes, (int)total_tokens, H, D,
                            (int)s_local, cp_size, rank, (int)strategy, softmax_scale,
-                           softmax_scale * kLog2e, mode == CP_BWD_STORE ? 1 : 0, s);
+                           softmax_scale * kLog2e, m, s);
 }
 
 extern "C" int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full,

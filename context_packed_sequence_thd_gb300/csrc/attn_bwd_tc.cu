@@ -60,14 +60,15 @@ constexpr float kLog2ef = 1.4426950408889634f;
 struct BwdArgs {
   const float* lse;    // [H, s_local]
   const float* delta;  // [H, s_local]
-  bf16* dq;            // [s_local, H, D]
+  void* dq;            // [s_local, H, D]: bf16, or fp32 when dq_mode != 0
   float* dk;           // [T, H, D]
   float* dv;
   const void* meta;
   size_t meta_bytes;
   int T, H, s_local, cp, rank, strategy;
   float scale, scale_log2;
-  int store;  // dK/dV partials stored (every row written) instead of added
+  int store;    // dK/dV partials stored (every row written) instead of added
+  int dq_mode;  // 0: dQ stored as bf16; 1: stored as fp32; 2: added into fp32
 };
 
 __device__ __forceinline__ bool meta_ok_bwd(const BwdArgs& a, const MetaHeader* h) {
@@ -121,18 +122,6 @@ __device__ __forceinline__ uint32_t kmajor_off(int kk) { return (kk >> 2) * kBox
 // column halves: elements [0,64) at columns [0,32), [64,128) at [64,96).
 __device__ __forceinline__ uint32_t ts_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else
-      return 148;
-  }
-  return n;
-}
 
 // ===========================================================================
 // dQ
@@ -434,12 +423,17 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       itm.load(m.qorder, m.qlists, k, a.H, n_qt);
       const int t = itm.tile * 128 + row;
       const bool in = t < a.s_local;
-      if (itm.nb == 0) {  // no real query row: dQ = 0
-        if (in) {
-          uint4* dst =
-              reinterpret_cast<uint4*>(a.dq + ((int64_t)t * a.H + itm.h) * D + hf * (D / 2));
+      if (itm.nb == 0) {  // no real query row: dQ = 0 (nothing to add in add mode)
+        if (in && a.dq_mode == 0) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(a.dq) +
+                                                ((int64_t)t * a.H + itm.h) * D + hf * (D / 2));
 #pragma unroll
           for (int q = 0; q < D / 16; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+        } else if (in && a.dq_mode == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.dq) +
+                                                ((int64_t)t * a.H + itm.h) * D + hf * (D / 2));
+#pragma unroll
+          for (int q = 0; q < D / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -504,8 +498,23 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const int col = hf * (D / 2) + cq * 32;  // dQ columns of this half
         uint32_t o[32];
         tmem_ld32(tmem + lb + 256 + col, o);
-        if (in) {
-          uint4* dst = reinterpret_cast<uint4*>(a.dq + ((int64_t)t * a.H + itm.h) * D + col);
+        if (in && a.dq_mode != 0) {  // fp32 dQ: a stored value is p + 0, like a first addition
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.dq) +
+                                                  ((int64_t)t * a.H + itm.h) * D + col);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 prev = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (a.dq_mode == 2) prev = dst[q];
+            float4 v;
+            v.x = __fadd_rn(prev.x, __uint_as_float(o[q * 4 + 0]) * a.scale);
+            v.y = __fadd_rn(prev.y, __uint_as_float(o[q * 4 + 1]) * a.scale);
+            v.z = __fadd_rn(prev.z, __uint_as_float(o[q * 4 + 2]) * a.scale);
+            v.w = __fadd_rn(prev.w, __uint_as_float(o[q * 4 + 3]) * a.scale);
+            dst[q] = v;
+          }
+        } else if (in) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(a.dq) +
+                                                ((int64_t)t * a.H + itm.h) * D + col);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 v;
@@ -1058,7 +1067,7 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
       cudaFuncSetAttribute(attn_dkdv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kv_smem) != cudaSuccess)
     return CP_ERR_CUDA;
-  const int sms = sm_count();
+  const int sms = cpthd_host::sm_count();
   const int64_t q_items = n_tiles_of(a.s_local) * (int64_t)a.H;
   attn_dq_tc<D><<<(int)(q_items < sms ? q_items : sms), kThr, dq_smem, s>>>(mq, mdo, mk, mv, a);
   if ((st = cpthd_host::launch_status()) != CP_OK) return st;
@@ -1084,12 +1093,12 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
                       const float* lse, const float* delta, void* dq, float* dk, float* dv,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale, float scale_log2,
-                      int store, cudaStream_t s) {
+                      int mode, cudaStream_t s) {
   using namespace cpthd;
   BwdArgs a{};
   a.lse = lse;
   a.delta = delta;
-  a.dq = (bf16*)dq;
+  a.dq = dq;
   a.dk = dk;
   a.dv = dv;
   a.meta = meta;
@@ -1097,7 +1106,8 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
   a.T = T; a.H = H; a.s_local = s_local; a.cp = cp; a.rank = rank; a.strategy = strategy;
   a.scale = scale;
   a.scale_log2 = scale_log2;
-  a.store = store;
+  a.store = mode & 1;
+  a.dq_mode = (mode & 2) ? 1 : (mode & 4) ? 2 : 0;
   return D == 64 ? launch_bwd_tc<64>(q, k, v, dout, a, s) : launch_bwd_tc<128>(q, k, v, dout, a, s);
 }
 

@@ -601,18 +601,6 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else
-      return 148;
-  }
-  return n;
-}
 
 template <int D>
 int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, cudaStream_t s) {
@@ -626,7 +614,7 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, 
       cudaSuccess)
     return CP_ERR_CUDA;
   const int64_t items = n_tiles_of(a.s_local) * (int64_t)a.H;
-  const int grid = (int)(items < sm_count() ? items : sm_count());
+  const int grid = (int)(items < cpthd_host::sm_count() ? items : cpthd_host::sm_count());
   attn_fwd_tc<D><<<grid, kThreadsTc, smem, s>>>(mq, mk, mv, a);
   return cpthd_host::launch_status();
 }

@@ -285,6 +285,20 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 inline int launch_status() {
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
+// SMs of the current device (queried once per translation unit; 148 if the
+// query fails, which only sizes grids)
+inline int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      return 148;
+  }
+  return n;
+}
 }  // namespace cpthd_host
 
 // per-translation-unit device status word accessors (defined in each .cu)
@@ -299,9 +313,10 @@ int cpthd_attn_fwd_tc(const void* q, const void* k, const void* v, void* o, floa
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale_log2, cudaStream_t s);
 
-// tcgen05 dQ and dK/dV kernels (attn_bwd_tc.cu); Delta already in `delta`
+// tcgen05 dQ and dK/dV kernels (attn_bwd_tc.cu); Delta already in `delta`;
+// mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added)
 int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
                       const float* lse, const float* delta, void* dq, float* dk, float* dv,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale, float scale_log2,
-                      int store, cudaStream_t s);
+                      int mode, cudaStream_t s);

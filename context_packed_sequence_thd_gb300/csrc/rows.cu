@@ -167,9 +167,7 @@ zero_tail_kernel(ZeroPtrs p, int n_tensors, int64_t rows, int64_t valid_end,
 }
 
 int grid_for(int64_t rows_of_work, int warps_per_row_unit) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = cpthd_host::sm_count();
   (void)warps_per_row_unit;
   const int64_t warps = kRowThreads / 32;
   int64_t want = (rows_of_work + warps - 1) / warps;

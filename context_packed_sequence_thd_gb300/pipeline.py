@@ -369,6 +369,108 @@ class CPA2AAttention(CPAttention):
             self.backward(stream=stream)
 
 
+class CPP2PAttention(CPAttention):
+    """The P2P (ring) comm type with every rank on one GPU ("THD P2P
+    context-parallel regression when padded cu_seqlens are value-equal but not
+    object-identical", §Describe the bug: the P2P context-parallel path).
+
+    Rank r keeps its token shard (partition of the plan's strategy) and at
+    ring step i attends it to the K/V shard of rank j = (r - i) mod cp.  The
+    ranks' shards lie side by side in the rank-concatenated buffers, so the
+    ring's send/receive of K/V is a pointer offset here.  Every step is a
+    cp_size = 1 attention call with per-step metadata; all steps of a rank get
+    their metadata from one cp_p2p_index launch (instead of the per-step
+    get_cu_seqlens_on_cp_rank helper calls).  Under NO_LOAD_BALANCE the shards
+    of later ranks hold only later tokens, so rank r runs steps 0..r only.
+
+    Forward: per-step partial (O_i, LSE_i), combined by cp_p2p_merge.
+    Backward: per step with the merged O / LSE; dQ is summed over the rank's
+    steps in an fp32 buffer (first step stores, later steps add), dK/dV of
+    shard j are summed in fp32 over the ranks that attended it (the partial
+    dK/dV that travel back along the ring to their owner), the first
+    contribution to each shard stored; one launch casts all three to bf16.
+    """
+
+    def __init__(self, plan: CPPlan):
+        super().__init__(plan)
+        p = plan
+        dev, T, H, D, S = p.device, p.T, p.H, p.D, p.s_local
+        self.k_full = self.v_full = None   # no restore: attention reads the shards
+        self.step_bytes = api.cp_p2p_meta_bytes(p.n_docs, T, p.cp)
+        self.p2p_meta = [torch.empty(p.cp * self.step_bytes, dtype=torch.uint8, device=dev)
+                         for _ in range(p.cp)]
+        self.o_steps = torch.empty(p.cp, S, H, D, dtype=torch.bfloat16, device=dev)
+        self.lse_steps = torch.empty(p.cp, H, S, dtype=torch.float32, device=dev)
+        self.dq_acc = torch.empty(T, H, D, dtype=torch.float32, device=dev)
+        self.build_p2p_index()
+
+    def n_steps(self, r: int) -> int:
+        return self.plan.cp if self.plan.strategy == DCS else r + 1
+
+    def step_meta(self, r: int, i: int) -> torch.Tensor:
+        return self.p2p_meta[r][i * self.step_bytes:(i + 1) * self.step_bytes]
+
+    def build_p2p_index(self, stream=None) -> int:
+        """One cp_p2p_index launch per rank (every ring step's metadata)."""
+        p = self.plan
+        for r in range(p.cp):
+            api.cp_p2p_index(p.d_cu if p.pad else None, p.d_cup, p.T, p.cp, r, p.strategy,
+                             p.pad, self.p2p_meta[r], stream)
+        return p.cp
+
+    def forward(self, stream=None):
+        p = self.plan
+        S = p.s_local
+        for r in range(p.cp):
+            n = self.n_steps(r)
+            for i in range(n):
+                j = (r - i) % p.cp
+                with self._timed("attn_fwd", stream):
+                    api.cp_attn_fwd(p.local(self.qc, r), p.local(self.kc, j), p.local(self.vc, j),
+                                    self.o_steps[i], self.lse_steps[i], self.step_meta(r, i), S,
+                                    1, 0, p.strategy, p.scale, stream)
+                self.launches += 1
+            with self._timed("p2p_merge", stream):
+                api.cp_p2p_merge(self.o_steps[:n], self.lse_steps[:n], p.local(self.oc, r),
+                                 self.lse[r], stream)
+            self.launches += 1
+        return None, None
+
+    def backward(self, k_full=None, v_full=None, stream=None):
+        p = self.plan
+        S = p.s_local
+        written = set()
+        for r in range(p.cp):
+            for i in range(self.n_steps(r)):
+                j = (r - i) % p.cp
+                mode = api.BWD_ACCUMULATE if j in written else api.BWD_STORE
+                mode |= api.BWD_DQ_F32_STORE if i == 0 else api.BWD_DQ_F32_ACCUMULATE
+                written.add(j)
+                with self._timed("attn_bwd", stream):
+                    api.cp_attn_bwd(p.local(self.qc, r), p.local(self.kc, j), p.local(self.vc, j),
+                                    p.local(self.oc, r), self.lse[r], p.local(self.doc, r),
+                                    p.local(self.dq_acc, r), p.local(self.dk_acc, j),
+                                    p.local(self.dv_acc, j), self.step_meta(r, i), S, 1, 0,
+                                    p.strategy, p.scale, self.ws, stream, mode=mode)
+                self.launches += 3
+        with self._timed("grad_cast", stream):
+            api.cp_reduce_scatter_emul([self.dq_acc, self.dk_acc, self.dv_acc],
+                                       [self.dqc, self.dkc, self.dvc], None, 0, p.T, stream)
+        self.launches += 1
+        for r, rm in enumerate(p.ranks):
+            if api.cp_zero_tail([p.local(self.dqc, r), p.local(self.dkc, r), p.local(self.dvc, r)],
+                                rm.valid_end, stream=stream):
+                self.launches += 1
+
+    def step(self, q, k, v, do=None, stream=None, rebuild_index: bool = True):
+        if rebuild_index:
+            self.launches += self.plan.build_index(stream) + self.build_p2p_index(stream)
+        self.shard_inputs(q, k, v, do, stream)
+        self.forward(stream)
+        if do is not None:
+            self.backward(stream=stream)
+
+
 # ---------------------------------------------------------------------------
 # bshd / sbhd batches ("[PyTorch] Extend no-load-balance CP to the a2a comm
 # type", §Tests: flat a2a over bshd, sbhd and THD)

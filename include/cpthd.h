@@ -241,10 +241,13 @@ int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full, con
                 int H, int D, int cp_size, int rank, cp_strategy_t strategy, float softmax_scale,
                 void* d_workspace, size_t workspace_bytes, void* stream);
 
-/* How cp_attn_bwd_ex delivers this rank's partial dK/dV to dk_accum / dv_accum. */
+/* How cp_attn_bwd_ex delivers its gradients: one dK/dV choice (bit 0) OR'd
+ * with at most one dQ choice (bits 1-2). */
 typedef enum {
-  CP_BWD_ACCUMULATE = 0, /* add into the buffers (cp_attn_bwd) */
-  CP_BWD_STORE = 1       /* store into the buffers, every row written */
+  CP_BWD_ACCUMULATE = 0,       /* dK/dV: add into the buffers (cp_attn_bwd) */
+  CP_BWD_STORE = 1,            /* dK/dV: store into the buffers, every row written */
+  CP_BWD_DQ_F32_STORE = 2,     /* dq_local is fp32 [s_local,H,D]: stored, every row */
+  CP_BWD_DQ_F32_ACCUMULATE = 4 /* dq_local is fp32 [s_local,H,D]: added into */
 } cp_bwd_mode_t;
 
 /* cp_attn_bwd with a choice of mode.  CP_BWD_STORE writes every element of
@@ -253,14 +256,64 @@ typedef enum {
  * sum started by CP_BWD_STORE on one rank and continued by CP_BWD_ACCUMULATE
  * on the others, in a fixed order on one stream, is bitwise the sum over
  * cleared buffers (a stored partial is p + 0.0, like the first addition).
+ * Without a dQ bit dq_local is bf16 and overwritten, as in cp_attn_bwd.  The
+ * dQ bits make dq_local an fp32 buffer, for sums of several calls over the
+ * same queries (the ring steps of cp_p2p_index): CP_BWD_DQ_F32_STORE starts
+ * the sum (every row written, +0.0 where nothing is attended) and
+ * CP_BWD_DQ_F32_ACCUMULATE adds one fp32 term per element and call.
  * Same arguments, results and errors as cp_attn_bwd otherwise; an unknown
- * mode returns CP_ERR_INVALID_ARG. */
+ * bit, or both dQ bits, returns CP_ERR_INVALID_ARG. */
 int cp_attn_bwd_ex(const void* q_local, const void* k_full, const void* v_full,
                    const void* o_local, const float* lse_local, const void* do_local,
                    void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
                    size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size, int rank,
                    cp_strategy_t strategy, float softmax_scale, cp_bwd_mode_t mode,
                    void* d_workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The P2P (ring) comm type, every rank on one GPU ([P2P] §Describe the bug:
+ * the P2P context-parallel path, whose per-step sequence metadata comes from
+ * repeated get_cu_seqlens_on_cp_rank calls).  At ring step i = 0..cp_size-1
+ * rank r holds the K/V shard of rank j = (r - i) mod cp_size (its partition
+ * rows, DUAL_CHUNK_SWAP or NO_LOAD_BALANCE) and attends its own queries to
+ * it.  Under both strategies every query row sees one contiguous run of the
+ * shard's rows, so a step is a cp_size = 1 attention call:
+ *   cp_attn_fwd(q_local, k_shard_j, v_shard_j, o_i, lse_i, step meta,
+ *               total_tokens = s_local, cp_size = 1, rank = 0, strategy, ...)
+ * the steps' partial outputs are combined by cp_p2p_merge, and the backward
+ * runs per step with the merged O / LSE (dQ summed over the steps in fp32,
+ * dK/dV of shard j summed over the ranks that attended it).
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of ONE ring step's metadata (a multiple of 16); a rank's metadata is
+ * cp_size of these blocks back to back, step i at i * cp_p2p_meta_bytes.
+ * Returns 0 for invalid sizes (total_tokens not divisible by cp_size). */
+size_t cp_p2p_meta_bytes(int n_docs, int64_t total_tokens, int cp_size);
+
+/* One launch (one CTA per step): the metadata of all cp_size ring steps of
+ * rank `rank`.  Step i's block describes queries = this rank's s_local local
+ * rows, keys = the s_local local rows of rank (rank - i) mod cp_size, with
+ * header cp_size = 1, rank = 0, total_tokens = s_local and the given strategy
+ * (the values the step's attention call passes); its row tables hold each
+ * query row's first and last visible key row of the shard (0 / -1 when it sees
+ * none: padding rows, and rows whose document has no earlier key in that
+ * shard).  d_cu / d_cup / pad_between_seqs as for cp_partition_index.
+ * d_meta: >= cp_size * cp_p2p_meta_bytes bytes, 16-byte aligned.  Offsets
+ * that break the strategy's constraints set every step's header status and
+ * the device status word. */
+int cp_p2p_index(const int32_t* d_cu, const int32_t* d_cup, int n_docs, int64_t total_tokens,
+                 int cp_size, int rank, cp_strategy_t strategy, int pad_between_seqs,
+                 void* d_meta, size_t meta_bytes, void* stream);
+
+/* Combination of n_steps partial attention outputs of the same queries over
+ * disjoint key sets (the ring steps): with l_i = lse_steps[i],
+ *   lse = log(sum_i exp(l_i)),   out = sum_i exp(l_i - lse) * o_i,
+ * in fp32, out rounded to bf16 once; rows with every l_i = -inf get lse = -inf
+ * and out = 0.  d_o_steps: bf16 [n_steps, s_local, H, D]; d_lse_steps: fp32
+ * [n_steps, H, s_local] (natural log, as cp_attn_fwd writes it); d_out: bf16
+ * [s_local, H, D]; d_lse: fp32 [H, s_local].  D in {64, 128}.  One launch. */
+int cp_p2p_merge(const void* d_o_steps, const float* d_lse_steps, int n_steps, int64_t s_local,
+                 int H, int D, void* d_out, float* d_lse, void* stream);
 
 /* Largest Delta scratch cp_attn_bwd_noalloc can use: s_local*H <= this many
  * floats (4 MiB of device memory per GPU that loads the library). */

@@ -31,7 +31,7 @@ from __future__ import annotations
 import ctypes
 import os
 import subprocess
-from typing import Optional, Sequence, Tuple
+from typing import List, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -164,6 +164,91 @@ def a2a_head_to_seq(head: np.ndarray, perm=None) -> np.ndarray:
     out = np.empty_like(ordered)
     out[rows] = ordered
     return out
+
+
+def p2p_schedule(cp: int, rank: int) -> List[int]:
+    """Ring order of the P2P comm type: at step i rank ``rank`` holds the K/V
+    shard that started on rank (rank - i) mod cp (each step passes K/V one rank
+    along the ring)."""
+    return [(rank - i) % cp for i in range(cp)]
+
+
+def p2p_step_rows(cu, cup, cp: int, rank: int, kv_rank: int, strategy: int, pad: int):
+    """Keys each local query row of ``rank`` sees in ``kv_rank``'s K/V shard,
+    as inclusive ranges [lo, hi] of that shard's local rows (lo = 0, hi = -1
+    when none): brute force over the two partition indices -- key global row
+    in [document start, query row], query a real token.  Asserts that every
+    row's keys form one contiguous range of the shard."""
+    G_r = partition_index(cup, cp, rank, strategy)
+    G_j = partition_index(cup, cp, kv_rank, strategy)
+    valid = valid_mask(cu, cup, pad)
+    cup_ = np.asarray(cup, dtype=np.int64)
+    start = np.repeat(cup_[:-1], np.diff(cup_))
+    lo = np.zeros(len(G_r), dtype=np.int32)
+    hi = np.full(len(G_r), -1, dtype=np.int32)
+    for t0 in range(0, len(G_r), 512):           # 512 query rows at a time
+        g = G_r[t0:t0 + 512]
+        vis = (G_j[None, :] >= start[g][:, None]) & (G_j[None, :] <= g[:, None])
+        vis &= valid[g][:, None]
+        n = vis.sum(axis=1)
+        first = np.argmax(vis, axis=1)
+        last = len(G_j) - 1 - np.argmax(vis[:, ::-1], axis=1)
+        some = n > 0
+        assert np.all(last[some] - first[some] + 1 == n[some]), "keys of a row are not contiguous"
+        lo[t0:t0 + 512] = np.where(some, first, 0)
+        hi[t0:t0 + 512] = np.where(some, last, -1)
+    return lo, hi
+
+
+def p2p_attn_fwd(q, k, v, cu, cup, pad: int, cp: int, strategy: int, scale=None):
+    """The P2P ring's forward, step by step in fp64: at every step each rank's
+    queries attend the visible keys of the K/V shard it holds (dense softmax
+    over those keys), giving a partial (O_i, LSE_i); the partials merge as
+    LSE = log sum_i exp(LSE_i), O = sum_i exp(LSE_i - LSE) O_i.  Returns O, LSE
+    in original row order (equal to attn_fwd: the ring only reorders the sum)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, H, D = q.shape
+    sc = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    o = np.zeros((T, H, D))
+    lse = np.full((H, T), -np.inf)
+    for r in range(cp):
+        G_r = partition_index(cup, cp, r, strategy)
+        parts = []
+        for j in p2p_schedule(cp, r):
+            G_j = partition_index(cup, cp, j, strategy)
+            lo, hi = p2p_step_rows(cu, cup, cp, r, j, strategy, pad)
+            o_i = np.zeros((len(G_r), H, D))
+            l_i = np.full((H, len(G_r)), -np.inf)
+            for t in range(len(G_r)):
+                if hi[t] < lo[t]:
+                    continue
+                keys = G_j[lo[t]:hi[t] + 1]
+                s = np.einsum("hd,khd->hk", q[G_r[t]], k[keys]) * sc
+                m = s.max(axis=1, keepdims=True)
+                e = np.exp(s - m)
+                l_i[:, t] = (m[:, 0] + np.log(e.sum(axis=1)))
+                o_i[t] = np.einsum("hk,khd->hd", e / e.sum(axis=1, keepdims=True), v[keys])
+            parts.append((o_i, l_i))
+        o_r, l_r = lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        o[G_r] = o_r
+        lse[:, G_r] = l_r
+    return o, lse
+
+
+def lse_merge(o_parts, lse_parts):
+    """Softmax-weighted combination of partial attention results of the same
+    queries over disjoint key sets, in fp64: o_parts [n, rows, H, D] (each
+    normalised over its own keys), lse_parts [n, H, rows] (-inf: no key).
+    LSE = log sum_i exp(LSE_i); O = sum_i exp(LSE_i - LSE) O_i; rows without
+    any key get O = 0, LSE = -inf."""
+    o_parts, L = _f64(o_parts), _f64(lse_parts)
+    Lm = L.max(axis=0)
+    fin = np.isfinite(Lm)
+    with np.errstate(divide="ignore"):            # log(0) of rows no part saw, discarded
+        Ltot = np.where(fin, Lm + np.log(np.exp(L - np.where(fin, Lm, 0)).sum(axis=0)), -np.inf)
+    w = np.where(fin, np.exp(L - np.where(fin, Ltot, 0)), 0.0)   # [n, H, rows]
+    o = np.einsum("nhr,nrhd->rhd", w, o_parts)
+    return o, Ltot
 
 
 def pad_between_seqs(cu: Sequence[int], cup: Optional[Sequence[int]]) -> int:

@@ -142,7 +142,33 @@ def test_argument_validation_before_launch(lib):
                             64, 2, 0, 0, f(0.1), 7, FAKE, 1 << 20, None) == -1    # unknown mode
     assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
                             64, 2, 0, 0, f(0.1), 1, FAKE, 8, None) == -6           # store mode, small workspace
+    assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
+                            64, 2, 0, 0, f(0.1), 6, FAKE, 1 << 20, None) == -1    # both dQ modes
     assert L.cp_reduce_scatter_emul(_arr(FAKE), _arr(FAKE), 1, None, 0, 10, 5, 2, 64, None) == -1
+
+
+def test_p2p_sizes_and_argument_validation(lib):
+    """Ring metadata: one cp_size = 1 block (header, segments, row tables of
+    s_local rows, lists and order entries of s_local/128 query tiles and as
+    many key blocks) per step, rounded to 16 bytes; arguments checked before
+    any launch."""
+    L = api.lib()
+    lists_off = (64 + 32 * 8 + 8 * 250 + 15) // 16 * 16
+    assert api.cp_p2p_meta_bytes(3, 1000, 4) == lists_off + (64 + 8) * (2 + 2)
+    assert api.cp_p2p_meta_bytes(3, 1001, 4) == 0
+    step = api.cp_p2p_meta_bytes(2, 24, 2)
+    # rank out of range, total not divisible, metadata for one step only,
+    # padding flag without cu, misaligned metadata
+    assert L.cp_p2p_index(None, FAKE, 2, 24, 2, 2, 0, 0, FAKE, 2 * step, None) == -1
+    assert L.cp_p2p_index(None, FAKE, 2, 25, 2, 0, 1, 0, FAKE, 2 * step, None) == -2
+    assert L.cp_p2p_index(None, FAKE, 2, 24, 2, 0, 1, 0, FAKE, step, None) == -6
+    assert L.cp_p2p_index(None, FAKE, 2, 24, 2, 0, 1, 1, FAKE, 2 * step, None) == -1
+    assert L.cp_p2p_index(None, FAKE, 2, 24, 2, 0, 1, 0, FAKE + 8, 2 * step, None) == -4
+    # merge: no steps, unsupported head dim, misaligned output
+    assert L.cp_p2p_merge(FAKE, FAKE, 0, 100, 2, 64, FAKE, FAKE, None) == -1
+    assert L.cp_p2p_merge(FAKE, FAKE, 2, 100, 2, 96, FAKE, FAKE, None) == -3
+    assert L.cp_p2p_merge(FAKE, FAKE, 2, 100, 2, 64, FAKE + 4, FAKE, None) == -4
+    assert L.cp_p2p_merge(FAKE, FAKE, 2, 0, 2, 64, FAKE, FAKE, None) == 0     # nothing to do
 
 
 def test_product_path_has_no_oracle_or_cpu_fallback():

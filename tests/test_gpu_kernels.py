@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from context_packed_sequence_thd_gb300 import api, inputs, pipeline
-from gpu_util import dev
+from gpu_util import check_block_lists, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -21,44 +21,6 @@ WORKLOADS = [inputs.tiny, inputs.cfg2, inputs.cfg3, inputs.cfg4, inputs.cfg5,
 
 def _hdr(meta: torch.Tensor) -> np.ndarray:
     return meta[:64].cpu().numpy().view(np.int32)
-
-
-def _check_block_lists(meta, h, lo, hi, T, cap=7):
-    """Block lists of the metadata against brute force over the row tables:
-    the key blocks of every 128-row query tile, the query tiles of every
-    128-key block, and the heaviest-first order of each family."""
-    s_local, lists_off = int(h[6]), int(h[14])
-    n_qt, n_kb = -(-s_local // 128), -(-T // 128)
-    raw = meta[lists_off:lists_off + 64 * (n_qt + n_kb)].cpu().numpy().view(np.int32)
-    raw = raw.reshape(n_qt + n_kb, 16)
-    ord_off = lists_off + 64 * (n_qt + n_kb)
-    orders = meta[ord_off:ord_off + 8 * (n_qt + n_kb)].cpu().numpy().view(np.int32).reshape(-1, 2)
-    want_q = [set() for _ in range(n_qt)]
-    want_k = [set() for _ in range(n_kb)]
-    for t in range(s_local):
-        if hi[t] >= 0:
-            for b in range(lo[t] // 128, hi[t] // 128 + 1):
-                want_q[t // 128].add(b)
-                want_k[b].add(t // 128)
-    for fam, want, order in ((raw[:n_qt], want_q, orders[:n_qt]), (raw[n_qt:], want_k, orders[n_qt:])):
-        counts = []
-        for q, l in enumerate(fam):
-            n = min(int(l[0]), cap)
-            got = set()
-            for i in range(n):
-                assert l[2 + 2 * i] <= l[3 + 2 * i]
-                got.update(range(int(l[2 + 2 * i]), int(l[3 + 2 * i]) + 1))
-            if int(l[0]) < cap:
-                assert got == want[q]
-            else:                      # over capacity the last interval widens
-                assert want[q] <= got
-            counts.append(len(got))
-            assert l[1] == len(got)        # header: {count, blocks covered}
-        tiles = order[:, 0]
-        assert sorted(tiles.tolist()) == list(range(len(fam)))
-        assert [counts[t] for t in tiles] == order[:, 1].tolist()
-        keys = [(-counts[t], t) for t in tiles]
-        assert keys == sorted(keys)    # heaviest first, ties by index
 
 
 @pytest.mark.parametrize("make", WORKLOADS)
@@ -85,7 +47,7 @@ def test_partition_index_bit_exact(make):
             start = np.repeat(wl.cup[:-1], np.diff(wl.cup))
             np.testing.assert_array_equal(hi, np.where(valid[want], want, -1))
             np.testing.assert_array_equal(lo, np.where(valid[want], start[want], 0))
-            _check_block_lists(plan.ranks[r].meta, h, lo, hi, wl.total_tokens)
+            check_block_lists(plan.ranks[r].meta, h, lo, hi, wl.total_tokens)
         np.testing.assert_array_equal(plan.restore.cpu().numpy(),
                                       oracle.restore_index(wl.cup, wl.cp, s))
 

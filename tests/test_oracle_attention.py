@@ -183,3 +183,85 @@ def test_head_subset_matches_all_heads():
     o2, lse2 = oracle.attn_fwd(t["q"], t["k"], t["v"], wl.cu, wl.cup, 0, heads=[1, 3])
     np.testing.assert_array_equal(o2[:, [1, 3]], o[:, [1, 3]])
     assert np.all(np.isnan(o2[:, [0, 2]]))
+
+
+# ---------------------------------------------------------------------------
+# P2P ring ("THD P2P context-parallel regression ..."; the ring comm type)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("strategy", [0, 1])
+def test_p2p_ring_visits_every_shard_once(strategy):
+    for cp in (1, 2, 4):
+        for r in range(cp):
+            assert sorted(oracle.p2p_schedule(cp, r)) == list(range(cp))
+            assert oracle.p2p_schedule(cp, r)[0] == r          # step 0: the rank's own K/V
+
+
+@pytest.mark.parametrize("strategy", [0, 1])
+def test_p2p_step_keys_cover_the_causal_range(strategy):
+    """Over the ring's steps a query row's visible key ranges, mapped back to
+    global rows, are disjoint and together exactly [document start, row]."""
+    cu = cup = [0, 32, 48, 96, 128]
+    cp = 2
+    valid = oracle.valid_mask(cu, cup, 0)
+    start = np.repeat(np.asarray(cup[:-1]), np.diff(cup))
+    for r in range(cp):
+        G_r = oracle.partition_index(cup, cp, r, strategy)
+        seen = [[] for _ in G_r]
+        for j in oracle.p2p_schedule(cp, r):
+            G_j = oracle.partition_index(cup, cp, j, strategy)
+            lo, hi = oracle.p2p_step_rows(cu, cup, cp, r, j, strategy, 0)
+            for t in range(len(G_r)):
+                seen[t].extend(G_j[lo[t]:hi[t] + 1].tolist())
+        for t, g in enumerate(G_r):
+            want = list(range(start[g], g + 1)) if valid[g] else []
+            assert sorted(seen[t]) == want
+
+
+@pytest.mark.parametrize("strategy", [0, 1])
+def test_p2p_merge_equals_full_attention(strategy):
+    """Merging the ring's per-step partial softmaxes by their LSE gives the
+    full causal attention (the ring only reorders the sum)."""
+    rng = np.random.default_rng(17)
+    cu = [0, 20, 23, 48]
+    cup = [0, 24, 32, 48]
+    T, H, D = 48, 2, 8
+    q, k, v = (rng.standard_normal((T, H, D)) for _ in range(3))
+    o, lse = oracle.attn_fwd(q, k, v, cu, cup, 1)
+    o2, lse2 = oracle.p2p_attn_fwd(q, k, v, cu, cup, 1, 2, strategy)
+    valid = oracle.valid_mask(cu, cup, 1)
+    np.testing.assert_allclose(o2[valid], o[valid], atol=1e-12)
+    np.testing.assert_allclose(lse2[:, valid], lse[:, valid], atol=1e-12)
+    assert np.all(np.isneginf(lse2[:, ~valid]))
+
+
+def test_lse_merge_of_a_key_split_is_the_full_softmax():
+    """Softmax over a key set split into disjoint parts: each part's
+    normalised output and log-sum-exp, merged, give the softmax over all keys
+    (brute force on a tiny case); one part is returned unchanged; parts that
+    saw no key (LSE = -inf) carry no weight; a row no part saw is 0 / -inf."""
+    rng = np.random.default_rng(23)
+    rows, H, D, nk = 5, 3, 4, 11
+    s = rng.standard_normal((rows, H, nk)) * 3.0
+    vals = rng.standard_normal((nk, H, D))
+    split = [[0, 4, 7], [1, 2, 9, 10], [], [3, 5, 6, 8]]
+    o_parts, l_parts = [], []
+    for keys in split:
+        o_i = np.zeros((rows, H, D))
+        l_i = np.full((H, rows), -np.inf)
+        if keys:
+            sk = s[:, :, keys]
+            l_i = np.log(np.exp(sk).sum(axis=2)).T
+            p = np.exp(sk) / np.exp(sk).sum(axis=2, keepdims=True)
+            o_i = np.einsum("rhk,khd->rhd", p, vals[keys])
+        o_parts.append(o_i)
+        l_parts.append(l_i)
+    o, lse = oracle.lse_merge(np.stack(o_parts), np.stack(l_parts))
+    p_all = np.exp(s) / np.exp(s).sum(axis=2, keepdims=True)
+    np.testing.assert_allclose(o, np.einsum("rhk,khd->rhd", p_all, vals), atol=1e-12)
+    np.testing.assert_allclose(lse, np.log(np.exp(s).sum(axis=2)).T, atol=1e-12)
+    o1, l1 = oracle.lse_merge(np.stack(o_parts[:1]), np.stack(l_parts[:1]))
+    np.testing.assert_allclose(o1, o_parts[0], atol=1e-15)
+    np.testing.assert_allclose(l1, l_parts[0], atol=1e-15)
+    o0, l0 = oracle.lse_merge(np.stack([o_parts[2]] * 2), np.stack([l_parts[2]] * 2))
+    assert np.all(o0 == 0) and np.all(np.isneginf(l0))
