@@ -1,5 +1,5 @@
 """Per-workload attention throughput of the C-ABI entry points (GB300), and
-the emulated a2a comm type (exchange GB/s, attention TFLOP/s).
+the emulated a2a and P2P comm types (exchange GB/s, attention TFLOP/s).
 
     python -m context_packed_sequence_thd_gb300.config_timing
 
@@ -97,13 +97,17 @@ def a2a_exchange(T, cp, H, D, strategy, reps=20, dev=None):
     return t, gbs
 
 
-def run_a2a(wl, strategies, label, reps=10, dev=None):
-    """Forward / backward TFLOP/s of the emulated a2a comm type (exchanges included)."""
+COMM_TYPES = {"a2a": pipeline.CPA2AAttention, "p2p": pipeline.CPP2PAttention}
+
+
+def run_comm(wl, strategies, label, comm, reps=10, dev=None):
+    """Forward / backward TFLOP/s of the emulated a2a or P2P comm type (its
+    exchanges, merges and casts included), with the time of each phase."""
     dev = dev or torch.device("cuda", torch.cuda.current_device())
     t = {k: v.to(dev) for k, v in wl.tensors(with_grad=True).items()}
     for s in strategies:
         plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, s, wl.pad_between_seqs, wl.H, wl.D, dev)
-        att = pipeline.CPA2AAttention(plan)
+        att = COMM_TYPES[comm](plan)
         att.shard_inputs(t["q"], t["k"], t["v"], t["do"])
         att.forward()
         att.backward()
@@ -120,8 +124,30 @@ def run_a2a(wl, strategies, label, reps=10, dev=None):
         f = att.flops(True)
         tf = f["fwd"] / (e[0].elapsed_time(e[1]) / reps) / 1e9
         tb = f["bwd"] / (e[1].elapsed_time(e[2]) / reps) / 1e9
-        print(f"{label:32s} a2a strategy {s}: fwd {tf:7.1f} TFLOP/s   bwd {tb:7.1f} TFLOP/s",
-              flush=True)
+        att.events = {}
+        att.forward()
+        att.backward()
+        torch.cuda.synchronize()
+        phases = "  ".join(f"{k} {sum(v):.3f} ms" for k, v in att.event_ms().items())
+        print(f"{label:32s} {comm} strategy {s}: fwd {tf:7.1f} TFLOP/s   bwd {tb:7.1f} TFLOP/s"
+              f"   [{phases}]", flush=True)
+
+
+def p2p_index_time(wl, strategy, reps=20, dev=None):
+    """Time of the ring metadata of every rank: one cp_p2p_index launch per rank."""
+    dev = dev or torch.device("cuda", torch.cuda.current_device())
+    plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, dev)
+    att = pipeline.CPP2PAttention(plan)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        att.build_p2p_index()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    print(f"{wl.name:32s} p2p metadata, {wl.cp} ranks x {wl.cp} steps, strategy {strategy}: "
+          f"{us:7.1f} us ({wl.cp} launches)", flush=True)
 
 
 def main():
@@ -130,7 +156,16 @@ def main():
     run(inputs.custom([32768], cp=8, H=16, D=128, seed=5), (pipeline.DCS, pipeline.NLB),
         "one 32k doc, cp8 H16")
     run(inputs.cfg3(), (pipeline.DCS, pipeline.NLB), "cfg3 32k seq, cp8 H40", bwd=False)
-    run_a2a(inputs.cfg2(), (pipeline.DCS, pipeline.NLB), "cfg2 32k tokens, 16 docs, cp4 H16")
+    run_comm(inputs.cfg2(), (pipeline.DCS, pipeline.NLB), "cfg2 32k tokens, 16 docs, cp4 H16",
+             "a2a")
+    run_comm(inputs.cfg2(), (pipeline.DCS, pipeline.NLB), "cfg2 32k tokens, 16 docs, cp4 H16",
+             "p2p")
+    for wl in (inputs.cfg5(), inputs.cfg5(value_equal=True)):
+        label = f"{wl.name} 64k padded, 24 docs, cp4 H32"
+        run(wl, (pipeline.DCS, pipeline.NLB), label)
+        run_comm(wl, (pipeline.DCS, pipeline.NLB), label, "p2p")
+        for s in (pipeline.DCS, pipeline.NLB):
+            p2p_index_time(wl, s)
     for T in (8192, 32768, 75600):
         for s in (pipeline.DCS, pipeline.NLB):
             a2a_exchange(T, 8, 40, 128, s)

@@ -18,9 +18,9 @@ def _heads_slice(t, heads):
     return {k: v[:, heads].contiguous() for k, v in t.items()}
 
 
-def _run_all(wl, strategy, d, g, bwd):
+def _run_all(wl, strategy, d, g, bwd, cls=pipeline.CPAttention):
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, d)
-    att = pipeline.CPAttention(plan)
+    att = cls(plan)
     att.step(g["q"], g["k"], g["v"], g["do"] if bwd else None)
     torch.cuda.synchronize()
     assert api.cp_device_status() == 0
@@ -57,6 +57,26 @@ def test_full_size_fwd_bwd(make, heads, bwd):
     grads = oracle.attn_bwd(s["q"], s["k"], s["v"], o, lse, s["do"], wl.cu, wl.cup, pad)
     for strategy in wl.strategies:
         plan, att = _run_all(wl, strategy, d, g, bwd)
+        _compare(wl, plan, att, heads, o, lse, grads)
+        del att
+
+
+@pytest.mark.parametrize("make,heads", [(inputs.cfg2, [3]), (inputs.cfg5, [0])],
+                         ids=["cfg2", "cfg5"])
+def test_full_size_p2p_ring(make, heads):
+    """The emulated P2P ring (per-step attention, LSE merge, per-step backward,
+    fp32 dQ/dK/dV sums) at full size, both strategies, against the oracle on
+    a subset of heads."""
+    d = dev()
+    wl = make()
+    t = wl.tensors()
+    g = {k: v.to(d) for k, v in t.items()}
+    s = _heads_slice(t, heads)
+    pad = wl.pad_between_seqs
+    o, lse = oracle.attn_fwd(s["q"], s["k"], s["v"], wl.cu, wl.cup, pad)
+    grads = oracle.attn_bwd(s["q"], s["k"], s["v"], o, lse, s["do"], wl.cu, wl.cup, pad)
+    for strategy in wl.strategies:
+        plan, att = _run_all(wl, strategy, d, g, True, cls=pipeline.CPP2PAttention)
         _compare(wl, plan, att, heads, o, lse, grads)
         del att
 
