@@ -43,6 +43,8 @@ _SIGNATURES = {
     "cp_a2a_exchange": ([_P, _P, _I, _P, _I64, _I, _I, _I, _I, _P], _I),
     "cp_zero_tail": ([_P, _I, _I64, _I64, _I64, _P, _P, ctypes.POINTER(_I)], _I),
     "cp_attn_fwd": ([_P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I, ctypes.c_float, _P], _I),
+    "cp_attn_fwd_gather": ([_P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
+                           ctypes.c_float, _P], _I),
     "cp_attn_bwd_workspace_bytes": ([_I64, _I], _SZ),
     "cp_attn_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
                      ctypes.c_float, _P, _SZ, _P], _I),
@@ -250,6 +252,19 @@ def cp_attn_fwd(q_local, k_full, v_full, o_local, lse_local, d_meta, total_token
                            d_meta.numel() * d_meta.element_size(), total_tokens, H, D, cp_size,
                            rank, strategy, float(softmax_scale), _stream(stream))
     _check("cp_attn_fwd", st)
+
+
+def cp_attn_fwd_gather(q_src, d_idx, k_full, v_full, o_local, lse_local, d_meta,
+                       total_tokens: int, cp_size: int, rank: int, strategy: int,
+                       softmax_scale: float, stream=None) -> None:
+    """cp_attn_fwd reading query row t from q_src[d_idx[t]] (no q_local copy)."""
+    _, H, D = k_full.shape
+    st = lib().cp_attn_fwd_gather(_dev(q_src, "q_src"), q_src.shape[0], _dev(d_idx, "idx"),
+                                  _dev(k_full, "k"), _dev(v_full, "v"), _dev(o_local, "o"),
+                                  _dev(lse_local, "lse"), _dev(d_meta, "meta"),
+                                  d_meta.numel() * d_meta.element_size(), total_tokens, H, D,
+                                  cp_size, rank, strategy, float(softmax_scale), _stream(stream))
+    _check("cp_attn_fwd_gather", st)
 
 
 BWD_ACCUMULATE, BWD_STORE, BWD_DQ_F32_STORE, BWD_DQ_F32_ACCUMULATE = 0, 1, 2, 4

@@ -150,12 +150,44 @@ def p2p_index_time(wl, strategy, reps=20, dev=None):
           f"{us:7.1f} us ({wl.cp} launches)", flush=True)
 
 
+def fused_gather_timing(wl, reps=10, dev=None):
+    """Forward-only DUAL_CHUNK_SWAP step (shard gather + restore + every rank's
+    forward) with the Q shard gathered by a copy kernel and with the gather
+    fused into the attention's loads (cp_attn_fwd_gather)."""
+    dev = dev or torch.device("cuda", torch.cuda.current_device())
+    t = {k: v.to(dev) for k, v in wl.tensors(with_grad=False).items()}
+    plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, pipeline.DCS, wl.pad_between_seqs, wl.H, wl.D,
+                           dev)
+    out = {}
+    for fuse in (False, True):
+        att = pipeline.CPAttention(plan, fuse_q_gather=fuse)
+        att.step(t["q"], t["k"], t["v"], rebuild_index=False)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            att.step(t["q"], t["k"], t["v"], rebuild_index=False)
+        e1.record()
+        torch.cuda.synchronize()
+        out[fuse] = e0.elapsed_time(e1) / reps
+        att.events = {}
+        att.step(t["q"], t["k"], t["v"], rebuild_index=False)
+        torch.cuda.synchronize()
+        phases = "  ".join(f"{k} {sum(v):.3f} ms" for k, v in att.event_ms().items())
+        tf = att.flops(False)["fwd"] / (out[fuse] * 1e-3) / 1e12
+        print(f"{wl.name:32s} fwd-only DCS step, {'fused Q gather' if fuse else 'Q shard copy  '}: "
+              f"{out[fuse]:.3f} ms ({tf:6.1f} TFLOP/s)  [{phases}]", flush=True)
+    return out
+
+
 def main():
     run(inputs.cfg2(), (pipeline.DCS, pipeline.NLB), "cfg2 32k tokens, 16 docs, cp4 H16")
     run(inputs.custom([32768], cp=1, H=16, D=128, seed=5), (pipeline.NLB,), "one 32k doc, cp1 H16")
     run(inputs.custom([32768], cp=8, H=16, D=128, seed=5), (pipeline.DCS, pipeline.NLB),
         "one 32k doc, cp8 H16")
     run(inputs.cfg3(), (pipeline.DCS, pipeline.NLB), "cfg3 32k seq, cp8 H40", bwd=False)
+    for s in (8192, 32768, 75600):
+        fused_gather_timing(inputs.cfg3(s))
     run_comm(inputs.cfg2(), (pipeline.DCS, pipeline.NLB), "cfg2 32k tokens, 16 docs, cp4 H16",
              "a2a")
     run_comm(inputs.cfg2(), (pipeline.DCS, pipeline.NLB), "cfg2 32k tokens, 16 docs, cp4 H16",

@@ -112,9 +112,30 @@ extern "C" int cp_attn_fwd(const void* q_local, const void* k_full, const void* 
   if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local)) return CP_ERR_ALIGNMENT;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
   if (s_local == 0) return CP_OK;
-  return cpthd_attn_fwd_tc(q_local, k_full, v_full, o_local, lse_local, d_meta, meta_bytes,
-                           (int)total_tokens, H, D, (int)s_local, cp_size, rank, (int)strategy,
-                           softmax_scale * kLog2e, cpthd_host::as_stream(stream));
+  return cpthd_attn_fwd_tc(q_local, nullptr, 0, k_full, v_full, o_local, lse_local, d_meta,
+                           meta_bytes, (int)total_tokens, H, D, (int)s_local, cp_size, rank,
+                           (int)strategy, softmax_scale * kLog2e, cpthd_host::as_stream(stream));
+}
+
+extern "C" int cp_attn_fwd_gather(const void* q_src, int64_t src_rows, const int32_t* d_idx,
+                                  const void* k_full, const void* v_full, void* o_local,
+                                  float* lse_local, const void* d_meta, size_t meta_bytes,
+                                  int64_t total_tokens, int H, int D, int cp_size, int rank,
+                                  cp_strategy_t strategy, float softmax_scale, void* stream) {
+  int64_t s_local = 0;
+  int st = common_checks(q_src, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
+                         rank, strategy, &s_local);
+  if (st != CP_OK) return st;
+  if (!o_local || !lse_local || !d_idx) return CP_ERR_INVALID_ARG;
+  if (src_rows < 1 || src_rows > INT32_MAX) return CP_ERR_INVALID_ARG;
+  if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local) ||
+      (reinterpret_cast<uintptr_t>(d_idx) & 3u))
+    return CP_ERR_ALIGNMENT;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
+  if (s_local == 0) return CP_OK;
+  return cpthd_attn_fwd_tc(q_src, d_idx, (int)src_rows, k_full, v_full, o_local, lse_local, d_meta,
+                           meta_bytes, (int)total_tokens, H, D, (int)s_local, cp_size, rank,
+                           (int)strategy, softmax_scale * kLog2e, cpthd_host::as_stream(stream));
 }
 
 extern "C" size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H) {

@@ -80,6 +80,8 @@ __host__ __device__ constexpr uint32_t o_col(int b) { return 256 + b * D; }
 struct TcArgs {
   bf16* o;
   float* lse;
+  const int32_t* q_idx;  // nullable: query row t is row q_idx[t] of a q_rows-row source
+  int q_rows;
   const void* meta;
   size_t meta_bytes;
   int T, H, s_local, cp, rank, strategy;
@@ -214,71 +216,106 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
   if (warp == kProdWarp) {
     // ---------------------------------------------------------------- TMA producer
+    // The whole warp walks the items; lane 0 waits, arms the barriers and
+    // issues the tiled copies, and every lane takes part in the row gathers
+    // of a fused-gather Q tile (four rows per lane).
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int ii = 0, g = 0, v_issued = 0;
-      int pv_h = 0, pv_key = 0;  // V of block v_issued still to load (when v_issued < g)
-      bool ok = true;
-      auto load_v = [&]() -> bool {
-        const int vs = v_issued % kVStages;
-        if (!mbar_wait(bar(bars.v_empty[vs]), ((v_issued / kVStages) & 1) ^ 1, &s_abort,
-                       kWaitLimitNs))
-          return false;
+    }
+    // lane 0 waits; the result is the warp's
+    auto wait0 = [&](uint64_t& b, uint32_t parity) -> bool {
+      const bool w = lane == 0 ? mbar_wait(bar(b), parity, &s_abort, kWaitLimitNs) : true;
+      return __shfl_sync(0xffffffffu, w, 0);
+    };
+    int ii = 0, g = 0, v_issued = 0;
+    int pv_h = 0, pv_key = 0;  // V of block v_issued still to load (when v_issued < g)
+    bool ok = true;
+    auto load_v = [&]() -> bool {
+      const int vs = v_issued % kVStages;
+      if (!wait0(bars.v_empty[vs], ((v_issued / kVStages) & 1) ^ 1)) return false;
+      if (lane == 0) {
         mbar_arrive_expect_tx(bar(bars.v_full[vs]), L::TILE);
 #pragma unroll
         for (int b = 0; b < L::BOXES; ++b)
           tma_load_3d(sb + L::V + vs * L::TILE + b * kBoxBytes, &tm_v, bar(bars.v_full[vs]),
                       b * 64, pv_h, pv_key);
-        ++v_issued;
-        return true;
-      };
-      for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
-        const int k = snake_item(j, blockIdx.x, gridDim.x);
-        if (k >= n_items) continue;
-        Item it;
-        it.load(m, k, n_qt, a.H);
-        if (it.nb == 0) continue;
-        const int qb = ii & 1;
-        if (!mbar_wait(bar(bars.q_free[qb]), ((ii >> 1) & 1) ^ 1, &s_abort, kWaitLimitNs)) {
-          fail(&s_abort);
-          break;
+      }
+      ++v_issued;
+      return true;
+    };
+    for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
+      const int k = snake_item(j, blockIdx.x, gridDim.x);
+      if (k >= n_items) continue;
+      Item it;
+      it.load(m, k, n_qt, a.H);
+      if (it.nb == 0) continue;
+      const int qb = ii & 1;
+      if (!wait0(bars.q_free[qb], ((ii >> 1) & 1) ^ 1)) {
+        if (lane == 0) fail(&s_abort);
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(bar(bars.q_full[qb]), L::TILE);
+      if (a.q_idx) {
+        // fused partition gather: the tile's rows come straight from the
+        // source by the rank's index, lane l gathering rows 4l..4l+3 (rows
+        // past s_local repeat the last row; they are masked)
+        __syncwarp();
+        const int t = it.t0 + 4 * lane, last = a.s_local - 1;
+        int r[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) r[e] = __ldg(a.q_idx + min(t + e, last));
+        bool bad = false;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if ((unsigned)r[e] >= (unsigned)a.q_rows) {  // outside the source: report, read row 0
+            bad = true;
+            r[e] = 0;
+          }
         }
-        mbar_arrive_expect_tx(bar(bars.q_full[qb]), L::TILE);
+        if (bad) atomicCAS(&g_status_fwd_tc, 0, (int)CP_ERR_INVALID_ARG);
+#pragma unroll
+        for (int b = 0; b < L::BOXES; ++b)
+          tma_gather4_2d(sb + L::Q + qb * L::TILE + b * kBoxBytes + lane * 512, &tm_q,
+                         bar(bars.q_full[qb]), it.h * D + b * 64, r[0], r[1], r[2], r[3]);
+      } else if (lane == 0) {
 #pragma unroll
         for (int b = 0; b < L::BOXES; ++b)
           tma_load_3d(sb + L::Q + qb * L::TILE + b * kBoxBytes, &tm_q, bar(bars.q_full[qb]),
                       b * 64, it.h, it.t0);
-        ++ii;
-        Iter bi;
-        bi.init(it.list + 1, it.n_iv());
-        for (int j = 0; j < it.nb; ++j, bi.next()) {
-          const int ks = g % kKStages;
-          if (!mbar_wait(bar(bars.k_empty[ks]), ((g / kKStages) & 1) ^ 1, &s_abort,
-                         kWaitLimitNs)) {
-            fail(&s_abort);
-            ok = false;
-            break;
-          }
-          const int key0 = bi.b * TBN;
+      }
+      ++ii;
+      Iter bi;
+      bi.init(it.list + 1, it.n_iv());
+      for (int j = 0; j < it.nb; ++j, bi.next()) {
+        const int ks = g % kKStages;
+        if (!wait0(bars.k_empty[ks], ((g / kKStages) & 1) ^ 1)) {
+          if (lane == 0) fail(&s_abort);
+          ok = false;
+          break;
+        }
+        const int key0 = bi.b * TBN;
+        if (lane == 0) {
           mbar_arrive_expect_tx(bar(bars.k_full[ks]), L::TILE);
 #pragma unroll
           for (int b = 0; b < L::BOXES; ++b)
             tma_load_3d(sb + L::K + ks * L::TILE + b * kBoxBytes, &tm_k, bar(bars.k_full[ks]),
                         b * 64, it.h, key0);
-          ++g;
-          if (v_issued < g - 1 && !load_v()) {  // V lags K by one block
-            fail(&s_abort);
-            ok = false;
-            break;
-          }
-          pv_h = it.h;
-          pv_key = key0;
         }
+        ++g;
+        if (v_issued < g - 1 && !load_v()) {  // V lags K by one block
+          if (lane == 0) fail(&s_abort);
+          ok = false;
+          break;
+        }
+        pv_h = it.h;
+        pv_key = key0;
       }
-      if (ok && v_issued < g && !load_v()) fail(&s_abort);
-      // drain: every copy this CTA issued must land before shared memory goes away
+    }
+    if (ok && v_issued < g && !load_v() && lane == 0) fail(&s_abort);
+    // drain: every copy this CTA issued must land before shared memory goes away
+    if (lane == 0) {
       int never = 0;
       for (int i = max(0, ii - 2); i < ii; ++i)
         mbar_wait(bar(bars.q_full[i & 1]), (i >> 1) & 1, &never, kWaitLimitNs);
@@ -287,6 +324,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       for (int j = max(0, v_issued - kVStages); j < v_issued; ++j)
         mbar_wait(bar(bars.v_full[j % kVStages]), (j / kVStages) & 1, &never, kWaitLimitNs);
     }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -606,7 +644,9 @@ template <int D>
 int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, cudaStream_t s) {
   alignas(64) CUtensorMap mq, mk, mv;
   int st;
-  if ((st = tma::make_thd_map(&mq, q, a.s_local, a.H, D, 128)) != CP_OK) return st;
+  st = a.q_idx ? tma::make_row_gather_map(&mq, q, a.q_rows, a.H, D)
+               : tma::make_thd_map(&mq, q, a.s_local, a.H, D, 128);
+  if (st != CP_OK) return st;
   if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128)) != CP_OK) return st;
   if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128)) != CP_OK) return st;
   const int smem = Layout<D>::BYTES + (int)sizeof(Ctl);
@@ -623,13 +663,16 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, 
 }  // namespace cpthd
 
 // Internal entry used by cp_attn_fwd (arguments already validated).
-int cpthd_attn_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse,
-                      const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
-                      int cp, int rank, int strategy, float scale_log2, cudaStream_t s) {
+int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const void* k,
+                      const void* v, void* o, float* lse, const void* meta, size_t meta_bytes,
+                      int T, int H, int D, int s_local, int cp, int rank, int strategy,
+                      float scale_log2, cudaStream_t s) {
   using namespace cpthd;
   TcArgs a{};
   a.o = (bf16*)o;
   a.lse = lse;
+  a.q_idx = q_idx;
+  a.q_rows = q_rows;
   a.meta = meta;
   a.meta_bytes = meta_bytes;
   a.T = T; a.H = H; a.s_local = s_local; a.cp = cp; a.rank = rank; a.strategy = strategy;

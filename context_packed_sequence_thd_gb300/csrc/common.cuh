@@ -308,10 +308,12 @@ extern "C" int cpthd_status_attn(int reset);
 extern "C" int cpthd_status_fwd_tc(int reset);
 extern "C" int cpthd_status_bwd_tc(int reset);
 
-// tcgen05 forward (attn_fwd_tc.cu); arguments validated by cp_attn_fwd
-int cpthd_attn_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse,
-                      const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
-                      int cp, int rank, int strategy, float scale_log2, cudaStream_t s);
+// tcgen05 forward (attn_fwd_tc.cu); arguments validated by cp_attn_fwd /
+// cp_attn_fwd_gather (q_idx null: q is the rank's [s_local, H, D] queries)
+int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const void* k,
+                      const void* v, void* o, float* lse, const void* meta, size_t meta_bytes,
+                      int T, int H, int D, int s_local, int cp, int rank, int strategy,
+                      float scale_log2, cudaStream_t s);
 
 // tcgen05 dQ and dK/dV kernels (attn_bwd_tc.cu); Delta already in `delta`;
 // mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added)

@@ -95,6 +95,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
       "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// Row gather of a 2-D tensor map (box one row high): the rows y0..y3 at
+// column c0 land in shared memory one after another at dst, swizzled as a
+// tiled load of the same box would be; completion counted on `bar` (bytes).
+__device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const void* map, uint32_t bar, int c0,
+                                               int y0, int y1, int y2, int y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];\n" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(c0), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
 // generic-proxy writes to shared memory -> visible to the async proxy (MMA)
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");

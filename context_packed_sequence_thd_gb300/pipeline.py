@@ -150,9 +150,13 @@ class CPPlan:
 class CPAttention:
     """Buffers and the full emulated CP forward/backward for one plan."""
 
-    def __init__(self, plan: CPPlan):
+    def __init__(self, plan: CPPlan, fuse_q_gather: bool = False):
         self.plan = plan
         p = plan
+        # forward-only steps under DUAL_CHUNK_SWAP: the attention loads query
+        # rows through the partition index (cp_attn_fwd_gather), no Q shard copy
+        self.fuse_q_gather = fuse_q_gather
+        self.q_src: Optional[torch.Tensor] = None
         dev, T, H, D = p.device, p.T, p.H, p.D
         bf = dict(dtype=torch.bfloat16, device=dev)
         # rank-concatenated buffers: rank r's shard is rows [r*s_local, (r+1)*s_local);
@@ -205,9 +209,12 @@ class CPAttention:
                 self.doc = do
             return
         # every rank's shard in one gather: the rank-concatenated buffer is the
-        # input gathered by the ranks' indices side by side
-        srcs = [q, k, v] + ([do] if do is not None else [])
-        dsts = [self.qc, self.kc, self.vc] + ([self.doc] if do is not None else [])
+        # input gathered by the ranks' indices side by side.  A forward-only
+        # step with the fused gather leaves Q where it is.
+        self.q_src = q if (self.fuse_q_gather and do is None) else None
+        srcs = ([q] if self.q_src is None else []) + [k, v] + ([do] if do is not None else [])
+        dsts = ([self.qc] if self.q_src is None else []) + [self.kc, self.vc] + \
+            ([self.doc] if do is not None else [])
         with self._timed("partition_gather", stream):
             api.cp_thd_gather(srcs, dsts, p.idx_all, stream)
         self.launches += 1
@@ -226,11 +233,17 @@ class CPAttention:
     def forward(self, stream=None):
         p = self.plan
         k_full, v_full = self.restore_kv(stream)
+        fused = self.q_src is not None and p.strategy == DCS
         for r in range(p.cp):
             with self._timed("attn_fwd", stream):
-                api.cp_attn_fwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
-                                self.lse[r], p.ranks[r].meta, p.T, p.cp, r, p.strategy, p.scale,
-                                stream)
+                if fused:
+                    api.cp_attn_fwd_gather(self.q_src, p.ranks[r].idx, k_full, v_full,
+                                           p.local(self.oc, r), self.lse[r], p.ranks[r].meta, p.T,
+                                           p.cp, r, p.strategy, p.scale, stream)
+                else:
+                    api.cp_attn_fwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
+                                    self.lse[r], p.ranks[r].meta, p.T, p.cp, r, p.strategy,
+                                    p.scale, stream)
             self.launches += 1
         return k_full, v_full
 

@@ -222,6 +222,23 @@ int cp_attn_fwd(const void* q_local, const void* k_full, const void* v_full, voi
                 int H, int D, int cp_size, int rank, cp_strategy_t strategy,
                 float softmax_scale, void* stream);
 
+/* cp_attn_fwd with the partition gather of the queries fused into the kernel
+ * (the index_select of get_batch_on_this_cp_rank, [AG] §Sequence Diagram,
+ * done by the attention's own loads): query row t of this
+ * rank is row d_idx[t] of q_src [src_rows, H, D] bf16 (e.g. the unsharded
+ * batch with d_idx from cp_partition_index), so no q_local copy is made.
+ * d_idx: device int32 [s_local], 4-byte aligned (a rank's slice of the
+ * ranks' indices side by side qualifies); a value outside
+ * [0, src_rows) reads row 0 instead and sets the device status word
+ * (CP_ERR_INVALID_ARG).  Everything else, including the results, as for
+ * cp_attn_fwd: the output is bitwise the same as cp_attn_fwd on the gathered
+ * q_local. */
+int cp_attn_fwd_gather(const void* q_src, int64_t src_rows, const int32_t* d_idx,
+                       const void* k_full, const void* v_full, void* o_local, float* lse_local,
+                       const void* d_meta, size_t meta_bytes, int64_t total_tokens, int H, int D,
+                       int cp_size, int rank, cp_strategy_t strategy, float softmax_scale,
+                       void* stream);
+
 /* Device scratch cp_attn_bwd needs: Delta = rowsum(dO * O), fp32 [H, s_local]. */
 size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H);
 

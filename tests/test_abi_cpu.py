@@ -136,6 +136,13 @@ def test_argument_validation_before_launch(lib):
     assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64, 2, 2, 0, f(0.1), None) == -1
     assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64, 2, 0, 0, f(-1.0), None) == -1
     assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 127, 2, 64, 2, 0, 0, f(0.1), None) == -2
+    # fused-gather forward: no index, misaligned index, empty source
+    assert L.cp_attn_fwd_gather(FAKE, 4096, None, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2, 64,
+                                2, 0, 0, f(0.1), None) == -1
+    assert L.cp_attn_fwd_gather(FAKE, 4096, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2,
+                                64, 2, 0, 0, f(0.1), None) == -4
+    assert L.cp_attn_fwd_gather(FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2, 64,
+                                2, 0, 0, f(0.1), None) == -1
     assert L.cp_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64,
                          2, 0, 0, f(0.1), FAKE, 8, None) == -6
     assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
