@@ -579,6 +579,13 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                           ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         l_run = l_run * alpha + sum;
 
+        {  // P (bf16 pairs) -> TMEM over the first 32 of this half's S columns;
+           // written before any O rescale so that S is dead while O is in registers
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
+          tmem_st32(tmem + lane_base + buf * 128 + 64 * hf, pk);
+        }
         // O only has to be complete (P V_{g-1} done) when it is rescaled; the
         // first block of an item starts a fresh accumulator.
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -599,12 +606,6 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             tmem_st32(tmem + lane_base + col, o);
           }
           tmem_st_wait();
-        }
-        {  // P (bf16 pairs) -> TMEM over the first 32 of this half's S columns
-          uint32_t pk[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
-          tmem_st32(tmem + lane_base + buf * 128 + 64 * hf, pk);
         }
         tmem_st_wait();
         tc_fence_before();
