@@ -69,6 +69,14 @@ struct BwdArgs {
   float scale, scale_log2;
   int store;    // dK/dV partials stored (every row written) instead of added
   int dq_mode;  // 0: dQ stored as bf16; 1: stored as fp32; 2: added into fp32
+  // finishing call of a sum over ranks: dk/dv are read (unless store), the
+  // total is rounded to bf16 and written to row out_idx[key] (key if null)
+  // of dk_out / dv_out instead of going back to dk/dv
+  int fin;
+  bf16* dk_out;
+  bf16* dv_out;
+  const int32_t* out_idx;
+  int out_rows;
 };
 
 __device__ __forceinline__ bool meta_ok_bwd(const BwdArgs& a, const MetaHeader* h) {
@@ -888,7 +896,33 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       itm.load(m.korder, m.klists, k, a.H, n_kb);
       if (itm.nb == 0) {
         // no query of this rank attends these keys: a stored partial is zero
-        if (a.store) {
+        if (a.fin) {  // the finished sum is what the earlier ranks left (or zero)
+          const int rb = itm.tile * 128 + (warp & 3) * 32;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32)
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int kr = rb + (lane >> 3) + 4 * it;
+              if (kr < a.T) {
+                const int64_t o = ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * (lane & 7);
+                const int64_t orow = a.out_idx ? a.out_idx[kr] : kr;
+                if ((uint64_t)orow >= (uint64_t)a.out_rows) {  // skipped, reported
+                  atomicCAS(&g_status_bwd_tc, 0, (int)CP_ERR_INVALID_ARG);
+                  continue;
+                }
+                const int64_t oo = (orow * a.H + itm.h) * D + c0 + 4 * (lane & 7);
+                float4 xk = make_float4(0.f, 0.f, 0.f, 0.f), xv = xk;
+                if (!a.store) {
+                  xk = *reinterpret_cast<const float4*>(a.dk + o);
+                  xv = *reinterpret_cast<const float4*>(a.dv + o);
+                }
+                *reinterpret_cast<uint2*>(a.dk_out + oo) =
+                    make_uint2(pack_bf16(xk.x, xk.y), pack_bf16(xk.z, xk.w));
+                *reinterpret_cast<uint2*>(a.dv_out + oo) =
+                    make_uint2(pack_bf16(xv.x, xv.y), pack_bf16(xv.z, xv.w));
+              }
+            }
+        } else if (a.store) {
           const int rb = itm.tile * 128 + (warp & 3) * 32;
           const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
@@ -937,7 +971,20 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           const float4 x =
               *reinterpret_cast<const float4*>(stg + rr * 32 + ((uu ^ (rr & 7)) * 4));
           const int kr = rbase + rr;
-          if (kr < a.T) {
+          if (kr < a.T && a.fin) {  // last term of the sum: add, round, write the bf16 row
+            const float* src = acc + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * uu;
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!a.store) t = *reinterpret_cast<const float4*>(src);
+            t = make_float4(__fadd_rn(t.x, x.x), __fadd_rn(t.y, x.y), __fadd_rn(t.z, x.z),
+                            __fadd_rn(t.w, x.w));
+            const int64_t orow = a.out_idx ? a.out_idx[kr] : kr;
+            bf16* out = is_v ? a.dv_out : a.dk_out;
+            if ((uint64_t)orow < (uint64_t)a.out_rows)
+              *reinterpret_cast<uint2*>(out + (orow * a.H + itm.h) * D + c0 + 4 * uu) =
+                  make_uint2(pack_bf16(t.x, t.y), pack_bf16(t.z, t.w));
+            else  // skipped, reported
+              atomicCAS(&g_status_bwd_tc, 0, (int)CP_ERR_INVALID_ARG);
+          } else if (kr < a.T) {
             float* dst = acc + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * uu;
             if (a.store)  // p + 0: the value the first addition into a cleared buffer gives
               *reinterpret_cast<float4*>(dst) =
@@ -1093,7 +1140,8 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
                       const float* lse, const float* delta, void* dq, float* dk, float* dv,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale, float scale_log2,
-                      int mode, cudaStream_t s) {
+                      int mode, void* dk_out, void* dv_out, const int32_t* out_idx,
+                      int out_rows, cudaStream_t s) {
   using namespace cpthd;
   BwdArgs a{};
   a.lse = lse;
@@ -1108,6 +1156,11 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
   a.scale_log2 = scale_log2;
   a.store = mode & 1;
   a.dq_mode = (mode & 2) ? 1 : (mode & 4) ? 2 : 0;
+  a.fin = dk_out != nullptr;
+  a.dk_out = (bf16*)dk_out;
+  a.dv_out = (bf16*)dv_out;
+  a.out_idx = out_idx;
+  a.out_rows = out_rows;
   return D == 64 ? launch_bwd_tc<64>(q, k, v, dout, a, s) : launch_bwd_tc<128>(q, k, v, dout, a, s);
 }
 

@@ -18,8 +18,11 @@ Diagram; "[PyTorch] Extend no-load-balance CP to the a2a comm type"):
                               order (the reorder the a2a page removes)
   attention fwd / bwd         cp_attn_fwd / cp_attn_bwd per rank
   unrestore + reduce-scatter  per-rank partial dK/dV summed in fp32 in
-                              original order, then cp_reduce_scatter_emul
-                              (gather by the rank's index + bf16 cast)
+                              original order; the last rank's call
+                              (cp_attn_bwd_final) adds its partial, rounds
+                              to bf16 and writes each row to its rank's shard
+                              (or cp_reduce_scatter_emul: gather by the
+                              rank's index + bf16 cast)
   dQ/dK/dV tail-zeroing       cp_zero_tail, gated by the host-known valid end
 
 Only argument marshalling and buffer management happen here; every step is
@@ -150,9 +153,13 @@ class CPPlan:
 class CPAttention:
     """Buffers and the full emulated CP forward/backward for one plan."""
 
-    def __init__(self, plan: CPPlan, fuse_q_gather: bool = False):
+    def __init__(self, plan: CPPlan, fuse_q_gather: bool = False,
+                 fuse_reduce_scatter: bool = True):
         self.plan = plan
         p = plan
+        # the last rank's backward finishes the dK/dV sums and writes the bf16
+        # shards itself (cp_attn_bwd_final) instead of a separate cast pass
+        self.fuse_reduce_scatter = fuse_reduce_scatter
         # forward-only steps under DUAL_CHUNK_SWAP: the attention loads query
         # rows through the partition index (cp_attn_fwd_gather), no Q shard copy
         self.fuse_q_gather = fuse_q_gather
@@ -250,23 +257,38 @@ class CPAttention:
     def backward(self, k_full, v_full, stream=None):
         """Every rank's backward; rank 0 stores its partial dK/dV into the fp32
         accumulators (no clearing pass), the others add theirs in rank order:
-        the emulated reduce-scatter's sum."""
+        the emulated reduce-scatter's sum.  The last rank finishes it: its call
+        adds its partial, rounds the sums to bf16 and writes every rank's shard
+        rows of the rank-concatenated dK/dV (through the restore index under
+        DUAL_CHUNK_SWAP; NO_LOAD_BALANCE rows are already in that order) --
+        the unrestore + scatter of the reduce-scatter, fused."""
         p = self.plan
+        last = p.cp - 1
         for r in range(p.cp):
+            mode = api.BWD_STORE if r == 0 else api.BWD_ACCUMULATE
             with self._timed("attn_bwd", stream):
-                api.cp_attn_bwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
-                                self.lse[r], p.local(self.doc, r), p.local(self.dqc, r),
-                                self.dk_acc, self.dv_acc, p.ranks[r].meta, p.T, p.cp, r,
-                                p.strategy, p.scale, self.ws, stream,
-                                mode=api.BWD_STORE if r == 0 else api.BWD_ACCUMULATE)
+                if r == last and self.fuse_reduce_scatter:
+                    api.cp_attn_bwd_final(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
+                                          self.lse[r], p.local(self.doc, r), p.local(self.dqc, r),
+                                          self.dk_acc, self.dv_acc, self.dkc, self.dvc,
+                                          p.restore if p.strategy == DCS else None,
+                                          p.ranks[r].meta, p.T, p.cp, r, p.strategy, p.scale,
+                                          self.ws, stream, mode=mode)
+                else:
+                    api.cp_attn_bwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
+                                    self.lse[r], p.local(self.doc, r), p.local(self.dqc, r),
+                                    self.dk_acc, self.dv_acc, p.ranks[r].meta, p.T, p.cp, r,
+                                    p.strategy, p.scale, self.ws, stream, mode=mode)
             self.launches += 3
-        # the scatter half of the reduce-scatter for every rank in one launch:
-        # rank r's rows of the rank-concatenated dK/dV are the summed
-        # accumulators at its partition index (NO_LOAD_BALANCE: contiguous)
-        with self._timed("reduce_scatter_emul", stream):
-            api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc], [self.dkc, self.dvc],
-                                       p.idx_all if p.strategy == DCS else None, 0, p.T, stream)
-        self.launches += 1
+        if not self.fuse_reduce_scatter:
+            # the scatter half of the reduce-scatter for every rank in one launch:
+            # rank r's rows of the rank-concatenated dK/dV are the summed
+            # accumulators at its partition index (NO_LOAD_BALANCE: contiguous)
+            with self._timed("reduce_scatter_emul", stream):
+                api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc], [self.dkc, self.dvc],
+                                           p.idx_all if p.strategy == DCS else None, 0, p.T,
+                                           stream)
+            self.launches += 1
         for r, rm in enumerate(p.ranks):
             if api.cp_zero_tail([p.local(self.dqc, r), p.local(self.dkc, r), p.local(self.dvc, r)],
                                 rm.valid_end, stream=stream):
