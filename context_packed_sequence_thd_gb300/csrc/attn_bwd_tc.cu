@@ -509,15 +509,17 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (in && a.dq_mode != 0) {  // fp32 dQ: a stored value is p + 0, like a first addition
           float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.dq) +
                                                   ((int64_t)t * a.H + itm.h) * D + col);
+          float4 prev[8];  // all loads in flight before the first add
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            prev[q] = a.dq_mode == 2 ? dst[q] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            float4 prev = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (a.dq_mode == 2) prev = dst[q];
             float4 v;
-            v.x = __fadd_rn(prev.x, __uint_as_float(o[q * 4 + 0]) * a.scale);
-            v.y = __fadd_rn(prev.y, __uint_as_float(o[q * 4 + 1]) * a.scale);
-            v.z = __fadd_rn(prev.z, __uint_as_float(o[q * 4 + 2]) * a.scale);
-            v.w = __fadd_rn(prev.w, __uint_as_float(o[q * 4 + 3]) * a.scale);
+            v.x = __fadd_rn(prev[q].x, __uint_as_float(o[q * 4 + 0]) * a.scale);
+            v.y = __fadd_rn(prev[q].y, __uint_as_float(o[q * 4 + 1]) * a.scale);
+            v.z = __fadd_rn(prev[q].z, __uint_as_float(o[q * 4 + 2]) * a.scale);
+            v.w = __fadd_rn(prev[q].w, __uint_as_float(o[q * 4 + 3]) * a.scale);
             dst[q] = v;
           }
         } else if (in) {
@@ -939,17 +941,37 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         continue;
       }
+      const int rbase = itm.tile * 128 + (warp & 3) * 32;  // first key row of this warp
+      const bool read_acc = a.fin && !a.store;  // finishing a sum the earlier ranks left
+      if (read_acc && rbase + lane < a.T) {
+        // the earlier ranks' sums of this item's rows go to L2 while its products run
+        const int64_t o = ((int64_t)(rbase + lane) * a.H + itm.h) * D;
+#pragma unroll
+        for (int l = 0; l < D / 32; ++l) {
+          prefetch_l2(a.dk + o + 32 * l);
+          prefetch_l2(a.dv + o + 32 * l);
+        }
+      }
       if (!wait_warp(bar_addr(c.done), ii & 1)) {
         fail(&s_abort);
         break;
       }
       ++ii;
       tc_fence_after();
-      const int rbase = itm.tile * 128 + (warp & 3) * 32;  // first key row of this warp
 #pragma unroll 1
       for (int ch = 0; ch < 2 * (D / 32); ++ch) {
         const bool is_v = ch < D / 32;  // dV first, then dK
         const int c0 = (is_v ? ch : ch - D / 32) * 32;
+        // the earlier sums of this chunk, all in flight before any is used
+        float4 prev[8];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int kr = rbase + (lane >> 3) + 4 * it;
+          prev[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (read_acc && kr < a.T)
+            prev[it] = __ldcs(reinterpret_cast<const float4*>(
+                (is_v ? a.dv : a.dk) + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * (lane & 7)));
+        }
         uint32_t v[32];
         tmem_ld32(tmem + lb + 256 + (is_v ? D : 0) + c0, v);
         if (ch == D / 32 - 1 || ch == 2 * (D / 32) - 1) {
@@ -972,11 +994,8 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
               *reinterpret_cast<const float4*>(stg + rr * 32 + ((uu ^ (rr & 7)) * 4));
           const int kr = rbase + rr;
           if (kr < a.T && a.fin) {  // last term of the sum: add, round, write the bf16 row
-            const float* src = acc + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * uu;
-            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (!a.store) t = *reinterpret_cast<const float4*>(src);
-            t = make_float4(__fadd_rn(t.x, x.x), __fadd_rn(t.y, x.y), __fadd_rn(t.z, x.z),
-                            __fadd_rn(t.w, x.w));
+            const float4 t = make_float4(__fadd_rn(prev[it].x, x.x), __fadd_rn(prev[it].y, x.y),
+                                         __fadd_rn(prev[it].z, x.z), __fadd_rn(prev[it].w, x.w));
             const int64_t orow = a.out_idx ? a.out_idx[kr] : kr;
             bf16* out = is_v ? a.dv_out : a.dk_out;
             if ((uint64_t)orow < (uint64_t)a.out_rows)

@@ -18,11 +18,11 @@ Diagram; "[PyTorch] Extend no-load-balance CP to the a2a comm type"):
                               order (the reorder the a2a page removes)
   attention fwd / bwd         cp_attn_fwd / cp_attn_bwd per rank
   unrestore + reduce-scatter  per-rank partial dK/dV summed in fp32 in
-                              original order; the last rank's call
-                              (cp_attn_bwd_final) adds its partial, rounds
-                              to bf16 and writes each row to its rank's shard
-                              (or cp_reduce_scatter_emul: gather by the
-                              rank's index + bf16 cast)
+                              original order, then cp_reduce_scatter_emul
+                              (gather by the rank's index + bf16 cast); or,
+                              optionally, the last rank's cp_attn_bwd_final
+                              adds its partial, rounds to bf16 and writes
+                              each row to its rank's shard
   dQ/dK/dV tail-zeroing       cp_zero_tail, gated by the host-known valid end
 
 Only argument marshalling and buffer management happen here; every step is
@@ -154,11 +154,15 @@ class CPAttention:
     """Buffers and the full emulated CP forward/backward for one plan."""
 
     def __init__(self, plan: CPPlan, fuse_q_gather: bool = False,
-                 fuse_reduce_scatter: bool = True):
+                 fuse_reduce_scatter: bool = False):
         self.plan = plan
         p = plan
-        # the last rank's backward finishes the dK/dV sums and writes the bf16
-        # shards itself (cp_attn_bwd_final) instead of a separate cast pass
+        # optionally the last rank's backward finishes the dK/dV sums and
+        # writes the bf16 shards itself (cp_attn_bwd_final) instead of a
+        # separate cast pass.  Off by default: it has to bring the earlier
+        # ranks' fp32 sums into the SM (the other ranks' adds happen in L2), and
+        # on the 32k-token / 16-document workload that costs more than the
+        # cast pass it saves.
         self.fuse_reduce_scatter = fuse_reduce_scatter
         # forward-only steps under DUAL_CHUNK_SWAP: the attention loads query
         # rows through the partition index (cp_attn_fwd_gather), no Q shard copy
@@ -257,11 +261,12 @@ class CPAttention:
     def backward(self, k_full, v_full, stream=None):
         """Every rank's backward; rank 0 stores its partial dK/dV into the fp32
         accumulators (no clearing pass), the others add theirs in rank order:
-        the emulated reduce-scatter's sum.  The last rank finishes it: its call
-        adds its partial, rounds the sums to bf16 and writes every rank's shard
-        rows of the rank-concatenated dK/dV (through the restore index under
-        DUAL_CHUNK_SWAP; NO_LOAD_BALANCE rows are already in that order) --
-        the unrestore + scatter of the reduce-scatter, fused."""
+        the emulated reduce-scatter's sum, then one cast launch scatters it to
+        the ranks' bf16 shards.  With fuse_reduce_scatter the last rank's call
+        finishes the sum instead: it adds its partial, rounds to bf16 and
+        writes every rank's shard rows of the rank-concatenated dK/dV (through
+        the restore index under DUAL_CHUNK_SWAP; NO_LOAD_BALANCE rows are
+        already in that order)."""
         p = self.plan
         last = p.cp - 1
         for r in range(p.cp):
