@@ -50,8 +50,6 @@ _SIGNATURES = {
                      ctypes.c_float, _P, _SZ, _P], _I),
     "cp_attn_bwd_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
                         ctypes.c_float, _I, _P, _SZ, _P], _I),
-    "cp_attn_bwd_final": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _SZ, _I64,
-                           _I, _I, _I, _I, _I, ctypes.c_float, _I, _P, _SZ, _P], _I),
     "cp_attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I,
                              _I, ctypes.c_float, _P], _I),
     "cp_p2p_meta_bytes": ([_I, _I64, _I], _SZ),
@@ -288,26 +286,6 @@ def cp_attn_bwd(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local,
         _check("cp_attn_bwd", lib().cp_attn_bwd(*args, *tail))
     else:
         _check("cp_attn_bwd_ex", lib().cp_attn_bwd_ex(*args, int(mode), *tail))
-
-
-def cp_attn_bwd_final(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local,
-                      dk_accum, dv_accum, dk_out, dv_out, d_out_idx, d_meta, total_tokens: int,
-                      cp_size: int, rank: int, strategy: int, softmax_scale: float, d_workspace,
-                      stream=None, mode: int = BWD_ACCUMULATE) -> None:
-    """The last rank's backward with the reduce-scatter epilogue fused in: the
-    finished dK/dV rows go, as bf16, to rows d_out_idx of dk_out / dv_out."""
-    _, H, D = k_full.shape
-    st = lib().cp_attn_bwd_final(
-        _dev(q_local, "q"), _dev(k_full, "k"), _dev(v_full, "v"), _dev(o_local, "o"),
-        _dev(lse_local, "lse"), _dev(do_local, "do"), _dev(dq_local, "dq"),
-        None if dk_accum is None else _dev(dk_accum, "dk_accum"),
-        None if dv_accum is None else _dev(dv_accum, "dv_accum"),
-        _dev(dk_out, "dk_out"), _dev(dv_out, "dv_out"),
-        None if d_out_idx is None else _dev(d_out_idx, "out_idx"), dk_out.shape[0],
-        _dev(d_meta, "meta"), d_meta.numel() * d_meta.element_size(), total_tokens, H, D,
-        cp_size, rank, strategy, float(softmax_scale), int(mode), _dev(d_workspace, "workspace"),
-        d_workspace.numel() * d_workspace.element_size(), _stream(stream))
-    _check("cp_attn_bwd_final", st)
 
 
 NOALLOC_MAX_SCRATCH_FLOATS = 1048576  # CP_NOALLOC_MAX_SCRATCH_FLOATS in cpthd.h

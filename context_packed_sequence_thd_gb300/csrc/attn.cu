@@ -143,32 +143,24 @@ extern "C" size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H) {
   return (size_t)s_local * H * sizeof(float);
 }
 
-namespace {
-
-// Shared body of the backward entry points; dk_out null: the partial dK/dV
-// go to the fp32 accumulators, else the finished sums go to dk_out / dv_out.
-int bwd_impl(const void* q_local, const void* k_full, const void* v_full, const void* o_local,
-             const float* lse_local, const void* do_local, void* dq_local, const float* dk_accum,
-             const float* dv_accum, void* dk_out, void* dv_out, const int32_t* out_idx,
-             int64_t out_rows, const void* d_meta, size_t meta_bytes, int64_t total_tokens, int H,
-             int D, int cp_size, int rank, cp_strategy_t strategy, float softmax_scale, int m,
-             void* d_workspace, size_t workspace_bytes, void* stream) {
+extern "C" int cp_attn_bwd_ex(const void* q_local, const void* k_full, const void* v_full,
+                              const void* o_local, const float* lse_local, const void* do_local,
+                              void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
+                              size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
+                              int rank, cp_strategy_t strategy, float softmax_scale,
+                              cp_bwd_mode_t mode, void* d_workspace, size_t workspace_bytes,
+                              void* stream) {
+  const int m = (int)mode;
   if ((m & ~7) != 0 || (m & 6) == 6) return CP_ERR_INVALID_ARG;
   int64_t s_local = 0;
   int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
                          rank, strategy, &s_local);
   if (st != CP_OK) return st;
-  const bool fin = dk_out != nullptr;
-  const bool need_acc = !fin || !(m & CP_BWD_STORE);  // a finishing first call reads none
-  if (!o_local || !lse_local || !do_local || !dq_local) return CP_ERR_INVALID_ARG;
-  if (need_acc && (!dk_accum || !dv_accum)) return CP_ERR_INVALID_ARG;
-  if (fin && (!dv_out || out_rows < total_tokens || out_rows > INT32_MAX))
+  if (!o_local || !lse_local || !do_local || !dq_local || !dk_accum || !dv_accum)
     return CP_ERR_INVALID_ARG;
   if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local) ||
       !cpthd_host::aligned16(do_local) || !cpthd_host::aligned16(dq_local) ||
-      !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum) ||
-      !cpthd_host::aligned16(dk_out) || !cpthd_host::aligned16(dv_out) ||
-      (reinterpret_cast<uintptr_t>(out_idx) & 3u))
+      !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum))
     return CP_ERR_ALIGNMENT;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
   if (s_local == 0) return CP_OK;
@@ -178,8 +170,7 @@ int bwd_impl(const void* q_local, const void* k_full, const void* v_full, const 
   AttnArgs a{};
   a.q = (const bf16*)q_local; a.k = (const bf16*)k_full; a.v = (const bf16*)v_full;
   a.out = (const bf16*)o_local; a.lse = const_cast<float*>(lse_local);
-  a.dout = (const bf16*)do_local; a.dq = (bf16*)dq_local;
-  a.dk = const_cast<float*>(dk_accum); a.dv = const_cast<float*>(dv_accum);
+  a.dout = (const bf16*)do_local; a.dq = (bf16*)dq_local; a.dk = dk_accum; a.dv = dv_accum;
   a.delta = (float*)d_workspace; a.meta = d_meta; a.meta_bytes = meta_bytes;
   a.T = (int)total_tokens; a.H = H; a.s_local = (int)s_local; a.cp = cp_size; a.rank = rank;
   a.strategy = (int)strategy; a.scale = softmax_scale; a.scale_log2 = softmax_scale * kLog2e;
@@ -190,39 +181,9 @@ int bwd_impl(const void* q_local, const void* k_full, const void* v_full, const 
   else attn_delta<128><<<dgrid, 256, 0, s>>>(a);
   if ((st = cpthd_host::launch_status()) != CP_OK) return st;
   return cpthd_attn_bwd_tc(q_local, k_full, v_full, do_local, lse_local, a.delta, dq_local,
-                           a.dk, a.dv, d_meta, meta_bytes, (int)total_tokens, H, D, (int)s_local,
-                           cp_size, rank, (int)strategy, softmax_scale, softmax_scale * kLog2e, m,
-                           dk_out, dv_out, out_idx, (int)(fin ? out_rows : 0), s);
-}
-
-}  // namespace
-
-extern "C" int cp_attn_bwd_ex(const void* q_local, const void* k_full, const void* v_full,
-                              const void* o_local, const float* lse_local, const void* do_local,
-                              void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
-                              size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
-                              int rank, cp_strategy_t strategy, float softmax_scale,
-                              cp_bwd_mode_t mode, void* d_workspace, size_t workspace_bytes,
-                              void* stream) {
-  return bwd_impl(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local, dk_accum,
-                  dv_accum, nullptr, nullptr, nullptr, 0, d_meta, meta_bytes, total_tokens, H, D,
-                  cp_size, rank, strategy, softmax_scale, (int)mode, d_workspace, workspace_bytes,
-                  stream);
-}
-
-extern "C" int cp_attn_bwd_final(const void* q_local, const void* k_full, const void* v_full,
-                                 const void* o_local, const float* lse_local, const void* do_local,
-                                 void* dq_local, const float* dk_accum, const float* dv_accum,
-                                 void* dk_out, void* dv_out, const int32_t* d_out_idx,
-                                 int64_t out_rows, const void* d_meta, size_t meta_bytes,
-                                 int64_t total_tokens, int H, int D, int cp_size, int rank,
-                                 cp_strategy_t strategy, float softmax_scale, cp_bwd_mode_t mode,
-                                 void* d_workspace, size_t workspace_bytes, void* stream) {
-  if (!dk_out) return CP_ERR_INVALID_ARG;
-  return bwd_impl(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local, dk_accum,
-                  dv_accum, dk_out, dv_out, d_out_idx, out_rows, d_meta, meta_bytes, total_tokens,
-                  H, D, cp_size, rank, strategy, softmax_scale, (int)mode, d_workspace,
-                  workspace_bytes, stream);
+                           dk_accum, dv_accum, d_meta, meta_bytes, (int)total_tokens, H, D,
+                           (int)s_local, cp_size, rank, (int)strategy, softmax_scale,
+                           softmax_scale * kLog2e, m, s);
 }
 
 extern "C" int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full,
@@ -314,5 +275,5 @@ extern "C" int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, cons
   return cpthd_attn_bwd_tc(q_local, k_full, v_full, do_local, lse_local, a.delta, dq_local,
                            dk_accum, dv_accum, d_meta, meta_bytes, (int)total_tokens, H, D,
                            (int)s_local, cp_size, rank, (int)strategy, softmax_scale,
-                           softmax_scale * kLog2e, 0, nullptr, nullptr, nullptr, 0, s);
+                           softmax_scale * kLog2e, 0, s);
 }

@@ -69,14 +69,6 @@ struct BwdArgs {
   float scale, scale_log2;
   int store;    // dK/dV partials stored (every row written) instead of added
   int dq_mode;  // 0: dQ stored as bf16; 1: stored as fp32; 2: added into fp32
-  // finishing call of a sum over ranks: dk/dv are read (unless store), the
-  // total is rounded to bf16 and written to row out_idx[key] (key if null)
-  // of dk_out / dv_out instead of going back to dk/dv
-  int fin;
-  bf16* dk_out;
-  bf16* dv_out;
-  const int32_t* out_idx;
-  int out_rows;
 };
 
 __device__ __forceinline__ bool meta_ok_bwd(const BwdArgs& a, const MetaHeader* h) {
@@ -898,33 +890,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       itm.load(m.korder, m.klists, k, a.H, n_kb);
       if (itm.nb == 0) {
         // no query of this rank attends these keys: a stored partial is zero
-        if (a.fin) {  // the finished sum is what the earlier ranks left (or zero)
-          const int rb = itm.tile * 128 + (warp & 3) * 32;
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32)
-#pragma unroll
-            for (int it = 0; it < 8; ++it) {
-              const int kr = rb + (lane >> 3) + 4 * it;
-              if (kr < a.T) {
-                const int64_t o = ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * (lane & 7);
-                const int64_t orow = a.out_idx ? a.out_idx[kr] : kr;
-                if ((uint64_t)orow >= (uint64_t)a.out_rows) {  // skipped, reported
-                  atomicCAS(&g_status_bwd_tc, 0, (int)CP_ERR_INVALID_ARG);
-                  continue;
-                }
-                const int64_t oo = (orow * a.H + itm.h) * D + c0 + 4 * (lane & 7);
-                float4 xk = make_float4(0.f, 0.f, 0.f, 0.f), xv = xk;
-                if (!a.store) {
-                  xk = *reinterpret_cast<const float4*>(a.dk + o);
-                  xv = *reinterpret_cast<const float4*>(a.dv + o);
-                }
-                *reinterpret_cast<uint2*>(a.dk_out + oo) =
-                    make_uint2(pack_bf16(xk.x, xk.y), pack_bf16(xk.z, xk.w));
-                *reinterpret_cast<uint2*>(a.dv_out + oo) =
-                    make_uint2(pack_bf16(xv.x, xv.y), pack_bf16(xv.z, xv.w));
-              }
-            }
-        } else if (a.store) {
+        if (a.store) {
           const int rb = itm.tile * 128 + (warp & 3) * 32;
           const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
@@ -941,37 +907,17 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         continue;
       }
-      const int rbase = itm.tile * 128 + (warp & 3) * 32;  // first key row of this warp
-      const bool read_acc = a.fin && !a.store;  // finishing a sum the earlier ranks left
-      if (read_acc && rbase + lane < a.T) {
-        // the earlier ranks' sums of this item's rows go to L2 while its products run
-        const int64_t o = ((int64_t)(rbase + lane) * a.H + itm.h) * D;
-#pragma unroll
-        for (int l = 0; l < D / 32; ++l) {
-          prefetch_l2(a.dk + o + 32 * l);
-          prefetch_l2(a.dv + o + 32 * l);
-        }
-      }
       if (!wait_warp(bar_addr(c.done), ii & 1)) {
         fail(&s_abort);
         break;
       }
       ++ii;
       tc_fence_after();
+      const int rbase = itm.tile * 128 + (warp & 3) * 32;  // first key row of this warp
 #pragma unroll 1
       for (int ch = 0; ch < 2 * (D / 32); ++ch) {
         const bool is_v = ch < D / 32;  // dV first, then dK
         const int c0 = (is_v ? ch : ch - D / 32) * 32;
-        // the earlier sums of this chunk, all in flight before any is used
-        float4 prev[8];
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int kr = rbase + (lane >> 3) + 4 * it;
-          prev[it] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (read_acc && kr < a.T)
-            prev[it] = __ldcs(reinterpret_cast<const float4*>(
-                (is_v ? a.dv : a.dk) + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * (lane & 7)));
-        }
         uint32_t v[32];
         tmem_ld32(tmem + lb + 256 + (is_v ? D : 0) + c0, v);
         if (ch == D / 32 - 1 || ch == 2 * (D / 32) - 1) {
@@ -993,17 +939,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           const float4 x =
               *reinterpret_cast<const float4*>(stg + rr * 32 + ((uu ^ (rr & 7)) * 4));
           const int kr = rbase + rr;
-          if (kr < a.T && a.fin) {  // last term of the sum: add, round, write the bf16 row
-            const float4 t = make_float4(__fadd_rn(prev[it].x, x.x), __fadd_rn(prev[it].y, x.y),
-                                         __fadd_rn(prev[it].z, x.z), __fadd_rn(prev[it].w, x.w));
-            const int64_t orow = a.out_idx ? a.out_idx[kr] : kr;
-            bf16* out = is_v ? a.dv_out : a.dk_out;
-            if ((uint64_t)orow < (uint64_t)a.out_rows)
-              *reinterpret_cast<uint2*>(out + (orow * a.H + itm.h) * D + c0 + 4 * uu) =
-                  make_uint2(pack_bf16(t.x, t.y), pack_bf16(t.z, t.w));
-            else  // skipped, reported
-              atomicCAS(&g_status_bwd_tc, 0, (int)CP_ERR_INVALID_ARG);
-          } else if (kr < a.T) {
+          if (kr < a.T) {
             float* dst = acc + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * uu;
             if (a.store)  // p + 0: the value the first addition into a cleared buffer gives
               *reinterpret_cast<float4*>(dst) =
@@ -1159,8 +1095,7 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
                       const float* lse, const float* delta, void* dq, float* dk, float* dv,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale, float scale_log2,
-                      int mode, void* dk_out, void* dv_out, const int32_t* out_idx,
-                      int out_rows, cudaStream_t s) {
+                      int mode, cudaStream_t s) {
   using namespace cpthd;
   BwdArgs a{};
   a.lse = lse;
@@ -1175,11 +1110,6 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
   a.scale_log2 = scale_log2;
   a.store = mode & 1;
   a.dq_mode = (mode & 2) ? 1 : (mode & 4) ? 2 : 0;
-  a.fin = dk_out != nullptr;
-  a.dk_out = (bf16*)dk_out;
-  a.dv_out = (bf16*)dv_out;
-  a.out_idx = out_idx;
-  a.out_rows = out_rows;
   return D == 64 ? launch_bwd_tc<64>(q, k, v, dout, a, s) : launch_bwd_tc<128>(q, k, v, dout, a, s);
 }
 

@@ -316,11 +316,9 @@ int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const voi
                       float scale_log2, cudaStream_t s);
 
 // tcgen05 dQ and dK/dV kernels (attn_bwd_tc.cu); Delta already in `delta`;
-// mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added);
-// dk_out non-null: finishing call (dK/dV sums rounded into dk_out/dv_out rows out_idx)
+// mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added)
 int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
                       const float* lse, const float* delta, void* dq, float* dk, float* dv,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale, float scale_log2,
-                      int mode, void* dk_out, void* dv_out, const int32_t* out_idx,
-                      int out_rows, cudaStream_t s);
+                      int mode, cudaStream_t s);

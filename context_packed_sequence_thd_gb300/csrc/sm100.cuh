@@ -106,10 +106,6 @@ __device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const void* map, ui
       "l"(map), "r"(bar), "r"(c0), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
       : "memory");
 }
-// bring one 128-byte line into L2 (no register result, nothing waits on it)
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
-}
 // generic-proxy writes to shared memory -> visible to the async proxy (MMA)
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");

@@ -19,10 +19,7 @@ Diagram; "[PyTorch] Extend no-load-balance CP to the a2a comm type"):
   attention fwd / bwd         cp_attn_fwd / cp_attn_bwd per rank
   unrestore + reduce-scatter  per-rank partial dK/dV summed in fp32 in
                               original order, then cp_reduce_scatter_emul
-                              (gather by the rank's index + bf16 cast); or,
-                              optionally, the last rank's cp_attn_bwd_final
-                              adds its partial, rounds to bf16 and writes
-                              each row to its rank's shard
+                              (gather by the rank's index + bf16 cast)
   dQ/dK/dV tail-zeroing       cp_zero_tail, gated by the host-known valid end
 
 Only argument marshalling and buffer management happen here; every step is
@@ -153,17 +150,9 @@ class CPPlan:
 class CPAttention:
     """Buffers and the full emulated CP forward/backward for one plan."""
 
-    def __init__(self, plan: CPPlan, fuse_q_gather: bool = False,
-                 fuse_reduce_scatter: bool = False):
+    def __init__(self, plan: CPPlan, fuse_q_gather: bool = False):
         self.plan = plan
         p = plan
-        # optionally the last rank's backward finishes the dK/dV sums and
-        # writes the bf16 shards itself (cp_attn_bwd_final) instead of a
-        # separate cast pass.  Off by default: it has to bring the earlier
-        # ranks' fp32 sums into the SM (the other ranks' adds happen in L2), and
-        # on the 32k-token / 16-document workload that costs more than the
-        # cast pass it saves.
-        self.fuse_reduce_scatter = fuse_reduce_scatter
         # forward-only steps under DUAL_CHUNK_SWAP: the attention loads query
         # rows through the partition index (cp_attn_fwd_gather), no Q shard copy
         self.fuse_q_gather = fuse_q_gather
@@ -261,39 +250,23 @@ class CPAttention:
     def backward(self, k_full, v_full, stream=None):
         """Every rank's backward; rank 0 stores its partial dK/dV into the fp32
         accumulators (no clearing pass), the others add theirs in rank order:
-        the emulated reduce-scatter's sum, then one cast launch scatters it to
-        the ranks' bf16 shards.  With fuse_reduce_scatter the last rank's call
-        finishes the sum instead: it adds its partial, rounds to bf16 and
-        writes every rank's shard rows of the rank-concatenated dK/dV (through
-        the restore index under DUAL_CHUNK_SWAP; NO_LOAD_BALANCE rows are
-        already in that order)."""
+        the emulated reduce-scatter's sum."""
         p = self.plan
-        last = p.cp - 1
         for r in range(p.cp):
-            mode = api.BWD_STORE if r == 0 else api.BWD_ACCUMULATE
             with self._timed("attn_bwd", stream):
-                if r == last and self.fuse_reduce_scatter:
-                    api.cp_attn_bwd_final(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
-                                          self.lse[r], p.local(self.doc, r), p.local(self.dqc, r),
-                                          self.dk_acc, self.dv_acc, self.dkc, self.dvc,
-                                          p.restore if p.strategy == DCS else None,
-                                          p.ranks[r].meta, p.T, p.cp, r, p.strategy, p.scale,
-                                          self.ws, stream, mode=mode)
-                else:
-                    api.cp_attn_bwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
-                                    self.lse[r], p.local(self.doc, r), p.local(self.dqc, r),
-                                    self.dk_acc, self.dv_acc, p.ranks[r].meta, p.T, p.cp, r,
-                                    p.strategy, p.scale, self.ws, stream, mode=mode)
+                api.cp_attn_bwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
+                                self.lse[r], p.local(self.doc, r), p.local(self.dqc, r),
+                                self.dk_acc, self.dv_acc, p.ranks[r].meta, p.T, p.cp, r,
+                                p.strategy, p.scale, self.ws, stream,
+                                mode=api.BWD_STORE if r == 0 else api.BWD_ACCUMULATE)
             self.launches += 3
-        if not self.fuse_reduce_scatter:
-            # the scatter half of the reduce-scatter for every rank in one launch:
-            # rank r's rows of the rank-concatenated dK/dV are the summed
-            # accumulators at its partition index (NO_LOAD_BALANCE: contiguous)
-            with self._timed("reduce_scatter_emul", stream):
-                api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc], [self.dkc, self.dvc],
-                                           p.idx_all if p.strategy == DCS else None, 0, p.T,
-                                           stream)
-            self.launches += 1
+        # the scatter half of the reduce-scatter for every rank in one launch:
+        # rank r's rows of the rank-concatenated dK/dV are the summed
+        # accumulators at its partition index (NO_LOAD_BALANCE: contiguous)
+        with self._timed("reduce_scatter_emul", stream):
+            api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc], [self.dkc, self.dvc],
+                                       p.idx_all if p.strategy == DCS else None, 0, p.T, stream)
+        self.launches += 1
         for r, rm in enumerate(p.ranks):
             if api.cp_zero_tail([p.local(self.dqc, r), p.local(self.dkc, r), p.local(self.dvc, r)],
                                 rm.valid_end, stream=stream):

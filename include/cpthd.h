@@ -332,31 +332,6 @@ int cp_p2p_index(const int32_t* d_cu, const int32_t* d_cup, int n_docs, int64_t 
 int cp_p2p_merge(const void* d_o_steps, const float* d_lse_steps, int n_steps, int64_t s_local,
                  int H, int D, void* d_out, float* d_lse, void* stream);
 
-/* The last call of an emulated reduce-scatter, with its epilogue fused in
- * ([AG] §Sequence Diagram: unrestore dK/dV, reduce-scatter): the same
- * backward as cp_attn_bwd_ex, but this rank's partial dK/dV is added to the
- * sums the earlier ranks left in dk_accum / dv_accum (read only; with
- * CP_BWD_STORE in mode there are no earlier ranks and they are not read and
- * may be NULL) and each finished row j, rounded to bf16, is written to row
- * d_out_idx[j] of dk_out / dv_out ([out_rows, H, D] bf16; d_out_idx int32
- * [total_tokens], 4-byte aligned, NULL = row j).  With d_out_idx = the
- * restore index of cp_partition_index this writes every rank's dK/dV shard
- * into the rank-concatenated buffer, the result cp_reduce_scatter_emul gives
- * after a plain last cp_attn_bwd_ex call, bitwise (the same fp32 addition,
- * the same rounding), without the fp32 write of the last partial and the
- * separate cast pass.  Every row of dk_out / dv_out named by d_out_idx is
- * written, including rows that no query of this rank attends.  A d_out_idx
- * value outside [0, out_rows) is skipped and sets the device status word.
- * dQ bits of mode as for cp_attn_bwd_ex. */
-int cp_attn_bwd_final(const void* q_local, const void* k_full, const void* v_full,
-                      const void* o_local, const float* lse_local, const void* do_local,
-                      void* dq_local, const float* dk_accum, const float* dv_accum, void* dk_out,
-                      void* dv_out, const int32_t* d_out_idx, int64_t out_rows,
-                      const void* d_meta, size_t meta_bytes, int64_t total_tokens, int H, int D,
-                      int cp_size, int rank, cp_strategy_t strategy, float softmax_scale,
-                      cp_bwd_mode_t mode, void* d_workspace, size_t workspace_bytes,
-                      void* stream);
-
 /* Largest Delta scratch cp_attn_bwd_noalloc can use: s_local*H <= this many
  * floats (4 MiB of device memory per GPU that loads the library). */
 #define CP_NOALLOC_MAX_SCRATCH_FLOATS 1048576

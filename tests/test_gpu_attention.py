@@ -14,10 +14,10 @@ from gpu_util import assert_close, assert_lse_close, dev, to_np
 pytestmark = pytest.mark.gpu
 
 
-def run(wl, strategy, d, tensors=None, bwd=True, fuse_reduce_scatter=False):
+def run(wl, strategy, d, tensors=None, bwd=True):
     t = wl.tensors() if tensors is None else tensors
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, d)
-    att = pipeline.CPAttention(plan, fuse_reduce_scatter=fuse_reduce_scatter)
+    att = pipeline.CPAttention(plan)
     g = {k: v.to(d) for k, v in t.items()}
     att.step(g["q"], g["k"], g["v"], g["do"] if bwd else None)
     torch.cuda.synchronize()
@@ -224,52 +224,3 @@ def test_tail_zeroing_gated_in_pipeline():
         last = plan.local(att.dqc, wl.cp - 1)
         assert torch.all(last[ends[-1]:] == 0)
 
-
-@pytest.mark.parametrize("make", [inputs.tiny, inputs.cfg2,
-                                  lambda: inputs.custom([7, 33, 1, 90], cp=4, padded=[8, 40, 8, 96]),
-                                  lambda: inputs.custom([300, 212], cp=1, H=2, D=128)],
-                         ids=["tiny", "cfg2", "ragged_padded", "cp1"])
-def test_fused_reduce_scatter_bitwise(make):
-    """The last rank's cp_attn_bwd_final (add its partial, round, write the
-    shard rows through the restore index) gives bitwise the dQ/dK/dV of the
-    plain last call followed by the separate cast pass."""
-    d = dev()
-    wl = make()
-    g = {k: v.to(d) for k, v in wl.tensors().items()}
-    for s in wl.strategies:
-        res = []
-        for fuse in (False, True):
-            plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, s, wl.pad_between_seqs, wl.H, wl.D, d)
-            att = pipeline.CPAttention(plan, fuse_reduce_scatter=fuse)
-            att.step(g["q"], g["k"], g["v"], g["do"])
-            torch.cuda.synchronize()
-            assert api.cp_device_status() == 0
-            res.append([x.clone() for x in (att.dqc, att.dkc, att.dvc)])
-        for a, b in zip(*res):
-            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-
-
-def test_fused_reduce_scatter_reports_bad_rows():
-    """An output row index outside dk_out is skipped and reported through the
-    device status word; the other rows are written."""
-    d = dev()
-    T, H, D = 256, 2, 64
-    cu = np.array([0, 256], dtype=np.int32)
-    plan = pipeline.CPPlan(cu, cu, 1, pipeline.NLB, 0, H, D, d)
-    g = torch.Generator().manual_seed(5)
-    q, k, v, do = (torch.randn(T, H, D, generator=g).bfloat16().to(d) for _ in range(4))
-    o = torch.empty_like(q)
-    lse = torch.empty(H, T, dtype=torch.float32, device=d)
-    api.cp_attn_fwd(q, k, v, o, lse, plan.ranks[0].meta, T, 1, 0, pipeline.NLB, plan.scale)
-    idx = torch.arange(T, dtype=torch.int32, device=d)
-    idx[3] = T + 7
-    dq = torch.empty_like(q)
-    dk = torch.zeros_like(q)
-    dv = torch.zeros_like(q)
-    ws = torch.empty(api.cp_attn_bwd_workspace_bytes(T, H), dtype=torch.uint8, device=d)
-    api.cp_attn_bwd_final(q, k, v, o, lse, do, dq, None, None, dk, dv, idx, plan.ranks[0].meta, T,
-                          1, 0, pipeline.NLB, plan.scale, ws, mode=api.BWD_STORE)
-    torch.cuda.synchronize()
-    assert api.cp_device_status(reset=True) == -1
-    assert api.cp_device_status() == 0
-    assert torch.all(dk[3] == 0) and torch.any(dk[4] != 0)
