@@ -39,10 +39,10 @@ WORKLOAD = "THD packed 32768 tokens: 16 docs, cp_size=4, H=16, D=128, bf16, caus
 
 
 # DRAM bytes (read + write) of one attn_bwd call, from one ncu capture of the current kernels
-# (profiles/attn_bwd_tc_cfg2_dcs_rank0.md): attn_dq_tc 494.5 + 23.0 MB, attn_dkdv_tc 467.8 +
-# 479.3 MB (rank 0, which stores its dK/dV partial); attn_delta (not captured) at its algorithmic
+# (profiles/attn_bwd_tc_cfg2_dcs_rank0.md): attn_dq_tc 495.0 + 22.9 MB, attn_dkdv_tc 467.9 +
+# 478.9 MB (rank 0, which stores its dK/dV partial); attn_delta (not captured) at its algorithmic
 # 2 x 33.6 MB read + 0.5 MB written.
-BWD_TRAFFIC_BYTES = int((494.5 + 23.0 + 467.8 + 479.3 + 67.1 + 0.5) * 1e6)
+BWD_TRAFFIC_BYTES = int((495.0 + 22.9 + 467.9 + 478.9 + 67.1 + 0.5) * 1e6)
 BWD_TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the DUAL_CHUNK_SWAP rank-0 call "
                     "(dq + dkdv kernels measured, delta at its algorithmic bytes); rank 0 stores its fp32 "
                     "dK/dV partial (479 MB written), ranks 1-3 add theirs and also read the 537 MB")
