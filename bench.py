@@ -65,6 +65,24 @@ def _dist():
     return ws, rank
 
 
+def _max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings over the process group (the
+    slowest replica sets the time); the values themselves with one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def _whole_job_value(ws, flop_per_step, ms_per_step):
+    """TFLOP/s of all replicas together: each of the ws replicas does
+    flop_per_step per step, and a step lasts the slowest replica's time."""
+    return ws * flop_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 def _workload():
     from context_packed_sequence_thd_gb300 import inputs
     return inputs.cfg2()
@@ -182,11 +200,7 @@ def run_own(args):
         torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    ms = t0.elapsed_time(t1) / args.steps
-    if ws > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = _max_over_ranks([t0.elapsed_time(t1) / args.steps], dev)[0]
     launches = sum(a.launches for a in atts)
 
     # per-call breakdown from the events recorded inside the timed region
@@ -289,16 +303,12 @@ def run_own(args):
     stream.wait_event(out_done[(e2e_steps - 1) & 1])
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if ws > 1:
-        tt = torch.tensor([e2e_ms, e2e_serial_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms, e2e_serial_ms = (float(x) for x in tt.tolist())
+    e2e_ms, e2e_serial_ms = _max_over_ranks([e0.elapsed_time(e1) / e2e_steps, e2e_serial_ms], dev)
     assert api.cp_device_status() == 0, "device status after timing"
 
     result = None
     if rank == 0:
-        value = ws * flop_step / (ms * 1e-3) / 1e12
+        value = _whole_job_value(ws, flop_step, ms)
         peak = bf16_sust
         result = {
             "metric": METRIC,
@@ -325,13 +335,13 @@ def run_own(args):
                          "traffic_note": BWD_TRAFFIC_NOTE if dominant == "attn_bwd" else None},
             "gpu_launches": launches,
             "clocks": clk.summary(),
-            "e2e": {"value": round(ws * flop_step / (e2e_ms * 1e-3) / 1e12, 3),
+            "e2e": {"value": round(_whole_job_value(ws, flop_step, e2e_ms), 3),
                     "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps,
                     "copies": "pinned host; next step's inputs in and previous step's outputs "
                               "out on copy streams, overlapped with the step",
-                    "serial": {"value": round(ws * flop_step / (e2e_serial_ms * 1e-3) / 1e12, 3),
+                    "serial": {"value": round(_whole_job_value(ws, flop_step, e2e_serial_ms), 3),
                                "ms_per_step": round(e2e_serial_ms, 4)}},
             "breakdown_ms_per_step": {k: round(v, 4) for k, v in cat_total.items()},
             "attn_fwd_tflops": round(fwd_flop_per_call / (fwd_ms * 1e-3) / 1e12, 2),
