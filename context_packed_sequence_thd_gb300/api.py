@@ -37,6 +37,7 @@ _SIGNATURES = {
     "cp_valid_end": ([_P, _P, _I, _I, _I, _I, _I, ctypes.POINTER(_I64)], _I),
     "cp_meta_bytes": ([_I, _I64, _I], _SZ),
     "cp_partition_index": ([_P, _P, _I, _I64, _I, _I, _I, _I, _P, _P, _P, _SZ, _P], _I),
+    "cp_partition_index_all": ([_P, _P, _I, _I64, _I, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "cp_thd_gather": ([_P, _P, _I, _P, _I64, _I64, _I64, _P], _I),
     "cp_thd_scatter": ([_P, _P, _I, _P, _I64, _I64, _I64, _P], _I),
     "cp_reduce_scatter_emul": ([_P, _P, _I, _P, _I64, _I64, _I64, _I, _I, _P], _I),
@@ -179,6 +180,23 @@ def cp_partition_index(d_cu: Optional[torch.Tensor], d_cup: torch.Tensor, total_
                                   _dev(d_meta, "meta"), d_meta.numel() * d_meta.element_size(),
                                   _stream(stream))
     _check("cp_partition_index", st)
+
+
+def cp_partition_index_all(d_cu: Optional[torch.Tensor], d_cup: torch.Tensor, total_tokens: int,
+                           cp_size: int, strategy: int, pad_between_seqs: int,
+                           d_idx_all: torch.Tensor, d_restore: Optional[torch.Tensor],
+                           d_meta: torch.Tensor, meta_stride: int, stream=None) -> None:
+    """Every rank's partition index and metadata in one launch (rank r's
+    metadata at byte r * meta_stride of d_meta)."""
+    if d_meta.numel() * d_meta.element_size() < cp_size * meta_stride:
+        raise ValueError("metadata buffer smaller than cp_size * meta_stride")
+    st = lib().cp_partition_index_all(None if d_cu is None else _dev(d_cu, "cu"),
+                                      _dev(d_cup, "cup"), d_cup.numel() - 1, total_tokens,
+                                      cp_size, strategy, pad_between_seqs,
+                                      _dev(d_idx_all, "idx_all"),
+                                      None if d_restore is None else _dev(d_restore, "restore"),
+                                      _dev(d_meta, "meta"), meta_stride, _stream(stream))
+    _check("cp_partition_index_all", st)
 
 
 def _row_bytes(t: torch.Tensor) -> int:

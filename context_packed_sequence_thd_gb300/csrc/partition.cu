@@ -98,8 +98,13 @@ __device__ void build_work_order(int2* lists, int n_qt, int n_kb, int* s_nb, boo
 
 __global__ void __launch_bounds__(kThreads, 1)
 partition_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup, int n_docs,
-                 int T, int cp, int rank, int strategy, int pad, int32_t* __restrict__ idx,
-                 int32_t* __restrict__ restore, char* __restrict__ meta) {
+                 int T, int cp, int rank0, int strategy, int pad, int32_t* __restrict__ idx0,
+                 int32_t* __restrict__ restore, char* __restrict__ meta0, size_t meta_stride) {
+  // CTA b builds rank rank0 + b: its index at idx0 + b*s_local, its metadata
+  // at meta0 + b*meta_stride (one CTA per rank, ranks independent)
+  const int rank = rank0 + blockIdx.x;
+  int32_t* idx = idx0 + (size_t)blockIdx.x * (T / cp);
+  char* meta = meta0 + (size_t)blockIdx.x * meta_stride;
   __shared__ int s_warp[32];
   __shared__ int s_err;
   __shared__ int s_valid_end;
@@ -476,7 +481,28 @@ extern "C" int cp_partition_index(const int32_t* d_cu, const int32_t* d_cup, int
   if (!cpthd_host::aligned16(d_meta)) return CP_ERR_ALIGNMENT;
   partition_kernel<<<1, 1024, 0, cpthd_host::as_stream(stream)>>>(
       d_cu, d_cup, n_docs, (int)total_tokens, cp_size, rank, (int)strategy,
-      pad_between_seqs ? 1 : 0, d_idx, d_restore, reinterpret_cast<char*>(d_meta));
+      pad_between_seqs ? 1 : 0, d_idx, d_restore, reinterpret_cast<char*>(d_meta), 0);
+  return cpthd_host::launch_status();
+}
+
+extern "C" int cp_partition_index_all(const int32_t* d_cu, const int32_t* d_cup, int n_docs,
+                                      int64_t total_tokens, int cp_size, cp_strategy_t strategy,
+                                      int pad_between_seqs, int32_t* d_idx_all,
+                                      int32_t* d_restore, void* d_meta, size_t meta_stride,
+                                      void* stream) {
+  if (!d_cup || !d_idx_all || !d_meta) return CP_ERR_INVALID_ARG;
+  if (pad_between_seqs && !d_cu) return CP_ERR_INVALID_ARG;
+  if (n_docs < 1 || cp_size < 1 || cp_size > 65535) return CP_ERR_INVALID_ARG;
+  if (strategy != CP_DUAL_CHUNK_SWAP && strategy != CP_NO_LOAD_BALANCE) return CP_ERR_INVALID_ARG;
+  if (total_tokens < 0 || total_tokens > INT32_MAX) return CP_ERR_INVALID_ARG;
+  if (total_tokens % cp_size) return CP_ERR_DIVISIBILITY;
+  const int64_t s_local = total_tokens / cp_size;
+  if (meta_stride < meta_bytes_for(n_docs, s_local, cp_size)) return CP_ERR_WORKSPACE;
+  if (!cpthd_host::aligned16(d_meta) || (meta_stride & 15)) return CP_ERR_ALIGNMENT;
+  partition_kernel<<<cp_size, 1024, 0, cpthd_host::as_stream(stream)>>>(
+      d_cu, d_cup, n_docs, (int)total_tokens, cp_size, 0, (int)strategy,
+      pad_between_seqs ? 1 : 0, d_idx_all, d_restore, reinterpret_cast<char*>(d_meta),
+      meta_stride);
   return cpthd_host::launch_status();
 }
 

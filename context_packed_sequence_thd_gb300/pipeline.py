@@ -5,8 +5,9 @@ on one stream.  The data movement the pages describe maps onto the library
 as follows ("[PyTorch] Add no-load-balance THD all-gather CP", §Sequence
 Diagram; "[PyTorch] Extend no-load-balance CP to the a2a comm type"):
 
-  get_batch_on_this_cp_rank   cp_partition_index + cp_thd_gather (Q/K/V/dO
-                              in one launch per rank, DUAL_CHUNK_SWAP); with
+  get_batch_on_this_cp_rank   cp_partition_index_all (every rank, one
+                              launch) + cp_thd_gather (Q/K/V/dO of every
+                              rank in one launch, DUAL_CHUNK_SWAP); with
                               NO_LOAD_BALANCE a rank's shard is a contiguous
                               slice, so no copy is made at all
   all-gather K/V              the ranks' local shards live side by side in one
@@ -111,11 +112,15 @@ class CPPlan:
         # [r*s_local, (r+1)*s_local), so idx_all indexes the rank-concatenated buffers
         self.idx_all = torch.empty(self.T, dtype=torch.int32, device=self.device)
         nbytes = api.cp_meta_bytes(self.n_docs, self.T, self.cp)
+        # the ranks' metadata side by side, 16-byte aligned: built in one launch
+        self.meta_stride = (nbytes + 15) // 16 * 16
+        self.meta_all = torch.empty(self.cp * self.meta_stride, dtype=torch.uint8,
+                                    device=self.device)
         self.ranks = []
         for r in range(self.cp):
             self.ranks.append(RankMeta(
                 idx=self.local(self.idx_all, r),
-                meta=torch.empty(nbytes, dtype=torch.uint8, device=self.device),
+                meta=self.meta_all[r * self.meta_stride:r * self.meta_stride + nbytes],
                 valid_end=api.cp_valid_end(self.cu, self.cup, self.cp, r, self.strategy, self.pad),
                 pairs=rank_pairs(self.cu, self.cup, self.cp, r, self.strategy, self.pad)))
         self.build_index()
@@ -137,11 +142,12 @@ class CPPlan:
         return 1.0 / math.sqrt(self.D)
 
     def build_index(self, stream=None) -> int:
-        """One partition launch per rank (fills idx, meta and the restore index)."""
-        for r, rm in enumerate(self.ranks):
-            api.cp_partition_index(self.d_cu if self.pad else None, self.d_cup, self.T, self.cp, r,
-                                   self.strategy, self.pad, rm.idx, self.restore, rm.meta, stream)
-        return self.cp
+        """Every rank's partition index, metadata and restore entries in one
+        launch (one CTA per rank)."""
+        api.cp_partition_index_all(self.d_cu if self.pad else None, self.d_cup, self.T, self.cp,
+                                   self.strategy, self.pad, self.idx_all, self.restore,
+                                   self.meta_all, self.meta_stride, stream)
+        return 1
 
     def local(self, buf: torch.Tensor, r: int) -> torch.Tensor:
         return buf[r * self.s_local:(r + 1) * self.s_local]

@@ -130,6 +130,18 @@ int cp_partition_index(const int32_t* d_cu, const int32_t* d_cup, int n_docs,
                        int pad_between_seqs, int32_t* d_idx, int32_t* d_restore, void* d_meta,
                        size_t meta_bytes, void* stream);
 
+/* Every rank's cp_partition_index in ONE launch (one CTA per rank): rank r
+ * writes d_idx_all[r*s_local .. (r+1)*s_local) (the ranks' indices side by
+ * side, i.e. the index of the rank-concatenated layout), its entries of
+ * d_restore (nullable; all total_tokens entries are written) and its
+ * metadata at d_meta + r*meta_stride.  meta_stride >= cp_meta_bytes and a
+ * multiple of 16 (else CP_ERR_WORKSPACE / CP_ERR_ALIGNMENT).  Results are
+ * byte for byte those of the cp_size single-rank calls. */
+int cp_partition_index_all(const int32_t* d_cu, const int32_t* d_cup, int n_docs,
+                           int64_t total_tokens, int cp_size, cp_strategy_t strategy,
+                           int pad_between_seqs, int32_t* d_idx_all, int32_t* d_restore,
+                           void* d_meta, size_t meta_stride, void* stream);
+
 /* ---------------------------------------------------------------------------
  * THD row gather / scatter: the index_select restore/unrestore of [AG]
  * §Sequence Diagram, bandwidth bound per [A2A] (paragraph on the 8xH200

@@ -126,6 +126,12 @@ def test_argument_validation_before_launch(lib):
     assert L.cp_partition_index(None, FAKE, 2, 25, 2, 0, 1, 0, FAKE, None, FAKE, 10 ** 6, None) == -2
     assert L.cp_partition_index(None, FAKE, 2, 24, 2, 0, 1, 0, FAKE, None, FAKE, 16, None) == -6
     assert L.cp_partition_index(None, FAKE, 2, 24, 2, 0, 1, 1, FAKE, None, FAKE, 10 ** 6, None) == -1
+    # every rank in one launch: stride not a multiple of 16, stride too small
+    step = api.cp_meta_bytes(2, 24, 2)
+    assert L.cp_partition_index_all(None, FAKE, 2, 24, 2, 0, 0, FAKE, None, FAKE,
+                                    (step + 15) // 16 * 16 + 8, None) == -4
+    assert L.cp_partition_index_all(None, FAKE, 2, 24, 2, 0, 0, FAKE, None, FAKE, 16, None) == -6
+    assert L.cp_partition_index_all(None, FAKE, 2, 25, 2, 1, 0, FAKE, None, FAKE, 4096, None) == -2
     # gather: misaligned pointer, bad row size, too many tensors
     assert L.cp_thd_gather(_arr(FAKE + 8), _arr(FAKE), 1, FAKE, 4, 4, 256, None) == -4
     assert L.cp_thd_gather(_arr(FAKE), _arr(FAKE), 1, FAKE, 4, 4, 255, None) == -4

@@ -141,3 +141,37 @@ def test_zero_tail_gate_and_device_form():
     w = torch.ones_like(z)
     api.cp_zero_tail([w], -1, ve)
     assert torch.all(w == 1)                                 # read on device: no tail, no writes
+
+
+@pytest.mark.parametrize("make", [inputs.tiny, inputs.cfg2, inputs.cfg5,
+                                  lambda: inputs.custom([0, 6, 0, 10], padded=[4, 8, 0, 12], cp=2),
+                                  lambda: inputs.custom([3, 5], padded=[4, 12], cp=1)],
+                         ids=["tiny", "cfg2", "cfg5", "empty_docs", "cp1"])
+def test_partition_index_all_ranks_one_launch_bytewise(make):
+    """cp_partition_index_all (one CTA per rank) writes byte for byte what the
+    cp single-rank calls write: indices, restore index and metadata."""
+    d = dev()
+    wl = make()
+    pad = wl.pad_between_seqs
+    d_cu = torch.from_numpy(np.asarray(wl.cu, dtype=np.int32)).to(d)
+    d_cup = torch.from_numpy(np.asarray(wl.cup, dtype=np.int32)).to(d)
+    T, cp, S = wl.total_tokens, wl.cp, wl.s_local
+    nbytes = api.cp_meta_bytes(wl.n_docs, T, cp)
+    stride = (nbytes + 15) // 16 * 16 + 32          # room between ranks stays untouched
+    for s in wl.strategies:
+        idx1 = torch.full((T,), -5, dtype=torch.int32, device=d)
+        res1 = torch.full((T,), -5, dtype=torch.int32, device=d)
+        meta1 = torch.full((cp * stride,), 0x5A, dtype=torch.uint8, device=d)
+        for r in range(cp):
+            api.cp_partition_index(d_cu if pad else None, d_cup, T, cp, r, s, pad,
+                                   idx1[r * S:(r + 1) * S], res1,
+                                   meta1[r * stride:r * stride + nbytes])
+        idx2 = torch.full_like(idx1, -5)
+        res2 = torch.full_like(res1, -5)
+        meta2 = torch.full_like(meta1, 0x5A)
+        api.cp_partition_index_all(d_cu if pad else None, d_cup, T, cp, s, pad, idx2, res2, meta2,
+                                   stride)
+        torch.cuda.synchronize()
+        assert api.cp_device_status() == 0
+        assert torch.equal(idx1, idx2) and torch.equal(res1, res2)
+        assert torch.equal(meta1, meta2)
