@@ -39,7 +39,7 @@ WORKLOAD = "THD packed 32768 tokens: 16 docs, cp_size=4, H=16, D=128, bf16, caus
 
 
 # DRAM bytes (read + write) of one attn_bwd call, from one ncu capture of the current kernels
-# (profiles/attn_bwd_tc_cfg2_dcs_rank0.md): attn_dq_tc 495.0 + 22.9 MB, attn_dkdv_tc 467.9 +
+# (the DUAL_CHUNK_SWAP rank-0 call of this workload): attn_dq_tc 495.0 + 22.9 MB, attn_dkdv_tc 467.9 +
 # 478.9 MB (rank 0, which stores its dK/dV partial); attn_delta (not captured) at its algorithmic
 # 2 x 33.6 MB read + 0.5 MB written.
 BWD_TRAFFIC_BYTES = int((495.0 + 22.9 + 467.9 + 478.9 + 67.1 + 0.5) * 1e6)

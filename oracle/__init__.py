@@ -21,10 +21,20 @@ Contents, each the plain definition of what the pages describe:
   gradient tail-zeroing clears, same issue, §Describe the bug).
 * ``attn_fwd`` / ``attn_bwd``  causal varlen attention, fp64, in
   ``cpthd_oracle.c`` (see its header for the formulas).
+* ``a2a_seq_to_head`` / ``a2a_head_to_seq``  the all-to-all exchange of the
+  a2a comm type, "[PyTorch] Extend no-load-balance CP to the a2a comm type",
+  first two paragraphs and §Diagram.
+* ``p2p_schedule`` / ``p2p_step_rows`` / ``p2p_attn_fwd`` / ``lse_merge``  the
+  ring (P2P) comm type of "THD P2P context-parallel regression when padded
+  cu_seqlens are value-equal but not object-identical", §Describe the bug.
+  The page names the comm type, not its arithmetic; these follow the usual
+  ring schedule (step i: the K/V shard of rank (r - i) mod cp) and the
+  log-sum-exp combination of partial softmaxes.
 
 Every function here is pinned by a ``-m "not gpu"`` test against something
 other than itself (hand-derived partitions, closed forms, torch's fp64 SDPA
-with an explicit mask and its autograd, finite differences).
+with an explicit mask and its autograd, finite differences, a brute-force
+softmax over a split key set).
 """
 from __future__ import annotations
 
