@@ -19,11 +19,15 @@
 //              from TMEM, masks by the row's key range, online softmax in the
 //              log2 domain (the row max is exchanged between the two warps
 //              through shared memory), rescales O only when the max grows by
-//              more than 2^8, writes P (bf16 pairs) back into TMEM over S, and
-//              normalises O and stores O / LSE.
+//              more than 2^8, writes P (bf16 pairs) back into TMEM over S
+//              (before any O rescale, so S and O are never live in registers
+//              together), and normalises O and stores O / LSE.
 //   warp 8     TMA producer: Q per item into one of two buffers, K tiles into
 //              a 3-stage ring released as soon as S is done, V tiles into a
 //              2-stage ring released after P V; K runs one block ahead of V.
+//              With a query index (cp_attn_fwd_gather) the Q tile is read
+//              straight from the unsharded source, every lane gathering four
+//              rows per copy (tile::gather4).
 //   warp 9     TMEM allocator and single-thread MMA issuer:
 //              S[g%2] = Q K_g^T (M=128, N=128, K=D, both operands K-major in
 //              shared memory) and O[item%2] += P_g V_g (M=128, N=D, K=128; A =

@@ -10,10 +10,15 @@
 // lists the attention kernels iterate: for every 128-row query tile the key
 // blocks it attends, for every 128-key block the query tiles attending it.
 //
-// One CTA of 1024 threads: documents are processed 1024 at a time; a
-// block-wide exclusive scan (warp __shfl_up_sync scans + one scan of the warp
-// totals) turns per-document segment counts and local row counts into
-// offsets.  A second pass writes the row tables, one warp per segment.
+// One CTA of 1024 threads per rank (cp_partition_index: one rank;
+// cp_partition_index_all: every rank of a plan in one launch): documents are
+// processed 1024 at a time; a block-wide exclusive scan (warp __shfl_up_sync
+// scans + one scan of the warp totals) turns per-document segment counts and
+// local row counts into offsets.  A second pass writes the row tables, one
+// warp per segment.
+//
+// Also the per-step metadata of the P2P ring comm type (p2p_index_kernel,
+// one CTA per ring step, every step of a rank in one launch).
 #include "common.cuh"
 
 namespace cpthd {
