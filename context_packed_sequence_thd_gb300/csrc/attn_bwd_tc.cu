@@ -588,6 +588,12 @@ struct KvCtl {
 // per-warp staging of the dK / dV epilogue follows KvCtl (16-byte aligned)
 __host__ __device__ constexpr int kv_ctl_bytes() { return (int)((sizeof(KvCtl) + 15) & ~(size_t)15); }
 constexpr int kStageBytes = 4 * 32 * 32 * 4;  // 4 epilogue warps x 32 rows x 32 fp32
+// the staging buffers start on a 1024-byte boundary: the 128-byte swizzle of
+// the bulk copies is a function of the shared-memory address
+template <int D>
+__host__ __device__ constexpr int kv_stage_offset() {
+  return (KvLayout<D>::BYTES + kv_ctl_bytes() + 1023) & ~1023;
+}
 
 
 // Per query step i the MMA thread issues S^T_i, then the previous step's
@@ -601,6 +607,7 @@ template <int D>
 __global__ void __launch_bounds__(kKvThr, 1)
 attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+             const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
              const BwdArgs a) {
   using L = KvLayout<D>;
   constexpr int BOXES = D / 64;
@@ -871,13 +878,15 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     // item's dV, then dK, 32 columns at a time, releases each accumulator as
     // soon as its last columns are in registers, and adds them into the fp32
     // accumulators.  This item is the only writer of these rows in this launch:
-    // one fp32 add per element, done in L2 without a round trip.  Each chunk
-    // is turned around in a private shared-memory buffer first (16-byte units
-    // of row r rotated by r & 7, conflict-free both ways), so one vector
-    // reduction covers 128 contiguous bytes of 4 rows.
+    // one fp32 add per element, done in L2 without a round trip.  Each 32 x 32
+    // chunk goes into a private shared-memory buffer in the 128-byte swizzle
+    // order (16-byte unit u of row r at u ^ (r & 7), conflict-free) and one
+    // bulk tensor copy per chunk adds it to (or, first rank, stores it in) the
+    // accumulators: cp.reduce.async.bulk.tensor ... .add, issued by lane 0.
     const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
-    float* stg = reinterpret_cast<float*>(smem_raw + L::BYTES + kv_ctl_bytes()) +
+    float* stg = reinterpret_cast<float*>(smem_raw + kv_stage_offset<D>()) +
                  (warp - kKvEpi0) * 32 * 32;
+    const uint32_t stg_s = smem_u32(stg);
     auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
       const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
       return __all_sync(0xffffffffu, w);
@@ -925,32 +934,39 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           mbar_arrive(bar_addr(is_v ? c.dv_free : c.dk_free));
         }
         const float sc = is_v ? 1.f : a.scale;
-        float* acc = is_v ? a.dv : a.dk;
+        // the previous chunk's bulk copy has finished reading the staging buffer
+        if (lane == 0) bulk_wait_read_all();
         __syncwarp();
+        // row `lane` of the 32 x 32 chunk, its 16-byte units in the 128-byte
+        // swizzle order the tensor map's box uses (unit u at u ^ (row & 7));
+        // a stored partial is p + 0, the value the first addition into a
+        // cleared buffer gives
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<float4*>(stg + lane * 32 + ((u ^ (lane & 7)) * 4)) =
-              make_float4(__uint_as_float(v[4 * u]) * sc, __uint_as_float(v[4 * u + 1]) * sc,
-                          __uint_as_float(v[4 * u + 2]) * sc, __uint_as_float(v[4 * u + 3]) * sc);
+        for (int u = 0; u < 8; ++u) {
+          float4 x = make_float4(__uint_as_float(v[4 * u]) * sc, __uint_as_float(v[4 * u + 1]) * sc,
+                                 __uint_as_float(v[4 * u + 2]) * sc,
+                                 __uint_as_float(v[4 * u + 3]) * sc);
+          if (a.store)
+            x = make_float4(__fadd_rn(x.x, 0.f), __fadd_rn(x.y, 0.f), __fadd_rn(x.z, 0.f),
+                            __fadd_rn(x.w, 0.f));
+          *reinterpret_cast<float4*>(stg + lane * 32 + ((u ^ (lane & 7)) * 4)) = x;
+        }
+        fence_proxy_async_smem();
         __syncwarp();
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int rr = (lane >> 3) + 4 * it, uu = lane & 7;
-          const float4 x =
-              *reinterpret_cast<const float4*>(stg + rr * 32 + ((uu ^ (rr & 7)) * 4));
-          const int kr = rbase + rr;
-          if (kr < a.T) {
-            float* dst = acc + ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * uu;
-            if (a.store)  // p + 0: the value the first addition into a cleared buffer gives
-              *reinterpret_cast<float4*>(dst) =
-                  make_float4(__fadd_rn(x.x, 0.f), __fadd_rn(x.y, 0.f), __fadd_rn(x.z, 0.f),
-                              __fadd_rn(x.w, 0.f));
-            else
-              red_add_v4(dst, x.x, x.y, x.z, x.w);
-          }
+        // one bulk copy moves the chunk: rows rbase.. (those past T are not
+        // written), columns c0.., added in L2 (or stored by the first rank)
+        if (lane == 0 && rbase < a.T) {  // (a box wholly past the last key row is skipped)
+          const CUtensorMap* map = is_v ? &tm_dv : &tm_dk;
+          if (a.store) tma_store_3d(map, stg_s, c0, itm.h, rbase);
+          else tma_reduce_add_3d(map, stg_s, c0, itm.h, rbase);
+          bulk_commit();
         }
       }
     }
+    // every bulk copy of this warp has landed before the CTA (and its shared
+    // memory) goes away
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   } else {
     reg_alloc<kRegsCompute>();
     const int row = (warp & 3) * 32 + lane;  // TMEM lane = key row of the block
@@ -1056,14 +1072,16 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 template <int D>
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
                   const BwdArgs& a, cudaStream_t s) {
-  alignas(64) CUtensorMap mq, mdo, mk, mv;
+  alignas(64) CUtensorMap mq, mdo, mk, mv, mdk, mdv;
   int st;
   if ((st = tma::make_thd_map(&mq, q, a.s_local, a.H, D, 128)) != CP_OK) return st;
   if ((st = tma::make_thd_map(&mdo, dout, a.s_local, a.H, D, 128)) != CP_OK) return st;
   if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128)) != CP_OK) return st;
   if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128)) != CP_OK) return st;
+  if ((st = tma::make_f32_rows_map(&mdk, a.dk, a.T, a.H, D)) != CP_OK) return st;
+  if ((st = tma::make_f32_rows_map(&mdv, a.dv, a.T, a.H, D)) != CP_OK) return st;
   const int dq_smem = DqLayout<D>::BYTES + (int)sizeof(DqCtl);
-  const int kv_smem = KvLayout<D>::BYTES + kv_ctl_bytes() + kStageBytes;
+  const int kv_smem = kv_stage_offset<D>() + kStageBytes;
   if (cudaFuncSetAttribute(attn_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem) !=
           cudaSuccess ||
       cudaFuncSetAttribute(attn_dkdv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1082,7 +1100,8 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
     kv_regs = fa.numRegs;
   }
   if (kv_regs != kKvLaunchRegs) return CP_ERR_UNSUPPORTED;
-  attn_dkdv_tc<D><<<(int)(k_items < sms ? k_items : sms), kKvThr, kv_smem, s>>>(mq, mdo, mk, mv, a);
+  attn_dkdv_tc<D><<<(int)(k_items < sms ? k_items : sms), kKvThr, kv_smem, s>>>(mq, mdo, mk, mv,
+                                                                                  mdk, mdv, a);
   return cpthd_host::launch_status();
 }
 

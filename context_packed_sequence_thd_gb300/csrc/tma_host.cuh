@@ -57,5 +57,21 @@ inline int make_row_gather_map(CUtensorMap* map, const void* base, int64_t rows,
   return r == CUDA_SUCCESS ? CP_OK : CP_ERR_CUDA;
 }
 
+// fp32 [rows, H, D] viewed as a 3-D tensor (D, H, rows): boxes of 32 (d) x
+// 1 (head) x 32 (rows) = 32 rows of 128 bytes, 128-byte swizzle (the
+// shared-memory layout of the dK/dV epilogue's staging buffers).
+inline int make_f32_rows_map(CUtensorMap* map, const void* base, int64_t rows, int H, int D) {
+  auto enc = encode_fn();
+  if (!enc) return CP_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
+  cuuint32_t box[3] = {32, 1, 32};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CP_OK : CP_ERR_CUDA;
+}
+
 }  // namespace tma
 }  // namespace cpthd
