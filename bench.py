@@ -38,14 +38,13 @@ METRIC = "CP-rank causal THD attention TFLOP/s (% BF16 peak); THD gather GB/s (%
 WORKLOAD = "THD packed 32768 tokens: 16 docs, cp_size=4, H=16, D=128, bf16, causal fwd+bwd, both strategies"
 
 
-# DRAM bytes (read + write) of one attn_bwd call, from one ncu capture of the current kernels
-# (the DUAL_CHUNK_SWAP rank-0 call of this workload): attn_dq_tc 495.0 + 22.9 MB, attn_dkdv_tc 467.9 +
-# 478.9 MB (rank 0, which stores its dK/dV partial); attn_delta (not captured) at its algorithmic
-# 2 x 33.6 MB read + 0.5 MB written.
-BWD_TRAFFIC_BYTES = int((495.0 + 22.9 + 467.9 + 478.9 + 67.1 + 0.5) * 1e6)
-BWD_TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the DUAL_CHUNK_SWAP rank-0 call "
-                    "(dq + dkdv kernels measured, delta at its algorithmic bytes); rank 0 stores its fp32 "
-                    "dK/dV partial (479 MB written), ranks 1-3 add theirs and also read the 537 MB")
+# DRAM bytes (read + write) of one attn_bwd call from an ncu capture.  The last capture
+# (attn_dq_tc 495.0 + 22.9 MB, attn_dkdv_tc 467.9 + 478.9 MB for the DUAL_CHUNK_SWAP rank-0 call)
+# predates the dK/dV epilogue's move to bulk tensor reduce / store, so the figure is not
+# reported until the counters are taken again on the current kernel.
+BWD_TRAFFIC_BYTES = None
+BWD_TRAFFIC_NOTE = ("not re-captured since the dK/dV epilogue changed; the previous capture of the "
+                    "DUAL_CHUNK_SWAP rank-0 call read 963 MB and wrote 502 MB (dq + dkdv)")
 
 
 def _peaks():

@@ -32,10 +32,10 @@ def _json_lines(text):
     return [json.loads(line) for line in text.splitlines() if line.startswith("{")]
 
 
-def test_max_over_ranks_and_whole_job_value_world2():
-    out = _torchrun([os.path.join(ROOT, "tests", "replica_reduce_worker.py")], 300)
+def test_max_over_ranks_and_whole_job_value_world2(tmp_path):
+    out = _torchrun([os.path.join(ROOT, "tests", "replica_reduce_worker.py"), str(tmp_path)], 300)
     assert out.returncode == 0, out.stderr[-3000:]
-    res = sorted(_json_lines(out.stdout), key=lambda d: d["rank"])
+    res = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(2)]
     assert [d["rank"] for d in res] == [0, 1]
     for d in res:
         assert d["ws"] == 2
