@@ -24,8 +24,9 @@
 //              dV += P^T dO and dK += dS^T Q (A from TMEM, B = dO / Q as
 //              MN-major operands).  Each item's partial dK/dV are added into
 //              the caller's fp32 accumulators by the item's only owner, with
-//              fire-and-forget vector reductions (one add per element per
-//              launch, so the sums are still bitwise reproducible).
+//              bulk tensor reduce-adds of staged 32 x 32 chunks (one add per
+//              element per launch, so the sums are still bitwise
+//              reproducible).
 // Warp roles: warps 0-7 compute (warp w serves TMEM lanes 32*(w%4).. and the
 // column half w/4 of every row, so two warps share each row's elementwise
 // work), warp 8 TMA producer, warp 9 TMEM allocator + single-thread MMA

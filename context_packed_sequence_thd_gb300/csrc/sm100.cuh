@@ -208,14 +208,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Fire-and-forget fp32 add of four consecutive floats into global memory (the
-// addition happens in L2; `addr` must be 16-byte aligned).
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-
 // Register reallocation between warpgroups (executed by all four warps of a
 // warpgroup).  The increases draw on what the decreases released; the block's
 // total stays the registers it was launched with.
