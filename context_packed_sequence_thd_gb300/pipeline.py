@@ -388,6 +388,23 @@ class CPA2AAttention(CPAttention):
             self.backward(stream=stream)
 
 
+def ring_steps(cp: int, strategy: int) -> List[tuple]:
+    """The emulated ring's backward calls in execution order: (rank r, step i,
+    K/V owner j = (r - i) mod cp, cp_bwd_mode bits).  Under NO_LOAD_BALANCE
+    rank r runs steps 0..r only (the shards of later ranks hold later tokens).
+    The first call that touches shard j stores its dK/dV partial, later ones
+    add; a rank's first step stores its fp32 dQ, later steps add."""
+    out, written = [], set()
+    for r in range(cp):
+        for i in range(cp if strategy == DCS else r + 1):
+            j = (r - i) % cp
+            mode = api.BWD_ACCUMULATE if j in written else api.BWD_STORE
+            mode |= api.BWD_DQ_F32_STORE if i == 0 else api.BWD_DQ_F32_ACCUMULATE
+            written.add(j)
+            out.append((r, i, j, mode))
+    return out
+
+
 class CPP2PAttention(CPAttention):
     """The P2P (ring) comm type with every rank on one GPU ("THD P2P
     context-parallel regression when padded cu_seqlens are value-equal but not
@@ -424,7 +441,7 @@ class CPP2PAttention(CPAttention):
         self.build_p2p_index()
 
     def n_steps(self, r: int) -> int:
-        return self.plan.cp if self.plan.strategy == DCS else r + 1
+        return sum(1 for rr, _, _, _ in ring_steps(self.plan.cp, self.plan.strategy) if rr == r)
 
     def step_meta(self, r: int, i: int) -> torch.Tensor:
         return self.p2p_meta[r][i * self.step_bytes:(i + 1) * self.step_bytes]
@@ -458,20 +475,14 @@ class CPP2PAttention(CPAttention):
     def backward(self, k_full=None, v_full=None, stream=None):
         p = self.plan
         S = p.s_local
-        written = set()
-        for r in range(p.cp):
-            for i in range(self.n_steps(r)):
-                j = (r - i) % p.cp
-                mode = api.BWD_ACCUMULATE if j in written else api.BWD_STORE
-                mode |= api.BWD_DQ_F32_STORE if i == 0 else api.BWD_DQ_F32_ACCUMULATE
-                written.add(j)
-                with self._timed("attn_bwd", stream):
-                    api.cp_attn_bwd(p.local(self.qc, r), p.local(self.kc, j), p.local(self.vc, j),
-                                    p.local(self.oc, r), self.lse[r], p.local(self.doc, r),
-                                    p.local(self.dq_acc, r), p.local(self.dk_acc, j),
-                                    p.local(self.dv_acc, j), self.step_meta(r, i), S, 1, 0,
-                                    p.strategy, p.scale, self.ws, stream, mode=mode)
-                self.launches += 3
+        for r, i, j, mode in ring_steps(p.cp, p.strategy):
+            with self._timed("attn_bwd", stream):
+                api.cp_attn_bwd(p.local(self.qc, r), p.local(self.kc, j), p.local(self.vc, j),
+                                p.local(self.oc, r), self.lse[r], p.local(self.doc, r),
+                                p.local(self.dq_acc, r), p.local(self.dk_acc, j),
+                                p.local(self.dv_acc, j), self.step_meta(r, i), S, 1, 0,
+                                p.strategy, p.scale, self.ws, stream, mode=mode)
+            self.launches += 3
         with self._timed("grad_cast", stream):
             api.cp_reduce_scatter_emul([self.dq_acc, self.dk_acc, self.dv_acc],
                                        [self.dqc, self.dkc, self.dvc], None, 0, p.T, stream)

@@ -265,3 +265,34 @@ def test_lse_merge_of_a_key_split_is_the_full_softmax():
     np.testing.assert_allclose(l1, l_parts[0], atol=1e-15)
     o0, l0 = oracle.lse_merge(np.stack([o_parts[2]] * 2), np.stack([l_parts[2]] * 2))
     assert np.all(o0 == 0) and np.all(np.isneginf(l0))
+
+
+@pytest.mark.parametrize("strategy", [0, 1])
+def test_ring_backward_schedule(strategy):
+    """The emulated ring's backward calls: each rank walks the oracle's ring
+    order (all cp steps under DUAL_CHUNK_SWAP, steps 0..r under
+    NO_LOAD_BALANCE, whose later shards hold only later tokens -- the oracle's
+    brute force finds no visible key there); the first call touching a K/V
+    shard stores its dK/dV partial and later ones add; a rank's first step
+    stores its fp32 dQ and later ones add."""
+    from context_packed_sequence_thd_gb300 import api, pipeline
+    cu = cup = [0, 32, 48, 96, 128]
+    for cp in (1, 2, 4):
+        steps = pipeline.ring_steps(cp, strategy)
+        seen = set()
+        for r in range(cp):
+            mine = [(i, j, m) for rr, i, j, m in steps if rr == r]
+            ring = oracle.p2p_schedule(cp, r)
+            assert [j for _, j, _ in mine] == ring[:len(mine)]
+            assert [i for i, _, _ in mine] == list(range(len(mine)))
+            for i, j, m in mine:
+                assert (m & (api.BWD_DQ_F32_STORE | api.BWD_DQ_F32_ACCUMULATE)) == \
+                    (api.BWD_DQ_F32_STORE if i == 0 else api.BWD_DQ_F32_ACCUMULATE)
+            # the skipped steps have no visible key at all
+            for j in ring[len(mine):]:
+                _, hi = oracle.p2p_step_rows(cu, cup, cp, r, j, strategy, 0)
+                assert np.all(hi < 0)
+        for r, i, j, m in steps:
+            assert (m & api.BWD_STORE) == (0 if j in seen else api.BWD_STORE)
+            seen.add(j)
+        assert seen == set(range(cp))
