@@ -182,9 +182,10 @@ typedef enum {
 } cp_a2a_dir_t;
 
 /* All-to-all exchange of the a2a comm type ("[PyTorch] Extend no-load-balance
- * CP to the a2a comm type", ¶1-2, §Diagram), every rank on one GPU.  After the
- * exchange each rank holds the whole sequence and only its own head slice, so
- * its attention uses cp_size = 1 metadata.
+ * CP to the a2a comm type", ¶1-2, §Diagram), every rank on one GPU.  The
+ * exchange trades token shards for head slices: rank r ends up with all T
+ * tokens of heads [r*H/cp, (r+1)*H/cp), which makes its attention a cp_size = 1
+ * problem on that slice.
  *   sequence side: [T, H, D] rank-concatenated buffer (rank r's token shard
  *     is rows [r*T/cp, (r+1)*T/cp)).
  *   head side: cp buffers [T, H/cp, D] side by side ([cp, T, H/cp, D]); rank
@@ -361,8 +362,11 @@ int cp_p2p_merge(const void* d_o_steps, const float* d_lse_steps, int n_steps, i
  * that loads the library until the process exits); nothing is allocated or
  * freed.  s_local*H above that maximum returns CP_ERR_WORKSPACE before any
  * launch.  The first call on a device looks up that array's device address
- * (once per device, with that device current); make that first call before
- * any stream capture.  Every call shares the one array and leaves its last
+ * (with that device current) and keeps it for the device's current context;
+ * make that first call before any stream capture.  After a cudaDeviceReset
+ * the device gets a new context with the library's module loaded anew, and
+ * the first call in it looks the address up again (again: before any
+ * capture).  Every call shares the one array and leaves its last
  * contents there; each call rewrites all the scratch it reads before reading
  * it, so nothing has to start at zero.  Calls whose work overlaps on the GPU
  * (other streams, other host threads) race on the array: serialise them. */

@@ -198,24 +198,31 @@ def test_p2p_ring_visits_every_shard_once(strategy):
 
 
 @pytest.mark.parametrize("strategy", [0, 1])
-def test_p2p_step_keys_cover_the_causal_range(strategy):
+@pytest.mark.parametrize("cu,cup,pad,cp", [
+    ([0, 32, 48, 96, 128], [0, 32, 48, 96, 128], 0, 2),
+    # padded: 4, 5 and 3 padding rows at the ends of the documents (a padding
+    # query sees no key; no query sees a padding key)
+    ([0, 20, 23, 36], [0, 24, 32, 48], 1, 2),
+    ([0, 13, 13, 33], [0, 16, 24, 48], 1, 2),
+], ids=["unpadded", "padded", "padded_empty_doc"])
+def test_p2p_step_keys_cover_the_causal_range(strategy, cu, cup, pad, cp):
     """Over the ring's steps a query row's visible key ranges, mapped back to
-    global rows, are disjoint and together exactly [document start, row]."""
-    cu = cup = [0, 32, 48, 96, 128]
-    cp = 2
-    valid = oracle.valid_mask(cu, cup, 0)
+    global rows, are disjoint and together exactly [document start, row] for a
+    real token, and empty for a padding row."""
+    valid = oracle.valid_mask(cu, cup, pad)
     start = np.repeat(np.asarray(cup[:-1]), np.diff(cup))
     for r in range(cp):
         G_r = oracle.partition_index(cup, cp, r, strategy)
         seen = [[] for _ in G_r]
         for j in oracle.p2p_schedule(cp, r):
             G_j = oracle.partition_index(cup, cp, j, strategy)
-            lo, hi = oracle.p2p_step_rows(cu, cup, cp, r, j, strategy, 0)
+            lo, hi = oracle.p2p_step_rows(cu, cup, cp, r, j, strategy, pad)
             for t in range(len(G_r)):
                 seen[t].extend(G_j[lo[t]:hi[t] + 1].tolist())
         for t, g in enumerate(G_r):
             want = list(range(start[g], g + 1)) if valid[g] else []
             assert sorted(seen[t]) == want
+            assert all(valid[x] for x in seen[t])
 
 
 @pytest.mark.parametrize("strategy", [0, 1])
@@ -223,7 +230,7 @@ def test_p2p_merge_equals_full_attention(strategy):
     """Merging the ring's per-step partial softmaxes by their LSE gives the
     full causal attention (the ring only reorders the sum)."""
     rng = np.random.default_rng(17)
-    cu = [0, 20, 23, 48]
+    cu = [0, 20, 23, 36]
     cup = [0, 24, 32, 48]
     T, H, D = 48, 2, 8
     q, k, v = (rng.standard_normal((T, H, D)) for _ in range(3))
@@ -293,6 +300,26 @@ def test_ring_backward_schedule(strategy):
                 _, hi = oracle.p2p_step_rows(cu, cup, cp, r, j, strategy, 0)
                 assert np.all(hi < 0)
         for r, i, j, m in steps:
-            assert (m & api.BWD_STORE) == (0 if j in seen else api.BWD_STORE)
             seen.add(j)
         assert seen == set(range(cp))
+        # Replay the calls in order on buffers that start as garbage (NaN):
+        # a store overwrites, an add adds.  Every dK/dV shard buffer must end
+        # as the sum of every partial aimed at that shard, and every rank's dQ
+        # buffer as the sum of its steps' partials -- a wrong store/add rule
+        # either keeps the garbage or drops / doubles a term.
+        rng = np.random.default_rng(cp)
+        dkv = np.full(cp, np.nan)
+        dq = np.full(cp, np.nan)
+        want_kv, want_q = np.zeros(cp), np.zeros(cp)
+        for r, i, j, m in steps:
+            p_kv, p_q = float(rng.integers(1, 1000)), float(rng.integers(1, 1000))
+            want_kv[j] += p_kv
+            want_q[r] += p_q
+            dkv[j] = p_kv if m & api.BWD_STORE else dkv[j] + p_kv
+            if m & api.BWD_DQ_F32_STORE:
+                dq[r] = p_q
+            else:
+                assert m & api.BWD_DQ_F32_ACCUMULATE
+                dq[r] += p_q
+        np.testing.assert_array_equal(dkv, want_kv)
+        np.testing.assert_array_equal(dq, want_q)
