@@ -43,19 +43,20 @@ _SIGNATURES = {
     "cp_reduce_scatter_emul": ([_P, _P, _I, _P, _I64, _I64, _I64, _I, _I, _P], _I),
     "cp_a2a_exchange": ([_P, _P, _I, _P, _I64, _I, _I, _I, _I, _P], _I),
     "cp_zero_tail": ([_P, _I, _I64, _I64, _I64, _P, _P, ctypes.POINTER(_I)], _I),
-    "cp_attn_fwd": ([_P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I, ctypes.c_float, _P], _I),
-    "cp_attn_fwd_gather": ([_P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
+    "cp_attn_fwd": ([_P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I, ctypes.c_float,
+                     _P], _I),
+    "cp_attn_fwd_gather": ([_P, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
                            ctypes.c_float, _P], _I),
     "cp_attn_bwd_workspace_bytes": ([_I64, _I], _SZ),
-    "cp_attn_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
+    "cp_attn_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
                      ctypes.c_float, _P, _SZ, _P], _I),
-    "cp_attn_bwd_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
-                        ctypes.c_float, _I, _P, _SZ, _P], _I),
-    "cp_attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I,
-                             _I, ctypes.c_float, _P], _I),
+    "cp_attn_bwd_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I,
+                        _I, ctypes.c_float, _I, _P, _SZ, _P], _I),
+    "cp_attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I,
+                             _I, _I, ctypes.c_float, _P], _I),
     "cp_p2p_meta_bytes": ([_I, _I64, _I], _SZ),
     "cp_p2p_index": ([_P, _P, _I, _I64, _I, _I, _I, _I, _P, _SZ, _P], _I),
-    "cp_p2p_merge": ([_P, _P, _I, _I64, _I, _I, _P, _P, _P], _I),
+    "cp_p2p_merge": ([_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P], _I),
     "cp_device_status": ([ctypes.POINTER(_I), _I], _I),
 }
 
@@ -261,12 +262,19 @@ def cp_zero_tail(tensors: Sequence[torch.Tensor], valid_end: int,
     return bool(launched.value)
 
 
+def _opt(t, name):
+    return None if t is None else _dev(t, name)
+
+
 def cp_attn_fwd(q_local, k_full, v_full, o_local, lse_local, d_meta, total_tokens: int,
                 cp_size: int, rank: int, strategy: int, softmax_scale: float,
-                stream=None) -> None:
+                stream=None, o_resid=None) -> None:
+    """o_resid (optional, bf16 like o_local) receives O's bf16 rounding remainder,
+    which the backward's Delta uses."""
     _, H, D = k_full.shape
     st = lib().cp_attn_fwd(_dev(q_local, "q"), _dev(k_full, "k"), _dev(v_full, "v"),
-                           _dev(o_local, "o"), _dev(lse_local, "lse"), _dev(d_meta, "meta"),
+                           _dev(o_local, "o"), _opt(o_resid, "o_resid"), _dev(lse_local, "lse"),
+                           _dev(d_meta, "meta"),
                            d_meta.numel() * d_meta.element_size(), total_tokens, H, D, cp_size,
                            rank, strategy, float(softmax_scale), _stream(stream))
     _check("cp_attn_fwd", st)
@@ -274,12 +282,12 @@ def cp_attn_fwd(q_local, k_full, v_full, o_local, lse_local, d_meta, total_token
 
 def cp_attn_fwd_gather(q_src, d_idx, k_full, v_full, o_local, lse_local, d_meta,
                        total_tokens: int, cp_size: int, rank: int, strategy: int,
-                       softmax_scale: float, stream=None) -> None:
+                       softmax_scale: float, stream=None, o_resid=None) -> None:
     """cp_attn_fwd reading query row t from q_src[d_idx[t]] (no q_local copy)."""
     _, H, D = k_full.shape
     st = lib().cp_attn_fwd_gather(_dev(q_src, "q_src"), q_src.shape[0], _dev(d_idx, "idx"),
                                   _dev(k_full, "k"), _dev(v_full, "v"), _dev(o_local, "o"),
-                                  _dev(lse_local, "lse"), _dev(d_meta, "meta"),
+                                  _opt(o_resid, "o_resid"), _dev(lse_local, "lse"), _dev(d_meta, "meta"),
                                   d_meta.numel() * d_meta.element_size(), total_tokens, H, D,
                                   cp_size, rank, strategy, float(softmax_scale), _stream(stream))
     _check("cp_attn_fwd_gather", st)
@@ -290,11 +298,14 @@ BWD_ACCUMULATE, BWD_STORE, BWD_DQ_F32_STORE, BWD_DQ_F32_ACCUMULATE = 0, 1, 2, 4
 
 def cp_attn_bwd(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local, dk_accum,
                 dv_accum, d_meta, total_tokens: int, cp_size: int, rank: int, strategy: int,
-                softmax_scale: float, d_workspace, stream=None, mode: int = BWD_ACCUMULATE) -> None:
-    """cp_attn_bwd (mode BWD_ACCUMULATE) or cp_attn_bwd_ex with the given mode."""
+                softmax_scale: float, d_workspace, stream=None, mode: int = BWD_ACCUMULATE,
+                o_resid=None) -> None:
+    """cp_attn_bwd (mode BWD_ACCUMULATE) or cp_attn_bwd_ex with the given mode;
+    o_resid: the forward's O rounding remainder (optional)."""
     _, H, D = k_full.shape
     args = (_dev(q_local, "q"), _dev(k_full, "k"), _dev(v_full, "v"),
-            _dev(o_local, "o"), _dev(lse_local, "lse"), _dev(do_local, "do"),
+            _dev(o_local, "o"), _opt(o_resid, "o_resid"), _dev(lse_local, "lse"),
+            _dev(do_local, "do"),
             _dev(dq_local, "dq"), _dev(dk_accum, "dk"), _dev(dv_accum, "dv"),
             _dev(d_meta, "meta"), d_meta.numel() * d_meta.element_size(),
             total_tokens, H, D, cp_size, rank, strategy, float(softmax_scale))
@@ -311,13 +322,14 @@ NOALLOC_MAX_SCRATCH_FLOATS = 1048576  # CP_NOALLOC_MAX_SCRATCH_FLOATS in cpthd.h
 
 def cp_attn_bwd_noalloc(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local,
                         dk_accum, dv_accum, d_meta, total_tokens: int, cp_size: int, rank: int,
-                        strategy: int, softmax_scale: float, stream=None) -> None:
+                        strategy: int, softmax_scale: float, stream=None, o_resid=None) -> None:
     """cp_attn_bwd for callers that cannot allocate device memory: the Delta
     scratch is a fixed array inside the library (s_local*H <= 1,048,576
     floats).  Calls that overlap on the GPU share that array and race."""
     _, H, D = k_full.shape
     st = lib().cp_attn_bwd_noalloc(_dev(q_local, "q"), _dev(k_full, "k"), _dev(v_full, "v"),
-                                   _dev(o_local, "o"), _dev(lse_local, "lse"),
+                                   _dev(o_local, "o"), _opt(o_resid, "o_resid"),
+                                   _dev(lse_local, "lse"),
                                    _dev(do_local, "do"), _dev(dq_local, "dq"),
                                    _dev(dk_accum, "dk"), _dev(dv_accum, "dv"),
                                    _dev(d_meta, "meta"), d_meta.numel() * d_meta.element_size(),
@@ -342,11 +354,13 @@ def cp_p2p_index(d_cu: Optional[torch.Tensor], d_cup: torch.Tensor, total_tokens
 
 
 def cp_p2p_merge(o_steps: torch.Tensor, lse_steps: torch.Tensor, out: torch.Tensor,
-                 lse: torch.Tensor, stream=None) -> None:
-    """o_steps [n, s_local, H, D] bf16, lse_steps [n, H, s_local] -> out, lse."""
+                 lse: torch.Tensor, stream=None, o_steps_resid=None, out_resid=None) -> None:
+    """o_steps [n, s_local, H, D] bf16, lse_steps [n, H, s_local] -> out, lse;
+    optionally the steps' O rounding remainders in and the output's out."""
     n, s_local, H, D = o_steps.shape
-    st = lib().cp_p2p_merge(_dev(o_steps, "o_steps"), _dev(lse_steps, "lse_steps"), n, s_local,
-                            H, D, _dev(out, "out"), _dev(lse, "lse"), _stream(stream))
+    st = lib().cp_p2p_merge(_dev(o_steps, "o_steps"), _opt(o_steps_resid, "o_steps_resid"),
+                            _dev(lse_steps, "lse_steps"), n, s_local, H, D, _dev(out, "out"),
+                            _opt(out_resid, "out_resid"), _dev(lse, "lse"), _stream(stream))
     _check("cp_p2p_merge", st)
 
 

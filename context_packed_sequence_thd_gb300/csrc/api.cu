@@ -22,7 +22,7 @@ extern "C" const char* cp_status_string(int status) {
   }
 }
 
-extern "C" int cp_version(void) { return 100; }
+extern "C" int cp_version(void) { return 200; }
 
 // "THD P2P context-parallel regression when padded cu_seqlens are value-equal
 // but not object-identical", §Expected behavior: equal values mean no padding

@@ -15,6 +15,8 @@
 //               only scratch.
 #include <math.h>
 
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -36,6 +38,7 @@ struct AttnArgs {
   float* lse;        // [H, s_local]
   const bf16* dout;  // [s_local, H, D]
   const bf16* out;   // [s_local, H, D]  (forward output, for Delta)
+  const bf16* out_resid;  // nullable: O - bf16(O) from the forward, rounded to bf16
   float* delta;      // [H, s_local]
   bf16* dq;          // [s_local, H, D]
   float* dk;         // [T, H, D] fp32 accumulators
@@ -60,12 +63,17 @@ __global__ void __launch_bounds__(256) attn_delta(const AttnArgs a) {
   if (pair < n_pairs) {
     const uint4 x = *reinterpret_cast<const uint4*>(a.dout + pair * D + part * 8);
     const uint4 y = *reinterpret_cast<const uint4*>(a.out + pair * D + part * 8);
+    const uint4 z = a.out_resid ? *reinterpret_cast<const uint4*>(a.out_resid + pair * D + part * 8)
+                                : make_uint4(0, 0, 0, 0);
     const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&x);
     const __nv_bfloat162* yp = reinterpret_cast<const __nv_bfloat162*>(&y);
+    const __nv_bfloat162* zp = reinterpret_cast<const __nv_bfloat162*>(&z);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float2 fx = __bfloat1622float2(xp[i]), fy = __bfloat1622float2(yp[i]);
-      acc += fx.x * fy.x + fx.y * fy.y;
+      // O to about 16 bits: the bf16 output plus its rounding remainder (exact in fp32)
+      const float2 fx = __bfloat1622float2(xp[i]), fy = __bfloat1622float2(yp[i]),
+                   fz = __bfloat1622float2(zp[i]);
+      acc += fx.x * (fy.x + fz.x) + fx.y * (fy.y + fz.y);
     }
   }
 #pragma unroll
@@ -101,27 +109,32 @@ int common_checks(const void* q, const void* k, const void* v, const void* meta,
 using namespace cpthd;
 
 extern "C" int cp_attn_fwd(const void* q_local, const void* k_full, const void* v_full,
-                           void* o_local, float* lse_local, const void* d_meta, size_t meta_bytes,
-                           int64_t total_tokens, int H, int D, int cp_size, int rank,
-                           cp_strategy_t strategy, float softmax_scale, void* stream) {
+                           void* o_local, void* o_resid_local, float* lse_local,
+                           const void* d_meta, size_t meta_bytes, int64_t total_tokens, int H,
+                           int D, int cp_size, int rank, cp_strategy_t strategy,
+                           float softmax_scale, void* stream) {
   int64_t s_local = 0;
   int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
                          rank, strategy, &s_local);
   if (st != CP_OK) return st;
   if (!o_local || !lse_local) return CP_ERR_INVALID_ARG;
-  if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local)) return CP_ERR_ALIGNMENT;
+  if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local) ||
+      !cpthd_host::aligned16(o_resid_local))
+    return CP_ERR_ALIGNMENT;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
   if (s_local == 0) return CP_OK;
-  return cpthd_attn_fwd_tc(q_local, nullptr, 0, k_full, v_full, o_local, lse_local, d_meta,
-                           meta_bytes, (int)total_tokens, H, D, (int)s_local, cp_size, rank,
-                           (int)strategy, softmax_scale * kLog2e, cpthd_host::as_stream(stream));
+  return cpthd_attn_fwd_tc(q_local, nullptr, 0, k_full, v_full, o_local, o_resid_local, lse_local,
+                           d_meta, meta_bytes, (int)total_tokens, H, D, (int)s_local, cp_size,
+                           rank, (int)strategy, softmax_scale * kLog2e,
+                           cpthd_host::as_stream(stream));
 }
 
 extern "C" int cp_attn_fwd_gather(const void* q_src, int64_t src_rows, const int32_t* d_idx,
                                   const void* k_full, const void* v_full, void* o_local,
-                                  float* lse_local, const void* d_meta, size_t meta_bytes,
-                                  int64_t total_tokens, int H, int D, int cp_size, int rank,
-                                  cp_strategy_t strategy, float softmax_scale, void* stream) {
+                                  void* o_resid_local, float* lse_local, const void* d_meta,
+                                  size_t meta_bytes, int64_t total_tokens, int H, int D,
+                                  int cp_size, int rank, cp_strategy_t strategy,
+                                  float softmax_scale, void* stream) {
   int64_t s_local = 0;
   int st = common_checks(q_src, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
                          rank, strategy, &s_local);
@@ -129,13 +142,39 @@ extern "C" int cp_attn_fwd_gather(const void* q_src, int64_t src_rows, const int
   if (!o_local || !lse_local || !d_idx) return CP_ERR_INVALID_ARG;
   if (src_rows < 1 || src_rows > INT32_MAX) return CP_ERR_INVALID_ARG;
   if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local) ||
-      (reinterpret_cast<uintptr_t>(d_idx) & 3u))
+      !cpthd_host::aligned16(o_resid_local) || (reinterpret_cast<uintptr_t>(d_idx) & 3u))
     return CP_ERR_ALIGNMENT;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
   if (s_local == 0) return CP_OK;
-  return cpthd_attn_fwd_tc(q_src, d_idx, (int)src_rows, k_full, v_full, o_local, lse_local, d_meta,
-                           meta_bytes, (int)total_tokens, H, D, (int)s_local, cp_size, rank,
-                           (int)strategy, softmax_scale * kLog2e, cpthd_host::as_stream(stream));
+  return cpthd_attn_fwd_tc(q_src, d_idx, (int)src_rows, k_full, v_full, o_local, o_resid_local,
+                           lse_local, d_meta, meta_bytes, (int)total_tokens, H, D, (int)s_local,
+                           cp_size, rank, (int)strategy, softmax_scale * kLog2e,
+                           cpthd_host::as_stream(stream));
+}
+
+// Failure-detection test hook (not part of the ABI header): cp_attn_fwd
+// with every mbarrier wait bounded by limit_ns and the first K tile of CTA 0
+// never loaded, so that the wait for it runs out.  The CTA then drains its
+// copies, frees its tensor memory and returns; the device status word reads
+// CP_ERR_TIMEOUT and the context stays usable.  Nothing else sets the flag.
+extern "C" int cpthd_test_attn_fwd_timeout(const void* q_local, const void* k_full,
+                                           const void* v_full, void* o_local, float* lse_local,
+                                           const void* d_meta, size_t meta_bytes,
+                                           int64_t total_tokens, int H, int D, int cp_size,
+                                           int rank, cp_strategy_t strategy, float softmax_scale,
+                                           uint64_t limit_ns, void* stream) {
+  int64_t s_local = 0;
+  int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
+                         rank, strategy, &s_local);
+  if (st != CP_OK) return st;
+  if (!o_local || !lse_local) return CP_ERR_INVALID_ARG;
+  if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local)) return CP_ERR_ALIGNMENT;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
+  if (s_local == 0 || limit_ns == 0) return CP_ERR_INVALID_ARG;
+  return cpthd_attn_fwd_tc(q_local, nullptr, 0, k_full, v_full, o_local, nullptr, lse_local,
+                           d_meta, meta_bytes, (int)total_tokens, H, D, (int)s_local, cp_size,
+                           rank, (int)strategy, softmax_scale * kLog2e,
+                           cpthd_host::as_stream(stream), limit_ns, 1);
 }
 
 extern "C" size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H) {
@@ -144,7 +183,8 @@ extern "C" size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H) {
 }
 
 extern "C" int cp_attn_bwd_ex(const void* q_local, const void* k_full, const void* v_full,
-                              const void* o_local, const float* lse_local, const void* do_local,
+                              const void* o_local, const void* o_resid_local,
+                              const float* lse_local, const void* do_local,
                               void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
                               size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
                               int rank, cp_strategy_t strategy, float softmax_scale,
@@ -160,7 +200,8 @@ extern "C" int cp_attn_bwd_ex(const void* q_local, const void* k_full, const voi
     return CP_ERR_INVALID_ARG;
   if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local) ||
       !cpthd_host::aligned16(do_local) || !cpthd_host::aligned16(dq_local) ||
-      !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum))
+      !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum) ||
+      !cpthd_host::aligned16(o_resid_local))
     return CP_ERR_ALIGNMENT;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
   if (s_local == 0) return CP_OK;
@@ -169,7 +210,8 @@ extern "C" int cp_attn_bwd_ex(const void* q_local, const void* k_full, const voi
   if (!cpthd_host::aligned16(d_workspace)) return CP_ERR_ALIGNMENT;
   AttnArgs a{};
   a.q = (const bf16*)q_local; a.k = (const bf16*)k_full; a.v = (const bf16*)v_full;
-  a.out = (const bf16*)o_local; a.lse = const_cast<float*>(lse_local);
+  a.out = (const bf16*)o_local; a.out_resid = (const bf16*)o_resid_local;
+  a.lse = const_cast<float*>(lse_local);
   a.dout = (const bf16*)do_local; a.dq = (bf16*)dq_local; a.dk = dk_accum; a.dv = dv_accum;
   a.delta = (float*)d_workspace; a.meta = d_meta; a.meta_bytes = meta_bytes;
   a.T = (int)total_tokens; a.H = H; a.s_local = (int)s_local; a.cp = cp_size; a.rank = rank;
@@ -187,12 +229,14 @@ extern "C" int cp_attn_bwd_ex(const void* q_local, const void* k_full, const voi
 }
 
 extern "C" int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full,
-                           const void* o_local, const float* lse_local, const void* do_local,
+                           const void* o_local, const void* o_resid_local,
+                           const float* lse_local, const void* do_local,
                            void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
                            size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
                            int rank, cp_strategy_t strategy, float softmax_scale,
                            void* d_workspace, size_t workspace_bytes, void* stream) {
-  return cp_attn_bwd_ex(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local, dk_accum,
+  return cp_attn_bwd_ex(q_local, k_full, v_full, o_local, o_resid_local, lse_local, do_local,
+                        dq_local, dk_accum,
                         dv_accum, d_meta, meta_bytes, total_tokens, H, D, cp_size, rank, strategy,
                         softmax_scale, CP_BWD_ACCUMULATE, d_workspace, workspace_bytes, stream);
 }
@@ -218,19 +262,51 @@ static __device__ __align__(256) float g_noalloc_scratch[CP_NOALLOC_MAX_SCRATCH_
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 float* g_noalloc_ptr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};  // context the address belongs to
+
+// Unique id of the calling thread's current CUDA context (0 when none is
+// current or the driver cannot say).  A cudaDeviceReset ends the primary
+// context; the one that replaces it has a new id.
+unsigned long long current_context_id() {
+  static std::once_flag once;
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 // Device address of g_noalloc_scratch on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device, with that device current, and cached.
+// with the device current, once per device and context, and kept: a new
+// context on the device (after a cudaDeviceReset) has the module loaded anew,
+// so the address is looked up again.  Without a context id the lookup is
+// repeated on every call.
 int noalloc_scratch(float** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CP_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return CP_ERR_UNSUPPORTED;
+  const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (!g_noalloc_ptr[dev] || id == 0 || id != g_noalloc_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return CP_ERR_CUDA;
     g_noalloc_ptr[dev] = static_cast<float*>(p);
+    // the lookup made the device's primary context current if none was
+    g_noalloc_ctx[dev] = id != 0 ? id : current_context_id();
   }
   *out = g_noalloc_ptr[dev];
   return CP_OK;
@@ -239,7 +315,8 @@ int noalloc_scratch(float** out) {
 }  // namespace
 
 extern "C" int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, const void* v_full,
-                                   const void* o_local, const float* lse_local,
+                                   const void* o_local, const void* o_resid_local,
+                                   const float* lse_local,
                                    const void* do_local, void* dq_local, float* dk_accum,
                                    float* dv_accum, const void* d_meta, size_t meta_bytes,
                                    int64_t total_tokens, int H, int D, int cp_size, int rank,
@@ -252,7 +329,8 @@ extern "C" int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, cons
     return CP_ERR_INVALID_ARG;
   if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local) ||
       !cpthd_host::aligned16(do_local) || !cpthd_host::aligned16(dq_local) ||
-      !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum))
+      !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum) ||
+      !cpthd_host::aligned16(o_resid_local))
     return CP_ERR_ALIGNMENT;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
   if (s_local * (int64_t)H > (int64_t)CP_NOALLOC_MAX_SCRATCH_FLOATS) return CP_ERR_WORKSPACE;
@@ -261,7 +339,8 @@ extern "C" int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, cons
   if ((st = noalloc_scratch(&scratch)) != CP_OK) return st;
   AttnArgs a{};
   a.q = (const bf16*)q_local; a.k = (const bf16*)k_full; a.v = (const bf16*)v_full;
-  a.out = (const bf16*)o_local; a.lse = const_cast<float*>(lse_local);
+  a.out = (const bf16*)o_local; a.out_resid = (const bf16*)o_resid_local;
+  a.lse = const_cast<float*>(lse_local);
   a.dout = (const bf16*)do_local; a.dq = (bf16*)dq_local; a.dk = dk_accum; a.dv = dv_accum;
   a.delta = scratch; a.meta = d_meta; a.meta_bytes = meta_bytes;
   a.T = (int)total_tokens; a.H = H; a.s_local = (int)s_local; a.cp = cp_size; a.rank = rank;

@@ -123,6 +123,39 @@ __device__ __forceinline__ uint32_t kmajor_off(int kk) { return (kk >> 2) * kBox
 // column halves: elements [0,64) at columns [0,32), [64,128) at [64,96).
 __device__ __forceinline__ uint32_t ts_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
+// Two-term (hi, lo) bf16 A operands written chunk by chunk over fp32 columns
+// that were read first: each half's 64 elements arrive as two chunks of 32,
+// chunk c of half h read from columns [64h + 32c, 64h + 32c + 32) and
+// written back as its rounded values (16 columns) followed by their rounding
+// remainders (16 columns).  Column of the rounded part of k-step kk; the
+// remainder is 16 columns further.
+__device__ __forceinline__ uint32_t hilo_col(int kk) {
+  return (kk >> 2) * 64 + ((kk >> 1) & 1) * 32 + (kk & 1) * 8;
+}
+
+// Rounds 32 fp32 values to bf16 pairs and keeps the rounding remainders as a
+// second set of bf16 pairs: hi + lo carries about 16 significant bits.
+__device__ __forceinline__ void split_bf16(const float* x, uint32_t* hi, uint32_t* lo) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    hi[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+    lo[e] = pack_bf16(x[2 * e] - bf16_lo_f(hi[e]), x[2 * e + 1] - bf16_hi_f(hi[e]));
+  }
+}
+
+// p[e] = 2^(p[e] * scl - lse2) for 64 scores (lse2 in the log2 domain, one
+// per element pair or shared), the products in paired instructions.
+__device__ __forceinline__ void exp2_scores(float* p, uint64_t scl2, const uint64_t* nlse2,
+                                            int nlse_stride) {
+#pragma unroll
+  for (int c2 = 0; c2 < 32; ++c2) {
+    float a, b;
+    f2_unpack(f2_fma(f2_pack(p[2 * c2], p[2 * c2 + 1]), scl2, nlse2[c2 * nlse_stride]), a, b);
+    p[2 * c2] = ex2_approx(a);
+    p[2 * c2 + 1] = ex2_approx(b);
+  }
+}
+
 
 // ===========================================================================
 // dQ
@@ -140,10 +173,8 @@ struct DqLayout {
   static constexpr int BYTES = V + kDqVStages * TILE;
 };
 
-// TMEM of attn_dq_tc: S [0,128), dP [128,256), dQ [256,256+D), and two dS
-// buffers (bf16 pairs, 64 columns each) after dQ.
-template <int D>
-__host__ __device__ constexpr uint32_t dq_ds_col(int b) { return 256 + D + 64 * b; }
+// TMEM of attn_dq_tc: S [0,128), dP [128,256), dQ [256,256+D).  dS goes over
+// the dP columns it was computed from, as two bf16 terms (hi, lo; hilo_col).
 
 struct DqCtl {
   uint64_t qd_full, qd_free;  // Q/dO of the item landed / all its S, dP products done
@@ -299,11 +330,14 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tc_fence_after();
         const int ks = pend % kDqKStages;
         const uint64_t bk = sdesc_add(dsc_kmn, ks * L::TILE);
-        const uint32_t ads = tmem + dq_ds_col<D>(pend & 1);
+        // dS is the sum of two bf16 terms (rounded values, then their
+        // remainders): two products per k-step
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          umma_bf16_ts(tmem + 256, ads + (kk >> 2) * 32 + (kk & 3) * 8, sdesc_add(bk, kk * 2048), idQ,
+          const uint64_t b = sdesc_add(bk, kk * 2048);
+          umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk), b, idQ,
                        (!pend_first || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk) + 16, b, idQ, 1u);
           if (kk == 4 && vs_next >= 0 && !seen_v)
             seen_v = mbar_test_wait(bar_addr(c.v_full[vs_next]), (g_next / kDqVStages) & 1);
         }
@@ -442,6 +476,8 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const int hi = in ? m.row_hi[t] : -1;
       const float lse2 = hi >= 0 ? a.lse[(int64_t)itm.h * a.s_local + t] * kLog2ef : 0.f;
       const float dl = hi >= 0 ? a.delta[(int64_t)itm.h * a.s_local + t] : 0.f;
+      const uint64_t scl2 = f2_pack(sl2, sl2), nlse2 = f2_pack(-lse2, -lse2);
+      const uint64_t dl2 = f2_pack(dl, dl);
       Iter bi;
       bi.init(itm.list + 1, itm.n_iv());
       for (int j = 0; j < itm.nb; ++j, bi.next(), ++g) {
@@ -457,30 +493,37 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tc_fence_before();
         mbar_arrive(bar_addr(c.s_free));  // S_{g+1} may now overwrite S
         const int k0 = bi.b * 128 + 64 * hf;  // key of this thread's first column
-        if (lo <= k0 && hi >= k0 + 63) {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) p[e] = ex2_approx(fmaf(p[e], sl2, -lse2));
-        } else {
+        if (!(lo <= k0 && hi >= k0 + 63)) {  // keys outside the row's range: P = 0
 #pragma unroll
           for (int e = 0; e < 64; ++e)
-            p[e] = (k0 + e >= lo && k0 + e <= hi) ? ex2_approx(fmaf(p[e], sl2, -lse2)) : 0.f;
+            if (!(k0 + e >= lo && k0 + e <= hi)) p[e] = -INFINITY;
         }
+        exp2_scores(p, scl2, &nlse2, 0);
         if (!wait_warp(bar_addr(c.dp_full), g & 1)) {
           fail(&s_abort);
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t dsc = dq_ds_col<D>(g & 1) + 32 * hf;
+        // dS = P (dP - Delta) over the dP columns just read, as hi and lo bf16 terms
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          uint32_t dp[32], pk[16];
-          tmem_ld32(tmem + lb + 128 + 64 * hf + 32 * cc, dp);
+          uint32_t dp[32], hi[16], lo[16];
+          const uint32_t col = tmem + lb + 128 + 64 * hf + 32 * cc;
+          tmem_ld32(col, dp);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16(p[cc * 32 + 2 * e] * (__uint_as_float(dp[2 * e]) - dl),
-                              p[cc * 32 + 2 * e + 1] * (__uint_as_float(dp[2 * e + 1]) - dl));
-          tmem_st16(tmem + lb + dsc + 16 * cc, pk);
+          for (int e2 = 0; e2 < 16; ++e2) {
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(p[cc * 32 + 2 * e2], p[cc * 32 + 2 * e2 + 1]),
+                             f2_sub(f2_pack(__uint_as_float(dp[2 * e2]),
+                                            __uint_as_float(dp[2 * e2 + 1])), dl2)),
+                      x0, x1);
+            dp[2 * e2] = __float_as_uint(x0);
+            dp[2 * e2 + 1] = __float_as_uint(x1);
+          }
+          split_bf16(reinterpret_cast<const float*>(dp), hi, lo);
+          tmem_st16(col, hi);
+          tmem_st16(col + 16, lo);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -571,7 +614,7 @@ struct KvLayout {
 struct __align__(16) QInfo {  // per-query data of one 128-query step
   int lo[128];
   int hi[128];
-  float lse2[128];
+  float nlse2[128];  // -LSE * log2(e)
   float dl[128];
   int max_lo, min_hi;
   int pad[2];
@@ -730,7 +773,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           const int lo = in ? m.row_lo[t] : 0;
           qi.lo[cq] = lo;
           qi.hi[cq] = hi;
-          qi.lse2[cq] = hi >= 0 ? a.lse[(int64_t)it.h * a.s_local + t] * kLog2ef : 0.f;
+          qi.nlse2[cq] = hi >= 0 ? -a.lse[(int64_t)it.h * a.s_local + t] * kLog2ef : 0.f;
           qi.dl[cq] = hi >= 0 ? a.delta[(int64_t)it.h * a.s_local + t] : 0.f;
           mlo = max(mlo, lo);
           mhi = min(mhi, hi);
@@ -780,10 +823,14 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           return false;
         tc_fence_after();
         const uint64_t bq = sdesc_add(dsc_qmn, pend_st * L::TILE);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + 256, tmem + 128 + ts_col(kk), sdesc_add(bq, kk * 2048), idG,
+        // dS^T is the sum of two bf16 terms: two products per k-step
+#pragma unroll (D == 64 ? 8 : 4)
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t b = sdesc_add(bq, kk * 2048);
+          umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk), b, idG,
                        (!pend_first || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk) + 16, b, idG, 1u);
+        }
         umma_commit(bar_addr(c.q_empty[pend_st]));
         return true;
       };
@@ -848,12 +895,16 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           }
           tc_fence_after();
           // dV += P^T dO : A = P^T (TMEM over S^T), B = dO tile as MN-major (N = d);
-          // an item's first dV starts afresh once the previous dV has been read out
+          // an item's first dV starts afresh once the previous dV has been read out.
+          // P^T is the sum of two bf16 terms (rounded P, then its remainder), so
+          // the product carries P to about 16 bits instead of bf16's 8.
           const uint64_t bdm = sdesc_add(dsc_domn, st * L::TILE);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk), sdesc_add(bdm, kk * 2048), idG,
-                         (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll (D == 64 ? 8 : 4)  // (the spill-free unrolling of each instantiation)
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t b = sdesc_add(bdm, kk * 2048);
+            umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk), b, idG, (i > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk) + 32, b, idG, 1u);
+          }
           pend = gs;
           pend_st = st;
           pend_first = (i == 0);
@@ -997,19 +1048,22 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         tc_fence_after();
         const QInfo& qi = c.qinfo[st];
-        const float4* l4 = reinterpret_cast<const float4*>(qi.lse2 + 64 * hf);
-        const float4* d4 = reinterpret_cast<const float4*>(qi.dl + 64 * hf);
+        const float* nl = qi.nlse2 + 64 * hf;
+        const float* dl = qi.dl + 64 * hf;
         float p[64];
         tmem_ld32(tmem + lb + 64 * hf, reinterpret_cast<uint32_t*>(p));
         tmem_ld32(tmem + lb + 64 * hf + 32, reinterpret_cast<uint32_t*>(p + 32));
+        // (scalar arithmetic here: the paired forms need register pairs that this
+        // kernel's compute warps cannot spare without spilling)
+        const float4* l4 = reinterpret_cast<const float4*>(nl);
         if (key >= qi.max_lo && key <= qi.min_hi) {  // every query of the step sees this key
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
             const float4 l = l4[c4];
-            p[4 * c4 + 0] = ex2_approx(fmaf(p[4 * c4 + 0], sl2, -l.x));
-            p[4 * c4 + 1] = ex2_approx(fmaf(p[4 * c4 + 1], sl2, -l.y));
-            p[4 * c4 + 2] = ex2_approx(fmaf(p[4 * c4 + 2], sl2, -l.z));
-            p[4 * c4 + 3] = ex2_approx(fmaf(p[4 * c4 + 3], sl2, -l.w));
+            p[4 * c4 + 0] = ex2_approx(fmaf(p[4 * c4 + 0], sl2, l.x));
+            p[4 * c4 + 1] = ex2_approx(fmaf(p[4 * c4 + 1], sl2, l.y));
+            p[4 * c4 + 2] = ex2_approx(fmaf(p[4 * c4 + 2], sl2, l.z));
+            p[4 * c4 + 3] = ex2_approx(fmaf(p[4 * c4 + 3], sl2, l.w));
           }
         } else {
           const int4* lo4 = reinterpret_cast<const int4*>(qi.lo + 64 * hf);
@@ -1018,17 +1072,21 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           for (int c4 = 0; c4 < 16; ++c4) {
             const float4 l = l4[c4];
             const int4 lo = lo4[c4], hi = hi4[c4];
-            p[4 * c4 + 0] = (key >= lo.x && key <= hi.x) ? ex2_approx(fmaf(p[4 * c4 + 0], sl2, -l.x)) : 0.f;
-            p[4 * c4 + 1] = (key >= lo.y && key <= hi.y) ? ex2_approx(fmaf(p[4 * c4 + 1], sl2, -l.y)) : 0.f;
-            p[4 * c4 + 2] = (key >= lo.z && key <= hi.z) ? ex2_approx(fmaf(p[4 * c4 + 2], sl2, -l.z)) : 0.f;
-            p[4 * c4 + 3] = (key >= lo.w && key <= hi.w) ? ex2_approx(fmaf(p[4 * c4 + 3], sl2, -l.w)) : 0.f;
+            p[4 * c4 + 0] = (key >= lo.x && key <= hi.x) ? ex2_approx(fmaf(p[4 * c4 + 0], sl2, l.x)) : 0.f;
+            p[4 * c4 + 1] = (key >= lo.y && key <= hi.y) ? ex2_approx(fmaf(p[4 * c4 + 1], sl2, l.y)) : 0.f;
+            p[4 * c4 + 2] = (key >= lo.z && key <= hi.z) ? ex2_approx(fmaf(p[4 * c4 + 2], sl2, l.z)) : 0.f;
+            p[4 * c4 + 3] = (key >= lo.w && key <= hi.w) ? ex2_approx(fmaf(p[4 * c4 + 3], sl2, l.w)) : 0.f;
           }
         }
-        {  // P^T -> TMEM (bf16 pairs over this half's S^T columns)
-          uint32_t pk[32];
+        {  // P^T -> TMEM as two bf16 terms over this half's S^T columns: the
+           // rounded P (first 32 columns) and its rounding remainder (next 32)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
-          tmem_st32(tmem + lb + 64 * hf, pk);
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t ph[16], pl[16];
+            split_bf16(p + 32 * cc, ph, pl);
+            tmem_st16(tmem + lb + 64 * hf + 16 * cc, ph);
+            tmem_st16(tmem + lb + 64 * hf + 32 + 16 * cc, pl);
+          }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -1039,21 +1097,25 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           break;
         }
         tc_fence_after();
-        // dS^T = P^T (dP^T - Delta) -> TMEM over this half's dP^T columns (already read)
+        // dS^T = P^T (dP^T - Delta) over the dP^T columns just read, as hi and
+        // lo bf16 terms
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          uint32_t dp[32], pk[16];
-          tmem_ld32(tmem + lb + 128 + 64 * hf + 32 * cc, dp);
+          uint32_t dp[32], hi[16], lo[16];
+          const uint32_t col = tmem + lb + 128 + 64 * hf + 32 * cc;
+          tmem_ld32(col, dp);
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 d = d4[cc * 8 + e4];
+            const float4 d = reinterpret_cast<const float4*>(dl)[cc * 8 + e4];
             const int c0 = cc * 32 + 4 * e4;
-            pk[2 * e4] = pack_bf16(p[c0] * (__uint_as_float(dp[4 * e4]) - d.x),
-                                   p[c0 + 1] * (__uint_as_float(dp[4 * e4 + 1]) - d.y));
-            pk[2 * e4 + 1] = pack_bf16(p[c0 + 2] * (__uint_as_float(dp[4 * e4 + 2]) - d.z),
-                                       p[c0 + 3] * (__uint_as_float(dp[4 * e4 + 3]) - d.w));
+            dp[4 * e4] = __float_as_uint(p[c0] * (__uint_as_float(dp[4 * e4]) - d.x));
+            dp[4 * e4 + 1] = __float_as_uint(p[c0 + 1] * (__uint_as_float(dp[4 * e4 + 1]) - d.y));
+            dp[4 * e4 + 2] = __float_as_uint(p[c0 + 2] * (__uint_as_float(dp[4 * e4 + 2]) - d.z));
+            dp[4 * e4 + 3] = __float_as_uint(p[c0 + 3] * (__uint_as_float(dp[4 * e4 + 3]) - d.w));
           }
-          tmem_st16(tmem + lb + 128 + 64 * hf + 16 * cc, pk);
+          split_bf16(reinterpret_cast<const float*>(dp), hi, lo);
+          tmem_st16(col, hi);
+          tmem_st16(col + 16, lo);
         }
         tmem_st_wait();
         tc_fence_before();

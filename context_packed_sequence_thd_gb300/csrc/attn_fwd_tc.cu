@@ -65,7 +65,7 @@ constexpr int kKStages = 3;        // K ring depth (released after S)
 constexpr int kVStages = 2;        // V ring depth (released after P V)
 constexpr int kBoxBytes = 128 * 128;  // one 128-row x 128-byte TMA box
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // default bound of a wait
 constexpr float kLn2f = 0.6931471805599453f;
 
 template <int D>
@@ -83,6 +83,7 @@ __host__ __device__ constexpr uint32_t o_col(int b) { return 256 + b * D; }
 
 struct TcArgs {
   bf16* o;
+  bf16* o_resid;  // nullable: O - bf16(O), rounded to bf16 (the backward's Delta reads O + it)
   float* lse;
   const int32_t* q_idx;  // nullable: query row t is row q_idx[t] of a q_rows-row source
   int q_rows;
@@ -90,6 +91,8 @@ struct TcArgs {
   size_t meta_bytes;
   int T, H, s_local, cp, rank, strategy;
   float scale_log2;
+  uint64_t limit_ns;  // bound of every mbarrier wait
+  int skip_first_k;   // failure-detection test only: CTA 0 never loads its first K tile
 };
 
 struct Bars {
@@ -230,7 +233,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     }
     // lane 0 waits; the result is the warp's
     auto wait0 = [&](uint64_t& b, uint32_t parity) -> bool {
-      const bool w = lane == 0 ? mbar_wait(bar(b), parity, &s_abort, kWaitLimitNs) : true;
+      const bool w = lane == 0 ? mbar_wait(bar(b), parity, &s_abort, a.limit_ns) : true;
       return __shfl_sync(0xffffffffu, w, 0);
     };
     int ii = 0, g = 0, v_issued = 0;
@@ -300,7 +303,9 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           break;
         }
         const int key0 = bi.b * TBN;
-        if (lane == 0) {
+        // (the failure-detection test leaves CTA 0's first K tile unloaded: the
+        // MMA thread's bounded wait for it runs out and the CTA drains)
+        if (lane == 0 && !(a.skip_first_k && blockIdx.x == 0 && g == 0)) {
           mbar_arrive_expect_tx(bar(bars.k_full[ks]), L::TILE);
 #pragma unroll
           for (int b = 0; b < L::BOXES; ++b)
@@ -322,11 +327,11 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (lane == 0) {
       int never = 0;
       for (int i = max(0, ii - 2); i < ii; ++i)
-        mbar_wait(bar(bars.q_full[i & 1]), (i >> 1) & 1, &never, kWaitLimitNs);
+        mbar_wait(bar(bars.q_full[i & 1]), (i >> 1) & 1, &never, a.limit_ns);
       for (int j = max(0, g - kKStages); j < g; ++j)
-        mbar_wait(bar(bars.k_full[j % kKStages]), (j / kKStages) & 1, &never, kWaitLimitNs);
+        mbar_wait(bar(bars.k_full[j % kKStages]), (j / kKStages) & 1, &never, a.limit_ns);
       for (int j = max(0, v_issued - kVStages); j < v_issued; ++j)
-        mbar_wait(bar(bars.v_full[j % kVStages]), (j / kVStages) & 1, &never, kWaitLimitNs);
+        mbar_wait(bar(bars.v_full[j % kVStages]), (j / kVStages) & 1, &never, a.limit_ns);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -339,8 +344,8 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       bool pv_first = false;
       auto issue_pv = [&]() -> bool {
         const int vs = pv_g % kVStages;
-        if (!mbar_wait(bar(bars.p_full[pv_g & 1]), (pv_g >> 1) & 1, &s_abort, kWaitLimitNs) ||
-            !mbar_wait(bar(bars.v_full[vs]), (pv_g / kVStages) & 1, &s_abort, kWaitLimitNs))
+        if (!mbar_wait(bar(bars.p_full[pv_g & 1]), (pv_g >> 1) & 1, &s_abort, a.limit_ns) ||
+            !mbar_wait(bar(bars.v_full[vs]), (pv_g / kVStages) & 1, &s_abort, a.limit_ns))
           return false;
         tc_fence_after();
         // A = P from TMEM: keys [0,64) over columns [0,32) and keys [64,128)
@@ -365,7 +370,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         it.load(m, k, n_qt, a.H);
         if (it.nb == 0) continue;
         const int qb = ii & 1;
-        if (!mbar_wait(bar(bars.q_full[qb]), (ii >> 1) & 1, &s_abort, kWaitLimitNs)) {
+        if (!mbar_wait(bar(bars.q_full[qb]), (ii >> 1) & 1, &s_abort, a.limit_ns)) {
           fail(&s_abort);
           break;
         }
@@ -374,7 +379,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           const int ks = g % kKStages, buf = g & 1;
           // S_g overwrites P_{g-2} (same TMEM columns); P V_{g-2} was issued
           // earlier by this thread and MMAs of one thread run in order
-          if (!mbar_wait(bar(bars.k_full[ks]), (g / kKStages) & 1, &s_abort, kWaitLimitNs)) {
+          if (!mbar_wait(bar(bars.k_full[ks]), (g / kKStages) & 1, &s_abort, a.limit_ns)) {
             fail(&s_abort);
             ok = false;
             break;
@@ -404,7 +409,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       // drain: all MMAs issued by this thread must finish before TMEM is freed
       umma_commit(bar(bars.mma_done));
       int never = 0;
-      mbar_wait(bar(bars.mma_done), 0, &never, kWaitLimitNs);
+      mbar_wait(bar(bars.mma_done), 0, &never, a.limit_ns);
     }
   } else {
     // ---------------------------------------------------------------- softmax (warps 0-7)
@@ -420,7 +425,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // waits of the softmax warps are made warp-uniform (tcgen05.ld/st are
     // .sync.aligned): the warp proceeds only when every lane saw the phase
     auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
-      const bool w = mbar_wait(b, parity, &s_abort, kWaitLimitNs);
+      const bool w = mbar_wait(b, parity, &s_abort, a.limit_ns);
       return __all_sync(0xffffffffu, w);
     };
     // exchange u of the two warps of a pair: publish a value, wait for the
@@ -464,15 +469,28 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         uint32_t o[32];
         tmem_ld32(tmem + lane_base + o_col<D>(pend.ob) + col, o);
         if (in) {
-          uint4* dst = reinterpret_cast<uint4*>(a.o + ((int64_t)pend.t * a.H + pend.h) * D + col);
+          const int64_t off = ((int64_t)pend.t * a.H + pend.h) * D + col;
+          uint4* dst = reinterpret_cast<uint4*>(a.o + off);
+          uint4* dst_r = reinterpret_cast<uint4*>(a.o_resid + off);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(o[q * 8 + e]) * inv;
             uint4 v;
-            v.x = pack_bf16(__uint_as_float(o[q * 8 + 0]) * inv, __uint_as_float(o[q * 8 + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(o[q * 8 + 2]) * inv, __uint_as_float(o[q * 8 + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(o[q * 8 + 4]) * inv, __uint_as_float(o[q * 8 + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(o[q * 8 + 6]) * inv, __uint_as_float(o[q * 8 + 7]) * inv);
+            v.x = pack_bf16(x[0], x[1]);
+            v.y = pack_bf16(x[2], x[3]);
+            v.z = pack_bf16(x[4], x[5]);
+            v.w = pack_bf16(x[6], x[7]);
             dst[q] = v;
+            if (a.o_resid) {
+              uint4 r;
+              r.x = pack_bf16(x[0] - bf16_lo_f(v.x), x[1] - bf16_hi_f(v.x));
+              r.y = pack_bf16(x[2] - bf16_lo_f(v.y), x[3] - bf16_hi_f(v.y));
+              r.z = pack_bf16(x[4] - bf16_lo_f(v.z), x[5] - bf16_hi_f(v.z));
+              r.w = pack_bf16(x[6] - bf16_lo_f(v.w), x[7] - bf16_hi_f(v.w));
+              dst_r[q] = r;
+            }
           }
         }
       }
@@ -503,10 +521,15 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       const int t = itm.t0 + row;
       if (itm.nb == 0) {  // no real query row in this tile: O = 0, LSE = -inf
         if (t < a.s_local) {
-          uint4* dst =
-              reinterpret_cast<uint4*>(a.o + ((int64_t)t * a.H + itm.h) * D + hf * (D / 2));
+          const int64_t off = ((int64_t)t * a.H + itm.h) * D + hf * (D / 2);
+          uint4* dst = reinterpret_cast<uint4*>(a.o + off);
 #pragma unroll
           for (int c = 0; c < D / 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+          if (a.o_resid) {
+            uint4* dst_r = reinterpret_cast<uint4*>(a.o_resid + off);
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) dst_r[c] = make_uint4(0, 0, 0, 0);
+          }
           if (hf == 0) a.lse[(int64_t)itm.h * a.s_local + t] = -INFINITY;
         }
         continue;
@@ -546,13 +569,17 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (key < lo || key > hi) s[c] = -INFINITY;
           }
         }
+        // this half's row max: eight independent chains of three-input maxima
         float mx8[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) mx8[q] = s[q];
-#pragma unroll
-        for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int q = 0; q < 8; ++q) {
+          mx8[q] = fmax3(s[q], s[8 + q], s[16 + q]);
+          mx8[q] = fmax3(mx8[q], s[24 + q], s[32 + q]);
+          mx8[q] = fmax3(mx8[q], s[40 + q], s[48 + q]);
+          mx8[q] = fmaxf(mx8[q], s[56 + q]);
+        }
+        float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                         fmaxf(mx8[6], mx8[7]));
         float mx_other;
         if (!exchange(mx, &mx_other)) {
           fail(&s_abort);
@@ -573,14 +600,30 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           m_run = m_new;
         }
         const float mref = m_run == -INFINITY ? 0.f : m_run * sl2;
-        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // P = 2^(s * scale_log2 - mref) in pairs; every fourth pair on the FMA
+        // pipe (ex2_poly2), the rest on the SFU, so that neither unit alone
+        // sets the pace of the softmax
+        const uint64_t scl2 = f2_pack(sl2, sl2), nref2 = f2_pack(-mref, -mref);
+        uint64_t sum2[4];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          s[c] = ex2_approx(fmaf(s[c], sl2, -mref));
-          sum8[c & 7] += s[c];
+        for (int q = 0; q < 4; ++q) sum2[q] = f2_pack(0.f, 0.f);
+#pragma unroll
+        for (int c2 = 0; c2 < 32; ++c2) {
+          float a, b;
+          f2_unpack(f2_fma(f2_pack(s[2 * c2], s[2 * c2 + 1]), scl2, nref2), a, b);
+          if ((c2 & 3) == 3) {
+            ex2_poly2(a, b);
+          } else {
+            a = ex2_approx(a);
+            b = ex2_approx(b);
+          }
+          s[2 * c2] = a;
+          s[2 * c2 + 1] = b;
+          sum2[c2 & 3] = f2_add(sum2[c2 & 3], f2_pack(a, b));
         }
-        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                          ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        float sum, sum_b;
+        f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), sum, sum_b);
+        sum += sum_b;
         l_run = l_run * alpha + sum;
 
         {  // P (bf16 pairs) -> TMEM over the first 32 of this half's S columns;
@@ -669,12 +712,14 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, 
 
 // Internal entry used by cp_attn_fwd (arguments already validated).
 int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const void* k,
-                      const void* v, void* o, float* lse, const void* meta, size_t meta_bytes,
+                      const void* v, void* o, void* o_resid, float* lse, const void* meta,
+                      size_t meta_bytes,
                       int T, int H, int D, int s_local, int cp, int rank, int strategy,
-                      float scale_log2, cudaStream_t s) {
+                      float scale_log2, cudaStream_t s, uint64_t limit_ns, int skip_first_k) {
   using namespace cpthd;
   TcArgs a{};
   a.o = (bf16*)o;
+  a.o_resid = (bf16*)o_resid;
   a.lse = lse;
   a.q_idx = q_idx;
   a.q_rows = q_rows;
@@ -682,6 +727,8 @@ int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const voi
   a.meta_bytes = meta_bytes;
   a.T = T; a.H = H; a.s_local = s_local; a.cp = cp; a.rank = rank; a.strategy = strategy;
   a.scale_log2 = scale_log2;
+  a.limit_ns = limit_ns ? limit_ns : kWaitLimitNs;
+  a.skip_first_k = skip_first_k;
   return D == 64 ? launch_fwd_tc<64>(q, k, v, a, s) : launch_fwd_tc<128>(q, k, v, a, s);
 }
 

@@ -130,14 +130,6 @@ inline __device__ bool meta_matches(const MetaHeader* h, size_t meta_bytes, int 
          h->rank == rank && h->cp_size == cp && h->strategy == strategy && h->total_tokens == T;
 }
 
-// Copies a precomputed block list (count, then intervals) to out[]; returns
-// the interval count.
-inline __device__ int copy_list(const int2* list, int2* out) {
-  const int n = min(list[0].x, kListCap);
-  for (int i = 0; i < n; ++i) out[i] = list[1 + i];
-  return n;
-}
-
 // Index of the last segment whose local_start <= t (segments are sorted and
 // tile [0, s_local) without gaps).
 inline __device__ int find_segment_local(const Segment* segs, int n_segs, int t) {
@@ -226,43 +218,10 @@ inline __device__ int build_q_intervals(const MetaView& m, int j0, int j1, int B
 }
 
 // ---------------------------------------------------------------------------
-// small PTX helpers (sm_80+ forms that remain valid on sm_103a)
+// small helpers
 // ---------------------------------------------------------------------------
 inline __device__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-inline __device__ void cp_async_16(uint32_t dst, const void* src, bool pred) {
-  const int n = pred ? 16 : 0;  // 0 source bytes = zero fill
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n)
-               : "memory");
-}
-inline __device__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-inline __device__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
-
-inline __device__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                               uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-inline __device__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                 uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulators.
-inline __device__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 inline __device__ uint32_t pack_bf16(float lo, float hi) {
@@ -270,11 +229,10 @@ inline __device__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Byte offset of 16-byte chunk `c` of row `r` in a [rows][row_chunks*16 B]
-// tile whose chunks are XOR-swizzled by (r & 7) (conflict-free ldmatrix).
-inline __device__ uint32_t swz(int r, int c, int row_chunks) {
-  return (uint32_t)((r * row_chunks + (c ^ (r & 7))) * 16);
-}
+// The two bf16 values of a packed pair as fp32 (exact: a bf16 is the upper
+// half of an fp32 bit pattern).
+inline __device__ float bf16_lo_f(uint32_t p) { return __uint_as_float(p << 16); }
+inline __device__ float bf16_hi_f(uint32_t p) { return __uint_as_float(p & 0xFFFF0000u); }
 
 }  // namespace cpthd
 
@@ -309,11 +267,16 @@ extern "C" int cpthd_status_fwd_tc(int reset);
 extern "C" int cpthd_status_bwd_tc(int reset);
 
 // tcgen05 forward (attn_fwd_tc.cu); arguments validated by cp_attn_fwd /
-// cp_attn_fwd_gather (q_idx null: q is the rank's [s_local, H, D] queries)
+// cp_attn_fwd_gather (q_idx null: q is the rank's [s_local, H, D] queries;
+// o_resid nullable: O's bf16 rounding remainder, as bf16).
+// limit_ns bounds every wait (0: the 4 s default); skip_first_k != 0 only in
+// the failure-detection test (CTA 0 never loads its first K tile).
 int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const void* k,
-                      const void* v, void* o, float* lse, const void* meta, size_t meta_bytes,
+                      const void* v, void* o, void* o_resid, float* lse, const void* meta,
+                      size_t meta_bytes,
                       int T, int H, int D, int s_local, int cp, int rank, int strategy,
-                      float scale_log2, cudaStream_t s);
+                      float scale_log2, cudaStream_t s, uint64_t limit_ns = 0,
+                      int skip_first_k = 0);
 
 // tcgen05 dQ and dK/dV kernels (attn_bwd_tc.cu); Delta already in `delta`;
 // mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added)

@@ -8,7 +8,10 @@
 // log-sum-exp LSE_i (-inf where a row saw no key of the shard).  Attention
 // over the union of the shards is the softmax-weighted combination
 //   LSE = log sum_i exp(LSE_i),   O = sum_i exp(LSE_i - LSE) * O_i,
-// computed here in fp32 and rounded to bf16 once.
+// computed here in fp32 and rounded to bf16 once.  With the steps' rounding
+// remainders (O_i's bf16 remainder, as the attention forward writes it) the
+// sum reads O_i to about 16 bits, and the merged output's own remainder can
+// be written too, for the backward's Delta.
 //
 // Design: bandwidth bound (n_steps + 1 rows of 2*H*D bytes per (row, head)
 // pair moved, a few flops per byte).  One thread owns 8 columns (16 bytes)
@@ -33,8 +36,9 @@ __device__ __forceinline__ uint4 ld_once(const uint4* p) {
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
-p2p_merge_kernel(const uint4* __restrict__ o_steps, const float* __restrict__ lse_steps,
-                 int n_steps, int64_t s_local, int H, uint4* __restrict__ out,
+p2p_merge_kernel(const uint4* __restrict__ o_steps, const uint4* __restrict__ o_steps_resid,
+                 const float* __restrict__ lse_steps, int n_steps, int64_t s_local, int H,
+                 uint4* __restrict__ out, uint4* __restrict__ out_resid,
                  float* __restrict__ lse_out) {
   constexpr int G = D / 8;  // threads per (row, head) pair
   const int64_t n_pairs = s_local * H;
@@ -61,12 +65,15 @@ p2p_merge_kernel(const uint4* __restrict__ o_steps, const float* __restrict__ ls
         if (l == -INFINITY) continue;
         const float w = expf(l - lse);
         const uint4 x = ld_once(o_steps + s * n_chunks + i);
+        const uint4 xr = o_steps_resid ? ld_once(o_steps_resid + s * n_chunks + i)
+                                       : make_uint4(0, 0, 0, 0);
         const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&x);
+        const __nv_bfloat162* rp = reinterpret_cast<const __nv_bfloat162*>(&xr);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(xp[e]);
-          acc[2 * e] = fmaf(w, f.x, acc[2 * e]);
-          acc[2 * e + 1] = fmaf(w, f.y, acc[2 * e + 1]);
+          const float2 f = __bfloat1622float2(xp[e]), fr = __bfloat1622float2(rp[e]);
+          acc[2 * e] = fmaf(w, f.x + fr.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(w, f.y + fr.y, acc[2 * e + 1]);
         }
       }
     }
@@ -76,6 +83,14 @@ p2p_merge_kernel(const uint4* __restrict__ o_steps, const float* __restrict__ ls
     r.z = pack_bf16(acc[4], acc[5]);
     r.w = pack_bf16(acc[6], acc[7]);
     out[i] = r;
+    if (out_resid) {
+      uint4 q;
+      q.x = pack_bf16(acc[0] - bf16_lo_f(r.x), acc[1] - bf16_hi_f(r.x));
+      q.y = pack_bf16(acc[2] - bf16_lo_f(r.y), acc[3] - bf16_hi_f(r.y));
+      q.z = pack_bf16(acc[4] - bf16_lo_f(r.z), acc[5] - bf16_hi_f(r.z));
+      q.w = pack_bf16(acc[6] - bf16_lo_f(r.w), acc[7] - bf16_hi_f(r.w));
+      out_resid[i] = q;
+    }
     if (i % G == 0) lse_out[li] = lse;
   }
 }
@@ -85,15 +100,16 @@ p2p_merge_kernel(const uint4* __restrict__ o_steps, const float* __restrict__ ls
 
 using namespace cpthd;
 
-extern "C" int cp_p2p_merge(const void* d_o_steps, const float* d_lse_steps, int n_steps,
-                            int64_t s_local, int H, int D, void* d_out, float* d_lse,
-                            void* stream) {
+extern "C" int cp_p2p_merge(const void* d_o_steps, const void* d_o_steps_resid,
+                            const float* d_lse_steps, int n_steps, int64_t s_local, int H, int D,
+                            void* d_out, void* d_out_resid, float* d_lse, void* stream) {
   if (!d_o_steps || !d_lse_steps || !d_out || !d_lse) return CP_ERR_INVALID_ARG;
   if (n_steps < 1 || s_local < 0 || H < 1) return CP_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return CP_ERR_UNSUPPORTED;
   if (s_local * H * (int64_t)D * n_steps > ((int64_t)1 << 40)) return CP_ERR_UNSUPPORTED;
   if (!cpthd_host::aligned16(d_o_steps) || !cpthd_host::aligned16(d_lse_steps) ||
-      !cpthd_host::aligned16(d_out) || !cpthd_host::aligned16(d_lse))
+      !cpthd_host::aligned16(d_out) || !cpthd_host::aligned16(d_lse) ||
+      !cpthd_host::aligned16(d_o_steps_resid) || !cpthd_host::aligned16(d_out_resid))
     return CP_ERR_ALIGNMENT;
   if (s_local == 0) return CP_OK;
   const int64_t chunks = s_local * H * (D / 8);
@@ -102,12 +118,14 @@ extern "C" int cp_p2p_merge(const void* d_o_steps, const float* d_lse_steps, int
   const int grid = (int)std::min<int64_t>(want, (int64_t)sms * 8);
   cudaStream_t s = cpthd_host::as_stream(stream);
   const uint4* o = reinterpret_cast<const uint4*>(d_o_steps);
+  const uint4* o_r = reinterpret_cast<const uint4*>(d_o_steps_resid);
   uint4* out = reinterpret_cast<uint4*>(d_out);
+  uint4* out_r = reinterpret_cast<uint4*>(d_out_resid);
   if (D == 64)
-    p2p_merge_kernel<64><<<grid, kMergeThreads, 0, s>>>(o, d_lse_steps, n_steps, s_local, H, out,
-                                                        d_lse);
+    p2p_merge_kernel<64><<<grid, kMergeThreads, 0, s>>>(o, o_r, d_lse_steps, n_steps, s_local, H,
+                                                        out, out_r, d_lse);
   else
-    p2p_merge_kernel<128><<<grid, kMergeThreads, 0, s>>>(o, d_lse_steps, n_steps, s_local, H, out,
-                                                         d_lse);
+    p2p_merge_kernel<128><<<grid, kMergeThreads, 0, s>>>(o, o_r, d_lse_steps, n_steps, s_local, H,
+                                                         out, out_r, d_lse);
   return cpthd_host::launch_status();
 }

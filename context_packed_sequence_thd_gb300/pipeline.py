@@ -173,6 +173,8 @@ class CPAttention:
         self.vc = torch.empty(T, H, D, **bf) if dcs else None
         self.doc = torch.empty(T, H, D, **bf) if dcs else None
         self.oc = torch.empty(T, H, D, **bf)
+        # O's bf16 rounding remainder: the backward's Delta = rowsum(dO * O) reads O + it
+        self.oc_resid = torch.empty(T, H, D, **bf)
         self.lse = torch.empty(p.cp, H, p.s_local, dtype=torch.float32, device=dev)
         self.k_full = torch.empty(T, H, D, **bf) if p.strategy == DCS else None
         self.v_full = torch.empty(T, H, D, **bf) if p.strategy == DCS else None
@@ -245,11 +247,12 @@ class CPAttention:
                 if fused:
                     api.cp_attn_fwd_gather(self.q_src, p.ranks[r].idx, k_full, v_full,
                                            p.local(self.oc, r), self.lse[r], p.ranks[r].meta, p.T,
-                                           p.cp, r, p.strategy, p.scale, stream)
+                                           p.cp, r, p.strategy, p.scale, stream,
+                                           o_resid=p.local(self.oc_resid, r))
                 else:
                     api.cp_attn_fwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
                                     self.lse[r], p.ranks[r].meta, p.T, p.cp, r, p.strategy,
-                                    p.scale, stream)
+                                    p.scale, stream, o_resid=p.local(self.oc_resid, r))
             self.launches += 1
         return k_full, v_full
 
@@ -264,7 +267,8 @@ class CPAttention:
                                 self.lse[r], p.local(self.doc, r), p.local(self.dqc, r),
                                 self.dk_acc, self.dv_acc, p.ranks[r].meta, p.T, p.cp, r,
                                 p.strategy, p.scale, self.ws, stream,
-                                mode=api.BWD_STORE if r == 0 else api.BWD_ACCUMULATE)
+                                mode=api.BWD_STORE if r == 0 else api.BWD_ACCUMULATE,
+                                o_resid=p.local(self.oc_resid, r))
             self.launches += 3
         # the scatter half of the reduce-scatter for every rank in one launch:
         # rank r's rows of the rank-concatenated dK/dV are the summed
@@ -327,6 +331,7 @@ class CPA2AAttention(CPAttention):
         shape = (p.cp, T, self.Hc, D)
         self.qh, self.kh, self.vh, self.doh = (torch.empty(shape, **bf) for _ in range(4))
         self.oh, self.dqh, self.dkh, self.dvh = (torch.empty(shape, **bf) for _ in range(4))
+        self.oh_resid = torch.empty(shape, **bf)
         self.lse_h = torch.empty(p.cp, self.Hc, T, dtype=torch.float32, device=dev)
         self.acc_k = torch.empty(T, self.Hc, D, dtype=torch.float32, device=dev)
         self.acc_v = torch.empty(T, self.Hc, D, dtype=torch.float32, device=dev)
@@ -345,7 +350,8 @@ class CPA2AAttention(CPAttention):
         for r in range(p.cp):
             with self._timed("attn_fwd", stream):
                 api.cp_attn_fwd(self.qh[r], self.kh[r], self.vh[r], self.oh[r], self.lse_h[r],
-                                self.full.ranks[0].meta, p.T, 1, 0, NLB, p.scale, stream)
+                                self.full.ranks[0].meta, p.T, 1, 0, NLB, p.scale, stream,
+                                o_resid=self.oh_resid[r])
             self.launches += 1
         with self._timed("a2a_exchange", stream):
             api.cp_a2a_exchange([self.oh], [self.oc], self._perm(), p.cp, api.A2A_HEAD_TO_SEQ,
@@ -364,7 +370,7 @@ class CPA2AAttention(CPAttention):
                 api.cp_attn_bwd(self.qh[r], self.kh[r], self.vh[r], self.oh[r], self.lse_h[r],
                                 self.doh[r], self.dqh[r], self.acc_k, self.acc_v,
                                 self.full.ranks[0].meta, p.T, 1, 0, NLB, p.scale, self.ws_h,
-                                stream, mode=api.BWD_STORE)
+                                stream, mode=api.BWD_STORE, o_resid=self.oh_resid[r])
             self.launches += 3
             with self._timed("grad_cast", stream):
                 api.cp_reduce_scatter_emul([self.acc_k, self.acc_v], [self.dkh[r], self.dvh[r]],
@@ -436,6 +442,7 @@ class CPP2PAttention(CPAttention):
         self.p2p_meta = [torch.empty(p.cp * self.step_bytes, dtype=torch.uint8, device=dev)
                          for _ in range(p.cp)]
         self.o_steps = torch.empty(p.cp, S, H, D, dtype=torch.bfloat16, device=dev)
+        self.o_steps_resid = torch.empty(p.cp, S, H, D, dtype=torch.bfloat16, device=dev)
         self.lse_steps = torch.empty(p.cp, H, S, dtype=torch.float32, device=dev)
         self.dq_acc = torch.empty(T, H, D, dtype=torch.float32, device=dev)
         self.build_p2p_index()
@@ -464,11 +471,13 @@ class CPP2PAttention(CPAttention):
                 with self._timed("attn_fwd", stream):
                     api.cp_attn_fwd(p.local(self.qc, r), p.local(self.kc, j), p.local(self.vc, j),
                                     self.o_steps[i], self.lse_steps[i], self.step_meta(r, i), S,
-                                    1, 0, p.strategy, p.scale, stream)
+                                    1, 0, p.strategy, p.scale, stream,
+                                    o_resid=self.o_steps_resid[i])
                 self.launches += 1
             with self._timed("p2p_merge", stream):
                 api.cp_p2p_merge(self.o_steps[:n], self.lse_steps[:n], p.local(self.oc, r),
-                                 self.lse[r], stream)
+                                 self.lse[r], stream, o_steps_resid=self.o_steps_resid[:n],
+                                 out_resid=p.local(self.oc_resid, r))
             self.launches += 1
         return None, None
 
@@ -481,7 +490,8 @@ class CPP2PAttention(CPAttention):
                                 p.local(self.oc, r), self.lse[r], p.local(self.doc, r),
                                 p.local(self.dq_acc, r), p.local(self.dk_acc, j),
                                 p.local(self.dv_acc, j), self.step_meta(r, i), S, 1, 0,
-                                p.strategy, p.scale, self.ws, stream, mode=mode)
+                                p.strategy, p.scale, self.ws, stream, mode=mode,
+                                o_resid=p.local(self.oc_resid, r))
             self.launches += 3
         with self._timed("grad_cast", stream):
             api.cp_reduce_scatter_emul([self.dq_acc, self.dk_acc, self.dv_acc],

@@ -227,13 +227,17 @@ int cp_zero_tail(void* const* d_rows, int n_tensors, int64_t rows, int64_t row_b
 
 /* q_local [s_local,H,D] bf16 (rank-local order); k_full, v_full [T,H,D] bf16
  * in original order (the restored all-gather); o_local [s_local,H,D] bf16;
- * lse_local [H, s_local] fp32.  d_meta is the rank's metadata from
- * cp_partition_index (same cp_size, rank, strategy).  D in {64, 128};
- * H*D*2 <= 65535*16.  Deterministic. */
+ * lse_local [H, s_local] fp32.  o_resid_local (nullable) [s_local,H,D] bf16
+ * receives O's rounding remainder, O - bf16(O), rounded to bf16: O_local +
+ * o_resid_local carries the output to about 16 bits, and the backward's
+ * Delta = rowsum(dO * O) taken from that sum keeps dQ/dK within the bf16
+ * tolerance on long documents (Delta from the bf16 O alone does not).
+ * d_meta is the rank's metadata from cp_partition_index (same cp_size, rank,
+ * strategy).  D in {64, 128}; H*D*2 <= 65535*16.  Deterministic. */
 int cp_attn_fwd(const void* q_local, const void* k_full, const void* v_full, void* o_local,
-                float* lse_local, const void* d_meta, size_t meta_bytes, int64_t total_tokens,
-                int H, int D, int cp_size, int rank, cp_strategy_t strategy,
-                float softmax_scale, void* stream);
+                void* o_resid_local, float* lse_local, const void* d_meta, size_t meta_bytes,
+                int64_t total_tokens, int H, int D, int cp_size, int rank,
+                cp_strategy_t strategy, float softmax_scale, void* stream);
 
 /* cp_attn_fwd with the partition gather of the queries fused into the kernel
  * (the index_select of get_batch_on_this_cp_rank, [AG] §Sequence Diagram,
@@ -247,16 +251,17 @@ int cp_attn_fwd(const void* q_local, const void* k_full, const void* v_full, voi
  * cp_attn_fwd: the output is bitwise the same as cp_attn_fwd on the gathered
  * q_local. */
 int cp_attn_fwd_gather(const void* q_src, int64_t src_rows, const int32_t* d_idx,
-                       const void* k_full, const void* v_full, void* o_local, float* lse_local,
-                       const void* d_meta, size_t meta_bytes, int64_t total_tokens, int H, int D,
-                       int cp_size, int rank, cp_strategy_t strategy, float softmax_scale,
-                       void* stream);
+                       const void* k_full, const void* v_full, void* o_local,
+                       void* o_resid_local, float* lse_local, const void* d_meta,
+                       size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
+                       int rank, cp_strategy_t strategy, float softmax_scale, void* stream);
 
 /* Device scratch cp_attn_bwd needs: Delta = rowsum(dO * O), fp32 [H, s_local]. */
 size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H);
 
 /* Backward of cp_attn_fwd for one rank.  Inputs as for cp_attn_fwd plus
- * o_local / lse_local from the forward and do_local [s_local,H,D] bf16.
+ * o_local / lse_local from the forward, o_resid_local (nullable) from the
+ * forward's o_resid_local output, and do_local [s_local,H,D] bf16.
  * Writes dq_local [s_local,H,D] bf16 (overwritten) and ADDS this rank's
  * partial dK/dV into dk_accum / dv_accum (fp32 [T,H,D], original order; zero
  * them before rank 0 -- e.g. cp_zero_tail with valid_end = 0 -- or start the
@@ -266,7 +271,8 @@ size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H);
  * cp_attn_bwd_workspace_bytes bytes of device scratch, contents need not be
  * initialised. */
 int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full, const void* o_local,
-                const float* lse_local, const void* do_local, void* dq_local, float* dk_accum,
+                const void* o_resid_local, const float* lse_local, const void* do_local,
+                void* dq_local, float* dk_accum,
                 float* dv_accum, const void* d_meta, size_t meta_bytes, int64_t total_tokens,
                 int H, int D, int cp_size, int rank, cp_strategy_t strategy, float softmax_scale,
                 void* d_workspace, size_t workspace_bytes, void* stream);
@@ -294,7 +300,8 @@ typedef enum {
  * Same arguments, results and errors as cp_attn_bwd otherwise; an unknown
  * bit, or both dQ bits, returns CP_ERR_INVALID_ARG. */
 int cp_attn_bwd_ex(const void* q_local, const void* k_full, const void* v_full,
-                   const void* o_local, const float* lse_local, const void* do_local,
+                   const void* o_local, const void* o_resid_local, const float* lse_local,
+                   const void* do_local,
                    void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
                    size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size, int rank,
                    cp_strategy_t strategy, float softmax_scale, cp_bwd_mode_t mode,
@@ -341,9 +348,14 @@ int cp_p2p_index(const int32_t* d_cu, const int32_t* d_cup, int n_docs, int64_t 
  * in fp32, out rounded to bf16 once; rows with every l_i = -inf get lse = -inf
  * and out = 0.  d_o_steps: bf16 [n_steps, s_local, H, D]; d_lse_steps: fp32
  * [n_steps, H, s_local] (natural log, as cp_attn_fwd writes it); d_out: bf16
- * [s_local, H, D]; d_lse: fp32 [H, s_local].  D in {64, 128}.  One launch. */
-int cp_p2p_merge(const void* d_o_steps, const float* d_lse_steps, int n_steps, int64_t s_local,
-                 int H, int D, void* d_out, float* d_lse, void* stream);
+ * [s_local, H, D]; d_lse: fp32 [H, s_local].  d_o_steps_resid (nullable, same
+ * layout as d_o_steps): the steps' O rounding remainders (cp_attn_fwd's
+ * o_resid_local output), added to o_i before weighting; d_out_resid
+ * (nullable, like d_out): receives the merged output's own bf16 rounding
+ * remainder, for the backward's Delta.  D in {64, 128}.  One launch. */
+int cp_p2p_merge(const void* d_o_steps, const void* d_o_steps_resid, const float* d_lse_steps,
+                 int n_steps, int64_t s_local, int H, int D, void* d_out, void* d_out_resid,
+                 float* d_lse, void* stream);
 
 /* Largest Delta scratch cp_attn_bwd_noalloc can use: s_local*H <= this many
  * floats (4 MiB of device memory per GPU that loads the library). */
@@ -371,7 +383,8 @@ int cp_p2p_merge(const void* d_o_steps, const float* d_lse_steps, int n_steps, i
  * it, so nothing has to start at zero.  Calls whose work overlaps on the GPU
  * (other streams, other host threads) race on the array: serialise them. */
 int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, const void* v_full,
-                        const void* o_local, const float* lse_local, const void* do_local,
+                        const void* o_local, const void* o_resid_local,
+                        const float* lse_local, const void* do_local,
                         void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
                         size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
                         int rank, cp_strategy_t strategy, float softmax_scale, void* stream);

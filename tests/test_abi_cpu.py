@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert api.lib().cp_version() == 100
+    assert api.lib().cp_version() == 200
     assert api.status_string(0) == "CP_OK"
     assert api.status_string(-2) == "CP_ERR_DIVISIBILITY"
     assert api.status_string(-99) == "CP_ERR_UNKNOWN"
@@ -138,24 +138,27 @@ def test_argument_validation_before_launch(lib):
     assert L.cp_thd_gather(_arr(*[FAKE] * 5), _arr(*[FAKE] * 5), 5, FAKE, 4, 4, 256, None) == -1
     # attention: unsupported head dim, bad rank, bad scale, missing workspace
     f = ctypes.c_float
-    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 96, 2, 0, 0, f(0.1), None) == -3
-    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64, 2, 2, 0, f(0.1), None) == -1
-    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64, 2, 0, 0, f(-1.0), None) == -1
-    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 127, 2, 64, 2, 0, 0, f(0.1), None) == -2
+    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 96, 2, 0, 0, f(0.1), None) == -3
+    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64, 2, 2, 0, f(0.1), None) == -1
+    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64, 2, 0, 0, f(-1.0), None) == -1
+    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 127, 2, 64, 2, 0, 0, f(0.1), None) == -2
+    # a misaligned O residual (the optional second output) is refused like any other pointer
+    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE + 8, FAKE, FAKE, 4096, 128, 2, 64, 2, 0, 0,
+                         f(0.1), None) == -4
     # fused-gather forward: no index, misaligned index, empty source
-    assert L.cp_attn_fwd_gather(FAKE, 4096, None, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2, 64,
+    assert L.cp_attn_fwd_gather(FAKE, 4096, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2, 64,
                                 2, 0, 0, f(0.1), None) == -1
-    assert L.cp_attn_fwd_gather(FAKE, 4096, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2,
+    assert L.cp_attn_fwd_gather(FAKE, 4096, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2,
                                 64, 2, 0, 0, f(0.1), None) == -4
-    assert L.cp_attn_fwd_gather(FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2, 64,
+    assert L.cp_attn_fwd_gather(FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2, 64,
                                 2, 0, 0, f(0.1), None) == -1
-    assert L.cp_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64,
+    assert L.cp_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64,
                          2, 0, 0, f(0.1), FAKE, 8, None) == -6
-    assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
+    assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
                             64, 2, 0, 0, f(0.1), 7, FAKE, 1 << 20, None) == -1    # unknown mode
-    assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
+    assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
                             64, 2, 0, 0, f(0.1), 1, FAKE, 8, None) == -6           # store mode, small workspace
-    assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
+    assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
                             64, 2, 0, 0, f(0.1), 6, FAKE, 1 << 20, None) == -1    # both dQ modes
     assert L.cp_reduce_scatter_emul(_arr(FAKE), _arr(FAKE), 1, None, 0, 10, 5, 2, 64, None) == -1
 
@@ -178,10 +181,11 @@ def test_p2p_sizes_and_argument_validation(lib):
     assert L.cp_p2p_index(None, FAKE, 2, 24, 2, 0, 1, 1, FAKE, 2 * step, None) == -1
     assert L.cp_p2p_index(None, FAKE, 2, 24, 2, 0, 1, 0, FAKE + 8, 2 * step, None) == -4
     # merge: no steps, unsupported head dim, misaligned output
-    assert L.cp_p2p_merge(FAKE, FAKE, 0, 100, 2, 64, FAKE, FAKE, None) == -1
-    assert L.cp_p2p_merge(FAKE, FAKE, 2, 100, 2, 96, FAKE, FAKE, None) == -3
-    assert L.cp_p2p_merge(FAKE, FAKE, 2, 100, 2, 64, FAKE + 4, FAKE, None) == -4
-    assert L.cp_p2p_merge(FAKE, FAKE, 2, 0, 2, 64, FAKE, FAKE, None) == 0     # nothing to do
+    assert L.cp_p2p_merge(FAKE, None, FAKE, 0, 100, 2, 64, FAKE, None, FAKE, None) == -1
+    assert L.cp_p2p_merge(FAKE, None, FAKE, 2, 100, 2, 96, FAKE, None, FAKE, None) == -3
+    assert L.cp_p2p_merge(FAKE, None, FAKE, 2, 100, 2, 64, FAKE + 4, None, FAKE, None) == -4
+    assert L.cp_p2p_merge(FAKE, FAKE + 8, FAKE, 2, 100, 2, 64, FAKE, None, FAKE, None) == -4
+    assert L.cp_p2p_merge(FAKE, None, FAKE, 2, 0, 2, 64, FAKE, None, FAKE, None) == 0  # nothing to do
 
 
 def test_product_path_has_no_oracle_or_cpu_fallback():

@@ -45,10 +45,11 @@ def _backward(plan, att, kf, vf, noalloc):
         args = (plan.local(att.qc, r), kf, vf, plan.local(att.oc, r), att.lse[r],
                 plan.local(att.doc, r), plan.local(dq, r), dk, dv, plan.ranks[r].meta, plan.T,
                 plan.cp, r, plan.strategy, plan.scale)
+        o_resid = plan.local(att.oc_resid, r)
         if noalloc:
-            api.cp_attn_bwd_noalloc(*args)
+            api.cp_attn_bwd_noalloc(*args, o_resid=o_resid)
         else:
-            api.cp_attn_bwd(*args, att.ws)
+            api.cp_attn_bwd(*args, att.ws, o_resid=o_resid)
     torch.cuda.synchronize()
     assert api.cp_device_status() == 0
     return dq, dk, dv
@@ -76,7 +77,7 @@ def test_noalloc_rejects_sizes_beyond_the_scratch():
     L = api.lib()
     fake = 0x10000
     T = 2 * api.NOALLOC_MAX_SCRATCH_FLOATS  # cp=1, H=1: s_local*H = 2x the maximum
-    st = L.cp_attn_bwd_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+    st = L.cp_attn_bwd_noalloc(fake, fake, fake, fake, None, fake, fake, fake, fake, fake, fake,
                                1 << 20, T, 1, 64, 1, 0, 1, ctypes.c_float(0.125), None)
     assert st == -6
     assert api.status_string(st) == "CP_ERR_WORKSPACE"
