@@ -391,8 +391,8 @@ def _fused_q_gather(dev, reps=5):
     g = {k: v.to(dev) for k, v in wl.tensors(with_grad=False).items()}
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, pipeline.DCS, 0, wl.H, wl.D, dev)
     out = {}
-    for fuse in (False, True):
-        att = pipeline.CPAttention(plan, fuse_q_gather=fuse)
+    for fuse in (False, True):   # the fused gather reads the bf16 batch: bf16 operands both
+        att = pipeline.CPAttention(plan, fuse_q_gather=fuse, operand_dtype=torch.bfloat16)
         t = _time_ms(lambda: att.step(g["q"], g["k"], g["v"], rebuild_index=False), reps)
         out["fused_gather_ms" if fuse else "copy_gather_ms"] = round(t, 4)
         del att
@@ -551,6 +551,8 @@ def run_own(args):
             "config": {"workload": WORKLOAD, "total_tokens": wl.total_tokens,
                        "n_docs": wl.n_docs, "cp_size": wl.cp, "H": wl.H, "D": wl.D,
                        "pad_between_seqs": wl.pad_between_seqs,
+                       "operands": "bf16 inputs; fp16 tensor-core operands (converted in the shard "
+                                   "gather), fp32 accumulation, bf16 outputs",
                        "strategies": ["dual_chunk_swap", "no_load_balance"],
                        "parallelism": f"replicas{ws}" if ws > 1 else "cp4 emulated on 1 GPU",
                        "l2": "inputs larger than L2 (4 x 537 MB bf16 inputs, ~25 GB touched "

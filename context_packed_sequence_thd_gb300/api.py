@@ -40,20 +40,21 @@ _SIGNATURES = {
     "cp_partition_index_all": ([_P, _P, _I, _I64, _I, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "cp_thd_gather": ([_P, _P, _I, _P, _I64, _I64, _I64, _P], _I),
     "cp_thd_scatter": ([_P, _P, _I, _P, _I64, _I64, _I64, _P], _I),
+    "cp_thd_gather_f16": ([_P, _P, _I, _P, _I64, _I64, _I64, _P], _I),
     "cp_reduce_scatter_emul": ([_P, _P, _I, _P, _I64, _I64, _I64, _I, _I, _P], _I),
     "cp_a2a_exchange": ([_P, _P, _I, _P, _I64, _I, _I, _I, _I, _P], _I),
     "cp_zero_tail": ([_P, _I, _I64, _I64, _I64, _P, _P, ctypes.POINTER(_I)], _I),
     "cp_attn_fwd": ([_P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I, ctypes.c_float,
-                     _P], _I),
+                     _I, _P], _I),
     "cp_attn_fwd_gather": ([_P, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
-                           ctypes.c_float, _P], _I),
+                           ctypes.c_float, _I, _P], _I),
     "cp_attn_bwd_workspace_bytes": ([_I64, _I], _SZ),
     "cp_attn_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I, _I,
-                     ctypes.c_float, _P, _SZ, _P], _I),
+                     ctypes.c_float, _I, _P, _SZ, _P], _I),
     "cp_attn_bwd_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I, _I,
-                        _I, ctypes.c_float, _I, _P, _SZ, _P], _I),
+                        _I, ctypes.c_float, _I, _I, _P, _SZ, _P], _I),
     "cp_attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I,
-                             _I, _I, ctypes.c_float, _P], _I),
+                             _I, _I, ctypes.c_float, _I, _P], _I),
     "cp_p2p_meta_bytes": ([_I, _I64, _I], _SZ),
     "cp_p2p_index": ([_P, _P, _I, _I64, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "cp_p2p_merge": ([_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P], _I),
@@ -214,6 +215,17 @@ def cp_thd_gather(srcs: Sequence[torch.Tensor], dsts: Sequence[torch.Tensor],
     _check("cp_thd_gather", st)
 
 
+def cp_thd_gather_f16(srcs: Sequence[torch.Tensor], dsts: Sequence[torch.Tensor],
+                      d_idx: Optional[torch.Tensor], stream=None) -> None:
+    """dst[k][i] = fp16(src[k][idx[i]]) for bf16 sources (idx None: row i)."""
+    n_rows = dsts[0].shape[0] if d_idx is None else d_idx.numel()
+    src_rows = srcs[0].shape[0]
+    st = lib().cp_thd_gather_f16(_ptr_array(srcs, "src"), _ptr_array(dsts, "dst"), len(srcs),
+                                 None if d_idx is None else _dev(d_idx, "idx"), n_rows, src_rows,
+                                 _row_bytes(srcs[0]), _stream(stream))
+    _check("cp_thd_gather_f16", st)
+
+
 def cp_thd_scatter(srcs: Sequence[torch.Tensor], dsts: Sequence[torch.Tensor],
                    d_idx: torch.Tensor, stream=None) -> None:
     n_rows = d_idx.numel()
@@ -266,17 +278,31 @@ def _opt(t, name):
     return None if t is None else _dev(t, name)
 
 
+OPERAND_BF16, OPERAND_F16 = 0, 1
+
+
+def _operand_dtype(*ts) -> int:
+    """The tensor-core operand type of Q/K/V(/dO): all bf16 or all fp16."""
+    kinds = {t.dtype for t in ts}
+    if kinds == {torch.bfloat16}:
+        return OPERAND_BF16
+    if kinds == {torch.float16}:
+        return OPERAND_F16
+    raise ValueError(f"attention operands must be all bf16 or all fp16, got {kinds}")
+
+
 def cp_attn_fwd(q_local, k_full, v_full, o_local, lse_local, d_meta, total_tokens: int,
                 cp_size: int, rank: int, strategy: int, softmax_scale: float,
                 stream=None, o_resid=None) -> None:
     """o_resid (optional, bf16 like o_local) receives O's bf16 rounding remainder,
     which the backward's Delta uses."""
     _, H, D = k_full.shape
+    dt = _operand_dtype(q_local, k_full, v_full)
     st = lib().cp_attn_fwd(_dev(q_local, "q"), _dev(k_full, "k"), _dev(v_full, "v"),
                            _dev(o_local, "o"), _opt(o_resid, "o_resid"), _dev(lse_local, "lse"),
                            _dev(d_meta, "meta"),
                            d_meta.numel() * d_meta.element_size(), total_tokens, H, D, cp_size,
-                           rank, strategy, float(softmax_scale), _stream(stream))
+                           rank, strategy, float(softmax_scale), dt, _stream(stream))
     _check("cp_attn_fwd", st)
 
 
@@ -285,11 +311,13 @@ def cp_attn_fwd_gather(q_src, d_idx, k_full, v_full, o_local, lse_local, d_meta,
                        softmax_scale: float, stream=None, o_resid=None) -> None:
     """cp_attn_fwd reading query row t from q_src[d_idx[t]] (no q_local copy)."""
     _, H, D = k_full.shape
+    dt = _operand_dtype(q_src, k_full, v_full)
     st = lib().cp_attn_fwd_gather(_dev(q_src, "q_src"), q_src.shape[0], _dev(d_idx, "idx"),
                                   _dev(k_full, "k"), _dev(v_full, "v"), _dev(o_local, "o"),
-                                  _opt(o_resid, "o_resid"), _dev(lse_local, "lse"), _dev(d_meta, "meta"),
-                                  d_meta.numel() * d_meta.element_size(), total_tokens, H, D,
-                                  cp_size, rank, strategy, float(softmax_scale), _stream(stream))
+                                  _opt(o_resid, "o_resid"), _dev(lse_local, "lse"),
+                                  _dev(d_meta, "meta"), d_meta.numel() * d_meta.element_size(),
+                                  total_tokens, H, D, cp_size, rank, strategy,
+                                  float(softmax_scale), dt, _stream(stream))
     _check("cp_attn_fwd_gather", st)
 
 
@@ -303,12 +331,13 @@ def cp_attn_bwd(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local,
     """cp_attn_bwd (mode BWD_ACCUMULATE) or cp_attn_bwd_ex with the given mode;
     o_resid: the forward's O rounding remainder (optional)."""
     _, H, D = k_full.shape
+    dt = _operand_dtype(q_local, k_full, v_full, do_local)
     args = (_dev(q_local, "q"), _dev(k_full, "k"), _dev(v_full, "v"),
             _dev(o_local, "o"), _opt(o_resid, "o_resid"), _dev(lse_local, "lse"),
             _dev(do_local, "do"),
             _dev(dq_local, "dq"), _dev(dk_accum, "dk"), _dev(dv_accum, "dv"),
             _dev(d_meta, "meta"), d_meta.numel() * d_meta.element_size(),
-            total_tokens, H, D, cp_size, rank, strategy, float(softmax_scale))
+            total_tokens, H, D, cp_size, rank, strategy, float(softmax_scale), dt)
     tail = (_dev(d_workspace, "workspace"), d_workspace.numel() * d_workspace.element_size(),
             _stream(stream))
     if mode == BWD_ACCUMULATE:
@@ -327,6 +356,7 @@ def cp_attn_bwd_noalloc(q_local, k_full, v_full, o_local, lse_local, do_local, d
     scratch is a fixed array inside the library (s_local*H <= 1,048,576
     floats).  Calls that overlap on the GPU share that array and race."""
     _, H, D = k_full.shape
+    dt = _operand_dtype(q_local, k_full, v_full, do_local)
     st = lib().cp_attn_bwd_noalloc(_dev(q_local, "q"), _dev(k_full, "k"), _dev(v_full, "v"),
                                    _dev(o_local, "o"), _opt(o_resid, "o_resid"),
                                    _dev(lse_local, "lse"),
@@ -334,7 +364,7 @@ def cp_attn_bwd_noalloc(q_local, k_full, v_full, o_local, lse_local, do_local, d
                                    _dev(dk_accum, "dk"), _dev(dv_accum, "dv"),
                                    _dev(d_meta, "meta"), d_meta.numel() * d_meta.element_size(),
                                    total_tokens, H, D, cp_size, rank, strategy,
-                                   float(softmax_scale), _stream(stream))
+                                   float(softmax_scale), dt, _stream(stream))
     _check("cp_attn_bwd_noalloc", st)
 
 

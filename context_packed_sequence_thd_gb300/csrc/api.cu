@@ -18,6 +18,7 @@ extern "C" const char* cp_status_string(int status) {
     case CP_ERR_WORKSPACE: return "CP_ERR_WORKSPACE";
     case CP_ERR_METADATA: return "CP_ERR_METADATA";
     case CP_ERR_TIMEOUT: return "CP_ERR_TIMEOUT";
+    case CP_ERR_RANGE: return "CP_ERR_RANGE";
     default: return "CP_ERR_UNKNOWN";
   }
 }

@@ -50,9 +50,9 @@ struct AttnArgs {
 };
 
 // ---------------------------------------------------------------------------
-// backward: Delta = rowsum(dO * O)
+// backward: Delta = rowsum(dO * O)   (dO of the operand type, O bf16)
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(256) attn_delta(const AttnArgs a) {
   constexpr int G = D / 8;  // threads per (row, head)
   const int64_t gid = int64_t(blockIdx.x) * 256 + threadIdx.x;
@@ -71,8 +71,9 @@ __global__ void __launch_bounds__(256) attn_delta(const AttnArgs a) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       // O to about 16 bits: the bf16 output plus its rounding remainder (exact in fp32)
-      const float2 fx = __bfloat1622float2(xp[i]), fy = __bfloat1622float2(yp[i]),
-                   fz = __bfloat1622float2(zp[i]);
+      const float2 fx = F16 ? __half22float2(reinterpret_cast<const __half2*>(&x)[i])
+                            : __bfloat1622float2(xp[i]);
+      const float2 fy = __bfloat1622float2(yp[i]), fz = __bfloat1622float2(zp[i]);
       acc += fx.x * (fy.x + fz.x) + fx.y * (fy.y + fz.y);
     }
   }
@@ -83,6 +84,23 @@ __global__ void __launch_bounds__(256) attn_delta(const AttnArgs a) {
     const int h = (int)(pair % a.H);
     a.delta[(int64_t)h * a.s_local + row] = acc;
   }
+}
+
+int launch_delta(const AttnArgs& a, int D, int f16, cudaStream_t s) {
+  const int64_t threads = (int64_t)a.s_local * a.H * (D / 8);
+  dim3 dgrid((unsigned)((threads + 255) / 256));
+  if (D == 64) {
+    if (f16) attn_delta<64, true><<<dgrid, 256, 0, s>>>(a);
+    else attn_delta<64, false><<<dgrid, 256, 0, s>>>(a);
+  } else {
+    if (f16) attn_delta<128, true><<<dgrid, 256, 0, s>>>(a);
+    else attn_delta<128, false><<<dgrid, 256, 0, s>>>(a);
+  }
+  return cpthd_host::launch_status();
+}
+
+int check_dtype(cp_dtype_t dtype) {
+  return (dtype == CP_OPERAND_BF16 || dtype == CP_OPERAND_F16) ? CP_OK : CP_ERR_INVALID_ARG;
 }
 
 int common_checks(const void* q, const void* k, const void* v, const void* meta, size_t meta_bytes,
@@ -112,11 +130,12 @@ extern "C" int cp_attn_fwd(const void* q_local, const void* k_full, const void* 
                            void* o_local, void* o_resid_local, float* lse_local,
                            const void* d_meta, size_t meta_bytes, int64_t total_tokens, int H,
                            int D, int cp_size, int rank, cp_strategy_t strategy,
-                           float softmax_scale, void* stream) {
+                           float softmax_scale, cp_dtype_t operand_dtype, void* stream) {
   int64_t s_local = 0;
   int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
                          rank, strategy, &s_local);
   if (st != CP_OK) return st;
+  if ((st = check_dtype(operand_dtype)) != CP_OK) return st;
   if (!o_local || !lse_local) return CP_ERR_INVALID_ARG;
   if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local) ||
       !cpthd_host::aligned16(o_resid_local))
@@ -125,7 +144,7 @@ extern "C" int cp_attn_fwd(const void* q_local, const void* k_full, const void* 
   if (s_local == 0) return CP_OK;
   return cpthd_attn_fwd_tc(q_local, nullptr, 0, k_full, v_full, o_local, o_resid_local, lse_local,
                            d_meta, meta_bytes, (int)total_tokens, H, D, (int)s_local, cp_size,
-                           rank, (int)strategy, softmax_scale * kLog2e,
+                           rank, (int)strategy, softmax_scale * kLog2e, (int)operand_dtype,
                            cpthd_host::as_stream(stream));
 }
 
@@ -134,11 +153,12 @@ extern "C" int cp_attn_fwd_gather(const void* q_src, int64_t src_rows, const int
                                   void* o_resid_local, float* lse_local, const void* d_meta,
                                   size_t meta_bytes, int64_t total_tokens, int H, int D,
                                   int cp_size, int rank, cp_strategy_t strategy,
-                                  float softmax_scale, void* stream) {
+                                  float softmax_scale, cp_dtype_t operand_dtype, void* stream) {
   int64_t s_local = 0;
   int st = common_checks(q_src, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
                          rank, strategy, &s_local);
   if (st != CP_OK) return st;
+  if ((st = check_dtype(operand_dtype)) != CP_OK) return st;
   if (!o_local || !lse_local || !d_idx) return CP_ERR_INVALID_ARG;
   if (src_rows < 1 || src_rows > INT32_MAX) return CP_ERR_INVALID_ARG;
   if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local) ||
@@ -149,7 +169,7 @@ extern "C" int cp_attn_fwd_gather(const void* q_src, int64_t src_rows, const int
   return cpthd_attn_fwd_tc(q_src, d_idx, (int)src_rows, k_full, v_full, o_local, o_resid_local,
                            lse_local, d_meta, meta_bytes, (int)total_tokens, H, D, (int)s_local,
                            cp_size, rank, (int)strategy, softmax_scale * kLog2e,
-                           cpthd_host::as_stream(stream));
+                           (int)operand_dtype, cpthd_host::as_stream(stream));
 }
 
 // Failure-detection test hook (not part of the ABI header): cp_attn_fwd
@@ -162,7 +182,8 @@ extern "C" int cpthd_test_attn_fwd_timeout(const void* q_local, const void* k_fu
                                            const void* d_meta, size_t meta_bytes,
                                            int64_t total_tokens, int H, int D, int cp_size,
                                            int rank, cp_strategy_t strategy, float softmax_scale,
-                                           uint64_t limit_ns, void* stream) {
+                                           cp_dtype_t operand_dtype, uint64_t limit_ns,
+                                           void* stream) {
   int64_t s_local = 0;
   int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
                          rank, strategy, &s_local);
@@ -170,10 +191,11 @@ extern "C" int cpthd_test_attn_fwd_timeout(const void* q_local, const void* k_fu
   if (!o_local || !lse_local) return CP_ERR_INVALID_ARG;
   if (!cpthd_host::aligned16(o_local) || !cpthd_host::aligned16(lse_local)) return CP_ERR_ALIGNMENT;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
-  if (s_local == 0 || limit_ns == 0) return CP_ERR_INVALID_ARG;
+  if (s_local == 0 || limit_ns == 0 || check_dtype(operand_dtype) != CP_OK)
+    return CP_ERR_INVALID_ARG;
   return cpthd_attn_fwd_tc(q_local, nullptr, 0, k_full, v_full, o_local, nullptr, lse_local,
                            d_meta, meta_bytes, (int)total_tokens, H, D, (int)s_local, cp_size,
-                           rank, (int)strategy, softmax_scale * kLog2e,
+                           rank, (int)strategy, softmax_scale * kLog2e, (int)operand_dtype,
                            cpthd_host::as_stream(stream), limit_ns, 1);
 }
 
@@ -188,10 +210,11 @@ extern "C" int cp_attn_bwd_ex(const void* q_local, const void* k_full, const voi
                               void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
                               size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
                               int rank, cp_strategy_t strategy, float softmax_scale,
-                              cp_bwd_mode_t mode, void* d_workspace, size_t workspace_bytes,
-                              void* stream) {
+                              cp_dtype_t operand_dtype, cp_bwd_mode_t mode, void* d_workspace,
+                              size_t workspace_bytes, void* stream) {
   const int m = (int)mode;
   if ((m & ~7) != 0 || (m & 6) == 6) return CP_ERR_INVALID_ARG;
+  if (check_dtype(operand_dtype) != CP_OK) return CP_ERR_INVALID_ARG;
   int64_t s_local = 0;
   int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
                          rank, strategy, &s_local);
@@ -217,15 +240,11 @@ extern "C" int cp_attn_bwd_ex(const void* q_local, const void* k_full, const voi
   a.T = (int)total_tokens; a.H = H; a.s_local = (int)s_local; a.cp = cp_size; a.rank = rank;
   a.strategy = (int)strategy; a.scale = softmax_scale; a.scale_log2 = softmax_scale * kLog2e;
   cudaStream_t s = cpthd_host::as_stream(stream);
-  const int64_t threads = s_local * H * (D / 8);
-  dim3 dgrid((unsigned)((threads + 255) / 256));
-  if (D == 64) attn_delta<64><<<dgrid, 256, 0, s>>>(a);
-  else attn_delta<128><<<dgrid, 256, 0, s>>>(a);
-  if ((st = cpthd_host::launch_status()) != CP_OK) return st;
+  if ((st = launch_delta(a, D, (int)operand_dtype, s)) != CP_OK) return st;
   return cpthd_attn_bwd_tc(q_local, k_full, v_full, do_local, lse_local, a.delta, dq_local,
                            dk_accum, dv_accum, d_meta, meta_bytes, (int)total_tokens, H, D,
                            (int)s_local, cp_size, rank, (int)strategy, softmax_scale,
-                           softmax_scale * kLog2e, m, s);
+                           softmax_scale * kLog2e, m, (int)operand_dtype, s);
 }
 
 extern "C" int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full,
@@ -234,11 +253,13 @@ extern "C" int cp_attn_bwd(const void* q_local, const void* k_full, const void* 
                            void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
                            size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
                            int rank, cp_strategy_t strategy, float softmax_scale,
-                           void* d_workspace, size_t workspace_bytes, void* stream) {
+                           cp_dtype_t operand_dtype, void* d_workspace, size_t workspace_bytes,
+                           void* stream) {
   return cp_attn_bwd_ex(q_local, k_full, v_full, o_local, o_resid_local, lse_local, do_local,
                         dq_local, dk_accum,
                         dv_accum, d_meta, meta_bytes, total_tokens, H, D, cp_size, rank, strategy,
-                        softmax_scale, CP_BWD_ACCUMULATE, d_workspace, workspace_bytes, stream);
+                        softmax_scale, operand_dtype, CP_BWD_ACCUMULATE, d_workspace,
+                        workspace_bytes, stream);
 }
 
 extern "C" int cpthd_status_attn(int reset) {
@@ -320,7 +341,8 @@ extern "C" int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, cons
                                    const void* do_local, void* dq_local, float* dk_accum,
                                    float* dv_accum, const void* d_meta, size_t meta_bytes,
                                    int64_t total_tokens, int H, int D, int cp_size, int rank,
-                                   cp_strategy_t strategy, float softmax_scale, void* stream) {
+                                   cp_strategy_t strategy, float softmax_scale,
+                                   cp_dtype_t operand_dtype, void* stream) {
   int64_t s_local = 0;
   int st = common_checks(q_local, k_full, v_full, d_meta, meta_bytes, total_tokens, H, D, cp_size,
                          rank, strategy, &s_local);
@@ -333,6 +355,7 @@ extern "C" int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, cons
       !cpthd_host::aligned16(o_resid_local))
     return CP_ERR_ALIGNMENT;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
+  if ((st = check_dtype(operand_dtype)) != CP_OK) return st;
   if (s_local * (int64_t)H > (int64_t)CP_NOALLOC_MAX_SCRATCH_FLOATS) return CP_ERR_WORKSPACE;
   if (s_local == 0) return CP_OK;
   float* scratch = nullptr;
@@ -346,13 +369,9 @@ extern "C" int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, cons
   a.T = (int)total_tokens; a.H = H; a.s_local = (int)s_local; a.cp = cp_size; a.rank = rank;
   a.strategy = (int)strategy; a.scale = softmax_scale; a.scale_log2 = softmax_scale * kLog2e;
   cudaStream_t s = cpthd_host::as_stream(stream);
-  const int64_t threads = s_local * H * (D / 8);
-  dim3 dgrid((unsigned)((threads + 255) / 256));
-  if (D == 64) attn_delta<64><<<dgrid, 256, 0, s>>>(a);
-  else attn_delta<128><<<dgrid, 256, 0, s>>>(a);
-  if ((st = cpthd_host::launch_status()) != CP_OK) return st;
+  if ((st = launch_delta(a, D, (int)operand_dtype, s)) != CP_OK) return st;
   return cpthd_attn_bwd_tc(q_local, k_full, v_full, do_local, lse_local, a.delta, dq_local,
                            dk_accum, dv_accum, d_meta, meta_bytes, (int)total_tokens, H, D,
                            (int)s_local, cp_size, rank, (int)strategy, softmax_scale,
-                           softmax_scale * kLog2e, 0, s);
+                           softmax_scale * kLog2e, 0, (int)operand_dtype, s);
 }

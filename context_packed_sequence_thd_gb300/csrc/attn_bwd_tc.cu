@@ -1,6 +1,11 @@
 // attn_bwd_tc.cu -- causal varlen attention backward of one CP rank on the
 // Blackwell tensor cores (tcgen05 + TMEM + TMA), built for sm_103a.
 //
+// The tensor-core operands are all bf16 or all fp16 (F16).  With bf16, the
+// probabilities P and dS go into the products as two bf16 terms each (the
+// rounded value and its rounding remainder: one extra product each), which
+// carries them to about 16 bits; fp16 (11 bits) needs one term.
+//
 // The backward of the forward in attn_fwd_tc.cu ("[PyTorch] Add
 // no-load-balance THD all-gather CP", §What changed: backward uses the
 // forward's token layout): with Delta_t = dO_t . O_t (attn_delta),
@@ -143,6 +148,25 @@ __device__ __forceinline__ void split_bf16(const float* x, uint32_t* hi, uint32_
   }
 }
 
+// 32 fp32 values -> TMEM columns [col, col+16) as an A operand: fp16 pairs
+// (F16), or bf16 pairs followed by the bf16 pairs of their rounding
+// remainders at [col+16, col+32) (two bf16 terms carry about 16 significant
+// bits; fp16 alone carries 11).
+template <bool F16>
+__device__ __forceinline__ void store_operand(uint32_t col, const float* x) {
+  uint32_t hi[16];
+  if (F16) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) hi[e] = pack_f16(x[2 * e], x[2 * e + 1]);
+    tmem_st16(col, hi);
+  } else {
+    uint32_t lo[16];
+    split_bf16(x, hi, lo);
+    tmem_st16(col, hi);
+    tmem_st16(col + 16, lo);
+  }
+}
+
 // p[e] = 2^(p[e] * scl - lse2) for 64 scores (lse2 in the log2 domain, one
 // per element pair or shared), the products in paired instructions.
 __device__ __forceinline__ void exp2_scores(float* p, uint64_t scl2, const uint64_t* nlse2,
@@ -194,7 +218,7 @@ struct DqCtl {
 // "wait ds_full(g-1) before committing dp_full(g)" (and "wait s_free(g-1)
 // before committing s_full(g)") keeps each of them at most one phase ahead of
 // its waiter, so the parity waits never alias.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThr, 1)
 attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
            const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -309,8 +333,8 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false, F16);
+      constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true, F16);
       // operand descriptors at the tiles' first bytes (K-major, and K as MN-major)
       const uint64_t dsc_q = sdesc_sw128(sb + L::Q, 16, 1024);
       const uint64_t dsc_do = sdesc_sw128(sb + L::DO, 16, 1024);
@@ -330,14 +354,14 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tc_fence_after();
         const int ks = pend % kDqKStages;
         const uint64_t bk = sdesc_add(dsc_kmn, ks * L::TILE);
-        // dS is the sum of two bf16 terms (rounded values, then their
-        // remainders): two products per k-step
+        // bf16 dS is the sum of two terms (rounded values, then their
+        // remainders): two products per k-step; fp16 dS one
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t b = sdesc_add(bk, kk * 2048);
           umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk), b, idQ,
                        (!pend_first || kk > 0) ? 1u : 0u);
-          umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk) + 16, b, idQ, 1u);
+          if (!F16) umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk) + 16, b, idQ, 1u);
           if (kk == 4 && vs_next >= 0 && !seen_v)
             seen_v = mbar_test_wait(bar_addr(c.v_full[vs_next]), (g_next / kDqVStages) & 1);
         }
@@ -505,10 +529,11 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           break;
         }
         tc_fence_after();
-        // dS = P (dP - Delta) over the dP columns just read, as hi and lo bf16 terms
+        // dS = P (dP - Delta) over the dP columns just read (one fp16 term, or
+        // hi and lo bf16 terms)
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          uint32_t dp[32], hi[16], lo[16];
+          uint32_t dp[32];
           const uint32_t col = tmem + lb + 128 + 64 * hf + 32 * cc;
           tmem_ld32(col, dp);
 #pragma unroll
@@ -521,9 +546,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             dp[2 * e2] = __float_as_uint(x0);
             dp[2 * e2 + 1] = __float_as_uint(x1);
           }
-          split_bf16(reinterpret_cast<const float*>(dp), hi, lo);
-          tmem_st16(col, hi);
-          tmem_st16(col + 16, lo);
+          store_operand<F16>(col, reinterpret_cast<const float*>(dp));
         }
         tmem_st_wait();
         tc_fence_before();
@@ -647,7 +670,7 @@ __host__ __device__ constexpr int kv_stage_offset() {
 // dP^T_i is committed only after the MMA thread has consumed ds_full(i-1) and
 // S^T_{i+1} only after it has consumed p_full(i), so no per-step barrier gets
 // two phases ahead of its waiter.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kKvThr, 1)
 attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -801,8 +824,8 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     }
   } else if (warp == kKvMma) {
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false, F16);
+      constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true, F16);
       // operand descriptors at the tiles' first bytes (K-major, and Q / dO as MN-major)
       const uint64_t dsc_k = sdesc_sw128(sb + L::K, 16, 1024);
       const uint64_t dsc_v = sdesc_sw128(sb + L::V, 16, 1024);
@@ -829,7 +852,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           const uint64_t b = sdesc_add(bq, kk * 2048);
           umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk), b, idG,
                        (!pend_first || kk > 0) ? 1u : 0u);
-          umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk) + 16, b, idG, 1u);
+          if (!F16) umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk) + 16, b, idG, 1u);
         }
         umma_commit(bar_addr(c.q_empty[pend_st]));
         return true;
@@ -903,7 +926,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t b = sdesc_add(bdm, kk * 2048);
             umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk), b, idG, (i > 0 || kk > 0) ? 1u : 0u);
-            umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk) + 32, b, idG, 1u);
+            if (!F16) umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk) + 32, b, idG, 1u);
           }
           pend = gs;
           pend_st = st;
@@ -1082,10 +1105,17 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
            // rounded P (first 32 columns) and its rounding remainder (next 32)
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            uint32_t ph[16], pl[16];
-            split_bf16(p + 32 * cc, ph, pl);
-            tmem_st16(tmem + lb + 64 * hf + 16 * cc, ph);
-            tmem_st16(tmem + lb + 64 * hf + 32 + 16 * cc, pl);
+            if (F16) {
+              uint32_t ph[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) ph[e] = pack_f16(p[32 * cc + 2 * e], p[32 * cc + 2 * e + 1]);
+              tmem_st16(tmem + lb + 64 * hf + 16 * cc, ph);
+            } else {
+              uint32_t ph[16], pl[16];
+              split_bf16(p + 32 * cc, ph, pl);
+              tmem_st16(tmem + lb + 64 * hf + 16 * cc, ph);
+              tmem_st16(tmem + lb + 64 * hf + 32 + 16 * cc, pl);
+            }
           }
         }
         tmem_st_wait();
@@ -1101,7 +1131,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // lo bf16 terms
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          uint32_t dp[32], hi[16], lo[16];
+          uint32_t dp[32];
           const uint32_t col = tmem + lb + 128 + 64 * hf + 32 * cc;
           tmem_ld32(col, dp);
 #pragma unroll
@@ -1113,9 +1143,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             dp[4 * e4 + 2] = __float_as_uint(p[c0 + 2] * (__uint_as_float(dp[4 * e4 + 2]) - d.z));
             dp[4 * e4 + 3] = __float_as_uint(p[c0 + 3] * (__uint_as_float(dp[4 * e4 + 3]) - d.w));
           }
-          split_bf16(reinterpret_cast<const float*>(dp), hi, lo);
-          tmem_st16(col, hi);
-          tmem_st16(col + 16, lo);
+          store_operand<F16>(col, reinterpret_cast<const float*>(dp));
         }
         tmem_st_wait();
         tc_fence_before();
@@ -1132,39 +1160,40 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   }
 }
 
-template <int D>
+template <int D, bool F16>
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
                   const BwdArgs& a, cudaStream_t s) {
   alignas(64) CUtensorMap mq, mdo, mk, mv, mdk, mdv;
   int st;
-  if ((st = tma::make_thd_map(&mq, q, a.s_local, a.H, D, 128)) != CP_OK) return st;
-  if ((st = tma::make_thd_map(&mdo, dout, a.s_local, a.H, D, 128)) != CP_OK) return st;
-  if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128)) != CP_OK) return st;
-  if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mq, q, a.s_local, a.H, D, 128, F16)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mdo, dout, a.s_local, a.H, D, 128, F16)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128, F16)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128, F16)) != CP_OK) return st;
   if ((st = tma::make_f32_rows_map(&mdk, a.dk, a.T, a.H, D)) != CP_OK) return st;
   if ((st = tma::make_f32_rows_map(&mdv, a.dv, a.T, a.H, D)) != CP_OK) return st;
   const int dq_smem = DqLayout<D>::BYTES + (int)sizeof(DqCtl);
   const int kv_smem = kv_stage_offset<D>() + kStageBytes;
-  if (cudaFuncSetAttribute(attn_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(attn_dkdv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(attn_dq_tc<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           dq_smem) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_dkdv_tc<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kv_smem) != cudaSuccess)
     return CP_ERR_CUDA;
   const int sms = cpthd_host::sm_count();
   const int64_t q_items = n_tiles_of(a.s_local) * (int64_t)a.H;
-  attn_dq_tc<D><<<(int)(q_items < sms ? q_items : sms), kThr, dq_smem, s>>>(mq, mdo, mk, mv, a);
+  attn_dq_tc<D, F16><<<(int)(q_items < sms ? q_items : sms), kThr, dq_smem, s>>>(mq, mdo, mk, mv,
+                                                                                   a);
   if ((st = cpthd_host::launch_status()) != CP_OK) return st;
   const int64_t k_items = n_tiles_of(a.T) * (int64_t)a.H;
   // the register split inside attn_dkdv_tc assumes exactly kKvLaunchRegs per thread at launch
   static int kv_regs = -1;
   if (kv_regs < 0) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, attn_dkdv_tc<D>) != cudaSuccess) return CP_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, attn_dkdv_tc<D, F16>) != cudaSuccess) return CP_ERR_CUDA;
     kv_regs = fa.numRegs;
   }
   if (kv_regs != kKvLaunchRegs) return CP_ERR_UNSUPPORTED;
-  attn_dkdv_tc<D><<<(int)(k_items < sms ? k_items : sms), kKvThr, kv_smem, s>>>(mq, mdo, mk, mv,
-                                                                                  mdk, mdv, a);
+  attn_dkdv_tc<D, F16><<<(int)(k_items < sms ? k_items : sms), kKvThr, kv_smem, s>>>(
+      mq, mdo, mk, mv, mdk, mdv, a);
   return cpthd_host::launch_status();
 }
 
@@ -1177,7 +1206,7 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
                       const float* lse, const float* delta, void* dq, float* dk, float* dv,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale, float scale_log2,
-                      int mode, cudaStream_t s) {
+                      int mode, int f16, cudaStream_t s) {
   using namespace cpthd;
   BwdArgs a{};
   a.lse = lse;
@@ -1192,7 +1221,11 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
   a.scale_log2 = scale_log2;
   a.store = mode & 1;
   a.dq_mode = (mode & 2) ? 1 : (mode & 4) ? 2 : 0;
-  return D == 64 ? launch_bwd_tc<64>(q, k, v, dout, a, s) : launch_bwd_tc<128>(q, k, v, dout, a, s);
+  if (f16)
+    return D == 64 ? launch_bwd_tc<64, true>(q, k, v, dout, a, s)
+                   : launch_bwd_tc<128, true>(q, k, v, dout, a, s);
+  return D == 64 ? launch_bwd_tc<64, false>(q, k, v, dout, a, s)
+                 : launch_bwd_tc<128, false>(q, k, v, dout, a, s);
 }
 
 extern "C" int cpthd_status_bwd_tc(int reset) {

@@ -1,6 +1,9 @@
 // attn_fwd_tc.cu -- causal varlen attention forward of one CP rank on the
 // Blackwell tensor cores (tcgen05 + TMEM + TMA), built for sm_103a.
 //
+// The tensor-core operands (Q, K, V and the probabilities P) are all bf16 or
+// all fp16 (F16), accumulation fp32.
+//
 // What it computes ("[PyTorch] Add no-load-balance THD all-gather CP", §Why
 // and §Scope and constraints): for every local query row t of the rank (global
 // row g of document i), O_t = softmax_j(scale * q_t . k_j) v_j over the keys
@@ -167,7 +170,7 @@ struct Iter {  // flattened walk over an item's key-block intervals
   }
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const TcArgs a) {
@@ -337,8 +340,8 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, TBN, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idS = idesc_bf16_f32(128, TBN, false, false, F16);
+      constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true, F16);
       // the previous block's P V is issued after the next block's S
       int pv_g = -1, pv_ob = 0;
       bool pv_first = false;
@@ -630,7 +633,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
            // written before any O rescale so that S is dead while O is in registers
           uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
+          for (int e = 0; e < 32; ++e) pk[e] = pack_op<F16>(s[2 * e], s[2 * e + 1]);
           tmem_st32(tmem + lane_base + buf * 128 + 64 * hf, pk);
         }
         // O only has to be complete (P V_{g-1} done) when it is rescaled; the
@@ -688,22 +691,22 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // host side
 // ---------------------------------------------------------------------------
 
-template <int D>
+template <int D, bool F16>
 int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, cudaStream_t s) {
   alignas(64) CUtensorMap mq, mk, mv;
   int st;
-  st = a.q_idx ? tma::make_row_gather_map(&mq, q, a.q_rows, a.H, D)
-               : tma::make_thd_map(&mq, q, a.s_local, a.H, D, 128);
+  st = a.q_idx ? tma::make_row_gather_map(&mq, q, a.q_rows, a.H, D, F16)
+               : tma::make_thd_map(&mq, q, a.s_local, a.H, D, 128, F16);
   if (st != CP_OK) return st;
-  if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128)) != CP_OK) return st;
-  if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128, F16)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128, F16)) != CP_OK) return st;
   const int smem = Layout<D>::BYTES + (int)sizeof(Ctl);
-  if (cudaFuncSetAttribute(attn_fwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(attn_fwd_tc<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
     return CP_ERR_CUDA;
   const int64_t items = n_tiles_of(a.s_local) * (int64_t)a.H;
   const int grid = (int)(items < cpthd_host::sm_count() ? items : cpthd_host::sm_count());
-  attn_fwd_tc<D><<<grid, kThreadsTc, smem, s>>>(mq, mk, mv, a);
+  attn_fwd_tc<D, F16><<<grid, kThreadsTc, smem, s>>>(mq, mk, mv, a);
   return cpthd_host::launch_status();
 }
 
@@ -715,7 +718,8 @@ int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const voi
                       const void* v, void* o, void* o_resid, float* lse, const void* meta,
                       size_t meta_bytes,
                       int T, int H, int D, int s_local, int cp, int rank, int strategy,
-                      float scale_log2, cudaStream_t s, uint64_t limit_ns, int skip_first_k) {
+                      float scale_log2, int f16, cudaStream_t s, uint64_t limit_ns,
+                      int skip_first_k) {
   using namespace cpthd;
   TcArgs a{};
   a.o = (bf16*)o;
@@ -729,7 +733,8 @@ int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const voi
   a.scale_log2 = scale_log2;
   a.limit_ns = limit_ns ? limit_ns : kWaitLimitNs;
   a.skip_first_k = skip_first_k;
-  return D == 64 ? launch_fwd_tc<64>(q, k, v, a, s) : launch_fwd_tc<128>(q, k, v, a, s);
+  if (f16) return D == 64 ? launch_fwd_tc<64, true>(q, k, v, a, s) : launch_fwd_tc<128, true>(q, k, v, a, s);
+  return D == 64 ? launch_fwd_tc<64, false>(q, k, v, a, s) : launch_fwd_tc<128, false>(q, k, v, a, s);
 }
 
 extern "C" int cpthd_status_fwd_tc(int reset) {

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "cpthd.h"
@@ -229,6 +230,16 @@ inline __device__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+inline __device__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);  // .x = lo (low 16 bits)
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// Packs a pair in the tensor-core operand type (fp16 or bf16).
+template <bool F16>
+inline __device__ uint32_t pack_op(float lo, float hi) {
+  return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+
 // The two bf16 values of a packed pair as fp32 (exact: a bf16 is the upper
 // half of an fp32 bit pattern).
 inline __device__ float bf16_lo_f(uint32_t p) { return __uint_as_float(p << 16); }
@@ -268,20 +279,22 @@ extern "C" int cpthd_status_bwd_tc(int reset);
 
 // tcgen05 forward (attn_fwd_tc.cu); arguments validated by cp_attn_fwd /
 // cp_attn_fwd_gather (q_idx null: q is the rank's [s_local, H, D] queries;
-// o_resid nullable: O's bf16 rounding remainder, as bf16).
+// o_resid nullable: O's bf16 rounding remainder, as bf16; f16: Q/K/V are fp16,
+// else bf16).
 // limit_ns bounds every wait (0: the 4 s default); skip_first_k != 0 only in
 // the failure-detection test (CTA 0 never loads its first K tile).
 int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const void* k,
                       const void* v, void* o, void* o_resid, float* lse, const void* meta,
                       size_t meta_bytes,
                       int T, int H, int D, int s_local, int cp, int rank, int strategy,
-                      float scale_log2, cudaStream_t s, uint64_t limit_ns = 0,
+                      float scale_log2, int f16, cudaStream_t s, uint64_t limit_ns = 0,
                       int skip_first_k = 0);
 
 // tcgen05 dQ and dK/dV kernels (attn_bwd_tc.cu); Delta already in `delta`;
-// mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added)
+// mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added);
+// f16: Q/K/V/dO are fp16, else bf16
 int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
                       const float* lse, const float* delta, void* dq, float* dk, float* dv,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale, float scale_log2,
-                      int mode, cudaStream_t s);
+                      int mode, int f16, cudaStream_t s);

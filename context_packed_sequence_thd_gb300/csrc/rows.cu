@@ -5,7 +5,8 @@
 // context-parallel regression when padded cu_seqlens are value-equal but not
 // object-identical" (§Describe the bug, §Expected behavior).
 //
-// Also the all-to-all exchange of the a2a comm type (see a2a_kernel).
+// Also the all-to-all exchange of the a2a comm type (see a2a_kernel), and the
+// gather that converts bf16 rows to fp16 tensor-core operands.
 //
 // Design: one warp moves one row at a time; lanes stride over the row's
 // 16-byte chunks with several independent loads in flight before the stores
@@ -49,7 +50,37 @@ __device__ __forceinline__ void copy_row(const uint4* __restrict__ s, uint4* __r
   for (; c < chunks; c += 32) d[c] = ld_stream(s + c);
 }
 
-// mode 0: dst[i] = src[idx[i]]; mode 1: dst[idx[i]] = src[i]
+// 16 bytes of bf16 -> 16 bytes of fp16 (round to nearest).  A finite value
+// beyond the fp16 range becomes +-65504 and is reported; infinities and NaN
+// keep their meaning.
+__device__ __forceinline__ uint4 bf16x8_to_f16(uint4 v, bool& out_of_range) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xFFFF0000u);
+    if (fabsf(a) > 65504.f && fabsf(a) != INFINITY) { out_of_range = true; a = copysignf(65504.f, a); }
+    if (fabsf(b) > 65504.f && fabsf(b) != INFINITY) { out_of_range = true; b = copysignf(65504.f, b); }
+    __half2 h = __floats2half2_rn(a, b);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ void copy_row_f16(const uint4* __restrict__ s, uint4* __restrict__ d,
+                                             int chunks, int lane, bool& oor) {
+  int c = lane;
+  for (; c + 32 * (kUnroll - 1) < chunks; c += 32 * kUnroll) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream(s + c + 32 * u);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) d[c + 32 * u] = bf16x8_to_f16(v[u], oor);
+  }
+  for (; c < chunks; c += 32) d[c] = bf16x8_to_f16(ld_stream(s + c), oor);
+}
+
+// mode 0: dst[i] = src[idx[i]]; mode 1: dst[idx[i]] = src[i];
+// mode 2: dst[i] = fp16(src[idx ? idx[i] : i]) (bf16 source rows)
 template <int MODE>
 __global__ void __launch_bounds__(kRowThreads)
 rows_kernel(Ptrs p, int n_tensors, const int32_t* __restrict__ idx, int64_t n_rows,
@@ -57,17 +88,24 @@ rows_kernel(Ptrs p, int n_tensors, const int32_t* __restrict__ idx, int64_t n_ro
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * kRowThreads + threadIdx.x) >> 5;
   const int64_t n_warps = (int64_t(gridDim.x) * kRowThreads) >> 5;
+  bool oor = false;
   for (int64_t i = warp; i < n_rows; i += n_warps) {
-    const int64_t j = idx[i];
+    const int64_t j = (MODE == 2 && !idx) ? i : idx[i];
     if (j < 0 || j >= bound_rows) {
       if (lane == 0) atomicCAS(&g_status_rows, 0, CP_ERR_INVALID_ARG);
       continue;
     }
-    const int64_t si = MODE == 0 ? j : i;
-    const int64_t di = MODE == 0 ? i : j;
-    for (int k = 0; k < n_tensors; ++k)
-      copy_row(p.src[k] + si * chunks, p.dst[k] + di * chunks, chunks, lane);
+    const int64_t si = MODE == 1 ? i : j;
+    const int64_t di = MODE == 1 ? j : i;
+    for (int k = 0; k < n_tensors; ++k) {
+      if (MODE == 2)
+        copy_row_f16(p.src[k] + si * chunks, p.dst[k] + di * chunks, chunks, lane, oor);
+      else
+        copy_row(p.src[k] + si * chunks, p.dst[k] + di * chunks, chunks, lane);
+    }
   }
+  if (MODE == 2 && __any_sync(0xffffffffu, oor) && lane == 0)
+    atomicCAS(&g_status_rows, 0, CP_ERR_RANGE);
 }
 
 // All-to-all exchange of the a2a comm type ("[PyTorch] Extend no-load-balance
@@ -199,7 +237,8 @@ static int rows_op(int mode, const void* const* src, void* const* dst, int n, co
                    int64_t n_rows, int64_t bound_rows, int64_t row_bytes, void* stream) {
   int st = validate_rows(src, reinterpret_cast<const void* const*>(dst), n, n_rows, row_bytes);
   if (st != CP_OK) return st;
-  if (!idx || bound_rows < 0) return CP_ERR_INVALID_ARG;
+  if ((!idx && mode != 2) || bound_rows < 0) return CP_ERR_INVALID_ARG;
+  if (!idx && bound_rows < n_rows) return CP_ERR_INVALID_ARG;
   if (n_rows == 0) return CP_OK;
   Ptrs p{};
   for (int k = 0; k < n; ++k) {
@@ -211,8 +250,10 @@ static int rows_op(int mode, const void* const* src, void* const* dst, int n, co
   cudaStream_t s = cpthd_host::as_stream(stream);
   if (mode == 0)
     rows_kernel<0><<<grid, kRowThreads, 0, s>>>(p, n, idx, n_rows, bound_rows, chunks);
-  else
+  else if (mode == 1)
     rows_kernel<1><<<grid, kRowThreads, 0, s>>>(p, n, idx, n_rows, bound_rows, chunks);
+  else
+    rows_kernel<2><<<grid, kRowThreads, 0, s>>>(p, n, idx, n_rows, bound_rows, chunks);
   return cpthd_host::launch_status();
 }
 
@@ -220,6 +261,12 @@ extern "C" int cp_thd_gather(const void* const* d_src, void* const* d_dst, int n
                              const int32_t* d_idx, int64_t n_rows, int64_t src_rows,
                              int64_t row_bytes, void* stream) {
   return rows_op(0, d_src, d_dst, n_tensors, d_idx, n_rows, src_rows, row_bytes, stream);
+}
+
+extern "C" int cp_thd_gather_f16(const void* const* d_src, void* const* d_dst, int n_tensors,
+                                 const int32_t* d_idx, int64_t n_rows, int64_t src_rows,
+                                 int64_t row_bytes, void* stream) {
+  return rows_op(2, d_src, d_dst, n_tensors, d_idx, n_rows, src_rows, row_bytes, stream);
 }
 
 extern "C" int cp_thd_scatter(const void* const* d_src, void* const* d_dst, int n_tensors,

@@ -8,7 +8,8 @@
 //    byte offset >> 4 in bits 32-45, the fixed value 0b001 in bits 46-48,
 //    base offset 0, swizzle mode in bits 61-63 (2 = 128-byte swizzle);
 //  * instruction descriptor for kind::f16 (32 bit): D format in bits 4-5
-//    (1 = f32), A / B format in bits 7-9 / 10-12 (1 = bf16), A / B major-ness
+//    (1 = f32), A / B format in bits 7-9 / 10-12 (0 = f16, 1 = bf16; A and B
+//    always of one type), A / B major-ness
 //    in bits 15 / 16 (0 = K-major, 1 = MN-major), N >> 3 in bits 17-22,
 //    M >> 4 in bits 24-28.
 #pragma once
@@ -320,11 +321,13 @@ __device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) {
   return d + (uint64_t)(bytes >> 4);
 }
 
-// kind::f16 instruction descriptor: bf16 x bf16 -> f32, M x N.
+// kind::f16 instruction descriptor: bf16 x bf16 -> f32 (or, with f16, fp16 x
+// fp16 -> f32: A / B format code 0 instead of 1), M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+                                                      bool b_mn_major, bool f16 = false) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,

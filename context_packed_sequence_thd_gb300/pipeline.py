@@ -6,8 +6,9 @@ as follows ("[PyTorch] Add no-load-balance THD all-gather CP", §Sequence
 Diagram; "[PyTorch] Extend no-load-balance CP to the a2a comm type"):
 
   get_batch_on_this_cp_rank   cp_partition_index_all (every rank, one
-                              launch) + cp_thd_gather (Q/K/V/dO of every
-                              rank in one launch, DUAL_CHUNK_SWAP); with
+                              launch) + cp_thd_gather_f16 (Q/K/V/dO of every
+                              rank in one launch, converted to the fp16
+                              tensor-core operands); with bf16 operands and
                               NO_LOAD_BALANCE a rank's shard is a contiguous
                               slice, so no copy is made at all
   all-gather K/V              the ranks' local shards live side by side in one
@@ -156,28 +157,42 @@ class CPPlan:
 class CPAttention:
     """Buffers and the full emulated CP forward/backward for one plan."""
 
-    def __init__(self, plan: CPPlan, fuse_q_gather: bool = False):
+    def __init__(self, plan: CPPlan, fuse_q_gather: bool = False,
+                 operand_dtype: Optional[torch.dtype] = None):
         self.plan = plan
         p = plan
         # forward-only steps under DUAL_CHUNK_SWAP: the attention loads query
         # rows through the partition index (cp_attn_fwd_gather), no Q shard copy
         self.fuse_q_gather = fuse_q_gather
         self.q_src: Optional[torch.Tensor] = None
+        # tensor-core operand type of Q/K/V/dO: fp16 (the shard gathers convert
+        # the bf16 inputs; 11 significant bits, one product per term) unless
+        # the queries are read straight from the bf16 batch (fused gather)
+        if operand_dtype is None:
+            operand_dtype = torch.bfloat16 if fuse_q_gather else torch.float16
+        if operand_dtype not in (torch.bfloat16, torch.float16):
+            raise ValueError("operand_dtype must be torch.bfloat16 or torch.float16")
+        if fuse_q_gather and operand_dtype != torch.bfloat16:
+            raise ValueError("the fused query gather reads the bf16 batch: bf16 operands")
+        self.operand_dtype = operand_dtype
+        self.f16 = operand_dtype == torch.float16
         dev, T, H, D = p.device, p.T, p.H, p.D
         bf = dict(dtype=torch.bfloat16, device=dev)
+        op = dict(dtype=operand_dtype, device=dev)
         # rank-concatenated buffers: rank r's shard is rows [r*s_local, (r+1)*s_local);
-        # NO_LOAD_BALANCE shards are views of the inputs, so nothing is allocated
-        dcs = p.strategy == DCS
-        self.qc = torch.empty(T, H, D, **bf) if dcs else None
-        self.kc = torch.empty(T, H, D, **bf) if dcs else None
-        self.vc = torch.empty(T, H, D, **bf) if dcs else None
-        self.doc = torch.empty(T, H, D, **bf) if dcs else None
+        # bf16 NO_LOAD_BALANCE shards are views of the inputs, so nothing is
+        # allocated; fp16 ones are converted copies
+        own = p.strategy == DCS or self.f16
+        self.qc = torch.empty(T, H, D, **op) if own else None
+        self.kc = torch.empty(T, H, D, **op) if own else None
+        self.vc = torch.empty(T, H, D, **op) if own else None
+        self.doc = torch.empty(T, H, D, **op) if own else None
         self.oc = torch.empty(T, H, D, **bf)
         # O's bf16 rounding remainder: the backward's Delta = rowsum(dO * O) reads O + it
         self.oc_resid = torch.empty(T, H, D, **bf)
         self.lse = torch.empty(p.cp, H, p.s_local, dtype=torch.float32, device=dev)
-        self.k_full = torch.empty(T, H, D, **bf) if p.strategy == DCS else None
-        self.v_full = torch.empty(T, H, D, **bf) if p.strategy == DCS else None
+        self.k_full = torch.empty(T, H, D, **op) if p.strategy == DCS else None
+        self.v_full = torch.empty(T, H, D, **op) if p.strategy == DCS else None
         self.dqc = torch.empty(T, H, D, **bf)
         self.dkc = torch.empty(T, H, D, **bf)
         self.dvc = torch.empty(T, H, D, **bf)
@@ -210,21 +225,26 @@ class CPAttention:
     def shard_inputs(self, q, k, v, do=None, stream=None):
         """get_batch_on_this_cp_rank for every rank (plus dO for the backward)."""
         p = self.plan
-        if p.strategy == NLB:
+        if p.strategy == NLB and not self.f16:
             # contiguous shards: the rank-concatenated buffer is the input itself
             self.qc, self.kc, self.vc = q, k, v
             if do is not None:
                 self.doc = do
             return
         # every rank's shard in one gather: the rank-concatenated buffer is the
-        # input gathered by the ranks' indices side by side.  A forward-only
+        # input gathered by the ranks' indices side by side (NO_LOAD_BALANCE:
+        # the identity), converted to fp16 operands on the way.  A forward-only
         # step with the fused gather leaves Q where it is.
         self.q_src = q if (self.fuse_q_gather and do is None) else None
         srcs = ([q] if self.q_src is None else []) + [k, v] + ([do] if do is not None else [])
         dsts = ([self.qc] if self.q_src is None else []) + [self.kc, self.vc] + \
             ([self.doc] if do is not None else [])
+        idx = p.idx_all if p.strategy == DCS else None
         with self._timed("partition_gather", stream):
-            api.cp_thd_gather(srcs, dsts, p.idx_all, stream)
+            if self.f16:
+                api.cp_thd_gather_f16(srcs, dsts, idx, stream)
+            else:
+                api.cp_thd_gather(srcs, dsts, idx, stream)
         self.launches += 1
 
     def restore_kv(self, stream=None):
@@ -318,8 +338,8 @@ class CPA2AAttention(CPAttention):
     back to token shards.
     """
 
-    def __init__(self, plan: CPPlan):
-        super().__init__(plan)
+    def __init__(self, plan: CPPlan, operand_dtype: Optional[torch.dtype] = None):
+        super().__init__(plan, operand_dtype=operand_dtype)
         p = plan
         if p.H % p.cp:
             raise ValueError("the a2a comm type needs H divisible by cp_size")
@@ -328,8 +348,9 @@ class CPA2AAttention(CPAttention):
         # cp = 1 metadata of the whole packed sequence, for every rank's head slice
         self.full = CPPlan(p.cu, p.cup, 1, NLB, p.pad, self.Hc, D, dev)
         bf = dict(dtype=torch.bfloat16, device=dev)
+        op = dict(dtype=self.operand_dtype, device=dev)
         shape = (p.cp, T, self.Hc, D)
-        self.qh, self.kh, self.vh, self.doh = (torch.empty(shape, **bf) for _ in range(4))
+        self.qh, self.kh, self.vh, self.doh = (torch.empty(shape, **op) for _ in range(4))
         self.oh, self.dqh, self.dkh, self.dvh = (torch.empty(shape, **bf) for _ in range(4))
         self.oh_resid = torch.empty(shape, **bf)
         self.lse_h = torch.empty(p.cp, self.Hc, T, dtype=torch.float32, device=dev)
@@ -433,8 +454,8 @@ class CPP2PAttention(CPAttention):
     contribution to each shard stored; one launch casts all three to bf16.
     """
 
-    def __init__(self, plan: CPPlan):
-        super().__init__(plan)
+    def __init__(self, plan: CPPlan, operand_dtype: Optional[torch.dtype] = None):
+        super().__init__(plan, operand_dtype=operand_dtype)
         p = plan
         dev, T, H, D, S = p.device, p.T, p.H, p.D, p.s_local
         self.k_full = self.v_full = None   # no restore: attention reads the shards

@@ -64,8 +64,19 @@ typedef enum {
   CP_ERR_CUDA = -5,         /* a CUDA launch or runtime call failed */
   CP_ERR_WORKSPACE = -6,    /* metadata or workspace buffer too small */
   CP_ERR_METADATA = -7,     /* cu_seqlens values inconsistent (device-detected) */
-  CP_ERR_TIMEOUT = -8       /* a bounded device-side wait ran out; results are invalid */
+  CP_ERR_TIMEOUT = -8,      /* a bounded device-side wait ran out; results are invalid */
+  CP_ERR_RANGE = -9         /* a bf16 value beyond the fp16 range met an fp16 conversion */
 } cp_status_t;
+
+/* Type of the attention's tensor-core operands (Q, K, V, dO; the outputs O,
+ * dQ and the dK/dV accumulators keep their own types).  With bf16 operands
+ * the backward carries P and dS as two bf16 terms (rounded value plus
+ * rounding remainder, one extra tensor-core product each) to stay within the
+ * 2e-2 bound on long documents; fp16 operands carry 11 significant bits and
+ * need one term.  bf16 inputs convert to fp16 exactly when |x| lies in
+ * [2^-14, 65504] (cp_thd_gather_f16); smaller values lose low bits (absolute
+ * error below 2^-25), larger ones do not fit. */
+typedef enum { CP_OPERAND_BF16 = 0, CP_OPERAND_F16 = 1 } cp_dtype_t;
 
 /* Human-readable name of a status code (static storage). */
 const char* cp_status_string(int status);
@@ -164,6 +175,17 @@ int cp_thd_scatter(const void* const* d_src, void* const* d_dst, int n_tensors,
                    const int32_t* d_idx, int64_t n_rows, int64_t dst_rows, int64_t row_bytes,
                    void* stream);
 
+/* cp_thd_gather that converts bf16 source rows to fp16 (the tensor-core
+ * operand type CP_OPERAND_F16): d_dst[k] row i = fp16(d_src[k] row
+ * (d_idx ? d_idx[i] : i)), element-wise, round to nearest.  d_idx nullable
+ * (identity, src_rows >= n_rows).  A finite value beyond the fp16 range
+ * (|x| > 65504) is written as +-65504 and sets the device status word to
+ * CP_ERR_RANGE (results computed from it are not valid); infinities and NaN
+ * keep their meaning.  Other arguments as cp_thd_gather. */
+int cp_thd_gather_f16(const void* const* d_src, void* const* d_dst, int n_tensors,
+                      const int32_t* d_idx, int64_t n_rows, int64_t src_rows, int64_t row_bytes,
+                      void* stream);
+
 /* Emulated reduce-scatter epilogue of the dK/dV path ([AG] §Sequence Diagram,
  * "unrestore dK/dV for reduce-scatter"): the fp32 accumulators hold the sum
  * over ranks of the per-rank partials in original order; rank r's local
@@ -225,8 +247,9 @@ int cp_zero_tail(void* const* d_rows, int n_tensors, int64_t rows, int64_t row_b
  * DUAL_CHUNK_SWAP's two chunks per rank are handled in ONE launch.
  * ------------------------------------------------------------------------- */
 
-/* q_local [s_local,H,D] bf16 (rank-local order); k_full, v_full [T,H,D] bf16
- * in original order (the restored all-gather); o_local [s_local,H,D] bf16;
+/* q_local [s_local,H,D] (rank-local order); k_full, v_full [T,H,D] in
+ * original order (the restored all-gather), all three of operand_dtype (bf16
+ * or fp16); o_local [s_local,H,D] bf16;
  * lse_local [H, s_local] fp32.  o_resid_local (nullable) [s_local,H,D] bf16
  * receives O's rounding remainder, O - bf16(O), rounded to bf16: O_local +
  * o_resid_local carries the output to about 16 bits, and the backward's
@@ -237,12 +260,13 @@ int cp_zero_tail(void* const* d_rows, int n_tensors, int64_t rows, int64_t row_b
 int cp_attn_fwd(const void* q_local, const void* k_full, const void* v_full, void* o_local,
                 void* o_resid_local, float* lse_local, const void* d_meta, size_t meta_bytes,
                 int64_t total_tokens, int H, int D, int cp_size, int rank,
-                cp_strategy_t strategy, float softmax_scale, void* stream);
+                cp_strategy_t strategy, float softmax_scale, cp_dtype_t operand_dtype,
+                void* stream);
 
 /* cp_attn_fwd with the partition gather of the queries fused into the kernel
  * (the index_select of get_batch_on_this_cp_rank, [AG] §Sequence Diagram,
  * done by the attention's own loads): query row t of this
- * rank is row d_idx[t] of q_src [src_rows, H, D] bf16 (e.g. the unsharded
+ * rank is row d_idx[t] of q_src [src_rows, H, D] of operand_dtype (e.g. the unsharded
  * batch with d_idx from cp_partition_index), so no q_local copy is made.
  * d_idx: device int32 [s_local], 4-byte aligned (a rank's slice of the
  * ranks' indices side by side qualifies); a value outside
@@ -254,14 +278,16 @@ int cp_attn_fwd_gather(const void* q_src, int64_t src_rows, const int32_t* d_idx
                        const void* k_full, const void* v_full, void* o_local,
                        void* o_resid_local, float* lse_local, const void* d_meta,
                        size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
-                       int rank, cp_strategy_t strategy, float softmax_scale, void* stream);
+                       int rank, cp_strategy_t strategy, float softmax_scale,
+                       cp_dtype_t operand_dtype, void* stream);
 
 /* Device scratch cp_attn_bwd needs: Delta = rowsum(dO * O), fp32 [H, s_local]. */
 size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H);
 
 /* Backward of cp_attn_fwd for one rank.  Inputs as for cp_attn_fwd plus
  * o_local / lse_local from the forward, o_resid_local (nullable) from the
- * forward's o_resid_local output, and do_local [s_local,H,D] bf16.
+ * forward's o_resid_local output, and do_local [s_local,H,D] of operand_dtype
+ * (like q_local, k_full, v_full).
  * Writes dq_local [s_local,H,D] bf16 (overwritten) and ADDS this rank's
  * partial dK/dV into dk_accum / dv_accum (fp32 [T,H,D], original order; zero
  * them before rank 0 -- e.g. cp_zero_tail with valid_end = 0 -- or start the
@@ -275,7 +301,8 @@ int cp_attn_bwd(const void* q_local, const void* k_full, const void* v_full, con
                 void* dq_local, float* dk_accum,
                 float* dv_accum, const void* d_meta, size_t meta_bytes, int64_t total_tokens,
                 int H, int D, int cp_size, int rank, cp_strategy_t strategy, float softmax_scale,
-                void* d_workspace, size_t workspace_bytes, void* stream);
+                cp_dtype_t operand_dtype, void* d_workspace, size_t workspace_bytes,
+                void* stream);
 
 /* How cp_attn_bwd_ex delivers its gradients: one dK/dV choice (bit 0) OR'd
  * with at most one dQ choice (bits 1-2). */
@@ -304,8 +331,8 @@ int cp_attn_bwd_ex(const void* q_local, const void* k_full, const void* v_full,
                    const void* do_local,
                    void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
                    size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size, int rank,
-                   cp_strategy_t strategy, float softmax_scale, cp_bwd_mode_t mode,
-                   void* d_workspace, size_t workspace_bytes, void* stream);
+                   cp_strategy_t strategy, float softmax_scale, cp_dtype_t operand_dtype,
+                   cp_bwd_mode_t mode, void* d_workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * The P2P (ring) comm type, every rank on one GPU ([P2P] §Describe the bug:
@@ -387,7 +414,8 @@ int cp_attn_bwd_noalloc(const void* q_local, const void* k_full, const void* v_f
                         const float* lse_local, const void* do_local,
                         void* dq_local, float* dk_accum, float* dv_accum, const void* d_meta,
                         size_t meta_bytes, int64_t total_tokens, int H, int D, int cp_size,
-                        int rank, cp_strategy_t strategy, float softmax_scale, void* stream);
+                        int rank, cp_strategy_t strategy, float softmax_scale,
+                        cp_dtype_t operand_dtype, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Diagnostics

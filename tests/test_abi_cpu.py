@@ -138,28 +138,36 @@ def test_argument_validation_before_launch(lib):
     assert L.cp_thd_gather(_arr(*[FAKE] * 5), _arr(*[FAKE] * 5), 5, FAKE, 4, 4, 256, None) == -1
     # attention: unsupported head dim, bad rank, bad scale, missing workspace
     f = ctypes.c_float
-    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 96, 2, 0, 0, f(0.1), None) == -3
-    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64, 2, 2, 0, f(0.1), None) == -1
-    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64, 2, 0, 0, f(-1.0), None) == -1
-    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 127, 2, 64, 2, 0, 0, f(0.1), None) == -2
+    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 96, 2, 0, 0, f(0.1), 0, None) == -3
+    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64, 2, 2, 0, f(0.1), 0, None) == -1
+    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64, 2, 0, 0, f(-1.0), 0, None) == -1
+    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 127, 2, 64, 2, 0, 0, f(0.1), 0, None) == -2
     # a misaligned O residual (the optional second output) is refused like any other pointer
     assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE + 8, FAKE, FAKE, 4096, 128, 2, 64, 2, 0, 0,
-                         f(0.1), None) == -4
+                         f(0.1), 0, None) == -4
+    # an unknown tensor-core operand type
+    assert L.cp_attn_fwd(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 4096, 128, 2, 64, 2, 0, 0,
+                         f(0.1), 2, None) == -1
     # fused-gather forward: no index, misaligned index, empty source
     assert L.cp_attn_fwd_gather(FAKE, 4096, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2, 64,
-                                2, 0, 0, f(0.1), None) == -1
+                                2, 0, 0, f(0.1), 0, None) == -1
     assert L.cp_attn_fwd_gather(FAKE, 4096, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2,
-                                64, 2, 0, 0, f(0.1), None) == -4
+                                64, 2, 0, 0, f(0.1), 0, None) == -4
     assert L.cp_attn_fwd_gather(FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 4096, 2, 64,
-                                2, 0, 0, f(0.1), None) == -1
+                                2, 0, 0, f(0.1), 0, None) == -1
     assert L.cp_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2, 64,
-                         2, 0, 0, f(0.1), FAKE, 8, None) == -6
+                         2, 0, 0, f(0.1), 1, FAKE, 8, None) == -6
     assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
-                            64, 2, 0, 0, f(0.1), 7, FAKE, 1 << 20, None) == -1    # unknown mode
+                            64, 2, 0, 0, f(0.1), 0, 7, FAKE, 1 << 20, None) == -1    # unknown mode
     assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
-                            64, 2, 0, 0, f(0.1), 1, FAKE, 8, None) == -6           # store mode, small workspace
+                            64, 2, 0, 0, f(0.1), 1, 1, FAKE, 8, None) == -6           # store mode, small workspace
     assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
-                            64, 2, 0, 0, f(0.1), 6, FAKE, 1 << 20, None) == -1    # both dQ modes
+                            64, 2, 0, 0, f(0.1), 0, 6, FAKE, 1 << 20, None) == -1    # both dQ modes
+    assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
+                            64, 2, 0, 0, f(0.1), 5, 0, FAKE, 1 << 20, None) == -1    # unknown operand type
+    # the fp16 gather: index optional, but then the source must cover the rows
+    assert L.cp_thd_gather_f16(_arr(FAKE), _arr(FAKE), 1, None, 8, 4, 256, None) == -1
+    assert L.cp_thd_gather_f16(_arr(FAKE), _arr(FAKE), 1, None, 0, 4, 250, None) == -4
     assert L.cp_reduce_scatter_emul(_arr(FAKE), _arr(FAKE), 1, None, 0, 10, 5, 2, 64, None) == -1
 
 

@@ -14,10 +14,10 @@ from gpu_util import assert_close, assert_lse_close, dev, to_np
 pytestmark = pytest.mark.gpu
 
 
-def run(wl, strategy, d, tensors=None, bwd=True):
+def run(wl, strategy, d, tensors=None, bwd=True, operand_dtype=None):
     t = wl.tensors() if tensors is None else tensors
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, d)
-    att = pipeline.CPAttention(plan)
+    att = pipeline.CPAttention(plan, operand_dtype=operand_dtype)
     g = {k: v.to(d) for k, v in t.items()}
     att.step(g["q"], g["k"], g["v"], g["do"] if bwd else None)
     torch.cuda.synchronize()
@@ -33,11 +33,11 @@ def oracle_all(wl, t, bwd=True):
     return o, lse, oracle.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], wl.cu, wl.cup, pad)
 
 
-def check_against_oracle(wl, strategy, bwd=True):
+def check_against_oracle(wl, strategy, bwd=True, operand_dtype=None):
     d = dev()
     t = wl.tensors()
     o, lse, grads = oracle_all(wl, t, bwd)
-    plan, att = run(wl, strategy, d, t, bwd)
+    plan, att = run(wl, strategy, d, t, bwd, operand_dtype)
     for r in range(wl.cp):
         rows = oracle.partition_index(wl.cup, wl.cp, r, strategy)
         np.testing.assert_array_equal(plan.ranks[r].idx.cpu().numpy(), rows)
@@ -69,11 +69,14 @@ SMALL = {
 }
 
 
+# both tensor-core operand types: fp16 (the pipeline's default) and bf16
+# (P and dS as two bf16 terms)
+@pytest.mark.parametrize("operand_dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 @pytest.mark.parametrize("strategy", [pipeline.DCS, pipeline.NLB], ids=["dcs", "nlb"])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_parity_small(name, strategy):
+def test_parity_small(name, strategy, operand_dtype):
     make, bwd = SMALL[name]
-    check_against_oracle(make(), strategy, bwd)
+    check_against_oracle(make(), strategy, bwd, operand_dtype)
 
 
 def test_nlb_documents_not_divisible():

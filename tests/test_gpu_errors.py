@@ -90,13 +90,13 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable():
     L = api.lib()
     fn = L.cpthd_test_attn_fwd_timeout
     fn.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_size_t, ctypes.c_int64] + \
-        [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_uint64, ctypes.c_void_p]
+        [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, ctypes.c_uint64, ctypes.c_void_p]
     fn.restype = ctypes.c_int
     limit_ns = 50_000_000   # 50 ms
     st = fn(api._dev(p.local(att.qc, r), "q"), api._dev(att.k_full, "k"),
             api._dev(att.v_full, "v"), api._dev(o, "o"), api._dev(lse, "lse"),
             api._dev(p.ranks[r].meta, "meta"), p.ranks[r].meta.numel(), p.T, wl.H, wl.D, p.cp, r,
-            p.strategy, p.scale, limit_ns, api._stream())
+            p.strategy, p.scale, api._operand_dtype(att.qc), limit_ns, api._stream())
     assert st == 0
     torch.cuda.synchronize()
     assert api.cp_device_status(reset=True) == CP_ERR_TIMEOUT

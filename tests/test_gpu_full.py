@@ -20,9 +20,9 @@ def _heads_slice(t, heads):
     return {k: v[:, heads].contiguous() for k, v in t.items()}
 
 
-def _run_all(wl, strategy, d, g, bwd, cls=pipeline.CPAttention):
+def _run_all(wl, strategy, d, g, bwd, cls=pipeline.CPAttention, operand_dtype=None):
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, d)
-    att = cls(plan)
+    att = cls(plan, operand_dtype=operand_dtype)
     att.step(g["q"], g["k"], g["v"], g["do"] if bwd else None)
     torch.cuda.synchronize()
     assert api.cp_device_status() == 0
@@ -58,8 +58,9 @@ def _compare_acc(att, heads, dk, dv, what, acc):
 
 # Every head of every workload with a backward: the heads are independent, so
 # the oracle computes them in groups of 8 while the GPU results of both
-# strategies stay on the device.  No head is left out, so no head can hide an
-# out-of-tolerance element.
+# strategies and both tensor-core operand types (fp16, the default; bf16 with
+# two-term P and dS) stay on the device.  No head is left out, so no head can
+# hide an out-of-tolerance element.
 @pytest.mark.parametrize("make", [inputs.cfg2, inputs.cfg4, inputs.cfg5], ids=["cfg2", "cfg4", "cfg5"])
 def test_full_size_fwd_bwd_all_heads(make):
     d = dev()
@@ -67,7 +68,8 @@ def test_full_size_fwd_bwd_all_heads(make):
     t = wl.tensors()
     g = {k: v.to(d) for k, v in t.items()}
     pad = wl.pad_between_seqs
-    runs = [_run_all(wl, strategy, d, g, True) for strategy in wl.strategies]
+    runs = [_run_all(wl, strategy, d, g, True, operand_dtype=dt)
+            for strategy in wl.strategies for dt in (torch.float16, torch.bfloat16)]
     worst = [{} for _ in runs]
     for h0 in range(0, wl.H, 8):
         heads = list(range(h0, min(h0 + 8, wl.H)))
@@ -77,9 +79,9 @@ def test_full_size_fwd_bwd_all_heads(make):
         for (plan, att), acc in zip(runs, worst):
             _compare(wl, plan, att, heads, o, lse, grads, acc=acc)
             _compare_acc(att, heads, grads[1], grads[2], f"heads {heads}", acc)
-    for (plan, _), acc in zip(runs, worst):
-        print(f"\n{wl.name} {pipeline.STRATEGY_NAMES[plan.strategy]} worst max-abs over all "
-              f"{wl.H} heads: " + ", ".join(f"{k} {v:.5f}" for k, v in acc.items()))
+    for (plan, att), acc in zip(runs, worst):
+        print(f"\n{wl.name} {pipeline.STRATEGY_NAMES[plan.strategy]} {att.operand_dtype} worst "
+              f"max-abs over all {wl.H} heads: " + ", ".join(f"{k} {v:.5f}" for k, v in acc.items()))
 
 
 @pytest.mark.parametrize("make,heads", [(inputs.cfg2, [3]), (inputs.cfg5, [0])],

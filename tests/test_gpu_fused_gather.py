@@ -32,7 +32,7 @@ def test_fused_gather_bitwise_equals_gathered_forward(name, strategy):
     wl = CASES[name]()
     t = {k: v.to(d) for k, v in wl.tensors(with_grad=False).items()}
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, d)
-    ref = pipeline.CPAttention(plan)
+    ref = pipeline.CPAttention(plan, operand_dtype=torch.bfloat16)
     ref.step(t["q"], t["k"], t["v"])
     kf, vf = (ref.k_full, ref.v_full) if strategy == pipeline.DCS else (t["k"], t["v"])
     o = torch.empty_like(ref.oc)

@@ -175,3 +175,43 @@ def test_partition_index_all_ranks_one_launch_bytewise(make):
         assert api.cp_device_status() == 0
         assert torch.equal(idx1, idx2) and torch.equal(res1, res2)
         assert torch.equal(meta1, meta2)
+
+
+def test_gather_f16_conversion_and_range():
+    """cp_thd_gather_f16: each element is the bf16 source value rounded to the
+    nearest fp16 (numpy's float32 -> float16 conversion of the same values,
+    ties to even), with and without an index; a finite value beyond 65504
+    becomes +-65504 and reports CP_ERR_RANGE; infinities and NaN stay."""
+    d = dev()
+    g = torch.Generator().manual_seed(91)
+    T, H, D = 300, 2, 64
+    src = (torch.randn(T, H, D, generator=g) * torch.exp2(torch.randint(-20, 15, (T, H, D), generator=g)
+                                                           .float())).bfloat16()
+    src[0, 0, :4] = torch.tensor([65504.0, 65520.0, -1e6, 2.0 ** -20]).bfloat16()
+    x = src.float().numpy()
+    small = np.abs(x) <= 65504
+    assert small.mean() > 0.9
+    dst = torch.empty(T, H, D, dtype=torch.float16, device=d)
+    # only in-range values first: exact agreement, no status
+    ok = src.clone()
+    ok[torch.from_numpy(~small)] = 1.0
+    api.cp_thd_gather_f16([ok.to(d)], [dst], None)
+    torch.cuda.synchronize()
+    assert api.cp_device_status() == 0
+    want = ok.float().numpy().astype(np.float16)
+    np.testing.assert_array_equal(dst.cpu().numpy().view(np.uint16), want.view(np.uint16))
+    # through an index
+    idx = torch.randperm(T, generator=g)[:128].to(torch.int32)
+    dst2 = torch.empty(128, H, D, dtype=torch.float16, device=d)
+    api.cp_thd_gather_f16([ok.to(d)], [dst2], idx.to(d))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(dst2.cpu().numpy().view(np.uint16),
+                                  want[idx.long().numpy()].view(np.uint16))
+    # out of range: clamped and reported; inf and nan pass through
+    bad = ok.clone()
+    bad[1, 1, :4] = torch.tensor([1e6, -7e4, float("inf"), float("nan")]).bfloat16()
+    api.cp_thd_gather_f16([bad.to(d)], [dst], None)
+    torch.cuda.synchronize()
+    assert api.cp_device_status(reset=True) == -9          # CP_ERR_RANGE
+    got = dst[1, 1, :4].cpu().float().numpy()
+    assert got[0] == 65504 and got[1] == -65504 and np.isposinf(got[2]) and np.isnan(got[3])

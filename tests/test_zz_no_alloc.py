@@ -23,13 +23,13 @@ from gpu_util import assert_close, dev, to_np
 pytestmark = pytest.mark.gpu
 
 
-def _forward(wl, strategy, d, seed_shift):
+def _forward(wl, strategy, d, seed_shift, operand_dtype):
     t = wl.tensors()
     if seed_shift:
         g = torch.Generator().manual_seed(wl.seed + seed_shift)
         t["do"] = torch.randn(t["do"].shape, generator=g).bfloat16()
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, d)
-    att = pipeline.CPAttention(plan)
+    att = pipeline.CPAttention(plan, operand_dtype=operand_dtype)
     g = {k: v.to(d) for k, v in t.items()}
     att.shard_inputs(g["q"], g["k"], g["v"], g["do"])
     kf, vf = att.forward()
@@ -55,14 +55,15 @@ def _backward(plan, att, kf, vf, noalloc):
     return dq, dk, dv
 
 
+@pytest.mark.parametrize("operand_dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 @pytest.mark.parametrize("strategy", [pipeline.DCS, pipeline.NLB], ids=["dcs", "nlb"])
-def test_noalloc_backward_matches_workspace_backward_twice(strategy):
+def test_noalloc_backward_matches_workspace_backward_twice(strategy, operand_dtype):
     d = dev()
     cases = [inputs.custom([176, 272, 64], cp=4, H=3, D=128, seed=81),
              inputs.custom([100, 7, 250, 33], padded=[112, 16, 256, 48], cp=4, H=2, D=64, seed=82)]
     for wl in cases:
         for call in range(2):  # two calls in a row: the scratch keeps the previous contents
-            plan, att, kf, vf = _forward(wl, strategy, d, seed_shift=call)
+            plan, att, kf, vf = _forward(wl, strategy, d, call, operand_dtype)
             ref = _backward(plan, att, kf, vf, noalloc=False)
             got = _backward(plan, att, kf, vf, noalloc=True)
             for name, a, b in zip(("dQ", "dK", "dV"), got, ref):
@@ -78,6 +79,6 @@ def test_noalloc_rejects_sizes_beyond_the_scratch():
     fake = 0x10000
     T = 2 * api.NOALLOC_MAX_SCRATCH_FLOATS  # cp=1, H=1: s_local*H = 2x the maximum
     st = L.cp_attn_bwd_noalloc(fake, fake, fake, fake, None, fake, fake, fake, fake, fake, fake,
-                               1 << 20, T, 1, 64, 1, 0, 1, ctypes.c_float(0.125), None)
+                               1 << 20, T, 1, 64, 1, 0, 1, ctypes.c_float(0.125), 0, None)
     assert st == -6
     assert api.status_string(st) == "CP_ERR_WORKSPACE"
