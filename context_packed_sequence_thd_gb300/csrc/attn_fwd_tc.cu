@@ -342,6 +342,11 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, TBN, false, false, F16);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true, F16);
+      // operand descriptors at the tiles' first bytes, built once (an MMA's
+      // descriptor is then one 64-bit add): Q and K K-major, V MN-major
+      const uint64_t dsc_q = sdesc_sw128(sb + L::Q, 16, 1024);
+      const uint64_t dsc_k = sdesc_sw128(sb + L::K, 16, 1024);
+      const uint64_t dsc_v = sdesc_sw128(sb + L::V, kBoxBytes, 1024);
       // the previous block's P V is issued after the next block's S
       int pv_g = -1, pv_ob = 0;
       bool pv_first = false;
@@ -353,13 +358,12 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tc_fence_after();
         // A = P from TMEM: keys [0,64) over columns [0,32) and keys [64,128)
         // over [64,96) of S_g's buffer (written by the two column halves)
+        const uint64_t bv = sdesc_add(dsc_v, vs * L::TILE);
+        const uint32_t dO = tmem + o_col<D>(pv_ob), aP = tmem + (pv_g & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < TBN / 16; ++kk) {
-          const uint64_t db = sdesc_sw128(sb + L::V + vs * L::TILE + kk * 2048, kBoxBytes, 1024);
-          umma_bf16_ts(tmem + o_col<D>(pv_ob),
-                       tmem + (pv_g & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8, db, idO,
+        for (int kk = 0; kk < TBN / 16; ++kk)
+          umma_bf16_ts(dO, aP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bv, kk * 2048), idO,
                        (!pv_first || kk > 0) ? 1u : 0u);
-        }
         umma_commit(bar(bars.v_empty[vs]));
         umma_commit(bar(bars.o_ready[pv_g & 1]));
         return true;
@@ -388,11 +392,11 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             break;
           }
           tc_fence_after();
+          const uint64_t bq = sdesc_add(dsc_q, qb * L::TILE), bk = sdesc_add(dsc_k, ks * L::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            umma_bf16(tmem + buf * 128, sdesc_sw128(sb + L::Q + qb * L::TILE + off, 16, 1024),
-                      sdesc_sw128(sb + L::K + ks * L::TILE + off, 16, 1024), idS,
+            umma_bf16(tmem + buf * 128, sdesc_add(bq, off), sdesc_add(bk, off), idS,
                       kk > 0 ? 1u : 0u);
           }
           umma_commit(bar(bars.s_full[buf]));
