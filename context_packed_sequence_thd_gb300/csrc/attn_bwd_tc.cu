@@ -17,9 +17,9 @@
 //
 // attn_dq_tc   items (128-query tile, head), iterating the key blocks the
 //              tile attends.  S = Q K^T and dP = dO V^T into TMEM (M=128
-//              queries, N=128 keys); the compute warps form dS into one of two
-//              separate TMEM buffers (bf16); dQ += dS K with A = dS from TMEM,
-//              B = K as an MN-major operand.  K tiles sit in a 3-stage ring
+//              queries, N=128 keys); the compute warps form dS into TMEM
+//              columns of its own; dQ += dS K with A = dS from TMEM, B = K as
+//              an MN-major operand.  K tiles sit in a 3-stage ring
 //              (released after dQ), V tiles in a 2-stage ring (released after
 //              dP).
 // attn_dkdv_tc items (128-key block, head), iterating the rank's query tiles
@@ -35,9 +35,9 @@
 // Warp roles: warps 0-7 compute (warp w serves TMEM lanes 32*(w%4).. and the
 // column half w/4 of every row, so two warps share each row's elementwise
 // work), warp 8 TMA producer, warp 9 TMEM allocator + single-thread MMA
-// issuer.  The MMA thread interleaves consecutive steps (the next S product
-// is issued before the previous step's gradient product) so the tensor core
-// keeps working while the compute warps run the elementwise part.  A compute
+// issuer.  The MMA thread interleaves consecutive steps (a step's products are
+// issued while the previous step's gradient product is still pending) so the
+// tensor core keeps working while the compute warps run the elementwise part.  A compute
 // thread writes P / dS back only into TMEM columns it has itself already read,
 // so the two column halves never race.  Every wait is bounded.
 #include <math.h>
@@ -197,27 +197,31 @@ struct DqLayout {
   static constexpr int BYTES = V + kDqVStages * TILE;
 };
 
-// TMEM of attn_dq_tc: S [0,128), dP [128,256), dQ [256,256+D).  dS goes over
-// the dP columns it was computed from, as two bf16 terms (hi, lo; hilo_col).
+// TMEM of attn_dq_tc: S [0,128), dP [128,256), dQ [256,256+D), dS [384,512)
+// (fp16 pairs, or two bf16 terms hi, lo; hilo_col).  dS has columns of its own
+// so that dP_g can be computed as soon as dP_{g-1} is in registers, while dS_{g-1}
+// is still being formed and read by dQ_{g-1}.
 
 struct DqCtl {
   uint64_t qd_full, qd_free;  // Q/dO of the item landed / all its S, dP products done
   uint64_t k_full[kDqKStages], k_empty[kDqKStages];
   uint64_t v_full[kDqVStages], v_empty[kDqVStages];
-  uint64_t s_full, s_free, dp_full, ds_full, done, mma_done;
+  uint64_t s_full, s_free, dp_full, dp_free, ds_full, ds_free, done, mma_done;
   uint32_t tmem;
   int abort;
 };
 
-// Per key block g the MMA thread issues S_g, then the previous block's
-// dQ_{g-1} (once dS_{g-1} is in TMEM), then dP_g.  S has its own release
-// barrier (s_free: the compute warps have read S_g into registers), so S_{g+1}
-// is computed while the compute warps are still forming dS_g, and dS goes to
-// one of two separate TMEM buffers so that dQ_{g-1} and S_{g+1} do not
-// conflict.  Every per-block barrier completes once per block; the order
-// "wait ds_full(g-1) before committing dp_full(g)" (and "wait s_free(g-1)
-// before committing s_full(g)") keeps each of them at most one phase ahead of
-// its waiter, so the parity waits never alias.
+// Per key block g the MMA thread issues dP_g as soon as the compute warps have
+// read dP_{g-1} into registers (dp_free), then dQ_{g-1} once dS_{g-1} is in
+// TMEM, then S_{g+1} once S_g has been read (s_free).  The compute warps are
+// then never waiting for dP: it is computed while they form dS_{g-1} and the
+// exponentials of block g.  dS_g is written only after dQ_{g-1} has finished
+// reading dS_{g-1} (ds_free).  Every per-block barrier completes once per
+// block, and each one's next phase needs a step of its waiter first (dP_{g+1}
+// waits for dp_free(g), which the compute warps arrive at after waiting for
+// dp_full(g); S_{g+1} waits for s_free(g), after s_full(g); dQ_g waits for
+// ds_full(g), which follows the wait for ds_free(g-1)), so a parity wait never
+// sees a phase two ahead.
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThr, 1)
 attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -254,7 +258,9 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     mbar_init(bar_addr(c.s_full), 1);
     mbar_init(bar_addr(c.s_free), kCompute);
     mbar_init(bar_addr(c.dp_full), 1);
+    mbar_init(bar_addr(c.dp_free), kCompute);
     mbar_init(bar_addr(c.ds_full), kCompute);
+    mbar_init(bar_addr(c.ds_free), 1);
     mbar_init(bar_addr(c.done), 1);
     mbar_init(bar_addr(c.mma_done), 1);
     fence_barrier_init();
@@ -332,7 +338,13 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mbar_wait(bar_addr(c.v_full[j % kDqVStages]), (j / kDqVStages) & 1, &never, kLimitNs);
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
+    // The whole warp runs the issue loop (uniform control flow, warp-uniform
+    // waits); one elected lane issues each MMA and commit.
+    auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
+      return __all_sync(0xffffffffu, w);
+    };
+    {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false, F16);
       constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, true, F16);
       // operand descriptors at the tiles' first bytes (K-major, and K as MN-major)
@@ -344,58 +356,44 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       int ii = 0, g = 0;
       int pend = -1;  // block whose dQ product is still to be issued
       bool pend_first = false;
-      // dQ += dS K : A = dS (bf16 pairs in TMEM), B = K tile as MN-major (N = d)
-      // Barrier phases of the next group, tested (without blocking) while the
-      // current group is still being issued; a phase seen complete needs no wait.
-      bool seen_k = false, seen_s = false, seen_ds = false, seen_v = false;
-      auto issue_dq = [&](int vs_next, int g_next) -> bool {
-        if (!seen_ds && !mbar_wait(bar_addr(c.ds_full), pend & 1, &s_abort, kLimitNs)) return false;
-        seen_ds = false;
+      // dQ_pend += dS K : A = dS (TMEM, its own columns), B = K tile as
+      // MN-major (N = d); bf16 dS is the sum of two terms (rounded values,
+      // then their remainders): two products per k-step, fp16 dS one.  An
+      // item's first dQ starts afresh: its ds_full comes after the compute
+      // warps have read the previous item's dQ out of TMEM.
+      auto issue_dq = [&]() -> bool {
+        if (!wait_w(bar_addr(c.ds_full), pend & 1)) return false;
         tc_fence_after();
-        const int ks = pend % kDqKStages;
-        const uint64_t bk = sdesc_add(dsc_kmn, ks * L::TILE);
-        // bf16 dS is the sum of two terms (rounded values, then their
-        // remainders): two products per k-step; fp16 dS one
+        const int pks = pend % kDqKStages;
+        const uint64_t bkm = sdesc_add(dsc_kmn, pks * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t b = sdesc_add(bk, kk * 2048);
-          umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk), b, idQ,
+          const uint64_t b = sdesc_add(bkm, kk * 2048);
+          umma_bf16_ts_w(tmem + 256, tmem + 384 + hilo_col(kk), b, idQ,
                        (!pend_first || kk > 0) ? 1u : 0u);
-          if (!F16) umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk) + 16, b, idQ, 1u);
-          if (kk == 4 && vs_next >= 0 && !seen_v)
-            seen_v = mbar_test_wait(bar_addr(c.v_full[vs_next]), (g_next / kDqVStages) & 1);
+          if (!F16) umma_bf16_ts_w(tmem + 256, tmem + 384 + hilo_col(kk) + 16, b, idQ, 1u);
         }
-        umma_commit(bar_addr(c.k_empty[ks]));
+        umma_commit_w(bar_addr(c.k_empty[pks]));
+        umma_commit_w(bar_addr(c.ds_free));
         return true;
       };
       // S_g = Q K_g^T into TMEM columns [0,128).  S_g overwrites S_{g-1}: the
       // compute warps must have read it (s_free), and K_g must have landed.
       auto issue_s = [&](int gs_) -> bool {
-        const int ks = gs_ % kDqKStages, vs = gs_ % kDqVStages;
-        if ((!seen_k &&
-             !mbar_wait(bar_addr(c.k_full[ks]), (gs_ / kDqKStages) & 1, &s_abort, kLimitNs)) ||
-            (gs_ > 0 && !seen_s &&
-             !mbar_wait(bar_addr(c.s_free), (gs_ - 1) & 1, &s_abort, kLimitNs)))
+        const int ks = gs_ % kDqKStages;
+        if (!wait_w(bar_addr(c.k_full[ks]), (gs_ / kDqKStages) & 1) ||
+            (gs_ > 0 && !wait_w(bar_addr(c.s_free), (gs_ - 1) & 1)))
           return false;
-        seen_k = seen_s = false;
         tc_fence_after();
         const uint64_t bk = sdesc_add(dsc_k, ks * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = kmajor_off(kk);
-          umma_bf16(tmem, sdesc_add(dsc_q, off), sdesc_add(bk, off), idS, kk > 0);
-          if (kk == D / 32) {  // the next groups' barriers: dS of the pending block, V_g
-            if (pend >= 0) seen_ds = mbar_test_wait(bar_addr(c.ds_full), pend & 1);
-            seen_v = mbar_test_wait(bar_addr(c.v_full[vs]), (gs_ / kDqVStages) & 1);
-          }
+          umma_bf16_w(tmem, sdesc_add(dsc_q, off), sdesc_add(bk, off), idS, kk > 0);
         }
-        umma_commit(bar_addr(c.s_full));
+        umma_commit_w(bar_addr(c.s_full));
         return true;
       };
-      // Order per key block g: [S_g issued earlier], dQ_{g-1}, dP_g, S_{g+1}.  The
-      // next block's S goes in right after dP_g -- before the buffer-release
-      // commits and the loop bookkeeping -- so the tensor pipe has queued work
-      // while this thread competes for issue slots with the compute warps.
       bool ok = true;
       for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
         const int k = snake_item(j, blockIdx.x, gridDim.x);
@@ -403,7 +401,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         Item it;
         it.load(m.qorder, m.qlists, k, a.H, n_qt);
         if (it.nb == 0) continue;
-        if (!mbar_wait(bar_addr(c.qd_full), ii & 1, &s_abort, kLimitNs)) {
+        if (!wait_w(bar_addr(c.qd_full), ii & 1)) {
           fail(&s_abort);
           break;
         }
@@ -414,33 +412,28 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         for (int j = 0; j < it.nb; ++j, ++g) {
           const int vs = g % kDqVStages;
-          // dQ of the previous block (waits for its dS; that also means the
-          // compute warps have read dP_{g-1}, which dP_g overwrites)
-          if (pend >= 0 && !issue_dq(vs, g)) {
+          // dP_g = dO V_g^T overwrites dP_{g-1}: the compute warps must have read it
+          if ((g > 0 && !wait_w(bar_addr(c.dp_free), (g - 1) & 1)) ||
+              !wait_w(bar_addr(c.v_full[vs]), (g / kDqVStages) & 1)) {
             fail(&s_abort);
             ok = false;
             break;
           }
-          if (!seen_v &&
-              !mbar_wait(bar_addr(c.v_full[vs]), (g / kDqVStages) & 1, &s_abort, kLimitNs)) {
-            fail(&s_abort);
-            ok = false;
-            break;
-          }
-          seen_v = false;
           tc_fence_after();
           const uint64_t bv = sdesc_add(dsc_v, vs * L::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = kmajor_off(kk);
-            umma_bf16(tmem + 128, sdesc_add(dsc_do, off), sdesc_add(bv, off), idS, kk > 0);
-            if (kk == D / 32) {  // the next block's S: its K tile, and S_g read out
-              const int gn = g + 1;
-              seen_k = mbar_test_wait(bar_addr(c.k_full[gn % kDqKStages]), (gn / kDqKStages) & 1);
-              seen_s = mbar_test_wait(bar_addr(c.s_free), g & 1);
-            }
+            umma_bf16_w(tmem + 128, sdesc_add(dsc_do, off), sdesc_add(bv, off), idS, kk > 0);
           }
-          umma_commit(bar_addr(c.dp_full));
+          umma_commit_w(bar_addr(c.dp_full));
+          umma_commit_w(bar_addr(c.v_empty[vs]));
+          if (j == it.nb - 1) umma_commit_w(bar_addr(c.qd_free));  // every S and dP of the item issued
+          if (pend >= 0 && !issue_dq()) {
+            fail(&s_abort);
+            ok = false;
+            break;
+          }
           pend = g;
           pend_first = (j == 0);
           if (j + 1 < it.nb && !issue_s(g + 1)) {
@@ -448,19 +441,17 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             ok = false;
             break;
           }
-          umma_commit(bar_addr(c.v_empty[vs]));
-          if (j == it.nb - 1) umma_commit(bar_addr(c.qd_free));
         }
         if (!ok) break;
         // the item's last dQ product, then its epilogue may read dQ
-        if (!issue_dq(-1, 0)) {
+        if (!issue_dq()) {
           fail(&s_abort);
           break;
         }
         pend = -1;
-        umma_commit(bar_addr(c.done));
+        umma_commit_w(bar_addr(c.done));
       }
-      umma_commit(bar_addr(c.mma_done));
+      umma_commit_w(bar_addr(c.mma_done));
       int never = 0;
       mbar_wait(bar_addr(c.mma_done), 0, &never, kLimitNs);
     }
@@ -529,25 +520,33 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           break;
         }
         tc_fence_after();
-        // dS = P (dP - Delta) over the dP columns just read (one fp16 term, or
-        // hi and lo bf16 terms)
+        // dP_g into registers; its columns are then free for dP_{g+1}
+        uint32_t dp[64];
+        tmem_ld32(tmem + lb + 128 + 64 * hf, dp);
+        tmem_ld32(tmem + lb + 128 + 64 * hf + 32, dp + 32);
+        tc_fence_before();
+        mbar_arrive(bar_addr(c.dp_free));
+        // dS = P (dP - Delta)
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t dp[32];
-          const uint32_t col = tmem + lb + 128 + 64 * hf + 32 * cc;
-          tmem_ld32(col, dp);
-#pragma unroll
-          for (int e2 = 0; e2 < 16; ++e2) {
-            float x0, x1;
-            f2_unpack(f2_mul(f2_pack(p[cc * 32 + 2 * e2], p[cc * 32 + 2 * e2 + 1]),
-                             f2_sub(f2_pack(__uint_as_float(dp[2 * e2]),
-                                            __uint_as_float(dp[2 * e2 + 1])), dl2)),
-                      x0, x1);
-            dp[2 * e2] = __float_as_uint(x0);
-            dp[2 * e2 + 1] = __float_as_uint(x1);
-          }
-          store_operand<F16>(col, reinterpret_cast<const float*>(dp));
+        for (int e2 = 0; e2 < 32; ++e2) {
+          float x0, x1;
+          f2_unpack(f2_mul(f2_pack(p[2 * e2], p[2 * e2 + 1]),
+                           f2_sub(f2_pack(__uint_as_float(dp[2 * e2]),
+                                          __uint_as_float(dp[2 * e2 + 1])), dl2)),
+                    x0, x1);
+          dp[2 * e2] = __float_as_uint(x0);
+          dp[2 * e2 + 1] = __float_as_uint(x1);
         }
+        // into the dS columns (one fp16 term, or hi and lo bf16 terms), once
+        // dQ_{g-1} has finished reading dS_{g-1}
+        if (g > 0 && !wait_warp(bar_addr(c.ds_free), (g - 1) & 1)) {
+          fail(&s_abort);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        store_operand<F16>(tmem + lb + 384 + 64 * hf, reinterpret_cast<const float*>(dp));
+        store_operand<F16>(tmem + lb + 384 + 64 * hf + 32, reinterpret_cast<const float*>(dp + 32));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar_addr(c.ds_full));
@@ -823,7 +822,13 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         mbar_wait(bar_addr(c.q_full[i % kStg]), (i / kStg) & 1, &never, kLimitNs);
     }
   } else if (warp == kKvMma) {
-    if (lane == 0) {
+    // The whole warp runs the issue loop (uniform control flow, warp-uniform
+    // waits); one elected lane issues each MMA and commit.
+    auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool w = mbar_wait(b, parity, &s_abort, kLimitNs);
+      return __all_sync(0xffffffffu, w);
+    };
+    {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false, F16);
       constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true, F16);
       // operand descriptors at the tiles' first bytes (K-major, and Q / dO as MN-major)
@@ -840,9 +845,9 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       // item's first dK starts dK afresh: the epilogue warps must have read the
       // previous item's dK out of TMEM first.
       auto issue_dk = [&]() -> bool {
-        if (!mbar_wait(bar_addr(c.ds_full), pend & 1, &s_abort, kLimitNs)) return false;
+        if (!wait_w(bar_addr(c.ds_full), pend & 1)) return false;
         if (pend_first && pend_item > 0 &&
-            !mbar_wait(bar_addr(c.dk_free), (pend_item - 1) & 1, &s_abort, kLimitNs))
+            !wait_w(bar_addr(c.dk_free), (pend_item - 1) & 1))
           return false;
         tc_fence_after();
         const uint64_t bq = sdesc_add(dsc_qmn, pend_st * L::TILE);
@@ -850,11 +855,11 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll (D == 64 ? 8 : 4)
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t b = sdesc_add(bq, kk * 2048);
-          umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk), b, idG,
+          umma_bf16_ts_w(tmem + 256, tmem + 128 + hilo_col(kk), b, idG,
                        (!pend_first || kk > 0) ? 1u : 0u);
-          if (!F16) umma_bf16_ts(tmem + 256, tmem + 128 + hilo_col(kk) + 16, b, idG, 1u);
+          if (!F16) umma_bf16_ts_w(tmem + 256, tmem + 128 + hilo_col(kk) + 16, b, idG, 1u);
         }
-        umma_commit(bar_addr(c.q_empty[pend_st]));
+        umma_commit_w(bar_addr(c.q_empty[pend_st]));
         return true;
       };
       bool ok = true;
@@ -865,13 +870,13 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         it.load(m.korder, m.klists, k, a.H, n_kb);
         if (it.nb == 0) continue;
         const int cur = ii++;
-        if (!mbar_wait(bar_addr(c.k_full), cur & 1, &s_abort, kLimitNs)) {
+        if (!wait_w(bar_addr(c.k_full), cur & 1)) {
           fail(&s_abort);
           break;
         }
         for (int i = 0; i < it.nb; ++i, ++gs) {
           const int st = gs % kStg;
-          if (!mbar_wait(bar_addr(c.q_full[st]), (gs / kStg) & 1, &s_abort, kLimitNs)) {
+          if (!wait_w(bar_addr(c.q_full[st]), (gs / kStg) & 1)) {
             fail(&s_abort);
             ok = false;
             break;
@@ -884,10 +889,10 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = kmajor_off(kk);
-            umma_bf16(tmem, sdesc_add(dsc_k, off), sdesc_add(bq, off), idS, kk > 0);
+            umma_bf16_w(tmem, sdesc_add(dsc_k, off), sdesc_add(bq, off), idS, kk > 0);
           }
-          umma_commit(bar_addr(c.s_full));
-          if (i == it.nb - 1) umma_commit(bar_addr(c.k_free));
+          umma_commit_w(bar_addr(c.s_full));
+          if (i == it.nb - 1) umma_commit_w(bar_addr(c.k_free));
           // dK of the previous step; its ds_full also means the compute warps
           // have read dP^T_{gs-1}, which dP^T_gs overwrites
           if (pend >= 0 && !issue_dk()) {
@@ -895,7 +900,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             ok = false;
             break;
           }
-          if (i == 0 && !mbar_wait(bar_addr(c.v_full), cur & 1, &s_abort, kLimitNs)) {
+          if (i == 0 && !wait_w(bar_addr(c.v_full), cur & 1)) {
             fail(&s_abort);
             ok = false;
             break;
@@ -905,13 +910,13 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = kmajor_off(kk);
-            umma_bf16(tmem + 128, sdesc_add(dsc_v, off), sdesc_add(bd, off), idS, kk > 0);
+            umma_bf16_w(tmem + 128, sdesc_add(dsc_v, off), sdesc_add(bd, off), idS, kk > 0);
           }
-          umma_commit(bar_addr(c.dp_full));
-          if (i == it.nb - 1) umma_commit(bar_addr(c.v_free));
-          if (!mbar_wait(bar_addr(c.p_full), gs & 1, &s_abort, kLimitNs) ||
+          umma_commit_w(bar_addr(c.dp_full));
+          if (i == it.nb - 1) umma_commit_w(bar_addr(c.v_free));
+          if (!wait_w(bar_addr(c.p_full), gs & 1) ||
               (i == 0 && cur > 0 &&
-               !mbar_wait(bar_addr(c.dv_free), (cur - 1) & 1, &s_abort, kLimitNs))) {
+               !wait_w(bar_addr(c.dv_free), (cur - 1) & 1))) {
             fail(&s_abort);
             ok = false;
             break;
@@ -925,8 +930,8 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll (D == 64 ? 8 : 4)  // (the spill-free unrolling of each instantiation)
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t b = sdesc_add(bdm, kk * 2048);
-            umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk), b, idG, (i > 0 || kk > 0) ? 1u : 0u);
-            if (!F16) umma_bf16_ts(tmem + 256 + D, tmem + ts_col(kk) + 32, b, idG, 1u);
+            umma_bf16_ts_w(tmem + 256 + D, tmem + ts_col(kk), b, idG, (i > 0 || kk > 0) ? 1u : 0u);
+            if (!F16) umma_bf16_ts_w(tmem + 256 + D, tmem + ts_col(kk) + 32, b, idG, 1u);
           }
           pend = gs;
           pend_st = st;
@@ -939,9 +944,9 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           break;
         }
         pend = -1;
-        umma_commit(bar_addr(c.done));
+        umma_commit_w(bar_addr(c.done));
       }
-      umma_commit(bar_addr(c.mma_done));
+      umma_commit_w(bar_addr(c.mma_done));
       int never = 0;
       mbar_wait(bar_addr(c.mma_done), 0, &never, kLimitNs);
     }

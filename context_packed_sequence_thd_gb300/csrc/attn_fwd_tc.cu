@@ -31,7 +31,7 @@
 //              With a query index (cp_attn_fwd_gather) the Q tile is read
 //              straight from the unsharded source, every lane gathering four
 //              rows per copy (tile::gather4).
-//   warp 9     TMEM allocator and single-thread MMA issuer:
+//   warp 9     TMEM allocator and MMA issuer (one elected lane per MMA):
 //              S[g%2] = Q K_g^T (M=128, N=128, K=D, both operands K-major in
 //              shared memory) and O[item%2] += P_g V_g (M=128, N=D, K=128; A =
 //              P from TMEM, B = V as an MN-major shared operand).  TMEM: S0
@@ -339,7 +339,13 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop (uniform control flow, warp-uniform
+    // waits); one elected lane issues each MMA and commit.
+    auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool w = mbar_wait(b, parity, &s_abort, a.limit_ns);
+      return __all_sync(0xffffffffu, w);
+    };
+    {
       constexpr uint32_t idS = idesc_bf16_f32(128, TBN, false, false, F16);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true, F16);
       // operand descriptors at the tiles' first bytes, built once (an MMA's
@@ -352,8 +358,8 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       bool pv_first = false;
       auto issue_pv = [&]() -> bool {
         const int vs = pv_g % kVStages;
-        if (!mbar_wait(bar(bars.p_full[pv_g & 1]), (pv_g >> 1) & 1, &s_abort, a.limit_ns) ||
-            !mbar_wait(bar(bars.v_full[vs]), (pv_g / kVStages) & 1, &s_abort, a.limit_ns))
+        if (!wait_w(bar(bars.p_full[pv_g & 1]), (pv_g >> 1) & 1) ||
+            !wait_w(bar(bars.v_full[vs]), (pv_g / kVStages) & 1))
           return false;
         tc_fence_after();
         // A = P from TMEM: keys [0,64) over columns [0,32) and keys [64,128)
@@ -362,10 +368,10 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const uint32_t dO = tmem + o_col<D>(pv_ob), aP = tmem + (pv_g & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < TBN / 16; ++kk)
-          umma_bf16_ts(dO, aP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bv, kk * 2048), idO,
-                       (!pv_first || kk > 0) ? 1u : 0u);
-        umma_commit(bar(bars.v_empty[vs]));
-        umma_commit(bar(bars.o_ready[pv_g & 1]));
+          umma_bf16_ts_w(dO, aP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bv, kk * 2048), idO,
+                         (!pv_first || kk > 0) ? 1u : 0u);
+        umma_commit_w(bar(bars.v_empty[vs]));
+        umma_commit_w(bar(bars.o_ready[pv_g & 1]));
         return true;
       };
       int ii = 0, g = 0;
@@ -377,7 +383,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         it.load(m, k, n_qt, a.H);
         if (it.nb == 0) continue;
         const int qb = ii & 1;
-        if (!mbar_wait(bar(bars.q_full[qb]), (ii >> 1) & 1, &s_abort, a.limit_ns)) {
+        if (!wait_w(bar(bars.q_full[qb]), (ii >> 1) & 1)) {
           fail(&s_abort);
           break;
         }
@@ -385,8 +391,8 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         for (int j = 0; j < it.nb; ++j, ++g) {
           const int ks = g % kKStages, buf = g & 1;
           // S_g overwrites P_{g-2} (same TMEM columns); P V_{g-2} was issued
-          // earlier by this thread and MMAs of one thread run in order
-          if (!mbar_wait(bar(bars.k_full[ks]), (g / kKStages) & 1, &s_abort, a.limit_ns)) {
+          // earlier by this warp and the MMAs of one issuer run in order
+          if (!wait_w(bar(bars.k_full[ks]), (g / kKStages) & 1)) {
             fail(&s_abort);
             ok = false;
             break;
@@ -396,12 +402,12 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            umma_bf16(tmem + buf * 128, sdesc_add(bq, off), sdesc_add(bk, off), idS,
-                      kk > 0 ? 1u : 0u);
+            umma_bf16_w(tmem + buf * 128, sdesc_add(bq, off), sdesc_add(bk, off), idS,
+                        kk > 0 ? 1u : 0u);
           }
-          umma_commit(bar(bars.s_full[buf]));
-          umma_commit(bar(bars.k_empty[ks]));
-          if (j == it.nb - 1) umma_commit(bar(bars.q_free[qb]));
+          umma_commit_w(bar(bars.s_full[buf]));
+          umma_commit_w(bar(bars.k_empty[ks]));
+          if (j == it.nb - 1) umma_commit_w(bar(bars.q_free[qb]));
           if (pv_g >= 0 && !issue_pv()) {
             fail(&s_abort);
             ok = false;
@@ -413,8 +419,8 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
       }
       if (ok && pv_g >= 0 && !issue_pv()) fail(&s_abort);
-      // drain: all MMAs issued by this thread must finish before TMEM is freed
-      umma_commit(bar(bars.mma_done));
+      // drain: all MMAs issued by this warp must finish before TMEM is freed
+      umma_commit_w(bar(bars.mma_done));
       int never = 0;
       mbar_wait(bar(bars.mma_done), 0, &never, a.limit_ns);
     }

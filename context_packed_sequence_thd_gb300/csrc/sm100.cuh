@@ -367,5 +367,25 @@ __device__ __forceinline__ uint32_t elect_one_sync() {
   return pred;
 }
 
+// MMA issue from a warp that runs its issue loop in uniform control flow (all
+// 32 lanes present): one elected lane issues each instruction and the warp
+// reconverges right after.  A lane that has diverged from its warp (an issue
+// loop under `if (lane == 0)`) pays several times as many cycles per
+// tcgen05.mma, enough to leave the tensor core idle between products.
+__device__ __forceinline__ void umma_bf16_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  if (elect_one_sync()) umma_bf16(d_tmem, a_desc, b_desc, idesc, accumulate);
+  __syncwarp();
+}
+__device__ __forceinline__ void umma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  if (elect_one_sync()) umma_bf16_ts(d_tmem, a_tmem, b_desc, idesc, accumulate);
+  __syncwarp();
+}
+__device__ __forceinline__ void umma_commit_w(uint32_t bar) {
+  if (elect_one_sync()) umma_commit(bar);
+  __syncwarp();
+}
+
 }  // namespace sm100
 }  // namespace cpthd
