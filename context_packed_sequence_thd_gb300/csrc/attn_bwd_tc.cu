@@ -852,7 +852,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         tc_fence_after();
         const uint64_t bq = sdesc_add(dsc_qmn, pend_st * L::TILE);
         // dS^T is the sum of two bf16 terms: two products per k-step
-#pragma unroll (D == 64 ? 8 : 4)
+#pragma unroll (D == 128 && !F16 ? 4 : 8)  // (spill-free in the 80-register share)
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t b = sdesc_add(bq, kk * 2048);
           umma_bf16_ts_w(tmem + 256, tmem + 128 + hilo_col(kk), b, idG,
@@ -927,7 +927,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           // P^T is the sum of two bf16 terms (rounded P, then its remainder), so
           // the product carries P to about 16 bits instead of bf16's 8.
           const uint64_t bdm = sdesc_add(dsc_domn, st * L::TILE);
-#pragma unroll (D == 64 ? 8 : 4)  // (the spill-free unrolling of each instantiation)
+#pragma unroll (D == 128 && !F16 ? 4 : 8)  // (spill-free in the 80-register share)
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t b = sdesc_add(bdm, kk * 2048);
             umma_bf16_ts_w(tmem + 256 + D, tmem + ts_col(kk), b, idG, (i > 0 || kk > 0) ? 1u : 0u);

@@ -368,23 +368,34 @@ __device__ __forceinline__ uint32_t elect_one_sync() {
 }
 
 // MMA issue from a warp that runs its issue loop in uniform control flow (all
-// 32 lanes present): one elected lane issues each instruction and the warp
-// reconverges right after.  A lane that has diverged from its warp (an issue
-// loop under `if (lane == 0)`) pays several times as many cycles per
-// tcgen05.mma, enough to leave the tensor core idle between products.
+// 32 lanes present): elect.sync picks one lane and the instruction is
+// predicated on it, so the warp never branches.  A lane that has diverged
+// from its warp (an issue loop under `if (lane == 0)`) pays several times as
+// many cycles per tcgen05.mma, enough to leave the tensor core idle between
+// products; a branch around each issue costs less, the predicate least.
 __device__ __forceinline__ void umma_bf16_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
-  if (elect_one_sync()) umma_bf16(d_tmem, a_desc, b_desc, idesc, accumulate);
-  __syncwarp();
+  asm volatile(
+      "{\n .reg .pred p, e;\n .reg .b32 rx;\n elect.sync rx|e, 0xffffffff;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 __device__ __forceinline__ void umma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                uint32_t idesc, uint32_t accumulate) {
-  if (elect_one_sync()) umma_bf16_ts(d_tmem, a_tmem, b_desc, idesc, accumulate);
-  __syncwarp();
+  asm volatile(
+      "{\n .reg .pred p, e;\n .reg .b32 rx;\n elect.sync rx|e, 0xffffffff;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 __device__ __forceinline__ void umma_commit_w(uint32_t bar) {
-  if (elect_one_sync()) umma_commit(bar);
-  __syncwarp();
+  asm volatile(
+      "{\n .reg .pred e;\n .reg .b32 rx;\n elect.sync rx|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+      : "memory");
 }
 
 }  // namespace sm100
