@@ -55,6 +55,9 @@ _SIGNATURES = {
                         _I, ctypes.c_float, _I, _I, _P, _SZ, _P], _I),
     "cp_attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I,
                              _I, _I, ctypes.c_float, _I, _P], _I),
+    "cp_attn_bwd_grouped_workspace_bytes": ([_I64, _I, _I, _I64], _SZ),
+    "cp_attn_bwd_grouped": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I,
+                             _I, ctypes.c_float, _I, _P, _SZ, _P], _I),
     "cp_p2p_meta_bytes": ([_I, _I64, _I], _SZ),
     "cp_p2p_index": ([_P, _P, _I, _I64, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "cp_p2p_merge": ([_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P], _I),
@@ -344,6 +347,30 @@ def cp_attn_bwd(q_local, k_full, v_full, o_local, lse_local, do_local, dq_local,
         _check("cp_attn_bwd", lib().cp_attn_bwd(*args, *tail))
     else:
         _check("cp_attn_bwd_ex", lib().cp_attn_bwd_ex(*args, int(mode), *tail))
+
+
+def cp_attn_bwd_grouped_workspace_bytes(s_local: int, H: int, cp_size: int,
+                                        total_tokens: int) -> int:
+    return int(lib().cp_attn_bwd_grouped_workspace_bytes(s_local, H, cp_size, total_tokens))
+
+
+def cp_attn_bwd_grouped(q_all, k_full, v_full, o_all, lse_all, do_all, dq_all, dk_accum,
+                        dv_accum, d_meta_all, meta_stride: int, total_tokens: int, cp_size: int,
+                        strategy: int, softmax_scale: float, d_workspace, stream=None,
+                        o_resid_all=None) -> None:
+    """cp_attn_bwd_grouped: every rank's backward, dK/dV summed over the ranks
+    inside one dK/dV launch and stored.  *_all are the ranks' tensors side by
+    side ([cp*s_local, H, D]; lse_all [cp, H, s_local]); d_meta_all holds the
+    ranks' metadata meta_stride bytes apart."""
+    _, H, D = k_full.shape
+    dt = _operand_dtype(q_all, k_full, v_full, do_all)
+    _check("cp_attn_bwd_grouped", lib().cp_attn_bwd_grouped(
+        _dev(q_all, "q"), _dev(k_full, "k"), _dev(v_full, "v"), _dev(o_all, "o"),
+        _opt(o_resid_all, "o_resid"), _dev(lse_all, "lse"), _dev(do_all, "do"),
+        _dev(dq_all, "dq"), _dev(dk_accum, "dk"), _dev(dv_accum, "dv"),
+        _dev(d_meta_all, "meta"), int(meta_stride), total_tokens, H, D, cp_size, strategy,
+        float(softmax_scale), dt, _dev(d_workspace, "workspace"),
+        d_workspace.numel() * d_workspace.element_size(), _stream(stream)))
 
 
 NOALLOC_MAX_SCRATCH_FLOATS = 1048576  # CP_NOALLOC_MAX_SCRATCH_FLOATS in cpthd.h

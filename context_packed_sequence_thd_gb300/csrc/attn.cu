@@ -262,6 +262,76 @@ extern "C" int cp_attn_bwd(const void* q_local, const void* k_full, const void* 
                         workspace_bytes, stream);
 }
 
+extern "C" size_t cp_attn_bwd_grouped_workspace_bytes(int64_t s_local, int H, int cp_size,
+                                                      int64_t total_tokens) {
+  if (s_local < 0 || H < 1 || cp_size < 1 || total_tokens < 0) return 0;
+  const size_t delta = (((size_t)cp_size * s_local * H * sizeof(float)) + 15) & ~(size_t)15;
+  return delta + grouped_scratch_bytes(total_tokens);
+}
+
+extern "C" int cp_attn_bwd_grouped(const void* q_all, const void* k_full, const void* v_full,
+                                   const void* o_all, const void* o_resid_all,
+                                   const float* lse_all, const void* do_all, void* dq_all,
+                                   float* dk_accum, float* dv_accum, const void* d_meta_all,
+                                   size_t meta_stride, int64_t total_tokens, int H, int D,
+                                   int cp_size, cp_strategy_t strategy, float softmax_scale,
+                                   cp_dtype_t operand_dtype, void* d_workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (check_dtype(operand_dtype) != CP_OK) return CP_ERR_INVALID_ARG;
+  int64_t s_local = 0;
+  int st = common_checks(q_all, k_full, v_full, d_meta_all, meta_stride, total_tokens, H, D,
+                         cp_size, 0, strategy, &s_local);
+  if (st != CP_OK) return st;
+  if (meta_stride % 16) return CP_ERR_ALIGNMENT;
+  if (!o_all || !lse_all || !do_all || !dq_all || !dk_accum || !dv_accum)
+    return CP_ERR_INVALID_ARG;
+  if (!cpthd_host::aligned16(o_all) || !cpthd_host::aligned16(lse_all) ||
+      !cpthd_host::aligned16(do_all) || !cpthd_host::aligned16(dq_all) ||
+      !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum) ||
+      !cpthd_host::aligned16(o_resid_all))
+    return CP_ERR_ALIGNMENT;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
+  if (s_local == 0) return CP_OK;
+  if (!d_workspace ||
+      workspace_bytes < cp_attn_bwd_grouped_workspace_bytes(s_local, H, cp_size, total_tokens))
+    return CP_ERR_WORKSPACE;
+  if (!cpthd_host::aligned16(d_workspace)) return CP_ERR_ALIGNMENT;
+  cudaStream_t s = cpthd_host::as_stream(stream);
+  float* delta_all = (float*)d_workspace;
+  void* scratch = (char*)d_workspace +
+                  ((((size_t)cp_size * s_local * H * sizeof(float)) + 15) & ~(size_t)15);
+  const size_t row_bytes = (size_t)H * D * 2;  // one row of a bf16 / fp16 [*, H, D] tensor
+  // per rank: Delta, then dQ (the dK/dV of every rank follows in one launch)
+  for (int r = 0; r < cp_size; ++r) {
+    const size_t ro = (size_t)r * s_local * row_bytes;
+    const void* meta_r = (const char*)d_meta_all + meta_stride * r;
+    AttnArgs a{};
+    a.out = (const bf16*)((const char*)o_all + ro);
+    a.out_resid = o_resid_all ? (const bf16*)((const char*)o_resid_all + ro) : nullptr;
+    a.dout = (const bf16*)((const char*)do_all + ro);
+    a.delta = delta_all + (size_t)r * H * s_local;
+    a.meta = meta_r; a.meta_bytes = meta_stride;
+    a.T = (int)total_tokens; a.H = H; a.s_local = (int)s_local; a.cp = cp_size; a.rank = r;
+    a.strategy = (int)strategy;
+    if ((st = launch_delta(a, D, (int)operand_dtype, s)) != CP_OK) return st;
+  }
+  for (int r = 0; r < cp_size; ++r) {
+    const size_t ro = (size_t)r * s_local * row_bytes;
+    const void* meta_r = (const char*)d_meta_all + meta_stride * r;
+    st = cpthd_attn_bwd_tc((const char*)q_all + ro, k_full, v_full, (const char*)do_all + ro,
+                           lse_all + (size_t)r * H * s_local, delta_all + (size_t)r * H * s_local,
+                           (char*)dq_all + ro, dk_accum, dv_accum, meta_r, meta_stride,
+                           (int)total_tokens, H, D, (int)s_local, cp_size, r, (int)strategy,
+                           softmax_scale, softmax_scale * kLog2e, kBwdDqOnly, (int)operand_dtype,
+                           s);
+    if (st != CP_OK) return st;
+  }
+  return cpthd_attn_dkdv_grouped_tc(q_all, k_full, v_full, do_all, lse_all, delta_all, dk_accum,
+                                    dv_accum, d_meta_all, meta_stride, (int)total_tokens, H, D,
+                                    (int)s_local, cp_size, (int)strategy, softmax_scale,
+                                    softmax_scale * kLog2e, (int)operand_dtype, scratch, s);
+}
+
 extern "C" int cpthd_status_attn(int reset) {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_status_attn, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;

@@ -145,10 +145,12 @@ __device__ __forceinline__ void fail(volatile int* abort) {
 struct Item {
   const int2* list;  // the tile's block list: count in list[0].x, intervals in list[1..]
   int t0, h, nb;
+  // item k: the q-th heaviest tile of head h, heaviest first over all heads
   __device__ void load(const MetaView& m, int k, int n_qt, int H) {
-    const int2 o = m.qorder[k / H];  // the (k / H)-th heaviest tile and its block count
+    int q;
+    item_of(k, n_qt, H, H, &q, &h);
+    const int2 o = m.qorder[min(max(q, 0), n_qt - 1)];  // that tile and its block count
     const int tile = min(max(o.x, 0), n_qt - 1);
-    h = k % H;
     t0 = tile * TBM;
     list = m.qlists + (kListBytes / 8) * tile;
     nb = o.y;

@@ -91,6 +91,22 @@ __host__ __device__ __forceinline__ int snake_item(int j, int c, int G) {
   return j * G + ((j & 1) ? G - 1 - c : c);
 }
 
+// Tile rank q (into a heaviest-first order of n_tiles tiles) and head h of
+// work item k of a launch over n_tiles * H items, heads taken in groups of G:
+// within a group the items are heaviest first across its heads (tile-major),
+// groups one after another.  G = H is the globally heaviest-first order (the
+// best balance); G = 1 keeps the CTAs on one head at a time, so that head's
+// streamed operands stay resident in L2.
+__host__ __device__ __forceinline__ void item_of(int k, int n_tiles, int H, int G, int* q,
+                                                 int* h) {
+  G = max(1, min(G, H));
+  const int group = k / (G * n_tiles);
+  const int hg = min(G, H - group * G);  // heads in this group (the last may have fewer)
+  const int within = k - group * G * n_tiles;
+  *q = within / hg;
+  *h = group * G + within % hg;
+}
+
 struct MetaView {
   const MetaHeader* hdr;
   const Segment* segs;
@@ -291,10 +307,31 @@ int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const voi
                       int skip_first_k = 0);
 
 // tcgen05 dQ and dK/dV kernels (attn_bwd_tc.cu); Delta already in `delta`;
-// mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added);
-// f16: Q/K/V/dO are fp16, else bf16
+// mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added)
+// and, internally, kBwdDqOnly (the dQ kernel alone); f16: Q/K/V/dO are fp16,
+// else bf16
+constexpr int kBwdDqOnly = 8;
 int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
                       const float* lse, const float* delta, void* dq, float* dk, float* dv,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale, float scale_log2,
                       int mode, int f16, cudaStream_t s);
+
+// Scratch of the rank-grouped dK/dV: n_kb int totals, then (16-aligned) the
+// n_kb int2 work order.
+inline __host__ __device__ size_t grouped_order_offset(int64_t T) {
+  return ((size_t)cpthd::n_tiles_of(T) * 4 + 15) & ~(size_t)15;
+}
+inline __host__ __device__ size_t grouped_scratch_bytes(int64_t T) {
+  return grouped_order_offset(T) + (size_t)cpthd::n_tiles_of(T) * 8;
+}
+
+// Rank-grouped dK/dV (attn_bwd_tc.cu): every key block walks the query tiles of
+// all cp ranks and is stored once; operands as the per-rank call, concatenated
+// over the ranks (see the definition).
+int cpthd_attn_dkdv_grouped_tc(const void* q_all, const void* k, const void* v,
+                               const void* dout_all, const float* lse_all,
+                               const float* delta_all, float* dk, float* dv,
+                               const void* meta_all, size_t meta_stride, int T, int H, int D,
+                               int s_local, int cp, int strategy, float scale, float scale_log2,
+                               int f16, void* scratch, cudaStream_t s);

@@ -158,9 +158,12 @@ class CPAttention:
     """Buffers and the full emulated CP forward/backward for one plan."""
 
     def __init__(self, plan: CPPlan, fuse_q_gather: bool = False,
-                 operand_dtype: Optional[torch.dtype] = None):
+                 operand_dtype: Optional[torch.dtype] = None, grouped_bwd: bool = True):
         self.plan = plan
         p = plan
+        # backward of all ranks in one call (cp_attn_bwd_grouped: dK/dV summed
+        # over the ranks inside one dK/dV launch) or rank by rank (cp_attn_bwd)
+        self.grouped_bwd = grouped_bwd
         # forward-only steps under DUAL_CHUNK_SWAP: the attention loads query
         # rows through the partition index (cp_attn_fwd_gather), no Q shard copy
         self.fuse_q_gather = fuse_q_gather
@@ -200,6 +203,8 @@ class CPAttention:
         self.dv_acc = torch.empty(T, H, D, dtype=torch.float32, device=dev)
         ws = api.cp_attn_bwd_workspace_bytes(p.s_local, H)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        wsg = api.cp_attn_bwd_grouped_workspace_bytes(p.s_local, H, p.cp, T) if grouped_bwd else 0
+        self.ws_grouped = torch.empty(max(wsg, 16), dtype=torch.uint8, device=dev)
         self.launches = 0
         # optional per-call CUDA-event timing: category -> [(start, end), ...]
         self.events: Optional[Dict[str, list]] = None
@@ -277,19 +282,29 @@ class CPAttention:
         return k_full, v_full
 
     def backward(self, k_full, v_full, stream=None):
-        """Every rank's backward; rank 0 stores its partial dK/dV into the fp32
-        accumulators (no clearing pass), the others add theirs in rank order:
-        the emulated reduce-scatter's sum."""
+        """Every rank's backward and the emulated reduce-scatter's sum of the
+        partial dK/dV: by default one grouped call whose dK/dV kernel sums the
+        ranks' terms per key block and stores them; rank by rank otherwise
+        (rank 0 stores its partial into the fp32 accumulators, the others add
+        theirs in rank order)."""
         p = self.plan
-        for r in range(p.cp):
+        if self.grouped_bwd:
             with self._timed("attn_bwd", stream):
-                api.cp_attn_bwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
-                                self.lse[r], p.local(self.doc, r), p.local(self.dqc, r),
-                                self.dk_acc, self.dv_acc, p.ranks[r].meta, p.T, p.cp, r,
-                                p.strategy, p.scale, self.ws, stream,
-                                mode=api.BWD_STORE if r == 0 else api.BWD_ACCUMULATE,
-                                o_resid=p.local(self.oc_resid, r))
-            self.launches += 3
+                api.cp_attn_bwd_grouped(self.qc, k_full, v_full, self.oc, self.lse, self.doc,
+                                        self.dqc, self.dk_acc, self.dv_acc, p.meta_all,
+                                        p.meta_stride, p.T, p.cp, p.strategy, p.scale,
+                                        self.ws_grouped, stream, o_resid_all=self.oc_resid)
+            self.launches += 2 * p.cp + 2
+        else:
+            for r in range(p.cp):
+                with self._timed("attn_bwd", stream):
+                    api.cp_attn_bwd(p.local(self.qc, r), k_full, v_full, p.local(self.oc, r),
+                                    self.lse[r], p.local(self.doc, r), p.local(self.dqc, r),
+                                    self.dk_acc, self.dv_acc, p.ranks[r].meta, p.T, p.cp, r,
+                                    p.strategy, p.scale, self.ws, stream,
+                                    mode=api.BWD_STORE if r == 0 else api.BWD_ACCUMULATE,
+                                    o_resid=p.local(self.oc_resid, r))
+                self.launches += 3
         # the scatter half of the reduce-scatter for every rank in one launch:
         # rank r's rows of the rank-concatenated dK/dV are the summed
         # accumulators at its partition index (NO_LOAD_BALANCE: contiguous)

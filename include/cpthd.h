@@ -334,6 +334,37 @@ int cp_attn_bwd_ex(const void* q_local, const void* k_full, const void* v_full,
                    cp_strategy_t strategy, float softmax_scale, cp_dtype_t operand_dtype,
                    cp_bwd_mode_t mode, void* d_workspace, size_t workspace_bytes, void* stream);
 
+/* Scratch cp_attn_bwd_grouped needs: every rank's Delta (fp32 [cp][H][s_local])
+ * and the key blocks' work order (12 bytes per 128-key block). */
+size_t cp_attn_bwd_grouped_workspace_bytes(int64_t s_local, int H, int cp_size,
+                                           int64_t total_tokens);
+
+/* The backward of every rank of an all-gather CP group in one call, with the
+ * emulated reduce-scatter's sum done inside the dK/dV kernel ([AG] §Sequence
+ * Diagram: per-rank partial dK/dV, summed over the group): each 128-key block
+ * walks the attending query tiles of all cp_size ranks and its dK/dV are
+ * stored once.  Operands are the ranks' tensors side by side: q_all, o_all,
+ * o_resid_all (nullable), do_all and dq_all are [cp_size*s_local, H, D] with
+ * rank r's rows at r*s_local (dq_all bf16, overwritten); lse_all is fp32
+ * [cp_size][H][s_local]; d_meta_all holds the ranks' metadata meta_stride
+ * bytes apart (as cp_partition_index_all writes it; meta_stride % 16 == 0).
+ * dk_accum / dv_accum (fp32 [T,H,D], original order) are stored, every
+ * element written (+0.0 where no query attends): the sum cp_attn_bwd_ex gives
+ * with CP_BWD_STORE on rank 0 and CP_BWD_ACCUMULATE on the others, with the
+ * ranks' terms accumulated in the tensor-core products instead of one fp32
+ * addition per rank (a different rounding order; deterministic).  dq_all is
+ * exactly what cp_attn_bwd gives rank by rank.  Launches: cp_size Delta and
+ * cp_size dQ kernels, one ordering kernel and one dK/dV kernel.  Errors as
+ * cp_attn_bwd; rank r's metadata must be rank r's (else CP_ERR_METADATA on
+ * the device status word and dK/dV are not written). */
+int cp_attn_bwd_grouped(const void* q_all, const void* k_full, const void* v_full,
+                        const void* o_all, const void* o_resid_all, const float* lse_all,
+                        const void* do_all, void* dq_all, float* dk_accum, float* dv_accum,
+                        const void* d_meta_all, size_t meta_stride, int64_t total_tokens, int H,
+                        int D, int cp_size, cp_strategy_t strategy, float softmax_scale,
+                        cp_dtype_t operand_dtype, void* d_workspace, size_t workspace_bytes,
+                        void* stream);
+
 /* ---------------------------------------------------------------------------
  * The P2P (ring) comm type, every rank on one GPU ([P2P] §Describe the bug:
  * the P2P context-parallel path, whose per-step sequence metadata comes from

@@ -93,6 +93,12 @@ def test_meta_and_workspace_sizes(lib):
     assert api.cp_meta_bytes(-1, 64, 1) == 0
     assert api.cp_meta_bytes(3, 65, 2) == 0
     assert api.cp_attn_bwd_workspace_bytes(8192, 16) == 8192 * 16 * 4
+    # grouped backward: every rank's Delta, then the key blocks' totals (16-aligned) and order
+    assert api.cp_attn_bwd_grouped_workspace_bytes(8192, 16, 4, 32768) == \
+        4 * 8192 * 16 * 4 + 256 * 4 + 256 * 8
+    assert api.cp_attn_bwd_grouped_workspace_bytes(100, 3, 3, 300) == \
+        (3 * 100 * 3 * 4 + 15) // 16 * 16 + (3 * 4 + 15) // 16 * 16 + 3 * 8
+    assert api.cp_attn_bwd_grouped_workspace_bytes(-1, 3, 3, 300) == 0
 
 
 FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced below
@@ -165,6 +171,13 @@ def test_argument_validation_before_launch(lib):
                             64, 2, 0, 0, f(0.1), 0, 6, FAKE, 1 << 20, None) == -1    # both dQ modes
     assert L.cp_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 128, 2,
                             64, 2, 0, 0, f(0.1), 5, 0, FAKE, 1 << 20, None) == -1    # unknown operand type
+    # grouped backward: stride not a multiple of 16, small workspace, unknown operand type
+    assert L.cp_attn_bwd_grouped(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4104,
+                                 4096, 2, 64, 2, 0, f(0.1), 0, FAKE, 1 << 24, None) == -4
+    assert L.cp_attn_bwd_grouped(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096,
+                                 4096, 2, 64, 2, 0, f(0.1), 0, FAKE, 8, None) == -6
+    assert L.cp_attn_bwd_grouped(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096,
+                                 4096, 2, 64, 2, 0, f(0.1), 3, FAKE, 1 << 24, None) == -1
     # the fp16 gather: index optional, but then the source must cover the rows
     assert L.cp_thd_gather_f16(_arr(FAKE), _arr(FAKE), 1, None, 8, 4, 256, None) == -1
     assert L.cp_thd_gather_f16(_arr(FAKE), _arr(FAKE), 1, None, 0, 4, 250, None) == -4
