@@ -48,9 +48,9 @@ WORKLOAD = ("THD fwd+bwd with inter-sequence padding: 65536 padded tokens, 24 lo
             "padded to multiples of 2*cp, cp_size=4, H=32, D=128, bf16, pad_between_seqs=1, "
             "both strategies")
 
-# DRAM bytes (read + write) per cp_attn_bwd call (attn_delta + attn_dq_tc + attn_dkdv_tc),
-# averaged over the 8 calls of a step (4 ranks x 2 strategies), from the ncu capture named in
-# BWD_TRAFFIC_NOTE; None until a capture of the current kernels exists.
+# DRAM bytes (read + write) per backward call (cp_attn_bwd_grouped: every rank's attn_delta
+# and attn_dq_tc, one attn_dkdv_tc), averaged over the 2 calls of a step (2 strategies), from
+# the ncu capture named in BWD_TRAFFIC_NOTE; None until a capture of the current kernels exists.
 BWD_TRAFFIC_BYTES = None
 BWD_TRAFFIC_NOTE = "no capture of the current backward kernels yet"
 
@@ -205,15 +205,17 @@ def _per_rank(att, steps, cp):
     return out
 
 
-def _workload_line(wl, strategies, dev, reps=5, bwd=True):
-    """Step time and attention TFLOP/s of one workload, every strategy."""
+def _workload_line(wl, strategies, dev, reps=5, bwd=True, grouped_bwd=True):
+    """Step time and attention TFLOP/s of one workload, every strategy
+    (grouped_bwd=False: the rank-by-rank backward, whose per-rank times are
+    then reported too)."""
     import torch
     from context_packed_sequence_thd_gb300 import pipeline
     g = {k: v.to(dev) for k, v in wl.tensors(with_grad=bwd).items()}
     res = {}
     for s in strategies:
         att = pipeline.CPAttention(pipeline.CPPlan(wl.cu, wl.cup, wl.cp, s, wl.pad_between_seqs,
-                                                   wl.H, wl.D, dev))
+                                                   wl.H, wl.D, dev), grouped_bwd=grouped_bwd)
         run = lambda: att.step(g["q"], g["k"], g["v"], g.get("do"))   # noqa: E731
         step_ms = _time_ms(run, reps)
         att.events = {}
@@ -406,6 +408,10 @@ def _secondary(dev, hbm):
     both = (pipeline.DCS, pipeline.NLB)
     return {
         "cfg2_32k_16docs_cp4_h16": _workload_line(inputs.cfg2(), both, dev),
+        # the headline workload with the rank-by-rank backward (cp_attn_bwd per
+        # rank, partial dK/dV added into the fp32 sums): per-rank backward times
+        "headline_workload_rank_by_rank_bwd": _workload_line(inputs.cfg5(), both, dev, reps=3,
+                                                             grouped_bwd=False),
         "cfg4_75600_nlb_cp8_h40": _workload_line(inputs.cfg4(), (pipeline.NLB,), dev, reps=3),
         "cfg3_32k_single_seq_cp8_h40_fwd": _workload_line(inputs.cfg3(), both, dev, reps=3,
                                                           bwd=False),
@@ -496,10 +502,13 @@ def run_own(args):
                 for a, s in zip(atts, strategies)}
     bwd_calls = per.get("attn_bwd", [])
     fwd_calls = per.get("attn_fwd", [])
-    n_rank_calls = len(strategies) * wl.cp
-    # algorithmic FLOP per launch: average over the per-rank calls of a step
-    bwd_flop_per_call = flop_bwd / n_rank_calls
-    fwd_flop_per_call = flop_fwd / n_rank_calls
+    # algorithmic FLOP per call, averaged over a step's calls: the forward is one
+    # cp_attn_fwd per rank and strategy, the backward one cp_attn_bwd_grouped
+    # per strategy (every rank's Delta and dQ launches and one dK/dV launch)
+    n_bwd_calls = max(1, len(bwd_calls) // args.steps)
+    n_fwd_calls = max(1, len(fwd_calls) // args.steps)
+    bwd_flop_per_call = flop_bwd / n_bwd_calls
+    fwd_flop_per_call = flop_fwd / n_fwd_calls
     bwd_ms = statistics.mean(bwd_calls) if bwd_calls else float("nan")
     fwd_ms = statistics.mean(fwd_calls) if fwd_calls else float("nan")
     dominant = "attn_bwd" if sum(bwd_calls) >= sum(fwd_calls) else "attn_fwd"
@@ -558,7 +567,8 @@ def run_own(args):
                        "l2": "inputs larger than L2 (4 x 537 MB bf16 inputs, ~25 GB touched "
                              "per step)"},
             "roofline": {"bound": "tensor", "kernel": dominant,
-                         "kernels": "attn_delta + attn_dq_tc + attn_dkdv_tc"
+                         "kernels": "cp_attn_bwd_grouped: attn_delta + attn_dq_tc per rank, "
+                                    "one rank-grouped attn_dkdv_tc"
                          if dominant == "attn_bwd" else "attn_fwd_tc",
                          "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(ach / peak, 4),
