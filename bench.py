@@ -51,8 +51,10 @@ WORKLOAD = ("THD fwd+bwd with inter-sequence padding: 65536 padded tokens, 24 lo
 # DRAM bytes (read + write) per backward call (cp_attn_bwd_grouped: every rank's attn_delta
 # and attn_dq_tc, one attn_dkdv_tc), averaged over the 2 calls of a step (2 strategies), from
 # the ncu capture named in BWD_TRAFFIC_NOTE; None until a capture of the current kernels exists.
-BWD_TRAFFIC_BYTES = None
-BWD_TRAFFIC_NOTE = "no capture of the current backward kernels yet"
+BWD_TRAFFIC_BYTES = 22286853888
+BWD_TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the kernels of the timed "
+                    "step's two cp_attn_bwd_grouped calls (DCS 25.52 GB, NLB 19.06 GB), full size, "
+                    "one pass; profiles/attn_bwd_dram_cfg5.md")
 
 # a timed region shorter than this, at the maximum SM clock, is a burst: the
 # denominator is the burst peak; otherwise the sustained one
