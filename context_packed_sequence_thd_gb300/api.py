@@ -62,6 +62,9 @@ _SIGNATURES = {
     "cp_p2p_index": ([_P, _P, _I, _I64, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "cp_p2p_merge": ([_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P], _I),
     "cp_device_status": ([ctypes.POINTER(_I), _I], _I),
+    "cp_attn_fwd_ring_workspace_bytes": ([_I64], _SZ),
+    "cp_attn_fwd_ring": ([_P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I64, _I, _I, _I, _I, _I,
+                          ctypes.c_float, _I, _P, _SZ, _P], _I),
 }
 
 EXPORTED = tuple(_SIGNATURES)
@@ -369,6 +372,25 @@ def cp_attn_bwd_grouped(q_all, k_full, v_full, o_all, lse_all, do_all, dq_all, d
         _opt(o_resid_all, "o_resid"), _dev(lse_all, "lse"), _dev(do_all, "do"),
         _dev(dq_all, "dq"), _dev(dk_accum, "dk"), _dev(dv_accum, "dv"),
         _dev(d_meta_all, "meta"), int(meta_stride), total_tokens, H, D, cp_size, strategy,
+        float(softmax_scale), dt, _dev(d_workspace, "workspace"),
+        d_workspace.numel() * d_workspace.element_size(), _stream(stream)))
+
+
+def cp_attn_fwd_ring_workspace_bytes(s_local: int) -> int:
+    return int(lib().cp_attn_fwd_ring_workspace_bytes(s_local))
+
+
+def cp_attn_fwd_ring(q_local, k_shards, v_shards, o_local, lse_local, d_step_meta, step_bytes: int,
+                     n_steps: int, cp_size: int, rank: int, strategy: int, softmax_scale: float,
+                     d_workspace, stream=None, o_resid=None) -> None:
+    """cp_attn_fwd_ring: every ring step of a rank in one pass (no partial outputs,
+    no merge); k_shards / v_shards are the ranks' shards side by side."""
+    s_local, H, D = q_local.shape
+    dt = _operand_dtype(q_local, k_shards, v_shards)
+    _check("cp_attn_fwd_ring", lib().cp_attn_fwd_ring(
+        _dev(q_local, "q"), _dev(k_shards, "k"), _dev(v_shards, "v"), _dev(o_local, "o"),
+        _opt(o_resid, "o_resid"), _dev(lse_local, "lse"), _dev(d_step_meta, "meta"),
+        int(step_bytes), int(n_steps), s_local, H, D, cp_size, rank, strategy,
         float(softmax_scale), dt, _dev(d_workspace, "workspace"),
         d_workspace.numel() * d_workspace.element_size(), _stream(stream)))
 

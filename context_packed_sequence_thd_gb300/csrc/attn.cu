@@ -199,6 +199,44 @@ extern "C" int cpthd_test_attn_fwd_timeout(const void* q_local, const void* k_fu
                            cpthd_host::as_stream(stream), limit_ns, 1);
 }
 
+extern "C" size_t cp_attn_fwd_ring_workspace_bytes(int64_t s_local) {
+  if (s_local < 0) return 0;
+  return ring_scratch_bytes(s_local);
+}
+
+extern "C" int cp_attn_fwd_ring(const void* q_local, const void* k_shards, const void* v_shards,
+                                void* o_local, void* o_resid_local, float* lse_local,
+                                const void* d_step_meta, size_t step_bytes, int n_steps,
+                                int64_t s_local, int H, int D, int cp_size, int rank,
+                                cp_strategy_t strategy, float softmax_scale,
+                                cp_dtype_t operand_dtype, void* d_workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (check_dtype(operand_dtype) != CP_OK) return CP_ERR_INVALID_ARG;
+  if (!q_local || !k_shards || !v_shards || !o_local || !lse_local || !d_step_meta)
+    return CP_ERR_INVALID_ARG;
+  if (H < 1 || cp_size < 1 || rank < 0 || rank >= cp_size || n_steps < 1 || n_steps > cp_size ||
+      s_local < 0 || s_local * cp_size > INT32_MAX)
+    return CP_ERR_INVALID_ARG;
+  if (strategy != CP_DUAL_CHUNK_SWAP && strategy != CP_NO_LOAD_BALANCE) return CP_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return CP_ERR_UNSUPPORTED;
+  if (H > 65535 || (int64_t)s_local * cp_size * H * D > ((int64_t)1 << 40)) return CP_ERR_UNSUPPORTED;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
+  if (step_bytes < 64) return CP_ERR_WORKSPACE;
+  if (step_bytes % 16) return CP_ERR_ALIGNMENT;
+  if (!cpthd_host::aligned16(q_local) || !cpthd_host::aligned16(k_shards) ||
+      !cpthd_host::aligned16(v_shards) || !cpthd_host::aligned16(o_local) ||
+      !cpthd_host::aligned16(o_resid_local) || !cpthd_host::aligned16(lse_local) ||
+      !cpthd_host::aligned16(d_step_meta))
+    return CP_ERR_ALIGNMENT;
+  if (s_local == 0) return CP_OK;
+  if (!d_workspace || workspace_bytes < ring_scratch_bytes(s_local)) return CP_ERR_WORKSPACE;
+  if (!cpthd_host::aligned16(d_workspace)) return CP_ERR_ALIGNMENT;
+  return cpthd_attn_fwd_ring_tc(q_local, k_shards, v_shards, o_local, o_resid_local, lse_local,
+                                d_step_meta, step_bytes, n_steps, H, D, (int)s_local, cp_size,
+                                rank, (int)strategy, softmax_scale * kLog2e, (int)operand_dtype,
+                                d_workspace, cpthd_host::as_stream(stream));
+}
+
 extern "C" size_t cp_attn_bwd_workspace_bytes(int64_t s_local, int H) {
   if (s_local < 0 || H < 1) return 0;
   return (size_t)s_local * H * sizeof(float);

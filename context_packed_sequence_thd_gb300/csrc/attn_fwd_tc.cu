@@ -96,7 +96,22 @@ struct TcArgs {
   float scale_log2;
   uint64_t limit_ns;  // bound of every mbarrier wait
   int skip_first_k;   // failure-detection test only: CTA 0 never loads its first K tile
+  // ring mode (n_steps > 1): every ring step of rank ring_rank in one pass.
+  // meta is step 0's metadata (cp_size = 1, as cp_p2p_index writes it) and
+  // step i's lies step_stride bytes further per step; step i's keys are the
+  // shard of rank (ring_rank - i) mod ring_cp, rows shard_rows * that rank of
+  // the K / V tensors (kv_rows rows in all); rorder holds the rank's query
+  // tiles heaviest first by their block count summed over the steps.
+  int n_steps;
+  int64_t step_stride;
+  int ring_rank, ring_cp, shard_rows, kv_rows;
+  const int2* rorder;
 };
+
+// Metadata of ring step i (step 0 outside ring mode).
+__device__ __forceinline__ const void* step_meta(const TcArgs& a, int i) {
+  return reinterpret_cast<const char*>(a.meta) + a.step_stride * i;
+}
 
 struct Bars {
   uint64_t q_full[2];
@@ -130,10 +145,63 @@ struct Ctl {
 };
 
 __device__ __forceinline__ bool meta_ok_tc(const TcArgs& a, const MetaHeader* h) {
-  const bool ok = meta_matches(h, a.meta_bytes, a.T, a.s_local, a.cp, a.rank, a.strategy);
-  if (!ok && threadIdx.x == 0)
-    atomicCAS(&g_status_fwd_tc, 0, h->status != 0 ? h->status : (int)CP_ERR_METADATA);
+  bool ok = true;
+  int bad = 0;
+  for (int i = 0; i < a.n_steps && ok; ++i) {  // every ring step's metadata in ring mode
+    const MetaHeader* hi = i == 0 ? h : reinterpret_cast<const MetaHeader*>(step_meta(a, i));
+    ok = meta_matches(hi, a.meta_bytes, a.T, a.s_local, a.cp, a.rank, a.strategy);
+    if (!ok) bad = hi->status != 0 ? hi->status : (int)CP_ERR_METADATA;
+  }
+  if (!ok && threadIdx.x == 0) atomicCAS(&g_status_fwd_tc, 0, bad);
   return ok;
+}
+
+// Ring mode: the rank's query tiles heaviest first by their block count summed
+// over the ring steps (each step's tile list header), ranked by comparison
+// against every tile (stable for equal counts).  One block; tot holds n_qt
+// ints of scratch.  Metadata that does not match leaves the identity order
+// with zero counts (the attention kernel then writes nothing).
+constexpr int kOrdThreads = 1024, kOrdChunk = 4096;
+__global__ void __launch_bounds__(kOrdThreads, 1)
+ring_order_kernel(const TcArgs a, int* tot, int2* order) {
+  __shared__ int s_t[kOrdChunk];
+  __shared__ int s_ok;
+  const int n = (int)n_tiles_of(a.s_local);
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    for (int i = 0; i < a.n_steps && ok; ++i)
+      ok = meta_matches(reinterpret_cast<const MetaHeader*>(step_meta(a, i)), a.meta_bytes, a.T,
+                        a.s_local, a.cp, a.rank, a.strategy) ? 1 : 0;
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (!s_ok) {
+    for (int q = threadIdx.x; q < n; q += blockDim.x) order[q] = make_int2(q, 0);
+    return;
+  }
+  for (int q = threadIdx.x; q < n; q += blockDim.x) {
+    int t = 0;
+    for (int i = 0; i < a.n_steps; ++i) t += meta_view(step_meta(a, i)).qlists[(kListBytes / 8) * q].y;
+    tot[q] = t;
+  }
+  __syncthreads();
+  for (int q0 = 0; q0 < n; q0 += blockDim.x) {
+    const int q = q0 + threadIdx.x;
+    const int mine = q < n ? tot[q] : 0;
+    int rank = 0;
+    for (int c0 = 0; c0 < n; c0 += kOrdChunk) {
+      const int cn = min(kOrdChunk, n - c0);
+      __syncthreads();
+      for (int i = threadIdx.x; i < cn; i += blockDim.x) s_t[i] = tot[c0 + i];
+      __syncthreads();
+      if (q < n)
+        for (int i = 0; i < cn; ++i) {
+          const int o = s_t[i];
+          rank += (o > mine || (o == mine && c0 + i < q)) ? 1 : 0;
+        }
+    }
+    if (q < n) order[rank] = make_int2(q, mine);
+  }
 }
 
 __device__ __forceinline__ void fail(volatile int* abort) {
@@ -141,21 +209,19 @@ __device__ __forceinline__ void fail(volatile int* abort) {
   atomicCAS(&g_status_fwd_tc, 0, (int)CP_ERR_TIMEOUT);
 }
 
-// One work item: its tile, head and the key blocks of the tile's block list.
+// One work item: its tile, head and number of key blocks (ring mode: summed
+// over the ring steps).
 struct Item {
-  const int2* list;  // the tile's block list: count in list[0].x, intervals in list[1..]
-  int t0, h, nb;
+  int tile, t0, h, nb;
   // item k: the q-th heaviest tile of head h, heaviest first over all heads
-  __device__ void load(const MetaView& m, int k, int n_qt, int H) {
+  __device__ void load(const TcArgs& a, const MetaView& m, int k, int n_qt) {
     int q;
-    item_of(k, n_qt, H, H, &q, &h);
-    const int2 o = m.qorder[min(max(q, 0), n_qt - 1)];  // that tile and its block count
-    const int tile = min(max(o.x, 0), n_qt - 1);
+    item_of(k, n_qt, a.H, a.H, &q, &h);
+    const int2 o = (a.n_steps > 1 ? a.rorder : m.qorder)[min(max(q, 0), n_qt - 1)];
+    tile = min(max(o.x, 0), n_qt - 1);
     t0 = tile * TBM;
-    list = m.qlists + (kListBytes / 8) * tile;
     nb = o.y;
   }
-  __device__ int n_iv() const { return min(list[0].x, kListCap); }
 };
 
 struct Iter {  // flattened walk over an item's key-block intervals
@@ -169,6 +235,42 @@ struct Iter {  // flattened walk over an item's key-block intervals
       ++i;
       if (i < n) b = iv[i].x;
     }
+  }
+};
+
+// The key blocks of a work item in order: the tile's block list, or in ring
+// mode the lists of the rank's ring steps one after another (the steps with
+// blocks), each step's blocks in its shard.  Producer and softmax warps walk
+// the same sequence; b is a block of the current step's shard, kv_off the
+// shard's first row in the K / V tensors.
+struct Walk {
+  const TcArgs* a;
+  Iter bi;
+  int tile, step, left, kv_off;
+  __device__ void init(const TcArgs& args, int t) {
+    a = &args;
+    tile = t;
+    step = -1;
+    left = 0;
+    kv_off = 0;
+    advance();
+  }
+  __device__ void advance() {
+    while (left == 0 && step + 1 < a->n_steps) {
+      ++step;
+      const int2* list = meta_view(step_meta(*a, step)).qlists + (kListBytes / 8) * tile;
+      left = list[0].y;
+      bi.init(list + 1, min(list[0].x, kListCap));
+      kv_off = a->n_steps > 1
+                   ? ((a->ring_rank - step + a->ring_cp) % a->ring_cp) * a->shard_rows
+                   : 0;
+    }
+  }
+  __device__ int b() const { return bi.b; }
+  __device__ void next() {
+    --left;
+    bi.next();
+    if (left == 0) advance();
   }
 };
 
@@ -261,7 +363,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       const int k = snake_item(j, blockIdx.x, gridDim.x);
       if (k >= n_items) continue;
       Item it;
-      it.load(m, k, n_qt, a.H);
+      it.load(a, m, k, n_qt);
       if (it.nb == 0) continue;
       const int qb = ii & 1;
       if (!wait0(bars.q_free[qb], ((ii >> 1) & 1) ^ 1)) {
@@ -298,16 +400,16 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                       b * 64, it.h, it.t0);
       }
       ++ii;
-      Iter bi;
-      bi.init(it.list + 1, it.n_iv());
-      for (int j = 0; j < it.nb; ++j, bi.next()) {
+      Walk w;
+      w.init(a, it.tile);
+      for (int j = 0; j < it.nb; ++j, w.next()) {
         const int ks = g % kKStages;
         if (!wait0(bars.k_empty[ks], ((g / kKStages) & 1) ^ 1)) {
           if (lane == 0) fail(&s_abort);
           ok = false;
           break;
         }
-        const int key0 = bi.b * TBN;
+        const int key0 = w.kv_off + w.b() * TBN;  // the block's first row in K / V
         // (the failure-detection test leaves CTA 0's first K tile unloaded: the
         // MMA thread's bounded wait for it runs out and the CTA drains)
         if (lane == 0 && !(a.skip_first_k && blockIdx.x == 0 && g == 0)) {
@@ -382,7 +484,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int k = snake_item(j, blockIdx.x, gridDim.x);
         if (k >= n_items) continue;
         Item it;
-        it.load(m, k, n_qt, a.H);
+        it.load(a, m, k, n_qt);
         if (it.nb == 0) continue;
         const int qb = ii & 1;
         if (!wait_w(bar(bars.q_full[qb]), (ii >> 1) & 1)) {
@@ -460,7 +562,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int k = snake_item(j, blockIdx.x, gridDim.x);
         if (k >= n_items) continue;
         Item nx;
-        nx.load(m, k, n_qt, a.H);
+        nx.load(a, m, k, n_qt);
         if (nx.nb > 0) return k;
       }
       return n_items;
@@ -523,7 +625,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     int lo_pre = 0, hi_pre = -1;
     if (k_pre < n_items) {
       Item f;
-      f.load(m, k_pre, n_qt, a.H);
+      f.load(a, m, k_pre, n_qt);
       const int t = f.t0 + row;
       lo_pre = t < a.s_local ? m.row_lo[t] : 0;
       hi_pre = t < a.s_local ? m.row_hi[t] : -1;
@@ -532,7 +634,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       const int k = snake_item(j, blockIdx.x, gridDim.x);
       if (k >= n_items) continue;
       Item itm;
-      itm.load(m, k, n_qt, a.H);
+      itm.load(a, m, k, n_qt);
       const int t = itm.t0 + row;
       if (itm.nb == 0) {  // no real query row in this tile: O = 0, LSE = -inf
         if (t < a.s_local) {
@@ -549,11 +651,11 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         continue;
       }
-      const int lo = lo_pre, hi = hi_pre;  // k == k_pre here
+      int lo = lo_pre, hi = hi_pre;  // step 0's key range of the row (k == k_pre here)
       k_pre = next_item(j);
       if (k_pre < n_items) {
         Item f;
-        f.load(m, k_pre, n_qt, a.H);
+        f.load(a, m, k_pre, n_qt);
         const int tn = f.t0 + row;
         lo_pre = tn < a.s_local ? m.row_lo[tn] : 0;
         hi_pre = tn < a.s_local ? m.row_hi[tn] : -1;
@@ -561,10 +663,17 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       const int ob = ii & 1;
       ++ii;
       float m_run = -INFINITY, l_run = 0.f;
-      Iter bi;
-      bi.init(itm.list + 1, itm.n_iv());
-      for (int j = 0; j < itm.nb; ++j, bi.next(), ++g) {
+      Walk w;
+      w.init(a, itm.tile);
+      int cur_step = 0;  // the ring step whose key range lo / hi hold
+      for (int j = 0; j < itm.nb; ++j, w.next(), ++g) {
         const int buf = g & 1;
+        if (w.step != cur_step) {  // ring mode: the row's key range in the next step's shard
+          const MetaView ms = meta_view(step_meta(a, w.step));
+          lo = t < a.s_local ? ms.row_lo[t] : 0;
+          hi = t < a.s_local ? ms.row_hi[t] : -1;
+          cur_step = w.step;
+        }
         if (!wait_warp(bar(bars.s_full[buf]), (g >> 1) & 1)) {
           fail(&s_abort);
           ok = false;
@@ -576,7 +685,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tmem_ld32(tmem + lane_base + buf * 128 + 64 * hf + 32,
                   reinterpret_cast<uint32_t*>(s + 32));
 
-        const int k0 = bi.b * TBN + 64 * hf;  // key of this thread's first column
+        const int k0 = w.b() * TBN + 64 * hf;  // key (of the step's shard) of this thread's first column
         if (!(lo <= k0 && hi >= k0 + 63)) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
@@ -710,8 +819,8 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, const TcArgs& a, 
   st = a.q_idx ? tma::make_row_gather_map(&mq, q, a.q_rows, a.H, D, F16)
                : tma::make_thd_map(&mq, q, a.s_local, a.H, D, 128, F16);
   if (st != CP_OK) return st;
-  if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128, F16)) != CP_OK) return st;
-  if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128, F16)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mk, k, a.kv_rows, a.H, D, 128, F16)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mv, v, a.kv_rows, a.H, D, 128, F16)) != CP_OK) return st;
   const int smem = Layout<D>::BYTES + (int)sizeof(Ctl);
   if (cudaFuncSetAttribute(attn_fwd_tc<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
@@ -745,8 +854,49 @@ int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const voi
   a.scale_log2 = scale_log2;
   a.limit_ns = limit_ns ? limit_ns : kWaitLimitNs;
   a.skip_first_k = skip_first_k;
+  a.n_steps = 1;
+  a.kv_rows = T;
   if (f16) return D == 64 ? launch_fwd_tc<64, true>(q, k, v, a, s) : launch_fwd_tc<128, true>(q, k, v, a, s);
   return D == 64 ? launch_fwd_tc<64, false>(q, k, v, a, s) : launch_fwd_tc<128, false>(q, k, v, a, s);
+}
+
+// Internal entry of the ring forward in one pass (arguments validated): rank
+// `rank`'s n_steps ring steps, step i attending q_local to the shard of rank
+// (rank - i) mod cp (rows s_local * that rank of k_shards / v_shards, the
+// ranks' shards side by side), with one online softmax over all of them;
+// step_meta holds the steps' cp_size = 1 metadata step_bytes apart; scratch
+// holds n_qt ints then (16-aligned) n_qt int2 of the work order.
+int cpthd_attn_fwd_ring_tc(const void* q, const void* k_shards, const void* v_shards, void* o,
+                           void* o_resid, float* lse, const void* step_meta, size_t step_bytes,
+                           int n_steps, int H, int D, int s_local, int cp, int rank, int strategy,
+                           float scale_log2, int f16, void* scratch, cudaStream_t s) {
+  using namespace cpthd;
+  TcArgs a{};
+  a.o = (bf16*)o;
+  a.o_resid = (bf16*)o_resid;
+  a.lse = lse;
+  a.meta = step_meta;
+  a.meta_bytes = step_bytes;
+  a.T = s_local; a.H = H; a.s_local = s_local; a.cp = 1; a.rank = 0; a.strategy = strategy;
+  a.scale_log2 = scale_log2;
+  a.limit_ns = kWaitLimitNs;
+  a.n_steps = n_steps;
+  a.step_stride = (int64_t)step_bytes;
+  a.ring_rank = rank;
+  a.ring_cp = cp;
+  a.shard_rows = s_local;
+  a.kv_rows = s_local * cp;
+  const int n_qt = (int)n_tiles_of(s_local);
+  int* tot = reinterpret_cast<int*>(scratch);
+  int2* order = reinterpret_cast<int2*>(reinterpret_cast<char*>(scratch) + ring_order_offset(s_local));
+  a.rorder = order;
+  ring_order_kernel<<<1, kOrdThreads, 0, s>>>(a, tot, order);
+  int st = cpthd_host::launch_status();
+  if (st != CP_OK || n_qt == 0) return st;
+  if (f16) return D == 64 ? launch_fwd_tc<64, true>(q, k_shards, v_shards, a, s)
+                          : launch_fwd_tc<128, true>(q, k_shards, v_shards, a, s);
+  return D == 64 ? launch_fwd_tc<64, false>(q, k_shards, v_shards, a, s)
+                 : launch_fwd_tc<128, false>(q, k_shards, v_shards, a, s);
 }
 
 extern "C" int cpthd_status_fwd_tc(int reset) {

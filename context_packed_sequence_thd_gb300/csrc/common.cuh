@@ -306,6 +306,19 @@ int cpthd_attn_fwd_tc(const void* q, const int32_t* q_idx, int q_rows, const voi
                       float scale_log2, int f16, cudaStream_t s, uint64_t limit_ns = 0,
                       int skip_first_k = 0);
 
+// The ring forward in one pass (attn_fwd_tc.cu): every ring step of a rank,
+// one online softmax over the steps' shards; scratch: ring_scratch_bytes.
+inline __host__ __device__ size_t ring_order_offset(int64_t s_local) {
+  return ((size_t)cpthd::n_tiles_of(s_local) * 4 + 15) & ~(size_t)15;
+}
+inline __host__ __device__ size_t ring_scratch_bytes(int64_t s_local) {
+  return ring_order_offset(s_local) + (size_t)cpthd::n_tiles_of(s_local) * 8;
+}
+int cpthd_attn_fwd_ring_tc(const void* q, const void* k_shards, const void* v_shards, void* o,
+                           void* o_resid, float* lse, const void* step_meta, size_t step_bytes,
+                           int n_steps, int H, int D, int s_local, int cp, int rank, int strategy,
+                           float scale_log2, int f16, void* scratch, cudaStream_t s);
+
 // tcgen05 dQ and dK/dV kernels (attn_bwd_tc.cu); Delta already in `delta`;
 // mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added)
 // and, internally, kBwdDqOnly (the dQ kernel alone); f16: Q/K/V/dO are fp16,

@@ -461,7 +461,10 @@ class CPP2PAttention(CPAttention):
     get_cu_seqlens_on_cp_rank helper calls).  Under NO_LOAD_BALANCE the shards
     of later ranks hold only later tokens, so rank r runs steps 0..r only.
 
-    Forward: per-step partial (O_i, LSE_i), combined by cp_p2p_merge.
+    Forward: by default one cp_attn_fwd_ring pass per rank, which walks the
+    held shards in ring order within one online softmax (the merge is its
+    rescaling, so no partial outputs are written); fused_ring=False runs the
+    per-step partials (O_i, LSE_i) and combines them with cp_p2p_merge.
     Backward: per step with the merged O / LSE; dQ is summed over the rank's
     steps in an fp32 buffer (first step stores, later steps add), dK/dV of
     shard j are summed in fp32 over the ranks that attended it (the partial
@@ -469,11 +472,15 @@ class CPP2PAttention(CPAttention):
     contribution to each shard stored; one launch casts all three to bf16.
     """
 
-    def __init__(self, plan: CPPlan, operand_dtype: Optional[torch.dtype] = None):
+    def __init__(self, plan: CPPlan, operand_dtype: Optional[torch.dtype] = None,
+                 fused_ring: bool = True):
         super().__init__(plan, operand_dtype=operand_dtype)
         p = plan
         dev, T, H, D, S = p.device, p.T, p.H, p.D, p.s_local
         self.k_full = self.v_full = None   # no restore: attention reads the shards
+        self.fused_ring = fused_ring
+        self.ws_ring = torch.empty(max(api.cp_attn_fwd_ring_workspace_bytes(S), 16),
+                                   dtype=torch.uint8, device=dev)
         self.step_bytes = api.cp_p2p_meta_bytes(p.n_docs, T, p.cp)
         self.p2p_meta = [torch.empty(p.cp * self.step_bytes, dtype=torch.uint8, device=dev)
                          for _ in range(p.cp)]
@@ -502,6 +509,14 @@ class CPP2PAttention(CPAttention):
         S = p.s_local
         for r in range(p.cp):
             n = self.n_steps(r)
+            if self.fused_ring:
+                with self._timed("attn_fwd", stream):
+                    api.cp_attn_fwd_ring(p.local(self.qc, r), self.kc, self.vc, p.local(self.oc, r),
+                                         self.lse[r], self.p2p_meta[r], self.step_bytes, n, p.cp, r,
+                                         p.strategy, p.scale, self.ws_ring, stream,
+                                         o_resid=p.local(self.oc_resid, r))
+                self.launches += 2
+                continue
             for i in range(n):
                 j = (r - i) % p.cp
                 with self._timed("attn_fwd", stream):

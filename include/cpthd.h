@@ -415,6 +415,34 @@ int cp_p2p_merge(const void* d_o_steps, const void* d_o_steps_resid, const float
                  int n_steps, int64_t s_local, int H, int D, void* d_out, void* d_out_resid,
                  float* d_lse, void* stream);
 
+/* Scratch cp_attn_fwd_ring needs: its work order, 12 bytes per 128-row query
+ * tile (16-aligned halves). */
+size_t cp_attn_fwd_ring_workspace_bytes(int64_t s_local);
+
+/* Every ring step of rank `rank` in one pass: the result of cp_attn_fwd on
+ * each of the n_steps steps followed by cp_p2p_merge, without the partial
+ * outputs.  Step i attends q_local to the K/V shard of rank
+ * j = (rank - i) mod cp_size, rows [j*s_local, (j+1)*s_local) of k_shards /
+ * v_shards ([cp_size*s_local, H, D] of operand_dtype, the ranks' shards side by
+ * side); the kernel walks the steps' key blocks in ring order within one
+ * online softmax per row, whose rescaling is the merge.  d_step_meta: the
+ * rank's step metadata, step_bytes apart, as cp_p2p_index writes it
+ * (step_bytes = cp_p2p_meta_bytes, % 16 == 0); n_steps in [1, cp_size] (the
+ * ring's steps of the rank: every step for DUAL_CHUNK_SWAP, steps 0..rank for
+ * NO_LOAD_BALANCE).  Outputs as cp_attn_fwd: o_local [s_local,H,D] bf16,
+ * o_resid_local (nullable) its rounding remainder, lse_local fp32 [H,s_local].
+ * The result equals the per-step path up to the rounding order (one fp32
+ * online softmax instead of bf16 partials combined in fp32).  Launches: one
+ * ordering kernel (the rank's query tiles heaviest first by their block count
+ * over the steps) and one attention kernel.  Errors as cp_attn_fwd; every
+ * step's header is checked on the device (CP_ERR_METADATA, nothing written). */
+int cp_attn_fwd_ring(const void* q_local, const void* k_shards, const void* v_shards,
+                     void* o_local, void* o_resid_local, float* lse_local,
+                     const void* d_step_meta, size_t step_bytes, int n_steps, int64_t s_local,
+                     int H, int D, int cp_size, int rank, cp_strategy_t strategy,
+                     float softmax_scale, cp_dtype_t operand_dtype, void* d_workspace,
+                     size_t workspace_bytes, void* stream);
+
 /* Largest Delta scratch cp_attn_bwd_noalloc can use: s_local*H <= this many
  * floats (4 MiB of device memory per GPU that loads the library). */
 #define CP_NOALLOC_MAX_SCRATCH_FLOATS 1048576

@@ -110,11 +110,14 @@ P2P_CASES = {
 }
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["one_pass", "per_step"])
 @pytest.mark.parametrize("strategy", [pipeline.DCS, pipeline.NLB], ids=["dcs", "nlb"])
 @pytest.mark.parametrize("name", list(P2P_CASES))
-def test_p2p_attention_matches_oracle(name, strategy):
+def test_p2p_attention_matches_oracle(name, strategy, fused):
     """Every rank's O, LSE, dQ, dK, dV after the emulated ring equal the fp64
-    oracle's causal attention at the rank's rows."""
+    oracle's causal attention at the rank's rows, with the forward as one pass
+    per rank over its ring steps (cp_attn_fwd_ring) or step by step with the
+    merge (cp_attn_fwd + cp_p2p_merge)."""
     d = dev()
     wl = P2P_CASES[name]()
     if strategy not in wl.strategies:
@@ -124,7 +127,7 @@ def test_p2p_attention_matches_oracle(name, strategy):
     o, lse = oracle.attn_fwd(t["q"], t["k"], t["v"], wl.cu, wl.cup, pad)
     dq, dk, dv = oracle.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], wl.cu, wl.cup, pad)
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, pad, wl.H, wl.D, d)
-    att = pipeline.CPP2PAttention(plan)
+    att = pipeline.CPP2PAttention(plan, fused_ring=fused)
     g = {k: v.to(d) for k, v in t.items()}
     att.step(g["q"], g["k"], g["v"], g["do"])
     torch.cuda.synchronize()
@@ -153,3 +156,48 @@ def test_p2p_step_is_deterministic():
         outs.append([x.clone() for x in (att.oc, att.dqc, att.dkc, att.dvc)])
     for a, b in zip(*outs):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("strategy", [pipeline.DCS, pipeline.NLB], ids=["dcs", "nlb"])
+def test_ring_one_pass_matches_per_step(strategy):
+    """The one-pass ring forward against the per-step partials + merge on the
+    same inputs: O within one bf16 rounding of each other, LSE within 1e-4
+    (one fp32 online softmax against bf16 partials combined in fp32)."""
+    d = dev()
+    wl = inputs.custom([304, 216, 504, 96, 400], cp=4, H=3, D=128, seed=75)  # lse rows 16-byte aligned
+    g = {k: v.to(d) for k, v in wl.tensors().items()}
+    res = []
+    for fused in (True, False):
+        plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, d)
+        att = pipeline.CPP2PAttention(plan, fused_ring=fused)
+        att.step(g["q"], g["k"], g["v"])
+        torch.cuda.synchronize()
+        assert api.cp_device_status() == 0
+        res.append((att.oc.float().clone(), att.lse.clone()))
+    (o1, l1), (o2, l2) = res
+    assert torch.equal(torch.isneginf(l1), torch.isneginf(l2))
+    fin = ~torch.isneginf(l1)
+    assert (l1[fin] - l2[fin]).abs().max().item() <= 1e-4
+    assert (o1 - o2).abs().max().item() <= 2.0 ** -7 * max(1.0, o2.abs().max().item())
+
+
+def test_ring_one_pass_refuses_other_metadata():
+    """Every step's header is checked on the device: the other strategy's step
+    metadata writes nothing and reports CP_ERR_METADATA."""
+    d = dev()
+    wl = inputs.custom([304, 216, 504], cp=4, H=2, D=64, seed=76)
+    g = {k: v.to(d) for k, v in wl.tensors().items()}
+    plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, pipeline.DCS, 0, wl.H, wl.D, d)
+    att = pipeline.CPP2PAttention(plan)
+    att.step(g["q"], g["k"], g["v"])
+    other = pipeline.CPP2PAttention(pipeline.CPPlan(wl.cu, wl.cup, wl.cp, pipeline.NLB, 0,
+                                                    wl.H, wl.D, d))
+    torch.cuda.synchronize()
+    sentinel = 3.0
+    o = torch.full_like(plan.local(att.oc, 1), sentinel)
+    lse = torch.full_like(att.lse[1], sentinel)
+    api.cp_attn_fwd_ring(plan.local(att.qc, 1), att.kc, att.vc, o, lse, other.p2p_meta[1],
+                         other.step_bytes, 2, plan.cp, 1, pipeline.DCS, plan.scale, att.ws_ring)
+    torch.cuda.synchronize()
+    assert api.cp_device_status(reset=True) == -7  # CP_ERR_METADATA
+    assert torch.all(o == sentinel) and torch.all(lse == sentinel)
