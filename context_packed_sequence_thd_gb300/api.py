@@ -63,6 +63,9 @@ _SIGNATURES = {
     "cp_p2p_merge": ([_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P], _I),
     "cp_device_status": ([ctypes.POINTER(_I), _I], _I),
     "cp_attn_fwd_ring_workspace_bytes": ([_I64], _SZ),
+    "cp_attn_bwd_ring_workspace_bytes": ([_I64, _I, _I], _SZ),
+    "cp_attn_bwd_ring": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _SZ, _I64, _I, _I, _I,
+                          _I, ctypes.c_float, _I, _P, _SZ, _P], _I),
     "cp_attn_fwd_ring": ([_P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I64, _I, _I, _I, _I, _I,
                           ctypes.c_float, _I, _P, _SZ, _P], _I),
 }
@@ -393,6 +396,28 @@ def cp_attn_fwd_ring(q_local, k_shards, v_shards, o_local, lse_local, d_step_met
         int(step_bytes), int(n_steps), s_local, H, D, cp_size, rank, strategy,
         float(softmax_scale), dt, _dev(d_workspace, "workspace"),
         d_workspace.numel() * d_workspace.element_size(), _stream(stream)))
+
+
+def cp_attn_bwd_ring_workspace_bytes(s_local: int, H: int, cp_size: int) -> int:
+    return int(lib().cp_attn_bwd_ring_workspace_bytes(s_local, H, cp_size))
+
+
+def cp_attn_bwd_ring(q_all, k_shards, v_shards, o_all, lse_all, do_all, dq_all, dk_accum,
+                     dv_accum, d_ring_meta, step_bytes: int, rank_stride: int, cp_size: int,
+                     strategy: int, softmax_scale: float, d_workspace, stream=None,
+                     o_resid_all=None) -> None:
+    """cp_attn_bwd_ring: the ring backward of every rank in one pass per gradient
+    (dq_all bf16, dk_accum / dv_accum fp32 rank-concatenated, all stored)."""
+    rows, H, D = q_all.shape
+    s_local = rows // cp_size
+    dt = _operand_dtype(q_all, k_shards, v_shards, do_all)
+    _check("cp_attn_bwd_ring", lib().cp_attn_bwd_ring(
+        _dev(q_all, "q"), _dev(k_shards, "k"), _dev(v_shards, "v"), _dev(o_all, "o"),
+        _opt(o_resid_all, "o_resid"), _dev(lse_all, "lse"), _dev(do_all, "do"),
+        _dev(dq_all, "dq"), _dev(dk_accum, "dk"), _dev(dv_accum, "dv"), _dev(d_ring_meta, "meta"),
+        int(step_bytes), int(rank_stride), s_local, H, D, cp_size, strategy, float(softmax_scale),
+        dt, _dev(d_workspace, "workspace"), d_workspace.numel() * d_workspace.element_size(),
+        _stream(stream)))
 
 
 NOALLOC_MAX_SCRATCH_FLOATS = 1048576  # CP_NOALLOC_MAX_SCRATCH_FLOATS in cpthd.h

@@ -370,6 +370,68 @@ extern "C" int cp_attn_bwd_grouped(const void* q_all, const void* k_full, const 
                                     softmax_scale * kLog2e, (int)operand_dtype, scratch, s);
 }
 
+extern "C" size_t cp_attn_bwd_ring_workspace_bytes(int64_t s_local, int H, int cp_size) {
+  if (s_local < 0 || H < 1 || cp_size < 1) return 0;
+  const size_t delta = (((size_t)cp_size * s_local * H * sizeof(float)) + 15) & ~(size_t)15;
+  return delta + ring_bwd_scratch_bytes(s_local, cp_size);
+}
+
+extern "C" int cp_attn_bwd_ring(const void* q_all, const void* k_shards, const void* v_shards,
+                                const void* o_all, const void* o_resid_all, const float* lse_all,
+                                const void* do_all, void* dq_all, float* dk_accum, float* dv_accum,
+                                const void* d_ring_meta, size_t step_bytes, size_t rank_stride,
+                                int64_t s_local, int H, int D, int cp_size,
+                                cp_strategy_t strategy, float softmax_scale,
+                                cp_dtype_t operand_dtype, void* d_workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (check_dtype(operand_dtype) != CP_OK) return CP_ERR_INVALID_ARG;
+  if (!q_all || !k_shards || !v_shards || !o_all || !lse_all || !do_all || !dq_all ||
+      !dk_accum || !dv_accum || !d_ring_meta)
+    return CP_ERR_INVALID_ARG;
+  if (H < 1 || cp_size < 1 || s_local < 0 || s_local * cp_size > INT32_MAX)
+    return CP_ERR_INVALID_ARG;
+  if (strategy != CP_DUAL_CHUNK_SWAP && strategy != CP_NO_LOAD_BALANCE) return CP_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return CP_ERR_UNSUPPORTED;
+  if (H > 65535 || (int64_t)s_local * cp_size * H * D > ((int64_t)1 << 40)) return CP_ERR_UNSUPPORTED;
+  // a shard's last key block may hold fewer than 128 rows; its 32-row output
+  // chunks must not reach into the next shard's rows
+  if (s_local % 32) return CP_ERR_UNSUPPORTED;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
+  if (step_bytes < 64 || rank_stride < step_bytes * (size_t)cp_size) return CP_ERR_WORKSPACE;
+  if (step_bytes % 16 || rank_stride % 16) return CP_ERR_ALIGNMENT;
+  if (!cpthd_host::aligned16(q_all) || !cpthd_host::aligned16(k_shards) ||
+      !cpthd_host::aligned16(v_shards) || !cpthd_host::aligned16(o_all) ||
+      !cpthd_host::aligned16(o_resid_all) || !cpthd_host::aligned16(lse_all) ||
+      !cpthd_host::aligned16(do_all) || !cpthd_host::aligned16(dq_all) ||
+      !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum) ||
+      !cpthd_host::aligned16(d_ring_meta))
+    return CP_ERR_ALIGNMENT;
+  if (s_local == 0) return CP_OK;
+  if (!d_workspace || workspace_bytes < cp_attn_bwd_ring_workspace_bytes(s_local, H, cp_size))
+    return CP_ERR_WORKSPACE;
+  if (!cpthd_host::aligned16(d_workspace)) return CP_ERR_ALIGNMENT;
+  cudaStream_t s = cpthd_host::as_stream(stream);
+  float* delta_all = (float*)d_workspace;
+  void* scratch = (char*)d_workspace +
+                  ((((size_t)cp_size * s_local * H * sizeof(float)) + 15) & ~(size_t)15);
+  const size_t row_bytes = (size_t)H * D * 2;
+  int st;
+  for (int r = 0; r < cp_size; ++r) {  // Delta of every rank, once (not once per ring step)
+    const size_t ro = (size_t)r * s_local * row_bytes;
+    AttnArgs a{};
+    a.out = (const bf16*)((const char*)o_all + ro);
+    a.out_resid = o_resid_all ? (const bf16*)((const char*)o_resid_all + ro) : nullptr;
+    a.dout = (const bf16*)((const char*)do_all + ro);
+    a.delta = delta_all + (size_t)r * H * s_local;
+    a.H = H; a.s_local = (int)s_local;
+    if ((st = launch_delta(a, D, (int)operand_dtype, s)) != CP_OK) return st;
+  }
+  return cpthd_attn_bwd_ring_tc(q_all, k_shards, v_shards, do_all, lse_all, delta_all, dq_all,
+                                dk_accum, dv_accum, d_ring_meta, step_bytes, rank_stride, H, D,
+                                (int)s_local, cp_size, (int)strategy, softmax_scale,
+                                softmax_scale * kLog2e, (int)operand_dtype, scratch, s);
+}
+
 extern "C" int cpthd_status_attn(int reset) {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_status_attn, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;

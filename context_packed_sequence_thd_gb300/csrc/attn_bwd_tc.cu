@@ -84,8 +84,40 @@ struct BwdArgs {
   int n_ranks;
   int64_t meta_stride;
   const int2* gorder;
-  int* gorder_tot;  // n_kb ints of scratch for the order's totals
+  int* gorder_tot;  // n ints of scratch for the order's totals
+  // ring mode: the P2P ring's steps in one pass.  dQ (n_steps > 1, or
+  // ring_cp > 0): rank ring_rank's n_steps steps, step i's metadata
+  // (cp_size = 1) step_stride bytes after meta, its keys the shard of rank
+  // (ring_rank - i) mod ring_cp, rows s_local * that rank of the K / V
+  // tensors; gorder is then the rank's query tiles heaviest first by their
+  // count over the steps.  dK/dV (ring = 1, n_ranks = ring_cp): items are the
+  // key blocks of every shard; the ranks' step metadata lie meta_stride bytes
+  // apart from meta; rank r reads shard j at its step (r - j) mod ring_cp;
+  // dK / dV rows are rank-concatenated.
+  int ring, n_steps, ring_rank, ring_cp;
+  int64_t step_stride;
 };
+
+// Metadata of ring step i of the dQ pass (step 0 outside ring mode).
+__device__ __forceinline__ const void* step_meta(const BwdArgs& a, int i) {
+  return reinterpret_cast<const char*>(a.meta) + a.step_stride * i;
+}
+
+// Ring steps of rank r: every step for DUAL_CHUNK_SWAP, steps 0..r for
+// NO_LOAD_BALANCE (later ranks' shards hold only later tokens).
+__device__ __forceinline__ int ring_steps_of(const BwdArgs& a, int r) {
+  return a.strategy == (int)CP_NO_LOAD_BALANCE ? min(r + 1, a.ring_cp) : a.ring_cp;
+}
+
+// Source s of a rank-grouped dK/dV item on key shard j: its metadata, or null
+// when the source has no step for that shard (ring mode).  Outside ring mode
+// the source is rank s; in ring mode rank s at its step (s - j) mod ring_cp.
+__device__ __forceinline__ const void* kv_source(const BwdArgs& a, int shard, int src) {
+  if (!a.ring) return reinterpret_cast<const char*>(a.meta) + a.meta_stride * src;
+  const int i = (src - shard + a.ring_cp) % a.ring_cp;
+  if (i >= ring_steps_of(a, src)) return nullptr;
+  return reinterpret_cast<const char*>(a.meta) + a.meta_stride * src + a.step_stride * i;
+}
 
 __device__ __forceinline__ bool meta_ok_bwd(const BwdArgs& a, const MetaHeader* h) {
   const bool ok = meta_matches(h, a.meta_bytes, a.T, a.s_local, a.cp, a.rank, a.strategy);
@@ -99,13 +131,37 @@ __device__ __forceinline__ const void* rank_meta(const BwdArgs& a, int r) {
   return reinterpret_cast<const char*>(a.meta) + a.meta_stride * r;
 }
 
-// Every rank's metadata of a rank-grouped call matches (rank r at r).
+// Every rank's metadata of a rank-grouped call matches (rank r at r); in ring
+// mode every step metadata the call reads (cp_size = 1, rank 0).
 __device__ __forceinline__ bool meta_ok_grouped(const BwdArgs& a) {
   bool ok = true;
   int bad = 0;
-  for (int r = 0; r < a.n_ranks && ok; ++r) {
-    const MetaHeader* h = reinterpret_cast<const MetaHeader*>(rank_meta(a, r));
-    ok = meta_matches(h, (size_t)a.meta_stride, a.T, a.s_local, a.cp, r, a.strategy);
+  if (a.ring) {
+    for (int r = 0; r < a.n_ranks && ok; ++r)
+      for (int i = 0; i < ring_steps_of(a, r) && ok; ++i) {
+        const MetaHeader* h = reinterpret_cast<const MetaHeader*>(
+            reinterpret_cast<const char*>(a.meta) + a.meta_stride * r + a.step_stride * i);
+        ok = meta_matches(h, (size_t)a.meta_bytes, a.T, a.s_local, a.cp, a.rank, a.strategy);
+        if (!ok) bad = h->status != 0 ? h->status : (int)CP_ERR_METADATA;
+      }
+  } else {
+    for (int r = 0; r < a.n_ranks && ok; ++r) {
+      const MetaHeader* h = reinterpret_cast<const MetaHeader*>(rank_meta(a, r));
+      ok = meta_matches(h, (size_t)a.meta_stride, a.T, a.s_local, a.cp, r, a.strategy);
+      if (!ok) bad = h->status != 0 ? h->status : (int)CP_ERR_METADATA;
+    }
+  }
+  if (!ok && threadIdx.x == 0) atomicCAS(&g_status_bwd_tc, 0, bad);
+  return ok;
+}
+
+// Every ring step's metadata of a dQ ring pass matches (cp_size = 1, rank 0).
+__device__ __forceinline__ bool meta_ok_steps(const BwdArgs& a) {
+  bool ok = true;
+  int bad = 0;
+  for (int i = 0; i < a.n_steps && ok; ++i) {
+    const MetaHeader* h = reinterpret_cast<const MetaHeader*>(step_meta(a, i));
+    ok = meta_matches(h, a.meta_bytes, a.T, a.s_local, a.cp, a.rank, a.strategy);
     if (!ok) bad = h->status != 0 ? h->status : (int)CP_ERR_METADATA;
   }
   if (!ok && threadIdx.x == 0) atomicCAS(&g_status_bwd_tc, 0, bad);
@@ -144,6 +200,7 @@ constexpr int kDqHeadGroup = 1 << 20, kKvHeadGroup = 1;
 struct Item {
   const int2* list;  // the tile's block list: count in list[0].x, intervals in list[1..]
   int tile, h, nb;
+  int shard = 0;  // ring-mode dK/dV: the key shard of block `tile`
   // item k: the q-th heaviest tile of head h, heads in groups of G (item_of)
   __device__ void load(const int2* order, const int2* lists, int k, int H, int n_tiles, int G) {
     int q;
@@ -169,11 +226,78 @@ __device__ __forceinline__ Item kv_item(const BwdArgs& a, const MetaView& m, int
   int q;
   item_of(k, n_kb, a.H, kKvHeadGroup, &q, &it.h);  // as Item::load
   const int2 o = a.gorder[min(max(q, 0), n_kb - 1)];
-  it.tile = min(max(o.x, 0), n_kb - 1);
+  const int x = min(max(o.x, 0), n_kb - 1);
+  if (a.ring) {  // every shard's blocks: x = shard * (blocks per shard) + block
+    const int per = (int)n_tiles_of(a.s_local);
+    it.shard = x / per;
+    it.tile = x % per;
+  } else {
+    it.tile = x;
+  }
   it.list = nullptr;
-  it.nb = o.y;  // the sum over the ranks, formed by the ordering kernel
+  it.nb = o.y;  // the sum over the ranks (steps), formed by the ordering kernel
   return it;
 }
+
+// The step count of dK/dV item k alone (what the MMA warp needs of it).
+__device__ __forceinline__ int kv_item_nb(const BwdArgs& a, const MetaView& m, int k, int n_kb) {
+  int q, h;
+  item_of(k, n_kb, a.H, kKvHeadGroup, &q, &h);
+  return (a.n_ranks > 1 ? a.gorder : m.korder)[min(max(q, 0), n_kb - 1)].y;
+}
+
+// dQ work item: outside ring mode as Item::load; in ring mode the q-th
+// heaviest of the rank's query tiles by their count over the ring steps.
+__device__ __forceinline__ Item dq_item(const BwdArgs& a, const MetaView& m, int k, int n_qt) {
+  Item it;
+  if (a.n_steps <= 1) {
+    it.load(m.qorder, m.qlists, k, a.H, n_qt, kDqHeadGroup);
+    return it;
+  }
+  int q;
+  item_of(k, n_qt, a.H, kDqHeadGroup, &q, &it.h);
+  const int2 o = a.gorder[min(max(q, 0), n_qt - 1)];
+  it.tile = min(max(o.x, 0), n_qt - 1);
+  it.list = nullptr;
+  it.nb = o.y;
+  return it;
+}
+
+// The key blocks of a dQ item in order: the tile's block list, or in ring mode
+// the lists of the rank's ring steps one after another (the steps with
+// blocks), each step's blocks in its shard; b is a block of the current step's
+// shard, kv_off the shard's first row in the K / V tensors, step the step.
+struct BwdWalk {
+  const BwdArgs* a;
+  Iter bi;
+  int tile, step, left, kv_off;
+  __device__ void init(const BwdArgs& args, int t) {
+    a = &args;
+    tile = t;
+    step = -1;
+    left = 0;
+    kv_off = 0;
+    advance();
+  }
+  __device__ void advance() {
+    const int n = a->n_steps > 1 ? a->n_steps : 1;
+    while (left == 0 && step + 1 < n) {
+      ++step;
+      const int2* list = meta_view(step_meta(*a, step)).qlists + (kListBytes / 8) * tile;
+      left = list[0].y;
+      bi.init(list + 1, min(list[0].x, kListCap));
+      kv_off = a->ring_cp > 0
+                   ? ((a->ring_rank - step + a->ring_cp) % a->ring_cp) * a->s_local
+                   : 0;
+    }
+  }
+  __device__ int b() const { return bi.b; }
+  __device__ void next() {
+    --left;
+    bi.next();
+    if (left == 0) advance();
+  }
+};
 
 __device__ __forceinline__ uint32_t bar_addr(uint64_t& b) { return smem_u32(&b); }
 
@@ -283,12 +407,12 @@ template <int D, bool F16>
 __global__ void __launch_bounds__(kThr, 1)
 attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
            const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-           const BwdArgs a) {
+           const __grid_constant__ BwdArgs a) {
   using L = DqLayout<D>;
   constexpr int BOXES = D / 64;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const MetaView m = meta_view(a.meta);
-  if (!meta_ok_bwd(a, m.hdr)) return;
+  if (a.n_steps > 1 ? !meta_ok_steps(a) : !meta_ok_bwd(a, m.hdr)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sb = smem_u32(smem_raw);  // tiles need 1024-byte alignment (128B swizzle)
   if (sb & 1023u) {
@@ -338,8 +462,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
         const int k = snake_item(j, blockIdx.x, gridDim.x);
         if (k >= n_items) continue;
-        Item it;
-        it.load(m.qorder, m.qlists, k, a.H, n_qt, kDqHeadGroup);
+        const Item it = dq_item(a, m, k, n_qt);
         if (it.nb == 0) continue;
         // single Q/dO buffer: free once the previous item's S, dP retired
         if (!mbar_wait(bar_addr(c.qd_free), (ii & 1) ^ 1, &s_abort, kLimitNs)) {
@@ -354,10 +477,10 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           tma_load_3d(sb + L::DO + b * kBox, &tm_do, bar_addr(c.qd_full), b * 64, it.h, t0);
         }
         ++ii;
-        Iter bi;
-        bi.init(it.list + 1, it.n_iv());
-        for (int j = 0; j < it.nb; ++j, bi.next()) {
-          const int key0 = bi.b * 128;
+        BwdWalk w;
+        w.init(a, it.tile);
+        for (int j = 0; j < it.nb; ++j, w.next()) {
+          const int key0 = w.kv_off + w.b() * 128;  // the block's first row in K / V
           const int ks = gk % kDqKStages;
           if (!mbar_wait(bar_addr(c.k_empty[ks]), ((gk / kDqKStages) & 1) ^ 1, &s_abort,
                          kLimitNs)) {
@@ -455,8 +578,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
         const int k = snake_item(j, blockIdx.x, gridDim.x);
         if (k >= n_items) continue;
-        Item it;
-        it.load(m.qorder, m.qlists, k, a.H, n_qt, kDqHeadGroup);
+        const Item it = dq_item(a, m, k, n_qt);
         if (it.nb == 0) continue;
         if (!wait_w(bar_addr(c.qd_full), ii & 1)) {
           fail(&s_abort);
@@ -526,8 +648,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
       const int k = snake_item(j, blockIdx.x, gridDim.x);
       if (k >= n_items) continue;
-      Item itm;
-      itm.load(m.qorder, m.qlists, k, a.H, n_qt, kDqHeadGroup);
+      const Item itm = dq_item(a, m, k, n_qt);
       const int t = itm.tile * 128 + row;
       const bool in = t < a.s_local;
       if (itm.nb == 0) {  // no real query row: dQ = 0 (nothing to add in add mode)
@@ -544,15 +665,22 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         continue;
       }
-      const int lo = in ? m.row_lo[t] : 0;
-      const int hi = in ? m.row_hi[t] : -1;
+      int lo = in ? m.row_lo[t] : 0;  // the row's key range (ring mode: per step, below)
+      int hi = in ? m.row_hi[t] : -1;
       const float lse2 = hi >= 0 ? a.lse[(int64_t)itm.h * a.s_local + t] * kLog2ef : 0.f;
       const float dl = hi >= 0 ? a.delta[(int64_t)itm.h * a.s_local + t] : 0.f;
       const uint64_t scl2 = f2_pack(sl2, sl2), nlse2 = f2_pack(-lse2, -lse2);
       const uint64_t dl2 = f2_pack(dl, dl);
-      Iter bi;
-      bi.init(itm.list + 1, itm.n_iv());
-      for (int j = 0; j < itm.nb; ++j, bi.next(), ++g) {
+      BwdWalk w;
+      w.init(a, itm.tile);
+      int cur_step = 0;  // the ring step whose key range lo / hi hold
+      for (int j = 0; j < itm.nb; ++j, w.next(), ++g) {
+        if (w.step != cur_step) {  // ring mode: the row's key range in the next step's shard
+          const MetaView ms = meta_view(step_meta(a, w.step));
+          lo = in ? ms.row_lo[t] : 0;
+          hi = in ? ms.row_hi[t] : -1;
+          cur_step = w.step;
+        }
         if (!wait_warp(bar_addr(c.s_full), g & 1)) {
           fail(&s_abort);
           ok = false;
@@ -564,7 +692,7 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tmem_ld32(tmem + lb + 64 * hf + 32, reinterpret_cast<uint32_t*>(p + 32));
         tc_fence_before();
         mbar_arrive(bar_addr(c.s_free));  // S_{g+1} may now overwrite S
-        const int k0 = bi.b * 128 + 64 * hf;  // key of this thread's first column
+        const int k0 = w.b() * 128 + 64 * hf;  // key (of the step's shard) of this thread's first column
         if (!(lo <= k0 && hi >= k0 + 63)) {  // keys outside the row's range: P = 0
 #pragma unroll
           for (int e = 0; e < 64; ++e)
@@ -731,7 +859,7 @@ __global__ void __launch_bounds__(kKvThr, 1)
 attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
              const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-             const BwdArgs a) {
+             const __grid_constant__ BwdArgs a) {
   using L = KvLayout<D>;
   constexpr int BOXES = D / 64;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -745,7 +873,9 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   }
   KvCtl& c = *reinterpret_cast<KvCtl*>(smem_raw + L::BYTES);
   volatile int& s_abort = *reinterpret_cast<volatile int*>(&c.abort);
-  const int n_kb = (int)n_tiles_of(a.T);
+  // key blocks: of the T keys, or in ring mode of every shard (blocks per shard
+  // times the shards)
+  const int n_kb = a.ring ? a.ring_cp * (int)n_tiles_of(a.s_local) : (int)n_tiles_of(a.T);
   const int n_items = n_kb * a.H;
 
   if (threadIdx.x == 0) {
@@ -794,7 +924,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       if (k >= n_items) continue;
       const Item it = kv_item(a, m, k, n_kb);
       if (it.nb == 0) continue;
-      const int j0 = it.tile * 128;
+      const int j0 = (a.ring ? it.shard * a.s_local : 0) + it.tile * 128;  // first key row
       // single K (V) tile: free once the previous item's last S^T (dP^T) retired
       if (!wait_all(bar_addr(c.k_free), (ii & 1) ^ 1)) {
         if (lane == 0) fail(&s_abort);
@@ -828,7 +958,9 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const int32_t* row_hi = m.row_hi;
         const int2* list = it.list;
         if (grouped) {
-          const MetaView mr = meta_view(rank_meta(a, r));
+          const void* src = kv_source(a, it.shard, r);
+          if (!src) continue;  // (ring mode) rank r never holds this shard
+          const MetaView mr = meta_view(src);
           row_lo = mr.row_lo;
           row_hi = mr.row_hi;
           list = mr.klists + (kListBytes / 8) * it.tile;
@@ -939,7 +1071,8 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       for (int j = 0; ok && j * (int)gridDim.x < n_items; ++j) {
         const int k = snake_item(j, blockIdx.x, gridDim.x);
         if (k >= n_items) continue;
-        const Item it = kv_item(a, m, k, n_kb);
+        Item it;  // (only its step count matters here)
+        it.nb = kv_item_nb(a, m, k, n_kb);
         if (it.nb == 0) continue;
         const int cur = ii++;
         if (!wait_w(bar_addr(c.k_full), cur & 1)) {
@@ -1051,14 +1184,15 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       if (itm.nb == 0) {
         // no query of this rank attends these keys: a stored partial is zero
         if (a.store) {
-          const int rb = itm.tile * 128 + (warp & 3) * 32;
+          const int rb = (a.ring ? itm.shard * a.s_local : 0) + itm.tile * 128 + (warp & 3) * 32;
+          const int row_end = a.ring ? (itm.shard + 1) * a.s_local : a.T;
           const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32)
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
               const int kr = rb + (lane >> 3) + 4 * it;
-              if (kr < a.T) {
+              if (kr < row_end) {
                 const int64_t o = ((int64_t)kr * a.H + itm.h) * D + c0 + 4 * (lane & 7);
                 *reinterpret_cast<float4*>(a.dk + o) = z;
                 *reinterpret_cast<float4*>(a.dv + o) = z;
@@ -1073,7 +1207,11 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       }
       ++ii;
       tc_fence_after();
-      const int rbase = itm.tile * 128 + (warp & 3) * 32;  // first key row of this warp
+      // first key row of this warp, and the end of the key rows the item owns
+      // (ring mode: its shard's; the 32-row chunks never straddle a shard end,
+      // s_local being a multiple of 32 there)
+      const int rbase = (a.ring ? itm.shard * a.s_local : 0) + itm.tile * 128 + (warp & 3) * 32;
+      const int row_end = a.ring ? (itm.shard + 1) * a.s_local : a.T;
 #pragma unroll 1
       for (int ch = 0; ch < 2 * (D / 32); ++ch) {
         const bool is_v = ch < D / 32;  // dV first, then dK
@@ -1106,7 +1244,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         __syncwarp();
         // one bulk copy moves the chunk: rows rbase.. (those past T are not
         // written), columns c0.., added in L2 (or stored by the first rank)
-        if (lane == 0 && rbase < a.T) {  // (a box wholly past the last key row is skipped)
+        if (lane == 0 && rbase < row_end) {  // (a box wholly past the item's rows is skipped)
           const CUtensorMap* map = is_v ? &tm_dv : &tm_dk;
           if (a.store) tma_store_3d(map, stg_s, c0, itm.h, rbase);
           else tma_reduce_add_3d(map, stg_s, c0, itm.h, rbase);
@@ -1235,56 +1373,61 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   }
 }
 
-// Heaviest-first order of the key blocks of a rank-grouped dK/dV launch: each
-// block's total over the ranks of its query-tile count (every rank's block
-// list header), ranked by comparison against every other block (stable for
-// equal totals).  One block; tot is n_kb ints of scratch.
-// Metadata that does not match (the dK/dV kernel then writes nothing) gives
-// the identity order and its lists are not read.
+// Heaviest-first work orders of the grouped and ring launches, ranked by
+// comparison against every entry (stable for equal counts).  One block; tot
+// holds n ints of scratch.
+//   family 1 (dK/dV, rank-grouped or ring): the key blocks (ring mode: of every
+//     shard, entry shard * blocks-per-shard + block) with their query-tile
+//     count summed over the sources (the ranks, or the ranks' steps that hold
+//     the shard);
+//   family 0 (dQ, ring mode): the rank's query tiles with their key-block count
+//     summed over its ring steps.
+// Metadata that does not match (the attention kernel then writes nothing)
+// gives the identity order and its lists are not read.
 constexpr int kOrdThreads = 1024, kOrdChunk = 4096;
 __global__ void __launch_bounds__(kOrdThreads, 1)
-grouped_korder_kernel(const BwdArgs a, int n_kb, int* tot, int2* order) {
+grouped_korder_kernel(const BwdArgs a, int family, int n, int* tot, int2* order) {
   __shared__ int s_t[kOrdChunk];
   __shared__ int s_ok;
-  const void* meta = a.meta;
-  const int64_t stride = a.meta_stride;
-  const int n_ranks = a.n_ranks;
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    for (int r = 0; r < n_ranks && ok; ++r)
-      ok = meta_matches(reinterpret_cast<const MetaHeader*>(rank_meta(a, r)), (size_t)stride,
-                        a.T, a.s_local, a.cp, r, a.strategy) ? 1 : 0;
-    s_ok = ok;
-  }
+  if (threadIdx.x == 0)
+    s_ok = (family == 0 ? meta_ok_steps(a) : meta_ok_grouped(a)) ? 1 : 0;
   __syncthreads();
   if (!s_ok) {
-    for (int q = threadIdx.x; q < n_kb; q += blockDim.x) order[q] = make_int2(q, 0);
+    for (int q = threadIdx.x; q < n; q += blockDim.x) order[q] = make_int2(q, 0);
     return;
   }
-  for (int q = threadIdx.x; q < n_kb; q += blockDim.x) {
+  const int per = (int)n_tiles_of(a.s_local);  // key blocks per shard (ring mode)
+  for (int q = threadIdx.x; q < n; q += blockDim.x) {
     int t = 0;
-    for (int r = 0; r < n_ranks; ++r)
-      t += meta_view(reinterpret_cast<const char*>(meta) + stride * r)
-               .klists[(kListBytes / 8) * q].y;
+    if (family == 0) {
+      for (int i = 0; i < a.n_steps; ++i)
+        t += meta_view(step_meta(a, i)).qlists[(kListBytes / 8) * q].y;
+    } else {
+      const int shard = a.ring ? q / per : 0, kb = a.ring ? q % per : q;
+      for (int r = 0; r < a.n_ranks; ++r) {
+        const void* src = kv_source(a, shard, r);
+        if (src) t += meta_view(src).klists[(kListBytes / 8) * kb].y;
+      }
+    }
     tot[q] = t;
   }
   __syncthreads();
-  for (int q0 = 0; q0 < n_kb; q0 += blockDim.x) {
+  for (int q0 = 0; q0 < n; q0 += blockDim.x) {
     const int q = q0 + threadIdx.x;
-    const int mine = q < n_kb ? tot[q] : 0;
+    const int mine = q < n ? tot[q] : 0;
     int rank = 0;
-    for (int c0 = 0; c0 < n_kb; c0 += kOrdChunk) {
-      const int cn = min(kOrdChunk, n_kb - c0);
+    for (int c0 = 0; c0 < n; c0 += kOrdChunk) {
+      const int cn = min(kOrdChunk, n - c0);
       __syncthreads();
       for (int i = threadIdx.x; i < cn; i += blockDim.x) s_t[i] = tot[c0 + i];
       __syncthreads();
-      if (q < n_kb)
+      if (q < n)
         for (int i = 0; i < cn; ++i) {
           const int o = s_t[i];
           rank += (o > mine || (o == mine && c0 + i < q)) ? 1 : 0;
         }
     }
-    if (q < n_kb) order[rank] = make_int2(q, mine);
+    if (q < n) order[rank] = make_int2(q, mine);
   }
 }
 
@@ -1292,16 +1435,19 @@ grouped_korder_kernel(const BwdArgs a, int n_kb, int* tot, int2* order) {
 // a.n_ranks > 1: Q / dO maps over the n_ranks * s_local concatenated rows).
 template <int D, bool F16>
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
-                  const BwdArgs& a, int parts, cudaStream_t s) {
+                  const BwdArgs& a, int parts, cudaStream_t s, int kv_rows_arg = 0) {
   alignas(64) CUtensorMap mq, mdo, mk, mv, mdk, mdv;
   int st;
   const int q_rows = a.s_local * (a.n_ranks > 1 ? a.n_ranks : 1);
   if ((st = tma::make_thd_map(&mq, q, q_rows, a.H, D, 128, F16)) != CP_OK) return st;
   if ((st = tma::make_thd_map(&mdo, dout, q_rows, a.H, D, 128, F16)) != CP_OK) return st;
-  if ((st = tma::make_thd_map(&mk, k, a.T, a.H, D, 128, F16)) != CP_OK) return st;
-  if ((st = tma::make_thd_map(&mv, v, a.T, a.H, D, 128, F16)) != CP_OK) return st;
-  if ((st = tma::make_f32_rows_map(&mdk, a.dk, a.T, a.H, D)) != CP_OK) return st;
-  if ((st = tma::make_f32_rows_map(&mdv, a.dv, a.T, a.H, D)) != CP_OK) return st;
+  const int kv_rows = kv_rows_arg > 0 ? kv_rows_arg : a.T;  // rows of K, V, dK, dV
+  if ((st = tma::make_thd_map(&mk, k, kv_rows, a.H, D, 128, F16)) != CP_OK) return st;
+  if ((st = tma::make_thd_map(&mv, v, kv_rows, a.H, D, 128, F16)) != CP_OK) return st;
+  if (parts & 2) {  // (the dQ pass never writes dK / dV; its callers may pass none)
+    if ((st = tma::make_f32_rows_map(&mdk, a.dk, kv_rows, a.H, D)) != CP_OK) return st;
+    if ((st = tma::make_f32_rows_map(&mdv, a.dv, kv_rows, a.H, D)) != CP_OK) return st;
+  }
   const int dq_smem = DqLayout<D>::BYTES + (int)sizeof(DqCtl);
   const int kv_smem = kv_stage_offset<D>() + kStageBytes;
   if (cudaFuncSetAttribute(attn_dq_tc<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1311,18 +1457,25 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
     return CP_ERR_CUDA;
   const int sms = cpthd_host::sm_count();
   if (parts & 1) {
+    if (a.n_steps > 1) {  // ring mode: the rank's query tiles by their count over the steps
+      grouped_korder_kernel<<<1, kOrdThreads, 0, s>>>(a, 0, (int)n_tiles_of(a.s_local),
+                                                      a.gorder_tot, const_cast<int2*>(a.gorder));
+      if ((st = cpthd_host::launch_status()) != CP_OK) return st;
+    }
     const int64_t q_items = n_tiles_of(a.s_local) * (int64_t)a.H;
     attn_dq_tc<D, F16><<<(int)(q_items < sms ? q_items : sms), kThr, dq_smem, s>>>(mq, mdo, mk,
                                                                                      mv, a);
     if ((st = cpthd_host::launch_status()) != CP_OK) return st;
   }
   if (!(parts & 2)) return CP_OK;
+  // key blocks: of the T keys, or in ring mode of every shard
+  const int n_kb = a.ring ? a.ring_cp * (int)n_tiles_of(a.s_local) : (int)n_tiles_of(a.T);
   if (a.n_ranks > 1) {
-    grouped_korder_kernel<<<1, kOrdThreads, 0, s>>>(a, (int)n_tiles_of(a.T), a.gorder_tot,
+    grouped_korder_kernel<<<1, kOrdThreads, 0, s>>>(a, 1, n_kb, a.gorder_tot,
                                                     const_cast<int2*>(a.gorder));
     if ((st = cpthd_host::launch_status()) != CP_OK) return st;
   }
-  const int64_t k_items = n_tiles_of(a.T) * (int64_t)a.H;
+  const int64_t k_items = (int64_t)n_kb * a.H;
   // the register split inside attn_dkdv_tc assumes exactly kKvLaunchRegs per thread at launch
   static int kv_regs = -1;
   if (kv_regs < 0) {
@@ -1403,6 +1556,79 @@ int cpthd_attn_dkdv_grouped_tc(const void* q_all, const void* k, const void* v,
                    : launch_bwd_tc<128, true>(q_all, k, v, dout_all, a, 2, s);
   return D == 64 ? launch_bwd_tc<64, false>(q_all, k, v, dout_all, a, 2, s)
                  : launch_bwd_tc<128, false>(q_all, k, v, dout_all, a, 2, s);
+}
+
+// Internal entry of the ring backward in one pass (arguments validated, every
+// rank's Delta in delta_all): per rank one dQ launch over all its ring steps
+// (dQ stored once, bf16), then one dK/dV launch over the key blocks of every
+// shard, each walking the ranks that hold the shard at some step, stored once
+// (fp32, rank-concatenated rows).  ring_meta: rank r's step metadata at
+// r * rank_stride, step i at + i * step_bytes (cp_size = 1 blocks); q_all /
+// dout_all / dq_all / k_shards / v_shards / dk / dv are [cp * s_local, H, D];
+// lse_all / delta_all [cp][H][s_local]; scratch: ring_bwd_scratch_bytes.
+int cpthd_attn_bwd_ring_tc(const void* q_all, const void* k_shards, const void* v_shards,
+                           const void* dout_all, const float* lse_all, const float* delta_all,
+                           void* dq_all, float* dk, float* dv, const void* ring_meta,
+                           size_t step_bytes, size_t rank_stride, int H, int D, int s_local,
+                           int cp, int strategy, float scale, float scale_log2, int f16,
+                           void* scratch, cudaStream_t s) {
+  using namespace cpthd;
+  const int n_qt = (int)n_tiles_of(s_local);
+  int* tot = reinterpret_cast<int*>(scratch);
+  int2* order = reinterpret_cast<int2*>(reinterpret_cast<char*>(scratch) +
+                                        ring_bwd_order_offset(s_local, cp));
+  const int kv_rows = s_local * cp;  // the ranks' shards side by side
+  auto launch = [&](const void* q, const void* dout, const BwdArgs& a, int parts) {
+    if (f16)
+      return D == 64 ? launch_bwd_tc<64, true>(q, k_shards, v_shards, dout, a, parts, s, kv_rows)
+                     : launch_bwd_tc<128, true>(q, k_shards, v_shards, dout, a, parts, s, kv_rows);
+    return D == 64 ? launch_bwd_tc<64, false>(q, k_shards, v_shards, dout, a, parts, s, kv_rows)
+                   : launch_bwd_tc<128, false>(q, k_shards, v_shards, dout, a, parts, s, kv_rows);
+  };
+  const size_t row_bytes = (size_t)H * D * 2;
+  for (int r = 0; r < cp; ++r) {  // dQ of rank r over its ring steps
+    BwdArgs a{};
+    a.lse = lse_all + (size_t)r * H * s_local;
+    a.delta = delta_all + (size_t)r * H * s_local;
+    a.dq = reinterpret_cast<char*>(dq_all) + (size_t)r * s_local * row_bytes;
+    a.meta = reinterpret_cast<const char*>(ring_meta) + rank_stride * r;
+    a.meta_bytes = step_bytes;
+    a.T = s_local; a.H = H; a.s_local = s_local; a.cp = 1; a.rank = 0; a.strategy = strategy;
+    a.scale = scale;
+    a.scale_log2 = scale_log2;
+    a.dq_mode = 0;
+    a.n_ranks = 1;
+    a.n_steps = strategy == (int)CP_NO_LOAD_BALANCE ? r + 1 : cp;
+    a.step_stride = (int64_t)step_bytes;
+    a.ring_rank = r;
+    a.ring_cp = cp;
+    a.gorder = order;
+    a.gorder_tot = tot;
+    if (n_qt == 0) continue;
+    const int st = launch(reinterpret_cast<const char*>(q_all) + (size_t)r * s_local * row_bytes,
+                          reinterpret_cast<const char*>(dout_all) + (size_t)r * s_local * row_bytes,
+                          a, 1);
+    if (st != CP_OK) return st;
+  }
+  BwdArgs a{};  // dK / dV of every shard
+  a.lse = lse_all;
+  a.delta = delta_all;
+  a.dk = dk;
+  a.dv = dv;
+  a.meta = ring_meta;
+  a.meta_bytes = step_bytes;
+  a.T = s_local; a.H = H; a.s_local = s_local; a.cp = 1; a.rank = 0; a.strategy = strategy;
+  a.scale = scale;
+  a.scale_log2 = scale_log2;
+  a.store = 1;
+  a.ring = 1;
+  a.n_ranks = cp;
+  a.ring_cp = cp;
+  a.step_stride = (int64_t)step_bytes;
+  a.meta_stride = (int64_t)rank_stride;
+  a.gorder = order;
+  a.gorder_tot = tot;
+  return launch(q_all, dout_all, a, 2);
 }
 
 extern "C" int cpthd_status_bwd_tc(int reset) {

@@ -261,7 +261,7 @@ struct Walk {
       const int2* list = meta_view(step_meta(*a, step)).qlists + (kListBytes / 8) * tile;
       left = list[0].y;
       bi.init(list + 1, min(list[0].x, kListCap));
-      kv_off = a->n_steps > 1
+      kv_off = a->ring_cp > 0
                    ? ((a->ring_rank - step + a->ring_cp) % a->ring_cp) * a->shard_rows
                    : 0;
     }

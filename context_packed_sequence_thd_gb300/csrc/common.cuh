@@ -319,6 +319,21 @@ int cpthd_attn_fwd_ring_tc(const void* q, const void* k_shards, const void* v_sh
                            int n_steps, int H, int D, int s_local, int cp, int rank, int strategy,
                            float scale_log2, int f16, void* scratch, cudaStream_t s);
 
+// The ring backward in one pass (attn_bwd_tc.cu); scratch: the work orders
+// (the larger of a rank's query tiles and every shard's key blocks).
+inline __host__ __device__ size_t ring_bwd_order_offset(int64_t s_local, int cp) {
+  return ((size_t)cpthd::n_tiles_of(s_local) * cp * 4 + 15) & ~(size_t)15;
+}
+inline __host__ __device__ size_t ring_bwd_scratch_bytes(int64_t s_local, int cp) {
+  return ring_bwd_order_offset(s_local, cp) + (size_t)cpthd::n_tiles_of(s_local) * cp * 8;
+}
+int cpthd_attn_bwd_ring_tc(const void* q_all, const void* k_shards, const void* v_shards,
+                           const void* dout_all, const float* lse_all, const float* delta_all,
+                           void* dq_all, float* dk, float* dv, const void* ring_meta,
+                           size_t step_bytes, size_t rank_stride, int H, int D, int s_local,
+                           int cp, int strategy, float scale, float scale_log2, int f16,
+                           void* scratch, cudaStream_t s);
+
 // tcgen05 dQ and dK/dV kernels (attn_bwd_tc.cu); Delta already in `delta`;
 // mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added)
 // and, internally, kBwdDqOnly (the dQ kernel alone); f16: Q/K/V/dO are fp16,

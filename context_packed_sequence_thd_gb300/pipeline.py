@@ -465,11 +465,15 @@ class CPP2PAttention(CPAttention):
     held shards in ring order within one online softmax (the merge is its
     rescaling, so no partial outputs are written); fused_ring=False runs the
     per-step partials (O_i, LSE_i) and combines them with cp_p2p_merge.
-    Backward: per step with the merged O / LSE; dQ is summed over the rank's
-    steps in an fp32 buffer (first step stores, later steps add), dK/dV of
-    shard j are summed in fp32 over the ranks that attended it (the partial
-    dK/dV that travel back along the ring to their owner), the first
-    contribution to each shard stored; one launch casts all three to bf16.
+    Backward: by default one cp_attn_bwd_ring call (s_local a multiple of 32):
+    per rank one dQ pass over its ring steps, one dK/dV pass over every
+    shard's key blocks walking the ranks that hold the shard, every sum formed
+    inside the kernels.  Otherwise per step with the merged O / LSE; dQ is
+    summed over the rank's steps in an fp32 buffer (first step stores, later
+    steps add), dK/dV of shard j are summed in fp32 over the ranks that
+    attended it (the partial dK/dV that travel back along the ring to their
+    owner), the first contribution to each shard stored; one launch casts all
+    three to bf16.
     """
 
     def __init__(self, plan: CPPlan, operand_dtype: Optional[torch.dtype] = None,
@@ -482,8 +486,14 @@ class CPP2PAttention(CPAttention):
         self.ws_ring = torch.empty(max(api.cp_attn_fwd_ring_workspace_bytes(S), 16),
                                    dtype=torch.uint8, device=dev)
         self.step_bytes = api.cp_p2p_meta_bytes(p.n_docs, T, p.cp)
-        self.p2p_meta = [torch.empty(p.cp * self.step_bytes, dtype=torch.uint8, device=dev)
-                         for _ in range(p.cp)]
+        # every rank's step metadata in one buffer, rank r at r * rank_stride
+        # (the one-pass ring backward reads all of them in one launch)
+        self.rank_stride = p.cp * self.step_bytes
+        self.p2p_meta_all = torch.empty(p.cp * self.rank_stride, dtype=torch.uint8, device=dev)
+        self.p2p_meta = [self.p2p_meta_all[r * self.rank_stride:(r + 1) * self.rank_stride]
+                         for r in range(p.cp)]
+        wsb = api.cp_attn_bwd_ring_workspace_bytes(S, H, p.cp) if S % 32 == 0 else 0
+        self.ws_ring_bwd = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
         self.o_steps = torch.empty(p.cp, S, H, D, dtype=torch.bfloat16, device=dev)
         self.o_steps_resid = torch.empty(p.cp, S, H, D, dtype=torch.bfloat16, device=dev)
         self.lse_steps = torch.empty(p.cp, H, S, dtype=torch.float32, device=dev)
@@ -535,6 +545,24 @@ class CPP2PAttention(CPAttention):
     def backward(self, k_full=None, v_full=None, stream=None):
         p = self.plan
         S = p.s_local
+        if self.fused_ring and S % 32 == 0:
+            # every rank's ring steps in one pass per gradient: dQ stored as bf16,
+            # dK/dV of every shard summed over the ranks inside the kernel
+            with self._timed("attn_bwd", stream):
+                api.cp_attn_bwd_ring(self.qc, self.kc, self.vc, self.oc, self.lse, self.doc,
+                                     self.dqc, self.dk_acc, self.dv_acc, self.p2p_meta_all,
+                                     self.step_bytes, self.rank_stride, p.cp, p.strategy, p.scale,
+                                     self.ws_ring_bwd, stream, o_resid_all=self.oc_resid)
+            self.launches += 3 * p.cp + 2
+            with self._timed("grad_cast", stream):
+                api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc], [self.dkc, self.dvc], None,
+                                           0, p.T, stream)
+            self.launches += 1
+            for r, rm in enumerate(p.ranks):
+                if api.cp_zero_tail([p.local(self.dqc, r), p.local(self.dkc, r),
+                                     p.local(self.dvc, r)], rm.valid_end, stream=stream):
+                    self.launches += 1
+            return
         for r, i, j, mode in ring_steps(p.cp, p.strategy):
             with self._timed("attn_bwd", stream):
                 api.cp_attn_bwd(p.local(self.qc, r), p.local(self.kc, j), p.local(self.vc, j),

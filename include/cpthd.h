@@ -415,6 +415,37 @@ int cp_p2p_merge(const void* d_o_steps, const void* d_o_steps_resid, const float
                  int n_steps, int64_t s_local, int H, int D, void* d_out, void* d_out_resid,
                  float* d_lse, void* stream);
 
+/* Scratch cp_attn_bwd_ring needs: every rank's Delta (fp32 [cp][H][s_local])
+ * and the work orders (12 bytes per 128-key block of every shard). */
+size_t cp_attn_bwd_ring_workspace_bytes(int64_t s_local, int H, int cp_size);
+
+/* The backward of every rank of the P2P ring in one pass per gradient: the
+ * result of the per-step backward (cp_attn_bwd_ex at every ring step with the
+ * merged O / LSE, dQ summed over a rank's steps, dK/dV of shard j summed over
+ * the ranks that attended it), with every sum formed inside the kernels.  Per
+ * rank one dQ launch walks the rank's ring steps in ring order (dq_all, bf16,
+ * stored once); one dK/dV launch covers the 128-key blocks of every shard,
+ * each walking the query tiles of the ranks that hold that shard at some step,
+ * and stores dk_accum / dv_accum once (fp32 [cp_size*s_local, H, D],
+ * rank-concatenated rows, +0.0 where nothing attends).  Operands are the
+ * ranks' tensors side by side: q_all, o_all, o_resid_all (nullable), do_all,
+ * dq_all [cp_size*s_local, H, D]; k_shards / v_shards the ranks' K/V shards
+ * side by side; lse_all fp32 [cp_size][H][s_local].  d_ring_meta: rank r's
+ * step metadata at r*rank_stride, step i at +i*step_bytes (cp_p2p_index
+ * output; rank_stride >= cp_size*step_bytes, both % 16 == 0).  s_local must be
+ * a multiple of 32 (else CP_ERR_UNSUPPORTED: a shard's output chunks would
+ * reach into the next shard).  Launches: cp_size Delta, per rank an ordering
+ * kernel and a dQ kernel, one ordering kernel and one dK/dV kernel.
+ * Deterministic.  Errors as cp_attn_bwd; every step header is checked on the
+ * device (CP_ERR_METADATA, gradients not written). */
+int cp_attn_bwd_ring(const void* q_all, const void* k_shards, const void* v_shards,
+                     const void* o_all, const void* o_resid_all, const float* lse_all,
+                     const void* do_all, void* dq_all, float* dk_accum, float* dv_accum,
+                     const void* d_ring_meta, size_t step_bytes, size_t rank_stride,
+                     int64_t s_local, int H, int D, int cp_size, cp_strategy_t strategy,
+                     float softmax_scale, cp_dtype_t operand_dtype, void* d_workspace,
+                     size_t workspace_bytes, void* stream);
+
 /* Scratch cp_attn_fwd_ring needs: its work order, 12 bytes per 128-row query
  * tile (16-aligned halves). */
 size_t cp_attn_fwd_ring_workspace_bytes(int64_t s_local);

@@ -160,25 +160,35 @@ def test_p2p_step_is_deterministic():
 
 @pytest.mark.parametrize("strategy", [pipeline.DCS, pipeline.NLB], ids=["dcs", "nlb"])
 def test_ring_one_pass_matches_per_step(strategy):
-    """The one-pass ring forward against the per-step partials + merge on the
-    same inputs: O within one bf16 rounding of each other, LSE within 1e-4
-    (one fp32 online softmax against bf16 partials combined in fp32)."""
+    """The one-pass ring forward and backward (cp_attn_fwd_ring, cp_attn_bwd_ring)
+    against the per-step path (cp_attn_fwd + cp_p2p_merge, cp_attn_bwd_ex per
+    step with fp32 sums) on the same inputs: outputs and gradients within two
+    bf16 roundings of each other, LSE within 1e-4 (the same terms summed in
+    another order)."""
     d = dev()
-    wl = inputs.custom([304, 216, 504, 96, 400], cp=4, H=3, D=128, seed=75)  # lse rows 16-byte aligned
+    # s_local = 384: lse rows 16-byte aligned, a multiple of 32 (one-pass backward)
+    wl = inputs.custom([304, 216, 504, 96, 416], cp=4, H=3, D=128, seed=75)
+    assert wl.total_tokens // wl.cp % 32 == 0
     g = {k: v.to(d) for k, v in wl.tensors().items()}
     res = []
     for fused in (True, False):
         plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, d)
         att = pipeline.CPP2PAttention(plan, fused_ring=fused)
-        att.step(g["q"], g["k"], g["v"])
+        att.launches = 0
+        att.step(g["q"], g["k"], g["v"], g["do"])
         torch.cuda.synchronize()
         assert api.cp_device_status() == 0
-        res.append((att.oc.float().clone(), att.lse.clone()))
-    (o1, l1), (o2, l2) = res
-    assert torch.equal(torch.isneginf(l1), torch.isneginf(l2))
-    fin = ~torch.isneginf(l1)
-    assert (l1[fin] - l2[fin]).abs().max().item() <= 1e-4
-    assert (o1 - o2).abs().max().item() <= 2.0 ** -7 * max(1.0, o2.abs().max().item())
+        res.append({"o": att.oc.float().clone(), "lse": att.lse.clone(), "dq": att.dqc.float().clone(),
+                    "dk": att.dkc.float().clone(), "dv": att.dvc.float().clone(),
+                    "launches": att.launches})
+    a, b = res
+    assert a["launches"] < b["launches"]  # the one-pass path ran
+    assert torch.equal(torch.isneginf(a["lse"]), torch.isneginf(b["lse"]))
+    fin = ~torch.isneginf(a["lse"])
+    assert (a["lse"][fin] - b["lse"][fin]).abs().max().item() <= 1e-4
+    for k in ("o", "dq", "dk", "dv"):
+        scale = max(1.0, b[k].abs().max().item())
+        assert (a[k] - b[k]).abs().max().item() <= 2.0 ** -6 * scale, k
 
 
 def test_ring_one_pass_refuses_other_metadata():
