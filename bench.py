@@ -51,9 +51,9 @@ WORKLOAD = ("THD fwd+bwd with inter-sequence padding: 65536 padded tokens, 24 lo
 # DRAM bytes (read + write) per backward call (cp_attn_bwd_grouped: every rank's attn_delta
 # and attn_dq_tc, one attn_dkdv_tc), averaged over the 2 calls of a step (2 strategies), from
 # the ncu capture named in BWD_TRAFFIC_NOTE; None until a capture of the current kernels exists.
-BWD_TRAFFIC_BYTES = 22286853888
+BWD_TRAFFIC_BYTES = 22729723392
 BWD_TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the kernels of the timed "
-                    "step's two cp_attn_bwd_grouped calls (DCS 25.52 GB, NLB 19.06 GB), full size, "
+                    "step's two cp_attn_bwd_grouped calls (DCS 25.88 GB, NLB 19.58 GB), full size, "
                     "one pass; profiles/attn_bwd_dram_cfg5.md")
 
 # a timed region shorter than this, at the maximum SM clock, is a burst: the
@@ -318,19 +318,26 @@ def _gather_sweep(dev, hbm, reps=10):
 def _comm_types(wl, dev, reps=3):
     """Forward / backward TFLOP/s of the emulated a2a and P2P (ring) comm types
     on one workload, every strategy (their exchanges, merges and casts
-    included)."""
+    included): the ring as one pass per rank and gradient (default) and step
+    by step, with all-gather CP beside them."""
     import torch
     from context_packed_sequence_thd_gb300 import pipeline
     g = {k: v.to(dev) for k, v in wl.tensors().items()}
     out = {}
-    for name, cls in (("a2a", pipeline.CPA2AAttention), ("p2p", pipeline.CPP2PAttention)):
+    variants = (("a2a", pipeline.CPA2AAttention),
+                ("p2p", pipeline.CPP2PAttention),   # one pass per rank and gradient
+                ("p2p_per_step", lambda plan: pipeline.CPP2PAttention(plan, fused_ring=False)),
+                ("allgather", pipeline.CPAttention))
+    for name, cls in variants:
         for s in (pipeline.DCS, pipeline.NLB):
             plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, s, wl.pad_between_seqs, wl.H, wl.D, dev)
             att = cls(plan)
             att.shard_inputs(g["q"], g["k"], g["v"], g["do"])
             f = att.flops(True)
+            kv = att.forward()
+            kv = kv if isinstance(kv, tuple) else (None, None)
             t_f = _time_ms(lambda: att.forward(), reps)
-            t_b = _time_ms(lambda: att.backward(), reps)
+            t_b = _time_ms(lambda: att.backward(*kv), reps)
             out[f"{name}_{pipeline.STRATEGY_NAMES[s]}"] = {
                 "fwd_ms": round(t_f, 4), "fwd_tflops": round(f["fwd"] / t_f / 1e9, 1),
                 "bwd_ms": round(t_b, 4), "bwd_tflops": round(f["bwd"] / t_b / 1e9, 1)}
