@@ -48,13 +48,14 @@ WORKLOAD = ("THD fwd+bwd with inter-sequence padding: 65536 padded tokens, 24 lo
             "padded to multiples of 2*cp, cp_size=4, H=32, D=128, bf16, pad_between_seqs=1, "
             "both strategies")
 
-# DRAM bytes (read + write) per backward call (cp_attn_bwd_grouped: every rank's attn_delta
-# and attn_dq_tc, one attn_dkdv_tc), averaged over the 2 calls of a step (2 strategies), from
-# the ncu capture named in BWD_TRAFFIC_NOTE; None until a capture of the current kernels exists.
-BWD_TRAFFIC_BYTES = 22729723392
+# DRAM bytes (read + write) per backward call (cp_attn_bwd_grouped_rs: every rank's
+# attn_delta and attn_dq_tc, one attn_dkdv_tc that also writes the reduce-scatter's bf16 rows),
+# averaged over the 2 calls of a step (2 strategies), from the ncu capture named in
+# BWD_TRAFFIC_NOTE; None until a capture of the current kernels exists.
+BWD_TRAFFIC_BYTES = 20754172800
 BWD_TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the kernels of the timed "
-                    "step's two cp_attn_bwd_grouped calls (DCS 25.88 GB, NLB 19.58 GB), full size, "
-                    "one pass; profiles/attn_bwd_dram_cfg5.md")
+                    "step's two cp_attn_bwd_grouped_rs calls (DCS 23.87 GB, NLB 17.64 GB), full "
+                    "size, one pass; profiles/attn_bwd_dram_cfg5.md")
 
 # a timed region shorter than this, at the maximum SM clock, is a burst: the
 # denominator is the burst peak; otherwise the sustained one
@@ -512,7 +513,7 @@ def run_own(args):
     bwd_calls = per.get("attn_bwd", [])
     fwd_calls = per.get("attn_fwd", [])
     # algorithmic FLOP per call, averaged over a step's calls: the forward is one
-    # cp_attn_fwd per rank and strategy, the backward one cp_attn_bwd_grouped
+    # cp_attn_fwd per rank and strategy, the backward one cp_attn_bwd_grouped_rs
     # per strategy (every rank's Delta and dQ launches and one dK/dV launch)
     n_bwd_calls = max(1, len(bwd_calls) // args.steps)
     n_fwd_calls = max(1, len(fwd_calls) // args.steps)
@@ -576,8 +577,9 @@ def run_own(args):
                        "l2": "inputs larger than L2 (4 x 537 MB bf16 inputs, ~25 GB touched "
                              "per step)"},
             "roofline": {"bound": "tensor", "kernel": dominant,
-                         "kernels": "cp_attn_bwd_grouped: attn_delta + attn_dq_tc per rank, "
-                                    "one rank-grouped attn_dkdv_tc"
+                         "kernels": "cp_attn_bwd_grouped_rs: attn_delta + attn_dq_tc per rank, "
+                                    "one rank-grouped attn_dkdv_tc writing the reduce-scatter's "
+                                    "bf16 rows"
                          if dominant == "attn_bwd" else "attn_fwd_tc",
                          "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(ach / peak, 4),

@@ -58,6 +58,8 @@ _SIGNATURES = {
     "cp_attn_bwd_grouped_workspace_bytes": ([_I64, _I, _I, _I64], _SZ),
     "cp_attn_bwd_grouped": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I, _I, _I,
                              _I, ctypes.c_float, _I, _P, _SZ, _P], _I),
+    "cp_attn_bwd_grouped_rs": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I,
+                                _I, _I, _I, ctypes.c_float, _I, _P, _SZ, _P], _I),
     "cp_p2p_meta_bytes": ([_I, _I64, _I], _SZ),
     "cp_p2p_index": ([_P, _P, _I, _I64, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "cp_p2p_merge": ([_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P], _I),
@@ -374,6 +376,25 @@ def cp_attn_bwd_grouped(q_all, k_full, v_full, o_all, lse_all, do_all, dq_all, d
         _dev(q_all, "q"), _dev(k_full, "k"), _dev(v_full, "v"), _dev(o_all, "o"),
         _opt(o_resid_all, "o_resid"), _dev(lse_all, "lse"), _dev(do_all, "do"),
         _dev(dq_all, "dq"), _dev(dk_accum, "dk"), _dev(dv_accum, "dv"),
+        _dev(d_meta_all, "meta"), int(meta_stride), total_tokens, H, D, cp_size, strategy,
+        float(softmax_scale), dt, _dev(d_workspace, "workspace"),
+        d_workspace.numel() * d_workspace.element_size(), _stream(stream)))
+
+
+def cp_attn_bwd_grouped_rs(q_all, k_full, v_full, o_all, lse_all, do_all, dq_all, dk_all, dv_all,
+                           d_restore, d_meta_all, meta_stride: int, total_tokens: int,
+                           cp_size: int, strategy: int, softmax_scale: float, d_workspace,
+                           stream=None, o_resid_all=None) -> None:
+    """cp_attn_bwd_grouped_rs: cp_attn_bwd_grouped with the reduce-scatter fused
+    into the dK/dV kernel: dk_all / dv_all are the rank-concatenated bf16
+    outputs (rank r's rows at r*s_local in its partition order), written
+    through d_restore (None under NO_LOAD_BALANCE)."""
+    _, H, D = k_full.shape
+    dt = _operand_dtype(q_all, k_full, v_full, do_all)
+    _check("cp_attn_bwd_grouped_rs", lib().cp_attn_bwd_grouped_rs(
+        _dev(q_all, "q"), _dev(k_full, "k"), _dev(v_full, "v"), _dev(o_all, "o"),
+        _opt(o_resid_all, "o_resid"), _dev(lse_all, "lse"), _dev(do_all, "do"),
+        _dev(dq_all, "dq"), _dev(dk_all, "dk"), _dev(dv_all, "dv"), _opt(d_restore, "restore"),
         _dev(d_meta_all, "meta"), int(meta_stride), total_tokens, H, D, cp_size, strategy,
         float(softmax_scale), dt, _dev(d_workspace, "workspace"),
         d_workspace.numel() * d_workspace.element_size(), _stream(stream)))

@@ -307,26 +307,27 @@ extern "C" size_t cp_attn_bwd_grouped_workspace_bytes(int64_t s_local, int H, in
   return delta + grouped_scratch_bytes(total_tokens);
 }
 
-extern "C" int cp_attn_bwd_grouped(const void* q_all, const void* k_full, const void* v_full,
-                                   const void* o_all, const void* o_resid_all,
-                                   const float* lse_all, const void* do_all, void* dq_all,
-                                   float* dk_accum, float* dv_accum, const void* d_meta_all,
-                                   size_t meta_stride, int64_t total_tokens, int H, int D,
-                                   int cp_size, cp_strategy_t strategy, float softmax_scale,
-                                   cp_dtype_t operand_dtype, void* d_workspace,
-                                   size_t workspace_bytes, void* stream) {
+static int bwd_grouped(const void* q_all, const void* k_full, const void* v_full,
+                       const void* o_all, const void* o_resid_all, const float* lse_all,
+                       const void* do_all, void* dq_all, float* dk_accum, float* dv_accum,
+                       const void* d_meta_all, size_t meta_stride, int64_t total_tokens, int H,
+                       int D, int cp_size, cp_strategy_t strategy, float softmax_scale,
+                       cp_dtype_t operand_dtype, void* d_workspace, size_t workspace_bytes,
+                       void* stream, void* dk_all, void* dv_all, const int32_t* d_restore) {
   if (check_dtype(operand_dtype) != CP_OK) return CP_ERR_INVALID_ARG;
   int64_t s_local = 0;
   int st = common_checks(q_all, k_full, v_full, d_meta_all, meta_stride, total_tokens, H, D,
                          cp_size, 0, strategy, &s_local);
   if (st != CP_OK) return st;
   if (meta_stride % 16) return CP_ERR_ALIGNMENT;
-  if (!o_all || !lse_all || !do_all || !dq_all || !dk_accum || !dv_accum)
+  const bool rs = dk_all != nullptr;  // the reduce-scatter's scatter fused in
+  if (!o_all || !lse_all || !do_all || !dq_all || (rs ? !dv_all : (!dk_accum || !dv_accum)))
     return CP_ERR_INVALID_ARG;
   if (!cpthd_host::aligned16(o_all) || !cpthd_host::aligned16(lse_all) ||
       !cpthd_host::aligned16(do_all) || !cpthd_host::aligned16(dq_all) ||
       !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum) ||
-      !cpthd_host::aligned16(o_resid_all))
+      !cpthd_host::aligned16(o_resid_all) || !cpthd_host::aligned16(dk_all) ||
+      !cpthd_host::aligned16(dv_all))
     return CP_ERR_ALIGNMENT;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return CP_ERR_INVALID_ARG;
   if (s_local == 0) return CP_OK;
@@ -367,7 +368,40 @@ extern "C" int cp_attn_bwd_grouped(const void* q_all, const void* k_full, const 
   return cpthd_attn_dkdv_grouped_tc(q_all, k_full, v_full, do_all, lse_all, delta_all, dk_accum,
                                     dv_accum, d_meta_all, meta_stride, (int)total_tokens, H, D,
                                     (int)s_local, cp_size, (int)strategy, softmax_scale,
-                                    softmax_scale * kLog2e, (int)operand_dtype, scratch, s);
+                                    softmax_scale * kLog2e, (int)operand_dtype, scratch, s,
+                                    dk_all, dv_all, d_restore);
+}
+
+extern "C" int cp_attn_bwd_grouped(const void* q_all, const void* k_full, const void* v_full,
+                                   const void* o_all, const void* o_resid_all,
+                                   const float* lse_all, const void* do_all, void* dq_all,
+                                   float* dk_accum, float* dv_accum, const void* d_meta_all,
+                                   size_t meta_stride, int64_t total_tokens, int H, int D,
+                                   int cp_size, cp_strategy_t strategy, float softmax_scale,
+                                   cp_dtype_t operand_dtype, void* d_workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return bwd_grouped(q_all, k_full, v_full, o_all, o_resid_all, lse_all, do_all, dq_all,
+                     dk_accum, dv_accum, d_meta_all, meta_stride, total_tokens, H, D, cp_size,
+                     strategy, softmax_scale, operand_dtype, d_workspace, workspace_bytes, stream,
+                     nullptr, nullptr, nullptr);
+}
+
+extern "C" int cp_attn_bwd_grouped_rs(const void* q_all, const void* k_full, const void* v_full,
+                                      const void* o_all, const void* o_resid_all,
+                                      const float* lse_all, const void* do_all, void* dq_all,
+                                      void* dk_all, void* dv_all, const int32_t* d_restore,
+                                      const void* d_meta_all, size_t meta_stride,
+                                      int64_t total_tokens, int H, int D, int cp_size,
+                                      cp_strategy_t strategy, float softmax_scale,
+                                      cp_dtype_t operand_dtype, void* d_workspace,
+                                      size_t workspace_bytes, void* stream) {
+  if (!dk_all || !dv_all) return CP_ERR_INVALID_ARG;
+  if (strategy == CP_DUAL_CHUNK_SWAP && !d_restore) return CP_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(d_restore) & 3u) return CP_ERR_ALIGNMENT;
+  return bwd_grouped(q_all, k_full, v_full, o_all, o_resid_all, lse_all, do_all, dq_all,
+                     nullptr, nullptr, d_meta_all, meta_stride, total_tokens, H, D, cp_size,
+                     strategy, softmax_scale, operand_dtype, d_workspace, workspace_bytes, stream,
+                     dk_all, dv_all, d_restore);
 }
 
 extern "C" size_t cp_attn_bwd_ring_workspace_bytes(int64_t s_local, int H, int cp_size) {

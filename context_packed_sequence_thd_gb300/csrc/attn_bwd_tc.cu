@@ -96,6 +96,14 @@ struct BwdArgs {
   // dK / dV rows are rank-concatenated.
   int ring, n_steps, ring_rank, ring_cp;
   int64_t step_stride;
+  // rank-grouped dK/dV with the reduce-scatter's scatter fused in (rs = 1):
+  // the summed dK / dV of global key row j go, rounded to bf16, to row
+  // rs_row[j] (j when rs_row is null) of the rank-concatenated dk16 / dv16
+  // [T, H, D] instead of the fp32 dk / dv.
+  int rs;
+  const int32_t* rs_row;
+  uint16_t* dk16;
+  uint16_t* dv16;
 };
 
 // Metadata of ring step i of the dQ pass (step 0 outside ring mode).
@@ -117,6 +125,19 @@ __device__ __forceinline__ const void* kv_source(const BwdArgs& a, int shard, in
   const int i = (src - shard + a.ring_cp) % a.ring_cp;
   if (i >= ring_steps_of(a, src)) return nullptr;
   return reinterpret_cast<const char*>(a.meta) + a.meta_stride * src + a.step_stride * i;
+}
+
+// Destination row of global key row kr under the fused scatter: rs_row[kr]
+// (kr without an index); -1 for a row past the tensor, or an index entry
+// outside [0, T), which also sets the status word.
+__device__ __forceinline__ int64_t rs_dst_row(const BwdArgs& a, int kr) {
+  if (kr >= a.T) return -1;
+  const int t = a.rs_row ? __ldg(a.rs_row + kr) : kr;
+  if (t < 0 || t >= a.T) {
+    atomicCAS(&g_status_bwd_tc, 0, (int)CP_ERR_INVALID_ARG);
+    return -1;
+  }
+  return t;
 }
 
 __device__ __forceinline__ bool meta_ok_bwd(const BwdArgs& a, const MetaHeader* h) {
@@ -1183,7 +1204,20 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const Item itm = kv_item(a, m, k, n_kb);
       if (itm.nb == 0) {
         // no query of this rank attends these keys: a stored partial is zero
-        if (a.store) {
+        if (a.rs) {
+          const int kr = itm.tile * 128 + (warp & 3) * 32 + lane;
+          const int64_t t = rs_dst_row(a, kr);
+          if (t >= 0) {
+            uint4* dk = reinterpret_cast<uint4*>(a.dk16 + (t * a.H + itm.h) * D);
+            uint4* dv = reinterpret_cast<uint4*>(a.dv16 + (t * a.H + itm.h) * D);
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 4
+            for (int u = 0; u < D / 8; ++u) {
+              dk[u] = z;
+              dv[u] = z;
+            }
+          }
+        } else if (a.store) {
           const int rb = (a.ring ? itm.shard * a.s_local : 0) + itm.tile * 128 + (warp & 3) * 32;
           const int row_end = a.ring ? (itm.shard + 1) * a.s_local : a.T;
           const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1212,6 +1246,8 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       // s_local being a multiple of 32 there)
       const int rbase = (a.ring ? itm.shard * a.s_local : 0) + itm.tile * 128 + (warp & 3) * 32;
       const int row_end = a.ring ? (itm.shard + 1) * a.s_local : a.T;
+      // fused scatter: this lane's key row and its destination row (-1: none)
+      const int64_t drow = a.rs ? rs_dst_row(a, rbase + lane) : -1;
 #pragma unroll 1
       for (int ch = 0; ch < 2 * (D / 32); ++ch) {
         const bool is_v = ch < D / 32;  // dV first, then dK
@@ -1223,6 +1259,24 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           mbar_arrive(bar_addr(is_v ? c.dv_free : c.dk_free));
         }
         const float sc = is_v ? 1.f : a.scale;
+        if (a.rs) {
+          // the lane's 32 values of its row, rounded to bf16 as the stored
+          // fp32 sum would be (+0 first), straight to the destination row
+          if (drow >= 0) {
+            uint4* d = reinterpret_cast<uint4*>((is_v ? a.dv16 : a.dk16) +
+                                                (drow * a.H + itm.h) * D + c0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16(__fadd_rn(__uint_as_float(v[8 * u + 2 * e]) * sc, 0.f),
+                                 __fadd_rn(__uint_as_float(v[8 * u + 2 * e + 1]) * sc, 0.f));
+              d[u] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          continue;
+        }
         // the previous chunk's bulk copy has finished reading the staging buffer
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
@@ -1436,7 +1490,7 @@ grouped_korder_kernel(const BwdArgs a, int family, int n, int* tot, int2* order)
 template <int D, bool F16>
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
                   const BwdArgs& a, int parts, cudaStream_t s, int kv_rows_arg = 0) {
-  alignas(64) CUtensorMap mq, mdo, mk, mv, mdk, mdv;
+  alignas(64) CUtensorMap mq, mdo, mk, mv, mdk{}, mdv{};
   int st;
   const int q_rows = a.s_local * (a.n_ranks > 1 ? a.n_ranks : 1);
   if ((st = tma::make_thd_map(&mq, q, q_rows, a.H, D, 128, F16)) != CP_OK) return st;
@@ -1444,7 +1498,7 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
   const int kv_rows = kv_rows_arg > 0 ? kv_rows_arg : a.T;  // rows of K, V, dK, dV
   if ((st = tma::make_thd_map(&mk, k, kv_rows, a.H, D, 128, F16)) != CP_OK) return st;
   if ((st = tma::make_thd_map(&mv, v, kv_rows, a.H, D, 128, F16)) != CP_OK) return st;
-  if (parts & 2) {  // (the dQ pass never writes dK / dV; its callers may pass none)
+  if ((parts & 2) && !a.rs) {  // (the dQ pass and the fused scatter use no fp32 map)
     if ((st = tma::make_f32_rows_map(&mdk, a.dk, kv_rows, a.H, D)) != CP_OK) return st;
     if ((st = tma::make_f32_rows_map(&mdv, a.dv, kv_rows, a.H, D)) != CP_OK) return st;
   }
@@ -1524,22 +1578,29 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
 
 // Internal entry of the rank-grouped dK/dV: one launch over every key block,
 // each walking the attending query tiles of all cp ranks, stored once into the
-// fp32 dK / dV (every row written).  q_all / dout_all are the rank-concatenated
-// [cp * s_local, H, D] operands, lse_all / delta_all [cp][H][s_local], meta_all
-// the cp ranks' metadata meta_stride bytes apart; scratch holds n_kb ints and
-// then (16-aligned) n_kb int2 of the work order.
+// fp32 dK / dV (every row written), or with dk16 / dv16 given, rounded to bf16
+// into row rs_row[j] (j without an index) of the rank-concatenated outputs
+// (the reduce-scatter's scatter fused in; dk / dv unused).  q_all / dout_all
+// are the rank-concatenated [cp * s_local, H, D] operands, lse_all / delta_all
+// [cp][H][s_local], meta_all the cp ranks' metadata meta_stride bytes apart;
+// scratch holds n_kb ints and then (16-aligned) n_kb int2 of the work order.
 int cpthd_attn_dkdv_grouped_tc(const void* q_all, const void* k, const void* v,
                                const void* dout_all, const float* lse_all,
                                const float* delta_all, float* dk, float* dv,
                                const void* meta_all, size_t meta_stride, int T, int H, int D,
                                int s_local, int cp, int strategy, float scale, float scale_log2,
-                               int f16, void* scratch, cudaStream_t s) {
+                               int f16, void* scratch, cudaStream_t s, void* dk16, void* dv16,
+                               const int32_t* rs_row) {
   using namespace cpthd;
   BwdArgs a{};
   a.lse = lse_all;
   a.delta = delta_all;
   a.dk = dk;
   a.dv = dv;
+  a.rs = dk16 != nullptr;
+  a.rs_row = rs_row;
+  a.dk16 = reinterpret_cast<uint16_t*>(dk16);
+  a.dv16 = reinterpret_cast<uint16_t*>(dv16);
   a.meta = meta_all;
   a.meta_bytes = meta_stride;
   a.T = T; a.H = H; a.s_local = s_local; a.cp = cp; a.rank = 0; a.strategy = strategy;

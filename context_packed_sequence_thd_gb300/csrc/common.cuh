@@ -362,4 +362,6 @@ int cpthd_attn_dkdv_grouped_tc(const void* q_all, const void* k, const void* v,
                                const float* delta_all, float* dk, float* dv,
                                const void* meta_all, size_t meta_stride, int T, int H, int D,
                                int s_local, int cp, int strategy, float scale, float scale_log2,
-                               int f16, void* scratch, cudaStream_t s);
+                               int f16, void* scratch, cudaStream_t s,
+                               void* dk16 = nullptr, void* dv16 = nullptr,
+                               const int32_t* rs_row = nullptr);

@@ -18,10 +18,15 @@ Diagram; "[PyTorch] Extend no-load-balance CP to the a2a comm type"):
                               (DUAL_CHUNK_SWAP); a no-op for NO_LOAD_BALANCE,
                               whose rank-concatenated order is the original
                               order (the reorder the a2a page removes)
-  attention fwd / bwd         cp_attn_fwd / cp_attn_bwd per rank
-  unrestore + reduce-scatter  per-rank partial dK/dV summed in fp32 in
-                              original order, then cp_reduce_scatter_emul
-                              (gather by the rank's index + bf16 cast)
+  attention fwd / bwd         cp_attn_fwd per rank; the backward of every
+                              rank in one call (cp_attn_bwd_grouped_rs)
+  unrestore + reduce-scatter  by default inside that call: the dK/dV kernel
+                              sums the ranks' partials per key block and
+                              writes each rank's rows, in bf16, through the
+                              restore index; otherwise fp32 sums in original
+                              order (grouped, or rank by rank), then
+                              cp_reduce_scatter_emul (gather by the rank's
+                              index + bf16 cast)
   dQ/dK/dV tail-zeroing       cp_zero_tail, gated by the host-known valid end
 
 Only argument marshalling and buffer management happen here; every step is
@@ -158,12 +163,16 @@ class CPAttention:
     """Buffers and the full emulated CP forward/backward for one plan."""
 
     def __init__(self, plan: CPPlan, fuse_q_gather: bool = False,
-                 operand_dtype: Optional[torch.dtype] = None, grouped_bwd: bool = True):
+                 operand_dtype: Optional[torch.dtype] = None, grouped_bwd: bool = True,
+                 fused_rs: bool = True):
         self.plan = plan
         p = plan
         # backward of all ranks in one call (cp_attn_bwd_grouped: dK/dV summed
         # over the ranks inside one dK/dV launch) or rank by rank (cp_attn_bwd)
         self.grouped_bwd = grouped_bwd
+        # with the grouped backward, the reduce-scatter's scatter and bf16 cast
+        # in the dK/dV kernel's epilogue (cp_attn_bwd_grouped_rs): no fp32 sums
+        self.fused_rs = grouped_bwd and fused_rs
         # forward-only steps under DUAL_CHUNK_SWAP: the attention loads query
         # rows through the partition index (cp_attn_fwd_gather), no Q shard copy
         self.fuse_q_gather = fuse_q_gather
@@ -199,8 +208,9 @@ class CPAttention:
         self.dqc = torch.empty(T, H, D, **bf)
         self.dkc = torch.empty(T, H, D, **bf)
         self.dvc = torch.empty(T, H, D, **bf)
-        self.dk_acc = torch.empty(T, H, D, dtype=torch.float32, device=dev)
-        self.dv_acc = torch.empty(T, H, D, dtype=torch.float32, device=dev)
+        acc = None if self.fused_rs else dict(dtype=torch.float32, device=dev)
+        self.dk_acc = torch.empty(T, H, D, **acc) if acc else None
+        self.dv_acc = torch.empty(T, H, D, **acc) if acc else None
         ws = api.cp_attn_bwd_workspace_bytes(p.s_local, H)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         wsg = api.cp_attn_bwd_grouped_workspace_bytes(p.s_local, H, p.cp, T) if grouped_bwd else 0
@@ -288,7 +298,17 @@ class CPAttention:
         (rank 0 stores its partial into the fp32 accumulators, the others add
         theirs in rank order)."""
         p = self.plan
-        if self.grouped_bwd:
+        if self.fused_rs:
+            # the whole reduce-scatter inside the dK/dV kernel: each rank's
+            # rows of dK/dV (its partition order) written once, in bf16
+            with self._timed("attn_bwd", stream):
+                api.cp_attn_bwd_grouped_rs(self.qc, k_full, v_full, self.oc, self.lse, self.doc,
+                                           self.dqc, self.dkc, self.dvc,
+                                           p.restore if p.strategy == DCS else None, p.meta_all,
+                                           p.meta_stride, p.T, p.cp, p.strategy, p.scale,
+                                           self.ws_grouped, stream, o_resid_all=self.oc_resid)
+            self.launches += 2 * p.cp + 2
+        elif self.grouped_bwd:
             with self._timed("attn_bwd", stream):
                 api.cp_attn_bwd_grouped(self.qc, k_full, v_full, self.oc, self.lse, self.doc,
                                         self.dqc, self.dk_acc, self.dv_acc, p.meta_all,
@@ -305,13 +325,15 @@ class CPAttention:
                                     mode=api.BWD_STORE if r == 0 else api.BWD_ACCUMULATE,
                                     o_resid=p.local(self.oc_resid, r))
                 self.launches += 3
-        # the scatter half of the reduce-scatter for every rank in one launch:
-        # rank r's rows of the rank-concatenated dK/dV are the summed
-        # accumulators at its partition index (NO_LOAD_BALANCE: contiguous)
-        with self._timed("reduce_scatter_emul", stream):
-            api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc], [self.dkc, self.dvc],
-                                       p.idx_all if p.strategy == DCS else None, 0, p.T, stream)
-        self.launches += 1
+        if not self.fused_rs:
+            # the scatter half of the reduce-scatter for every rank in one launch:
+            # rank r's rows of the rank-concatenated dK/dV are the summed
+            # accumulators at its partition index (NO_LOAD_BALANCE: contiguous)
+            with self._timed("reduce_scatter_emul", stream):
+                api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc], [self.dkc, self.dvc],
+                                           p.idx_all if p.strategy == DCS else None, 0, p.T,
+                                           stream)
+            self.launches += 1
         for r, rm in enumerate(p.ranks):
             if api.cp_zero_tail([p.local(self.dqc, r), p.local(self.dkc, r), p.local(self.dvc, r)],
                                 rm.valid_end, stream=stream):
@@ -354,7 +376,7 @@ class CPA2AAttention(CPAttention):
     """
 
     def __init__(self, plan: CPPlan, operand_dtype: Optional[torch.dtype] = None):
-        super().__init__(plan, operand_dtype=operand_dtype)
+        super().__init__(plan, operand_dtype=operand_dtype, fused_rs=False)
         p = plan
         if p.H % p.cp:
             raise ValueError("the a2a comm type needs H divisible by cp_size")
@@ -478,7 +500,7 @@ class CPP2PAttention(CPAttention):
 
     def __init__(self, plan: CPPlan, operand_dtype: Optional[torch.dtype] = None,
                  fused_ring: bool = True):
-        super().__init__(plan, operand_dtype=operand_dtype)
+        super().__init__(plan, operand_dtype=operand_dtype, fused_rs=False)
         p = plan
         dev, T, H, D, S = p.device, p.T, p.H, p.D, p.s_local
         self.k_full = self.v_full = None   # no restore: attention reads the shards

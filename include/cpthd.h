@@ -365,6 +365,30 @@ int cp_attn_bwd_grouped(const void* q_all, const void* k_full, const void* v_ful
                         cp_dtype_t operand_dtype, void* d_workspace, size_t workspace_bytes,
                         void* stream);
 
+/* cp_attn_bwd_grouped with the whole emulated reduce-scatter inside the dK/dV
+ * kernel ([AG] §Sequence Diagram: the partial dK/dV are summed over the group
+ * and each rank keeps its own rows): the sum over the ranks is taken in the
+ * tensor-core products as in cp_attn_bwd_grouped, and the dK/dV kernel's
+ * epilogue writes it, rounded to bf16, straight into the rank-concatenated
+ * outputs -- the result cp_reduce_scatter_emul gives from cp_attn_bwd_grouped's
+ * fp32 sums, bit for bit, without the fp32 buffers and the extra pass.
+ *   dk_all / dv_all: bf16 [T, H, D], rank r's rows at r * s_local in its
+ *     partition order (overwritten, every row written).
+ *   d_restore: device int32 [T], the rank-concatenated row of global row j
+ *     (cp_partition_index_all's restore index); required for
+ *     DUAL_CHUNK_SWAP, NULL for NO_LOAD_BALANCE (rank-concatenated order is
+ *     the original order).  An entry outside [0, T) skips that row and sets
+ *     the device status word (CP_ERR_INVALID_ARG).
+ * Other arguments, workspace (cp_attn_bwd_grouped_workspace_bytes), launches
+ * and errors as cp_attn_bwd_grouped; dk_all / dv_all 16-byte aligned. */
+int cp_attn_bwd_grouped_rs(const void* q_all, const void* k_full, const void* v_full,
+                           const void* o_all, const void* o_resid_all, const float* lse_all,
+                           const void* do_all, void* dq_all, void* dk_all, void* dv_all,
+                           const int32_t* d_restore, const void* d_meta_all, size_t meta_stride,
+                           int64_t total_tokens, int H, int D, int cp_size,
+                           cp_strategy_t strategy, float softmax_scale, cp_dtype_t operand_dtype,
+                           void* d_workspace, size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------
  * The P2P (ring) comm type, every rank on one GPU ([P2P] §Describe the bug:
  * the P2P context-parallel path, whose per-step sequence metadata comes from

@@ -178,6 +178,22 @@ def test_argument_validation_before_launch(lib):
                                  4096, 2, 64, 2, 0, f(0.1), 0, FAKE, 8, None) == -6
     assert L.cp_attn_bwd_grouped(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096,
                                  4096, 2, 64, 2, 0, f(0.1), 3, FAKE, 1 << 24, None) == -1
+    # grouped backward with the reduce-scatter fused: DUAL_CHUNK_SWAP needs the
+    # restore index, which must be int-aligned; outputs required and 16-aligned;
+    # then the grouped call's own checks (stride, workspace)
+    rs = L.cp_attn_bwd_grouped_rs
+    assert rs(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 4096,
+              4096, 2, 64, 2, 0, f(0.1), 0, FAKE, 1 << 24, None) == -1
+    assert rs(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, FAKE, 4096,
+              4096, 2, 64, 2, 0, f(0.1), 0, FAKE, 1 << 24, None) == -4
+    assert rs(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 4096,
+              4096, 2, 64, 2, 0, f(0.1), 0, FAKE, 1 << 24, None) == -1
+    assert rs(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 8, FAKE, None, FAKE, 4096,
+              4096, 2, 64, 2, 1, f(0.1), 0, FAKE, 1 << 24, None) == -4
+    assert rs(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 4104,
+              4096, 2, 64, 2, 1, f(0.1), 0, FAKE, 1 << 24, None) == -4
+    assert rs(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096,
+              4096, 2, 64, 2, 0, f(0.1), 0, FAKE, 8, None) == -6
     # the fp16 gather: index optional, but then the source must cover the rows
     assert L.cp_thd_gather_f16(_arr(FAKE), _arr(FAKE), 1, None, 8, 4, 256, None) == -1
     assert L.cp_thd_gather_f16(_arr(FAKE), _arr(FAKE), 1, None, 0, 4, 250, None) == -4

@@ -14,10 +14,10 @@ from gpu_util import assert_close, assert_lse_close, dev, to_np
 pytestmark = pytest.mark.gpu
 
 
-def run(wl, strategy, d, tensors=None, bwd=True, operand_dtype=None):
+def run(wl, strategy, d, tensors=None, bwd=True, operand_dtype=None, fused_rs=True):
     t = wl.tensors() if tensors is None else tensors
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, d)
-    att = pipeline.CPAttention(plan, operand_dtype=operand_dtype)
+    att = pipeline.CPAttention(plan, operand_dtype=operand_dtype, fused_rs=fused_rs)
     g = {k: v.to(d) for k, v in t.items()}
     att.step(g["q"], g["k"], g["v"], g["do"] if bwd else None)
     torch.cuda.synchronize()
@@ -49,9 +49,15 @@ def check_against_oracle(wl, strategy, bwd=True, operand_dtype=None):
             assert_close(to_np(plan.local(att.dkc, r)), dk[rows], f"dK rank {r}")
             assert_close(to_np(plan.local(att.dvc, r)), dv[rows], f"dV rank {r}")
     if bwd:
-        # the fp32 accumulators hold the cp=1 gradient before the cast
-        assert_close(to_np(att.dk_acc), grads[1], "dK fp32 accumulator")
-        assert_close(to_np(att.dv_acc), grads[2], "dV fp32 accumulator")
+        # the reduce-scatter as a separate pass: its fp32 sums hold the cp=1
+        # gradient before the cast, and its bf16 rows are bitwise the ones the
+        # dK/dV kernel writes itself
+        _, sep = run(wl, strategy, d, t, bwd, operand_dtype, fused_rs=False)
+        assert_close(to_np(sep.dk_acc), grads[1], "dK fp32 accumulator")
+        assert_close(to_np(sep.dv_acc), grads[2], "dV fp32 accumulator")
+        for name in ("dqc", "dkc", "dvc"):
+            assert torch.equal(getattr(att, name).view(torch.int16),
+                               getattr(sep, name).view(torch.int16)), name
 
 
 SMALL = {
@@ -93,7 +99,7 @@ def test_rank_partial_accumulators():
     t = wl.tensors()
     o, lse = oracle.attn_fwd(t["q"], t["k"], t["v"], wl.cu, wl.cup, 0)
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, pipeline.DCS, 0, wl.H, wl.D, d)
-    att = pipeline.CPAttention(plan)
+    att = pipeline.CPAttention(plan, fused_rs=False)
     g = {k: v.to(d) for k, v in t.items()}
     att.shard_inputs(g["q"], g["k"], g["v"], g["do"])
     kf, vf = att.forward()
@@ -119,7 +125,7 @@ def test_store_mode_starts_the_sum_bitwise(strategy):
     d = dev()
     wl = inputs.custom([200, 56, 128, 640], cp=4, H=2, D=64, seed=71)
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, 0, wl.H, wl.D, d)
-    att = pipeline.CPAttention(plan)
+    att = pipeline.CPAttention(plan, fused_rs=False)
     g = {k: v.to(d) for k, v in wl.tensors().items()}
     att.shard_inputs(g["q"], g["k"], g["v"], g["do"])
     kf, vf = att.forward()
@@ -205,7 +211,11 @@ def test_deterministic():
     t = wl.tensors()
     _, a = run(wl, pipeline.DCS, d, t)
     _, b = run(wl, pipeline.DCS, d, t)
-    for name in ("oc", "dqc", "dkc", "dvc", "dk_acc", "dv_acc"):
+    for name in ("oc", "dqc", "dkc", "dvc"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    _, a = run(wl, pipeline.DCS, d, t, fused_rs=False)
+    _, b = run(wl, pipeline.DCS, d, t, fused_rs=False)
+    for name in ("dk_acc", "dv_acc"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
 
 

@@ -20,9 +20,9 @@ def _heads_slice(t, heads):
     return {k: v[:, heads].contiguous() for k, v in t.items()}
 
 
-def _run_all(wl, strategy, d, g, bwd, cls=pipeline.CPAttention, operand_dtype=None):
+def _run_all(wl, strategy, d, g, bwd, cls=pipeline.CPAttention, operand_dtype=None, **kw):
     plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, d)
-    att = cls(plan, operand_dtype=operand_dtype)
+    att = cls(plan, operand_dtype=operand_dtype, **kw)
     att.step(g["q"], g["k"], g["v"], g["do"] if bwd else None)
     torch.cuda.synchronize()
     assert api.cp_device_status() == 0
@@ -58,9 +58,11 @@ def _compare_acc(att, heads, dk, dv, what, acc):
 
 # Every head of every workload with a backward: the heads are independent, so
 # the oracle computes them in groups of 8 while the GPU results of both
-# strategies and both tensor-core operand types (fp16, the default; bf16 with
-# two-term P and dS) stay on the device.  No head is left out, so no head can
-# hide an out-of-tolerance element.
+# strategies and both tensor-core operand types (fp16, the default, with the
+# reduce-scatter inside the dK/dV kernel as timed; bf16 with two-term P and dS,
+# with the reduce-scatter as its own pass over fp32 sums, which are checked
+# too) stay on the device.  No head is left out, so no head can hide an
+# out-of-tolerance element.
 @pytest.mark.parametrize("make", [inputs.cfg2, inputs.cfg4, inputs.cfg5], ids=["cfg2", "cfg4", "cfg5"])
 def test_full_size_fwd_bwd_all_heads(make):
     d = dev()
@@ -68,7 +70,7 @@ def test_full_size_fwd_bwd_all_heads(make):
     t = wl.tensors()
     g = {k: v.to(d) for k, v in t.items()}
     pad = wl.pad_between_seqs
-    runs = [_run_all(wl, strategy, d, g, True, operand_dtype=dt)
+    runs = [_run_all(wl, strategy, d, g, True, operand_dtype=dt, fused_rs=dt == torch.float16)
             for strategy in wl.strategies for dt in (torch.float16, torch.bfloat16)]
     worst = [{} for _ in runs]
     for h0 in range(0, wl.H, 8):
@@ -78,7 +80,8 @@ def test_full_size_fwd_bwd_all_heads(make):
         grads = oracle.attn_bwd(s["q"], s["k"], s["v"], o, lse, s["do"], wl.cu, wl.cup, pad)
         for (plan, att), acc in zip(runs, worst):
             _compare(wl, plan, att, heads, o, lse, grads, acc=acc)
-            _compare_acc(att, heads, grads[1], grads[2], f"heads {heads}", acc)
+            if att.dk_acc is not None:
+                _compare_acc(att, heads, grads[1], grads[2], f"heads {heads}", acc)
     for (plan, att), acc in zip(runs, worst):
         print(f"\n{wl.name} {pipeline.STRATEGY_NAMES[plan.strategy]} {att.operand_dtype} worst "
               f"max-abs over all {wl.H} heads: " + ", ".join(f"{k} {v:.5f}" for k, v in acc.items()))

@@ -37,7 +37,7 @@ def _forward(wl, strategy, d, seed_shift, operand_dtype):
 
 
 def _backward(plan, att, kf, vf, noalloc):
-    T, H, D = att.dk_acc.shape
+    T, H, D = att.dqc.shape
     dq = torch.zeros_like(att.dqc)
     dk = torch.zeros(T, H, D, dtype=torch.float32, device=dq.device)
     dv = torch.zeros_like(dk)
