@@ -68,6 +68,8 @@ _SIGNATURES = {
     "cp_attn_bwd_ring_workspace_bytes": ([_I64, _I, _I], _SZ),
     "cp_attn_bwd_ring": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _SZ, _I64, _I, _I, _I,
                           _I, ctypes.c_float, _I, _P, _SZ, _P], _I),
+    "cp_attn_bwd_ring_rs": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _SZ, _I64, _I, _I,
+                             _I, _I, ctypes.c_float, _I, _P, _SZ, _P], _I),
     "cp_attn_fwd_ring": ([_P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I64, _I, _I, _I, _I, _I,
                           ctypes.c_float, _I, _P, _SZ, _P], _I),
 }
@@ -436,6 +438,25 @@ def cp_attn_bwd_ring(q_all, k_shards, v_shards, o_all, lse_all, do_all, dq_all, 
         _dev(q_all, "q"), _dev(k_shards, "k"), _dev(v_shards, "v"), _dev(o_all, "o"),
         _opt(o_resid_all, "o_resid"), _dev(lse_all, "lse"), _dev(do_all, "do"),
         _dev(dq_all, "dq"), _dev(dk_accum, "dk"), _dev(dv_accum, "dv"), _dev(d_ring_meta, "meta"),
+        int(step_bytes), int(rank_stride), s_local, H, D, cp_size, strategy, float(softmax_scale),
+        dt, _dev(d_workspace, "workspace"), d_workspace.numel() * d_workspace.element_size(),
+        _stream(stream)))
+
+
+def cp_attn_bwd_ring_rs(q_all, k_shards, v_shards, o_all, lse_all, do_all, dq_all, dk_all,
+                        dv_all, d_ring_meta, step_bytes: int, rank_stride: int, cp_size: int,
+                        strategy: int, softmax_scale: float, d_workspace, stream=None,
+                        o_resid_all=None) -> None:
+    """cp_attn_bwd_ring_rs: cp_attn_bwd_ring with dK/dV written as bf16
+    rank-concatenated shards by the dK/dV kernel itself (no fp32 sums, no cast
+    pass)."""
+    rows, H, D = q_all.shape
+    s_local = rows // cp_size
+    dt = _operand_dtype(q_all, k_shards, v_shards, do_all)
+    _check("cp_attn_bwd_ring_rs", lib().cp_attn_bwd_ring_rs(
+        _dev(q_all, "q"), _dev(k_shards, "k"), _dev(v_shards, "v"), _dev(o_all, "o"),
+        _opt(o_resid_all, "o_resid"), _dev(lse_all, "lse"), _dev(do_all, "do"),
+        _dev(dq_all, "dq"), _dev(dk_all, "dk"), _dev(dv_all, "dv"), _dev(d_ring_meta, "meta"),
         int(step_bytes), int(rank_stride), s_local, H, D, cp_size, strategy, float(softmax_scale),
         dt, _dev(d_workspace, "workspace"), d_workspace.numel() * d_workspace.element_size(),
         _stream(stream)))

@@ -410,17 +410,17 @@ extern "C" size_t cp_attn_bwd_ring_workspace_bytes(int64_t s_local, int H, int c
   return delta + ring_bwd_scratch_bytes(s_local, cp_size);
 }
 
-extern "C" int cp_attn_bwd_ring(const void* q_all, const void* k_shards, const void* v_shards,
-                                const void* o_all, const void* o_resid_all, const float* lse_all,
-                                const void* do_all, void* dq_all, float* dk_accum, float* dv_accum,
-                                const void* d_ring_meta, size_t step_bytes, size_t rank_stride,
-                                int64_t s_local, int H, int D, int cp_size,
-                                cp_strategy_t strategy, float softmax_scale,
-                                cp_dtype_t operand_dtype, void* d_workspace,
-                                size_t workspace_bytes, void* stream) {
+static int bwd_ring(const void* q_all, const void* k_shards, const void* v_shards,
+                    const void* o_all, const void* o_resid_all, const float* lse_all,
+                    const void* do_all, void* dq_all, float* dk_accum, float* dv_accum,
+                    const void* d_ring_meta, size_t step_bytes, size_t rank_stride, int64_t s_local,
+                    int H, int D, int cp_size, cp_strategy_t strategy, float softmax_scale,
+                    cp_dtype_t operand_dtype, void* d_workspace, size_t workspace_bytes,
+                    void* stream, void* dk_all, void* dv_all) {
   if (check_dtype(operand_dtype) != CP_OK) return CP_ERR_INVALID_ARG;
+  const bool rs = dk_all != nullptr;  // bf16 dK / dV out, the cast fused in
   if (!q_all || !k_shards || !v_shards || !o_all || !lse_all || !do_all || !dq_all ||
-      !dk_accum || !dv_accum || !d_ring_meta)
+      (rs ? !dv_all : (!dk_accum || !dv_accum)) || !d_ring_meta)
     return CP_ERR_INVALID_ARG;
   if (H < 1 || cp_size < 1 || s_local < 0 || s_local * cp_size > INT32_MAX)
     return CP_ERR_INVALID_ARG;
@@ -438,7 +438,8 @@ extern "C" int cp_attn_bwd_ring(const void* q_all, const void* k_shards, const v
       !cpthd_host::aligned16(o_resid_all) || !cpthd_host::aligned16(lse_all) ||
       !cpthd_host::aligned16(do_all) || !cpthd_host::aligned16(dq_all) ||
       !cpthd_host::aligned16(dk_accum) || !cpthd_host::aligned16(dv_accum) ||
-      !cpthd_host::aligned16(d_ring_meta))
+      !cpthd_host::aligned16(d_ring_meta) || !cpthd_host::aligned16(dk_all) ||
+      !cpthd_host::aligned16(dv_all))
     return CP_ERR_ALIGNMENT;
   if (s_local == 0) return CP_OK;
   if (!d_workspace || workspace_bytes < cp_attn_bwd_ring_workspace_bytes(s_local, H, cp_size))
@@ -463,7 +464,37 @@ extern "C" int cp_attn_bwd_ring(const void* q_all, const void* k_shards, const v
   return cpthd_attn_bwd_ring_tc(q_all, k_shards, v_shards, do_all, lse_all, delta_all, dq_all,
                                 dk_accum, dv_accum, d_ring_meta, step_bytes, rank_stride, H, D,
                                 (int)s_local, cp_size, (int)strategy, softmax_scale,
-                                softmax_scale * kLog2e, (int)operand_dtype, scratch, s);
+                                softmax_scale * kLog2e, (int)operand_dtype, scratch, s, dk_all,
+                                dv_all);
+}
+
+extern "C" int cp_attn_bwd_ring(const void* q_all, const void* k_shards, const void* v_shards,
+                                const void* o_all, const void* o_resid_all, const float* lse_all,
+                                const void* do_all, void* dq_all, float* dk_accum, float* dv_accum,
+                                const void* d_ring_meta, size_t step_bytes, size_t rank_stride,
+                                int64_t s_local, int H, int D, int cp_size,
+                                cp_strategy_t strategy, float softmax_scale,
+                                cp_dtype_t operand_dtype, void* d_workspace,
+                                size_t workspace_bytes, void* stream) {
+  return bwd_ring(q_all, k_shards, v_shards, o_all, o_resid_all, lse_all, do_all, dq_all,
+                  dk_accum, dv_accum, d_ring_meta, step_bytes, rank_stride, s_local, H, D, cp_size,
+                  strategy, softmax_scale, operand_dtype, d_workspace, workspace_bytes, stream,
+                  nullptr, nullptr);
+}
+
+extern "C" int cp_attn_bwd_ring_rs(const void* q_all, const void* k_shards, const void* v_shards,
+                                   const void* o_all, const void* o_resid_all,
+                                   const float* lse_all, const void* do_all, void* dq_all,
+                                   void* dk_all, void* dv_all, const void* d_ring_meta,
+                                   size_t step_bytes, size_t rank_stride, int64_t s_local, int H,
+                                   int D, int cp_size, cp_strategy_t strategy,
+                                   float softmax_scale, cp_dtype_t operand_dtype,
+                                   void* d_workspace, size_t workspace_bytes, void* stream) {
+  if (!dk_all || !dv_all) return CP_ERR_INVALID_ARG;
+  return bwd_ring(q_all, k_shards, v_shards, o_all, o_resid_all, lse_all, do_all, dq_all, nullptr,
+                  nullptr, d_ring_meta, step_bytes, rank_stride, s_local, H, D, cp_size, strategy,
+                  softmax_scale, operand_dtype, d_workspace, workspace_bytes, stream, dk_all,
+                  dv_all);
 }
 
 extern "C" int cpthd_status_attn(int reset) {

@@ -127,13 +127,15 @@ __device__ __forceinline__ const void* kv_source(const BwdArgs& a, int shard, in
   return reinterpret_cast<const char*>(a.meta) + a.meta_stride * src + a.step_stride * i;
 }
 
-// Destination row of global key row kr under the fused scatter: rs_row[kr]
-// (kr without an index); -1 for a row past the tensor, or an index entry
-// outside [0, T), which also sets the status word.
-__device__ __forceinline__ int64_t rs_dst_row(const BwdArgs& a, int kr) {
-  if (kr >= a.T) return -1;
+// Destination row of key row kr under the fused scatter: rs_row[kr] (kr
+// without an index); -1 for a row at or past row_end (the end of the item's
+// rows), or an index entry outside the output's rows (T; ring mode: the
+// ranks' shards, ring_cp * s_local), which also sets the status word.
+__device__ __forceinline__ int64_t rs_dst_row(const BwdArgs& a, int kr, int row_end) {
+  if (kr >= row_end) return -1;
+  const int n = a.ring ? a.ring_cp * a.s_local : a.T;
   const int t = a.rs_row ? __ldg(a.rs_row + kr) : kr;
-  if (t < 0 || t >= a.T) {
+  if (t < 0 || t >= n) {
     atomicCAS(&g_status_bwd_tc, 0, (int)CP_ERR_INVALID_ARG);
     return -1;
   }
@@ -1205,8 +1207,9 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       if (itm.nb == 0) {
         // no query of this rank attends these keys: a stored partial is zero
         if (a.rs) {
-          const int kr = itm.tile * 128 + (warp & 3) * 32 + lane;
-          const int64_t t = rs_dst_row(a, kr);
+          const int kr = (a.ring ? itm.shard * a.s_local : 0) + itm.tile * 128 + (warp & 3) * 32 +
+                         lane;
+          const int64_t t = rs_dst_row(a, kr, a.ring ? (itm.shard + 1) * a.s_local : a.T);
           if (t >= 0) {
             uint4* dk = reinterpret_cast<uint4*>(a.dk16 + (t * a.H + itm.h) * D);
             uint4* dv = reinterpret_cast<uint4*>(a.dv16 + (t * a.H + itm.h) * D);
@@ -1247,7 +1250,7 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       const int rbase = (a.ring ? itm.shard * a.s_local : 0) + itm.tile * 128 + (warp & 3) * 32;
       const int row_end = a.ring ? (itm.shard + 1) * a.s_local : a.T;
       // fused scatter: this lane's key row and its destination row (-1: none)
-      const int64_t drow = a.rs ? rs_dst_row(a, rbase + lane) : -1;
+      const int64_t drow = a.rs ? rs_dst_row(a, rbase + lane, row_end) : -1;
 #pragma unroll 1
       for (int ch = 0; ch < 2 * (D / 32); ++ch) {
         const bool is_v = ch < D / 32;  // dV first, then dK
@@ -1626,13 +1629,15 @@ int cpthd_attn_dkdv_grouped_tc(const void* q_all, const void* k, const void* v,
 // (fp32, rank-concatenated rows).  ring_meta: rank r's step metadata at
 // r * rank_stride, step i at + i * step_bytes (cp_size = 1 blocks); q_all /
 // dout_all / dq_all / k_shards / v_shards / dk / dv are [cp * s_local, H, D];
-// lse_all / delta_all [cp][H][s_local]; scratch: ring_bwd_scratch_bytes.
+// lse_all / delta_all [cp][H][s_local]; scratch: ring_bwd_scratch_bytes.  With
+// dk16 / dv16 given, dK / dV go out rounded to bf16 there instead (dk / dv
+// unused): the cast of the reduce-scatter in the same epilogue.
 int cpthd_attn_bwd_ring_tc(const void* q_all, const void* k_shards, const void* v_shards,
                            const void* dout_all, const float* lse_all, const float* delta_all,
                            void* dq_all, float* dk, float* dv, const void* ring_meta,
                            size_t step_bytes, size_t rank_stride, int H, int D, int s_local,
                            int cp, int strategy, float scale, float scale_log2, int f16,
-                           void* scratch, cudaStream_t s) {
+                           void* scratch, cudaStream_t s, void* dk16, void* dv16) {
   using namespace cpthd;
   const int n_qt = (int)n_tiles_of(s_local);
   int* tot = reinterpret_cast<int*>(scratch);
@@ -1676,6 +1681,9 @@ int cpthd_attn_bwd_ring_tc(const void* q_all, const void* k_shards, const void* 
   a.delta = delta_all;
   a.dk = dk;
   a.dv = dv;
+  a.rs = dk16 != nullptr;  // bf16 straight out: the shards are already rank-concatenated
+  a.dk16 = reinterpret_cast<uint16_t*>(dk16);
+  a.dv16 = reinterpret_cast<uint16_t*>(dv16);
   a.meta = ring_meta;
   a.meta_bytes = step_bytes;
   a.T = s_local; a.H = H; a.s_local = s_local; a.cp = 1; a.rank = 0; a.strategy = strategy;

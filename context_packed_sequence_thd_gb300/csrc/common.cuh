@@ -332,7 +332,8 @@ int cpthd_attn_bwd_ring_tc(const void* q_all, const void* k_shards, const void* 
                            void* dq_all, float* dk, float* dv, const void* ring_meta,
                            size_t step_bytes, size_t rank_stride, int H, int D, int s_local,
                            int cp, int strategy, float scale, float scale_log2, int f16,
-                           void* scratch, cudaStream_t s);
+                           void* scratch, cudaStream_t s, void* dk16 = nullptr,
+                           void* dv16 = nullptr);
 
 // tcgen05 dQ and dK/dV kernels (attn_bwd_tc.cu); Delta already in `delta`;
 // mode holds cp_bwd_mode_t bits (1: dK/dV stored; 2 / 4: dQ fp32 stored / added)

@@ -569,17 +569,15 @@ class CPP2PAttention(CPAttention):
         S = p.s_local
         if self.fused_ring and S % 32 == 0:
             # every rank's ring steps in one pass per gradient: dQ stored as bf16,
-            # dK/dV of every shard summed over the ranks inside the kernel
+            # dK/dV of every shard summed over the ranks inside the kernel and
+            # written as bf16 by its epilogue (the reduce-scatter's cast fused)
             with self._timed("attn_bwd", stream):
-                api.cp_attn_bwd_ring(self.qc, self.kc, self.vc, self.oc, self.lse, self.doc,
-                                     self.dqc, self.dk_acc, self.dv_acc, self.p2p_meta_all,
-                                     self.step_bytes, self.rank_stride, p.cp, p.strategy, p.scale,
-                                     self.ws_ring_bwd, stream, o_resid_all=self.oc_resid)
+                api.cp_attn_bwd_ring_rs(self.qc, self.kc, self.vc, self.oc, self.lse, self.doc,
+                                        self.dqc, self.dkc, self.dvc, self.p2p_meta_all,
+                                        self.step_bytes, self.rank_stride, p.cp, p.strategy,
+                                        p.scale, self.ws_ring_bwd, stream,
+                                        o_resid_all=self.oc_resid)
             self.launches += 3 * p.cp + 2
-            with self._timed("grad_cast", stream):
-                api.cp_reduce_scatter_emul([self.dk_acc, self.dv_acc], [self.dkc, self.dvc], None,
-                                           0, p.T, stream)
-            self.launches += 1
             for r, rm in enumerate(p.ranks):
                 if api.cp_zero_tail([p.local(self.dqc, r), p.local(self.dkc, r),
                                      p.local(self.dvc, r)], rm.valid_end, stream=stream):

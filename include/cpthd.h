@@ -470,6 +470,21 @@ int cp_attn_bwd_ring(const void* q_all, const void* k_shards, const void* v_shar
                      float softmax_scale, cp_dtype_t operand_dtype, void* d_workspace,
                      size_t workspace_bytes, void* stream);
 
+/* cp_attn_bwd_ring with the reduce-scatter's cast in the dK/dV kernel's
+ * epilogue: dk_all / dv_all are bf16 [cp_size*s_local, H, D] (rank-concatenated
+ * shards, the ring's own layout, so no index is needed), every row written, each
+ * value the bf16 rounding of the fp32 sum cp_attn_bwd_ring stores (bitwise what
+ * cp_reduce_scatter_emul makes of it).  Other arguments, workspace
+ * (cp_attn_bwd_ring_workspace_bytes), launches and errors as cp_attn_bwd_ring;
+ * dk_all / dv_all 16-byte aligned. */
+int cp_attn_bwd_ring_rs(const void* q_all, const void* k_shards, const void* v_shards,
+                        const void* o_all, const void* o_resid_all, const float* lse_all,
+                        const void* do_all, void* dq_all, void* dk_all, void* dv_all,
+                        const void* d_ring_meta, size_t step_bytes, size_t rank_stride,
+                        int64_t s_local, int H, int D, int cp_size, cp_strategy_t strategy,
+                        float softmax_scale, cp_dtype_t operand_dtype, void* d_workspace,
+                        size_t workspace_bytes, void* stream);
+
 /* Scratch cp_attn_fwd_ring needs: its work order, 12 bytes per 128-row query
  * tile (16-aligned halves). */
 size_t cp_attn_fwd_ring_workspace_bytes(int64_t s_local);

@@ -223,6 +223,16 @@ def test_p2p_sizes_and_argument_validation(lib):
     assert L.cp_p2p_merge(FAKE, None, FAKE, 2, 100, 2, 64, FAKE + 4, None, FAKE, None) == -4
     assert L.cp_p2p_merge(FAKE, FAKE + 8, FAKE, 2, 100, 2, 64, FAKE, None, FAKE, None) == -4
     assert L.cp_p2p_merge(FAKE, None, FAKE, 2, 0, 2, 64, FAKE, None, FAKE, None) == 0  # nothing to do
+    # one-pass ring backward with bf16 dK/dV out: outputs required and aligned,
+    # s_local a multiple of 32
+    f = ctypes.c_float
+    rs = L.cp_attn_bwd_ring_rs
+    assert rs(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, FAKE, FAKE, 64, 128, 64, 2, 64,
+              2, 0, f(0.1), 0, FAKE, 1 << 24, None) == -1
+    assert rs(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE + 8, FAKE, FAKE, 64, 128, 64, 2,
+              64, 2, 0, f(0.1), 0, FAKE, 1 << 24, None) == -4
+    assert rs(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 128, 48, 2, 64,
+              2, 0, f(0.1), 0, FAKE, 1 << 24, None) == -3
 
 
 def test_product_path_has_no_oracle_or_cpu_fallback():

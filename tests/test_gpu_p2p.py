@@ -191,6 +191,32 @@ def test_ring_one_pass_matches_per_step(strategy):
         assert (a[k] - b[k]).abs().max().item() <= 2.0 ** -6 * scale, k
 
 
+@pytest.mark.parametrize("strategy", [pipeline.DCS, pipeline.NLB], ids=["dcs", "nlb"])
+def test_ring_cast_in_epilogue_is_bitwise_the_separate_cast(strategy):
+    """cp_attn_bwd_ring_rs (the pipeline's one-pass backward) writes dK/dV as
+    bf16 from the dK/dV kernel's epilogue: bitwise cp_attn_bwd_ring's fp32 sums
+    cast by cp_reduce_scatter_emul, and the same dQ."""
+    d = dev()
+    wl = inputs.custom([304, 216, 504, 96, 416], cp=4, H=3, D=128, seed=77)
+    g = {k: v.to(d) for k, v in wl.tensors().items()}
+    plan = pipeline.CPPlan(wl.cu, wl.cup, wl.cp, strategy, wl.pad_between_seqs, wl.H, wl.D, d)
+    att = pipeline.CPP2PAttention(plan)
+    att.step(g["q"], g["k"], g["v"], g["do"])
+    dq = torch.empty_like(att.dqc)
+    dk = torch.empty_like(att.dkc)
+    dv = torch.empty_like(att.dvc)
+    api.cp_attn_bwd_ring(att.qc, att.kc, att.vc, att.oc, att.lse, att.doc, dq, att.dk_acc,
+                         att.dv_acc, att.p2p_meta_all, att.step_bytes, att.rank_stride, plan.cp,
+                         plan.strategy, plan.scale, att.ws_ring_bwd, o_resid_all=att.oc_resid)
+    api.cp_reduce_scatter_emul([att.dk_acc, att.dv_acc], [dk, dv], None, 0, plan.T)
+    for r, rm in enumerate(plan.ranks):
+        api.cp_zero_tail([plan.local(dq, r), plan.local(dk, r), plan.local(dv, r)], rm.valid_end)
+    torch.cuda.synchronize()
+    assert api.cp_device_status() == 0
+    for name, sep in (("dqc", dq), ("dkc", dk), ("dvc", dv)):
+        assert torch.equal(getattr(att, name).view(torch.int16), sep.view(torch.int16)), name
+
+
 def test_ring_one_pass_refuses_other_metadata():
     """Every step's header is checked on the device: the other strategy's step
     metadata writes nothing and reports CP_ERR_METADATA."""
