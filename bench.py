@@ -57,8 +57,9 @@ BWD_TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the ker
                     "step's two cp_attn_bwd_grouped_rs calls (DCS 23.87 GB, NLB 17.64 GB), full "
                     "size, one pass; profiles/attn_bwd_dram_cfg5.md")
 
-# a timed region shorter than this, at the maximum SM clock, is a burst: the
-# denominator is the burst peak; otherwise the sustained one
+# a timed region shorter than this, at the maximum SM clock and with no power
+# capping, is a burst: the denominator is the burst peak; otherwise the
+# sustained one
 BURST_REGION_S = 1.0
 
 
@@ -109,10 +110,13 @@ def _pairs_all(wl, strategies):
 
 
 def _pick_peak(region_s, clocks, burst, sustained):
-    """Burst peak for a short region run at the maximum clock, else sustained."""
+    """Burst peak for a short region run at the maximum clock with no power
+    capping, else sustained (the kernel then runs in the power-limited regime
+    the sustained figure was measured in)."""
     sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
     at_max = sm is not None and mx is not None and sm >= 0.97 * mx
-    if region_s < BURST_REGION_S and at_max:
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    if region_s < BURST_REGION_S and at_max and not capped:
         return burst, "burst"
     return sustained, "sustained"
 

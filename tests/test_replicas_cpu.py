@@ -54,3 +54,18 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_roofline_peak_choice():
+    """The burst BF16 peak is the denominator only for a short timed region at
+    the maximum SM clock without power capping; a capped or long region uses
+    the sustained one."""
+    sys.path.insert(0, ROOT)
+    import bench
+    at_max = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    capped = {"sm_mhz": 2010.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    slow = {"sm_mhz": 1800.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert bench._pick_peak(0.5, at_max, 1943.5, 1725.2) == (1943.5, "burst")
+    assert bench._pick_peak(0.5, capped, 1943.5, 1725.2) == (1725.2, "sustained")
+    assert bench._pick_peak(0.5, slow, 1943.5, 1725.2) == (1725.2, "sustained")
+    assert bench._pick_peak(2.0, at_max, 1943.5, 1725.2) == (1725.2, "sustained")
