@@ -362,14 +362,18 @@ static int bwd_grouped(const void* q_all, const void* k_full, const void* v_full
                            (char*)dq_all + ro, dk_accum, dv_accum, meta_r, meta_stride,
                            (int)total_tokens, H, D, (int)s_local, cp_size, r, (int)strategy,
                            softmax_scale, softmax_scale * kLog2e, kBwdDqOnly, (int)operand_dtype,
-                           s);
+                           s, r > 0 ? 1 : 0);
     if (st != CP_OK) return st;
   }
+  // the ranks' dQ launches after the first, the work-order kernel and the
+  // dK/dV kernel each start as the previous grid drains (programmatic
+  // dependent launch): none of them reads what the one before writes, except
+  // the dK/dV kernel, which waits for the work order on the device
   return cpthd_attn_dkdv_grouped_tc(q_all, k_full, v_full, do_all, lse_all, delta_all, dk_accum,
                                     dv_accum, d_meta_all, meta_stride, (int)total_tokens, H, D,
                                     (int)s_local, cp_size, (int)strategy, softmax_scale,
                                     softmax_scale * kLog2e, (int)operand_dtype, scratch, s,
-                                    dk_all, dv_all, d_restore);
+                                    dk_all, dv_all, d_restore, 2);
 }
 
 extern "C" int cp_attn_bwd_grouped(const void* q_all, const void* k_full, const void* v_full,

@@ -434,6 +434,10 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   using L = DqLayout<D>;
   constexpr int BOXES = D / 64;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the next launch of the rank-grouped backward (the next rank's dQ, or the
+  // dK/dV work order) reads nothing this grid writes: it may start as soon as
+  // SMs free up (its CTAs land where this grid's CTAs have finished)
+  if (threadIdx.x == 0) pdl_launch_dependents();
   const MetaView m = meta_view(a.meta);
   if (a.n_steps > 1 ? !meta_ok_steps(a) : !meta_ok_bwd(a, m.hdr)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -886,6 +890,9 @@ attn_dkdv_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
   using L = KvLayout<D>;
   constexpr int BOXES = D / 64;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // launched early after the work-order kernel: its order and totals must be
+  // complete and visible before any item is read
+  pdl_wait();
   const MetaView m = meta_view(a.meta);
   if (a.n_ranks > 1 ? !meta_ok_grouped(a) : !meta_ok_bwd(a, m.hdr)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1488,11 +1495,33 @@ grouped_korder_kernel(const BwdArgs a, int family, int n, int* tot, int2* order)
   }
 }
 
+// One launch, with programmatic stream serialization when pdl is set (the
+// kernel may then start before the previous grid in the stream has finished).
+template <typename... P, typename... A>
+cudaError_t launch_ex(void (*kernel)(P...), int grid, int block, int smem, cudaStream_t s,
+                      bool pdl, A&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+}
+
 // parts: 1 = the dQ kernel, 2 = the dK/dV kernel (rank-grouped when
 // a.n_ranks > 1: Q / dO maps over the n_ranks * s_local concatenated rows).
+// pdl bit 1: the dQ kernel may start while the previous grid finishes (it
+// reads nothing that grid writes); bit 2: so may the dK/dV work-order kernel,
+// and the dK/dV kernel may start as the order kernel completes (it waits for
+// the order before reading it).
 template <int D, bool F16>
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
-                  const BwdArgs& a, int parts, cudaStream_t s, int kv_rows_arg = 0) {
+                  const BwdArgs& a, int parts, cudaStream_t s, int kv_rows_arg = 0, int pdl = 0) {
   alignas(64) CUtensorMap mq, mdo, mk, mv, mdk{}, mdv{};
   int st;
   const int q_rows = a.s_local * (a.n_ranks > 1 ? a.n_ranks : 1);
@@ -1520,16 +1549,18 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
       if ((st = cpthd_host::launch_status()) != CP_OK) return st;
     }
     const int64_t q_items = n_tiles_of(a.s_local) * (int64_t)a.H;
-    attn_dq_tc<D, F16><<<(int)(q_items < sms ? q_items : sms), kThr, dq_smem, s>>>(mq, mdo, mk,
-                                                                                     mv, a);
+    if (launch_ex(attn_dq_tc<D, F16>, (int)(q_items < sms ? q_items : sms), kThr, dq_smem, s,
+                  (pdl & 1) != 0, mq, mdo, mk, mv, a) != cudaSuccess)
+      return CP_ERR_CUDA;
     if ((st = cpthd_host::launch_status()) != CP_OK) return st;
   }
   if (!(parts & 2)) return CP_OK;
   // key blocks: of the T keys, or in ring mode of every shard
   const int n_kb = a.ring ? a.ring_cp * (int)n_tiles_of(a.s_local) : (int)n_tiles_of(a.T);
   if (a.n_ranks > 1) {
-    grouped_korder_kernel<<<1, kOrdThreads, 0, s>>>(a, 1, n_kb, a.gorder_tot,
-                                                    const_cast<int2*>(a.gorder));
+    if (launch_ex(grouped_korder_kernel, 1, kOrdThreads, 0, s, (pdl & 2) != 0, a, 1, n_kb,
+                  a.gorder_tot, const_cast<int2*>(a.gorder)) != cudaSuccess)
+      return CP_ERR_CUDA;
     if ((st = cpthd_host::launch_status()) != CP_OK) return st;
   }
   const int64_t k_items = (int64_t)n_kb * a.H;
@@ -1541,8 +1572,9 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* dout,
     kv_regs = fa.numRegs;
   }
   if (kv_regs != kKvLaunchRegs) return CP_ERR_UNSUPPORTED;
-  attn_dkdv_tc<D, F16><<<(int)(k_items < sms ? k_items : sms), kKvThr, kv_smem, s>>>(
-      mq, mdo, mk, mv, mdk, mdv, a);
+  if (launch_ex(attn_dkdv_tc<D, F16>, (int)(k_items < sms ? k_items : sms), kKvThr, kv_smem, s,
+                (pdl & 2) != 0, mq, mdo, mk, mv, mdk, mdv, a) != cudaSuccess)
+    return CP_ERR_CUDA;
   return cpthd_host::launch_status();
 }
 
@@ -1555,7 +1587,7 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
                       const float* lse, const float* delta, void* dq, float* dk, float* dv,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale, float scale_log2,
-                      int mode, int f16, cudaStream_t s) {
+                      int mode, int f16, cudaStream_t s, int pdl) {
   using namespace cpthd;
   BwdArgs a{};
   a.lse = lse;
@@ -1573,10 +1605,10 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
   a.n_ranks = 1;
   const int parts = (mode & kBwdDqOnly) ? 1 : 3;
   if (f16)
-    return D == 64 ? launch_bwd_tc<64, true>(q, k, v, dout, a, parts, s)
-                   : launch_bwd_tc<128, true>(q, k, v, dout, a, parts, s);
-  return D == 64 ? launch_bwd_tc<64, false>(q, k, v, dout, a, parts, s)
-                 : launch_bwd_tc<128, false>(q, k, v, dout, a, parts, s);
+    return D == 64 ? launch_bwd_tc<64, true>(q, k, v, dout, a, parts, s, 0, pdl)
+                   : launch_bwd_tc<128, true>(q, k, v, dout, a, parts, s, 0, pdl);
+  return D == 64 ? launch_bwd_tc<64, false>(q, k, v, dout, a, parts, s, 0, pdl)
+                 : launch_bwd_tc<128, false>(q, k, v, dout, a, parts, s, 0, pdl);
 }
 
 // Internal entry of the rank-grouped dK/dV: one launch over every key block,
@@ -1593,7 +1625,7 @@ int cpthd_attn_dkdv_grouped_tc(const void* q_all, const void* k, const void* v,
                                const void* meta_all, size_t meta_stride, int T, int H, int D,
                                int s_local, int cp, int strategy, float scale, float scale_log2,
                                int f16, void* scratch, cudaStream_t s, void* dk16, void* dv16,
-                               const int32_t* rs_row) {
+                               const int32_t* rs_row, int pdl) {
   using namespace cpthd;
   BwdArgs a{};
   a.lse = lse_all;
@@ -1616,10 +1648,10 @@ int cpthd_attn_dkdv_grouped_tc(const void* q_all, const void* k, const void* v,
   a.gorder = reinterpret_cast<const int2*>(reinterpret_cast<char*>(scratch) +
                                            grouped_order_offset(T));
   if (f16)
-    return D == 64 ? launch_bwd_tc<64, true>(q_all, k, v, dout_all, a, 2, s)
-                   : launch_bwd_tc<128, true>(q_all, k, v, dout_all, a, 2, s);
-  return D == 64 ? launch_bwd_tc<64, false>(q_all, k, v, dout_all, a, 2, s)
-                 : launch_bwd_tc<128, false>(q_all, k, v, dout_all, a, 2, s);
+    return D == 64 ? launch_bwd_tc<64, true>(q_all, k, v, dout_all, a, 2, s, 0, pdl)
+                   : launch_bwd_tc<128, true>(q_all, k, v, dout_all, a, 2, s, 0, pdl);
+  return D == 64 ? launch_bwd_tc<64, false>(q_all, k, v, dout_all, a, 2, s, 0, pdl)
+                 : launch_bwd_tc<128, false>(q_all, k, v, dout_all, a, 2, s, 0, pdl);
 }
 
 // Internal entry of the ring backward in one pass (arguments validated, every

@@ -344,7 +344,7 @@ int cpthd_attn_bwd_tc(const void* q, const void* k, const void* v, const void* d
                       const float* lse, const float* delta, void* dq, float* dk, float* dv,
                       const void* meta, size_t meta_bytes, int T, int H, int D, int s_local,
                       int cp, int rank, int strategy, float scale, float scale_log2,
-                      int mode, int f16, cudaStream_t s);
+                      int mode, int f16, cudaStream_t s, int pdl = 0);
 
 // Scratch of the rank-grouped dK/dV: n_kb int totals, then (16-aligned) the
 // n_kb int2 work order.
@@ -365,4 +365,4 @@ int cpthd_attn_dkdv_grouped_tc(const void* q_all, const void* k, const void* v,
                                int s_local, int cp, int strategy, float scale, float scale_log2,
                                int f16, void* scratch, cudaStream_t s,
                                void* dk16 = nullptr, void* dv16 = nullptr,
-                               const int32_t* rs_row = nullptr);
+                               const int32_t* rs_row = nullptr, int pdl = 0);

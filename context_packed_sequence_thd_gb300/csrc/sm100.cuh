@@ -21,6 +21,18 @@ namespace cpthd {
 namespace sm100 {
 
 // ----------------------------------------------------------------------------
+// programmatic dependent launch: a grid launched with programmatic stream
+// serialization after this one may be scheduled once every CTA of this grid
+// has signalled (or exited); griddepcontrol.wait makes the calling thread wait
+// until the grids it depends on have completed and their writes are visible
+// (a no-op in a grid launched without the attribute)
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+// ----------------------------------------------------------------------------
 // mbarrier
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
