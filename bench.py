@@ -100,7 +100,7 @@ def _whole_job_value(ws, flop_per_step, ms_per_step):
 
 def _workload(name="cfg5"):
     from context_packed_sequence_thd_gb300 import inputs
-    return {"cfg5": inputs.cfg5, "cfg2": inputs.cfg2}[name]()
+    return {"cfg5": inputs.cfg5, "cfg2": inputs.cfg2, "cfg3": inputs.cfg3}[name]()
 
 
 def _pairs_all(wl, strategies):
@@ -459,7 +459,7 @@ def run_own(args):
     hbm, bf16_burst, bf16_sust, peak_src = _peaks()
     wl = _workload(args.workload)
     strategies = (pipeline.DCS, pipeline.NLB)
-    host = wl.tensors()
+    host = wl.tensors(with_grad=wl.bwd)
     g = {k: v.to(dev) for k, v in host.items()}
     atts = [pipeline.CPAttention(pipeline.CPPlan(wl.cu, wl.cup, wl.cp, s, wl.pad_between_seqs,
                                                  wl.H, wl.D, dev)) for s in strategies]
@@ -470,7 +470,7 @@ def run_own(args):
 
     def step():
         for a in atts:
-            a.step(g["q"], g["k"], g["v"], g["do"])
+            a.step(g["q"], g["k"], g["v"], g.get("do"))  # (forward-only workloads: no dO)
 
     for _ in range(args.warmup):
         step()
@@ -776,13 +776,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--capture", action="store_true",
                     help="run warm-up + --steps headline steps only (for ncu captures)")
-    ap.add_argument("--workload", choices=["cfg5", "cfg2"], default="cfg5",
-                    help="cfg2 (32768 tokens, H=16) only for small ncu captures with --capture")
+    ap.add_argument("--workload", choices=["cfg5", "cfg2", "cfg3"], default="cfg5",
+                    help="with --capture only: cfg2 (32768 tokens, H=16, fwd+bwd) or cfg3 (one "
+                         "32768-token sequence, cp=8, H=40, forward only) for smaller ncu captures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.workload != "cfg5" and not args.capture:
-        ap.error("--workload cfg2 is for --capture runs only")
+        ap.error("--workload cfg2 / cfg3 are for --capture runs only")
     if args.impl == "reference":
         run_reference(args)
     else:
