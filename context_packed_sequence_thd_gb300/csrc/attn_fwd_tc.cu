@@ -14,17 +14,20 @@
 // Persistent kernel: one CTA per SM walks a static list of work items
 // (128-row query tile, head), heaviest tiles first, dealt to the CTAs in
 // rounds of alternating direction.  The pipeline never drains between items: all barrier phases
-// follow global counters, Q and the O accumulator are double buffered, and an
-// item's epilogue is deferred until the next item's first block has been
-// handed to the tensor core, so it overlaps tensor-core work.  10 warps:
+// follow global counters, Q is double buffered, and an item's epilogue is
+// deferred until the next item's first block has been handed to the tensor
+// core, so it overlaps the next item's S products.  10 warps:
 //   warps 0-7  softmax: TMEM lane r = query row r, shared by warps r/32 and
 //              r/32+4 which take one half of the key columns each.  Loads S
 //              from TMEM, masks by the row's key range, online softmax in the
-//              log2 domain (the row max is exchanged between the two warps
-//              through shared memory), rescales O only when the max grows by
-//              more than 2^8, writes P (bf16 pairs) back into TMEM over S
-//              (before any O rescale, so S and O are never live in registers
-//              together), and normalises O and stores O / LSE.
+//              log2 domain over its own key half -- its own running max and
+//              sum, and its own accumulator O_half, so the two warps of a row
+//              never wait for each other within an item -- rescales O_half
+//              only when its max grows by more than 2^8, writes P (bf16
+//              pairs) back into TMEM over S (before any O rescale, so S and O
+//              are never live in registers together).  The epilogue combines
+//              the halves (maxima and sums swapped once through shared
+//              memory), normalises and stores O / LSE, and frees O_0 / O_1.
 //   warp 8     TMA producer: Q per item into one of two buffers, K tiles into
 //              a 3-stage ring released as soon as S is done, V tiles into a
 //              2-stage ring released after P V; K runs one block ahead of V.
@@ -33,9 +36,11 @@
 //              rows per copy (tile::gather4).
 //   warp 9     TMEM allocator and MMA issuer (one elected lane per MMA):
 //              S[g%2] = Q K_g^T (M=128, N=128, K=D, both operands K-major in
-//              shared memory) and O[item%2] += P_g V_g (M=128, N=D, K=128; A =
-//              P from TMEM, B = V as an MN-major shared operand).  TMEM: S0
-//              cols [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+//              shared memory) and O_h += P_g[:, keys of half h] V_g[keys of
+//              half h] (M=128, N=D, K=64 each; A = P from TMEM, B = V as an
+//              MN-major shared operand); an item's first P V waits until the
+//              previous item's epilogue has read O_0 / O_1.  TMEM: S0 cols
+//              [0,128), S1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
 // The MMA of S_{g+1} overlaps the softmax of S_g; P_g goes to the other S
 // buffer than P_{g-1}, and the softmax waits for P V_{g-1} only when it has to
 // rescale O, so consecutive P V products are issued back to back.
@@ -123,6 +128,7 @@ struct Bars {
   uint64_t s_full[2];
   uint64_t p_full[2];   // P_g ready: p_full[g % 2]
   uint64_t o_ready[2];  // P V_g done: o_ready[g % 2]
+  uint64_t o_free;      // the item's epilogue has read O_0 / O_1 (one phase per item)
   uint64_t mma_done;
 };
 // Why two alternating barriers suffice for s_full / p_full / o_ready: the MMA
@@ -130,14 +136,16 @@ struct Bars {
 // P V up to g-2 is complete, and P V_{g+1} cannot be issued before the
 // softmax has produced P_{g+1}.  A parity wait on o_ready[(g-1) % 2] (or, for
 // a deferred epilogue at block L+1, on o_ready[L % 2]) therefore always sees
-// exactly the phase it is waiting for.
+// exactly the phase it is waiting for.  o_free completes one phase per item
+// epilogue; the MMA thread waits for item q-1's before item q's first P V,
+// and item q's epilogue needs that P V done, so it is never two phases behind.
 
 // Barriers and small per-CTA state, placed right after the tiles in the
 // dynamic shared memory (the kernel has no static shared memory, so the
 // dynamic window starts 1024-aligned and the tiles need no alignment slack).
 struct Ctl {
   Bars bars;
-  uint64_t pair[4][2];  // row-max / row-sum exchange of softmax warps w, w+4
+  uint64_t pair[4][2];  // epilogue exchange of running max / sum of softmax warps w, w+4
   uint32_t tmem;
   int abort;
   int pad[2];
@@ -312,6 +320,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       mbar_init(bar(bars.v_full[s]), 1);
       mbar_init(bar(bars.v_empty[s]), 1);
     }
+    mbar_init(bar(bars.o_free), kSoftmax);
     mbar_init(bar(bars.mma_done), 1);
     for (int w = 0; w < 4; ++w) {
       mbar_init(bar(ctl.pair[w][0]), 64);
@@ -458,22 +467,27 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       const uint64_t dsc_k = sdesc_sw128(sb + L::K, 16, 1024);
       const uint64_t dsc_v = sdesc_sw128(sb + L::V, kBoxBytes, 1024);
       // the previous block's P V is issued after the next block's S
-      int pv_g = -1, pv_ob = 0;
+      int pv_g = -1, pv_item = 0;  // pv_item: the CTA's non-empty items begun before pv_g's
       bool pv_first = false;
       auto issue_pv = [&]() -> bool {
         const int vs = pv_g % kVStages;
         if (!wait_w(bar(bars.p_full[pv_g & 1]), (pv_g >> 1) & 1) ||
             !wait_w(bar(bars.v_full[vs]), (pv_g / kVStages) & 1))
           return false;
+        // an item's first P V starts O_0 / O_1 afresh: the previous item's
+        // epilogue must have read them
+        if (pv_first && pv_item > 0 && !wait_w(bar(bars.o_free), (pv_item - 1) & 1)) return false;
         tc_fence_after();
         // A = P from TMEM: keys [0,64) over columns [0,32) and keys [64,128)
-        // over [64,96) of S_g's buffer (written by the two column halves)
+        // over [64,96) of S_g's buffer (written by the two column halves);
+        // each key half accumulates into its own O (O_0, O_1), against its
+        // own running max
         const uint64_t bv = sdesc_add(dsc_v, vs * L::TILE);
-        const uint32_t dO = tmem + o_col<D>(pv_ob), aP = tmem + (pv_g & 1) * 128;
+        const uint32_t aP = tmem + (pv_g & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < TBN / 16; ++kk)
-          umma_bf16_ts_w(dO, aP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bv, kk * 2048), idO,
-                         (!pv_first || kk > 0) ? 1u : 0u);
+          umma_bf16_ts_w(tmem + o_col<D>(kk >> 2), aP + (kk >> 2) * 64 + (kk & 3) * 8,
+                         sdesc_add(bv, kk * 2048), idO, (!pv_first || (kk & 3) > 0) ? 1u : 0u);
         umma_commit_w(bar(bars.v_empty[vs]));
         umma_commit_w(bar(bars.o_ready[pv_g & 1]));
         return true;
@@ -518,8 +532,8 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             break;
           }
           pv_g = g;
-          pv_ob = qb;
           pv_first = (j == 0);
+          if (pv_first) pv_item = ii - 1;
         }
       }
       if (ok && pv_g >= 0 && !issue_pv()) fail(&s_abort);
@@ -532,9 +546,13 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // ---------------------------------------------------------------- softmax (warps 0-7)
     // Warps w and w+4 share TMEM lanes 32*(w%4).. (one query row per lane):
     // warp w takes key columns [0,64) of each block, warp w+4 columns
-    // [64,128).  The row max is combined through shared memory once per
-    // block (an mbarrier of the two warps, bounded wait); each half keeps its
-    // own partial row sum and rescales / normalises its half of O.
+    // [64,128).  Each half runs its own online softmax over its key columns
+    // -- its own running max, row sum and accumulator O_hf (the P V products
+    // of its keys) -- so the two warps never wait for each other within an
+    // item.  The epilogue combines the halves once per item: with M the
+    // larger of the two running maxima, O = sum_h O_h 2^(m_h - M) /
+    // sum_h l_h 2^(m_h - M) (maxima and sums swapped through shared memory),
+    // each warp normalising and storing one half of the D columns.
     const int row = (warp & 3) * 32 + lane;  // = TMEM lane
     const int hf = warp >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -569,22 +587,30 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     };
     // the finished item whose O still has to be normalised and stored
     struct Pending {
-      int t, h, ob, last;
+      int t, h, last;
       float m, l;
-    } pend{0, 0, 0, -1, 0.f, 0.f};
+    } pend{0, 0, -1, 0.f, 0.f};
     auto epilogue = [&]() -> bool {
       if (!wait_warp(bar(bars.o_ready[pend.last & 1]), (pend.last >> 1) & 1)) return false;
-      float l_other = 0.f;
-      if (!exchange(pend.l, &l_other)) return false;
-      const float l_tot = pend.l + l_other;
+      float m_other = 0.f, l_other = 0.f;
+      if (!exchange(pend.m, &m_other) || !exchange(pend.l, &l_other)) return false;
+      // the halves' weights against the larger running max (a half that saw
+      // no key of the row has m = -inf, l = 0 and weight 0)
+      const float m_max = fmaxf(pend.m, m_other);
+      const float w_own = pend.m == -INFINITY ? 0.f : ex2_approx((pend.m - m_max) * sl2);
+      const float w_oth = m_other == -INFINITY ? 0.f : ex2_approx((m_other - m_max) * sl2);
+      const float l_tot = pend.l * w_own + l_other * w_oth;
+      const float w0 = hf == 0 ? w_own : w_oth, w1 = hf == 0 ? w_oth : w_own;
       const bool in = pend.t < a.s_local;
       tc_fence_after();
       const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+      const float s0 = w0 * inv, s1 = w1 * inv;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         const int col = hf * (D / 2) + c * 32;
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_base + o_col<D>(pend.ob) + col, o);
+        uint32_t o[32], o1[32];
+        tmem_ld32(tmem + lane_base + o_col<D>(0) + col, o);
+        tmem_ld32(tmem + lane_base + o_col<D>(1) + col, o1);
         if (in) {
           const int64_t off = ((int64_t)pend.t * a.H + pend.h) * D + col;
           uint4* dst = reinterpret_cast<uint4*>(a.o + off);
@@ -593,7 +619,8 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           for (int q = 0; q < 4; ++q) {
             float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(o[q * 8 + e]) * inv;
+            for (int e = 0; e < 8; ++e)
+              x[e] = __uint_as_float(o[q * 8 + e]) * s0 + __uint_as_float(o1[q * 8 + e]) * s1;
             uint4 v;
             v.x = pack_bf16(x[0], x[1]);
             v.y = pack_bf16(x[2], x[3]);
@@ -613,7 +640,10 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       }
       if (in && hf == 0)
         a.lse[(int64_t)pend.h * a.s_local + pend.t] =
-            l_tot > 0.f ? (pend.m * sl2 + log2f(l_tot)) * kLn2f : -INFINITY;
+            l_tot > 0.f ? (m_max * sl2 + log2f(l_tot)) * kLn2f : -INFINITY;
+      // O_0 / O_1 are read: the next item's first P V may overwrite them
+      tc_fence_before();
+      mbar_arrive(bar(bars.o_free));
       pend.last = -1;
       return true;
     };
@@ -660,9 +690,8 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         lo_pre = tn < a.s_local ? m.row_lo[tn] : 0;
         hi_pre = tn < a.s_local ? m.row_hi[tn] : -1;
       }
-      const int ob = ii & 1;
       ++ii;
-      float m_run = -INFINITY, l_run = 0.f;
+      float m_run = -INFINITY, l_run = 0.f;  // this column half's running max and sum
       Walk w;
       w.init(a, itm.tile);
       int cur_step = 0;  // the ring step whose key range lo / hi hold
@@ -702,15 +731,8 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           mx8[q] = fmax3(mx8[q], s[40 + q], s[48 + q]);
           mx8[q] = fmaxf(mx8[q], s[56 + q]);
         }
-        float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                         fmaxf(mx8[6], mx8[7]));
-        float mx_other;
-        if (!exchange(mx, &mx_other)) {
-          fail(&s_abort);
-          ok = false;
-          break;
-        }
-        mx = fmaxf(mx, mx_other);
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
         // The running max m_run is only moved (and O, l rescaled) when the new
         // block's max exceeds it by more than 8 in log2 units; otherwise the
         // stale max stays in use for this block's P, which then stays below
@@ -768,8 +790,8 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           }
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            const uint32_t col = o_col<D>(ob) + hf * (D / 2) + c * 32;
+          for (int c = 0; c < D / 32; ++c) {  // this half's accumulator, every column
+            const uint32_t col = o_col<D>(hf) + c * 32;
             uint32_t o[32];
             tmem_ld32(tmem + lane_base + col, o);
 #pragma unroll
@@ -792,7 +814,6 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       if (!ok) break;
       pend.t = t;
       pend.h = itm.h;
-      pend.ob = ob;
       pend.last = g - 1;
       pend.m = m_run;
       pend.l = l_run;
