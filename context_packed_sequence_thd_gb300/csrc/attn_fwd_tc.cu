@@ -746,9 +746,9 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           m_run = m_new;
         }
         const float mref = m_run == -INFINITY ? 0.f : m_run * sl2;
-        // P = 2^(s * scale_log2 - mref) in pairs; every fourth pair on the FMA
-        // pipe (ex2_poly2), the rest on the SFU, so that neither unit alone
-        // sets the pace of the softmax
+        // P = 2^(s * scale_log2 - mref): the scaling in paired FMAs, 2^x on
+        // the SFU (with the two halves of a row no longer in lockstep, taking
+        // a share on the FMA pipe by a polynomial measured 2-4% slower)
         const uint64_t scl2 = f2_pack(sl2, sl2), nref2 = f2_pack(-mref, -mref);
         uint64_t sum2[4];
 #pragma unroll
@@ -757,12 +757,8 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         for (int c2 = 0; c2 < 32; ++c2) {
           float a, b;
           f2_unpack(f2_fma(f2_pack(s[2 * c2], s[2 * c2 + 1]), scl2, nref2), a, b);
-          if ((c2 & 3) == 3) {
-            ex2_poly2(a, b);
-          } else {
-            a = ex2_approx(a);
-            b = ex2_approx(b);
-          }
+          a = ex2_approx(a);
+          b = ex2_approx(b);
           s[2 * c2] = a;
           s[2 * c2 + 1] = b;
           sum2[c2 & 3] = f2_add(sum2[c2 & 3], f2_pack(a, b));

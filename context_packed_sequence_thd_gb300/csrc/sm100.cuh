@@ -263,43 +263,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// 2^x on the FMA pipe instead of the SFU, for x <= 8 (the softmax's range).
-// x = j + f with j = round(x) -- adding 1.5 * 2^23 leaves round(x) in the low
-// mantissa bits of t -- and f in [-1/2, 1/2]; 2^f is the cubic
-// 1 + f (c1 + f (c2 + f c3)), fitted to 2^f on [-1/2, 1/2] for least maximum
-// relative error (iteratively reweighted least squares on a dense grid, with
-// the constant term held at 1): relative error <= 1.1e-4, far below a bf16
-// half-ulp (2^-9).  j is then added to the exponent field.  x is clamped at
-// -127, where f = 0, p = 1 exactly and the sum of the bit patterns is exactly
-// +0 (so -inf gives 0, as ex2.approx.ftz does); for x in (-127, -126) the
-// result is a tiny denormal instead of 2^x (both below 1.2e-38).
-__device__ __forceinline__ float ex2_poly(float x) {
-  x = fmaxf(x, -127.f);
-  const float t = x + 12582912.f;
-  const float f = x - (t - 12582912.f);
-  float p = fmaf(f, 0x1.c2a20ep-5f, 0x1.f00c52p-3f);
-  p = fmaf(p, f, 0x1.62f5fcp-1f);
-  p = fmaf(p, f, 1.f);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
-// ex2_poly of a pair, the additions and the cubic in paired instructions.
-__device__ __forceinline__ void ex2_poly2(float& a, float& b) {
-  const uint64_t magic = f2_pack(12582912.f, 12582912.f);
-  const uint64_t x = f2_pack(fmaxf(a, -127.f), fmaxf(b, -127.f));
-  const uint64_t t = f2_add(x, magic);
-  const uint64_t f = f2_sub(x, f2_sub(t, magic));
-  uint64_t p = f2_fma(f, f2_pack(0x1.c2a20ep-5f, 0x1.c2a20ep-5f),
-                      f2_pack(0x1.f00c52p-3f, 0x1.f00c52p-3f));
-  p = f2_fma(p, f, f2_pack(0x1.62f5fcp-1f, 0x1.62f5fcp-1f));
-  p = f2_fma(p, f, f2_pack(1.f, 1.f));
-  float pa, pb, ta, tb;
-  f2_unpack(p, pa, pb);
-  f2_unpack(t, ta, tb);
-  a = __int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23));
-  b = __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
-}
-
 // Register reallocation between warpgroups (executed by all four warps of a
 // warpgroup).  The increases draw on what the decreases released; the block's
 // total stays the registers it was launched with.
