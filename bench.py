@@ -52,9 +52,9 @@ WORKLOAD = ("THD fwd+bwd with inter-sequence padding: 65536 padded tokens, 24 lo
 # attn_delta and attn_dq_tc, one attn_dkdv_tc that also writes the reduce-scatter's bf16 rows),
 # averaged over the 2 calls of a step (2 strategies), from the ncu capture named in
 # BWD_TRAFFIC_NOTE; None until a capture of the current kernels exists.
-BWD_TRAFFIC_BYTES = 20069418240
+BWD_TRAFFIC_BYTES = 19984964352
 BWD_TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the kernels of the timed "
-                    "step's two cp_attn_bwd_grouped_rs calls (DCS 22.96 GB, NLB 17.18 GB), full "
+                    "step's two cp_attn_bwd_grouped_rs calls (DCS 22.67 GB, NLB 17.30 GB), full "
                     "size, one pass; profiles/attn_bwd_dram_cfg5.md")
 
 # a timed region shorter than this, at the maximum SM clock and with no power

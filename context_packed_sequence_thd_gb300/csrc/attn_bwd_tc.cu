@@ -721,9 +721,13 @@ attn_dq_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mbar_arrive(bar_addr(c.s_free));  // S_{g+1} may now overwrite S
         const int k0 = w.b() * 128 + 64 * hf;  // key (of the step's shard) of this thread's first column
         if (!(lo <= k0 && hi >= k0 + 63)) {  // keys outside the row's range: P = 0
+          // (one unsigned compare per column, as in the forward)
+          const bool any = hi >= lo;
+          const int c_lo = any ? lo - k0 : (1 << 30);
+          const unsigned span = any ? (unsigned)(hi - lo) : 0u;
 #pragma unroll
           for (int e = 0; e < 64; ++e)
-            if (!(k0 + e >= lo && k0 + e <= hi)) p[e] = -INFINITY;
+            if ((unsigned)(e - c_lo) > span) p[e] = -INFINITY;
         }
         exp2_scores(p, scl2, &nlse2, 0);
         if (!wait_warp(bar_addr(c.dp_full), g & 1)) {

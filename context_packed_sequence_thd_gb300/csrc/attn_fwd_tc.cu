@@ -716,11 +716,14 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
         const int k0 = w.b() * TBN + 64 * hf;  // key (of the step's shard) of this thread's first column
         if (!(lo <= k0 && hi >= k0 + 63)) {
+          // column c is visible iff lo <= k0 + c <= hi: one unsigned compare of
+          // c - (lo - k0) against hi - lo (a row with no key masks everything)
+          const bool any = hi >= lo;
+          const int c_lo = any ? lo - k0 : (1 << 30);
+          const unsigned span = any ? (unsigned)(hi - lo) : 0u;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int key = k0 + c;
-            if (key < lo || key > hi) s[c] = -INFINITY;
-          }
+          for (int c = 0; c < 64; ++c)
+            if ((unsigned)(c - c_lo) > span) s[c] = -INFINITY;
         }
         // this half's row max: eight independent chains of three-input maxima
         float mx8[8];
