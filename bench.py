@@ -57,9 +57,8 @@ BWD_TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the ker
                     "step's two cp_attn_bwd_grouped_rs calls (DCS 22.67 GB, NLB 17.30 GB), full "
                     "size, one pass; profiles/attn_bwd_dram_cfg5.md")
 
-# a timed region shorter than this, at the maximum SM clock and with no power
-# capping, is a burst: the denominator is the burst peak; otherwise the
-# sustained one
+# without clock samples, a timed region shorter than this is a burst (burst
+# peak as the denominator), a longer one sustained
 BURST_REGION_S = 1.0
 
 
@@ -110,13 +109,16 @@ def _pairs_all(wl, strategies):
 
 
 def _pick_peak(region_s, clocks, burst, sustained):
-    """Burst peak for a short region run at the maximum clock with no power
-    capping, else sustained (the kernel then runs in the power-limited regime
-    the sustained figure was measured in)."""
+    """The measured peak of the regime the kernel ran in.  The sustained
+    figure was taken with the SM clock pulled far below its maximum by the
+    power limit; a region whose median SM clock stays within 10% of the
+    maximum runs in the burst regime (whatever its length or a power-cap flag
+    that barely binds), so its denominator is the burst peak.  Without clock
+    samples the region's length decides."""
     sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
-    at_max = sm is not None and mx is not None and sm >= 0.97 * mx
-    capped = "sw_power_cap" in (clocks.get("reasons") or [])
-    if region_s < BURST_REGION_S and at_max and not capped:
+    if sm is None or mx is None:
+        return (burst, "burst") if region_s < BURST_REGION_S else (sustained, "sustained")
+    if sm >= 0.9 * mx:
         return burst, "burst"
     return sustained, "sustained"
 

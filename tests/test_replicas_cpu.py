@@ -57,15 +57,19 @@ def test_reference_arm_under_torchrun_prints_once():
 
 
 def test_roofline_peak_choice():
-    """The burst BF16 peak is the denominator only for a short timed region at
-    the maximum SM clock without power capping; a capped or long region uses
-    the sustained one."""
+    """The burst BF16 peak is the denominator while the median SM clock stays
+    within 10% of its maximum (a barely binding power cap included); the
+    sustained one once the clock is pulled well below it; without clock
+    samples the region's length decides."""
     sys.path.insert(0, ROOT)
     import bench
     at_max = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
     capped = {"sm_mhz": 2010.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
-    slow = {"sm_mhz": 1800.0, "sm_max_mhz": 2070.0, "reasons": []}
+    slow = {"sm_mhz": 1500.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    none = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
     assert bench._pick_peak(0.5, at_max, 1943.5, 1725.2) == (1943.5, "burst")
-    assert bench._pick_peak(0.5, capped, 1943.5, 1725.2) == (1725.2, "sustained")
-    assert bench._pick_peak(0.5, slow, 1943.5, 1725.2) == (1725.2, "sustained")
-    assert bench._pick_peak(2.0, at_max, 1943.5, 1725.2) == (1725.2, "sustained")
+    assert bench._pick_peak(2.0, at_max, 1943.5, 1725.2) == (1943.5, "burst")
+    assert bench._pick_peak(1.0, capped, 1943.5, 1725.2) == (1943.5, "burst")
+    assert bench._pick_peak(1.0, slow, 1943.5, 1725.2) == (1725.2, "sustained")
+    assert bench._pick_peak(0.5, none, 1943.5, 1725.2) == (1943.5, "burst")
+    assert bench._pick_peak(2.0, none, 1943.5, 1725.2) == (1725.2, "sustained")
